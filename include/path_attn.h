@@ -1,0 +1,169 @@
+/*
+ * path_attn.h — C ABI of libpathattn.so: PaTH causal attention (forward,
+ * PaTH-FoX forward, decode with in-place key transport) on GB300 (sm_103a).
+ *
+ * The operation ("Resumo Técnico: Atenção PaTH", gist.science/pt/paper/2505.16381):
+ *   §2 "Mecanismo Central", attention-logit equation: for each head and query i,
+ *       s_ij = scale * k_j^T (H_{j+1} H_{j+2} ... H_i) q_i        for j <= i,
+ *       o_i  = sum_j softmax_j(s_i.) v_j,
+ *   §2 "Mecanismo Central", transition equation: H_s = I - beta_s w_s w_s^T.
+ *   The product is ascending (H_{j+1} leftmost) and empty (= I) at j = i.
+ *   §2 "Extensões: PaTH-FoX": adds the forget-gate bias sum_{s=j+1..i} log f_s,
+ *   unscaled, to s_ij.
+ *   §3 "Inferência": decoding applies the current step's H_t in place to every
+ *   cached key, so the cache holds transported keys and attention over it is
+ *   ordinary one-query attention.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named q, k, v, w, o, kcache, vcache, *_t, beta*, log_f, lse and
+ *     workspace are DEVICE pointers.  The caller owns every buffer; the library
+ *     never allocates, frees, or keeps a pointer after the call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  A returned PATH_OK means "validated and
+ *     launched", not "finished".
+ *   - Argument errors (null pointer, bad size, unsupported d or dtype,
+ *     misaligned pointer, too-small workspace) are returned synchronously
+ *     before anything is launched.  A launch error reported by the CUDA
+ *     runtime is returned as PATH_ERR_CUDA.  Errors detected on the device
+ *     (a bounded wait that expired) are written to the status word at the
+ *     start of the workspace and read back with path_get_status().
+ *   - dtype PATH_F32: q, k, v, w, o, caches are float; arithmetic is fp32
+ *     (no TF32).  dtype PATH_BF16: those tensors are bfloat16; products are
+ *     taken on bf16 tensor cores with fp32 accumulation, softmax in fp32.
+ *     beta, log_f and lse are always float.
+ *   - Preconditions that are NOT checked: beta in [0, 2] and |w| = 1.  The
+ *     library neither clips beta nor normalises w; values are used as given.
+ *   - All device pointers must be 16-byte aligned.
+ */
+#ifndef PATH_ATTN_H
+#define PATH_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* path_stream_t; /* identical to cudaStream_t */
+
+enum path_status {
+    PATH_OK = 0,
+    PATH_ERR_INVALID = 1,     /* bad pointer, size, alignment or capacity */
+    PATH_ERR_UNSUPPORTED = 2, /* valid request outside what is implemented (non-causal, d, dtype) */
+    PATH_ERR_CUDA = 3,        /* the CUDA runtime reported an error */
+    PATH_ERR_TIMEOUT = 4,     /* a device-side bounded wait expired (read via path_get_status) */
+    PATH_ERR_WORKSPACE = 5    /* workspace null or smaller than the *_workspace_bytes() value */
+};
+
+enum path_dtype { PATH_F32 = 0, PATH_BF16 = 1 };
+
+/* Library version, (major << 16) | minor. */
+int path_version(void);
+
+/* Human-readable name of a path_status code (static storage). */
+const char* path_status_string(int code);
+
+/*
+ * Workspace size in bytes for path_attn_fwd / path_attn_fwd_fox with these
+ * sizes.  The workspace holds the per-chunk UT-transform products (the
+ * boundary-adjusted queries and keys, and the chunk factors used by the
+ * right-to-left scan) and a status word.  Returns 0 for unsupported sizes.
+ */
+size_t path_attn_workspace_bytes(int B, int H, int L, int d, int dtype);
+
+/*
+ * PaTH causal attention forward (§2 "Mecanismo Central"; computed blockwise as
+ * in §3 "Algoritmo Estilo FlashAttention": per-chunk UT transform
+ * (§3 "Representação de Transformação UT"), boundary-adjusted queries and keys,
+ * and a right-to-left scan over key/value blocks, never forming the L x L
+ * matrix).
+ *
+ *   q, k, v, w : [B, H, L, d] row-major (element (b,h,i,c) at ((b*H+h)*L+i)*d+c)
+ *   beta       : [B, H, L] float
+ *   o          : [B, H, L, d], same dtype as q (written)
+ *   lse        : [B, H, L] float, natural-log log-sum-exp of the scaled logits
+ *                per query (written), or NULL
+ *   B, H >= 1; L >= 1; d in {16, 32, 64, 128} for PATH_F32, {64, 128} for PATH_BF16
+ *   causal     : must be 1 (the PaTH product is defined only for j <= i);
+ *                0 returns PATH_ERR_UNSUPPORTED
+ *   scale      : multiplies k_j^T(...)q_i (typically 1/sqrt(d))
+ *   workspace  : >= path_attn_workspace_bytes(B,H,L,d,dtype) bytes, device,
+ *                16-byte aligned, contents need not be initialised
+ *
+ * o may not alias any input.  The workspace must not be used by another call
+ * that can run concurrently.
+ */
+int path_attn_fwd(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                  void* o, float* lse, int B, int H, int L, int d, int dtype, int causal, float scale,
+                  void* workspace, size_t workspace_bytes, path_stream_t stream);
+
+/*
+ * PaTH-FoX forward (§2 "Extensões: PaTH-FoX"): as path_attn_fwd, with the
+ * forget-gate bias  sum_{s=j+1..i} log_f[s]  added unscaled to the scaled
+ * logit of (i, j).  log_f: [B, H, L] float (log of the forget gate, <= 0).
+ */
+int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                      const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype,
+                      int causal, float scale, void* workspace, size_t workspace_bytes,
+                      path_stream_t stream);
+
+/*
+ * Workspace size in bytes for path_decode_step (split-K partial results and a
+ * status word) for caches of capacity n_max.  Returns 0 for unsupported sizes.
+ */
+size_t path_decode_workspace_bytes(int B, int H, int n_max, int d);
+
+/*
+ * In-place key transport alone (§3 "Inferência"): for every head and every
+ * cached row j < n_cached,
+ *     kcache[b,h,j,:] <- (I - beta_t[b,h] w_t[b,h] w_t[b,h]^T) kcache[b,h,j,:]
+ * computed in fp32 and stored in the cache dtype (round to nearest even).
+ *   kcache : [B, H, n_max, d] (updated in place); 0 <= n_cached <= n_max
+ *   w_t    : [B, H, d] cache dtype;  beta_t : [B, H] float
+ *   d in {16, 32, 64, 128}
+ */
+int path_kcache_update(void* kcache, int B, int H, int n_cached, int n_max, int d, const void* w_t,
+                       const float* beta_t, int dtype, path_stream_t stream);
+
+/*
+ * One decode step for every head (§3 "Inferência"; one-query attention over
+ * the cache as in FlashDecoding, split over the key axis and merged by
+ * log-sum-exp):
+ *   1. kcache[j] <- H_t kcache[j] for j < n_cached   (fp32 math, stored in cache dtype)
+ *   2. kcache[n_cached] <- k_t, vcache[n_cached] <- v_t   (the new key is not transported)
+ *   3. o_t = softmax_j(scale * q_t . kcache[j]) vcache[j] over j = 0..n_cached,
+ *      scoring each key with the value just stored.
+ *   q_t, k_t, v_t, w_t : [B, H, d] cache dtype;  beta_t : [B, H] float
+ *   kcache, vcache     : [B, H, n_max, d]; requires n_cached + 1 <= n_max
+ *                        (else PATH_ERR_INVALID); 0 <= n_cached
+ *   o_t                : [B, H, d] cache dtype (written);  lse_t : [B, H] float or NULL
+ *   workspace          : >= path_decode_workspace_bytes(B, H, n_max, d) bytes
+ *   d in {16, 32, 64, 128}
+ * The caller advances n_cached by one after each step.
+ */
+int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                     const float* beta_t, void* kcache, void* vcache, int n_cached, int n_max, void* o_t,
+                     float* lse_t, int B, int H, int d, float scale, int dtype, void* workspace,
+                     size_t workspace_bytes, path_stream_t stream);
+
+/*
+ * Status of the most recent call that used `workspace` (each call clears the
+ * word when it starts).  Synchronises `stream` first.  Returns a path_status
+ * code: PATH_OK, PATH_ERR_TIMEOUT if a device-side bounded wait expired, or
+ * PATH_ERR_CUDA if the synchronisation or read failed.
+ */
+int path_get_status(const void* workspace, path_stream_t stream);
+
+/*
+ * Test hook for the device-side failure path.  A non-zero mask makes the next
+ * bf16 forward launches skip one producer signal on purpose, so that the
+ * consumer's bounded wait expires and the call reports PATH_ERR_TIMEOUT
+ * through path_get_status() instead of hanging.  0 (the default) disables it.
+ */
+void path_debug_set_fault(int mask);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PATH_ATTN_H */

@@ -1,0 +1,184 @@
+/*
+ * fp64 CPU oracle for PaTH causal attention — TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * leg may load this library.  It shares no code, header, table or constant with
+ * the CUDA library in attention_causal_attn_fwd_gb300/csrc; neither side
+ * includes or links the other.
+ *
+ * Source of the definitions: "Resumo Técnico: Atenção PaTH"
+ * (gist.science/pt/paper/2505.16381):
+ *   - §2 "Mecanismo Central", attention-logit equation:
+ *         A_ij ∝ exp( k_j^T (prod_{s=j+1}^{i} H_s) q_i ),  j <= i,
+ *   - §2 "Mecanismo Central", transition equation:  H_s = I - beta_s w_s w_s^T,
+ *   - §2 "Extensões: PaTH-FoX": FoX's additive, data-dependent forget gates on
+ *     top of the PaTH logits,
+ *   - §3 "Treinamento e Inferência Eficientes", "Inferência" bullet: at decode
+ *     time the historical keys are updated in place with the current step's
+ *     transition.
+ *
+ * Readings taken where the page is silent (each also listed in the design doc):
+ *   - the product is ascending, H_{j+1} H_{j+2} ... H_i (the only order under
+ *     which the in-place key update of the "Inferência" bullet is exact);
+ *   - the product is empty (= I) at j = i, and j = i takes part in the softmax;
+ *   - logits are multiplied by `scale` after transport; the FoX bias
+ *     sum_{s=j+1..i} log f_s is added unscaled to the scaled logit;
+ *   - decode step t first applies H_t to every cached key, then appends the
+ *     new key k_t untransported, then attends over all keys.
+ *
+ * The walk: s_ij = k_j^T H_{j+1} ... H_i q_i is evaluated by walking the query
+ * backwards: u <- q_i; for j = i, i-1, ..., 0 { s_ij = k_j . u; u <- H_j u }.
+ * No blocking, no UT transform, no fusion: one row at a time, in fp64.
+ *
+ * parity pins: see tests/test_oracle.py (dense product, beta = 0 library
+ * attention, closed forms, orthogonality, decode = prefill, hand-derived
+ * golden values).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int path_oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+static double dot(const double* a, const double* b, int d) {
+    double s = 0.0;
+    for (int c = 0; c < d; ++c) s += a[c] * b[c];
+    return s;
+}
+
+/* u <- (I - beta w w^T) u  (one Householder-like transition, §2 Mecanismo Central) */
+static void apply_transition(double* u, const double* w, double beta, int d) {
+    double t = beta * dot(w, u, d);
+    for (int c = 0; c < d; ++c) u[c] -= t * w[c];
+}
+
+/*
+ * Logits of one query row i of one head, written to s[0..i].
+ * q_i: [d]; k, w: [L, d] of this head; beta, log_f: [L] of this head
+ * (log_f may be NULL).  u is a scratch vector of length d.
+ */
+static void row_logits(const double* qi, const double* k, const double* w,
+                       const double* beta, const double* log_f, int i, int d,
+                       double scale, double* s, double* u) {
+    memcpy(u, qi, sizeof(double) * (size_t)d);
+    double bias = 0.0; /* sum_{s=j+1..i} log f_s, empty (0) at j = i */
+    for (int j = i; j >= 0; --j) {
+        s[j] = scale * dot(k + (size_t)j * d, u, d) + bias;
+        /* next key j-1 sees H_j ... H_i q_i */
+        apply_transition(u, w + (size_t)j * d, beta[j], d);
+        if (log_f) bias += log_f[j];
+    }
+}
+
+/* softmax over s[0..n-1] (max-subtracted), o = sum_j p_j v_j, returns lse */
+static double softmax_combine(const double* s, const double* v, int n, int d, double* o) {
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) m = s[j] > m ? s[j] : m;
+    double l = 0.0;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double p = exp(s[j] - m);
+        l += p;
+        const double* vj = v + (size_t)j * d;
+        for (int c = 0; c < d; ++c) o[c] += p * vj[c];
+    }
+    for (int c = 0; c < d; ++c) o[c] /= l;
+    return m + log(l);
+}
+
+/*
+ * PaTH (or PaTH-FoX when log_f != NULL) causal attention forward for a list of
+ * rows.  Tensors are [B*H, L, d] row-major fp64 (beta, log_f: [B*H, L]).
+ * rows[r] = bh * L + i selects query i of head bh; n_rows rows are computed
+ * and o_rows[r*d ...], lse_rows[r] receive the results.  rows == NULL means
+ * every row of every head in natural order (n_rows must be BH*L).
+ */
+void path_oracle_fwd_rows(const double* q, const double* k, const double* v,
+                          const double* w, const double* beta, const double* log_f,
+                          int BH, int L, int d, double scale,
+                          const int64_t* rows, int64_t n_rows,
+                          double* o_rows, double* lse_rows) {
+    (void)BH;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* u = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            int64_t gi = rows ? rows[r] : r;
+            int64_t bh = gi / L;
+            int i = (int)(gi % L);
+            size_t hoff = (size_t)bh * (size_t)L;
+            row_logits(q + (size_t)gi * d, k + hoff * d, w + hoff * d, beta + hoff,
+                       log_f ? log_f + hoff : NULL, i, d, scale, s, u);
+            double lse = softmax_combine(s, v + hoff * d, i + 1, d, o_rows + (size_t)r * d);
+            if (lse_rows) lse_rows[r] = lse;
+        }
+        free(s);
+        free(u);
+    }
+}
+
+/*
+ * Full L x L logit matrix of one head (tiny inputs; for pins).  Entries above
+ * the diagonal (j > i) are set to -INFINITY.
+ */
+void path_oracle_logits(const double* q, const double* k, const double* w,
+                        const double* beta, const double* log_f, int L, int d,
+                        double scale, double* S) {
+    double* u = (double*)malloc(sizeof(double) * (size_t)d);
+    for (int i = 0; i < L; ++i) {
+        double* row = S + (size_t)i * L;
+        for (int j = i + 1; j < L; ++j) row[j] = -INFINITY;
+        row_logits(q + (size_t)i * d, k, w, beta, log_f, i, d, scale, row, u);
+    }
+    free(u);
+}
+
+/*
+ * Decode for ONE head, following the "Inferência" bullet of §3: the cache holds
+ * transported keys  k~_j = H_{t-1} ... H_{j+1} k_j  (rows 0..n0-1 on entry).
+ * For each step t = 0..T-1 (token position p = n0 + t):
+ *     k~_j <- H_p k~_j for every cached j < p         (in-place key update)
+ *     append k_p (untransported) and v_p at slot p
+ *     o_t = softmax_j(scale * q_p . k~_j) v_j over j = 0..p
+ * kc, vc: [n_max, d] fp64, updated in place; q, k, v, w: [T, d]; beta: [T];
+ * o: [T, d]; lse: [T] (nullable).  n_max >= n0 + T.
+ */
+void path_oracle_decode(double* kc, double* vc, int n0, int n_max, int d,
+                        const double* q, const double* k, const double* v,
+                        const double* w, const double* beta, int T, double scale,
+                        double* o, double* lse) {
+    (void)n_max;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(n0 + T));
+    for (int t = 0; t < T; ++t) {
+        int p = n0 + t;
+        const double* wt = w + (size_t)t * d;
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j < p; ++j) apply_transition(kc + (size_t)j * d, wt, beta[t], d);
+        memcpy(kc + (size_t)p * d, k + (size_t)t * d, sizeof(double) * (size_t)d);
+        memcpy(vc + (size_t)p * d, v + (size_t)t * d, sizeof(double) * (size_t)d);
+        const double* qt = q + (size_t)t * d;
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j <= p; ++j) s[j] = scale * dot(kc + (size_t)j * d, qt, d);
+        double l = softmax_combine(s, vc, p + 1, d, o + (size_t)t * d);
+        if (lse) lse[t] = l;
+    }
+    free(s);
+}
+
+/* The in-place key update alone: k~_j <- (I - beta w w^T) k~_j for j < n. */
+void path_oracle_kcache_update(double* kc, int n, int d, const double* w, double beta) {
+#pragma omp parallel for schedule(static)
+    for (int j = 0; j < n; ++j) apply_transition(kc + (size_t)j * d, w, beta, d);
+}
