@@ -1,1 +1,227 @@
-"""PaTH causal attention forward and decode on GB300 (sm_103a)."""
+"""PaTH causal attention (forward, PaTH-FoX forward, decode) on GB300 (sm_103a).
+
+Thin ctypes binding over libpathattn.so (C ABI in include/path_attn.h).  Every
+step of the computation runs in the library's CUDA kernels; this module only
+checks tensor layouts, allocates outputs and workspaces through torch, and
+passes raw device pointers plus the current CUDA stream.  There is no CPU
+fallback: a missing library raises ``PathLibraryError``.
+
+Functions keep the C names:
+
+- ``path_attn_fwd(q, k, v, w, beta, scale=None, lse=False)``
+- ``path_attn_fwd_fox(q, k, v, w, beta, log_f, scale=None, lse=False)``
+- ``path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, scale=None)``
+- ``path_kcache_update(kcache, n_cached, w_t, beta_t)``
+- ``path_get_status(workspace)``, ``path_attn_workspace_bytes(...)``,
+  ``path_decode_workspace_bytes(...)``
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libpathattn.so")
+
+PATH_OK, PATH_ERR_INVALID, PATH_ERR_UNSUPPORTED, PATH_ERR_CUDA, PATH_ERR_TIMEOUT, PATH_ERR_WORKSPACE = range(6)
+PATH_F32, PATH_BF16 = 0, 1
+_DT = {torch.float32: PATH_F32, torch.bfloat16: PATH_BF16}
+
+EXPORTED = ("path_version", "path_status_string", "path_attn_workspace_bytes", "path_attn_fwd",
+            "path_attn_fwd_fox", "path_decode_workspace_bytes", "path_kcache_update", "path_decode_step",
+            "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events")
+
+
+class PathLibraryError(RuntimeError):
+    """libpathattn.so is missing or could not be loaded."""
+
+
+class PathError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__("%s: %s (status %d)" % (where, status_string(code), code))
+
+
+_lib = None
+_vp, _fp, _i, _sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libpathattn.so (build it with ``attention_causal_attn_fwd_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise PathLibraryError("libpathattn.so not found at %s; run __graft_entry__.build()" % p)
+    try:
+        lib = ctypes.CDLL(p)
+    except OSError as e:
+        raise PathLibraryError("cannot load %s: %s" % (p, e)) from e
+    lib.path_version.restype = _i
+    lib.path_status_string.argtypes = [_i]
+    lib.path_status_string.restype = ctypes.c_char_p
+    lib.path_attn_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+    lib.path_attn_workspace_bytes.restype = _sz
+    lib.path_attn_fwd.argtypes = [_vp, _vp, _vp, _vp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp,
+                                  _sz, _vp]
+    lib.path_attn_fwd.restype = _i
+    lib.path_attn_fwd_fox.argtypes = [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i,
+                                      ctypes.c_float, _vp, _sz, _vp]
+    lib.path_attn_fwd_fox.restype = _i
+    lib.path_decode_workspace_bytes.argtypes = [_i, _i, _i, _i]
+    lib.path_decode_workspace_bytes.restype = _sz
+    lib.path_kcache_update.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _fp, _i, _vp]
+    lib.path_kcache_update.restype = _i
+    lib.path_decode_step.argtypes = [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _i, _i, _vp, _fp, _i, _i, _i,
+                                     ctypes.c_float, _i, _vp, _sz, _vp]
+    lib.path_decode_step.restype = _i
+    lib.path_get_status.argtypes = [_vp, _vp]
+    lib.path_get_status.restype = _i
+    lib.path_debug_set_fault.argtypes = [_i]
+    lib.path_debug_set_fault.restype = None
+    lib.path_debug_set_timing_events.argtypes = [_vp, _vp]
+    lib.path_debug_set_timing_events.restype = None
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    try:
+        return load().path_status_string(int(code)).decode()
+    except PathLibraryError:
+        return "status %d" % code
+
+
+def _check(code: int, where: str):
+    if code != PATH_OK:
+        raise PathError(code, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    return t
+
+
+def path_attn_workspace_bytes(B: int, H: int, L: int, d: int, dtype: torch.dtype) -> int:
+    return int(load().path_attn_workspace_bytes(B, H, L, d, _DT[dtype]))
+
+
+def path_decode_workspace_bytes(B: int, H: int, n_max: int, d: int) -> int:
+    return int(load().path_decode_workspace_bytes(B, H, n_max, d))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    """A device workspace buffer of at least nbytes (uint8, 256-byte aligned by torch)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _fwd(q, k, v, w, beta, log_f, scale, lse, out, ws):
+    lib = load()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d]")
+    B, H, L, d = q.shape
+    dt = q.dtype
+    if dt not in _DT:
+        raise ValueError("dtype must be float32 or bfloat16")
+    for name, t in (("q", q), ("k", k), ("v", v), ("w", w)):
+        _dev(t, name, dt, (B, H, L, d))
+    _dev(beta, "beta", torch.float32, (B, H, L))
+    if log_f is not None:
+        _dev(log_f, "log_f", torch.float32, (B, H, L))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else _dev(out, "out", dt, (B, H, L, d))
+    lse_t = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse else None
+    need = lib.path_attn_workspace_bytes(B, H, L, d, _DT[dt])
+    if need == 0:
+        raise PathError(PATH_ERR_UNSUPPORTED, "path_attn_fwd")
+    if ws is None:
+        ws = alloc_workspace(need, q.device)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta)]
+    tail = [_ptr(o), _ptr(lse_t), B, H, L, d, _DT[dt], 1, ctypes.c_float(scale), _ptr(ws), ws.numel(), _stream()]
+    if log_f is None:
+        _check(lib.path_attn_fwd(*args, *tail), "path_attn_fwd")
+    else:
+        _check(lib.path_attn_fwd_fox(*args, _ptr(log_f), *tail), "path_attn_fwd_fox")
+    return (o, lse_t) if lse else o
+
+
+def path_attn_fwd(q, k, v, w, beta, scale=None, lse=False, out=None, workspace=None):
+    """PaTH causal attention forward.  q, k, v, w: [B, H, L, d] CUDA (fp32 or bf16); beta [B, H, L] fp32."""
+    return _fwd(q, k, v, w, beta, None, scale, lse, out, workspace)
+
+
+def path_attn_fwd_fox(q, k, v, w, beta, log_f, scale=None, lse=False, out=None, workspace=None):
+    """PaTH-FoX forward: adds sum_{s=j+1..i} log_f[s] to the scaled logit of (i, j)."""
+    if log_f is None:
+        raise ValueError("log_f is required")
+    return _fwd(q, k, v, w, beta, log_f, scale, lse, out, workspace)
+
+
+def path_kcache_update(kcache, n_cached: int, w_t, beta_t):
+    """In place: kcache[:, :, j] <- (I - beta_t w_t w_t^T) kcache[:, :, j] for j < n_cached."""
+    lib = load()
+    B, H, n_max, d = kcache.shape
+    _dev(kcache, "kcache")
+    _dev(w_t, "w_t", kcache.dtype, (B, H, d))
+    _dev(beta_t, "beta_t", torch.float32, (B, H))
+    _check(lib.path_kcache_update(_ptr(kcache), B, H, int(n_cached), n_max, d, _ptr(w_t), _ptr(beta_t),
+                                  _DT[kcache.dtype], _stream()), "path_kcache_update")
+
+
+def path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached: int, scale=None, out=None,
+                     lse=False, workspace=None):
+    """One decode step for all heads; updates kcache/vcache in place and returns o_t [B, H, d]."""
+    lib = load()
+    B, H, n_max, d = kcache.shape
+    dt = kcache.dtype
+    _dev(kcache, "kcache")
+    _dev(vcache, "vcache", dt, (B, H, n_max, d))
+    for name, t in (("q_t", q_t), ("k_t", k_t), ("v_t", v_t), ("w_t", w_t)):
+        _dev(t, name, dt, (B, H, d))
+    _dev(beta_t, "beta_t", torch.float32, (B, H))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q_t) if out is None else out
+    lse_t = torch.empty((B, H), dtype=torch.float32, device=q_t.device) if lse else None
+    if workspace is None:
+        workspace = alloc_workspace(lib.path_decode_workspace_bytes(B, H, n_max, d), q_t.device)
+    _check(lib.path_decode_step(_ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(kcache),
+                                _ptr(vcache), int(n_cached), n_max, _ptr(o), _ptr(lse_t), B, H, d,
+                                ctypes.c_float(scale), _DT[dt], _ptr(workspace), workspace.numel(), _stream()),
+           "path_decode_step")
+    return (o, lse_t) if lse else o
+
+
+def path_get_status(workspace_tensor) -> int:
+    """Status word of the last call that used this workspace (synchronises the current stream)."""
+    return int(load().path_get_status(_ptr(workspace_tensor), _stream()))
+
+
+def path_debug_set_fault(mask: int):
+    load().path_debug_set_fault(int(mask))
+
+
+def path_debug_set_timing_events(ev_start=None, ev_end=None):
+    """Record two torch.cuda.Events around the dominant kernel of each later call (None, None stops)."""
+    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    load().path_debug_set_timing_events(h(ev_start), h(ev_end))

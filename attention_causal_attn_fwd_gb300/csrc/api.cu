@@ -1,0 +1,167 @@
+// C ABI of libpathattn.so (declarations and contracts in include/path_attn.h).
+// Host side only: argument validation, workspace carve-up and kernel dispatch.
+// Nothing here allocates device memory; every launch goes to the caller's stream.
+#include <atomic>
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace pathattn {
+int simt_chunk(int d);
+cudaError_t fwd_simt_f32(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                         const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
+                         unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
+int tc_chunk(int d);
+bool tc_supported(int d);
+cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                        const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
+                        unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st);
+cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                        const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t, float* lse_t,
+                        int BH, float scale, unsigned char* ws, const DecLayout& lay, cudaStream_t st);
+cudaError_t kcache_update_launch(int dtype, int d, void* kc, int n_cached, int n_max, const void* w_t,
+                                 const float* beta_t, int BH, cudaStream_t st);
+
+static std::atomic<int> g_fault_mask{0};
+static std::atomic<void*> g_ev_start{nullptr}, g_ev_end{nullptr};
+
+void timing_events(cudaEvent_t* start, cudaEvent_t* end) {
+    *start = static_cast<cudaEvent_t>(g_ev_start.load());
+    *end = static_cast<cudaEvent_t>(g_ev_end.load());
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static size_t elt_size(int dtype) { return dtype == PATH_F32 ? 4 : 2; }
+
+static bool fwd_d_ok(int d, int dtype) {
+    if (dtype == PATH_F32) return d == 16 || d == 32 || d == 64 || d == 128;
+    if (dtype == PATH_BF16) return tc_supported(d);
+    return false;
+}
+static int fwd_chunk(int d, int dtype) { return dtype == PATH_F32 ? simt_chunk(d) : tc_chunk(d); }
+static bool dec_d_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+static int fwd_common(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                      const float* log_f, bool fox, void* o, float* lse, int B, int H, int L, int d, int dtype,
+                      int causal, float scale, void* ws, size_t ws_bytes, cudaStream_t st) {
+    if (B < 1 || H < 1 || L < 1 || d < 1) return PATH_ERR_INVALID;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
+    if (!causal) return PATH_ERR_UNSUPPORTED;
+    if (!fwd_d_ok(d, dtype)) return PATH_ERR_UNSUPPORTED;
+    if ((long long)B * H * L > (1ll << 31) / 256) return PATH_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !w || !beta || !o || (fox && !log_f)) return PATH_ERR_INVALID;
+    const void* ptrs[] = {q, k, v, w, beta, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PATH_ERR_INVALID;
+    if ((fox && !aligned16(log_f)) || (lse && !aligned16(lse))) return PATH_ERR_INVALID;
+    const FwdLayout lay = fwd_layout(B, H, L, d, fwd_chunk(d, dtype), elt_size(dtype));
+    if (!ws || ws_bytes < lay.total || !aligned16(ws)) return PATH_ERR_WORKSPACE;
+    unsigned char* wsb = static_cast<unsigned char*>(ws);
+    cudaError_t e;
+    if (dtype == PATH_F32)
+        e = fwd_simt_f32(q, k, v, w, beta, fox ? log_f : nullptr, o, lse, B * H, L, d, scale, wsb, lay, st);
+    else
+        e = fwd_tc_bf16(q, k, v, w, beta, fox ? log_f : nullptr, o, lse, B * H, L, d, scale, wsb, lay,
+                        g_fault_mask.load(), st);
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "pathattn: forward launch failed: %s\n", cudaGetErrorString(e));
+        return PATH_ERR_CUDA;
+    }
+    return PATH_OK;
+}
+
+}  // namespace pathattn
+
+using namespace pathattn;
+
+extern "C" {
+
+int path_version(void) { return (0 << 16) | 1; }
+
+const char* path_status_string(int code) {
+    switch (code) {
+        case PATH_OK: return "ok";
+        case PATH_ERR_INVALID: return "invalid argument";
+        case PATH_ERR_UNSUPPORTED: return "unsupported request";
+        case PATH_ERR_CUDA: return "CUDA runtime error";
+        case PATH_ERR_TIMEOUT: return "device-side wait timed out";
+        case PATH_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+size_t path_attn_workspace_bytes(int B, int H, int L, int d, int dtype) {
+    if (B < 1 || H < 1 || L < 1 || !fwd_d_ok(d, dtype)) return 0;
+    return fwd_layout(B, H, L, d, fwd_chunk(d, dtype), elt_size(dtype)).total;
+}
+
+int path_attn_fwd(const void* q, const void* k, const void* v, const void* w, const float* beta, void* o,
+                  float* lse, int B, int H, int L, int d, int dtype, int causal, float scale, void* workspace,
+                  size_t workspace_bytes, path_stream_t stream) {
+    return fwd_common(q, k, v, w, beta, nullptr, false, o, lse, B, H, L, d, dtype, causal, scale, workspace,
+                      workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                      const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype, int causal,
+                      float scale, void* workspace, size_t workspace_bytes, path_stream_t stream) {
+    return fwd_common(q, k, v, w, beta, log_f, true, o, lse, B, H, L, d, dtype, causal, scale, workspace,
+                      workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t path_decode_workspace_bytes(int B, int H, int n_max, int d) {
+    if (B < 1 || H < 1 || n_max < 1 || !dec_d_ok(d)) return 0;
+    return dec_layout(B, H, n_max, d).total;
+}
+
+int path_kcache_update(void* kcache, int B, int H, int n_cached, int n_max, int d, const void* w_t,
+                       const float* beta_t, int dtype, path_stream_t stream) {
+    if (B < 1 || H < 1 || n_max < 1 || n_cached < 0 || n_cached > n_max) return PATH_ERR_INVALID;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
+    if (!dec_d_ok(d)) return PATH_ERR_UNSUPPORTED;
+    if (!kcache || !w_t || !beta_t) return PATH_ERR_INVALID;
+    if (!aligned16(kcache) || !aligned16(w_t)) return PATH_ERR_INVALID;
+    cudaError_t e = kcache_update_launch(dtype, d, kcache, n_cached, n_max, w_t, beta_t, B * H,
+                                         reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA;
+}
+
+int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const void* w_t, const float* beta_t,
+                     void* kcache, void* vcache, int n_cached, int n_max, void* o_t, float* lse_t, int B, int H,
+                     int d, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                     path_stream_t stream) {
+    if (B < 1 || H < 1 || n_max < 1 || n_cached < 0) return PATH_ERR_INVALID;
+    if (n_cached + 1 > n_max) return PATH_ERR_INVALID;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
+    if (!dec_d_ok(d)) return PATH_ERR_UNSUPPORTED;
+    if (!q_t || !k_t || !v_t || !w_t || !beta_t || !kcache || !vcache || !o_t) return PATH_ERR_INVALID;
+    const void* ptrs[] = {q_t, k_t, v_t, w_t, kcache, vcache, o_t};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PATH_ERR_INVALID;
+    const DecLayout lay = dec_layout(B, H, n_max, d);
+    if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PATH_ERR_WORKSPACE;
+    cudaError_t e = decode_step(dtype, d, q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, n_max, o_t, lse_t,
+                                B * H, scale, static_cast<unsigned char*>(workspace), lay,
+                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA;
+}
+
+int path_get_status(const void* workspace, path_stream_t stream) {
+    if (!workspace) return PATH_ERR_INVALID;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int status = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PATH_ERR_CUDA;
+    if (cudaMemcpyAsync(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return PATH_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return PATH_ERR_CUDA;
+    return status;
+}
+
+void path_debug_set_fault(int mask) { g_fault_mask.store(mask); }
+
+void path_debug_set_timing_events(void* ev_start, void* ev_end) {
+    g_ev_start.store(ev_end ? ev_start : nullptr);
+    g_ev_end.store(ev_start ? ev_end : nullptr);
+}
+
+}  // extern "C"

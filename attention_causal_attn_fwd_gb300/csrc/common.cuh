@@ -1,0 +1,144 @@
+// Shared device/host helpers for libpathattn (PaTH causal attention on sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "path_attn.h"
+
+namespace pathattn {
+
+// ----------------------------------------------------------------------------- element conversion
+template <typename T> struct Elt;
+template <> struct Elt<float> {
+    static __device__ __forceinline__ float to_f(float x) { return x; }
+    static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Elt<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+template <typename T> __device__ __forceinline__ float to_f(T x) { return Elt<T>::to_f(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x) { return Elt<T>::from_f(x); }
+
+// 16-byte vector of T: 4 floats or 8 bf16.
+template <typename T> struct Vec16 {
+    static constexpr int N = 16 / sizeof(T);
+    uint4 raw;
+    __device__ __forceinline__ float get(int i) const {
+        const T* p = reinterpret_cast<const T*>(&raw);
+        return to_f<T>(p[i]);
+    }
+    __device__ __forceinline__ void set(int i, float x) {
+        T* p = reinterpret_cast<T*>(&raw);
+        p[i] = from_f<T>(x);
+    }
+};
+
+__device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint4 ld_global_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+// Streaming load (no L1 allocation): data touched once per step.
+__device__ __forceinline__ uint4 ld_global_stream_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ----------------------------------------------------------------------------- status word
+// The first 256 bytes of every workspace form a header; word 0 is the status.
+struct WsHeader {
+    int status;
+    int fault_site;     // which wait expired (debugging aid)
+    unsigned work_next; // tile counter for persistent schedulers
+    int pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+__device__ __forceinline__ void report_status(WsHeader* h, int code, int site) {
+    if (atomicCAS(&h->status, 0, code) == 0) h->fault_site = site;
+}
+
+// Optional events recorded around the dominant kernel of each call (set by
+// path_debug_set_timing_events; both null when unused).
+void timing_events(cudaEvent_t* start, cudaEvent_t* end);
+inline void mark_start(cudaStream_t st) {
+    cudaEvent_t a, b;
+    timing_events(&a, &b);
+    if (a && b) cudaEventRecord(a, st);
+}
+inline void mark_end(cudaStream_t st) {
+    cudaEvent_t a, b;
+    timing_events(&a, &b);
+    if (a && b) cudaEventRecord(b, st);
+}
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// ----------------------------------------------------------------------------- forward workspace
+// Per-chunk UT-transform products for a forward call with chunk size C.
+// Every per-head array is padded to Lp = ceil(L / C) * C rows so that chunk
+// reads never cross into the next head; padded rows hold zeros.
+//   qhat : float [BH, Lp, d]  queries transported to their chunk start
+//   khat : T     [BH, Lp, d]  keys transported to their chunk end
+//   un   : T     [BH, Lp, d]  -U = -A^T W per chunk (query-side scan factor)
+//   y    : T     [BH, Lp, C]  Y = tril(Q W^T) A^T per chunk (diagonal blocks)
+//   zn   : T     [BH, Lp, C]  -Z = -triu_1(K W^T) per chunk (diagonal blocks)
+//   cum  : float [BH, Lp]     inclusive cumulative sum of log f (PaTH-FoX)
+struct FwdLayout {
+    size_t qhat, khat, un, y, zn, cum, total;
+    int Lp;
+};
+inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt) {
+    FwdLayout s;
+    s.Lp = cdiv(L, C) * C;
+    const size_t rows = (size_t)B * H * s.Lp;
+    size_t off = sizeof(WsHeader);
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
+    s.qhat = take(rows * d * sizeof(float));
+    s.khat = take(rows * d * elt);
+    s.un = take(rows * d * elt);
+    s.y = take(rows * C * elt);
+    s.zn = take(rows * C * elt);
+    s.cum = take(rows * sizeof(float));
+    s.total = off;
+    return s;
+}
+
+// ----------------------------------------------------------------------------- decode workspace
+constexpr int kDecodeRowsPerSplit = 2048;
+inline int decode_splits(int n_rows) { return cdiv(n_rows > 0 ? n_rows : 1, kDecodeRowsPerSplit); }
+struct DecLayout {
+    size_t part_m, part_l, part_o, total;
+    int splits;
+};
+inline DecLayout dec_layout(int B, int H, int n_max, int d) {
+    DecLayout s;
+    s.splits = decode_splits(n_max);
+    const size_t n = (size_t)B * H * s.splits;
+    size_t off = sizeof(WsHeader);
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 256); return o; };
+    s.part_m = take(n * sizeof(float));
+    s.part_l = take(n * sizeof(float));
+    s.part_o = take(n * d * sizeof(float));
+    s.total = off;
+    return s;
+}
+
+}  // namespace pathattn

@@ -1,0 +1,357 @@
+"""Benchmark: PaTH forward TFLOP/s (B8 H12 L4096 d128 bf16) and decode us/step at a 32K cache.
+
+One step = one PaTH forward over the 760M-shaped workload (B8 H12 L4096 d128
+bf16, inputs resident in HBM) followed by a 256-token decode sequence over the
+32K-token cache (B64 H12 d128 bf16), i.e. the whole hot path once.  ``value``
+is the forward's attention-equivalent TFLOP/s (4 B H d L^2 / 2 FLOP per call);
+decode is reported alongside in us/step.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica of the workload (the path
+shards by (batch, head) with no exchange, so there is no collective on the
+data path); the barrier and max-over-ranks timing use torch.distributed.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+FWD_NAME = "path760m_bf16"
+DEC_NAME = "decode32k_bf16"
+METRIC = "PaTH fwd TFLOP/s (L=4096,d=128,bf16) & decode µs/step @32K cache, % roofline"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(n_heads: int, seed_heads: int = 0):
+    """Time the fp64 oracle on n_heads full heads of the forward workload; returns
+    (attention-equivalent TFLOP/s, seconds, threads, description)."""
+    import numpy as np
+    from attention_causal_attn_fwd_gb300 import inputs
+    from oracle import oracle as orc
+    cfg = inputs.FWD_CONFIGS[FWD_NAME]
+    x = cfg.make()
+    f = inputs.f64
+    rng = np.random.default_rng(seed_heads)
+    picks = [(int(rng.integers(0, cfg.B)), int(rng.integers(0, cfg.H))) for _ in range(n_heads)]
+    sel = lambda t: np.stack([t[b, h] for b, h in picks])
+    args = [sel(f(t)) for t in (x.q, x.k, x.v, x.w, x.beta)]
+    orc.build()
+    t0 = time.perf_counter()
+    orc.path_attn(*args, scale=x.scale)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * cfg.d * cfg.L * cfg.L / 2.0 * n_heads
+    desc = "fp64 oracle, %d full head(s) of %d (B%d H%d L%d d%d), attention-equivalent FLOPs of those heads" % (
+        n_heads, cfg.B * cfg.H, cfg.B, cfg.H, cfg.L, cfg.d)
+    return flops / dt / 1e12, dt, orc.threads(), desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_sample(1)
+    times = []
+    vals = []
+    for s in range(args.steps):
+        v, dt, cores, desc = oracle_sample(1, seed_heads=s)
+        times.append(dt)
+        vals.append(v)
+    value = 4.0 * 128 * 4096 * 4096 / 2.0 * args.steps / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded CPU generator)",
+            "config": {"workload": "PaTH forward B8 H12 L4096 d128 (one head per step on the CPU oracle)",
+                       "B": 8, "H": 12, "L": 4096, "d": 128},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU leg
+def run_ours(args, rank, world, local):
+    import attention_causal_attn_fwd_gb300 as P
+    from attention_causal_attn_fwd_gb300 import inputs
+
+    dev = torch.device("cuda", local)
+    hbm_gbs, bf16_tf, bf16_sust, peak_src = _peaks()
+    fc = inputs.FWD_CONFIGS[FWD_NAME]
+    dc = inputs.DECODE_CONFIGS[DEC_NAME]
+    x = fc.make()
+    q, k, v, w, beta = (t.to(dev) for t in (x.q, x.k, x.v, x.w, x.beta))
+    o = torch.empty_like(q)
+    ws_f = P.alloc_workspace(P.path_attn_workspace_bytes(fc.B, fc.H, fc.L, fc.d, q.dtype), dev)
+
+    Td = args.decode_steps
+    n_max = dc.n0 + Td
+    if Td > 0:
+        kc, vc = inputs.make_decode_cache(dc.B, dc.H, dc.n0, dc.d, n_max, dc.dtype, dc.seed)
+        kc, vc = kc.to(dev), vc.to(dev)
+        dq, dk, dv, dw, db = (t.to(dev) for t in inputs.make_decode_steps(dc.B, dc.H, dc.d, Td, dc.dtype, dc.seed))
+        od = torch.empty((Td, dc.B, dc.H, dc.d), dtype=kc.dtype, device=dev)
+        ws_d = P.alloc_workspace(P.path_decode_workspace_bytes(dc.B, dc.H, n_max, dc.d), dev)
+
+    def mk():
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+    def one_step(rec, s=0):
+        # rec: dict of per-step event lists (timed steps), or None (warm-up)
+        if rec is not None:
+            P.path_debug_set_timing_events(rec["fk0"][s], rec["fk1"][s])
+            rec["f0"][s].record()
+        P.path_attn_fwd(q, k, v, w, beta, scale=x.scale, out=o, workspace=ws_f)
+        if rec is not None:
+            rec["f1"][s].record()
+        for t in range(Td):
+            if rec is not None:
+                P.path_debug_set_timing_events(rec["dk0"][s][t], rec["dk1"][s][t])
+            P.path_decode_step(dq[t], dk[t], dv[t], dw[t], db[t], kc, vc, dc.n0 + t, scale=dc.d ** -0.5,
+                               out=od[t], workspace=ws_d)
+        if rec is not None:
+            P.path_debug_set_timing_events(None, None)
+            rec["d1"][s].record()
+
+    P.path_debug_set_timing_events(None, None)
+    for _ in range(args.warmup):
+        one_step(None)
+    torch.cuda.synchronize()
+    rec = {kk: [] for kk in ("f0", "f1", "fk0", "fk1", "d1", "dk0", "dk1")}
+    for _ in range(args.steps):
+        for kk in ("f0", "f1", "fk0", "fk1", "d1"):
+            rec[kk].append(mk())
+        rec["dk0"].append([mk() for _ in range(Td)])
+        rec["dk1"].append([mk() for _ in range(Td)])
+    torch.cuda.synchronize()
+
+    clocks = Clocks(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for s in range(args.steps):
+        one_step(rec, s)
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    fwd_ms = [a.elapsed_time(b) for a, b in zip(rec["f0"], rec["f1"])]
+    fwd_kernel_ms = [a.elapsed_time(b) for a, b in zip(rec["fk0"], rec["fk1"])]
+    dec_ms = [a.elapsed_time(b) for a, b in zip(rec["f1"], rec["d1"])] if Td else [0.0]
+    dec_kernel_ms = [a.elapsed_time(b) for s in range(args.steps) for a, b in zip(rec["dk0"][s], rec["dk1"][s])]
+    fwd_ms_max = max_over_ranks(sum(fwd_ms), world)
+    dec_ms_max = max_over_ranks(sum(dec_ms), world)
+
+    attn_flops = fc.attn_flops
+    value = attn_flops * world * args.steps / (fwd_ms_max * 1e-3) / 1e12
+    fk = statistics.mean(fwd_kernel_ms)
+    achieved = attn_flops / (fk * 1e-3) / 1e12
+    lines = {}
+    lines["roofline"] = {"kernel": "path_fwd (right-to-left scan; UT prep excluded)", "bound": "tensor",
+                         "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s", "frac": achieved / bf16_tf,
+                         "peak_source": peak_src + " bf16 burst", "traffic": None,
+                         "flops_per_launch": attn_flops, "flops_kind": "attention-equivalent 4*B*H*d*L^2/2"}
+    dec_obj = None
+    if Td:
+        # algorithmic bytes per decode step: K read + K write + V read of every cached row
+        bytes_steps = [3.0 * dc.B * dc.H * (dc.n0 + t) * dc.d * 2 for t in range(Td)]
+        avg_bytes = sum(bytes_steps) / Td
+        dk_mean = statistics.mean(dec_kernel_ms)
+        dec_gbs = avg_bytes / (dk_mean * 1e-3) / 1e9
+        us_per_step = dec_ms_max * 1e3 / (args.steps * Td)
+        dec_obj = {"us_per_step": us_per_step, "steps_per_sequence": Td, "cache_tokens": dc.n0,
+                   "B": dc.B, "H": dc.H, "d": dc.d,
+                   "roofline": {"kernel": "decode_update_score", "bound": "hbm", "achieved": dec_gbs,
+                                "peak": hbm_gbs, "unit": "GB/s", "frac": dec_gbs / hbm_gbs,
+                                "peak_source": peak_src, "traffic": None, "bytes_per_launch": avg_bytes},
+                   "step_gbs": avg_bytes / (us_per_step * 1e-6) / 1e9}
+
+    # end to end through the public API with host buffers: pinned inputs -> device, forward, o -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        hq, hk, hv, hw = (t.pin_memory() for t in (x.q, x.k, x.v, x.w))
+        hb = x.beta.pin_memory()
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        dq_, dk_, dv_, dw_, db_ = (torch.empty_like(t) for t in (q, k, v, w, beta))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hw, hb))
+        d2h = ho.numel() * ho.element_size()
+
+        def e2e_step():
+            for dst, src in ((dq_, hq), (dk_, hk), (dv_, hv), (dw_, hw), (db_, hb)):
+                dst.copy_(src, non_blocking=True)
+            P.path_attn_fwd(dq_, dk_, dv_, dw_, db_, scale=x.scale, out=o, workspace=ws_f)
+            ho.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        ms = max_over_ranks(a.elapsed_time(b), world)
+        e2e = {"value": attn_flops * world * args.e2e_steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        v_cpu, dt, cores, desc = oracle_sample(args.cpu_heads)
+        cpu = {"value": v_cpu, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "seconds": dt}
+
+    launches_per_step = 2 + 2 * Td  # UT prep + scan; decode: update/score + combine
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded CPU generator; no dataset or trained weights)",
+            "config": {"workload": "PaTH forward B8 H12 L4096 d128 bf16 (760M-shaped) + decode B64 H12 d128 "
+                                   "bf16 at a 32768-token cache, %d steps" % Td,
+                       "B": fc.B, "H": fc.H, "L": fc.L, "d": fc.d, "global_batch": fc.B * world,
+                       "seq_len": fc.L, "parallelism": "replicas (b,h)-independent" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (forward 384 MiB of q,k,v,w; decode caches 13 GB)"},
+            "fwd_ms": fwd_ms_max / args.steps, "fwd_kernel_ms": fk,
+            "decode": dec_obj, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": launches_per_step * args.steps}
+    if rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-heads", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        sys.stderr.write("note: warm-up raised to 3 steps\n")
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, rank, world)
+    else:
+        rc = run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

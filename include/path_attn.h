@@ -163,6 +163,16 @@ int path_get_status(const void* workspace, path_stream_t stream);
  */
 void path_debug_set_fault(int mask);
 
+/*
+ * Measurement hook.  When both are non-NULL, every later forward or decode
+ * call records `ev_start` (a cudaEvent_t) on its stream immediately before
+ * launching its dominant kernel (the scan kernel of the forward, the fused
+ * update + score kernel of decode) and `ev_end` immediately after it, so the
+ * caller can time that kernel alone with cudaEventElapsedTime.  Pass NULL,
+ * NULL to stop.  The events are not owned by the library.
+ */
+void path_debug_set_timing_events(void* ev_start, void* ev_end);
+
 #ifdef __cplusplus
 }
 #endif

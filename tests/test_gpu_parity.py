@@ -1,0 +1,139 @@
+"""GPU forward parity: path_attn_fwd / path_attn_fwd_fox (through the C ABI) against the fp64 oracle.
+
+Cases follow the workloads of attention_causal_attn_fwd_gb300.inputs (tiny fp32, small bf16
+with beta = 0 / beta = 2 edge positions, 760M-shaped L=4096 d=128, PaTH-FoX L=16384) plus
+ragged lengths, single-token sequences, beta special values and determinism.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_causal_attn_fwd_gb300 as P
+from attention_causal_attn_fwd_gb300 import inputs
+from gpu_common import check, check_lse, cuda, to_np
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_fwd(x: inputs.FwdInputs):
+    args = [cuda(t) for t in (x.q, x.k, x.v, x.w, x.beta)]
+    if x.log_f is not None:
+        o, lse = P.path_attn_fwd_fox(*args, cuda(x.log_f), scale=x.scale, lse=True)
+    else:
+        o, lse = P.path_attn_fwd(*args, scale=x.scale, lse=True)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _oracle(x: inputs.FwdInputs, heads=None, rows=None):
+    """Oracle on all heads, or on (head, row) samples: heads = list of (b, h), rows = list of i."""
+    f = inputs.f64
+    lf = None if x.log_f is None else f(x.log_f)
+    if heads is None:
+        return orc.path_attn(f(x.q), f(x.k), f(x.v), f(x.w), f(x.beta), lf, x.scale)
+    sel = lambda t: np.stack([t[b, h] for (b, h) in heads])
+    qs, ks, vs, ws, bs = (sel(f(t)) for t in (x.q, x.k, x.v, x.w, x.beta))
+    ls = None if lf is None else np.stack([lf[b, h] for (b, h) in heads])
+    L = x.q.shape[2]
+    flat = [hi * L + i for hi in range(len(heads)) for i in rows]
+    return orc.path_attn(qs, ks, vs, ws, bs, ls, x.scale, rows=flat)
+
+
+def _full_case(x, what):
+    o, lse = _gpu_fwd(x)
+    o_ref, lse_ref = _oracle(x)
+    check(to_np(o), o_ref, x.q.dtype, what)
+    check_lse(to_np(lse), lse_ref, x.q.dtype, what)
+
+
+def test_tiny_f32_config():
+    _full_case(inputs.FWD_CONFIGS["tiny_f32"].make(), "tiny_f32")
+
+
+def test_small_bf16_config():
+    _full_case(inputs.FWD_CONFIGS["small_bf16"].make(), "small_bf16")
+
+
+@pytest.mark.parametrize("dtype,B,H,L,d", [
+    ("f32", 1, 2, 77, 32), ("f32", 2, 1, 1, 64), ("f32", 1, 1, 200, 128), ("f32", 1, 1, 50, 16),
+    ("bf16", 1, 2, 300, 128), ("bf16", 1, 1, 1, 64), ("bf16", 2, 2, 129, 64), ("bf16", 1, 1, 257, 128),
+    ("bf16", 1, 1, 640, 128),
+])
+def test_ragged_shapes(dtype, B, H, L, d):
+    x = inputs.make_fwd(B, H, L, d, dtype, seed=100 + L + d, edge_frac=0.05)
+    _full_case(x, "ragged %s %s" % (dtype, (B, H, L, d)))
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128)])
+@pytest.mark.parametrize("beta_kind", ["zero", "two", "half_zero"])
+def test_beta_special_values(dtype, d, beta_kind):
+    x = inputs.make_fwd(1, 2, 260, d, dtype, seed=7)
+    if beta_kind == "zero":
+        x.beta.zero_()
+    elif beta_kind == "two":
+        x.beta.fill_(2.0)
+    else:
+        x.beta[..., ::2] = 0.0
+    _full_case(x, "beta %s" % beta_kind)
+
+
+@pytest.mark.parametrize("dtype,L,d", [("f32", 100, 32), ("bf16", 300, 128), ("bf16", 200, 64)])
+def test_fox_small(dtype, L, d):
+    x = inputs.make_fwd(1, 2, L, d, dtype, seed=11, fox=True)
+    _full_case(x, "fox %s" % dtype)
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 32), ("bf16", 128)])
+def test_fox_zero_gates_equal_plain(dtype, d):
+    x = inputs.make_fwd(1, 2, 200, d, dtype, seed=12)
+    args = [cuda(t) for t in (x.q, x.k, x.v, x.w, x.beta)]
+    o1 = P.path_attn_fwd(*args, scale=x.scale)
+    o2 = P.path_attn_fwd_fox(*args, torch.zeros_like(args[4]), scale=x.scale)
+    torch.cuda.synchronize()
+    assert float((o1.float() - o2.float()).abs().max()) <= (1e-6 if dtype == "f32" else 1e-2)
+
+
+def test_deterministic():
+    x = inputs.make_fwd(1, 2, 300, 128, "bf16", seed=13)
+    o1, l1 = _gpu_fwd(x)
+    o2, l2 = _gpu_fwd(x)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def _sampled_rows(L, rng, n=10):
+    rows = {0, 1, 63, 64, 127, 128, L - 1, L // 2}
+    rows |= set(int(i) for i in rng.integers(0, L, n))
+    return sorted(r for r in rows if r < L)
+
+
+def test_760m_shaped_full_size_sampled():
+    """B8 H12 L4096 d128 bf16 (the timed workload): the whole forward on the GPU, sampled rows on the oracle."""
+    cfg = inputs.FWD_CONFIGS["path760m_bf16"]
+    x = cfg.make()
+    o, lse = _gpu_fwd(x)
+    rng = np.random.default_rng(0)
+    heads = [(0, 0), (3, 7), (7, 11)]
+    rows = _sampled_rows(cfg.L, rng)
+    o_ref, lse_ref = _oracle(x, heads, rows)
+    got = np.concatenate([to_np(o[b, h, rows]) for (b, h) in heads])
+    got_lse = np.concatenate([to_np(lse[b, h, rows]) for (b, h) in heads])
+    check(got, o_ref, torch.bfloat16, "path760m sampled")
+    check_lse(got_lse, lse_ref, torch.bfloat16, "path760m sampled")
+    assert torch.isfinite(o).all()
+
+
+def test_fox_16k_full_size_sampled():
+    """B1 H12 L16384 d128 bf16 PaTH-FoX: whole forward on the GPU, sampled rows on the oracle."""
+    cfg = inputs.FWD_CONFIGS["fox16k_bf16"]
+    x = cfg.make()
+    o, lse = _gpu_fwd(x)
+    rng = np.random.default_rng(1)
+    heads = [(0, 0), (0, 5), (0, 11)]
+    rows = _sampled_rows(cfg.L, rng, n=6)
+    o_ref, lse_ref = _oracle(x, heads, rows)
+    got = np.concatenate([to_np(o[b, h, rows]) for (b, h) in heads])
+    got_lse = np.concatenate([to_np(lse[b, h, rows]) for (b, h) in heads])
+    check(got, o_ref, torch.bfloat16, "fox16k sampled")
+    check_lse(got_lse, lse_ref, torch.bfloat16, "fox16k sampled")
+    assert torch.isfinite(o).all()
