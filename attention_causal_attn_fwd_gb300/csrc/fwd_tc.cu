@@ -1,16 +1,494 @@
-// bf16 forward entry (staging: routes to the CUDA-core kernel at chunk 64).
+// PaTH causal attention forward on GB300 tensor cores (bf16 in, fp32 accumulate).
+//
+// Blockwise algorithm of "Resumo Técnico: Atenção PaTH"
+// (gist.science/pt/paper/2505.16381), §3 "Algoritmo Estilo FlashAttention":
+// boundary-adjusted queries/keys per chunk (from the UT-prep kernel,
+// ut_prep.cu), then a right-to-left scan over key/value blocks that carries
+// the Householder product on the query side, never forming the L x L matrix.
+//
+// One CTA owns a tile of 128 queries (= one chunk n of one head) and walks the
+// key/value blocks m = n (diagonal), n-1, ..., 0.  Per block m < n, with the
+// transported query q~ (fp32 master in TMEM, bf16 copy in shared memory):
+//   MMA1  [S_k | S_w] = q~ [khat_m ; W_m]^T          (M=128, N=256, K=d)
+//   MMA3  q~ += bf16(S_w) (-U_m)                       (M=128, N=d, K=128)
+//   MMA2  O  += P V_m,  P = exp2(S_k * scale*log2e - m)  (M=128, N=d, K=128)
+// and the diagonal block uses S = Q K^T + Y (-Z)^T with the causal mask.
+// Online softmax keeps one query row per thread (TMEM lane = row), so row
+// max and sum need no cross-thread reduction.  The running max is only
+// raised (and O rescaled) when it grows by more than 2^8, which keeps every
+// exponent <= 2^8 and makes rescales rare.
+//
+// Warp roles (320 threads):
+//   warp 0      TMA producer (one lane) + TMEM allocation
+//   warp 1      tcgen05.mma issuer (one lane)
+//   warps 2-5   softmax: S_k -> P (bf16, into TMEM), row statistics, epilogue
+//   warps 6-9   query transport: S_w -> bf16 (TMEM), fp32 q~ -> bf16 q~ (smem)
+//
+// TMEM (512 columns x 128 lanes, fp32): [0,128) S_k / P, [128,256) S_w /
+// bf16(S_w), [256,256+d) O, [384,384+d) q~ master.
+// Shared memory (1024-aligned, 128-byte swizzled tiles as TMA writes them):
+//   SM_Q  32 KB  Q (diagonal) then bf16 q~, K-major, 64-column chunks of 16 KB
+//   SM_KW 64 KB  per 64-column chunk c (32 KB): rows 0-127 khat_m (or K),
+//                rows 128-255 W_m (or -Z): one N=256 B operand for MMA1
+//   SM_V  32 KB  V_m, MN-major B operand (64-column boxes of 16 KB)
+//   SM_U  32 KB  -U_m (MN-major) or, on the diagonal, Y (K-major)
+// Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
+// PATH_ERR_TIMEOUT in the workspace status word, every role stops, pending
+// copies and MMAs are drained (bounded) and TMEM is freed before exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "sm100_ptx.cuh"
+#include "ut_prep.cuh"
 
 namespace pathattn {
-cudaError_t fwd_simt_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                          const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
-                          unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
-int tc_chunk(int d) { (void)d; return 64; }
+using namespace sm100;
+
+constexpr int kTcC = 128;
+constexpr int kTcThreads = 320;
+constexpr uint32_t SM_Q = 0, SM_KW = 32768, SM_V = 98304, SM_U = 131072, SM_BAR = 163840;
+constexpr uint32_t SM_TOTAL = SM_BAR + 256;
+constexpr size_t kTcSmem = SM_TOTAL + 1024;  // + alignment slack
+constexpr uint32_t TM_S = 0, TM_SW = 128, TM_O = 256, TM_Q = 384;
+
+enum Bar { B_QFULL = 0, B_KWFULL, B_VUFULL, B_KWEMPTY, B_VUEMPTY, B_SFULL, B_SWREADY, B_PREADY, B_QUPD, B_QTREADY,
+           B_ODONE, B_DRAIN, B_COUNT };
+
+struct TcParams {
+    int L, Lp, ntiles;
+    float sl2;                 // scale * log2(e)
+    const float* qhat;         // [BH, Lp, d] fp32
+    const float* cum;          // [BH, Lp] fp32 (FoX)
+    __nv_bfloat16* o;          // [BH, L, d]
+    float* lse;                // [BH, L] or null
+    WsHeader* hdr;
+    unsigned long long limit_ns;
+    int fault;                 // test hook: skip one producer signal
+};
+
+// K-major, 128-byte-swizzled operand: 64-column chunks `chunk_stride` apart,
+// k-step kk (16 columns) inside a chunk is a 32-byte offset.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, uint32_t chunk_stride) {
+    return sdesc_sw128(base + (uint32_t)(kk >> 2) * chunk_stride + (uint32_t)(kk & 3) * 32u, 16, 1024);
+}
+// MN-major, 128-byte-swizzled B operand [128 K-rows x N]: 64-wide N chunks
+// 16 KB apart (LBO), 8-row groups 1 KB apart (SBO); k-step = 16 rows.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
+    return sdesc_sw128(base + (uint32_t)kk * 2048u, 16384, 1024);
+}
+
+// Drain wait used after an abort: bounded, ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > limit) break;
+}
+
+template <int D, bool FOX>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    path_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_khat, const __grid_constant__ CUtensorMap tm_un,
+                const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_zn,
+                const TcParams p) {
+    static_assert(D == 64 || D == 128, "head dim");
+    constexpr int KCH = D / 64;          // 64-column chunks of the head dim
+    constexpr uint32_t ROWB = 128u * D * 2u;  // bytes of one [128 x D] bf16 tile
+    constexpr uint32_t IDESC_S256 = idesc_bf16(256, false);
+    constexpr uint32_t IDESC_S128 = idesc_bf16(128, false);
+    constexpr uint32_t IDESC_PV = idesc_bf16(D, true);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t bar0 = sb + SM_BAR;
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 128);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_BAR + 132);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x;
+    const int n = p.ntiles - 1 - (int)blockIdx.y;  // longest tiles first
+    const int row0 = n * kTcC;
+
+    if (threadIdx.x == 0) {
+        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 1, 128, 128, 1, 128, 1, 1};
+        for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.hdr, p.limit_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_w);
+            prefetch_tmap(&tm_khat); prefetch_tmap(&tm_un); prefetch_tmap(&tm_y); prefetch_tmap(&tm_zn);
+            int kw_issued = 0, vu_issued = 0;
+            bool ok = true;
+            mbar_expect_tx(bar(B_QFULL), ROWB);
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_Q + c * 16384, &tm_q, bar(B_QFULL), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_KWFULL), ROWB + 32768);
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_KW + c * 32768, &tm_k, bar(B_KWFULL), c * 64, row0, bh);
+            for (int c = 0; c < 2; ++c)
+                tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_zn, bar(B_KWFULL), c * 64, row0, bh);
+            ++kw_issued;
+            mbar_expect_tx(bar(B_VUFULL), ROWB + 32768);
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V + c * 16384, &tm_v, bar(B_VUFULL), c * 64, row0, bh);
+            for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_U + c * 16384, &tm_y, bar(B_VUFULL), c * 64, row0, bh);
+            ++vu_issued;
+            for (int it = 1; it <= n && ok; ++it) {
+                const int r = (n - it) * kTcC;
+                if (!(ok = mbar_wait(bar(B_KWEMPTY), (it - 1) & 1, wc, 1))) break;
+                mbar_expect_tx(bar(B_KWFULL), 2 * ROWB);
+                for (int c = 0; c < KCH; ++c) {
+                    tma_load_3d(sb + SM_KW + c * 32768, &tm_khat, bar(B_KWFULL), c * 64, r, bh);
+                    tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_w, bar(B_KWFULL), c * 64, r, bh);
+                }
+                ++kw_issued;
+                if (!(ok = mbar_wait(bar(B_VUEMPTY), (it - 1) & 1, wc, 2))) break;
+                if (p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
+                mbar_expect_tx(bar(B_VUFULL), 2 * ROWB);
+                for (int c = 0; c < KCH; ++c) {
+                    tma_load_3d(sb + SM_V + c * 16384, &tm_v, bar(B_VUFULL), c * 64, r, bh);
+                    tma_load_3d(sb + SM_U + c * 16384, &tm_un, bar(B_VUFULL), c * 64, r, bh);
+                }
+                ++vu_issued;
+            }
+            // copies still in flight must land before the CTA exits
+            drain_wait(bar(B_QFULL), 0, p.limit_ns);
+            drain_wait(bar(B_KWFULL), (kw_issued - 1) & 1, p.limit_ns);
+            drain_wait(bar(B_VUFULL), (vu_issued - 1) & 1, p.limit_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KWFULL), 0, wc, 11) &&
+                      mbar_wait(bar(B_VUFULL), 0, wc, 12);
+            if (ok) {
+                tc_fence_after();
+                // diagonal: S = Q K^T + Y (-Z)^T
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
+                           IDESC_S128, kk > 0);
+                for (int kk = 0; kk < kTcC / 16; ++kk)
+                    mma_ss(tmem + TM_S, kmajor_desc(sb + SM_U, kk, 16384),
+                           kmajor_desc(sb + SM_KW + 16384, kk, 32768), IDESC_S128, 1);
+                mma_commit(bar(B_SFULL));
+                mma_commit(bar(B_KWEMPTY));
+                ok = mbar_wait(bar(B_PREADY), 0, wc, 13);
+            }
+            if (ok) {
+                tc_fence_after();
+                for (int kk = 0; kk < kTcC / 16; ++kk)
+                    mma_ts(tmem + TM_O, tmem + TM_S + kk * 8, mnmajor_desc(sb + SM_V, kk), IDESC_PV, kk > 0);
+                mma_commit(bar(B_ODONE));
+                mma_commit(bar(B_VUEMPTY));
+            }
+            for (int it = 1; it <= n && ok; ++it) {
+                const int m = n - it;
+                if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
+                if (!(ok = mbar_wait(bar(B_KWFULL), it & 1, wc, 15))) break;
+                tc_fence_after();
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
+                           IDESC_S256, kk > 0);
+                mma_commit(bar(B_SFULL));
+                mma_commit(bar(B_KWEMPTY));
+                if (!(ok = mbar_wait(bar(B_VUFULL), it & 1, wc, 16))) break;
+                if (m > 0) {
+                    if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < kTcC / 16; ++kk)
+                        mma_ts(tmem + TM_Q, tmem + TM_SW + kk * 8, mnmajor_desc(sb + SM_U, kk), IDESC_PV, 1);
+                    mma_commit(bar(B_QUPD));
+                }
+                if (!(ok = mbar_wait(bar(B_PREADY), it & 1, wc, 18))) break;
+                tc_fence_after();
+                for (int kk = 0; kk < kTcC / 16; ++kk)
+                    mma_ts(tmem + TM_O, tmem + TM_S + kk * 8, mnmajor_desc(sb + SM_V, kk), IDESC_PV, 1);
+                mma_commit(bar(B_ODONE));
+                mma_commit(bar(B_VUEMPTY));
+            }
+            // every issued MMA completes before TMEM is released
+            mma_commit(bar(B_DRAIN));
+            drain_wait(bar(B_DRAIN), 0, p.limit_ns);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------------ softmax warps
+        const int r = 32 * (warp & 3) + lane;  // query row within the tile (= TMEM lane)
+        const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const float* cumh = FOX ? p.cum + (size_t)bh * p.Lp : nullptr;
+        const float ci = FOX ? cumh[row0 + r] : 0.f;
+        constexpr float kL2e = 1.4426950408889634f;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int it = 0; it <= n; ++it) {
+            const int m = n - it;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 20));
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tl + TM_S + 32 * c, raw);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]) * p.sl2;
+                if (FOX) {
+                    const float4* cj = reinterpret_cast<const float4*>(cumh + m * kTcC + 32 * c);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 cv = __ldg(cj + j4);
+                        s[32 * c + 4 * j4 + 0] += (ci - cv.x) * kL2e;
+                        s[32 * c + 4 * j4 + 1] += (ci - cv.y) * kL2e;
+                        s[32 * c + 4 * j4 + 2] += (ci - cv.z) * kL2e;
+                        s[32 * c + 4 * j4 + 3] += (ci - cv.w) * kL2e;
+                    }
+                }
+            }
+            if (it == 0) {
+#pragma unroll
+                for (int j = 0; j < 128; ++j)
+                    if (j > r) s[j] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 128; ++j) mx = fmaxf(mx, s[j]);
+            const float m_new = fmaxf(m_run, mx);
+            const bool rescale = m_new > m_run + 8.0f;
+            const float m_use = rescale ? m_new : m_run;
+            const float alpha = rescale ? exp2f(m_run - m_use) : 1.0f;
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = exp2f(s[64 * c + 2 * j] - m_use);
+                    const float p1 = exp2f(s[64 * c + 2 * j + 1] - m_use);
+                    sum += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tl + TM_S + 32 * c, pk);
+            }
+            l_run = l_run * alpha + sum;
+            if (rescale && it > 0) {
+                // O is stable once the previous block's P V has completed
+                const bool ok2 = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (it - 1) & 1, wc, 21));
+                if (!ok2) { ok = false; break; }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tl + TM_O + 32 * c, ov);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+                    tmem_st32(tl + TM_O + 32 * c, ov);
+                }
+            }
+            m_run = m_use;
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_PREADY));
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), n & 1, wc, 22));
+        if (ok) {
+            tc_fence_after();
+            const int row = row0 + r;
+            const float inv = 1.0f / l_run;
+            __nv_bfloat16* orow = p.o + ((size_t)bh * p.L + row) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(tl + TM_O + 32 * c, ov);
+                tmem_wait_ld();
+                if (row < p.L) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4 v;
+                        v.x = pack_bf16x2(__uint_as_float(ov[8 * g + 0]) * inv, __uint_as_float(ov[8 * g + 1]) * inv);
+                        v.y = pack_bf16x2(__uint_as_float(ov[8 * g + 2]) * inv, __uint_as_float(ov[8 * g + 3]) * inv);
+                        v.z = pack_bf16x2(__uint_as_float(ov[8 * g + 4]) * inv, __uint_as_float(ov[8 * g + 5]) * inv);
+                        v.w = pack_bf16x2(__uint_as_float(ov[8 * g + 6]) * inv, __uint_as_float(ov[8 * g + 7]) * inv);
+                        st_global_v4(orow + 32 * c + 8 * g, v);
+                    }
+                }
+            }
+            if (p.lse && row < p.L) p.lse[(size_t)bh * p.L + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+        }
+    } else {
+        // ------------------------------------------------------------------ query-transport warps
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        uint8_t* qrow_s = sm + SM_Q + r * 128;  // this row's 128-byte line in chunk 0
+        const int sw = r & 7;
+        // bf16 q~ row -> swizzled K-major tile (16-byte granule g of chunk c at (g ^ (r & 7)))
+        auto put_granule = [&](int G, uint4 v) {
+            *reinterpret_cast<uint4*>(qrow_s + (G >> 3) * 16384 + (((G & 7) ^ sw) << 4)) = v;
+        };
+        bool ok = n > 0 && __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), 0, wc, 30));
+        if (ok) {
+            // the diagonal MMA has consumed Q: load qhat (fp32) as the initial q~
+            tc_fence_after();
+            const float4* src = reinterpret_cast<const float4*>(p.qhat + ((size_t)bh * p.Lp + row0 + r) * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 x = __ldg(src + 8 * c + j4);
+                    v[4 * j4 + 0] = __float_as_uint(x.x);
+                    v[4 * j4 + 1] = __float_as_uint(x.y);
+                    v[4 * j4 + 2] = __float_as_uint(x.z);
+                    v[4 * j4 + 3] = __float_as_uint(x.w);
+                }
+                tmem_st32(tl + TM_Q + 32 * c, v);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint4 q;
+                    q.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
+                    q.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+                    q.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+                    q.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+                    put_granule(4 * c + g, q);
+                }
+            }
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_QTREADY));
+        }
+        for (int it = 1; it < n && ok; ++it) {  // block m = n - it > 0 needs the transport
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 31));
+            if (!ok) break;
+            tc_fence_after();
+            // S_w (fp32, columns [128,256)) -> bf16 pairs in columns [128,192)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32], pk[16];
+                tmem_ld32(tl + TM_SW + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                tmem_st16(tl + TM_SW + 16 * c, pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(B_SWREADY));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QUPD), (it - 1) & 1, wc, 32));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tl + TM_Q + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint4 q;
+                    q.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
+                    q.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
+                    q.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
+                    q.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
+                    put_granule(4 * c + g, q);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_QTREADY));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ----------------------------------------------------------------------------- host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 3-D bf16 map over [bh][rows][cols] with 64 x 128 boxes and 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, int cols, int rows, int bh) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)bh};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int tc_chunk(int d) { (void)d; return kTcC; }
 bool tc_supported(int d) { return d == 64 || d == 128; }
+
+template <int D>
+static cudaError_t launch_tc(const void* q, const void* k, const void* v, const void* w, const float* log_f,
+                            void* o, float* lse, int BH, int L, float scale, unsigned char* ws, const FwdLayout& lay,
+                            int fault, cudaStream_t st) {
+    CUtensorMap mq, mk, mv, mw, mkh, mun, my, mzn;
+    if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mv, v, D, L, BH) ||
+        !make_map(&mw, w, D, L, BH) || !make_map(&mkh, ws + lay.khat, D, lay.Lp, BH) ||
+        !make_map(&mun, ws + lay.un, D, lay.Lp, BH) || !make_map(&my, ws + lay.y, kTcC, lay.Lp, BH) ||
+        !make_map(&mzn, ws + lay.zn, kTcC, lay.Lp, BH))
+        return cudaErrorInvalidValue;
+    TcParams p;
+    p.L = L;
+    p.Lp = lay.Lp;
+    p.ntiles = cdiv(L, kTcC);
+    p.sl2 = scale * 1.4426950408889634f;
+    p.qhat = reinterpret_cast<const float*>(ws + lay.qhat);
+    p.cum = reinterpret_cast<const float*>(ws + lay.cum);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    p.hdr = reinterpret_cast<WsHeader*>(ws);
+    p.limit_ns = fault ? 20000000ull : 2000000000ull;  // 20 ms under the test hook, else 2 s
+    p.fault = fault;
+    auto kern = log_f ? path_fwd_tc<D, true> : path_fwd_tc<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    if (e != cudaSuccess) return e;
+    mark_start(st);
+    kern<<<dim3(BH, p.ntiles), kTcThreads, kTcSmem, st>>>(mq, mk, mv, mw, mkh, mun, my, mzn, p);
+    mark_end(st);
+    return cudaGetLastError();
+}
+
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
                         const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
                         unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st) {
-    (void)fault_mask;
-    return fwd_simt_bf16(q, k, v, w, beta, log_f, o, lse, BH, L, d, scale, ws, lay, st);
+    cudaError_t e = launch_ut_prep(PATH_BF16, kTcC, d, q, k, w, beta, log_f, BH, L, ws, lay, st);
+    if (e != cudaSuccess) return e;
+    if (d == 64) return launch_tc<64>(q, k, v, w, log_f, o, lse, BH, L, scale, ws, lay, fault_mask, st);
+    if (d == 128) return launch_tc<128>(q, k, v, w, log_f, o, lse, BH, L, scale, ws, lay, fault_mask, st);
+    return cudaErrorInvalidValue;
 }
+
 }  // namespace pathattn

@@ -45,8 +45,12 @@ def test_decode_small_vs_oracle(dtype, d):
                 f(steps[4][:, b, h]), scale)
             check(to_np(o[:, b, h]), o_ref, kc.dtype, "decode o b%d h%d" % (b, h))
             check_lse(to_np(lse[:, b, h]), lse_ref, kc.dtype, "decode lse")
-            tol = 1e-5 if dtype == "f32" else 3e-2
-            assert np.abs(to_np(kcg[b, h]) - kc_ref).max() <= tol
+            err = np.abs(to_np(kcg[b, h]) - kc_ref)
+            if dtype == "f32":
+                assert err.max() <= 1e-5
+            else:  # the bf16 cache is rounded once per step: at most T half-ulps of drift per element
+                bound = T * 2.0 ** -8 * np.abs(kc_ref).max(axis=1, keepdims=True)
+                assert np.all(err <= bound), float((err - bound).max())
             assert np.array_equal(to_np(vcg[b, h]), vc_ref)
 
 
