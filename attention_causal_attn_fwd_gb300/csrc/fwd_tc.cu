@@ -283,7 +283,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_st32(tl + TM_S + 32 * c, pk);
             }
             l_run = l_run * alpha + sum;
-            if (rescale && it > 0) {
+            // The O rescale uses warp-collective TMEM loads/stores, so the whole
+            // warp takes it when any of its rows needs it (alpha = 1 elsewhere).
+            if (__any_sync(0xffffffffu, rescale && it > 0)) {
                 // O is stable once the previous block's P V has completed
                 const bool ok2 = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (it - 1) & 1, wc, 21));
                 if (!ok2) { ok = false; break; }
