@@ -35,6 +35,21 @@ DEC_NAME = "decode32k_bf16"
 METRIC = "PaTH fwd TFLOP/s (L=4096,d=128,bf16) & decode µs/step @32K cache, % roofline"
 
 
+def _traffic(kernel: str, units: float):
+    """DRAM bytes per launch from the committed ncu capture (profiles/traffic.json), scaled
+    to `units`; None when the kernel's source changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        t = json.load(open(p))[kernel]
+        src = open(os.path.join(ROOT, t["source"]), "rb").read()
+    except (OSError, KeyError, ValueError):
+        return None
+    if hashlib.sha256(src).hexdigest()[:16] != t["sha256_16"]:
+        return None
+    return t["captured_bytes"] * units / t["captured_units"]
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -179,8 +194,13 @@ def run_ours(args, rank, world, local):
 
     dev = torch.device("cuda", local)
     hbm_gbs, bf16_tf, bf16_sust, peak_src = _peaks()
+    import dataclasses
     fc = inputs.FWD_CONFIGS[FWD_NAME]
     dc = inputs.DECODE_CONFIGS[DEC_NAME]
+    if args.fwd_B != fc.B:  # smaller batch, only for profiling captures
+        fc = dataclasses.replace(fc, B=args.fwd_B)
+    if args.decode_B != dc.B:
+        dc = dataclasses.replace(dc, B=args.decode_B)
     x = fc.make()
     q, k, v, w, beta = (t.to(dev) for t in (x.q, x.k, x.v, x.w, x.beta))
     o = torch.empty_like(q)
@@ -258,7 +278,7 @@ def run_ours(args, rank, world, local):
     lines = {}
     lines["roofline"] = {"kernel": "path_fwd (right-to-left scan; UT prep excluded)", "bound": "tensor",
                          "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s", "frac": achieved / bf16_tf,
-                         "peak_source": peak_src + " bf16 burst", "traffic": None,
+                         "peak_source": peak_src + " bf16 burst", "traffic": _traffic("path_fwd_tc", fc.B * fc.H),
                          "flops_per_launch": attn_flops, "flops_kind": "attention-equivalent 4*B*H*d*L^2/2"}
     dec_obj = None
     if Td:
@@ -272,7 +292,8 @@ def run_ours(args, rank, world, local):
                    "B": dc.B, "H": dc.H, "d": dc.d,
                    "roofline": {"kernel": "decode_update_score", "bound": "hbm", "achieved": dec_gbs,
                                 "peak": hbm_gbs, "unit": "GB/s", "frac": dec_gbs / hbm_gbs,
-                                "peak_source": peak_src, "traffic": None, "bytes_per_launch": avg_bytes},
+                                "peak_source": peak_src, "traffic": _traffic("decode_update_score", dc.B * dc.H),
+                                "bytes_per_launch": avg_bytes},
                    "step_gbs": avg_bytes / (us_per_step * 1e-6) / 1e9}
 
     # end to end through the public API with host buffers: pinned inputs -> device, forward, o -> host
@@ -315,8 +336,8 @@ def run_ours(args, rank, world, local):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded CPU generator; no dataset or trained weights)",
-            "config": {"workload": "PaTH forward B8 H12 L4096 d128 bf16 (760M-shaped) + decode B64 H12 d128 "
-                                   "bf16 at a 32768-token cache, %d steps" % Td,
+            "config": {"workload": "PaTH forward B%d H12 L4096 d128 bf16 (760M-shaped) + decode B%d H12 d128 "
+                                   "bf16 at a 32768-token cache, %d steps" % (fc.B, dc.B, Td),
                        "B": fc.B, "H": fc.H, "L": fc.L, "d": fc.d, "global_batch": fc.B * world,
                        "seq_len": fc.L, "parallelism": "replicas (b,h)-independent" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (forward 384 MiB of q,k,v,w; decode caches 13 GB)"},
@@ -336,8 +357,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-heads", type=int, default=8)
+    ap.add_argument("--cpu-heads", type=int, default=96)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fwd-B", type=int, default=8, help="forward batch (8 = the timed workload)")
+    ap.add_argument("--decode-B", type=int, default=64, help="decode batch (64 = the timed workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         sys.stderr.write("note: warm-up raised to 3 steps\n")
