@@ -33,7 +33,7 @@ _DT = {torch.float32: PATH_F32, torch.bfloat16: PATH_BF16}
 
 EXPORTED = ("path_version", "path_status_string", "path_attn_workspace_bytes", "path_attn_fwd",
             "path_attn_fwd_fox", "path_decode_workspace_bytes", "path_kcache_update", "path_decode_step",
-            "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events")
+            "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events", "path_decode_step_noalloc")
 
 
 class PathLibraryError(RuntimeError):
@@ -80,6 +80,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.path_decode_step.argtypes = [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _i, _i, _vp, _fp, _i, _i, _i,
                                      ctypes.c_float, _i, _vp, _sz, _vp]
     lib.path_decode_step.restype = _i
+    lib.path_decode_step_noalloc.argtypes = [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _i, _i, _vp, _fp, _i, _i, _i,
+                                             ctypes.c_float, _i, _vp]
+    lib.path_decode_step_noalloc.restype = _i
     lib.path_get_status.argtypes = [_vp, _vp]
     lib.path_get_status.restype = _i
     lib.path_debug_set_fault.argtypes = [_i]
@@ -225,3 +228,29 @@ def path_debug_set_timing_events(ev_start=None, ev_end=None):
     """Record two torch.cuda.Events around the dominant kernel of each later call (None, None stops)."""
     h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
     load().path_debug_set_timing_events(h(ev_start), h(ev_end))
+
+
+def path_decode_step_noalloc(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached: int, scale=None, out=None,
+                             lse=False):
+    """path_decode_step without a workspace: for callers that cannot allocate device memory while decoding.
+
+    The library's built-in scratch (PATH_DECODE_NOALLOC_SCRATCH_BYTES = 8 MiB per GPU) replaces the
+    workspace; sizes that need more raise PathError(PATH_ERR_WORKSPACE).  Calls that may overlap on the
+    GPU share that scratch and must be ordered.  Pass ``out`` (and no ``lse``) to avoid any allocation
+    here as well.
+    """
+    lib = load()
+    B, H, n_max, d = kcache.shape
+    dt = kcache.dtype
+    _dev(kcache, "kcache")
+    _dev(vcache, "vcache", dt, (B, H, n_max, d))
+    for name, t in (("q_t", q_t), ("k_t", k_t), ("v_t", v_t), ("w_t", w_t)):
+        _dev(t, name, dt, (B, H, d))
+    _dev(beta_t, "beta_t", torch.float32, (B, H))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q_t) if out is None else out
+    lse_t = torch.empty((B, H), dtype=torch.float32, device=q_t.device) if lse else None
+    _check(lib.path_decode_step_noalloc(_ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(kcache),
+                                        _ptr(vcache), int(n_cached), n_max, _ptr(o), _ptr(lse_t), B, H, d,
+                                        ctypes.c_float(scale), _DT[dt], _stream()), "path_decode_step_noalloc")
+    return (o, lse_t) if lse else o

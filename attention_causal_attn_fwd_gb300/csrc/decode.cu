@@ -294,3 +294,72 @@ cudaError_t kcache_update_launch(int dtype, int d, void* kc, int n_cached, int n
 }
 
 }  // namespace pathattn
+
+// ----------------------------------------------------------------------------- allocation-free decode step
+// Scratch for path_decode_step_noalloc: the split-K partials and the status
+// header live in this file-scope device array instead of a caller workspace.
+// Every GPU that loads the library holds it until the process exits.
+#include <cstdio>
+#include <mutex>
+
+namespace pathattn {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[PATH_DECODE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_decode_scratch for the current device, looked up once per
+// device.  In host code the array's name is only a host-side stand-in, so the
+// kernels are given this address instead.
+static int noalloc_scratch_address(unsigned char** out) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return PATH_ERR_CUDA;
+    if (dev >= kMaxDevices) return PATH_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            std::fprintf(stderr, "pathattn: cudaGetSymbolAddress for the decode scratch failed: %s\n",
+                         cudaGetErrorString(e));
+            return PATH_ERR_CUDA;
+        }
+        addr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(addr[dev]);
+    return PATH_OK;
+}
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace pathattn
+
+extern "C" int path_decode_step_noalloc(const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                                        const float* beta_t, void* kcache, void* vcache, int n_cached, int n_max,
+                                        void* o_t, float* lse_t, int B, int H, int d, float scale, int dtype,
+                                        path_stream_t stream) {
+    using namespace pathattn;
+    if (B < 1 || H < 1 || n_max < 1 || n_cached < 0) return PATH_ERR_INVALID;
+    if (n_cached + 1 > n_max) return PATH_ERR_INVALID;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
+    if (d != 16 && d != 32 && d != 64 && d != 128) return PATH_ERR_UNSUPPORTED;
+    if (!q_t || !k_t || !v_t || !w_t || !beta_t || !kcache || !vcache || !o_t) return PATH_ERR_INVALID;
+    const void* ptrs[] = {q_t, k_t, v_t, w_t, kcache, vcache, o_t};
+    for (const void* p : ptrs)
+        if (!al16(p)) return PATH_ERR_INVALID;
+    const DecLayout lay = dec_layout(B, H, n_max, d);
+    if (lay.total > (size_t)PATH_DECODE_NOALLOC_SCRATCH_BYTES) {
+        std::fprintf(stderr,
+                     "pathattn: path_decode_step_noalloc needs %zu bytes of scratch for B=%d H=%d n_max=%d d=%d, "
+                     "more than its built-in %zu bytes; use path_decode_step with a caller workspace\n",
+                     lay.total, B, H, n_max, d, (size_t)PATH_DECODE_NOALLOC_SCRATCH_BYTES);
+        return PATH_ERR_WORKSPACE;
+    }
+    unsigned char* ws = nullptr;
+    const int rc = noalloc_scratch_address(&ws);
+    if (rc != PATH_OK) return rc;
+    const cudaError_t e = decode_step(dtype, d, q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, n_max, o_t,
+                                      lse_t, B * H, scale, ws, lay, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA;
+}

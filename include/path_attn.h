@@ -173,6 +173,36 @@ void path_debug_set_fault(int mask);
  */
 void path_debug_set_timing_events(void* ev_start, void* ev_end);
 
+/*
+ * Allocation-free decode step.  The paper has no counterpart: this entry point
+ * exists for callers that cannot allocate device memory when they decode, for
+ * instance a runtime whose device memory is wholly owned by another allocator,
+ * or a latency-critical serving loop that must never call cudaMalloc (which can
+ * fail, and can synchronise the device) once it is running.  It computes
+ * exactly what path_decode_step computes, with the same arguments except the
+ * workspace: the split-K scratch is a fixed device array inside the library,
+ * PATH_DECODE_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the
+ * library until the process exits.
+ *   - Scratch needed is path_decode_workspace_bytes(B, H, n_max, d); sizes that
+ *     need more than PATH_DECODE_NOALLOC_SCRATCH_BYTES are rejected with
+ *     PATH_ERR_WORKSPACE (and a message on stderr) before anything is launched.
+ *     The 8 MiB covers B*H = 768 heads of d = 128 up to n_max = 43008.
+ *   - The first call on each device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - No call allocates or frees memory.  All calls share the one array, which
+ *     keeps the previous call's contents; everything a step reads from it is
+ *     written earlier in the same step.  Calls that can overlap on the GPU (two
+ *     streams, or two host threads on one device) race on the array: order them.
+ *   - Launch errors are returned; there is no device-side status to read with
+ *     path_get_status (the decode kernels have no waits that can expire).
+ */
+#define PATH_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int path_decode_step_noalloc(const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                             const float* beta_t, void* kcache, void* vcache, int n_cached, int n_max,
+                             void* o_t, float* lse_t, int B, int H, int d, float scale, int dtype,
+                             path_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

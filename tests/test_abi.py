@@ -112,3 +112,16 @@ def test_package_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"(import\s+oracle|from\s+oracle|oracle/|path_oracle)", src), f
+
+
+def test_noalloc_decode_rejects_sizes_beyond_its_scratch(lib):
+    """The allocation-free decode step refuses, before touching the GPU, any size whose
+    scratch would not fit in its built-in PATH_DECODE_NOALLOC_SCRATCH_BYTES (8 MiB)."""
+    limit = 8 << 20
+    assert P.path_decode_workspace_bytes(64, 12, 43008, 128) <= limit
+    assert P.path_decode_workspace_bytes(64, 12, 65537, 128) > limit
+    rc = lib.path_decode_step_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 65536, 65537, FAKE, None, 64, 12,
+                                      128, ctypes.c_float(0.1), P.PATH_BF16, None)
+    assert rc == P.PATH_ERR_WORKSPACE
+    assert lib.path_decode_step_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 5, 5, FAKE, None, 1, 1, 128,
+                                        ctypes.c_float(0.1), P.PATH_BF16, None) == P.PATH_ERR_INVALID
