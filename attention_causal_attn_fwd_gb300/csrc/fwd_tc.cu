@@ -40,6 +40,7 @@
 
 #include "common.cuh"
 #include "sm100_ptx.cuh"
+#include "tma_host.cuh"
 #include "ut_prep.cuh"
 
 namespace pathattn {
@@ -66,24 +67,6 @@ struct TcParams {
     unsigned long long limit_ns;
     int fault;                 // test hook: skip one producer signal
 };
-
-// K-major, 128-byte-swizzled operand: 64-column chunks `chunk_stride` apart,
-// k-step kk (16 columns) inside a chunk is a 32-byte offset.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, uint32_t chunk_stride) {
-    return sdesc_sw128(base + (uint32_t)(kk >> 2) * chunk_stride + (uint32_t)(kk & 3) * 32u, 16, 1024);
-}
-// MN-major, 128-byte-swizzled B operand [128 K-rows x N]: 64-wide N chunks
-// 16 KB apart (LBO), 8-row groups 1 KB apart (SBO); k-step = 16 rows.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
-    return sdesc_sw128(base + (uint32_t)kk * 2048u, 16384, 1024);
-}
-
-// Drain wait used after an abort: bounded, ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > limit) break;
-}
 
 template <int D, bool FOX>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -422,33 +405,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 // ----------------------------------------------------------------------------- host side
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 3-D bf16 map over [bh][rows][cols] with 64 x 128 boxes and 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* base, int cols, int rows, int bh) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)bh};
-    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
-    cuuint32_t box[3] = {64, 128, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
-}
-
 int tc_chunk(int d) { (void)d; return kTcC; }
 bool tc_supported(int d) { return d == 64 || d == 128; }
 

@@ -57,7 +57,7 @@ struct WaitCtl {
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false (after recording PATH_ERR_TIMEOUT and raising the abort flag) if the
 // limit expires, or false if another thread already aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
+static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
@@ -129,6 +129,36 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int N, bool b_mn_major) {
            | ((b_mn_major ? 1u : 0u) << 16)   // B major
            | ((uint32_t)(N >> 3) << 17)       // N / 8
            | ((uint32_t)(128 >> 4) << 24);    // M / 16
+}
+
+
+// Instruction descriptor with both operand majors selectable (MN-major A is
+// the transposed-A form, valid for bf16).
+__host__ __device__ constexpr uint32_t idesc_bf16_ab(int N, bool a_mn_major, bool b_mn_major) {
+    return idesc_bf16(N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
+// Barrier over a subset of the CTA's warps (ids 1..15; id 0 is __syncthreads).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// K-major, 128-byte-swizzled operand: 64-column chunks `chunk_stride` apart,
+// k-step kk (16 columns) inside a chunk is a 32-byte offset.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, uint32_t chunk_stride) {
+    return sdesc_sw128(base + (uint32_t)(kk >> 2) * chunk_stride + (uint32_t)(kk & 3) * 32u, 16, 1024);
+}
+// MN-major, 128-byte-swizzled B operand [128 K-rows x N]: 64-wide N chunks
+// 16 KB apart (LBO), 8-row groups 1 KB apart (SBO); k-step = 16 rows.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
+    return sdesc_sw128(base + (uint32_t)kk * 2048u, 16384, 1024);
+}
+
+// Drain wait used after an abort: bounded, ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > limit) break;
 }
 
 // D[tmem] (+)= A[smem] * B[smem]

@@ -1,0 +1,529 @@
+// UT-transform preparation on GB300 tensor cores (bf16 inputs, chunk C = 128).
+//
+// "Resumo Técnico: Atenção PaTH" (gist.science/pt/paper/2505.16381), §3
+// "Representação de Transformação UT": the product of a chunk's transitions
+// is I - W^T A W with A = (I + D triu_1(W W^T))^{-1} D, D = diag(beta); §3
+// "Algoritmo Estilo FlashAttention", first sub-bullet: the chunk's
+// boundary-adjusted queries and keys.  Per chunk this kernel writes
+//     -U   = -A^T W                       (scan factor, bf16)
+//      Y   = tril(Q W^T) A^T              (diagonal block, bf16)
+//     qhat = Q - Y W                      (fp32)
+//     -Z   = -triu_1(K W^T)               (diagonal block, bf16)
+//     khat = K - (Z A) W                  (bf16)
+// exactly the quantities of the CUDA-core version in ut_prep.cu.
+//
+// Products run as tcgen05 MMAs (M = 128) with fp32 accumulation in TMEM.
+// Operands that are not exact in bf16 (A, tril(QW^T), Y, Z, ZA) are split
+// into hi + lo bf16 parts and multiplied term by term (hi*hi + hi*lo + lo*hi),
+// which keeps those products close to fp32 accuracy.  The unit upper-
+// triangular inverse X = (I + D triu_1(G))^{-1} (A = X D) is solved in fp32 on
+// CUDA cores, blocked: 16 x 16 diagonal blocks by back substitution, then
+// three doubling merges X_PQ = -X_PP (D G)_PQ X_QQ on a dense copy of X kept
+// in the shared memory that held Q and K.
+//
+// One shared-memory layout — rows of 64-element, 128-byte-swizzled chunks,
+// exactly what a TMA box {64, 128} writes — serves as a K-major operand, an
+// MN-major B operand and an MN-major ("transposed") A operand, so W and A are
+// staged once each.
+//
+// Roles (320 threads): warp 0 TMA + TMEM allocation, warp 1 MMA issue,
+// warps 2-9 solve, conversions and stores (one TMEM lane = one chunk row; the
+// two warps sharing a lane quarter split the columns).  Waits are bounded;
+// a timeout sets PATH_ERR_TIMEOUT and every role stops, drains and frees TMEM.
+#include <cstdio>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+#include "tma_host.cuh"
+#include "ut_prep.cuh"
+
+namespace pathattn {
+using namespace sm100;
+
+namespace utk {
+constexpr int C = 128;
+constexpr int kThreads = 320;
+constexpr int kCompute = 256;   // warps 2-9: two warps per TMEM lane quarter
+constexpr uint32_t R0 = 0;        // W            (K-major / MN-major source)
+constexpr uint32_t R1 = 32768;    // Q, then solve temp, then A_hi
+constexpr uint32_t R2 = 65536;    // K, then A_lo
+constexpr uint32_t R3 = 98304;    // G fp32 [128][129] for the solve, then hi/lo operand (hi, hi + 32 KB = lo)
+constexpr int LDG = 129;
+constexpr uint32_t RB = R3 + 128 * LDG * 4;  // barriers, beta
+constexpr uint32_t RT = RB + 1024;            // solve temp T [64][68] fp32
+constexpr int LDT = 68;
+constexpr uint32_t TOTAL = RT + 64 * LDT * 4;
+constexpr size_t kSmem = TOTAL + 1024;
+constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
+enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN, B_COUNT };
+}  // namespace utk
+
+struct UtParams {
+    int L, Lp;
+    const float* beta;           // [BH, L]
+    const __nv_bfloat16* q;      // [BH, L, d] (row reads for the "Q -" epilogue)
+    const __nv_bfloat16* k;
+    float* qhat;                 // [BH, Lp, d]
+    __nv_bfloat16* khat;         // [BH, Lp, d]
+    __nv_bfloat16* un;           // [BH, Lp, d]
+    __nv_bfloat16* y;            // [BH, Lp, C]
+    __nv_bfloat16* zn;           // [BH, Lp, C]
+    WsHeader* hdr;
+    unsigned long long limit_ns;
+};
+
+// 8 consecutive values of row r, granule G (columns 8G..8G+7) of a K-major
+// 128-row operand, written as hi and lo bf16 parts.
+__device__ __forceinline__ void put_hilo(uint8_t* hi, uint8_t* lo, int r, int G, const float* v) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(hv);
+        const __nv_bfloat162 lv = __floats2bfloat162_rn(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+        h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+        l[e] = *reinterpret_cast<const uint32_t*>(&lv);
+    }
+    const uint32_t off = (uint32_t)(G >> 3) * 16384u + (uint32_t)r * 128u + ((uint32_t)((G & 7) ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+
+// One doubling merge of the blocked inverse, for 256 threads t: for each pair
+// of S-blocks (P, Q = P + S) on the diagonal,
+//     T    = (D G)_PQ X_QQ
+//     X_PQ = -X_PP T
+// with X dense (zeros below the diagonal, ones on it), so the products are
+// plain register-tiled loops.
+template <int S, int TM, int TN>
+__device__ __forceinline__ void merge_level(const float* sG, const float* sB, float* sX, float* sT, int t) {
+    using namespace utk;
+    constexpr int NP = C / (2 * S);
+    constexpr int TR = S / TM, TC = S / TN;
+    static_assert(NP * TR * TC == kCompute, "one tile per thread");
+    const int p = t / (TR * TC), rem = t % (TR * TC);
+    const int i0 = (rem / TC) * TM, j0 = (rem % TC) * TN;
+    const int P = 2 * p * S, Q = P + S;
+    float acc[TM][TN];
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < S; ++kk) {
+        float g[TM], x[TN];
+#pragma unroll
+        for (int u = 0; u < TM; ++u) g[u] = sG[(P + i0 + u) * LDG + Q + kk];
+#pragma unroll
+        for (int v = 0; v < TN; ++v) x[v] = sX[(Q + kk) * C + Q + j0 + v];
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+            for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(g[u], x[v], acc[u][v]);
+    }
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) sT[(p * S + i0 + u) * LDT + j0 + v] = sB[P + i0 + u] * acc[u][v];
+    named_bar_sync(1, kCompute);
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < S; ++kk) {
+        float xp[TM], tv[TN];
+#pragma unroll
+        for (int u = 0; u < TM; ++u) xp[u] = sX[(P + i0 + u) * C + P + kk];
+#pragma unroll
+        for (int v = 0; v < TN; ++v) tv[v] = sT[(p * S + kk) * LDT + j0 + v];
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+            for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(xp[u], tv[v], acc[u][v]);
+    }
+#pragma unroll
+    for (int u = 0; u < TM; ++u)
+#pragma unroll
+        for (int v = 0; v < TN; ++v) sX[(P + i0 + u) * C + Q + j0 + v] = -acc[u][v];
+    named_bar_sync(1, kCompute);
+}
+
+// X = (I + D triu_1(G))^{-1} (unit upper triangular) into the dense, zeroed
+// sX [128][128], for 256 threads t; sG holds G (upper part read).
+__device__ __forceinline__ void solve_unit_upper(const float* sG, const float* sB, float* sX, float* sT, int t) {
+    using namespace utk;
+    if (t < 128) {  // 16 x 16 diagonal blocks: thread (block I, column j) back-substitutes its column
+        const int I = t >> 4, j = t & 15, b0 = I * 16;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 14; i >= 0; --i) {
+            float acc = 0.f;
+#pragma unroll
+            for (int kk = i + 1; kk < 16; ++kk) acc = fmaf(sG[(b0 + i) * LDG + b0 + kk], x[kk], acc);
+            const float val = -sB[b0 + i] * acc;
+            if (i < j) x[i] = val;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (i <= j) sX[(b0 + i) * C + b0 + j] = x[i];
+    }
+    named_bar_sync(1, kCompute);
+    merge_level<16, 2, 2>(sG, sB, sX, sT, t);
+    merge_level<32, 2, 4>(sG, sB, sX, sT, t);
+    merge_level<64, 4, 4>(sG, sB, sX, sT, t);
+}
+
+template <int D>
+__global__ void __launch_bounds__(utk::kThreads, 1)
+    ut_prep_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_w, const UtParams p) {
+    using namespace utk;
+    static_assert(D == 64 || D == 128, "head dim");
+    constexpr int KCH = D / 64;
+    constexpr uint32_t TILE = 128u * D * 2u;
+    constexpr uint32_t ID_KK128 = idesc_bf16_ab(128, false, false);
+    constexpr uint32_t ID_KMN_D = idesc_bf16_ab(D, false, true);
+    constexpr uint32_t ID_KMN_128 = idesc_bf16_ab(128, false, true);
+    constexpr uint32_t ID_MNMN_D = idesc_bf16_ab(D, true, true);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    auto bar = [&](int i) { return sb + RB + 8u * (uint32_t)i; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + RB + 128);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + RB + 132);
+    float* sBeta = reinterpret_cast<float*>(sm + RB + 256);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x, bh = blockIdx.y;
+    const int row0 = chunk * C;
+    if (chunk == 0 && bh == 0 && threadIdx.x == 0) p.hdr->status = 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || i == B_OPS4) ? kCompute : 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.hdr, p.limit_ns};
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_w);
+            mbar_expect_tx(bar(B_LOAD), 3 * TILE);
+            for (int c = 0; c < KCH; ++c) {
+                tma_load_3d(sb + R0 + c * 16384, &tm_w, bar(B_LOAD), c * 64, row0, bh);
+                tma_load_3d(sb + R1 + c * 16384, &tm_q, bar(B_LOAD), c * 64, row0, bh);
+                tma_load_3d(sb + R2 + c * 16384, &tm_k, bar(B_LOAD), c * 64, row0, bh);
+            }
+            drain_wait(bar(B_LOAD), 0, p.limit_ns);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = mbar_wait(bar(B_LOAD), 0, wc, 40);
+            if (ok) {
+                tc_fence_after();
+                for (int kk = 0; kk < D / 16; ++kk) {  // G = W W^T, Q W^T, K W^T
+                    const uint64_t bw = kmajor_desc(sb + R0, kk, 16384);
+                    mma_ss(tmem + T0, kmajor_desc(sb + R0, kk, 16384), bw, ID_KK128, kk > 0);
+                    mma_ss(tmem + T128, kmajor_desc(sb + R1, kk, 16384), bw, ID_KK128, kk > 0);
+                    mma_ss(tmem + T256, kmajor_desc(sb + R2, kk, 16384), bw, ID_KK128, kk > 0);
+                }
+                mma_commit(bar(B_G));
+                ok = mbar_wait(bar(B_OPS1), 0, wc, 41);
+            }
+            if (ok) {
+                tc_fence_after();
+                // -U = -(A^T W): A^T is the MN-major view of A (hi, lo)
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T384, mnmajor_desc(sb + R1, kk), mnmajor_desc(sb + R0, kk), ID_MNMN_D, kk > 0);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T384, mnmajor_desc(sb + R2, kk), mnmajor_desc(sb + R0, kk), ID_MNMN_D, 1);
+                // Y = Y' A^T = Y'hi Ahi + Y'hi Alo + Y'lo Ahi  (A rows as K-major B)
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), kmajor_desc(sb + R1, kk, 16384), ID_KK128, kk > 0);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), kmajor_desc(sb + R2, kk, 16384), ID_KK128, 1);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3 + 32768, kk, 16384), kmajor_desc(sb + R1, kk, 16384),
+                           ID_KK128, 1);
+                mma_commit(bar(B_UY));
+                ok = mbar_wait(bar(B_OPS2), 0, wc, 42);
+            }
+            if (ok) {
+                tc_fence_after();
+                // Y W  (W as MN-major B)
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T384, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, kk > 0);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T384, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
+                mma_commit(bar(B_Q));
+                ok = mbar_wait(bar(B_OPS3), 0, wc, 43);
+            }
+            if (ok) {
+                tc_fence_after();
+                // Z A = Zhi Ahi + Zhi Alo + Zlo Ahi  (A as MN-major B)
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R1, kk), ID_KMN_128, kk > 0);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R2, kk), ID_KMN_128, 1);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R1, kk),
+                           ID_KMN_128, 1);
+                mma_commit(bar(B_ZA));
+                ok = mbar_wait(bar(B_OPS4), 0, wc, 44);
+            }
+            if (ok) {
+                tc_fence_after();
+                // (Z A) W
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T128, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, kk > 0);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T128, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
+                mma_commit(bar(B_K));
+            }
+            mma_commit(bar(B_DRAIN));
+            drain_wait(bar(B_DRAIN), 0, p.limit_ns);
+        }
+    } else {
+        // ---------------------------------------------------------------- compute warps (rows)
+        const int t = threadIdx.x - 64;         // 0..255
+        const int r = 32 * (warp & 3) + lane;    // chunk row = TMEM lane
+        const int h = (warp - 2) >> 2;           // column half handled by this warp
+        const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const int grow = row0 + r;               // sequence position of this row
+        const size_t ws_row = (size_t)bh * p.Lp + grow;
+        float* sG = reinterpret_cast<float*>(sm + R3);
+        float* sX = reinterpret_cast<float*>(sm + R1);  // dense X [128][128], over Q and K
+        float* sT = reinterpret_cast<float*>(sm + RT);
+        uint8_t* opHi = sm + R3;
+        uint8_t* opLo = sm + R3 + 32768;
+        if (h == 0) sBeta[r] = grow < p.L ? p.beta[(size_t)bh * p.L + grow] : 0.f;
+        // All compute warps wait on the same barriers, so they agree on `ok`
+        // and reach the named barriers below together.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_G), 0, wc, 50));
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {  // G row -> shared fp32 (this warp's half)
+                uint32_t v[32];
+                tmem_ld32(tl + T0 + 64 * h + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sG[r * LDG + 64 * h + 32 * c + j] = __uint_as_float(v[j]);
+            }
+            {  // Q and K are consumed: zero the dense X
+                float4* x4 = reinterpret_cast<float4*>(sX);
+                for (int i = t; i < C * C / 4; i += kCompute) x4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            named_bar_sync(1, kCompute);
+            solve_unit_upper(sG, sBeta, sX, sT, t);
+            // A = X D: this thread's half row, staged in registers (the hi/lo
+            // tiles overwrite the dense X)
+            float a[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) a[j] = sX[r * C + 64 * h + j] * sBeta[64 * h + j];
+            named_bar_sync(1, kCompute);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) put_hilo(sm + R1, sm + R2, r, 8 * h + g, a + 8 * g);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {  // Y' = tril(Q W^T) -> hi/lo operand (G is no longer read)
+                uint32_t v[32];
+                tmem_ld32(tl + T128 + 64 * h + 32 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float y8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int b = 64 * h + 32 * c + 8 * g + e;
+                        y8[e] = b <= r ? __uint_as_float(v[8 * g + e]) : 0.f;
+                    }
+                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, y8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_OPS1));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_UY), 0, wc, 51));
+        }
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {  // -U row -> global
+                uint32_t v[32];
+                const int col = (D / 2) * h + 32 * c;
+                tmem_ld32(tl + T384 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float u8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) u8[e] = -__uint_as_float(v[8 * g + e]);
+                    st_global_v4(p.un + ws_row * D + col + 8 * g, pack8(u8));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {  // Y row -> global (bf16) and hi/lo operand
+                uint32_t v[32];
+                const int col = 64 * h + 32 * c;
+                tmem_ld32(tl + T0 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float y8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y8[e] = __uint_as_float(v[8 * g + e]);
+                    st_global_v4(p.y + ws_row * C + col + 8 * g, pack8(y8));
+                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, y8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_OPS2));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 52));
+        }
+        if (ok) {
+            tc_fence_after();
+            const __nv_bfloat16* qrow = p.q + ((size_t)bh * p.L + grow) * D;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {  // qhat = Q - Y W  (fp32)
+                uint32_t v[32];
+                const int col = (D / 2) * h + 32 * c;
+                tmem_ld32(tl + T384 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    Vec16<__nv_bfloat16> qv;
+                    qv.raw = grow < p.L ? ld_global_nc_v4(qrow + col + 8 * g) : make_uint4(0, 0, 0, 0);
+                    float4* dst = reinterpret_cast<float4*>(p.qhat + ws_row * D + col + 8 * g);
+                    dst[0] = make_float4(qv.get(0) - __uint_as_float(v[8 * g + 0]), qv.get(1) - __uint_as_float(v[8 * g + 1]),
+                                         qv.get(2) - __uint_as_float(v[8 * g + 2]), qv.get(3) - __uint_as_float(v[8 * g + 3]));
+                    dst[1] = make_float4(qv.get(4) - __uint_as_float(v[8 * g + 4]), qv.get(5) - __uint_as_float(v[8 * g + 5]),
+                                         qv.get(6) - __uint_as_float(v[8 * g + 6]), qv.get(7) - __uint_as_float(v[8 * g + 7]));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {  // Z = triu_1(K W^T): -Z -> global, Z -> hi/lo operand
+                uint32_t v[32];
+                const int col = 64 * h + 32 * c;
+                tmem_ld32(tl + T256 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float z8[8], nz8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int b = col + 8 * g + e;
+                        z8[e] = b > r ? __uint_as_float(v[8 * g + e]) : 0.f;
+                        nz8[e] = -z8[e];
+                    }
+                    st_global_v4(p.zn + ws_row * C + col + 8 * g, pack8(nz8));
+                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, z8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_OPS3));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ZA), 0, wc, 53));
+        }
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {  // Z A -> hi/lo operand
+                uint32_t v[32];
+                const int col = 64 * h + 32 * c;
+                tmem_ld32(tl + T0 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float z8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) z8[e] = __uint_as_float(v[8 * g + e]);
+                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, z8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_OPS4));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_K), 0, wc, 54));
+        }
+        if (ok) {
+            tc_fence_after();
+            const __nv_bfloat16* krow = p.k + ((size_t)bh * p.L + grow) * D;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {  // khat = K - (Z A) W
+                uint32_t v[32];
+                const int col = (D / 2) * h + 32 * c;
+                tmem_ld32(tl + T128 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    Vec16<__nv_bfloat16> kv;
+                    kv.raw = grow < p.L ? ld_global_nc_v4(krow + col + 8 * g) : make_uint4(0, 0, 0, 0);
+                    float k8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) k8[e] = kv.get(e) - __uint_as_float(v[8 * g + e]);
+                    st_global_v4(p.khat + ws_row * D + col + 8 * g, pack8(k8));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, const float* beta, int BH, int L,
+                                  unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
+    CUtensorMap mq, mk, mw;
+    if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mw, w, D, L, BH))
+        return cudaErrorInvalidValue;
+    UtParams p;
+    p.L = L;
+    p.Lp = lay.Lp;
+    p.beta = beta;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.k = static_cast<const __nv_bfloat16*>(k);
+    p.qhat = reinterpret_cast<float*>(ws + lay.qhat);
+    p.khat = reinterpret_cast<__nv_bfloat16*>(ws + lay.khat);
+    p.un = reinterpret_cast<__nv_bfloat16*>(ws + lay.un);
+    p.y = reinterpret_cast<__nv_bfloat16*>(ws + lay.y);
+    p.zn = reinterpret_cast<__nv_bfloat16*>(ws + lay.zn);
+    p.hdr = reinterpret_cast<WsHeader*>(ws);
+    p.limit_ns = 2000000000ull;
+    auto kern = ut_prep_tc<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)utk::kSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(cdiv(L, utk::C), BH), utk::kThreads, utk::kSmem, st>>>(mq, mk, mw, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w, const float* beta, int BH, int L,
+                              unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
+    if (d == 64) return launch_ut_tc_d<64>(q, k, w, beta, BH, L, ws, lay, st);
+    if (d == 128) return launch_ut_tc_d<128>(q, k, w, beta, BH, L, ws, lay, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pathattn
