@@ -30,8 +30,10 @@
 //   SM_Q  32 KB  Q (diagonal) then bf16 q~, K-major, 64-column chunks of 16 KB
 //   SM_KW 64 KB  per 64-column chunk c (32 KB): rows 0-127 khat_m (or K),
 //                rows 128-255 W_m (or -Z): one N=256 B operand for MMA1
-//   SM_V  32 KB  V_m, MN-major B operand (64-column boxes of 16 KB)
+//   SM_V  64 KB  V_m, MN-major B operand (64-column boxes of 16 KB), two
+//                slots by block parity
 //   SM_U  32 KB  -U_m (MN-major) or, on the diagonal, Y (K-major)
+//   SM_P  32 KB  P (bf16, K-major A operand of P V)
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
 // PATH_ERR_TIMEOUT in the workspace status word, every role stops, pending
 // copies and MMAs are drained (bounded) and TMEM is freed before exit.
@@ -48,16 +50,33 @@ using namespace sm100;
 
 constexpr int kTcC = 128;
 constexpr int kTcThreads = 320;
-constexpr uint32_t SM_Q = 0, SM_KW = 32768, SM_V = 98304, SM_U = 131072, SM_BAR = 163840;
+constexpr uint32_t SM_Q = 0, SM_KW = 32768, SM_V = 98304, SM_U = 163840, SM_P = 196608, SM_BAR = 229376;
 constexpr uint32_t SM_TOTAL = SM_BAR + 256;
 constexpr size_t kTcSmem = SM_TOTAL + 1024;  // + alignment slack
 constexpr uint32_t TM_S = 0, TM_SW = 128, TM_O = 256, TM_Q = 384;
 
-enum Bar { B_QFULL = 0, B_KWFULL, B_VUFULL, B_KWEMPTY, B_VUEMPTY, B_SFULL, B_SWREADY, B_PREADY, B_QUPD, B_QTREADY,
-           B_ODONE, B_DRAIN, B_COUNT };
+// Every barrier below is waited on in a way that it can never run two phases
+// ahead of its waiter (a parity wait cannot tell those apart).
+// Each operand slot (khat, W, -U, V) has its own full/empty pair, released
+// by the MMA that consumes it, so every refill starts as early as possible.
+// V is double-buffered by block parity (slot it & 1).
+enum Bar { B_QFULL = 0, B_KFULL, B_WFULL, B_UFULL, B_VFULL0, B_KEMPTY, B_WEMPTY, B_UEMPTY, B_VEMPTY0, B_SFULL,
+           B_SWREADY, B_PREADY, B_QUPD, B_QTREADY, B_ODONE, B_DRAIN, B_SREAD, B_VFULL1, B_VEMPTY1, B_PFREE,
+           B_SWFULL, B_COUNT };
+
+constexpr int kHeadGroup = 8;
+
+// Phase timestamps of CTA 0 (SM cycle counter), compiled in only for
+// instrumented builds (-DPATH_TRACE): slot s of block iteration it.
+#ifdef PATH_TRACE
+#define TC_TRACE(slot, it) \
+    do { if (p.trace && blockIdx.x == 0 && (it) < 64) p.trace[(it) * 32 + (slot)] = clock64(); } while (0)
+#else
+#define TC_TRACE(slot, it) do { } while (0)
+#endif
 
 struct TcParams {
-    int L, Lp, ntiles;
+    int L, Lp, ntiles, BH;
     float sl2;                 // scale * log2(e)
     const float* qhat;         // [BH, Lp, d] fp32
     const float* cum;          // [BH, Lp] fp32 (FoX)
@@ -66,6 +85,9 @@ struct TcParams {
     WsHeader* hdr;
     unsigned long long limit_ns;
     int fault;                 // test hook: skip one producer signal
+#ifdef PATH_TRACE
+    unsigned long long* trace;
+#endif
 };
 
 template <int D, bool FOX>
@@ -78,7 +100,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     static_assert(D == 64 || D == 128, "head dim");
     constexpr int KCH = D / 64;          // 64-column chunks of the head dim
     constexpr uint32_t ROWB = 128u * D * 2u;  // bytes of one [128 x D] bf16 tile
-    constexpr uint32_t IDESC_S256 = idesc_bf16(256, false);
+        constexpr uint32_t IDESC_S256 = idesc_bf16(256, false);
     constexpr uint32_t IDESC_S128 = idesc_bf16(128, false);
     constexpr uint32_t IDESC_PV = idesc_bf16(D, true);
 
@@ -91,12 +113,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_BAR + 132);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int n = p.ntiles - 1 - (int)blockIdx.y;  // longest tiles first
+    // Launch order: heads in groups of kHeadGroup; inside a group, tiles
+    // longest first with the heads interleaved.  The ~150 resident CTAs then
+    // cover a few heads each, so their key/value blocks are re-read from L2,
+    // and the short tiles of the last group fill the tail.
+    int bh, n;
+    {
+        const int idx = (int)blockIdx.x;
+        const int per_group = kHeadGroup * p.ntiles;
+        const int g = idx / per_group, rem = idx - g * per_group;
+        const int gsize = min(kHeadGroup, p.BH - g * kHeadGroup);
+        n = p.ntiles - 1 - rem / gsize;
+        bh = g * kHeadGroup + rem % gsize;
+    }
     const int row0 = n * kTcC;
 
     if (threadIdx.x == 0) {
-        const uint32_t counts[B_COUNT] = {1, 1, 1, 1, 1, 1, 128, 128, 1, 128, 1, 1};
+        uint32_t counts[B_COUNT];
+        for (int i = 0; i < B_COUNT; ++i) counts[i] = 1;
+        counts[B_SWREADY] = counts[B_PREADY] = counts[B_QTREADY] = counts[B_SREAD] = 128;
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         *abort_flag = 0;
         fence_mbar_init();
@@ -116,47 +151,92 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_w);
             prefetch_tmap(&tm_khat); prefetch_tmap(&tm_un); prefetch_tmap(&tm_y); prefetch_tmap(&tm_zn);
-            int kw_issued = 0, vu_issued = 0;
             bool ok = true;
+            // diagonal block: Q, K (khat slot), -Z (W slot), Y (-U slot), V
             mbar_expect_tx(bar(B_QFULL), ROWB);
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_Q + c * 16384, &tm_q, bar(B_QFULL), c * 64, row0, bh);
-            mbar_expect_tx(bar(B_KWFULL), ROWB + 32768);
-            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_KW + c * 32768, &tm_k, bar(B_KWFULL), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_KFULL), ROWB);
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_KW + c * 32768, &tm_k, bar(B_KFULL), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_WFULL), 32768);
             for (int c = 0; c < 2; ++c)
-                tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_zn, bar(B_KWFULL), c * 64, row0, bh);
-            ++kw_issued;
-            mbar_expect_tx(bar(B_VUFULL), ROWB + 32768);
-            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V + c * 16384, &tm_v, bar(B_VUFULL), c * 64, row0, bh);
-            for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_U + c * 16384, &tm_y, bar(B_VUFULL), c * 64, row0, bh);
-            ++vu_issued;
-            for (int it = 1; it <= n && ok; ++it) {
-                const int r = (n - it) * kTcC;
-                if (!(ok = mbar_wait(bar(B_KWEMPTY), (it - 1) & 1, wc, 1))) break;
-                mbar_expect_tx(bar(B_KWFULL), 2 * ROWB);
-                for (int c = 0; c < KCH; ++c) {
-                    tma_load_3d(sb + SM_KW + c * 32768, &tm_khat, bar(B_KWFULL), c * 64, r, bh);
-                    tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_w, bar(B_KWFULL), c * 64, r, bh);
+                tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_zn, bar(B_WFULL), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_UFULL), 32768);
+            for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_U + c * 16384, &tm_y, bar(B_UFULL), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_VFULL0), ROWB);
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V + c * 16384, &tm_v, bar(B_VFULL0), c * 64, row0, bh);
+            // scan blocks: refill each slot as soon as its consumer has finished.
+            // Slot s for block iteration it needs the (it)-th completion of its
+            // empty barrier (V: slot it & 1, its (it >> 1)-th completion).  W
+            // and -U are not used by the last block (m = 0).
+            enum { SW = 0, SK, SU, SV };
+            int nxt[4] = {1, 1, 1, 1}, issued[5] = {1, 1, 1, 1, 0};  // issued[3]/[4]: V slots 0/1
+            const int emp[3] = {B_WEMPTY, B_KEMPTY, B_UEMPTY};
+            const uint64_t t0 = globaltimer();
+            for (uint32_t spin = 0; ok && (nxt[0] <= n || nxt[1] <= n || nxt[2] <= n || nxt[3] <= n); ++spin) {
+                for (int sl = 0; sl < 4; ++sl) {
+                    const int it = nxt[sl];
+                    if (it > n) continue;
+                    if ((sl == SW || sl == SU) && it == n) { nxt[sl] = n + 1; continue; }
+                    if (sl == SV) {
+                        if (it >= 2 && !mbar_test_wait(bar((it & 1) ? B_VEMPTY1 : B_VEMPTY0), (uint32_t)(((it >> 1) - 1) & 1)))
+                            continue;
+                    } else if (!mbar_test_wait(bar(emp[sl]), (it - 1) & 1)) {
+                        continue;
+                    }
+                    const int r = (n - it) * kTcC;
+                    nxt[sl] = it + 1;
+                    if (sl == SV && p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
+                    const int fb = sl == SW ? B_WFULL : sl == SK ? B_KFULL : sl == SU ? B_UFULL : ((it & 1) ? B_VFULL1 : B_VFULL0);
+                    mbar_expect_tx(bar(fb), ROWB);
+                    for (int c = 0; c < KCH; ++c) {
+                        if (sl == SK) tma_load_3d(sb + SM_KW + c * 32768, &tm_khat, bar(fb), c * 64, r, bh);
+                        if (sl == SW) tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_w, bar(fb), c * 64, r, bh);
+                        if (sl == SU) tma_load_3d(sb + SM_U + c * 16384, &tm_un, bar(fb), c * 64, r, bh);
+                        if (sl == SV) tma_load_3d(sb + SM_V + (it & 1) * 32768 + c * 16384, &tm_v, bar(fb), c * 64, r, bh);
+                    }
+                    ++issued[sl == SV ? 3 + (it & 1) : sl];
+                    TC_TRACE(12 + sl, it);
                 }
-                ++kw_issued;
-                if (!(ok = mbar_wait(bar(B_VUEMPTY), (it - 1) & 1, wc, 2))) break;
-                if (p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
-                mbar_expect_tx(bar(B_VUFULL), 2 * ROWB);
-                for (int c = 0; c < KCH; ++c) {
-                    tma_load_3d(sb + SM_V + c * 16384, &tm_v, bar(B_VUFULL), c * 64, r, bh);
-                    tma_load_3d(sb + SM_U + c * 16384, &tm_un, bar(B_VUFULL), c * 64, r, bh);
+                if ((spin & 255u) == 255u) {
+                    if (*abort_flag) { ok = false; break; }
+                    if (globaltimer() - t0 > p.limit_ns * (uint64_t)(n + 1)) {
+                        report_status(p.hdr, PATH_ERR_TIMEOUT, 1);
+                        *abort_flag = 1;
+                        ok = false;
+                    }
                 }
-                ++vu_issued;
             }
             // copies still in flight must land before the CTA exits
             drain_wait(bar(B_QFULL), 0, p.limit_ns);
-            drain_wait(bar(B_KWFULL), (kw_issued - 1) & 1, p.limit_ns);
-            drain_wait(bar(B_VUFULL), (vu_issued - 1) & 1, p.limit_ns);
+            const int ful[5] = {B_WFULL, B_KFULL, B_UFULL, B_VFULL0, B_VFULL1};
+            for (int sl = 0; sl < 5; ++sl)
+                if (issued[sl] > 0) drain_wait(bar(ful[sl]), (uint32_t)((issued[sl] - 1) & 1), p.limit_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
+        // Per block: MMA1 (scores) and MMA3 (query transport) form the
+        // critical chain; the P V product of the previous block (MMA2, P in
+        // shared memory) is issued whenever its P is ready, before or after
+        // the next MMA1, whichever inputs arrive first.
         if (lane == 0) {
-            bool ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KWFULL), 0, wc, 11) &&
-                      mbar_wait(bar(B_VUFULL), 0, wc, 12);
+            auto issue_pv = [&](int blk) {  // O (+)= P V for block iteration blk
+                tc_fence_after();
+                const uint32_t vbuf = sb + SM_V + (uint32_t)(blk & 1) * 32768u;
+                for (int kk = 0; kk < kTcC / 16; ++kk)
+                    mma_ss(tmem + TM_O, kmajor_desc(sb + SM_P, kk, 16384), mnmajor_desc(vbuf, kk), IDESC_PV,
+                           (blk > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(bar(B_ODONE));
+                mma_commit(bar((blk & 1) ? B_VEMPTY1 : B_VEMPTY0));
+                mma_commit(bar(B_PFREE));
+            };
+            // P V of block blk needs its P (p_ready, (blk+1)-th completion) and
+            // its V slot (blk & 1, (blk >> 1)+1-th completion).
+            auto wait_pv = [&](int blk) {
+                return mbar_wait(bar(B_PREADY), (uint32_t)(blk & 1), wc, 18) &&
+                       mbar_wait(bar((blk & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((blk >> 1) & 1), wc, 19);
+            };
+            bool ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL), 0, wc, 11) &&
+                      mbar_wait(bar(B_WFULL), 0, wc, 12) && mbar_wait(bar(B_UFULL), 0, wc, 12);
             if (ok) {
                 tc_fence_after();
                 // diagonal: S = Q K^T + Y (-Z)^T
@@ -167,41 +247,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_ss(tmem + TM_S, kmajor_desc(sb + SM_U, kk, 16384),
                            kmajor_desc(sb + SM_KW + 16384, kk, 32768), IDESC_S128, 1);
                 mma_commit(bar(B_SFULL));
-                mma_commit(bar(B_KWEMPTY));
-                ok = mbar_wait(bar(B_PREADY), 0, wc, 13);
+                mma_commit(bar(B_KEMPTY));
+                mma_commit(bar(B_WEMPTY));
+                mma_commit(bar(B_UEMPTY));
             }
-            if (ok) {
-                tc_fence_after();
-                for (int kk = 0; kk < kTcC / 16; ++kk)
-                    mma_ts(tmem + TM_O, tmem + TM_S + kk * 8, mnmajor_desc(sb + SM_V, kk), IDESC_PV, kk > 0);
-                mma_commit(bar(B_ODONE));
-                mma_commit(bar(B_VUEMPTY));
-            }
+            // Issue is blocking (an MMA group's issue returns about when it has
+            // executed), so the issue order is the tensor pipe's schedule:
+            //   MMA1(it) [S_k | S_w, N = 256] -> MMA3(it) -> P V(it-1)
+            // (P V covers the conversion of q~ for the next MMA1).
             for (int it = 1; it <= n && ok; ++it) {
                 const int m = n - it;
                 if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
-                if (!(ok = mbar_wait(bar(B_KWFULL), it & 1, wc, 15))) break;
+                if (!(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
+                if (m > 0 && !(ok = mbar_wait(bar(B_WFULL), it & 1, wc, 15))) break;
+                if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
                 tc_fence_after();
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
-                           IDESC_S256, kk > 0);
+                           m > 0 ? IDESC_S256 : IDESC_S128, kk > 0);
                 mma_commit(bar(B_SFULL));
-                mma_commit(bar(B_KWEMPTY));
-                if (!(ok = mbar_wait(bar(B_VUFULL), it & 1, wc, 16))) break;
+                mma_commit(bar(B_KEMPTY));
                 if (m > 0) {
+                    mma_commit(bar(B_SWFULL));
+                    mma_commit(bar(B_WEMPTY));
+                }
+                TC_TRACE(1, it);
+                if (m > 0) {
+                    TC_TRACE(21, it);
+                    if (!(ok = mbar_wait(bar(B_UFULL), it & 1, wc, 16))) break;
+                    TC_TRACE(22, it);
                     if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
+                    TC_TRACE(23, it);
                     tc_fence_after();
                     for (int kk = 0; kk < kTcC / 16; ++kk)
                         mma_ts(tmem + TM_Q, tmem + TM_SW + kk * 8, mnmajor_desc(sb + SM_U, kk), IDESC_PV, 1);
                     mma_commit(bar(B_QUPD));
+                    mma_commit(bar(B_UEMPTY));
+                    TC_TRACE(3, it);
                 }
-                if (!(ok = mbar_wait(bar(B_PREADY), it & 1, wc, 18))) break;
-                tc_fence_after();
-                for (int kk = 0; kk < kTcC / 16; ++kk)
-                    mma_ts(tmem + TM_O, tmem + TM_S + kk * 8, mnmajor_desc(sb + SM_V, kk), IDESC_PV, 1);
-                mma_commit(bar(B_ODONE));
-                mma_commit(bar(B_VUEMPTY));
+                if (!(ok = wait_pv(it - 1))) break;
+                TC_TRACE(20, it);
+                issue_pv(it - 1);
+                TC_TRACE(2, it);
             }
+            if (ok && wait_pv(n)) issue_pv(n);  // the last block's P V
             // every issued MMA completes before TMEM is released
             mma_commit(bar(B_DRAIN));
             drain_wait(bar(B_DRAIN), 0, p.limit_ns);
@@ -219,6 +308,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int m = n - it;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 20));
             if (!ok) break;
+            if (r == 0) TC_TRACE(4, it);
             tc_fence_after();
             float s[128];
 #pragma unroll
@@ -228,7 +318,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]) * p.sl2;
-                if (FOX) {
+            }
+            // S_k is in registers: the next block's MMA1 may overwrite it
+            tc_fence_before();
+            mbar_arrive(bar(B_SREAD));
+            if (r == 0) TC_TRACE(5, it);
+            if (FOX) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
                     const float4* cj = reinterpret_cast<const float4*>(cumh + m * kTcC + 32 * c);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
@@ -253,24 +350,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float m_use = rescale ? m_new : m_run;
             const float alpha = rescale ? exp2f(m_run - m_use) : 1.0f;
             float sum = 0.f;
+            uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = exp2f(s[64 * c + 2 * j] - m_use);
-                    const float p1 = exp2f(s[64 * c + 2 * j + 1] - m_use);
-                    sum += p0 + p1;
-                    pk[j] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tl + TM_S + 32 * c, pk);
+            for (int j = 0; j < 64; ++j) {
+                const float p0 = exp2f(s[2 * j] - m_use);
+                const float p1 = exp2f(s[2 * j + 1] - m_use);
+                sum += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
             }
             l_run = l_run * alpha + sum;
+            if (r == 0) TC_TRACE(6, it);
             // The O rescale uses warp-collective TMEM loads/stores, so the whole
             // warp takes it when any of its rows needs it (alpha = 1 elsewhere).
+            bool waited_prev = false;
             if (__any_sync(0xffffffffu, rescale && it > 0)) {
                 // O is stable once the previous block's P V has completed
                 const bool ok2 = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (it - 1) & 1, wc, 21));
+                waited_prev = true;
                 if (!ok2) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -284,9 +380,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             m_run = m_use;
+            // the P buffer is free once the P V of block it-1 has completed
+            // (the it-th completion of the P-free barrier)
+            if (it >= 1 && !waited_prev) {
+                const bool ok3 = __all_sync(0xffffffffu, mbar_wait(bar(B_PFREE), (uint32_t)((it - 1) & 1), wc, 23));
+                if (!ok3) { ok = false; break; }
+            }
+            {
+                uint8_t* prow = sm + SM_P + r * 128;
+#pragma unroll
+                for (int G = 0; G < 16; ++G)
+                    *reinterpret_cast<uint4*>(prow + (G >> 3) * 16384 + (((G & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * G], pk[4 * G + 1], pk[4 * G + 2], pk[4 * G + 3]);
+            }
             tmem_wait_st();
+            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_PREADY));
+            if (r == 0) TC_TRACE(7, it);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), n & 1, wc, 22));
         if (ok) {
@@ -356,43 +467,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(bar(B_QTREADY));
         }
         for (int it = 1; it < n && ok; ++it) {  // block m = n - it > 0 needs the transport
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 31));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SWFULL), (it - 1) & 1, wc, 31));
             if (!ok) break;
+            if (r == 0) TC_TRACE(8, it);
             tc_fence_after();
             // S_w (fp32, columns [128,256)) -> bf16 pairs in columns [128,192)
+            {
+                uint32_t v[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t v[32], pk[16];
-                tmem_ld32(tl + TM_SW + 32 * c, v);
+                for (int c = 0; c < 4; ++c) tmem_ld32(tl + TM_SW + 32 * c, v[c]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-                tmem_st16(tl + TM_SW + 16 * c, pk);
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]), __uint_as_float(v[c][2 * j + 1]));
+                    tmem_st16(tl + TM_SW + 16 * c, pk);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(B_SWREADY));
+            if (r == 0) TC_TRACE(9, it);
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QUPD), (it - 1) & 1, wc, 32));
             if (!ok) break;
+            if (r == 0) TC_TRACE(10, it);
             tc_fence_after();
+            {
+                uint32_t v[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tl + TM_Q + 32 * c, v);
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + TM_Q + 32 * c, v[c]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    uint4 q;
-                    q.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
-                    q.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
-                    q.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
-                    q.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
-                    put_granule(4 * c + g, q);
-                }
+                for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        uint4 q;
+                        q.x = pack_bf16x2(__uint_as_float(v[c][8 * g + 0]), __uint_as_float(v[c][8 * g + 1]));
+                        q.y = pack_bf16x2(__uint_as_float(v[c][8 * g + 2]), __uint_as_float(v[c][8 * g + 3]));
+                        q.z = pack_bf16x2(__uint_as_float(v[c][8 * g + 4]), __uint_as_float(v[c][8 * g + 5]));
+                        q.w = pack_bf16x2(__uint_as_float(v[c][8 * g + 6]), __uint_as_float(v[c][8 * g + 7]));
+                        put_granule(4 * c + g, q);
+                    }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_QTREADY));
+            if (r == 0) TC_TRACE(11, it);
         }
     }
 
@@ -408,6 +530,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 int tc_chunk(int d) { (void)d; return kTcC; }
 bool tc_supported(int d) { return d == 64 || d == 128; }
 
+#ifdef PATH_TRACE
+static unsigned long long* trace_buffer() {
+    static unsigned long long* buf = nullptr;
+    if (!buf && cudaMalloc(&buf, 64 * 32 * sizeof(unsigned long long)) == cudaSuccess)
+        cudaMemset(buf, 0, 64 * 32 * sizeof(unsigned long long));
+    return buf;
+}
+}  // namespace pathattn
+extern "C" void path_trace_dump(unsigned long long* host) {
+    cudaDeviceSynchronize();
+    cudaMemcpy(host, pathattn::trace_buffer(), 64 * 32 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+}
+namespace pathattn {
+#endif
+
 template <int D>
 static cudaError_t launch_tc(const void* q, const void* k, const void* v, const void* w, const float* log_f,
                             void* o, float* lse, int BH, int L, float scale, unsigned char* ws, const FwdLayout& lay,
@@ -422,6 +559,7 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     p.L = L;
     p.Lp = lay.Lp;
     p.ntiles = cdiv(L, kTcC);
+    p.BH = BH;
     p.sl2 = scale * 1.4426950408889634f;
     p.qhat = reinterpret_cast<const float*>(ws + lay.qhat);
     p.cum = reinterpret_cast<const float*>(ws + lay.cum);
@@ -430,11 +568,14 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.limit_ns = fault ? 20000000ull : 2000000000ull;  // 20 ms under the test hook, else 2 s
     p.fault = fault;
+#ifdef PATH_TRACE
+    p.trace = trace_buffer();
+#endif
     auto kern = log_f ? path_fwd_tc<D, true> : path_fwd_tc<D, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     mark_start(st);
-    kern<<<dim3(BH, p.ntiles), kTcThreads, kTcSmem, st>>>(mq, mk, mv, mw, mkh, mun, my, mzn, p);
+    kern<<<dim3(BH * p.ntiles), kTcThreads, kTcSmem, st>>>(mq, mk, mv, mw, mkh, mun, my, mzn, p);
     mark_end(st);
     return cudaGetLastError();
 }

@@ -46,6 +46,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of a phase (no suspension, so no wake-up latency).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Shared control block for bounded waits: every wait gives up after
 // `limit_ns` of global time, or as soon as another thread has set `abort`.
 struct WaitCtl {
@@ -56,12 +67,13 @@ struct WaitCtl {
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false (after recording PATH_ERR_TIMEOUT and raising the abort flag) if the
-// limit expires, or false if another thread already aborted.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
-    if (mbar_try_wait(bar, parity)) return true;
+// limit expires, or false if another thread already aborted.  It polls with
+// test_wait: a suspended try_wait costs a few hundred cycles of wake-up
+// latency after the phase completes, which every handoff would pay.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_test_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (*c.abort) return false;
             if (globaltimer() - t0 > c.limit_ns) {
@@ -72,6 +84,15 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, con
             }
         }
     }
+}
+// The common case (phase already complete, or completing within a few dozen
+// polls) stays inline: an out-of-line call costs a few hundred cycles of
+// register save/restore, which every handoff would pay.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, c, site);
 }
 
 // ----------------------------------------------------------------------------- TMA
