@@ -333,14 +333,28 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             }
             named_bar_sync(1, kCompute);
             solve_unit_upper(sG, sBeta, sX, sT, t);
-            // A = X D: this thread's half row, staged in registers (the hi/lo
-            // tiles overwrite the dense X)
-            float a[64];
+            // A = X D as hi/lo bf16 tiles.  The tiles overwrite the dense X, so
+            // each thread first reads its 8 granules (8 consecutive columns of
+            // one row; consecutive threads walk along a row, free of bank
+            // conflicts) into registers, then writes them after a barrier.
+            {
+                float a[8][8];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) a[j] = sX[r * C + 64 * h + j] * sBeta[64 * h + j];
-            named_bar_sync(1, kCompute);
+                for (int i = 0; i < 8; ++i) {
+                    const int q = t + kCompute * i, row = q >> 4, G = q & 15;
+                    const float4 x0 = *reinterpret_cast<const float4*>(sX + row * C + 8 * G);
+                    const float4 x1 = *reinterpret_cast<const float4*>(sX + row * C + 8 * G + 4);
+                    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-            for (int g = 0; g < 8; ++g) put_hilo(sm + R1, sm + R2, r, 8 * h + g, a + 8 * g);
+                    for (int e = 0; e < 8; ++e) a[i][e] = xv[e] * sBeta[8 * G + e];
+                }
+                named_bar_sync(1, kCompute);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int q = t + kCompute * i;
+                    put_hilo(sm + R1, sm + R2, q >> 4, q & 15, a[i]);
+                }
+            }
 #pragma unroll
             for (int c = 0; c < 2; ++c) {  // Y' = tril(Q W^T) -> hi/lo operand (G is no longer read)
                 uint32_t v[32];
