@@ -33,7 +33,8 @@ _DT = {torch.float32: PATH_F32, torch.bfloat16: PATH_BF16}
 
 EXPORTED = ("path_version", "path_status_string", "path_attn_workspace_bytes", "path_attn_fwd",
             "path_attn_fwd_fox", "path_decode_workspace_bytes", "path_kcache_update", "path_decode_step",
-            "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events", "path_decode_step_noalloc")
+            "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events", "path_decode_step_noalloc",
+            "path_prefill_workspace_bytes", "path_prefill_kcache")
 
 
 class PathLibraryError(RuntimeError):
@@ -83,6 +84,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.path_decode_step_noalloc.argtypes = [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _i, _i, _vp, _fp, _i, _i, _i,
                                              ctypes.c_float, _i, _vp]
     lib.path_decode_step_noalloc.restype = _i
+    lib.path_prefill_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+    lib.path_prefill_workspace_bytes.restype = _sz
+    lib.path_prefill_kcache.argtypes = [_vp, _vp, _fp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]
+    lib.path_prefill_kcache.restype = _i
     lib.path_get_status.argtypes = [_vp, _vp]
     lib.path_get_status.restype = _i
     lib.path_debug_set_fault.argtypes = [_i]
@@ -179,6 +184,34 @@ def path_attn_fwd_fox(q, k, v, w, beta, log_f, scale=None, lse=False, out=None, 
     if log_f is None:
         raise ValueError("log_f is required")
     return _fwd(q, k, v, w, beta, log_f, scale, lse, out, workspace)
+
+
+def path_prefill_workspace_bytes(B: int, H: int, L: int, d: int, dtype: torch.dtype) -> int:
+    return int(load().path_prefill_workspace_bytes(B, H, L, d, _DT[dtype]))
+
+
+def path_prefill_kcache(k, w, beta, kcache=None, n_max=None, workspace=None):
+    """Transported key cache of a prompt: kcache[:, :, j] = H_{L-1} ... H_{j+1} k[:, :, j] for j < L.
+
+    k, w: [B, H, L, d] CUDA (fp32 or bf16); beta [B, H, L] fp32.  Allocates kcache [B, H, n_max, d]
+    (n_max defaults to L) unless one is given; returns it.  Decoding continues with n_cached = L.
+    """
+    lib = load()
+    B, H, L, d = k.shape
+    dt = k.dtype
+    _dev(k, "k", dt, (B, H, L, d))
+    _dev(w, "w", dt, (B, H, L, d))
+    _dev(beta, "beta", torch.float32, (B, H, L))
+    if kcache is None:
+        kcache = torch.zeros((B, H, n_max or L, d), dtype=dt, device=k.device)
+    _dev(kcache, "kcache", dt)
+    need = lib.path_prefill_workspace_bytes(B, H, L, d, _DT[dt])
+    if need == 0:
+        raise PathError(PATH_ERR_UNSUPPORTED, "path_prefill_kcache")
+    ws = alloc_workspace(need, k.device) if workspace is None else workspace
+    _check(lib.path_prefill_kcache(_ptr(k), _ptr(w), _ptr(beta), _ptr(kcache), B, H, L, kcache.shape[2], d,
+                                   _DT[dt], _ptr(ws), ws.numel(), _stream()), "path_prefill_kcache")
+    return kcache
 
 
 def path_kcache_update(kcache, n_cached: int, w_t, beta_t):

@@ -16,6 +16,8 @@ bool tc_supported(int d);
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
                         const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
                         unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st);
+cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w, const float* beta, void* kcache,
+                           int BH, int L, int n_max, unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
 cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                         const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t, float* lse_t,
                         int BH, float scale, unsigned char* ws, const DecLayout& lay, cudaStream_t st);
@@ -107,6 +109,29 @@ int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w
                       float scale, void* workspace, size_t workspace_bytes, path_stream_t stream) {
     return fwd_common(q, k, v, w, beta, log_f, true, o, lse, B, H, L, d, dtype, causal, scale, workspace,
                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t path_prefill_workspace_bytes(int B, int H, int L, int d, int dtype) {
+    if (B < 1 || H < 1 || L < 1 || !fwd_d_ok(d, dtype)) return 0;
+    return fwd_layout(B, H, L, d, fwd_chunk(d, dtype), elt_size(dtype), true).total;
+}
+
+int path_prefill_kcache(const void* k, const void* w, const float* beta, void* kcache, int B, int H, int L,
+                        int n_max, int d, int dtype, void* workspace, size_t workspace_bytes, path_stream_t stream) {
+    if (B < 1 || H < 1 || L < 1 || n_max < L) return PATH_ERR_INVALID;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
+    if (!fwd_d_ok(d, dtype)) return PATH_ERR_UNSUPPORTED;
+    if (!k || !w || !beta || !kcache) return PATH_ERR_INVALID;
+    if (!aligned16(k) || !aligned16(w) || !aligned16(beta) || !aligned16(kcache)) return PATH_ERR_INVALID;
+    const FwdLayout lay = fwd_layout(B, H, L, d, fwd_chunk(d, dtype), elt_size(dtype), true);
+    if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PATH_ERR_WORKSPACE;
+    cudaError_t e = prefill_kcache(dtype, fwd_chunk(d, dtype), d, k, w, beta, kcache, B * H, L, n_max,
+                                   static_cast<unsigned char*>(workspace), lay, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "pathattn: prefill launch failed: %s\n", cudaGetErrorString(e));
+        return PATH_ERR_CUDA;
+    }
+    return PATH_OK;
 }
 
 size_t path_decode_workspace_bytes(int B, int H, int n_max, int d) {

@@ -101,11 +101,13 @@ __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
 //   y    : T     [BH, Lp, C]  Y = tril(Q W^T) A^T per chunk (diagonal blocks)
 //   zn   : T     [BH, Lp, C]  -Z = -triu_1(K W^T) per chunk (diagonal blocks)
 //   cum  : float [BH, Lp]     inclusive cumulative sum of log f (PaTH-FoX)
+//   vfac : T     [BH, Lp, d]  V = A W per chunk (key-side transport; prefill
+//                             cache only, absent from forward workspaces)
 struct FwdLayout {
-    size_t qhat, khat, un, y, zn, cum, total;
+    size_t qhat, khat, un, y, zn, cum, vfac, total;
     int Lp;
 };
-inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt) {
+inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt, bool with_vfac = false) {
     FwdLayout s;
     s.Lp = cdiv(L, C) * C;
     const size_t rows = (size_t)B * H * s.Lp;
@@ -117,6 +119,7 @@ inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt) {
     s.y = take(rows * C * elt);
     s.zn = take(rows * C * elt);
     s.cum = take(rows * sizeof(float));
+    s.vfac = with_vfac ? take(rows * d * elt) : 0;
     s.total = off;
     return s;
 }

@@ -35,7 +35,8 @@ __global__ void __launch_bounds__(NT) ut_prep_simt(const T* __restrict__ q, cons
                                                    const T* __restrict__ w, const float* __restrict__ beta,
                                                    int L, int Lp, float* __restrict__ qhat,
                                                    T* __restrict__ khat, T* __restrict__ un,
-                                                   T* __restrict__ y, T* __restrict__ zn, WsHeader* hdr) {
+                                                   T* __restrict__ y, T* __restrict__ zn, T* __restrict__ vfac,
+                                                   WsHeader* hdr) {
     using SM = UtSmem<T, C, D, NT>;
     constexpr int LDT = SM::LDT, LDF = SM::LDF;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -83,6 +84,11 @@ __global__ void __launch_bounds__(NT) ut_prep_simt(const T* __restrict__ q, cons
     block_gemm<C, D, C, NT>([&](int m, int kk) { return sA[kk * LDF + m]; },
                             [&](int kk, int n) { return to_f<T>(sW[kk * LDT + n]); },
                             [&](int m, int n, float acc) { un[(wrow + m) * D + n] = from_f<T>(-acc); });
+    // V = A W (key-side transport factor, prefill cache only)
+    if (vfac)
+        block_gemm<C, D, C, NT>([&](int m, int kk) { return sA[m * LDF + kk]; },
+                                [&](int kk, int n) { return to_f<T>(sW[kk * LDT + n]); },
+                                [&](int m, int n, float acc) { vfac[(wrow + m) * D + n] = from_f<T>(acc); });
 
     // Queries: Y' = tril(Q W^T), Y = Y' A^T, qhat = Q - Y W.
     load_rows<C, D, LDT, NT>(sX, qh, r0, L);
@@ -175,7 +181,8 @@ static cudaError_t launch_ut_t(const void* q, const void* k, const void* w, cons
     ut<<<dim3(cdiv(L, C), BH), NT, smem, st>>>(
         static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(w), beta, L, lay.Lp,
         reinterpret_cast<float*>(ws + lay.qhat), reinterpret_cast<T*>(ws + lay.khat), reinterpret_cast<T*>(ws + lay.un),
-        reinterpret_cast<T*>(ws + lay.y), reinterpret_cast<T*>(ws + lay.zn), reinterpret_cast<WsHeader*>(ws));
+        reinterpret_cast<T*>(ws + lay.y), reinterpret_cast<T*>(ws + lay.zn),
+        lay.vfac ? reinterpret_cast<T*>(ws + lay.vfac) : nullptr, reinterpret_cast<WsHeader*>(ws));
     if (log_f) fox_cumsum<<<BH, 1024, 0, st>>>(log_f, L, lay.Lp, reinterpret_cast<float*>(ws + lay.cum));
     return cudaGetLastError();
 }

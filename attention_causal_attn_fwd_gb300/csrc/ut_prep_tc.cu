@@ -68,6 +68,7 @@ struct UtParams {
     __nv_bfloat16* un;           // [BH, Lp, d]
     __nv_bfloat16* y;            // [BH, Lp, C]
     __nv_bfloat16* zn;           // [BH, Lp, C]
+    __nv_bfloat16* vfac;         // [BH, Lp, d] V = A W (prefill cache only) or null
     WsHeader* hdr;
     unsigned long long limit_ns;
 };
@@ -262,6 +263,12 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 for (int kk = 0; kk < C / 16; ++kk)
                     mma_ss(tmem + T0, kmajor_desc(sb + R3 + 32768, kk, 16384), kmajor_desc(sb + R1, kk, 16384),
                            ID_KK128, 1);
+                if (p.vfac) {  // V = A W = Ahi W + Alo W (A rows as K-major A operand)
+                    for (int kk = 0; kk < C / 16; ++kk)
+                        mma_ss(tmem + T128, kmajor_desc(sb + R1, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, kk > 0);
+                    for (int kk = 0; kk < C / 16; ++kk)
+                        mma_ss(tmem + T128, kmajor_desc(sb + R2, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
+                }
                 mma_commit(bar(B_UY));
                 ok = mbar_wait(bar(B_OPS2), 0, wc, 42);
             }
@@ -390,6 +397,22 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) u8[e] = -__uint_as_float(v[8 * g + e]);
                     st_global_v4(p.un + ws_row * D + col + 8 * g, pack8(u8));
+                }
+            }
+            if (p.vfac) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {  // V = A W row -> global
+                    uint32_t v[32];
+                    const int col = (D / 2) * h + 32 * c;
+                    tmem_ld32(tl + T128 + col, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float v8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v8[e] = __uint_as_float(v[8 * g + e]);
+                        st_global_v4(p.vfac + ws_row * D + col + 8 * g, pack8(v8));
+                    }
                 }
             }
 #pragma unroll
@@ -524,6 +547,7 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
     p.un = reinterpret_cast<__nv_bfloat16*>(ws + lay.un);
     p.y = reinterpret_cast<__nv_bfloat16*>(ws + lay.y);
     p.zn = reinterpret_cast<__nv_bfloat16*>(ws + lay.zn);
+    p.vfac = lay.vfac ? reinterpret_cast<__nv_bfloat16*>(ws + lay.vfac) : nullptr;
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.limit_ns = 2000000000ull;
     auto kern = ut_prep_tc<D>;

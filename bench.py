@@ -325,6 +325,24 @@ def run_ours(args, rank, world, local):
         e2e = {"value": attn_flops * world * args.e2e_steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
 
+    # prefill -> decode hand-off on the forward workload (timed separately, not part of the step)
+    prefill = None
+    if args.prefill_steps > 0:
+        kc_p = torch.empty((fc.B, fc.H, fc.L, fc.d), dtype=q.dtype, device=dev)
+        ws_p = P.alloc_workspace(P.path_prefill_workspace_bytes(fc.B, fc.H, fc.L, fc.d, q.dtype), dev)
+        P.path_prefill_kcache(k, w, beta, kcache=kc_p, workspace=ws_p)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.prefill_steps):
+            P.path_prefill_kcache(k, w, beta, kcache=kc_p, workspace=ws_p)
+        b.record()
+        torch.cuda.synchronize()
+        prefill = {"ms": a.elapsed_time(b) / args.prefill_steps, "steps": args.prefill_steps,
+                   "workload": "transported key cache of a B%d H%d L%d d%d bf16 prompt" % (fc.B, fc.H, fc.L, fc.d)}
+        del kc_p, ws_p
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, dt, cores, desc = oracle_sample(args.cpu_heads)
@@ -342,7 +360,7 @@ def run_ours(args, rank, world, local):
                        "seq_len": fc.L, "parallelism": "replicas (b,h)-independent" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (forward 384 MiB of q,k,v,w; decode caches 13 GB)"},
             "fwd_ms": fwd_ms_max / args.steps, "fwd_kernel_ms": fk,
-            "decode": dec_obj, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "decode": dec_obj, "prefill_kcache": prefill, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps}
     if rank == 0:
         print(json.dumps(line))
@@ -357,6 +375,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--cpu-heads", type=int, default=96)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-B", type=int, default=8, help="forward batch (8 = the timed workload)")

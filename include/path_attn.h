@@ -115,6 +115,28 @@ int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w
 size_t path_decode_workspace_bytes(int B, int H, int n_max, int d);
 
 /*
+ * Workspace size in bytes for path_prefill_kcache (the UT-prep products plus
+ * the key-side chunk factors).  Returns 0 for unsupported sizes.
+ */
+size_t path_prefill_workspace_bytes(int B, int H, int L, int d, int dtype);
+
+/*
+ * Prefill -> decode hand-off (§3 "Inferência"): writes the transported key
+ * cache of a prompt of L tokens,
+ *     kcache[b,h,j,:] = H_{L-1} ... H_{j+1} k[b,h,j,:]      for j < L,
+ * i.e. the cache that token-by-token path_decode_step calls from an empty
+ * cache would leave, so that decoding continues with n_cached = L.  Computed
+ * per chunk from the UT representation (§3 "Representação de Transformação
+ * UT"): keys transported to their chunk end, then through every later chunk.
+ *   k, w   : [B, H, L, d] (dtype);  beta : [B, H, L] float
+ *   kcache : [B, H, n_max, d] (dtype), n_max >= L; rows >= L are not touched.
+ *            The value cache is the caller's copy of v (values are not transported).
+ *   d      : as for path_attn_fwd;  workspace >= path_prefill_workspace_bytes(...)
+ */
+int path_prefill_kcache(const void* k, const void* w, const float* beta, void* kcache, int B, int H, int L,
+                        int n_max, int d, int dtype, void* workspace, size_t workspace_bytes, path_stream_t stream);
+
+/*
  * In-place key transport alone (§3 "Inferência"): for every head and every
  * cached row j < n_cached,
  *     kcache[b,h,j,:] <- (I - beta_t[b,h] w_t[b,h] w_t[b,h]^T) kcache[b,h,j,:]

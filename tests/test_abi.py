@@ -125,3 +125,18 @@ def test_noalloc_decode_rejects_sizes_beyond_its_scratch(lib):
     assert rc == P.PATH_ERR_WORKSPACE
     assert lib.path_decode_step_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 5, 5, FAKE, None, 1, 1, 128,
                                         ctypes.c_float(0.1), P.PATH_BF16, None) == P.PATH_ERR_INVALID
+
+
+def test_prefill_argument_errors(lib):
+    def call(**kw):
+        a = dict(L=100, n_max=100, d=128, dt=P.PATH_BF16, ws_bytes=1 << 34, kc=FAKE)
+        a.update(kw)
+        return lib.path_prefill_kcache(FAKE, FAKE, FAKE, a["kc"], 1, 2, a["L"], a["n_max"], a["d"], a["dt"], FAKE,
+                                       a["ws_bytes"], None)
+    assert call(n_max=99) == P.PATH_ERR_INVALID      # the cache cannot hold the prompt
+    assert call(L=0) == P.PATH_ERR_INVALID
+    assert call(d=16) == P.PATH_ERR_UNSUPPORTED       # bf16 path: d in {64, 128}
+    assert call(kc=None) == P.PATH_ERR_INVALID
+    assert call(ws_bytes=64) == P.PATH_ERR_WORKSPACE
+    assert lib.path_prefill_workspace_bytes(1, 2, 100, 128, P.PATH_BF16) > lib.path_attn_workspace_bytes(
+        1, 2, 100, 128, P.PATH_BF16)
