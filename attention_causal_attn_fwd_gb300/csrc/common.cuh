@@ -103,8 +103,10 @@ __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
 //   cum  : float [BH, Lp]     inclusive cumulative sum of log f (PaTH-FoX)
 //   vfac : T     [BH, Lp, d]  V = A W per chunk (key-side transport; prefill
 //                             cache only, absent from forward workspaces)
+//   kmax : float [BH, Lp / C] max over the chunk of |khat_j|^2 (PaTH-FoX
+//                             far-block skipping)
 struct FwdLayout {
-    size_t qhat, khat, un, y, zn, cum, vfac, total;
+    size_t qhat, khat, un, y, zn, cum, vfac, kmax, total;
     int Lp;
 };
 inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt, bool with_vfac = false) {
@@ -120,6 +122,7 @@ inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt, bool 
     s.zn = take(rows * C * elt);
     s.cum = take(rows * sizeof(float));
     s.vfac = with_vfac ? take(rows * d * elt) : 0;
+    s.kmax = take((size_t)B * H * (s.Lp / C) * sizeof(float));
     s.total = off;
     return s;
 }

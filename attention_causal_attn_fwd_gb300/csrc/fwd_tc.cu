@@ -84,6 +84,9 @@ struct TcParams {
     float* lse;                // [BH, L] or null
     WsHeader* hdr;
     unsigned long long limit_ns;
+    const __nv_bfloat16* q;    // [BH, L, d] (FoX: query norms for far-block skipping)
+    const float* kmax2;        // [BH, nch] max |khat|^2 per chunk (FoX)
+    int nch;
     int fault;                 // test hook: skip one producer signal
 #ifdef PATH_TRACE
     unsigned long long* trace;
@@ -111,6 +114,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 128);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_BAR + 132);
+    // PaTH-FoX far-block skipping: the scan stops before block iteration
+    // *stop_it (n + 1 = never); set by the softmax warps before they release S_k.
+    volatile int* stop_it = reinterpret_cast<volatile int*>(sm + SM_BAR + 136);
+    int* votes = reinterpret_cast<int*>(sm + SM_BAR + 144);     // [2][4]
+    float* s_kmax2 = reinterpret_cast<float*>(sm + SM_BAR + 176);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Launch order: heads in groups of kHeadGroup; inside a group, tiles
@@ -134,6 +142,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         counts[B_SWREADY] = counts[B_PREADY] = counts[B_QTREADY] = counts[B_SREAD] = 128;
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         *abort_flag = 0;
+        *stop_it = n + 1;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -173,9 +182,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int emp[3] = {B_WEMPTY, B_KEMPTY, B_UEMPTY};
             const uint64_t t0 = globaltimer();
             for (uint32_t spin = 0; ok && (nxt[0] <= n || nxt[1] <= n || nxt[2] <= n || nxt[3] <= n); ++spin) {
+                const int stop = FOX ? *stop_it : n + 1;
                 for (int sl = 0; sl < 4; ++sl) {
                     const int it = nxt[sl];
                     if (it > n) continue;
+                    if (it >= stop) { nxt[sl] = n + 1; continue; }  // beyond the last block the scan visits
                     if ((sl == SW || sl == SU) && it == n) { nxt[sl] = n + 1; continue; }
                     if (sl == SV) {
                         if (it >= 2 && !mbar_test_wait(bar((it & 1) ? B_VEMPTY1 : B_VEMPTY0), (uint32_t)(((it >> 1) - 1) & 1)))
@@ -255,12 +266,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // executed), so the issue order is the tensor pipe's schedule:
             //   MMA1(it) [S_k | S_w, N = 256] -> MMA3(it) -> P V(it-1)
             // (P V covers the conversion of q~ for the next MMA1).
+            int last = n;  // last block iteration whose P V is issued
             for (int it = 1; it <= n && ok; ++it) {
                 const int m = n - it;
+                if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
+                if (FOX && *stop_it <= it) {  // every block from here on contributes exactly zero
+                    last = it - 1;
+                    break;
+                }
                 if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
                 if (!(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
                 if (m > 0 && !(ok = mbar_wait(bar(B_WFULL), it & 1, wc, 15))) break;
-                if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
                 tc_fence_after();
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
@@ -290,7 +306,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 issue_pv(it - 1);
                 TC_TRACE(2, it);
             }
-            if (ok && wait_pv(n)) issue_pv(n);  // the last block's P V
+            if (ok && wait_pv(last)) issue_pv(last);  // the last block's P V
             // every issued MMA completes before TMEM is released
             mma_commit(bar(B_DRAIN));
             drain_wait(bar(B_DRAIN), 0, p.limit_ns);
@@ -303,6 +319,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float ci = FOX ? cumh[row0 + r] : 0.f;
         constexpr float kL2e = 1.4426950408889634f;
         float m_run = -INFINITY, l_run = 0.f;
+        float m_true = -INFINITY;  // largest logit seen (log2 units)
+        float qk_bound = 0.f;      // FoX: scale log2e |q_i| max_j |khat_j|, with a 2x margin
+        if (FOX && n > 0) {
+            if (warp == 2) {  // max |khat|^2 over the chunks left of this tile
+                float x = 0.f;
+                for (int c = lane; c < n; c += 32) x = fmaxf(x, p.kmax2[(size_t)bh * p.nch + c]);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+                if (lane == 0) *s_kmax2 = x;
+            }
+            float qn2 = 0.f;
+            if (row0 + r < p.L) {
+                const uint4* qv = reinterpret_cast<const uint4*>(p.q + ((size_t)bh * p.L + row0 + r) * D);
+#pragma unroll 4
+                for (int g = 0; g < D / 8; ++g) {
+                    Vec16<__nv_bfloat16> v;
+                    v.raw = __ldg(qv + g);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qn2 = fmaf(v.get(e), v.get(e), qn2);
+                }
+            }
+            named_bar_sync(2, 128);
+            // |q~_i . khat_j| <= |q_i| |khat_j|: the transitions are non-expansive for
+            // beta in [0, 2] and unit w; the factor 2 covers bf16 rounding of w.
+            qk_bound = 2.0f * p.sl2 * sqrtf(qn2 * *s_kmax2);
+        }
+        int last = n;
         bool ok = true;
         for (int it = 0; it <= n; ++it) {
             const int m = n - it;
@@ -319,9 +362,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]) * p.sl2;
             }
-            // S_k is in registers: the next block's MMA1 may overwrite it
-            tc_fence_before();
-            mbar_arrive(bar(B_SREAD));
+            // S_k is in registers: the next block's MMA1 may overwrite it (FoX
+            // first decides whether there is a next block)
+            if (!FOX) {
+                tc_fence_before();
+                mbar_arrive(bar(B_SREAD));
+            }
             if (r == 0) TC_TRACE(5, it);
             if (FOX) {
 #pragma unroll
@@ -345,6 +391,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float mx = -INFINITY;
 #pragma unroll
             for (int j = 0; j < 128; ++j) mx = fmaxf(mx, s[j]);
+            bool stop = false;
+            if (FOX) {
+                m_true = fmaxf(m_true, mx);
+                if (m > 0) {
+                    // Every key left of this block has bias <= c_i - c_(128 m - 1) and
+                    // |logit| <= qk_bound: below m_true - 160 (log2) its exp2 is 0 in fp32.
+                    const float bound = qk_bound + (ci - cumh[m * kTcC - 1]) * kL2e - m_true;
+                    const bool sat = (row0 + r >= p.L) || bound < -160.0f;
+                    const int vote = __all_sync(0xffffffffu, sat);
+                    if (lane == 0) votes[(it & 1) * 4 + (warp & 3)] = vote;
+                    named_bar_sync(2, 128);
+                    const int* vv = votes + (it & 1) * 4;
+                    stop = vv[0] && vv[1] && vv[2] && vv[3];
+                    if (stop && warp == 2 && lane == 0) *stop_it = it + 1;
+                }
+                tc_fence_before();
+                mbar_arrive(bar(B_SREAD));
+            }
             const float m_new = fmaxf(m_run, mx);
             const bool rescale = m_new > m_run + 8.0f;
             const float m_use = rescale ? m_new : m_run;
@@ -398,8 +462,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(B_PREADY));
             if (r == 0) TC_TRACE(7, it);
+            if (stop) {
+                last = it;
+                break;
+            }
         }
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), n & 1, wc, 22));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (uint32_t)(last & 1), wc, 22));
         if (ok) {
             tc_fence_after();
             const int row = row0 + r;
@@ -467,7 +535,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(bar(B_QTREADY));
         }
         for (int it = 1; it < n && ok; ++it) {  // block m = n - it > 0 needs the transport
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SWFULL), (it - 1) & 1, wc, 31));
+            if (FOX) {  // S_w of block iteration it, unless the scan stopped before it
+                int st = 0;  // 0 waiting, 1 ready, 2 stopped, 3 failed
+                const uint64_t t0 = globaltimer();
+                for (uint32_t spin = 0; st == 0; ++spin) {
+                    if (mbar_test_wait(bar(B_SWFULL), (it - 1) & 1)) st = 1;
+                    else if (*stop_it <= it) st = 2;
+                    else if ((spin & 255u) == 255u && (*abort_flag || globaltimer() - t0 > p.limit_ns)) {
+                        if (!*abort_flag) { report_status(p.hdr, PATH_ERR_TIMEOUT, 33); *abort_flag = 1; }
+                        st = 3;
+                    }
+                }
+                st = __reduce_max_sync(0xffffffffu, (unsigned)st);
+                if (st == 2) break;
+                ok = st == 1;
+            } else {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SWFULL), (it - 1) & 1, wc, 31));
+            }
             if (!ok) break;
             if (r == 0) TC_TRACE(8, it);
             tc_fence_after();
@@ -568,6 +652,9 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.limit_ns = fault ? 20000000ull : 2000000000ull;  // 20 ms under the test hook, else 2 s
     p.fault = fault;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.kmax2 = reinterpret_cast<const float*>(ws + lay.kmax);
+    p.nch = lay.Lp / kTcC;
 #ifdef PATH_TRACE
     p.trace = trace_buffer();
 #endif

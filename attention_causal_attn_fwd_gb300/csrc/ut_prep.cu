@@ -20,7 +20,7 @@
 namespace pathattn {
 
 cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w, const float* beta, int BH, int L,
-                              unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
+                              unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st);
 
 template <typename T, int C, int D, int NT>
 struct UtSmem {
@@ -196,7 +196,7 @@ cudaError_t launch_ut_prep(int dtype, int C, int d, const void* q, const void* k
         if (C == 32 && d == 64) return launch_ut_t<float, 32, 64>(q, k, w, beta, log_f, BH, L, ws, lay, st);
         if (C == 32 && d == 128) return launch_ut_t<float, 32, 128>(q, k, w, beta, log_f, BH, L, ws, lay, st);
     } else if (C == 128) {  // bf16: tensor-core UT prep (ut_prep_tc.cu)
-        cudaError_t e = launch_ut_prep_tc(d, q, k, w, beta, BH, L, ws, lay, st);
+        cudaError_t e = launch_ut_prep_tc(d, q, k, w, beta, BH, L, ws, lay, log_f != nullptr, st);
         if (e == cudaSuccess && log_f)
             fox_cumsum<<<BH, 1024, 0, st>>>(log_f, L, lay.Lp, reinterpret_cast<float*>(ws + lay.cum));
         return e == cudaSuccess ? cudaGetLastError() : e;

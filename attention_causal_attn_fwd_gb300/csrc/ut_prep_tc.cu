@@ -69,6 +69,8 @@ struct UtParams {
     __nv_bfloat16* y;            // [BH, Lp, C]
     __nv_bfloat16* zn;           // [BH, Lp, C]
     __nv_bfloat16* vfac;         // [BH, Lp, d] V = A W (prefill cache only) or null
+    float* kmax2;                // [BH, nch] max |khat|^2 per chunk (PaTH-FoX) or null
+    int nch;
     WsHeader* hdr;
     unsigned long long limit_ns;
 };
@@ -503,6 +505,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         if (ok) {
             tc_fence_after();
             const __nv_bfloat16* krow = p.k + ((size_t)bh * p.L + grow) * D;
+            float n2 = 0.f;  // this thread's part of |khat_row|^2
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {  // khat = K - (Z A) W
                 uint32_t v[32];
@@ -515,9 +518,25 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     kv.raw = grow < p.L ? ld_global_nc_v4(krow + col + 8 * g) : make_uint4(0, 0, 0, 0);
                     float k8[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) k8[e] = kv.get(e) - __uint_as_float(v[8 * g + e]);
+                    for (int e = 0; e < 8; ++e) {
+                        k8[e] = kv.get(e) - __uint_as_float(v[8 * g + e]);
+                        n2 = fmaf(k8[e], k8[e], n2);
+                    }
                     st_global_v4(p.khat + ws_row * D + col + 8 * g, pack8(k8));
                 }
+            }
+            if (p.kmax2) {  // chunk max of |khat|^2 over rows < L (the solve temp is free)
+                float* red = reinterpret_cast<float*>(sm + RT);
+                red[r + 128 * h] = grow < p.L ? n2 : 0.f;
+                named_bar_sync(1, kCompute);
+                if (h == 0) {
+                    float x = red[r] + red[r + 128];
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+                    if (lane == 0) red[256 + (warp & 3)] = x;
+                }
+                named_bar_sync(1, kCompute);
+                if (t == 0) p.kmax2[(size_t)bh * p.nch + chunk] = fmaxf(fmaxf(red[256], red[257]), fmaxf(red[258], red[259]));
             }
         }
     }
@@ -532,7 +551,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
 
 template <int D>
 static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, const float* beta, int BH, int L,
-                                  unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
+                                  unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st) {
     CUtensorMap mq, mk, mw;
     if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mw, w, D, L, BH))
         return cudaErrorInvalidValue;
@@ -548,6 +567,8 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
     p.y = reinterpret_cast<__nv_bfloat16*>(ws + lay.y);
     p.zn = reinterpret_cast<__nv_bfloat16*>(ws + lay.zn);
     p.vfac = lay.vfac ? reinterpret_cast<__nv_bfloat16*>(ws + lay.vfac) : nullptr;
+    p.kmax2 = want_kmax ? reinterpret_cast<float*>(ws + lay.kmax) : nullptr;
+    p.nch = lay.Lp / utk::C;
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.limit_ns = 2000000000ull;
     auto kern = ut_prep_tc<D>;
@@ -558,9 +579,9 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
 }
 
 cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w, const float* beta, int BH, int L,
-                              unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
-    if (d == 64) return launch_ut_tc_d<64>(q, k, w, beta, BH, L, ws, lay, st);
-    if (d == 128) return launch_ut_tc_d<128>(q, k, w, beta, BH, L, ws, lay, st);
+                              unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st) {
+    if (d == 64) return launch_ut_tc_d<64>(q, k, w, beta, BH, L, ws, lay, want_kmax, st);
+    if (d == 128) return launch_ut_tc_d<128>(q, k, w, beta, BH, L, ws, lay, want_kmax, st);
     return cudaErrorInvalidValue;
 }
 

@@ -137,3 +137,13 @@ def test_fox_16k_full_size_sampled():
     check(got, o_ref, torch.bfloat16, "fox16k sampled")
     check_lse(got_lse, lse_ref, torch.bfloat16, "fox16k sampled")
     assert torch.isfinite(o).all()
+
+
+@pytest.mark.parametrize("L", [1000, 2048])
+def test_fox_strong_gates_far_blocks_skipped(L):
+    """Strong forget gates (log f = logsigmoid(N(0,1))) make every key more than a few hundred
+    tokens away contribute exactly zero, so the scan stops early; every row must still match."""
+    x = inputs.make_fwd(1, 3, L, 128, "bf16", seed=61, fox=True)
+    g = torch.Generator().manual_seed(61)
+    x.log_f = torch.nn.functional.logsigmoid(torch.randn(x.beta.shape, generator=g)).float()
+    _full_case(x, "fox strong gates L=%d" % L)
