@@ -24,7 +24,7 @@
 //   warps 2-5   softmax: S_k -> P (bf16, into TMEM), row statistics, epilogue
 //   warps 6-9   query transport: S_w -> bf16 (TMEM), fp32 q~ -> bf16 q~ (smem)
 //
-// TMEM (512 columns x 128 lanes, fp32): [0,128) S_k / P, [128,256) S_w /
+// TMEM (512 columns x 128 lanes, fp32): [0,128) S_k / P (bf16), [128,256) S_w /
 // bf16(S_w), [256,256+d) O, [384,384+d) q~ master.
 // Shared memory (1024-aligned, 128-byte swizzled tiles as TMA writes them):
 //   SM_Q  32 KB  Q (diagonal) then bf16 q~, K-major, 64-column chunks of 16 KB
@@ -33,7 +33,8 @@
 //   SM_V  64 KB  V_m, MN-major B operand (64-column boxes of 16 KB), two
 //                slots by block parity
 //   SM_U  32 KB  -U_m (MN-major) or, on the diagonal, Y (K-major)
-//   SM_P  32 KB  P (bf16, K-major A operand of P V)
+//   SM_P  32 KB  W slot 1 (W of odd block iterations; slot 0 is interleaved
+//                with khat in SM_KW)
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
 // PATH_ERR_TIMEOUT in the workspace status word, every role stops, pending
 // copies and MMAs are drained (bounded) and TMEM is freed before exit.
@@ -59,10 +60,10 @@ constexpr uint32_t TM_S = 0, TM_SW = 128, TM_O = 256, TM_Q = 384;
 // ahead of its waiter (a parity wait cannot tell those apart).
 // Each operand slot (khat, W, -U, V) has its own full/empty pair, released
 // by the MMA that consumes it, so every refill starts as early as possible.
-// V is double-buffered by block parity (slot it & 1).
-enum Bar { B_QFULL = 0, B_KFULL, B_WFULL, B_UFULL, B_VFULL0, B_KEMPTY, B_WEMPTY, B_UEMPTY, B_VEMPTY0, B_SFULL,
-           B_SWREADY, B_PREADY, B_QUPD, B_QTREADY, B_ODONE, B_DRAIN, B_SREAD, B_VFULL1, B_VEMPTY1, B_PFREE,
-           B_SWFULL, B_COUNT };
+// W and V are double-buffered by block parity (slot it & 1).
+enum Bar { B_QFULL = 0, B_KFULL, B_WFULL0, B_UFULL, B_VFULL0, B_KEMPTY, B_WEMPTY0, B_UEMPTY, B_VEMPTY0, B_SFULL,
+           B_SWREADY, B_PREADY, B_QUPD, B_QTREADY, B_ODONE, B_DRAIN, B_SREAD, B_VFULL1, B_VEMPTY1, B_WFULL1,
+           B_WEMPTY1, B_SWFULL, B_COUNT };
 
 constexpr int kHeadGroup = 8;
 
@@ -103,7 +104,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     static_assert(D == 64 || D == 128, "head dim");
     constexpr int KCH = D / 64;          // 64-column chunks of the head dim
     constexpr uint32_t ROWB = 128u * D * 2u;  // bytes of one [128 x D] bf16 tile
-        constexpr uint32_t IDESC_S256 = idesc_bf16(256, false);
     constexpr uint32_t IDESC_S128 = idesc_bf16(128, false);
     constexpr uint32_t IDESC_PV = idesc_bf16(D, true);
 
@@ -166,20 +166,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_Q + c * 16384, &tm_q, bar(B_QFULL), c * 64, row0, bh);
             mbar_expect_tx(bar(B_KFULL), ROWB);
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_KW + c * 32768, &tm_k, bar(B_KFULL), c * 64, row0, bh);
-            mbar_expect_tx(bar(B_WFULL), 32768);
+            mbar_expect_tx(bar(B_WFULL0), 32768);
             for (int c = 0; c < 2; ++c)
-                tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_zn, bar(B_WFULL), c * 64, row0, bh);
+                tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_zn, bar(B_WFULL0), c * 64, row0, bh);
             mbar_expect_tx(bar(B_UFULL), 32768);
             for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_U + c * 16384, &tm_y, bar(B_UFULL), c * 64, row0, bh);
             mbar_expect_tx(bar(B_VFULL0), ROWB);
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V + c * 16384, &tm_v, bar(B_VFULL0), c * 64, row0, bh);
             // scan blocks: refill each slot as soon as its consumer has finished.
-            // Slot s for block iteration it needs the (it)-th completion of its
-            // empty barrier (V: slot it & 1, its (it >> 1)-th completion).  W
-            // and -U are not used by the last block (m = 0).
+            // khat / -U for block iteration it need the (it)-th completion of
+            // their empty barrier; W and V use slot it & 1 and, from it = 2 on,
+            // the (it >> 1)-th completion of that slot's empty barrier.  W and
+            // -U are not used by the last block (m = 0).
             enum { SW = 0, SK, SU, SV };
-            int nxt[4] = {1, 1, 1, 1}, issued[5] = {1, 1, 1, 1, 0};  // issued[3]/[4]: V slots 0/1
-            const int emp[3] = {B_WEMPTY, B_KEMPTY, B_UEMPTY};
+            // issued: W slot 0, khat, -U, V slot 0, V slot 1, W slot 1
+            int nxt[4] = {1, 1, 1, 1}, issued[6] = {1, 1, 1, 1, 0, 0};
+            const int emp[3] = {B_WEMPTY0, B_KEMPTY, B_UEMPTY};
             const uint64_t t0 = globaltimer();
             for (uint32_t spin = 0; ok && (nxt[0] <= n || nxt[1] <= n || nxt[2] <= n || nxt[3] <= n); ++spin) {
                 const int stop = FOX ? *stop_it : n + 1;
@@ -188,24 +190,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (it > n) continue;
                     if (it >= stop) { nxt[sl] = n + 1; continue; }  // beyond the last block the scan visits
                     if ((sl == SW || sl == SU) && it == n) { nxt[sl] = n + 1; continue; }
-                    if (sl == SV) {
-                        if (it >= 2 && !mbar_test_wait(bar((it & 1) ? B_VEMPTY1 : B_VEMPTY0), (uint32_t)(((it >> 1) - 1) & 1)))
-                            continue;
+                    if (sl == SV || sl == SW) {
+                        const int eb = sl == SV ? ((it & 1) ? B_VEMPTY1 : B_VEMPTY0) : ((it & 1) ? B_WEMPTY1 : B_WEMPTY0);
+                        if (it >= 2 && !mbar_test_wait(bar(eb), (uint32_t)(((it >> 1) - 1) & 1))) continue;
                     } else if (!mbar_test_wait(bar(emp[sl]), (it - 1) & 1)) {
                         continue;
                     }
                     const int r = (n - it) * kTcC;
                     nxt[sl] = it + 1;
                     if (sl == SV && p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
-                    const int fb = sl == SW ? B_WFULL : sl == SK ? B_KFULL : sl == SU ? B_UFULL : ((it & 1) ? B_VFULL1 : B_VFULL0);
+                    const int fb = sl == SW ? ((it & 1) ? B_WFULL1 : B_WFULL0)
+                                   : sl == SK ? B_KFULL : sl == SU ? B_UFULL : ((it & 1) ? B_VFULL1 : B_VFULL0);
                     mbar_expect_tx(bar(fb), ROWB);
                     for (int c = 0; c < KCH; ++c) {
                         if (sl == SK) tma_load_3d(sb + SM_KW + c * 32768, &tm_khat, bar(fb), c * 64, r, bh);
-                        if (sl == SW) tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_w, bar(fb), c * 64, r, bh);
+                        if (sl == SW) {
+                            const uint32_t dst = (it & 1) ? sb + SM_P + c * 16384 : sb + SM_KW + c * 32768 + 16384;
+                            tma_load_3d(dst, &tm_w, bar(fb), c * 64, r, bh);
+                        }
                         if (sl == SU) tma_load_3d(sb + SM_U + c * 16384, &tm_un, bar(fb), c * 64, r, bh);
                         if (sl == SV) tma_load_3d(sb + SM_V + (it & 1) * 32768 + c * 16384, &tm_v, bar(fb), c * 64, r, bh);
                     }
-                    ++issued[sl == SV ? 3 + (it & 1) : sl];
+                    ++issued[sl == SV ? 3 + (it & 1) : (sl == SW && (it & 1)) ? 5 : sl];
                     TC_TRACE(12 + sl, it);
                 }
                 if ((spin & 255u) == 255u) {
@@ -219,8 +225,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             // copies still in flight must land before the CTA exits
             drain_wait(bar(B_QFULL), 0, p.limit_ns);
-            const int ful[5] = {B_WFULL, B_KFULL, B_UFULL, B_VFULL0, B_VFULL1};
-            for (int sl = 0; sl < 5; ++sl)
+            const int ful[6] = {B_WFULL0, B_KFULL, B_UFULL, B_VFULL0, B_VFULL1, B_WFULL1};
+            for (int sl = 0; sl < 6; ++sl)
                 if (issued[sl] > 0) drain_wait(bar(ful[sl]), (uint32_t)((issued[sl] - 1) & 1), p.limit_ns);
         }
     } else if (warp == 1) {
@@ -230,15 +236,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // shared memory) is issued whenever its P is ready, before or after
         // the next MMA1, whichever inputs arrive first.
         if (lane == 0) {
-            auto issue_pv = [&](int blk) {  // O (+)= P V for block iteration blk
+            auto issue_pv = [&](int blk) {  // O (+)= P V for block iteration blk (P in TMEM)
                 tc_fence_after();
                 const uint32_t vbuf = sb + SM_V + (uint32_t)(blk & 1) * 32768u;
                 for (int kk = 0; kk < kTcC / 16; ++kk)
-                    mma_ss(tmem + TM_O, kmajor_desc(sb + SM_P, kk, 16384), mnmajor_desc(vbuf, kk), IDESC_PV,
+                    mma_ts(tmem + TM_O, tmem + TM_S + kk * 8, mnmajor_desc(vbuf, kk), IDESC_PV,
                            (blk > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(B_ODONE));
                 mma_commit(bar((blk & 1) ? B_VEMPTY1 : B_VEMPTY0));
-                mma_commit(bar(B_PFREE));
             };
             // P V of block blk needs its P (p_ready, (blk+1)-th completion) and
             // its V slot (blk & 1, (blk >> 1)+1-th completion).
@@ -247,7 +252,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                        mbar_wait(bar((blk & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((blk >> 1) & 1), wc, 19);
             };
             bool ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL), 0, wc, 11) &&
-                      mbar_wait(bar(B_WFULL), 0, wc, 12) && mbar_wait(bar(B_UFULL), 0, wc, 12);
+                      mbar_wait(bar(B_WFULL0), 0, wc, 12) && mbar_wait(bar(B_UFULL), 0, wc, 12);
             if (ok) {
                 tc_fence_after();
                 // diagonal: S = Q K^T + Y (-Z)^T
@@ -259,34 +264,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                            kmajor_desc(sb + SM_KW + 16384, kk, 32768), IDESC_S128, 1);
                 mma_commit(bar(B_SFULL));
                 mma_commit(bar(B_KEMPTY));
-                mma_commit(bar(B_WEMPTY));
+                mma_commit(bar(B_WEMPTY0));
                 mma_commit(bar(B_UEMPTY));
             }
             // Issue is blocking (an MMA group's issue returns about when it has
             // executed), so the issue order is the tensor pipe's schedule:
-            //   MMA1(it) [S_k | S_w, N = 256] -> MMA3(it) -> P V(it-1)
-            // (P V covers the conversion of q~ for the next MMA1).
+            //   S_w(it) -> P V(it-1) -> S_k(it) -> MMA3(it)
+            // P V and S_k cover the conversion of S_w; S_k follows P V because it
+            // overwrites the TMEM columns that hold P.
             int last = n;  // last block iteration whose P V is issued
             for (int it = 1; it <= n && ok; ++it) {
                 const int m = n - it;
-                if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
-                if (FOX && *stop_it <= it) {  // every block from here on contributes exactly zero
-                    last = it - 1;
-                    break;
+                if (FOX) {  // the softmax warps decide first whether block it is visited
+                    if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
+                    if (*stop_it <= it) {  // every block from here on contributes exactly zero
+                        last = it - 1;
+                        break;
+                    }
                 }
                 if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
+                if (m > 0) {
+                    if (!(ok = mbar_wait(bar((it & 1) ? B_WFULL1 : B_WFULL0), (uint32_t)((it >> 1) & 1), wc, 15)))
+                        break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t bdesc = (it & 1) ? kmajor_desc(sb + SM_P, kk, 16384)
+                                                        : kmajor_desc(sb + SM_KW + 16384, kk, 32768);
+                        mma_ss(tmem + TM_SW, kmajor_desc(sb + SM_Q, kk, 16384), bdesc, IDESC_S128, kk > 0);
+                    }
+                    mma_commit(bar(B_SWFULL));
+                    mma_commit(bar((it & 1) ? B_WEMPTY1 : B_WEMPTY0));
+                    TC_TRACE(0, it);
+                }
+                if (!(ok = wait_pv(it - 1))) break;
+                TC_TRACE(20, it);
+                issue_pv(it - 1);
+                TC_TRACE(2, it);
                 if (!(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
-                if (m > 0 && !(ok = mbar_wait(bar(B_WFULL), it & 1, wc, 15))) break;
                 tc_fence_after();
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
-                           m > 0 ? IDESC_S256 : IDESC_S128, kk > 0);
+                           IDESC_S128, kk > 0);
                 mma_commit(bar(B_SFULL));
                 mma_commit(bar(B_KEMPTY));
-                if (m > 0) {
-                    mma_commit(bar(B_SWFULL));
-                    mma_commit(bar(B_WEMPTY));
-                }
                 TC_TRACE(1, it);
                 if (m > 0) {
                     TC_TRACE(21, it);
@@ -301,10 +321,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_commit(bar(B_UEMPTY));
                     TC_TRACE(3, it);
                 }
-                if (!(ok = wait_pv(it - 1))) break;
-                TC_TRACE(20, it);
-                issue_pv(it - 1);
-                TC_TRACE(2, it);
             }
             if (ok && wait_pv(last)) issue_pv(last);  // the last block's P V
             // every issued MMA completes before TMEM is released
@@ -360,8 +376,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_ld32(tl + TM_S + 32 * c, raw);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]) * p.sl2;
+                for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]);
             }
+            // Without FoX the scores stay raw (the scale is applied inside the
+            // exponent, one FFMA each); with FoX they become log2-unit logits.
+            const float sl2 = p.sl2;
             // S_k is in registers: the next block's MMA1 may overwrite it (FoX
             // first decides whether there is a next block)
             if (!FOX) {
@@ -376,10 +395,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
                         const float4 cv = __ldg(cj + j4);
-                        s[32 * c + 4 * j4 + 0] += (ci - cv.x) * kL2e;
-                        s[32 * c + 4 * j4 + 1] += (ci - cv.y) * kL2e;
-                        s[32 * c + 4 * j4 + 2] += (ci - cv.z) * kL2e;
-                        s[32 * c + 4 * j4 + 3] += (ci - cv.w) * kL2e;
+                        s[32 * c + 4 * j4 + 0] = fmaf(s[32 * c + 4 * j4 + 0], sl2, (ci - cv.x) * kL2e);
+                        s[32 * c + 4 * j4 + 1] = fmaf(s[32 * c + 4 * j4 + 1], sl2, (ci - cv.y) * kL2e);
+                        s[32 * c + 4 * j4 + 2] = fmaf(s[32 * c + 4 * j4 + 2], sl2, (ci - cv.z) * kL2e);
+                        s[32 * c + 4 * j4 + 3] = fmaf(s[32 * c + 4 * j4 + 3], sl2, (ci - cv.w) * kL2e);
                     }
                 }
             }
@@ -388,9 +407,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int j = 0; j < 128; ++j)
                     if (j > r) s[j] = -INFINITY;
             }
-            float mx = -INFINITY;
+            float mx;  // row max in log2 units (8 independent partial maxima)
+            {
+                float pm[8];
 #pragma unroll
-            for (int j = 0; j < 128; ++j) mx = fmaxf(mx, s[j]);
+                for (int u = 0; u < 8; ++u) pm[u] = s[u];
+#pragma unroll
+                for (int j = 8; j < 128; ++j) pm[j & 7] = fmaxf(pm[j & 7], s[j]);
+                mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                if (!FOX) mx *= sl2;  // sl2 > 0: the max of raw scores scales
+            }
             bool stop = false;
             if (FOX) {
                 m_true = fmaxf(m_true, mx);
@@ -412,25 +438,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float m_new = fmaxf(m_run, mx);
             const bool rescale = m_new > m_run + 8.0f;
             const float m_use = rescale ? m_new : m_run;
-            const float alpha = rescale ? exp2f(m_run - m_use) : 1.0f;
-            float sum = 0.f;
+            const float alpha = rescale ? ex2_approx(m_run - m_use) : 1.0f;
+            float psum[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) psum[u] = 0.f;
             uint32_t pk[64];
+            const float neg_m = -m_use;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
-                const float p0 = exp2f(s[2 * j] - m_use);
-                const float p1 = exp2f(s[2 * j + 1] - m_use);
-                sum += p0 + p1;
+                const float p0 = ex2_approx(FOX ? s[2 * j] + neg_m : fmaf(s[2 * j], sl2, neg_m));
+                const float p1 = ex2_approx(FOX ? s[2 * j + 1] + neg_m : fmaf(s[2 * j + 1], sl2, neg_m));
+                psum[j & 7] += p0 + p1;
                 pk[j] = pack_bf16x2(p0, p1);
             }
+            const float sum = ((psum[0] + psum[1]) + (psum[2] + psum[3])) + ((psum[4] + psum[5]) + (psum[6] + psum[7]));
             l_run = l_run * alpha + sum;
             if (r == 0) TC_TRACE(6, it);
             // The O rescale uses warp-collective TMEM loads/stores, so the whole
             // warp takes it when any of its rows needs it (alpha = 1 elsewhere).
-            bool waited_prev = false;
             if (__any_sync(0xffffffffu, rescale && it > 0)) {
                 // O is stable once the previous block's P V has completed
                 const bool ok2 = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (it - 1) & 1, wc, 21));
-                waited_prev = true;
                 if (!ok2) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
@@ -444,21 +472,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             m_run = m_use;
-            // the P buffer is free once the P V of block it-1 has completed
-            // (the it-th completion of the P-free barrier)
-            if (it >= 1 && !waited_prev) {
-                const bool ok3 = __all_sync(0xffffffffu, mbar_wait(bar(B_PFREE), (uint32_t)((it - 1) & 1), wc, 23));
-                if (!ok3) { ok = false; break; }
-            }
-            {
-                uint8_t* prow = sm + SM_P + r * 128;
-#pragma unroll
-                for (int G = 0; G < 16; ++G)
-                    *reinterpret_cast<uint4*>(prow + (G >> 3) * 16384 + (((G & 7) ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * G], pk[4 * G + 1], pk[4 * G + 2], pk[4 * G + 3]);
-            }
+            // P (bf16 pairs) over S_k's first 64 columns: the A operand of P V.  The
+            // next S_k is issued after this P V, so it cannot overwrite P early.
+            tmem_st32(tl + TM_S, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+            tmem_st32(tl + TM_S + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_PREADY));
             if (r == 0) TC_TRACE(7, it);
