@@ -14,7 +14,8 @@
 //     r <- r P_c = r - (r W_c^T)(A_c W_c) = r - (r W_c^T) V_c,
 // a left-to-right scan over later chunks with the factor V_c = A_c W_c, which
 // the UT prep writes when asked to.  This kernel runs that scan on CUDA cores
-// in fp32 (one CTA per key chunk and head).
+// in fp32 (one CTA per key chunk and head); it serves fp32 and bf16 at d = 64.
+// bf16 at d = 128 uses the tensor-core suffix-product form (prefill_tc.cu).
 #include "common.cuh"
 #include "simt_gemm.cuh"
 #include "ut_prep.cuh"
@@ -81,6 +82,10 @@ static cudaError_t launch_prefill_t(const void* w, void* kcache, int BH, int L, 
     return cudaGetLastError();
 }
 
+// Tensor-core suffix-product transport for bf16, d = 128 (prefill_tc.cu).
+cudaError_t launch_prefill_tc(const void* w, void* kcache, int BH, int L, int n_max, unsigned char* ws,
+                              const FwdLayout& lay, cudaStream_t st);
+
 // UT prep (with the V factor) followed by the key transport.  C is the
 // dtype's forward chunk size; the prompt's q is not needed, k stands in for it.
 cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w, const float* beta, void* kcache,
@@ -95,7 +100,7 @@ cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w
         if (C == 32 && d == 128) return launch_prefill_t<float, 32, 128>(w, kcache, BH, L, n_max, ws, lay, st);
     } else {
         if (C == 128 && d == 64) return launch_prefill_t<bf, 128, 64>(w, kcache, BH, L, n_max, ws, lay, st);
-        if (C == 128 && d == 128) return launch_prefill_t<bf, 128, 128>(w, kcache, BH, L, n_max, ws, lay, st);
+        if (C == 128 && d == 128) return launch_prefill_tc(w, kcache, BH, L, n_max, ws, lay, st);
     }
     return cudaErrorInvalidValue;
 }

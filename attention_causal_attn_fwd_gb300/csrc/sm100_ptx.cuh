@@ -251,5 +251,22 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 8 consecutive values of row r, granule G (columns 8G..8G+7) of a K-major
+// 128-row operand, written as hi and lo bf16 parts.
+__device__ __forceinline__ void put_hilo(uint8_t* hi, uint8_t* lo, int r, int G, const float* v) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(hv);
+        const __nv_bfloat162 lv = __floats2bfloat162_rn(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
+        h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+        l[e] = *reinterpret_cast<const uint32_t*>(&lv);
+    }
+    const uint32_t off = (uint32_t)(G >> 3) * 16384u + (uint32_t)r * 128u + ((uint32_t)((G & 7) ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 }  // namespace sm100
 }  // namespace pathattn

@@ -75,23 +75,6 @@ struct UtParams {
     unsigned long long limit_ns;
 };
 
-// 8 consecutive values of row r, granule G (columns 8G..8G+7) of a K-major
-// 128-row operand, written as hi and lo bf16 parts.
-__device__ __forceinline__ void put_hilo(uint8_t* hi, uint8_t* lo, int r, int G, const float* v) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 hv = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
-        const float2 hf = __bfloat1622float2(hv);
-        const __nv_bfloat162 lv = __floats2bfloat162_rn(v[2 * e] - hf.x, v[2 * e + 1] - hf.y);
-        h[e] = *reinterpret_cast<const uint32_t*>(&hv);
-        l[e] = *reinterpret_cast<const uint32_t*>(&lv);
-    }
-    const uint32_t off = (uint32_t)(G >> 3) * 16384u + (uint32_t)r * 128u + ((uint32_t)((G & 7) ^ (r & 7)) << 4);
-    *reinterpret_cast<uint4*>(hi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-}
-
 __device__ __forceinline__ uint4 pack8(const float* v) {
     return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                       pack_bf16x2(v[6], v[7]));
@@ -435,11 +418,18 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_OPS2));
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 52));
         }
+        // This thread's half of the Q row, loaded while Y W runs on the tensor cores.
+        uint4 qpre[D / 16];
+        {
+            const __nv_bfloat16* qrow = p.q + ((size_t)bh * p.L + grow) * D;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i)
+                qpre[i] = (ok && grow < p.L) ? ld_global_nc_v4(qrow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 52));
         if (ok) {
             tc_fence_after();
-            const __nv_bfloat16* qrow = p.q + ((size_t)bh * p.L + grow) * D;
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {  // qhat = Q - Y W  (fp32)
                 uint32_t v[32];
@@ -449,7 +439,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     Vec16<__nv_bfloat16> qv;
-                    qv.raw = grow < p.L ? ld_global_nc_v4(qrow + col + 8 * g) : make_uint4(0, 0, 0, 0);
+                    qv.raw = qpre[4 * c + g];
                     float4* dst = reinterpret_cast<float4*>(p.qhat + ws_row * D + col + 8 * g);
                     dst[0] = make_float4(qv.get(0) - __uint_as_float(v[8 * g + 0]), qv.get(1) - __uint_as_float(v[8 * g + 1]),
                                          qv.get(2) - __uint_as_float(v[8 * g + 2]), qv.get(3) - __uint_as_float(v[8 * g + 3]));
@@ -500,11 +490,18 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_OPS4));
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_K), 0, wc, 54));
         }
+        // This thread's half of the K row, loaded while (Z A) W runs.
+        uint4 kpre[D / 16];
+        {
+            const __nv_bfloat16* krow = p.k + ((size_t)bh * p.L + grow) * D;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i)
+                kpre[i] = (ok && grow < p.L) ? ld_global_nc_v4(krow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_K), 0, wc, 54));
         if (ok) {
             tc_fence_after();
-            const __nv_bfloat16* krow = p.k + ((size_t)bh * p.L + grow) * D;
             float n2 = 0.f;  // this thread's part of |khat_row|^2
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {  // khat = K - (Z A) W
@@ -515,7 +512,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     Vec16<__nv_bfloat16> kv;
-                    kv.raw = grow < p.L ? ld_global_nc_v4(krow + col + 8 * g) : make_uint4(0, 0, 0, 0);
+                    kv.raw = kpre[4 * c + g];
                     float k8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {

@@ -37,7 +37,9 @@ def _check_cache(got, ref, dtype, what):
 
 
 @pytest.mark.parametrize("dtype,B,H,L,d", [("f32", 1, 2, 200, 64), ("f32", 1, 1, 37, 16), ("bf16", 1, 2, 300, 128),
-                                           ("bf16", 2, 2, 257, 64), ("bf16", 1, 1, 1, 128)])
+                                           ("bf16", 2, 2, 257, 64), ("bf16", 1, 1, 1, 128), ("bf16", 1, 1, 128, 128),
+                                           ("bf16", 1, 2, 129, 128), ("bf16", 2, 1, 256, 128),
+                                           ("bf16", 1, 1, 1500, 128)])
 def test_prefill_kcache_vs_oracle(dtype, B, H, L, d):
     x = inputs.make_fwd(B, H, L, d, dtype, seed=51, edge_frac=0.05)
     kc = P.path_prefill_kcache(x.k.cuda(), x.w.cuda(), x.beta.cuda(), n_max=L + 5)
