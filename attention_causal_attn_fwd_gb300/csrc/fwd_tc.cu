@@ -247,9 +247,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             };
             // P V of block blk needs its P (p_ready, (blk+1)-th completion) and
             // its V slot (blk & 1, (blk >> 1)+1-th completion).
+            // Without FoX the warps that arrive on P-ready, q~-ready and S_w-ready
+            // first wait for the V, khat / W and -U copies of that block, so the
+            // MMA thread (whose every wait costs a few hundred cycles while SS
+            // MMAs hold the shared-memory port) only waits for the handoffs.
             auto wait_pv = [&](int blk) {
                 return mbar_wait(bar(B_PREADY), (uint32_t)(blk & 1), wc, 18) &&
-                       mbar_wait(bar((blk & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((blk >> 1) & 1), wc, 19);
+                       (!FOX || mbar_wait(bar((blk & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((blk >> 1) & 1), wc, 19));
             };
             bool ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL), 0, wc, 11) &&
                       mbar_wait(bar(B_WFULL0), 0, wc, 12) && mbar_wait(bar(B_UFULL), 0, wc, 12);
@@ -284,7 +288,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
                 if (m > 0) {
-                    if (!(ok = mbar_wait(bar((it & 1) ? B_WFULL1 : B_WFULL0), (uint32_t)((it >> 1) & 1), wc, 15)))
+                    if (FOX && !(ok = mbar_wait(bar((it & 1) ? B_WFULL1 : B_WFULL0), (uint32_t)((it >> 1) & 1), wc, 15)))
                         break;
                     tc_fence_after();
                     for (int kk = 0; kk < D / 16; ++kk) {
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 TC_TRACE(20, it);
                 issue_pv(it - 1);
                 TC_TRACE(2, it);
-                if (!(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
+                if (FOX && !(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
                 tc_fence_after();
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
@@ -310,7 +314,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 TC_TRACE(1, it);
                 if (m > 0) {
                     TC_TRACE(21, it);
-                    if (!(ok = mbar_wait(bar(B_UFULL), it & 1, wc, 16))) break;
+                    if (FOX && !(ok = mbar_wait(bar(B_UFULL), it & 1, wc, 16))) break;
                     TC_TRACE(22, it);
                     if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
                     TC_TRACE(23, it);
@@ -477,6 +481,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tmem_st32(tl + TM_S, *reinterpret_cast<const uint32_t(*)[32]>(pk));
             tmem_st32(tl + TM_S + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
+            if (!FOX && warp == 2) {  // V of this block has landed (the MMA thread does not check)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar((it & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((it >> 1) & 1), wc, 24));
+                if (!ok) break;
+            }
             tc_fence_before();
             mbar_arrive(bar(B_PREADY));
             if (r == 0) TC_TRACE(7, it);
@@ -520,6 +528,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto put_granule = [&](int G, uint4 v) {
             *reinterpret_cast<uint4*>(qrow_s + (G >> 3) * 16384 + (((G & 7) ^ sw) << 4)) = v;
         };
+        // Without FoX, warp 6 waits for the khat and W copies of block blk
+        // before q~-ready, and for -U before S_w-ready (see wait_pv).
+        auto loads_for_q = [&](int blk) -> bool {
+            if (FOX || warp != 6) return true;
+            return __all_sync(0xffffffffu, mbar_wait(bar(B_KFULL), blk & 1, wc, 34) &&
+                                               (n - blk == 0 || mbar_wait(bar((blk & 1) ? B_WFULL1 : B_WFULL0),
+                                                                          (uint32_t)((blk >> 1) & 1), wc, 35)));
+        };
         bool ok = n > 0 && __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), 0, wc, 30));
         if (ok) {
             // the diagonal MMA has consumed Q: load qhat (fp32) as the initial q~
@@ -549,8 +565,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tmem_wait_st();
             fence_proxy_async_smem();
+            ok = loads_for_q(1);
             tc_fence_before();
-            mbar_arrive(bar(B_QTREADY));
+            if (ok) mbar_arrive(bar(B_QTREADY));
         }
         for (int it = 1; it < n && ok; ++it) {  // block m = n - it > 0 needs the transport
             if (FOX) {  // S_w of block iteration it, unless the scan stopped before it
@@ -589,6 +606,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             tmem_wait_st();
+            if (!FOX && warp == 6 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_UFULL), it & 1, wc, 36)))) break;
             tc_fence_before();
             mbar_arrive(bar(B_SWREADY));
             if (r == 0) TC_TRACE(9, it);
@@ -614,6 +632,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
             }
             fence_proxy_async_smem();
+            if (!(ok = loads_for_q(it + 1))) break;
             tc_fence_before();
             mbar_arrive(bar(B_QTREADY));
             if (r == 0) TC_TRACE(11, it);
