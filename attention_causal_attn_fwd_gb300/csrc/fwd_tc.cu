@@ -18,11 +18,12 @@
 // raised (and O rescaled) when it grows by more than 2^8, which keeps every
 // exponent <= 2^8 and makes rescales rare.
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warp 0      TMA producer (one lane) + TMEM allocation
-//   warp 1      tcgen05.mma issuer (one lane)
+//   warp 1      tcgen05.mma issuer (one lane): S_w and MMA3 (with FoX: all MMAs)
 //   warps 2-5   softmax: S_k -> P (bf16, into TMEM), row statistics, epilogue
 //   warps 6-9   query transport: S_w -> bf16 (TMEM), fp32 q~ -> bf16 q~ (smem)
+//   warp 10     tcgen05.mma issuer (one lane): diagonal, S_k and P V (idle with FoX)
 //
 // TMEM (512 columns x 128 lanes, fp32): [0,128) S_k / P (bf16), [128,256) S_w /
 // bf16(S_w), [256,256+d) O, [384,384+d) q~ master.
@@ -50,7 +51,7 @@ namespace pathattn {
 using namespace sm100;
 
 constexpr int kTcC = 128;
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 352;
 constexpr uint32_t SM_Q = 0, SM_KW = 32768, SM_V = 98304, SM_U = 163840, SM_P = 196608, SM_BAR = 229376;
 constexpr uint32_t SM_TOTAL = SM_BAR + 256;
 constexpr size_t kTcSmem = SM_TOTAL + 1024;  // + alignment slack
@@ -63,7 +64,12 @@ constexpr uint32_t TM_S = 0, TM_SW = 128, TM_O = 256, TM_Q = 384;
 // W and V are double-buffered by block parity (slot it & 1).
 enum Bar { B_QFULL = 0, B_KFULL, B_WFULL0, B_UFULL, B_VFULL0, B_KEMPTY, B_WEMPTY0, B_UEMPTY, B_VEMPTY0, B_SFULL,
            B_SWREADY, B_PREADY, B_QUPD, B_QTREADY, B_ODONE, B_DRAIN, B_SREAD, B_VFULL1, B_VEMPTY1, B_WFULL1,
-           B_WEMPTY1, B_SWFULL, B_COUNT };
+           B_WEMPTY1, B_SWFULL, B_DRAIN2, B_COUNT };
+// Barriers at SM_BAR, then the control words (TMEM address, abort flag, FoX
+// stop index and votes, max |khat|^2) at SM_CTL, all inside SM_BAR + 256.
+constexpr uint32_t SM_CTL = SM_BAR + 192;
+static_assert(B_COUNT * 8 <= 192, "barriers overlap the control words");
+static_assert(SM_CTL + 52 <= SM_TOTAL, "control words exceed the barrier region");
 
 constexpr int kHeadGroup = 8;
 
@@ -112,13 +118,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t sb = smem_u32(sm);
     const uint32_t bar0 = sb + SM_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 128);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_BAR + 132);
+    // control words after the barriers (B_COUNT * 8 bytes)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_CTL);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_CTL + 4);
     // PaTH-FoX far-block skipping: the scan stops before block iteration
     // *stop_it (n + 1 = never); set by the softmax warps before they release S_k.
-    volatile int* stop_it = reinterpret_cast<volatile int*>(sm + SM_BAR + 136);
-    int* votes = reinterpret_cast<int*>(sm + SM_BAR + 144);     // [2][4]
-    float* s_kmax2 = reinterpret_cast<float*>(sm + SM_BAR + 176);
+    volatile int* stop_it = reinterpret_cast<volatile int*>(sm + SM_CTL + 8);
+    int* votes = reinterpret_cast<int*>(sm + SM_CTL + 16);     // [2][4]
+    float* s_kmax2 = reinterpret_cast<float*>(sm + SM_CTL + 48);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // Launch order: heads in groups of kHeadGroup; inside a group, tiles
@@ -229,13 +236,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int sl = 0; sl < 6; ++sl)
                 if (issued[sl] > 0) drain_wait(bar(ful[sl]), (uint32_t)((issued[sl] - 1) & 1), p.limit_ns);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------------ MMA issuer
-        // Per block: MMA1 (scores) and MMA3 (query transport) form the
-        // critical chain; the P V product of the previous block (MMA2, P in
-        // shared memory) is issued whenever its P is ready, before or after
-        // the next MMA1, whichever inputs arrive first.
-        if (lane == 0) {
+    } else if (warp == 1 || warp == 10) {
+        // ------------------------------------------------------------------ MMA issuers
+        // Issue is blocking (an MMA group's issue returns about when it has
+        // executed), and every barrier poll costs a few hundred cycles while SS
+        // MMAs hold the shared-memory port.  Without FoX two threads issue:
+        //   warp 1  (transport chain)  S_w(it), MMA3(it)             it = 1 .. n-1
+        //   warp 10 (softmax chain)    diagonal, P V(it-1), S_k(it)   it = 1 .. n
+        // so that one thread's waits overlap the other's MMAs.  Their TMEM
+        // columns are disjoint (S_w / q~ against S_k, P / O); the transport
+        // warps wait for S_k(it) as well as MMA3(it) before they overwrite the
+        // shared q~ tile.  With FoX (far-block stopping) warp 1 issues all of
+        // it in the order S_w(it), P V(it-1), S_k(it), MMA3(it).
+        const bool issuer_b = FOX ? warp == 1 : warp == 10;  // diagonal, P V, S_k
+        const bool issuer_a = warp == 1;                      // S_w, MMA3
+        if (lane == 0 && (issuer_a || issuer_b)) {
             auto issue_pv = [&](int blk) {  // O (+)= P V for block iteration blk (P in TMEM)
                 tc_fence_after();
                 const uint32_t vbuf = sb + SM_V + (uint32_t)(blk & 1) * 32768u;
@@ -246,65 +261,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mma_commit(bar((blk & 1) ? B_VEMPTY1 : B_VEMPTY0));
             };
             // P V of block blk needs its P (p_ready, (blk+1)-th completion) and
-            // its V slot (blk & 1, (blk >> 1)+1-th completion).
-            // Without FoX the warps that arrive on P-ready, q~-ready and S_w-ready
-            // first wait for the V, khat / W and -U copies of that block, so the
-            // MMA thread (whose every wait costs a few hundred cycles while SS
-            // MMAs hold the shared-memory port) only waits for the handoffs.
+            // its V slot (blk & 1, (blk >> 1)+1-th completion).  Without FoX the
+            // warps that arrive on P-ready, q~-ready and S_w-ready first wait for
+            // the V, khat / W and -U copies of that block, so the issuers only
+            // wait for the handoffs.
             auto wait_pv = [&](int blk) {
                 return mbar_wait(bar(B_PREADY), (uint32_t)(blk & 1), wc, 18) &&
                        (!FOX || mbar_wait(bar((blk & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((blk >> 1) & 1), wc, 19));
             };
-            bool ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL), 0, wc, 11) &&
-                      mbar_wait(bar(B_WFULL0), 0, wc, 12) && mbar_wait(bar(B_UFULL), 0, wc, 12);
-            if (ok) {
+            auto issue_sw = [&](int it) {  // S_w = q~ W^T (W slot it & 1)
                 tc_fence_after();
-                // diagonal: S = Q K^T + Y (-Z)^T
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
-                           IDESC_S128, kk > 0);
-                for (int kk = 0; kk < kTcC / 16; ++kk)
-                    mma_ss(tmem + TM_S, kmajor_desc(sb + SM_U, kk, 16384),
-                           kmajor_desc(sb + SM_KW + 16384, kk, 32768), IDESC_S128, 1);
-                mma_commit(bar(B_SFULL));
-                mma_commit(bar(B_KEMPTY));
-                mma_commit(bar(B_WEMPTY0));
-                mma_commit(bar(B_UEMPTY));
-            }
-            // Issue is blocking (an MMA group's issue returns about when it has
-            // executed), so the issue order is the tensor pipe's schedule:
-            //   S_w(it) -> P V(it-1) -> S_k(it) -> MMA3(it)
-            // P V and S_k cover the conversion of S_w; S_k follows P V because it
-            // overwrites the TMEM columns that hold P.
-            int last = n;  // last block iteration whose P V is issued
-            for (int it = 1; it <= n && ok; ++it) {
-                const int m = n - it;
-                if (FOX) {  // the softmax warps decide first whether block it is visited
-                    if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
-                    if (*stop_it <= it) {  // every block from here on contributes exactly zero
-                        last = it - 1;
-                        break;
-                    }
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t bdesc = (it & 1) ? kmajor_desc(sb + SM_P, kk, 16384)
+                                                    : kmajor_desc(sb + SM_KW + 16384, kk, 32768);
+                    mma_ss(tmem + TM_SW, kmajor_desc(sb + SM_Q, kk, 16384), bdesc, IDESC_S128, kk > 0);
                 }
-                if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
-                if (m > 0) {
-                    if (FOX && !(ok = mbar_wait(bar((it & 1) ? B_WFULL1 : B_WFULL0), (uint32_t)((it >> 1) & 1), wc, 15)))
-                        break;
-                    tc_fence_after();
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t bdesc = (it & 1) ? kmajor_desc(sb + SM_P, kk, 16384)
-                                                        : kmajor_desc(sb + SM_KW + 16384, kk, 32768);
-                        mma_ss(tmem + TM_SW, kmajor_desc(sb + SM_Q, kk, 16384), bdesc, IDESC_S128, kk > 0);
-                    }
-                    mma_commit(bar(B_SWFULL));
-                    mma_commit(bar((it & 1) ? B_WEMPTY1 : B_WEMPTY0));
-                    TC_TRACE(0, it);
-                }
-                if (!(ok = wait_pv(it - 1))) break;
-                TC_TRACE(20, it);
-                issue_pv(it - 1);
-                TC_TRACE(2, it);
-                if (FOX && !(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
+                mma_commit(bar(B_SWFULL));
+                mma_commit(bar((it & 1) ? B_WEMPTY1 : B_WEMPTY0));
+                TC_TRACE(0, it);
+            };
+            auto issue_sk = [&](int it) {  // S_k = q~ khat^T
                 tc_fence_after();
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
@@ -312,24 +288,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 mma_commit(bar(B_SFULL));
                 mma_commit(bar(B_KEMPTY));
                 TC_TRACE(1, it);
-                if (m > 0) {
-                    TC_TRACE(21, it);
-                    if (FOX && !(ok = mbar_wait(bar(B_UFULL), it & 1, wc, 16))) break;
-                    TC_TRACE(22, it);
-                    if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
-                    TC_TRACE(23, it);
+            };
+            auto issue_m3 = [&](int it) {  // q~ += bf16(S_w) (-U)
+                tc_fence_after();
+                for (int kk = 0; kk < kTcC / 16; ++kk)
+                    mma_ts(tmem + TM_Q, tmem + TM_SW + kk * 8, mnmajor_desc(sb + SM_U, kk), IDESC_PV, 1);
+                mma_commit(bar(B_QUPD));
+                mma_commit(bar(B_UEMPTY));
+                TC_TRACE(3, it);
+            };
+            bool ok = true;
+            if (issuer_b) {
+                ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL), 0, wc, 11) &&
+                     mbar_wait(bar(B_WFULL0), 0, wc, 12) && mbar_wait(bar(B_UFULL), 0, wc, 12);
+                if (ok) {
                     tc_fence_after();
+                    // diagonal: S = Q K^T + Y (-Z)^T
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
+                               IDESC_S128, kk > 0);
                     for (int kk = 0; kk < kTcC / 16; ++kk)
-                        mma_ts(tmem + TM_Q, tmem + TM_SW + kk * 8, mnmajor_desc(sb + SM_U, kk), IDESC_PV, 1);
-                    mma_commit(bar(B_QUPD));
+                        mma_ss(tmem + TM_S, kmajor_desc(sb + SM_U, kk, 16384),
+                               kmajor_desc(sb + SM_KW + 16384, kk, 32768), IDESC_S128, 1);
+                    mma_commit(bar(B_SFULL));
+                    mma_commit(bar(B_KEMPTY));
+                    mma_commit(bar(B_WEMPTY0));
                     mma_commit(bar(B_UEMPTY));
-                    TC_TRACE(3, it);
                 }
             }
-            if (ok && wait_pv(last)) issue_pv(last);  // the last block's P V
-            // every issued MMA completes before TMEM is released
-            mma_commit(bar(B_DRAIN));
-            drain_wait(bar(B_DRAIN), 0, p.limit_ns);
+            if (FOX) {
+                // single issuer: S_w(it) -> P V(it-1) -> S_k(it) -> MMA3(it); P V and S_k
+                // cover the conversion of S_w, and S_k follows P V because it
+                // overwrites the TMEM columns that hold P.
+                int last = n;  // last block iteration whose P V is issued
+                for (int it = 1; it <= n && ok; ++it) {
+                    const int m = n - it;
+                    // the softmax warps decide first whether block it is visited
+                    if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
+                    if (*stop_it <= it) {  // every block from here on contributes exactly zero
+                        last = it - 1;
+                        break;
+                    }
+                    if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
+                    if (m > 0) {
+                        if (!(ok = mbar_wait(bar((it & 1) ? B_WFULL1 : B_WFULL0), (uint32_t)((it >> 1) & 1), wc, 15)))
+                            break;
+                        issue_sw(it);
+                    }
+                    if (!(ok = wait_pv(it - 1))) break;
+                    issue_pv(it - 1);
+                    TC_TRACE(2, it);
+                    if (!(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
+                    issue_sk(it);
+                    if (m > 0) {
+                        if (!(ok = mbar_wait(bar(B_UFULL), it & 1, wc, 16))) break;
+                        if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
+                        issue_m3(it);
+                    }
+                }
+                if (ok && wait_pv(last)) issue_pv(last);  // the last block's P V
+            } else if (issuer_b) {
+                for (int it = 1; it <= n && ok; ++it) {
+                    if (!(ok = wait_pv(it - 1))) break;
+                    TC_TRACE(20, it);
+                    issue_pv(it - 1);
+                    TC_TRACE(2, it);
+                    if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14) &&
+                               mbar_wait(bar(B_KFULL), it & 1, wc, 15)))
+                        break;
+                    issue_sk(it);
+                }
+                if (ok && wait_pv(n)) issue_pv(n);  // the last block's P V
+            } else {
+                for (int it = 1; it < n && ok; ++it) {
+                    if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
+                    issue_sw(it);
+                    if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
+                    TC_TRACE(23, it);
+                    issue_m3(it);
+                }
+            }
+            // every MMA this thread issued completes before TMEM is released
+            const int drain = (FOX || issuer_a) ? B_DRAIN : B_DRAIN2;
+            mma_commit(bar(drain));
+            drain_wait(bar(drain), 0, p.limit_ns);
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------------ softmax warps
@@ -528,13 +570,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         auto put_granule = [&](int G, uint4 v) {
             *reinterpret_cast<uint4*>(qrow_s + (G >> 3) * 16384 + (((G & 7) ^ sw) << 4)) = v;
         };
-        // Without FoX, warp 6 waits for the khat and W copies of block blk
-        // before q~-ready, and for -U before S_w-ready (see wait_pv).
+        // Without FoX, warp 6 waits for the W copy of block blk before q~-ready
+        // (S_w is the first MMA that reads q~), and for -U before S_w-ready.
         auto loads_for_q = [&](int blk) -> bool {
-            if (FOX || warp != 6) return true;
-            return __all_sync(0xffffffffu, mbar_wait(bar(B_KFULL), blk & 1, wc, 34) &&
-                                               (n - blk == 0 || mbar_wait(bar((blk & 1) ? B_WFULL1 : B_WFULL0),
-                                                                          (uint32_t)((blk >> 1) & 1), wc, 35)));
+            if (FOX || warp != 6 || n - blk == 0) return true;
+            return __all_sync(0xffffffffu, mbar_wait(bar((blk & 1) ? B_WFULL1 : B_WFULL0),
+                                                     (uint32_t)((blk >> 1) & 1), wc, 35));
         };
         bool ok = n > 0 && __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), 0, wc, 30));
         if (ok) {
@@ -611,6 +652,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive(bar(B_SWREADY));
             if (r == 0) TC_TRACE(9, it);
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QUPD), (it - 1) & 1, wc, 32));
+            // with two issuers S_k(it), which also reads the q~ tile, completes on its own
+            if (!FOX && ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 37));
             if (!ok) break;
             if (r == 0) TC_TRACE(10, it);
             tc_fence_after();
@@ -635,7 +678,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!(ok = loads_for_q(it + 1))) break;
             tc_fence_before();
             mbar_arrive(bar(B_QTREADY));
-            if (r == 0) TC_TRACE(11, it);
+            if (r == 64) TC_TRACE(11, it);
         }
     }
 

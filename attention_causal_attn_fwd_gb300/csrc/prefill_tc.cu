@@ -47,6 +47,7 @@ enum {
     B_VFULL = 0, B_WFULL, B_KFULL, B_VEMPTY, B_WEMPTY, B_KEMPTY,
     B_T, B_N, B_KOUT, B_TREADY, B_NREADY, B_KREAD, B_DRAIN, B_COUNT
 };
+static_assert(B_COUNT * 8 <= 128, "barriers overlap the TMEM slot and abort flag at +128");
 }  // namespace pfk
 
 struct PfParams {

@@ -56,6 +56,7 @@ constexpr uint32_t TOTAL = RT + 64 * LDT * 4;
 constexpr size_t kSmem = TOTAL + 1024;
 constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN, B_COUNT };
+static_assert(B_COUNT * 8 <= 128, "barriers overlap the TMEM slot and abort flag at +128");
 }  // namespace utk
 
 struct UtParams {
