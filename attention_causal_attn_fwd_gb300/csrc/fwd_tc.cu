@@ -353,10 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     TC_TRACE(20, it);
                     issue_pv(it - 1);
                     TC_TRACE(2, it);
-                    if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14) &&
-                               mbar_wait(bar(B_KFULL), it & 1, wc, 15)))
-                        break;
-                    issue_sk(it);
+                    issue_sk(it);  // its khat and q~ were awaited before P-ready (softmax warps 3, 4)
                 }
                 if (ok && wait_pv(n)) issue_pv(n);  // the last block's P V
             } else {
@@ -523,13 +520,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tmem_st32(tl + TM_S, *reinterpret_cast<const uint32_t(*)[32]>(pk));
             tmem_st32(tl + TM_S + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
-            if (!FOX && warp == 2) {  // V of this block has landed (the MMA thread does not check)
+            // Without FoX, P-ready also stands for the inputs of the issuer's next two
+            // MMAs: warp 2 waits for this block's V (P V), warp 3 for the next
+            // block's khat and warp 4 for the next q~ (S_k of block it + 1), each in
+            // parallel, so the issuer polls P-ready alone.
+            if (!FOX && warp == 2) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar((it & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((it >> 1) & 1), wc, 24));
+                if (!ok) break;
+            }
+            if (!FOX && warp == 3 && it < n) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KFULL), (it + 1) & 1, wc, 25));
+                if (!ok) break;
+            }
+            if (!FOX && warp == 4 && it < n) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QTREADY), it & 1, wc, 26));
                 if (!ok) break;
             }
             tc_fence_before();
             mbar_arrive(bar(B_PREADY));
             if (r == 0) TC_TRACE(7, it);
+            if (lane == 0) TC_TRACE(14 + warp, it);  // 16..19: P-ready arrival of warps 2..5
             if (stop) {
                 last = it;
                 break;
@@ -650,6 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!FOX && warp == 6 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_UFULL), it & 1, wc, 36)))) break;
             tc_fence_before();
             mbar_arrive(bar(B_SWREADY));
+            if (lane == 0) TC_TRACE(22 + warp, it);  // 28..31: S_w-ready arrival of warps 6..9
             if (r == 0) TC_TRACE(9, it);
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QUPD), (it - 1) & 1, wc, 32));
             // with two issuers S_k(it), which also reads the q~ tile, completes on its own
@@ -679,6 +690,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(B_QTREADY));
             if (r == 64) TC_TRACE(11, it);
+            if (lane == 0) TC_TRACE(18 + warp, it);  // 24..27: q~-ready arrival of warps 6..9
         }
     }
 
