@@ -47,17 +47,28 @@ constexpr int kCompute = 256;   // warps 2-9: two warps per TMEM lane quarter
 constexpr uint32_t R0 = 0;        // W            (K-major / MN-major source)
 constexpr uint32_t R1 = 32768;    // Q, then solve temp, then A_hi
 constexpr uint32_t R2 = 65536;    // K, then A_lo
-constexpr uint32_t R3 = 98304;    // G fp32 [128][129] for the solve, then hi/lo operand (hi, hi + 32 KB = lo)
-constexpr int LDG = 129;
+constexpr uint32_t R3 = 98304;    // G fp32 [128][132] for the solve, then hi/lo operand (hi, hi + 32 KB = lo)
+constexpr int LDG = 132;          // rows start on 16-byte boundaries
 constexpr uint32_t RB = R3 + 128 * LDG * 4;  // barriers, beta
 constexpr uint32_t RT = RB + 1024;            // solve temp T [64][68] fp32
 constexpr int LDT = 68;
-constexpr uint32_t TOTAL = RT + 64 * LDT * 4;
+constexpr uint32_t RS = RT + 64 * LDT * 4;    // output staging tile for TMA stores (32 KB)
+static_assert(RS % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte boundaries");
+constexpr uint32_t TOTAL = RS + 32768;
 constexpr size_t kSmem = TOTAL + 1024;
 constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN, B_COUNT };
 static_assert(B_COUNT * 8 <= 128, "barriers overlap the TMEM slot and abort flag at +128");
 }  // namespace utk
+
+// Phase timestamps of one CTA in the middle of the grid (SM cycle counter),
+// compiled in only for instrumented builds (-DPATH_TRACE).
+#ifdef PATH_TRACE
+#define UT_TRACE(slot) \
+    do { if (p.trace && blockIdx.x == 10 && blockIdx.y == 40) p.trace[(slot)] = clock64(); } while (0)
+#else
+#define UT_TRACE(slot) do { } while (0)
+#endif
 
 struct UtParams {
     int L, Lp;
@@ -74,11 +85,21 @@ struct UtParams {
     int nch;
     WsHeader* hdr;
     unsigned long long limit_ns;
+#ifdef PATH_TRACE
+    unsigned long long* trace;
+#endif
 };
 
 __device__ __forceinline__ uint4 pack8(const float* v) {
     return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                       pack_bf16x2(v[6], v[7]));
+}
+// 16 bytes of row r into a staging tile laid out as a TMA store box sequence:
+// 128-byte rows, 128 rows per 16 KB box, 128-byte swizzle; `box` selects the
+// box and `g` the 16-byte granule of the row.
+__device__ __forceinline__ void stage16(uint8_t* base, int r, int box, int g, uint4 v) {
+    *reinterpret_cast<uint4*>(base + (uint32_t)box * 16384u + (uint32_t)r * 128u +
+                              ((uint32_t)((g & 7) ^ (r & 7)) << 4)) = v;
 }
 
 // One doubling merge of the blocked inverse, for 256 threads t: for each pair
@@ -86,13 +107,27 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
 //     T    = (D G)_PQ X_QQ
 //     X_PQ = -X_PP T
 // with X dense (zeros below the diagonal, ones on it), so the products are
-// plain register-tiled loops.
+// plain register-tiled loops.  The k loop takes 4 steps at a time so that
+// every operand is read as 16- or 8-byte row segments (rows of G, X and T
+// start on 16-byte boundaries): 2 x (TM + 4) vector loads per 4 x TM x TN FMAs.
+template <int TN>
+__device__ __forceinline__ void ld_row(float (&dst)[TN], const float* src) {
+    static_assert(TN == 2 || TN == 4, "row segment");
+    if constexpr (TN == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+    } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        dst[0] = v.x; dst[1] = v.y;
+    }
+}
 template <int S, int TM, int TN>
 __device__ __forceinline__ void merge_level(const float* sG, const float* sB, float* sX, float* sT, int t) {
     using namespace utk;
     constexpr int NP = C / (2 * S);
     constexpr int TR = S / TM, TC = S / TN;
     static_assert(NP * TR * TC == kCompute, "one tile per thread");
+    static_assert(S % 4 == 0 && LDG % 4 == 0 && LDT % 4 == 0 && C % 4 == 0, "16-byte row segments");
     const int p = t / (TR * TC), rem = t % (TR * TC);
     const int i0 = (rem / TC) * TM, j0 = (rem % TC) * TN;
     const int P = 2 * p * S, Q = P + S;
@@ -101,17 +136,19 @@ __device__ __forceinline__ void merge_level(const float* sG, const float* sB, fl
     for (int u = 0; u < TM; ++u)
 #pragma unroll
         for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
-#pragma unroll 4
-    for (int kk = 0; kk < S; ++kk) {
-        float g[TM], x[TN];
+#pragma unroll 2
+    for (int k4 = 0; k4 < S; k4 += 4) {
+        float g[TM][4], x[4][TN];
 #pragma unroll
-        for (int u = 0; u < TM; ++u) g[u] = sG[(P + i0 + u) * LDG + Q + kk];
+        for (int u = 0; u < TM; ++u) ld_row<4>(g[u], sG + (P + i0 + u) * LDG + Q + k4);
 #pragma unroll
-        for (int v = 0; v < TN; ++v) x[v] = sX[(Q + kk) * C + Q + j0 + v];
+        for (int e = 0; e < 4; ++e) ld_row<TN>(x[e], sX + (Q + k4 + e) * C + Q + j0);
 #pragma unroll
-        for (int u = 0; u < TM; ++u)
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-            for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(g[u], x[v], acc[u][v]);
+            for (int u = 0; u < TM; ++u)
+#pragma unroll
+                for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(g[u][e], x[e][v], acc[u][v]);
     }
 #pragma unroll
     for (int u = 0; u < TM; ++u)
@@ -122,17 +159,19 @@ __device__ __forceinline__ void merge_level(const float* sG, const float* sB, fl
     for (int u = 0; u < TM; ++u)
 #pragma unroll
         for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
-#pragma unroll 4
-    for (int kk = 0; kk < S; ++kk) {
-        float xp[TM], tv[TN];
+#pragma unroll 2
+    for (int k4 = 0; k4 < S; k4 += 4) {
+        float xp[TM][4], tv[4][TN];
 #pragma unroll
-        for (int u = 0; u < TM; ++u) xp[u] = sX[(P + i0 + u) * C + P + kk];
+        for (int u = 0; u < TM; ++u) ld_row<4>(xp[u], sX + (P + i0 + u) * C + P + k4);
 #pragma unroll
-        for (int v = 0; v < TN; ++v) tv[v] = sT[(p * S + kk) * LDT + j0 + v];
+        for (int e = 0; e < 4; ++e) ld_row<TN>(tv[e], sT + (p * S + k4 + e) * LDT + j0);
 #pragma unroll
-        for (int u = 0; u < TM; ++u)
+        for (int e = 0; e < 4; ++e)
 #pragma unroll
-            for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(xp[u], tv[v], acc[u][v]);
+            for (int u = 0; u < TM; ++u)
+#pragma unroll
+                for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(xp[u][e], tv[e][v], acc[u][v]);
     }
 #pragma unroll
     for (int u = 0; u < TM; ++u)
@@ -141,9 +180,11 @@ __device__ __forceinline__ void merge_level(const float* sG, const float* sB, fl
     named_bar_sync(1, kCompute);
 }
 
-// X = (I + D triu_1(G))^{-1} (unit upper triangular) into the dense, zeroed
-// sX [128][128], for 256 threads t; sG holds G (upper part read).
-__device__ __forceinline__ void solve_unit_upper(const float* sG, const float* sB, float* sX, float* sT, int t) {
+// The 16 x 16 diagonal blocks of X = (I + D triu_1(G))^{-1} (unit upper
+// triangular) by back substitution into the dense, zeroed sX [128][128], for
+// 256 threads t (the merges above then fill the rest); sG holds G (upper
+// part read).
+__device__ __forceinline__ void solve_diag_blocks(const float* sG, const float* sB, float* sX, int t) {
     using namespace utk;
     if (t < 128) {  // 16 x 16 diagonal blocks: thread (block I, column j) back-substitutes its column
         const int I = t >> 4, j = t & 15, b0 = I * 16;
@@ -163,15 +204,15 @@ __device__ __forceinline__ void solve_unit_upper(const float* sG, const float* s
             if (i <= j) sX[(b0 + i) * C + b0 + j] = x[i];
     }
     named_bar_sync(1, kCompute);
-    merge_level<16, 2, 2>(sG, sB, sX, sT, t);
-    merge_level<32, 2, 4>(sG, sB, sX, sT, t);
-    merge_level<64, 4, 4>(sG, sB, sX, sT, t);
 }
 
 template <int D>
 __global__ void __launch_bounds__(utk::kThreads, 1)
     ut_prep_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_w, const UtParams p) {
+               const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_un,
+               const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_zn,
+               const __grid_constant__ CUtensorMap tm_khat, const __grid_constant__ CUtensorMap tm_qhat,
+               const UtParams p) {
     using namespace utk;
     static_assert(D == 64 || D == 128, "head dim");
     constexpr int KCH = D / 64;
@@ -223,6 +264,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = mbar_wait(bar(B_LOAD), 0, wc, 40);
+            UT_TRACE(13);
             if (ok) {
                 tc_fence_after();
                 for (int kk = 0; kk < D / 16; ++kk) {  // G = W W^T, Q W^T, K W^T
@@ -232,7 +274,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     mma_ss(tmem + T256, kmajor_desc(sb + R2, kk, 16384), bw, ID_KK128, kk > 0);
                 }
                 mma_commit(bar(B_G));
+                UT_TRACE(14);
                 ok = mbar_wait(bar(B_OPS1), 0, wc, 41);
+                UT_TRACE(15);
             }
             if (ok) {
                 tc_fence_after();
@@ -256,7 +300,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                         mma_ss(tmem + T128, kmajor_desc(sb + R2, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
                 }
                 mma_commit(bar(B_UY));
+                UT_TRACE(16);
                 ok = mbar_wait(bar(B_OPS2), 0, wc, 42);
+                UT_TRACE(17);
             }
             if (ok) {
                 tc_fence_after();
@@ -266,7 +312,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 for (int kk = 0; kk < C / 16; ++kk)
                     mma_ss(tmem + T384, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
                 mma_commit(bar(B_Q));
+                UT_TRACE(18);
                 ok = mbar_wait(bar(B_OPS3), 0, wc, 43);
+                UT_TRACE(19);
             }
             if (ok) {
                 tc_fence_after();
@@ -279,7 +327,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     mma_ss(tmem + T0, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R1, kk),
                            ID_KMN_128, 1);
                 mma_commit(bar(B_ZA));
+                UT_TRACE(20);
                 ok = mbar_wait(bar(B_OPS4), 0, wc, 44);
+                UT_TRACE(21);
             }
             if (ok) {
                 tc_fence_after();
@@ -289,6 +339,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 for (int kk = 0; kk < C / 16; ++kk)
                     mma_ss(tmem + T128, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
                 mma_commit(bar(B_K));
+                UT_TRACE(22);
             }
             mma_commit(bar(B_DRAIN));
             drain_wait(bar(B_DRAIN), 0, p.limit_ns);
@@ -309,7 +360,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         if (h == 0) sBeta[r] = grow < p.L ? p.beta[(size_t)bh * p.L + grow] : 0.f;
         // All compute warps wait on the same barriers, so they agree on `ok`
         // and reach the named barriers below together.
+        if (t == 0) UT_TRACE(0);
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_G), 0, wc, 50));
+        if (t == 0) UT_TRACE(1);
         if (ok) {
             tc_fence_after();
 #pragma unroll
@@ -318,14 +371,25 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 tmem_ld32(tl + T0 + 64 * h + 32 * c, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sG[r * LDG + 64 * h + 32 * c + j] = __uint_as_float(v[j]);
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(sG + r * LDG + 64 * h + 32 * c + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                    __uint_as_float(v[j + 3]));
             }
             {  // Q and K are consumed: zero the dense X
                 float4* x4 = reinterpret_cast<float4*>(sX);
                 for (int i = t; i < C * C / 4; i += kCompute) x4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             named_bar_sync(1, kCompute);
-            solve_unit_upper(sG, sBeta, sX, sT, t);
+            if (t == 0) UT_TRACE(2);
+            solve_diag_blocks(sG, sBeta, sX, t);
+            if (t == 0) UT_TRACE(23);
+            merge_level<16, 2, 2>(sG, sBeta, sX, sT, t);
+            if (t == 0) UT_TRACE(24);
+            merge_level<32, 2, 4>(sG, sBeta, sX, sT, t);
+            if (t == 0) UT_TRACE(25);
+            merge_level<64, 4, 4>(sG, sBeta, sX, sT, t);
+            if (t == 0) UT_TRACE(3);
             // A = X D as hi/lo bf16 tiles.  The tiles overwrite the dense X, so
             // each thread first reads its 8 granules (8 consecutive columns of
             // one row; consecutive threads walk along a row, free of bank
@@ -367,12 +431,14 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_OPS1));
+            if (t == 0) UT_TRACE(4);
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_UY), 0, wc, 51));
+            if (t == 0) UT_TRACE(5);
         }
         if (ok) {
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // -U row -> global
+            for (int c = 0; c < D / 64; ++c) {  // -U row -> staging tile (bf16)
                 uint32_t v[32];
                 const int col = (D / 2) * h + 32 * c;
                 tmem_ld32(tl + T384 + col, v);
@@ -382,7 +448,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     float u8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) u8[e] = -__uint_as_float(v[8 * g + e]);
-                    st_global_v4(p.un + ws_row * D + col + 8 * g, pack8(u8));
+                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(u8));
                 }
             }
             if (p.vfac) {
@@ -402,7 +468,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 }
             }
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {  // Y row -> global (bf16) and hi/lo operand
+            for (int c = 0; c < 2; ++c) {  // Y row -> hi/lo operand; its hi part is the bf16 Y output
                 uint32_t v[32];
                 const int col = 64 * h + 32 * c;
                 tmem_ld32(tl + T0 + col, v);
@@ -412,13 +478,19 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     float y8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) y8[e] = __uint_as_float(v[8 * g + e]);
-                    st_global_v4(p.y + ws_row * C + col + 8 * g, pack8(y8));
                     put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, y8);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_OPS2));
+            if (t == 0) UT_TRACE(6);
+            named_bar_sync(1, kCompute);
+            if (t == 0) {  // -U and Y tiles -> workspace
+                for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_un, sb + RS + b * 16384, 64 * b, row0, bh);
+                for (int b = 0; b < 2; ++b) tma_store_3d(&tm_y, sb + R3 + b * 16384, 64 * b, row0, bh);
+                bulk_commit();
+            }
         }
         // This thread's half of the Q row, loaded while Y W runs on the tensor cores.
         uint4 qpre[D / 16];
@@ -429,10 +501,39 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 qpre[i] = (ok && grow < p.L) ? ld_global_nc_v4(qrow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 52));
+        if (t == 0) UT_TRACE(7);
         if (ok) {
             tc_fence_after();
+            // the -U and Y stores have read their tiles before R3 and RS are rewritten
+            if (t == 0) bulk_wait_read0();
+            named_bar_sync(1, kCompute);
+            // Z = triu_1(K W^T) -> hi/lo operand, negated: its hi part is the bf16 -Z
+            // output, Z A comes out as -(Z A) and (Z A) W as -(Z A) W
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // qhat = Q - Y W  (fp32)
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                const int col = 64 * h + 32 * c;
+                tmem_ld32(tl + T256 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float nz8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int b = col + 8 * g + e;
+                        nz8[e] = b > r ? -__uint_as_float(v[8 * g + e]) : 0.f;
+                    }
+                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, nz8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_OPS3));
+            if (t == 0) UT_TRACE(8);
+            // qhat = Q - Y W (fp32) through the staging tile, 32 columns of each
+            // half per round, while Z A runs
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t v[32];
                 const int col = (D / 2) * h + 32 * c;
                 tmem_ld32(tl + T384 + col, v);
@@ -441,41 +542,33 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 for (int g = 0; g < 4; ++g) {
                     Vec16<__nv_bfloat16> qv;
                     qv.raw = qpre[4 * c + g];
-                    float4* dst = reinterpret_cast<float4*>(p.qhat + ws_row * D + col + 8 * g);
-                    dst[0] = make_float4(qv.get(0) - __uint_as_float(v[8 * g + 0]), qv.get(1) - __uint_as_float(v[8 * g + 1]),
-                                         qv.get(2) - __uint_as_float(v[8 * g + 2]), qv.get(3) - __uint_as_float(v[8 * g + 3]));
-                    dst[1] = make_float4(qv.get(4) - __uint_as_float(v[8 * g + 4]), qv.get(5) - __uint_as_float(v[8 * g + 5]),
-                                         qv.get(6) - __uint_as_float(v[8 * g + 6]), qv.get(7) - __uint_as_float(v[8 * g + 7]));
+                    float q8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) q8[e] = qv.get(e) - __uint_as_float(v[8 * g + e]);
+                    stage16(sm + RS, r, h, 2 * g, make_uint4(__float_as_uint(q8[0]), __float_as_uint(q8[1]),
+                                                             __float_as_uint(q8[2]), __float_as_uint(q8[3])));
+                    stage16(sm + RS, r, h, 2 * g + 1, make_uint4(__float_as_uint(q8[4]), __float_as_uint(q8[5]),
+                                                                 __float_as_uint(q8[6]), __float_as_uint(q8[7])));
                 }
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {  // Z = triu_1(K W^T): -Z -> global, Z -> hi/lo operand
-                uint32_t v[32];
-                const int col = 64 * h + 32 * c;
-                tmem_ld32(tl + T256 + col, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float z8[8], nz8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int b = col + 8 * g + e;
-                        z8[e] = b > r ? __uint_as_float(v[8 * g + e]) : 0.f;
-                        nz8[e] = -z8[e];
-                    }
-                    st_global_v4(p.zn + ws_row * C + col + 8 * g, pack8(nz8));
-                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, z8);
+                fence_proxy_async_smem();
+                named_bar_sync(1, kCompute);
+                if (t == 0) {
+                    for (int b = 0; b < 2; ++b) tma_store_3d(&tm_qhat, sb + RS + b * 16384, (D / 2) * b + 32 * c, row0, bh);
+                    if (c == 0) for (int b = 0; b < 2; ++b) tma_store_3d(&tm_zn, sb + R3 + b * 16384, 64 * b, row0, bh);
+                    bulk_commit();
+                    if (c + 1 < D / 64) bulk_wait_read0();
                 }
+                if (c + 1 < D / 64) named_bar_sync(1, kCompute);
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(B_OPS3));
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ZA), 0, wc, 53));
+            if (t == 0) UT_TRACE(9);
         }
         if (ok) {
             tc_fence_after();
+            if (t == 0) bulk_wait_read0();  // the -Z and qhat stores have read R3 and RS
+            named_bar_sync(1, kCompute);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {  // Z A -> hi/lo operand
+            for (int c = 0; c < 2; ++c) {  // -(Z A) -> hi/lo operand
                 uint32_t v[32];
                 const int col = 64 * h + 32 * c;
                 tmem_ld32(tl + T0 + col, v);
@@ -491,6 +584,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_OPS4));
+            if (t == 0) UT_TRACE(10);
         }
         // This thread's half of the K row, loaded while (Z A) W runs.
         uint4 kpre[D / 16];
@@ -501,11 +595,12 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 kpre[i] = (ok && grow < p.L) ? ld_global_nc_v4(krow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_K), 0, wc, 54));
+        if (t == 0) UT_TRACE(11);
         if (ok) {
             tc_fence_after();
             float n2 = 0.f;  // this thread's part of |khat_row|^2
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // khat = K - (Z A) W
+            for (int c = 0; c < D / 64; ++c) {  // khat = K - (Z A) W; TMEM holds -(Z A) W
                 uint32_t v[32];
                 const int col = (D / 2) * h + 32 * c;
                 tmem_ld32(tl + T128 + col, v);
@@ -517,11 +612,17 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     float k8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        k8[e] = kv.get(e) - __uint_as_float(v[8 * g + e]);
+                        k8[e] = kv.get(e) + __uint_as_float(v[8 * g + e]);
                         n2 = fmaf(k8[e], k8[e], n2);
                     }
-                    st_global_v4(p.khat + ws_row * D + col + 8 * g, pack8(k8));
+                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(k8));
                 }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, kCompute);
+            if (t == 0) {
+                for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_khat, sb + RS + b * 16384, 64 * b, row0, bh);
+                bulk_commit();
             }
             if (p.kmax2) {  // chunk max of |khat|^2 over rows < L (the solve temp is free)
                 float* red = reinterpret_cast<float*>(sm + RT);
@@ -539,6 +640,10 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         }
     }
 
+    if (threadIdx.x == 64) {
+        bulk_wait0();  // the workspace stores have landed (and read their tiles) before exit
+        UT_TRACE(12);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -547,11 +652,29 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     }
 }
 
+#ifdef PATH_TRACE
+static unsigned long long* ut_trace_buffer() {
+    static unsigned long long* buf = nullptr;
+    if (!buf && cudaMalloc(&buf, 64 * sizeof(unsigned long long)) == cudaSuccess)
+        cudaMemset(buf, 0, 64 * sizeof(unsigned long long));
+    return buf;
+}
+}  // namespace pathattn
+extern "C" void path_ut_trace_dump(unsigned long long* host) {
+    cudaDeviceSynchronize();
+    cudaMemcpy(host, pathattn::ut_trace_buffer(), 64 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+}
+namespace pathattn {
+#endif
+
 template <int D>
 static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, const float* beta, int BH, int L,
                                   unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st) {
-    CUtensorMap mq, mk, mw;
-    if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mw, w, D, L, BH))
+    CUtensorMap mq, mk, mw, mun, my, mzn, mkh, mqh;
+    if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mw, w, D, L, BH) ||
+        !make_map(&mun, ws + lay.un, D, lay.Lp, BH) || !make_map(&my, ws + lay.y, utk::C, lay.Lp, BH) ||
+        !make_map(&mzn, ws + lay.zn, utk::C, lay.Lp, BH) || !make_map(&mkh, ws + lay.khat, D, lay.Lp, BH) ||
+        !make_map_t(&mqh, ws + lay.qhat, D, lay.Lp, BH, true))
         return cudaErrorInvalidValue;
     UtParams p;
     p.L = L;
@@ -569,10 +692,13 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
     p.nch = lay.Lp / utk::C;
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.limit_ns = 2000000000ull;
+#ifdef PATH_TRACE
+    p.trace = ut_trace_buffer();
+#endif
     auto kern = ut_prep_tc<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)utk::kSmem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(cdiv(L, utk::C), BH), utk::kThreads, utk::kSmem, st>>>(mq, mk, mw, p);
+    kern<<<dim3(cdiv(L, utk::C), BH), utk::kThreads, utk::kSmem, st>>>(mq, mk, mw, mun, my, mzn, mkh, mqh, p);
     return cudaGetLastError();
 }
 
