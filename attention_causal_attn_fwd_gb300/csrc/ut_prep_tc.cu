@@ -180,6 +180,83 @@ __device__ __forceinline__ void merge_level(const float* sG, const float* sB, fl
     named_bar_sync(1, kCompute);
 }
 
+// The same merge without the zero halves of the triangular factors:
+// T = (D G)_PQ X_QQ needs only k <= j and X_PQ = -X_PP T only k >= i (both X
+// blocks are upper triangular).  Pass 1 gives each warp WC adjacent column
+// tiles and pass 2 WR adjacent row tiles, so a warp's k range is uniform; the
+// two warps that share a scheduler (compute warps cw and cw + 4) get
+// complementary ranges.  G is symmetric, so the G column needed for row
+// segment i0.. is read as 16- or 8-byte segments of row Q + k.
+template <int S, int TM, int TN>
+__device__ __forceinline__ void merge_level_tri(const float* sG, const float* sB, float* sX, float* sT, int t) {
+    using namespace utk;
+    constexpr int NP = C / (2 * S);
+    constexpr int TR = S / TM, TC = S / TN;
+    constexpr int WPP = TR * TC / 32;  // warps per diagonal pair
+    constexpr int WC = 32 / TR, WR = 32 / TC;
+    static_assert(NP * WPP == kCompute / 32 && 32 % TR == 0 && 32 % TC == 0, "warp tiling");
+    static_assert((WC * TN) % 4 == 0 && (WR * TM) % 4 == 0, "k ranges in steps of 4");
+    const int cw = t >> 5, lane = t & 31;
+    const int pr = cw / WPP;
+    const int wp = cw < 4 ? cw % WPP : WPP - 1 - (cw - 4) % WPP;
+    const int P = 2 * pr * S, Q = P + S;
+    float acc[TM][TN];
+    {  // pass 1: T = (D G)_PQ X_QQ over k < kend
+        const int i0 = (lane % TR) * TM, j0 = (wp * WC + lane / TR) * TN;
+        const int kend = (wp + 1) * WC * TN;
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+            for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
+#pragma unroll 2
+        for (int k4 = 0; k4 < kend; k4 += 4) {
+            float g[4][TM], x[4][TN];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ld_row<TM>(g[e], sG + (Q + k4 + e) * LDG + P + i0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ld_row<TN>(x[e], sX + (Q + k4 + e) * C + Q + j0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int u = 0; u < TM; ++u)
+#pragma unroll
+                    for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(g[e][u], x[e][v], acc[u][v]);
+        }
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+            for (int v = 0; v < TN; ++v) sT[(pr * S + i0 + u) * LDT + j0 + v] = sB[P + i0 + u] * acc[u][v];
+    }
+    named_bar_sync(1, kCompute);
+    {  // pass 2: X_PQ = -X_PP T over k >= kbeg
+        const int i0 = (wp * WR + lane / TC) * TM, j0 = (lane % TC) * TN;
+        const int kbeg = wp * WR * TM;
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+            for (int v = 0; v < TN; ++v) acc[u][v] = 0.f;
+#pragma unroll 2
+        for (int k4 = kbeg; k4 < S; k4 += 4) {
+            float xp[TM][4], tv[4][TN];
+#pragma unroll
+            for (int u = 0; u < TM; ++u) ld_row<4>(xp[u], sX + (P + i0 + u) * C + P + k4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) ld_row<TN>(tv[e], sT + (pr * S + k4 + e) * LDT + j0);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int u = 0; u < TM; ++u)
+#pragma unroll
+                    for (int v = 0; v < TN; ++v) acc[u][v] = fmaf(xp[u][e], tv[e][v], acc[u][v]);
+        }
+#pragma unroll
+        for (int u = 0; u < TM; ++u)
+#pragma unroll
+            for (int v = 0; v < TN; ++v) sX[(P + i0 + u) * C + Q + j0 + v] = -acc[u][v];
+    }
+    named_bar_sync(1, kCompute);
+}
+
 // The 16 x 16 diagonal blocks of X = (I + D triu_1(G))^{-1} (unit upper
 // triangular) by back substitution into the dense, zeroed sX [128][128], for
 // 256 threads t (the merges above then fill the rest); sG holds G (upper
@@ -386,9 +463,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             if (t == 0) UT_TRACE(23);
             merge_level<16, 2, 2>(sG, sBeta, sX, sT, t);
             if (t == 0) UT_TRACE(24);
-            merge_level<32, 2, 4>(sG, sBeta, sX, sT, t);
+            merge_level_tri<32, 2, 4>(sG, sBeta, sX, sT, t);
             if (t == 0) UT_TRACE(25);
-            merge_level<64, 4, 4>(sG, sBeta, sX, sT, t);
+            merge_level_tri<64, 4, 4>(sG, sBeta, sX, sT, t);
             if (t == 0) UT_TRACE(3);
             // A = X D as hi/lo bf16 tiles.  The tiles overwrite the dense X, so
             // each thread first reads its 8 granules (8 consecutive columns of
