@@ -93,6 +93,8 @@ FWD_CONFIGS = {
     "small_bf16": FwdConfig("small_bf16", 2, 4, 1024, 64, "bf16", 1, beta_std=2.0, edge_frac=0.05),
     "path760m_bf16": FwdConfig("path760m_bf16", 8, 12, 4096, 128, "bf16", 2),
     "fox16k_bf16": FwdConfig("fox16k_bf16", 1, 12, 16384, 128, "bf16", 3, fox=True),
+    # the long end of the pages' length-extrapolation range (16K-64K)
+    "fox64k_bf16": FwdConfig("fox64k_bf16", 1, 12, 65536, 128, "bf16", 5, fox=True),
 }
 DECODE_CONFIGS = {
     "decode32k_bf16": DecodeConfig("decode32k_bf16", 64, 12, 128, 32768, 256, "bf16", 4),

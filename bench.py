@@ -325,28 +325,34 @@ def run_ours(args, rank, world, local):
         e2e = {"value": attn_flops * world * args.e2e_steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
 
-    # PaTH-FoX forward at L=16384 (far blocks skipped exactly), timed separately, not part of the step
-    fox = None
-    if args.fox_steps > 0:
-        fxc = inputs.FWD_CONFIGS["fox16k_bf16"]
+    # PaTH-FoX forwards at L=16384 and L=65536 (far blocks skipped exactly), timed separately,
+    # not part of the step
+    fox = {}
+    for key, cname in (("fox16k", "fox16k_bf16"), ("fox64k", "fox64k_bf16")):
+        if args.fox_steps <= 0:
+            break
+        fxc = inputs.FWD_CONFIGS[cname]
         fx = fxc.make()
         fargs = [t.to(dev) for t in (fx.q, fx.k, fx.v, fx.w, fx.beta, fx.log_f)]
+        fscale = fx.scale
+        del fx
         fo = torch.empty_like(fargs[0])
         fws = P.alloc_workspace(P.path_attn_workspace_bytes(fxc.B, fxc.H, fxc.L, fxc.d, fargs[0].dtype), dev)
         for _ in range(2):
-            P.path_attn_fwd_fox(*fargs, scale=fx.scale, out=fo, workspace=fws)
+            P.path_attn_fwd_fox(*fargs, scale=fscale, out=fo, workspace=fws)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(args.fox_steps):
-            P.path_attn_fwd_fox(*fargs, scale=fx.scale, out=fo, workspace=fws)
+            P.path_attn_fwd_fox(*fargs, scale=fscale, out=fo, workspace=fws)
         b.record()
         torch.cuda.synchronize()
         fms = a.elapsed_time(b) / args.fox_steps
-        fox = {"ms": fms, "attn_equiv_tflops": fxc.attn_flops / (fms * 1e-3) / 1e12, "steps": args.fox_steps,
-               "workload": "PaTH-FoX forward B1 H12 L16384 d128 bf16, log f = logsigmoid(N(3,1)); FLOPs counted "
-                           "over the full causal triangle although far key blocks are skipped"}
+        fox[key] = {"ms": fms, "attn_equiv_tflops": fxc.attn_flops / (fms * 1e-3) / 1e12, "steps": args.fox_steps,
+                    "workload": "PaTH-FoX forward B%d H%d L%d d%d bf16, log f = logsigmoid(N(3,1)); FLOPs counted "
+                                "over the full causal triangle although far key blocks are skipped"
+                                % (fxc.B, fxc.H, fxc.L, fxc.d)}
         del fargs, fo, fws
 
     # prefill -> decode hand-off on the forward workload (timed separately, not part of the step)
@@ -384,7 +390,7 @@ def run_ours(args, rank, world, local):
                        "seq_len": fc.L, "parallelism": "replicas (b,h)-independent" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (forward 384 MiB of q,k,v,w; decode caches 13 GB)"},
             "fwd_ms": fwd_ms_max / args.steps, "fwd_kernel_ms": fk,
-            "decode": dec_obj, "prefill_kcache": prefill, "fox16k": fox, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "decode": dec_obj, "prefill_kcache": prefill, "fox16k": fox.get("fox16k"), "fox64k": fox.get("fox64k"), "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps}
     if rank == 0:
         print(json.dumps(line))

@@ -147,3 +147,47 @@ def test_fox_strong_gates_far_blocks_skipped(L):
     g = torch.Generator().manual_seed(61)
     x.log_f = torch.nn.functional.logsigmoid(torch.randn(x.beta.shape, generator=g)).float()
     _full_case(x, "fox strong gates L=%d" % L)
+
+
+def test_fox_64k_full_size_sampled():
+    """B1 H12 L65536 d128 bf16 PaTH-FoX (the long end of the pages' 16K-64K extrapolation range):
+    whole forward on the GPU, sampled rows on the oracle."""
+    cfg = inputs.FWD_CONFIGS["fox64k_bf16"]
+    x = cfg.make()
+    o, lse = _gpu_fwd(x)
+    rng = np.random.default_rng(2)
+    heads = [(0, 0), (0, 11)]
+    rows = _sampled_rows(cfg.L, rng, n=4)
+    o_ref, lse_ref = _oracle(x, heads, rows)
+    got = np.concatenate([to_np(o[b, h, rows]) for (b, h) in heads])
+    got_lse = np.concatenate([to_np(lse[b, h, rows]) for (b, h) in heads])
+    check(got, o_ref, torch.bfloat16, "fox64k sampled")
+    check_lse(got_lse, lse_ref, torch.bfloat16, "fox64k sampled")
+    assert torch.isfinite(o).all()
+
+
+@pytest.mark.parametrize("dtype,d,beta_zero", [("bf16", 128, True), ("bf16", 64, True), ("f32", 32, True),
+                                               ("bf16", 128, False)])
+def test_alibi_as_constant_forget_gate(dtype, d, beta_zero):
+    """A per-head ALiBi bias -slope (i - j) is the FoX bias with log f_s = -slope for every s.  With
+    beta = 0 the result must be textbook ALiBi attention (fp64 SDPA with the explicit bias matrix,
+    independent of the PaTH oracle); with random beta it is PaTH + ALiBi, checked on the oracle."""
+    B, H, L = 1, 4, 700
+    x = inputs.make_fwd(B, H, L, d, dtype, seed=71)
+    if beta_zero:
+        x.beta.zero_()
+    slopes = torch.tensor([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)])
+    x.log_f = (-slopes).view(1, H, 1).expand(B, H, L).contiguous().float()
+    o, lse = _gpu_fwd(x)
+    f = inputs.f64
+    if beta_zero:
+        i = torch.arange(L, dtype=torch.float64)
+        rel = i.view(L, 1) - i.view(1, L)
+        bias = torch.where(rel >= 0, -slopes.double().view(H, 1, 1) * rel, torch.tensor(float("-inf"), dtype=torch.float64))
+        qd, kd, vd = (t.double() for t in (x.q, x.k, x.v))
+        ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, attn_mask=bias.unsqueeze(0), scale=x.scale)
+        check(to_np(o), ref.numpy(), x.q.dtype, "alibi %s d%d" % (dtype, d))
+    else:
+        o_ref, lse_ref = _oracle(x)
+        check(to_np(o), o_ref, x.q.dtype, "PaTH + alibi")
+        check_lse(to_np(lse), lse_ref, x.q.dtype, "PaTH + alibi")
