@@ -27,8 +27,9 @@ def path_product(w, beta, j, i):
     return P
 
 
-def logits(q, k, w, beta, scale=1.0, log_f=None):
-    """[L, L] PaTH logits of one head; -inf above the diagonal."""
+def logits(q, k, w, beta, scale=1.0, log_f=None, rel_bias=None):
+    """[L, L] PaTH logits of one head; -inf above the diagonal.  rel_bias[i - j] (optional)
+    is added unscaled to entry (i, j)."""
     q, k, w, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, w, beta))
     L = q.shape[0]
     S = np.full((L, L), -np.inf)
@@ -37,13 +38,15 @@ def logits(q, k, w, beta, scale=1.0, log_f=None):
             s = scale * (k[j] @ path_product(w, beta, j, i) @ q[i])
             if log_f is not None:
                 s += sum(float(log_f[t]) for t in range(j + 1, i + 1))
+            if rel_bias is not None:
+                s += float(rel_bias[i - j])
             S[i, j] = s
     return S
 
 
-def attention(q, k, v, w, beta, scale=1.0, log_f=None):
+def attention(q, k, v, w, beta, scale=1.0, log_f=None, rel_bias=None):
     """Causal softmax attention over the dense-product logits; returns (o [L, d], lse [L])."""
-    S = logits(q, k, w, beta, scale, log_f)
+    S = logits(q, k, w, beta, scale, log_f, rel_bias)
     m = S.max(axis=1, keepdims=True)
     P = np.exp(S - m)
     l = P.sum(axis=1, keepdims=True)

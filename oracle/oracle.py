@@ -55,6 +55,8 @@ def _load():
             lib.path_oracle_fwd_rows.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_double, _i64p, ctypes.c_int64, _dp, _dp]
             lib.path_oracle_fwd_rows.restype = None
+            lib.path_oracle_fwd_rows_relbias.argtypes = lib.path_oracle_fwd_rows.argtypes
+            lib.path_oracle_fwd_rows_relbias.restype = None
             lib.path_oracle_logits.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_double, _dp]
             lib.path_oracle_logits.restype = None
@@ -82,16 +84,23 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(_dp)
 
 
-def path_attn(q, k, v, w, beta, log_f=None, scale=None, rows=None):
+def path_attn(q, k, v, w, beta, log_f=None, scale=None, rows=None, rel_bias=None):
     """Causal PaTH(-FoX) attention in fp64.
 
     q, k, v, w: [..., L, d]; beta, log_f: [..., L].  Leading dims are flattened
     into heads.  ``rows`` (optional, int array) selects flat row indices
     ``head * L + i``; then o is [len(rows), d] and lse [len(rows)].  Otherwise
     o has q's shape and lse q's shape without d.
+
+    ``rel_bias`` ([..., L] like beta; exclusive with log_f) adds rel_bias[..., i - j]
+    unscaled to the logit of (i, j): a relative-position prior such as GGD-BAM's
+    ("Resumo Técnico: Mecanismo de Atenção Bayesiana (BAM)", §"Solução Proposta:
+    GGD-BAM") or ALiBi's, on top of the PaTH logits.
     """
     q, k, v, w, beta = (_f64(x) for x in (q, k, v, w, beta))
     lf = None if log_f is None else _f64(log_f)
+    rb = None if rel_bias is None else _f64(rel_bias)
+    assert lf is None or rb is None, "log_f and rel_bias are exclusive"
     L, d = q.shape[-2], q.shape[-1]
     BH = int(np.prod(q.shape[:-2])) if q.ndim > 2 else 1
     for x in (k, v, w):
@@ -99,22 +108,25 @@ def path_attn(q, k, v, w, beta, log_f=None, scale=None, rows=None):
     assert beta.shape == q.shape[:-1]
     if lf is not None:
         assert lf.shape == beta.shape
+    if rb is not None:
+        assert rb.shape == beta.shape
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     lib = _load()
+    fn, extra = (lib.path_oracle_fwd_rows, lf) if rb is None else (lib.path_oracle_fwd_rows_relbias, rb)
     if rows is None:
         n = BH * L
         o = np.empty((n, d))
         lse = np.empty(n)
-        lib.path_oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(lf), BH, L, d,
-                                 float(scale), None, n, _ptr(o), _ptr(lse))
+        fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(extra), BH, L, d, float(scale), None, n,
+           _ptr(o), _ptr(lse))
         return o.reshape(q.shape), lse.reshape(q.shape[:-1])
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     assert rows.min() >= 0 and rows.max() < BH * L
     o = np.empty((rows.size, d))
     lse = np.empty(rows.size)
-    lib.path_oracle_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(lf), BH, L, d,
-                             float(scale), rows.ctypes.data_as(_i64p), rows.size, _ptr(o), _ptr(lse))
+    fn(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(extra), BH, L, d, float(scale),
+       rows.ctypes.data_as(_i64p), rows.size, _ptr(o), _ptr(lse))
     return o, lse
 
 

@@ -65,15 +65,17 @@ static void apply_transition(double* u, const double* w, double beta, int d) {
 /*
  * Logits of one query row i of one head, written to s[0..i].
  * q_i: [d]; k, w: [L, d] of this head; beta, log_f: [L] of this head
- * (log_f may be NULL).  u is a scratch vector of length d.
+ * (log_f may be NULL); rel: [L] relative-position bias of this head, rel[i - j]
+ * added to s_ij (may be NULL).  u is a scratch vector of length d.
  */
 static void row_logits(const double* qi, const double* k, const double* w,
-                       const double* beta, const double* log_f, int i, int d,
+                       const double* beta, const double* log_f, const double* rel, int i, int d,
                        double scale, double* s, double* u) {
     memcpy(u, qi, sizeof(double) * (size_t)d);
     double bias = 0.0; /* sum_{s=j+1..i} log f_s, empty (0) at j = i */
     for (int j = i; j >= 0; --j) {
         s[j] = scale * dot(k + (size_t)j * d, u, d) + bias;
+        if (rel) s[j] += rel[i - j];
         /* next key j-1 sees H_j ... H_i q_i */
         apply_transition(u, w + (size_t)j * d, beta[j], d);
         if (log_f) bias += log_f[j];
@@ -103,12 +105,9 @@ static double softmax_combine(const double* s, const double* v, int n, int d, do
  * and o_rows[r*d ...], lse_rows[r] receive the results.  rows == NULL means
  * every row of every head in natural order (n_rows must be BH*L).
  */
-void path_oracle_fwd_rows(const double* q, const double* k, const double* v,
-                          const double* w, const double* beta, const double* log_f,
-                          int BH, int L, int d, double scale,
-                          const int64_t* rows, int64_t n_rows,
-                          double* o_rows, double* lse_rows) {
-    (void)BH;
+static void fwd_rows(const double* q, const double* k, const double* v, const double* w,
+                     const double* beta, const double* log_f, const double* rel, int L, int d,
+                     double scale, const int64_t* rows, int64_t n_rows, double* o_rows, double* lse_rows) {
 #pragma omp parallel
     {
         double* s = (double*)malloc(sizeof(double) * (size_t)L);
@@ -120,13 +119,38 @@ void path_oracle_fwd_rows(const double* q, const double* k, const double* v,
             int i = (int)(gi % L);
             size_t hoff = (size_t)bh * (size_t)L;
             row_logits(q + (size_t)gi * d, k + hoff * d, w + hoff * d, beta + hoff,
-                       log_f ? log_f + hoff : NULL, i, d, scale, s, u);
+                       log_f ? log_f + hoff : NULL, rel ? rel + hoff : NULL, i, d, scale, s, u);
             double lse = softmax_combine(s, v + hoff * d, i + 1, d, o_rows + (size_t)r * d);
             if (lse_rows) lse_rows[r] = lse;
         }
         free(s);
         free(u);
     }
+}
+
+void path_oracle_fwd_rows(const double* q, const double* k, const double* v,
+                          const double* w, const double* beta, const double* log_f,
+                          int BH, int L, int d, double scale,
+                          const int64_t* rows, int64_t n_rows,
+                          double* o_rows, double* lse_rows) {
+    (void)BH;
+    fwd_rows(q, k, v, w, beta, log_f, NULL, L, d, scale, rows, n_rows, o_rows, lse_rows);
+}
+
+/*
+ * As path_oracle_fwd_rows, with a relative-position bias instead of forget
+ * gates: rel [B*H, L], rel[bh*L + (i - j)] added unscaled to s_ij — the additive
+ * positional prior of "Resumo Técnico: Mecanismo de Atenção Bayesiana (BAM)",
+ * §"Solução Proposta: GGD-BAM" (bias matrix b_ij depending on i - j only),
+ * on top of the PaTH logits.
+ */
+void path_oracle_fwd_rows_relbias(const double* q, const double* k, const double* v,
+                                  const double* w, const double* beta, const double* rel,
+                                  int BH, int L, int d, double scale,
+                                  const int64_t* rows, int64_t n_rows,
+                                  double* o_rows, double* lse_rows) {
+    (void)BH;
+    fwd_rows(q, k, v, w, beta, NULL, rel, L, d, scale, rows, n_rows, o_rows, lse_rows);
 }
 
 /*
@@ -140,7 +164,7 @@ void path_oracle_logits(const double* q, const double* k, const double* w,
     for (int i = 0; i < L; ++i) {
         double* row = S + (size_t)i * L;
         for (int j = i + 1; j < L; ++j) row[j] = -INFINITY;
-        row_logits(q + (size_t)i * d, k, w, beta, log_f, i, d, scale, row, u);
+        row_logits(q + (size_t)i * d, k, w, beta, log_f, NULL, i, d, scale, row, u);
     }
     free(u);
 }

@@ -315,3 +315,57 @@ def test_pins_reject_planted_mistakes(mutation):
     np.testing.assert_allclose(good[mask], exp[mask], atol=1e-12)
     bad = _walk_mutant(q, k, w, beta, mutation)
     assert np.max(np.abs(bad[mask] - exp[mask])) > 0.1
+
+
+# --------------------------------------------------------------------------- relative-position bias
+def _ggd_table(L, mu, alpha, p):
+    """GGD-BAM prior ("Mecanismo de Atenção Bayesiana (BAM)", §"Solução Proposta: GGD-BAM"):
+    b_ij = -|(j - i - mu) / alpha|^p, tabulated by the distance i - j."""
+    delta = np.arange(L, dtype=np.float64)
+    return -np.abs((-delta - mu) / alpha) ** p
+
+
+def test_relbias_with_beta_zero_is_textbook_biased_attention():
+    """beta = 0 (every transition the identity): PaTH + relative bias is softmax attention with
+    the explicit bias matrix b[i, j] = rel[i - j]; reference: torch SDPA in fp64."""
+    import torch
+    rng = np.random.default_rng(81)
+    L, d = 48, 8
+    q, k, v, w, _ = _rand_case(rng, L, d)
+    rel = _ggd_table(L, 0.5, 6.0, 0.7)
+    o, lse = orc.path_attn(q, k, v, w, np.zeros(L), scale=0.35, rel_bias=rel)
+    idx = np.arange(L)
+    bias = np.where(idx[:, None] >= idx[None, :], rel[np.clip(idx[:, None] - idx[None, :], 0, L - 1)], -np.inf)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None],
+        attn_mask=torch.from_numpy(bias)[None], scale=0.35)[0].numpy()
+    np.testing.assert_allclose(o, ref, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed,p", [(82, 0.6), (83, 1.3)])
+def test_relbias_equals_dense_product_with_bias(seed, p):
+    """Random beta: the walk oracle with a relative bias equals the explicit d x d products plus the
+    bias matrix (brute force)."""
+    rng = np.random.default_rng(seed)
+    L, d = 20, 5
+    q, k, v, w, beta = _rand_case(rng, L, d)
+    rel = _ggd_table(L, 0.0, 3.0, p)
+    o, lse = orc.path_attn(q, k, v, w, beta, scale=0.5, rel_bias=rel)
+    o_ref, lse_ref = dense.attention(q, k, v, w, beta, scale=0.5, rel_bias=rel)
+    np.testing.assert_allclose(o, o_ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-12)
+    # a table shifted by one position is a different operator: the pin discriminates
+    o_bad, _ = orc.path_attn(q, k, v, w, beta, scale=0.5, rel_bias=np.roll(rel, 1))
+    assert np.abs(o_bad - o_ref).max() > 1e-6
+
+
+def test_linear_relbias_equals_constant_forget_gates():
+    """ALiBi: rel[delta] = -slope * delta is the FoX bias with log f_s = -slope for every s."""
+    rng = np.random.default_rng(84)
+    L, d = 64, 8
+    q, k, v, w, beta = _rand_case(rng, L, d)
+    slope = 0.3
+    o1, l1 = orc.path_attn(q, k, v, w, beta, scale=0.4, rel_bias=-slope * np.arange(L, dtype=np.float64))
+    o2, l2 = orc.path_attn(q, k, v, w, beta, scale=0.4, log_f=np.full(L, -slope))
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
