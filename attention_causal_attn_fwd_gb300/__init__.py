@@ -10,6 +10,7 @@ Functions keep the C names:
 
 - ``path_attn_fwd(q, k, v, w, beta, scale=None, lse=False)``
 - ``path_attn_fwd_fox(q, k, v, w, beta, log_f, scale=None, lse=False)``
+- ``path_attn_fwd_relbias(q, k, v, w, beta, rel_bias, scale=None, lse=False)``
 - ``path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, scale=None)``
 - ``path_kcache_update(kcache, n_cached, w_t, beta_t)``
 - ``path_get_status(workspace)``, ``path_attn_workspace_bytes(...)``,
@@ -34,7 +35,7 @@ _DT = {torch.float32: PATH_F32, torch.bfloat16: PATH_BF16}
 EXPORTED = ("path_version", "path_status_string", "path_attn_workspace_bytes", "path_attn_fwd",
             "path_attn_fwd_fox", "path_decode_workspace_bytes", "path_kcache_update", "path_decode_step",
             "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events", "path_decode_step_noalloc",
-            "path_prefill_workspace_bytes", "path_prefill_kcache")
+            "path_prefill_workspace_bytes", "path_prefill_kcache", "path_attn_fwd_relbias")
 
 
 class PathLibraryError(RuntimeError):
@@ -74,6 +75,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.path_attn_fwd_fox.argtypes = [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i,
                                       ctypes.c_float, _vp, _sz, _vp]
     lib.path_attn_fwd_fox.restype = _i
+    lib.path_attn_fwd_relbias.argtypes = lib.path_attn_fwd_fox.argtypes
+    lib.path_attn_fwd_relbias.restype = _i
     lib.path_decode_workspace_bytes.argtypes = [_i, _i, _i, _i]
     lib.path_decode_workspace_bytes.restype = _sz
     lib.path_kcache_update.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _fp, _i, _vp]
@@ -144,7 +147,7 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
-def _fwd(q, k, v, w, beta, log_f, scale, lse, out, ws):
+def _fwd(q, k, v, w, beta, log_f, scale, lse, out, ws, rel_bias=None):
     lib = load()
     if q.dim() != 4:
         raise ValueError("q must be [B, H, L, d]")
@@ -157,6 +160,8 @@ def _fwd(q, k, v, w, beta, log_f, scale, lse, out, ws):
     _dev(beta, "beta", torch.float32, (B, H, L))
     if log_f is not None:
         _dev(log_f, "log_f", torch.float32, (B, H, L))
+    if rel_bias is not None:
+        _dev(rel_bias, "rel_bias", torch.float32, (H, L))
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else _dev(out, "out", dt, (B, H, L, d))
     lse_t = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse else None
@@ -167,7 +172,9 @@ def _fwd(q, k, v, w, beta, log_f, scale, lse, out, ws):
         ws = alloc_workspace(need, q.device)
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta)]
     tail = [_ptr(o), _ptr(lse_t), B, H, L, d, _DT[dt], 1, ctypes.c_float(scale), _ptr(ws), ws.numel(), _stream()]
-    if log_f is None:
+    if rel_bias is not None:
+        _check(lib.path_attn_fwd_relbias(*args, _ptr(rel_bias), *tail), "path_attn_fwd_relbias")
+    elif log_f is None:
         _check(lib.path_attn_fwd(*args, *tail), "path_attn_fwd")
     else:
         _check(lib.path_attn_fwd_fox(*args, _ptr(log_f), *tail), "path_attn_fwd_fox")
@@ -184,6 +191,15 @@ def path_attn_fwd_fox(q, k, v, w, beta, log_f, scale=None, lse=False, out=None, 
     if log_f is None:
         raise ValueError("log_f is required")
     return _fwd(q, k, v, w, beta, log_f, scale, lse, out, workspace)
+
+
+def path_attn_fwd_relbias(q, k, v, w, beta, rel_bias, scale=None, lse=False, out=None, workspace=None):
+    """PaTH forward with a relative-position bias: adds rel_bias[h, i - j] to the scaled logit of (i, j).
+
+    rel_bias: [H, L] fp32 CUDA, shared by every batch entry (e.g. a GGD-BAM or ALiBi prior)."""
+    if rel_bias is None:
+        raise ValueError("rel_bias is required")
+    return _fwd(q, k, v, w, beta, None, scale, lse, out, workspace, rel_bias=rel_bias)
 
 
 def path_prefill_workspace_bytes(B: int, H: int, L: int, d: int, dtype: torch.dtype) -> int:

@@ -9,13 +9,13 @@
 namespace pathattn {
 int simt_chunk(int d);
 cudaError_t fwd_simt_f32(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                         const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
-                         unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
+                         const float* log_f, const float* rel_bias, int H, void* o, float* lse, int BH, int L, int d,
+                         float scale, unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
 int tc_chunk(int d);
 bool tc_supported(int d);
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                        const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
-                        unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st);
+                        const float* log_f, const float* rel_bias, int H, void* o, float* lse, int BH, int L, int d,
+                        float scale, unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st);
 cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w, const float* beta, void* kcache,
                            int BH, int L, int n_max, unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
 cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
@@ -43,27 +43,31 @@ static bool fwd_d_ok(int d, int dtype) {
 static int fwd_chunk(int d, int dtype) { return dtype == PATH_F32 ? simt_chunk(d) : tc_chunk(d); }
 static bool dec_d_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
+// extra: 0 plain, 1 FoX (bias = log forget gates), 2 relative-position bias table
 static int fwd_common(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                      const float* log_f, bool fox, void* o, float* lse, int B, int H, int L, int d, int dtype,
+                      const float* bias, int extra, void* o, float* lse, int B, int H, int L, int d, int dtype,
                       int causal, float scale, void* ws, size_t ws_bytes, cudaStream_t st) {
+    const bool fox = extra == 1, rel = extra == 2;
     if (B < 1 || H < 1 || L < 1 || d < 1) return PATH_ERR_INVALID;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
     if (!causal) return PATH_ERR_UNSUPPORTED;
     if (!fwd_d_ok(d, dtype)) return PATH_ERR_UNSUPPORTED;
     if ((long long)B * H * L > (1ll << 31) / 256) return PATH_ERR_UNSUPPORTED;
-    if (!q || !k || !v || !w || !beta || !o || (fox && !log_f)) return PATH_ERR_INVALID;
+    if (!q || !k || !v || !w || !beta || !o || (extra != 0 && !bias)) return PATH_ERR_INVALID;
     const void* ptrs[] = {q, k, v, w, beta, o};
     for (const void* p : ptrs)
         if (!aligned16(p)) return PATH_ERR_INVALID;
-    if ((fox && !aligned16(log_f)) || (lse && !aligned16(lse))) return PATH_ERR_INVALID;
+    if ((extra != 0 && !aligned16(bias)) || (lse && !aligned16(lse))) return PATH_ERR_INVALID;
     const FwdLayout lay = fwd_layout(B, H, L, d, fwd_chunk(d, dtype), elt_size(dtype));
     if (!ws || ws_bytes < lay.total || !aligned16(ws)) return PATH_ERR_WORKSPACE;
     unsigned char* wsb = static_cast<unsigned char*>(ws);
     cudaError_t e;
+    const float* log_f = fox ? bias : nullptr;
+    const float* rel_bias = rel ? bias : nullptr;
     if (dtype == PATH_F32)
-        e = fwd_simt_f32(q, k, v, w, beta, fox ? log_f : nullptr, o, lse, B * H, L, d, scale, wsb, lay, st);
+        e = fwd_simt_f32(q, k, v, w, beta, log_f, rel_bias, H, o, lse, B * H, L, d, scale, wsb, lay, st);
     else
-        e = fwd_tc_bf16(q, k, v, w, beta, fox ? log_f : nullptr, o, lse, B * H, L, d, scale, wsb, lay,
+        e = fwd_tc_bf16(q, k, v, w, beta, log_f, rel_bias, H, o, lse, B * H, L, d, scale, wsb, lay,
                         g_fault_mask.load(), st);
     if (e != cudaSuccess) {
         std::fprintf(stderr, "pathattn: forward launch failed: %s\n", cudaGetErrorString(e));
@@ -100,14 +104,21 @@ size_t path_attn_workspace_bytes(int B, int H, int L, int d, int dtype) {
 int path_attn_fwd(const void* q, const void* k, const void* v, const void* w, const float* beta, void* o,
                   float* lse, int B, int H, int L, int d, int dtype, int causal, float scale, void* workspace,
                   size_t workspace_bytes, path_stream_t stream) {
-    return fwd_common(q, k, v, w, beta, nullptr, false, o, lse, B, H, L, d, dtype, causal, scale, workspace,
+    return fwd_common(q, k, v, w, beta, nullptr, 0, o, lse, B, H, L, d, dtype, causal, scale, workspace,
                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w, const float* beta,
                       const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype, int causal,
                       float scale, void* workspace, size_t workspace_bytes, path_stream_t stream) {
-    return fwd_common(q, k, v, w, beta, log_f, true, o, lse, B, H, L, d, dtype, causal, scale, workspace,
+    return fwd_common(q, k, v, w, beta, log_f, 1, o, lse, B, H, L, d, dtype, causal, scale, workspace,
+                      workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int path_attn_fwd_relbias(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                          const float* rel_bias, void* o, float* lse, int B, int H, int L, int d, int dtype,
+                          int causal, float scale, void* workspace, size_t workspace_bytes, path_stream_t stream) {
+    return fwd_common(q, k, v, w, beta, rel_bias, 2, o, lse, B, H, L, d, dtype, causal, scale, workspace,
                       workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 

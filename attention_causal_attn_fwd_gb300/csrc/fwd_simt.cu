@@ -41,14 +41,18 @@ struct FwdSmem {
 };
 
 // One CTA per (query chunk, head).  Query chunks are visited longest-first.
-template <typename T, int C, int D, int NT, bool FOX>
+// MODE 0: PaTH; 1: PaTH-FoX (bias c_i - c_j from the log-gate cumsum);
+// 2: relative-position bias rel[h][i - j] ([H, L] table).
+template <typename T, int C, int D, int NT, int MODE>
 __global__ void __launch_bounds__(NT) path_fwd_simt(const T* __restrict__ q, const T* __restrict__ k,
                                                     const T* __restrict__ v, const T* __restrict__ w,
                                                     const float* __restrict__ qhat,
                                                     const T* __restrict__ khat, const T* __restrict__ un,
                                                     const T* __restrict__ y, const T* __restrict__ zn,
-                                                    const float* __restrict__ cum, T* __restrict__ o,
-                                                    float* __restrict__ lse, int L, int Lp, float scale) {
+                                                    const float* __restrict__ cum, const float* __restrict__ rel,
+                                                    int H, T* __restrict__ o, float* __restrict__ lse, int L, int Lp,
+                                                    float scale) {
+    constexpr bool FOX = MODE == 1, REL = MODE == 2;
     using SM = FwdSmem<T, C, D, NT>;
     constexpr int LDT = SM::LDT, LDS = SM::LDS;
     constexpr int RG = NT / C;  // threads per row in the softmax
@@ -76,6 +80,7 @@ __global__ void __launch_bounds__(NT) path_fwd_simt(const T* __restrict__ q, con
     const size_t woff = (size_t)bh * Lp;
     const float sl2 = scale * 1.4426950408889634f;  // logits in log2 units
     constexpr float kLog2e = 1.4426950408889634f;
+    const float* relh = REL ? rel + (size_t)(bh % H) * L : nullptr;  // this head's bias by distance
 
     if (FOX)
         for (int i = threadIdx.x; i < C; i += NT) sCi[i] = cum[woff + r0 + i];
@@ -99,6 +104,7 @@ __global__ void __launch_bounds__(NT) path_fwd_simt(const T* __restrict__ q, con
         for (int j = g; j < C; j += RG) {
             float s = sS[r * LDS + j] * sl2;
             if (FOX) s += (sCi[r] - sCi[j]) * kLog2e;
+            if (REL) s += __ldg(relh + min(max(r - j, 0), L - 1)) * kLog2e;
             if (j > r) s = -INFINITY;
             sS[r * LDS + j] = s;
             mx = fmaxf(mx, s);
@@ -146,6 +152,7 @@ __global__ void __launch_bounds__(NT) path_fwd_simt(const T* __restrict__ q, con
             for (int j = g; j < C; j += RG) {
                 float s = sS[r * LDS + j] * sl2;
                 if (FOX) s += (sCi[r] - sCj[j]) * kLog2e;
+                if (REL) s += __ldg(relh + min(r0 + r - c0 - j, L - 1)) * kLog2e;  // padding rows clamp
                 sS[r * LDS + j] = s;
                 mx = fmaxf(mx, s);
             }
@@ -194,8 +201,8 @@ __global__ void __launch_bounds__(NT) path_fwd_simt(const T* __restrict__ q, con
 // ----------------------------------------------------------------------------- host launchers
 template <typename T, int C, int D>
 static cudaError_t launch_simt(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                               const float* log_f, void* o, float* lse, int BH, int L, float scale,
-                               unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
+                               const float* log_f, const float* rel_bias, int H, void* o, float* lse, int BH, int L,
+                               float scale, unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
     constexpr int NT = 256;
     const int nch = cdiv(L, C);
     cudaError_t e = launch_ut_prep(PATH_F32, C, D, q, k, w, beta, log_f, BH, L, ws, lay, st);
@@ -211,12 +218,13 @@ static cudaError_t launch_simt(const void* q, const void* k, const void* v, cons
     const T* zn = reinterpret_cast<const T*>(ws + lay.zn);
     const float* cum = reinterpret_cast<const float*>(ws + lay.cum);
     const size_t fsm = FwdSmem<T, C, D, NT>::bytes;
-    auto kf = log_f ? path_fwd_simt<T, C, D, NT, true> : path_fwd_simt<T, C, D, NT, false>;
+    auto kf = log_f ? path_fwd_simt<T, C, D, NT, 1> : rel_bias ? path_fwd_simt<T, C, D, NT, 2>
+                                                               : path_fwd_simt<T, C, D, NT, 0>;
     e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsm);
     if (e != cudaSuccess) return e;
     mark_start(st);
-    kf<<<dim3(nch, BH), NT, fsm, st>>>(tq, tk, tv, tw, qhat, khat, un, y, zn, cum, static_cast<T*>(o), lse, L,
-                                       lay.Lp, scale);
+    kf<<<dim3(nch, BH), NT, fsm, st>>>(tq, tk, tv, tw, qhat, khat, un, y, zn, cum, rel_bias, H,
+                                       static_cast<T*>(o), lse, L, lay.Lp, scale);
     mark_end(st);
     return cudaGetLastError();
 }
@@ -225,13 +233,15 @@ static cudaError_t launch_simt(const void* q, const void* k, const void* v, cons
 int simt_chunk(int d) { return d <= 16 ? 16 : 32; }
 
 cudaError_t fwd_simt_f32(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                         const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
-                         unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
+                         const float* log_f, const float* rel_bias, int H, void* o, float* lse, int BH, int L, int d,
+                         float scale, unsigned char* ws, const FwdLayout& lay, cudaStream_t st) {
+#define PATH_SIMT_ARGS q, k, v, w, beta, log_f, rel_bias, H, o, lse, BH, L, scale, ws, lay, st
     switch (d) {
-        case 16: return launch_simt<float, 16, 16>(q, k, v, w, beta, log_f, o, lse, BH, L, scale, ws, lay, st);
-        case 32: return launch_simt<float, 32, 32>(q, k, v, w, beta, log_f, o, lse, BH, L, scale, ws, lay, st);
-        case 64: return launch_simt<float, 32, 64>(q, k, v, w, beta, log_f, o, lse, BH, L, scale, ws, lay, st);
-        case 128: return launch_simt<float, 32, 128>(q, k, v, w, beta, log_f, o, lse, BH, L, scale, ws, lay, st);
+        case 16: return launch_simt<float, 16, 16>(PATH_SIMT_ARGS);
+        case 32: return launch_simt<float, 32, 32>(PATH_SIMT_ARGS);
+        case 64: return launch_simt<float, 32, 64>(PATH_SIMT_ARGS);
+        case 128: return launch_simt<float, 32, 128>(PATH_SIMT_ARGS);
+#undef PATH_SIMT_ARGS
         default: return cudaErrorInvalidValue;
     }
 }

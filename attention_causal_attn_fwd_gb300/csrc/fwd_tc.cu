@@ -93,6 +93,8 @@ struct TcParams {
     unsigned long long limit_ns;
     const __nv_bfloat16* q;    // [BH, L, d] (FoX: query norms for far-block skipping)
     const float* kmax2;        // [BH, nch] max |khat|^2 per chunk (FoX)
+    const float* rbias;        // [H, L] bias by distance i - j (relative-bias mode)
+    int H;
     int nch;
     int fault;                 // test hook: skip one producer signal
 #ifdef PATH_TRACE
@@ -100,7 +102,9 @@ struct TcParams {
 #endif
 };
 
-template <int D, bool FOX>
+// MODE 0: PaTH; 1: PaTH-FoX (forget-gate bias, far blocks skipped); 2: PaTH
+// with a relative-position bias table rel[h][i - j].
+template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     path_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
@@ -108,6 +112,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_zn,
                 const TcParams p) {
     static_assert(D == 64 || D == 128, "head dim");
+    constexpr bool FOX = MODE == 1, REL = MODE == 2;
+    constexpr bool BIASED = MODE != 0;   // logits carry an additive bias (log2 units in the softmax)
     constexpr int KCH = D / 64;          // 64-column chunks of the head dim
     constexpr uint32_t ROWB = 128u * D * 2u;  // bytes of one [128 x D] bf16 tile
     constexpr uint32_t IDESC_S128 = idesc_bf16(128, false);
@@ -375,6 +381,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int r = 32 * (warp & 3) + lane;  // query row within the tile (= TMEM lane)
         const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const float* cumh = FOX ? p.cum + (size_t)bh * p.Lp : nullptr;
+        const float* relh = REL ? p.rbias + (size_t)(bh % p.H) * p.L : nullptr;
         const float ci = FOX ? cumh[row0 + r] : 0.f;
         constexpr float kL2e = 1.4426950408889634f;
         float m_run = -INFINITY, l_run = 0.f;
@@ -445,6 +452,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
+            if (REL) {  // bias at distance i - j, clamped into the table (masked or padding entries)
+                const int base = row0 + r - m * kTcC;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float bv[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) bv[j] = __ldg(relh + min(max(base - 32 * c - j, 0), p.L - 1));
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) s[32 * c + j] = fmaf(s[32 * c + j], sl2, bv[j] * kL2e);
+                }
+            }
             if (it == 0) {
 #pragma unroll
                 for (int j = 0; j < 128; ++j)
@@ -458,7 +476,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int j = 8; j < 128; ++j) pm[j & 7] = fmaxf(pm[j & 7], s[j]);
                 mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
-                if (!FOX) mx *= sl2;  // sl2 > 0: the max of raw scores scales
+                if (!BIASED) mx *= sl2;  // sl2 > 0: the max of raw scores scales
             }
             bool stop = false;
             if (FOX) {
@@ -489,8 +507,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float neg_m = -m_use;
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
-                const float p0 = ex2_approx(FOX ? s[2 * j] + neg_m : fmaf(s[2 * j], sl2, neg_m));
-                const float p1 = ex2_approx(FOX ? s[2 * j + 1] + neg_m : fmaf(s[2 * j + 1], sl2, neg_m));
+                const float p0 = ex2_approx(BIASED ? s[2 * j] + neg_m : fmaf(s[2 * j], sl2, neg_m));
+                const float p1 = ex2_approx(BIASED ? s[2 * j + 1] + neg_m : fmaf(s[2 * j + 1], sl2, neg_m));
                 psum[j & 7] += p0 + p1;
                 pk[j] = pack_bf16x2(p0, p1);
             }
@@ -723,8 +741,8 @@ namespace pathattn {
 
 template <int D>
 static cudaError_t launch_tc(const void* q, const void* k, const void* v, const void* w, const float* log_f,
-                            void* o, float* lse, int BH, int L, float scale, unsigned char* ws, const FwdLayout& lay,
-                            int fault, cudaStream_t st) {
+                            const float* rel_bias, int H, void* o, float* lse, int BH, int L, float scale,
+                            unsigned char* ws, const FwdLayout& lay, int fault, cudaStream_t st) {
     CUtensorMap mq, mk, mv, mw, mkh, mun, my, mzn;
     if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mv, v, D, L, BH) ||
         !make_map(&mw, w, D, L, BH) || !make_map(&mkh, ws + lay.khat, D, lay.Lp, BH) ||
@@ -747,10 +765,12 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.kmax2 = reinterpret_cast<const float*>(ws + lay.kmax);
     p.nch = lay.Lp / kTcC;
+    p.rbias = rel_bias;
+    p.H = H;
 #ifdef PATH_TRACE
     p.trace = trace_buffer();
 #endif
-    auto kern = log_f ? path_fwd_tc<D, true> : path_fwd_tc<D, false>;
+    auto kern = log_f ? path_fwd_tc<D, 1> : rel_bias ? path_fwd_tc<D, 2> : path_fwd_tc<D, 0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     mark_start(st);
@@ -760,12 +780,12 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
 }
 
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                        const float* log_f, void* o, float* lse, int BH, int L, int d, float scale,
-                        unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st) {
+                        const float* log_f, const float* rel_bias, int H, void* o, float* lse, int BH, int L, int d,
+                        float scale, unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st) {
     cudaError_t e = launch_ut_prep(PATH_BF16, kTcC, d, q, k, w, beta, log_f, BH, L, ws, lay, st);
     if (e != cudaSuccess) return e;
-    if (d == 64) return launch_tc<64>(q, k, v, w, log_f, o, lse, BH, L, scale, ws, lay, fault_mask, st);
-    if (d == 128) return launch_tc<128>(q, k, v, w, log_f, o, lse, BH, L, scale, ws, lay, fault_mask, st);
+    if (d == 64) return launch_tc<64>(q, k, v, w, log_f, rel_bias, H, o, lse, BH, L, scale, ws, lay, fault_mask, st);
+    if (d == 128) return launch_tc<128>(q, k, v, w, log_f, rel_bias, H, o, lse, BH, L, scale, ws, lay, fault_mask, st);
     return cudaErrorInvalidValue;
 }
 

@@ -8,7 +8,7 @@ compute dtype.  beta and log f stay fp32.  The oracle reads the rounded values
 (upcast to fp64), so both sides consume identical numbers.
 
 Workloads (stand-ins for the 760M-parameter, 4K-context language-model setting
-and the 16K/32K length-extrapolation setting of "Resumo Técnico: Atenção PaTH",
+and the 16K-64K length-extrapolation setting of "Resumo Técnico: Atenção PaTH",
 §4 "Modelagem de Linguagem (760M Parâmetros)"; no dataset or trained weight is
 used):
 
@@ -19,10 +19,14 @@ small_bf16         B2 H4 L1024 d64 bf16; beta = 2 sigmoid(N(0, std 2)), 5% of
 path760m_bf16      B8 H12 L4096 d128 bf16 (hidden 1536); beta = 2 sigmoid(N(0,1));
                    seed 2 — the headline forward workload
 fox16k_bf16        B1 H12 L16384 d128 bf16 + log f = logsigmoid(N(3,1)); seed 3
+fox64k_bf16        B1 H12 L65536 d128 bf16 + log f = logsigmoid(N(3,1)); seed 5
 decode32k_bf16     B64 H12 d128 bf16; cache of 32768 Gaussian (already
                    transported) keys and values; 256 steps, each with fresh
                    q, k, v ~ N(0,1), unit w_t, beta_t = 2 sigmoid(N(0,1)); seed 4
 =================  ==============================================================
+
+ggd_bam_bias() draws the per-head relative-position tables of the GGD-BAM prior used
+with path_attn_fwd_relbias (the bias is an input of that call, like log f).
 """
 from __future__ import annotations
 
@@ -99,6 +103,19 @@ FWD_CONFIGS = {
 DECODE_CONFIGS = {
     "decode32k_bf16": DecodeConfig("decode32k_bf16", 64, 12, 128, 32768, 256, "bf16", 4),
 }
+
+
+def ggd_bam_bias(H: int, L: int, seed: int) -> torch.Tensor:
+    """Per-head relative-position bias table [H, L] (fp32): entry (h, delta) is the GGD-BAM prior
+    -|(j - i - mu_h) / alpha_h|^p_h at distance delta = i - j ("Resumo Técnico: Mecanismo de Atenção
+    Bayesiana (BAM)", §"Solução Proposta: GGD-BAM").  Seeded per-head parameters: mu = 0, alpha_h
+    log-uniform in [16, 512], p_h uniform in [0.5, 1.5] (heavy- to light-tailed around the Laplace /
+    ALiBi case p = 1)."""
+    g = _gen(seed)
+    alpha = torch.exp(math.log(16.0) + (math.log(512.0) - math.log(16.0)) * torch.rand(H, generator=g, dtype=torch.float64))
+    p = 0.5 + torch.rand(H, generator=g, dtype=torch.float64)
+    delta = torch.arange(L, dtype=torch.float64)
+    return (-(delta.view(1, L) / alpha.view(H, 1)).abs() ** p.view(H, 1)).float().contiguous()
 
 
 def _gen(seed: int) -> torch.Generator:

@@ -280,6 +280,13 @@ def run_ours(args, rank, world, local):
                          "achieved": achieved, "peak": bf16_tf, "unit": "TFLOP/s", "frac": achieved / bf16_tf,
                          "peak_source": peak_src + " bf16 burst", "traffic": _traffic("path_fwd_tc", fc.B * fc.H),
                          "flops_per_launch": attn_flops, "flops_kind": "attention-equivalent 4*B*H*d*L^2/2"}
+    # the scan's actual tensor-core work, for context: per (query tile, earlier key block) pair
+    # [S_k | S_w] = q~ [khat; W]^T, q~ += S_w (-U), O += P V (8 * 128^2 * d); per diagonal tile
+    # S = Q K^T + Y (-Z)^T and O = P V (2 * 128^2 * (2 d + 128))
+    nt = -(-fc.L // 128)
+    tensor_flops = fc.B * fc.H * (nt * (nt - 1) // 2 * 8 * 128 * 128 * fc.d + nt * 2 * 128 * 128 * (2 * fc.d + 128))
+    lines["roofline"]["tensor_flops_per_launch"] = float(tensor_flops)
+    lines["roofline"]["tensor_frac"] = tensor_flops / (fk * 1e-3) / 1e12 / bf16_tf
     dec_obj = None
     if Td:
         # algorithmic bytes per decode step: K read + K write + V read of every cached row
@@ -355,6 +362,27 @@ def run_ours(args, rank, world, local):
                                 % (fxc.B, fxc.H, fxc.L, fxc.d)}
         del fargs, fo, fws
 
+    # PaTH + GGD-BAM relative-position prior on the forward workload (side measurement)
+    relb = None
+    if args.fox_steps > 0:
+        rel = inputs.ggd_bam_bias(fc.H, fc.L, seed=fc.seed).to(dev)
+        ws_r = P.alloc_workspace(P.path_attn_workspace_bytes(fc.B, fc.H, fc.L, fc.d, q.dtype), dev)
+        o_r = torch.empty_like(q)
+        for _ in range(2):
+            P.path_attn_fwd_relbias(q, k, v, w, beta, rel, scale=x.scale, out=o_r, workspace=ws_r)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.fox_steps):
+            P.path_attn_fwd_relbias(q, k, v, w, beta, rel, scale=x.scale, out=o_r, workspace=ws_r)
+        b.record()
+        torch.cuda.synchronize()
+        rms = a.elapsed_time(b) / args.fox_steps
+        relb = {"ms": rms, "attn_equiv_tflops": fc.attn_flops / (rms * 1e-3) / 1e12, "steps": args.fox_steps,
+                "workload": "PaTH + GGD-BAM relative-position bias, B%d H%d L%d d%d bf16" % (fc.B, fc.H, fc.L, fc.d)}
+        del rel, ws_r, o_r
+
     # prefill -> decode hand-off on the forward workload (timed separately, not part of the step)
     prefill = None
     if args.prefill_steps > 0:
@@ -390,7 +418,7 @@ def run_ours(args, rank, world, local):
                        "seq_len": fc.L, "parallelism": "replicas (b,h)-independent" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (forward 384 MiB of q,k,v,w; decode caches 13 GB)"},
             "fwd_ms": fwd_ms_max / args.steps, "fwd_kernel_ms": fk,
-            "decode": dec_obj, "prefill_kcache": prefill, "fox16k": fox.get("fox16k"), "fox64k": fox.get("fox64k"), "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "decode": dec_obj, "prefill_kcache": prefill, "fox16k": fox.get("fox16k"), "fox64k": fox.get("fox64k"), "relbias_ggd": relb, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps}
     if rank == 0:
         print(json.dumps(line))

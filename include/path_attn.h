@@ -109,6 +109,23 @@ int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w
                       path_stream_t stream);
 
 /*
+ * PaTH forward with a relative-position bias: as path_attn_fwd, with
+ * rel_bias[h*L + (i - j)] added unscaled to the scaled logit of (i, j).  This
+ * is the additive positional prior of "Resumo Técnico: Mecanismo de Atenção
+ * Bayesiana (BAM)", §"Solução Proposta: GGD-BAM" (b_ij = -|(j - i - mu)/alpha|^p,
+ * a function of i - j with per-head parameters), or ALiBi's -slope (i - j),
+ * applied on top of the PaTH logits.
+ *   rel_bias : [H, L] float, device, shared by every batch entry; entry
+ *              (h, delta) is the bias at distance delta = i - j.  Values must
+ *              be finite (not checked).
+ * Everything else as path_attn_fwd (same workspace size).
+ */
+int path_attn_fwd_relbias(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                          const float* rel_bias, void* o, float* lse, int B, int H, int L, int d, int dtype,
+                          int causal, float scale, void* workspace, size_t workspace_bytes,
+                          path_stream_t stream);
+
+/*
  * Workspace size in bytes for path_decode_step (split-K partial results and a
  * status word) for caches of capacity n_max.  Returns 0 for unsupported sizes.
  */

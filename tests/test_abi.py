@@ -74,6 +74,15 @@ def test_forward_argument_errors(lib):
     fox = lib.path_attn_fwd_fox(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 1, 64, 16, P.PATH_F32, 1,
                                 ctypes.c_float(0.25), FAKE, 1 << 30, None)
     assert fox == P.PATH_ERR_INVALID  # log_f is required
+    rel = lib.path_attn_fwd_relbias(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 1, 64, 16, P.PATH_F32, 1,
+                                    ctypes.c_float(0.25), FAKE, 1 << 30, None)
+    assert rel == P.PATH_ERR_INVALID  # rel_bias is required
+    rel = lib.path_attn_fwd_relbias(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.c_void_p((1 << 20) + 8), FAKE, None, 1, 1,
+                                    64, 16, P.PATH_F32, 1, ctypes.c_float(0.25), FAKE, 1 << 30, None)
+    assert rel == P.PATH_ERR_INVALID  # misaligned table
+    rel = lib.path_attn_fwd_relbias(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 1, 1, 64, 16, P.PATH_F32, 0,
+                                    ctypes.c_float(0.25), FAKE, 1 << 30, None)
+    assert rel == P.PATH_ERR_UNSUPPORTED  # non-causal
 
 
 def test_decode_argument_errors(lib):

@@ -191,3 +191,59 @@ def test_alibi_as_constant_forget_gate(dtype, d, beta_zero):
         o_ref, lse_ref = _oracle(x)
         check(to_np(o), o_ref, x.q.dtype, "PaTH + alibi")
         check_lse(to_np(lse), lse_ref, x.q.dtype, "PaTH + alibi")
+
+
+def _relbias_case(x, rel):
+    """GPU relative-bias forward against the oracle (table expanded over the batch)."""
+    args = [cuda(t) for t in (x.q, x.k, x.v, x.w, x.beta)]
+    o, lse = P.path_attn_fwd_relbias(*args, cuda(rel), scale=x.scale, lse=True)
+    torch.cuda.synchronize()
+    B = x.q.shape[0]
+    f = inputs.f64
+    rb = np.broadcast_to(f(rel)[None], x.beta.shape).copy()
+    return o, lse, rb
+
+
+@pytest.mark.parametrize("dtype,B,H,L,d", [("bf16", 2, 3, 300, 128), ("bf16", 1, 2, 129, 64), ("bf16", 1, 1, 1, 128),
+                                           ("f32", 1, 2, 150, 32), ("f32", 2, 1, 77, 64)])
+def test_relbias_ggd_bam_vs_oracle(dtype, B, H, L, d):
+    """PaTH + GGD-BAM relative-position prior (random beta, ragged L) against the oracle."""
+    x = inputs.make_fwd(B, H, L, d, dtype, seed=91 + L, edge_frac=0.05)
+    rel = inputs.ggd_bam_bias(H, L, seed=91)
+    o, lse, rb = _relbias_case(x, rel)
+    f = inputs.f64
+    o_ref, lse_ref = orc.path_attn(f(x.q), f(x.k), f(x.v), f(x.w), f(x.beta), scale=x.scale, rel_bias=rb)
+    check(to_np(o), o_ref, x.q.dtype, "relbias %s %s" % (dtype, (B, H, L, d)))
+    check_lse(to_np(lse), lse_ref, x.q.dtype, "relbias lse")
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
+def test_relbias_with_beta_zero_is_textbook_ggd_bam(dtype, d):
+    """beta = 0: plain softmax attention with the GGD-BAM bias matrix (fp64 SDPA, independent of the
+    PaTH oracle)."""
+    B, H, L = 1, 3, 600
+    x = inputs.make_fwd(B, H, L, d, dtype, seed=92)
+    x.beta.zero_()
+    rel = inputs.ggd_bam_bias(H, L, seed=92)
+    o, _, _ = _relbias_case(x, rel)
+    i = torch.arange(L)
+    delta = (i.view(L, 1) - i.view(1, L)).clamp(min=0)
+    bias = torch.where(i.view(L, 1) >= i.view(1, L), rel.double()[:, delta], torch.tensor(float("-inf"), dtype=torch.float64))
+    ref = torch.nn.functional.scaled_dot_product_attention(*(t.double() for t in (x.q, x.k, x.v)),
+                                                           attn_mask=bias.unsqueeze(0), scale=x.scale)
+    check(to_np(o), ref.numpy(), x.q.dtype, "ggd-bam beta=0 %s" % dtype)
+
+
+def test_relbias_linear_table_equals_fox_constant_gates():
+    """An ALiBi table -slope * delta through the relative-bias path equals constant forget gates through
+    the FoX path (two kernels, one operator)."""
+    B, H, L, d = 1, 2, 520, 128
+    x = inputs.make_fwd(B, H, L, d, "bf16", seed=93)
+    slopes = torch.tensor([0.01, 0.05])
+    rel = (-slopes.view(H, 1) * torch.arange(L, dtype=torch.float32).view(1, L)).contiguous()
+    o1, _, _ = _relbias_case(x, rel)
+    args = [cuda(t) for t in (x.q, x.k, x.v, x.w, x.beta)]
+    lf = (-slopes).view(1, H, 1).expand(B, H, L).contiguous().float()
+    o2 = P.path_attn_fwd_fox(*args, cuda(lf), scale=x.scale)
+    torch.cuda.synchronize()
+    assert float((o1.float() - o2.float()).abs().max()) <= 2e-2
