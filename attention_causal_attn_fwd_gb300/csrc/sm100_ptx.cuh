@@ -95,6 +95,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     return mbar_wait_slow(bar, parity, c, site);
 }
 
+// For waits off the critical path that may last long (a thread with nothing
+// else to do): suspending try_wait leaves the scheduler's issue slots to the
+// other warps, at the price of a few hundred cycles of wake-up latency.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtl& c, int site) {
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*c.abort) return false;
+        if (globaltimer() - t0 > c.limit_ns) {
+            report_status(c.hdr, PATH_ERR_TIMEOUT, site);
+            *c.abort = 1;
+            __threadfence_block();
+            return false;
+        }
+    }
+}
+
 // ----------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
                                             int z) {

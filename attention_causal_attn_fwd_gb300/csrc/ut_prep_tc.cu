@@ -57,8 +57,13 @@ static_assert(RS % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte bounda
 constexpr uint32_t TOTAL = RS + 32768;
 constexpr size_t kSmem = TOTAL + 1024;
 constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
-enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN, B_COUNT };
-static_assert(B_COUNT * 8 <= 128, "barriers overlap the TMEM slot and abort flag at +128");
+// B_STG*: a workspace-store group is staged (compute warps); B_FREE*: its
+// tiles have been read by the bulk stores (store thread).  Groups: 0 -U, Y;
+// 1 -Z, qhat columns 0-31 of each half; 2 qhat 32-63 (d = 128); last khat.
+enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN,
+       B_STG0, B_STG1, B_STG2, B_STG3, B_FREE0, B_FREE1, B_FREE2, B_FREE3, B_COUNT };
+constexpr uint32_t RB_SLOT = 200;  // TMEM address and abort flag after the barriers
+static_assert(B_COUNT * 8 <= RB_SLOT && RB_SLOT + 8 <= 256, "barriers overlap the TMEM slot, abort flag or beta");
 }  // namespace utk
 
 // Phase timestamps of one CTA in the middle of the grid (SM cycle counter),
@@ -303,8 +308,8 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     auto bar = [&](int i) { return sb + RB + 8u * (uint32_t)i; };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + RB + 128);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + RB + 132);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + RB + RB_SLOT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + RB + RB_SLOT + 4);
     float* sBeta = reinterpret_cast<float*>(sm + RB + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -313,7 +318,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     if (chunk == 0 && bh == 0 && threadIdx.x == 0) p.hdr->status = 0;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || i == B_OPS4) ? kCompute : 1);
+        for (int i = 0; i < B_COUNT; ++i)
+            mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || i == B_OPS4 || (i >= B_STG0 && i <= B_STG3))
+                                  ? kCompute : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -337,6 +344,30 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 tma_load_3d(sb + R2 + c * 16384, &tm_k, bar(B_LOAD), c * 64, row0, bh);
             }
             drain_wait(bar(B_LOAD), 0, p.limit_ns);
+            // Workspace stores: this thread issues each group once the compute
+            // warps have staged it and frees its tiles once the stores have read
+            // them, so no compute thread waits on a bulk store.
+            constexpr int kGroups = D == 128 ? 4 : 3;
+            bool ok = true;
+            for (int g = 0; g < kGroups && ok; ++g) {
+                if (!(ok = mbar_wait_sleep(bar(B_STG0 + g), 0, wc, 45 + g))) break;
+                if (g == 0) {
+                    for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_un, sb + RS + b * 16384, 64 * b, row0, bh);
+                    for (int b = 0; b < 2; ++b) tma_store_3d(&tm_y, sb + R3 + b * 16384, 64 * b, row0, bh);
+                } else if (g == 1 || (D == 128 && g == 2)) {
+                    const int c = g - 1;  // qhat columns 32c .. 32c+31 of each half
+                    for (int b = 0; b < 2; ++b)
+                        tma_store_3d(&tm_qhat, sb + RS + b * 16384, (D / 2) * b + 32 * c, row0, bh);
+                    if (g == 1)
+                        for (int b = 0; b < 2; ++b) tma_store_3d(&tm_zn, sb + R3 + b * 16384, 64 * b, row0, bh);
+                } else {
+                    for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_khat, sb + RS + b * 16384, 64 * b, row0, bh);
+                }
+                bulk_commit();
+                bulk_wait_read0();
+                mbar_arrive(bar(B_FREE0 + g));
+            }
+            bulk_wait0();  // the workspace stores have landed before the CTA exits
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -561,13 +592,8 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_OPS2));
+            mbar_arrive(bar(B_STG0));  // -U and Y tiles -> workspace
             if (t == 0) UT_TRACE(6);
-            named_bar_sync(1, kCompute);
-            if (t == 0) {  // -U and Y tiles -> workspace
-                for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_un, sb + RS + b * 16384, 64 * b, row0, bh);
-                for (int b = 0; b < 2; ++b) tma_store_3d(&tm_y, sb + R3 + b * 16384, 64 * b, row0, bh);
-                bulk_commit();
-            }
         }
         // This thread's half of the Q row, loaded while Y W runs on the tensor cores.
         uint4 qpre[D / 16];
@@ -582,8 +608,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         if (ok) {
             tc_fence_after();
             // the -U and Y stores have read their tiles before R3 and RS are rewritten
-            if (t == 0) bulk_wait_read0();
-            named_bar_sync(1, kCompute);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE0), 0, wc, 55));
+        }
+        if (ok) {
             // Z = triu_1(K W^T) -> hi/lo operand, negated: its hi part is the bf16 -Z
             // output, Z A comes out as -(Z A) and (Z A) W as -(Z A) W
 #pragma unroll
@@ -628,22 +655,16 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                                                                  __float_as_uint(q8[6]), __float_as_uint(q8[7])));
                 }
                 fence_proxy_async_smem();
-                named_bar_sync(1, kCompute);
-                if (t == 0) {
-                    for (int b = 0; b < 2; ++b) tma_store_3d(&tm_qhat, sb + RS + b * 16384, (D / 2) * b + 32 * c, row0, bh);
-                    if (c == 0) for (int b = 0; b < 2; ++b) tma_store_3d(&tm_zn, sb + R3 + b * 16384, 64 * b, row0, bh);
-                    bulk_commit();
-                    if (c + 1 < D / 64) bulk_wait_read0();
-                }
-                if (c + 1 < D / 64) named_bar_sync(1, kCompute);
+                mbar_arrive(bar(B_STG1 + c));  // (c = 0 with the -Z tile)
+                if (c + 1 < D / 64 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE1 + c), 0, wc, 56)))) break;
             }
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ZA), 0, wc, 53));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ZA), 0, wc, 53));
             if (t == 0) UT_TRACE(9);
         }
+        // the -Z store (group 1) has read R3 before -(Z A) is written there
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE1), 0, wc, 57));
         if (ok) {
             tc_fence_after();
-            if (t == 0) bulk_wait_read0();  // the -Z and qhat stores have read R3 and RS
-            named_bar_sync(1, kCompute);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {  // -(Z A) -> hi/lo operand
                 uint32_t v[32];
@@ -673,6 +694,8 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_K), 0, wc, 54));
         if (t == 0) UT_TRACE(11);
+        // the last qhat store has read the staging tile before khat is staged there
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE0 + D / 64), 0, wc, 58));
         if (ok) {
             tc_fence_after();
             float n2 = 0.f;  // this thread's part of |khat_row|^2
@@ -696,11 +719,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            named_bar_sync(1, kCompute);
-            if (t == 0) {
-                for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_khat, sb + RS + b * 16384, 64 * b, row0, bh);
-                bulk_commit();
-            }
+            mbar_arrive(bar(B_STG1 + D / 64));  // khat tile -> workspace
             if (p.kmax2) {  // chunk max of |khat|^2 over rows < L (the solve temp is free)
                 float* red = reinterpret_cast<float*>(sm + RT);
                 red[r + 128 * h] = grow < p.L ? n2 : 0.f;
@@ -717,10 +736,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         }
     }
 
-    if (threadIdx.x == 64) {
-        bulk_wait0();  // the workspace stores have landed (and read their tiles) before exit
-        UT_TRACE(12);
-    }
+    if (threadIdx.x == 64) UT_TRACE(12);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
