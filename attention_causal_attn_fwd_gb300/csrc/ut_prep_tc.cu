@@ -58,8 +58,10 @@ constexpr uint32_t TOTAL = RS + 32768;
 constexpr size_t kSmem = TOTAL + 1024;
 constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 // B_STG*: a workspace-store group is staged (compute warps); B_FREE*: its
-// tiles have been read by the bulk stores (store thread).  Groups: 0 -U, Y;
-// 1 -Z, qhat columns 0-31 of each half; 2 qhat 32-63 (d = 128); last khat.
+// tiles have been read by the bulk stores (store thread).  Groups: 0 -U
+// (staging tile), Y (R3); 1 -Z (R3), qhat columns 0-31 of each half (staging
+// tile); 2 qhat columns 32-63 (d = 128; R1, free once Z A has completed);
+// last khat (R2, likewise free).
 enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN,
        B_STG0, B_STG1, B_STG2, B_STG3, B_FREE0, B_FREE1, B_FREE2, B_FREE3, B_COUNT };
 constexpr uint32_t RB_SLOT = 200;  // TMEM address and abort flag after the barriers
@@ -356,12 +358,13 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     for (int b = 0; b < 2; ++b) tma_store_3d(&tm_y, sb + R3 + b * 16384, 64 * b, row0, bh);
                 } else if (g == 1 || (D == 128 && g == 2)) {
                     const int c = g - 1;  // qhat columns 32c .. 32c+31 of each half
+                    const uint32_t src = sb + (c == 0 ? RS : R1);
                     for (int b = 0; b < 2; ++b)
-                        tma_store_3d(&tm_qhat, sb + RS + b * 16384, (D / 2) * b + 32 * c, row0, bh);
+                        tma_store_3d(&tm_qhat, src + b * 16384, (D / 2) * b + 32 * c, row0, bh);
                     if (g == 1)
                         for (int b = 0; b < 2; ++b) tma_store_3d(&tm_zn, sb + R3 + b * 16384, 64 * b, row0, bh);
                 } else {
-                    for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_khat, sb + RS + b * 16384, 64 * b, row0, bh);
+                    for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_khat, sb + R2 + b * 16384, 64 * b, row0, bh);
                 }
                 bulk_commit();
                 bulk_wait_read0();
@@ -603,6 +606,26 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             for (int i = 0; i < D / 16; ++i)
                 qpre[i] = (ok && grow < p.L) ? ld_global_nc_v4(qrow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
         }
+        // qhat = Q - Y W (fp32, Y W in TMEM at T384), columns 32c .. 32c+31 of this
+        // thread's half, into a staging tile laid out as two 32-column boxes
+        auto stage_qhat = [&](int c, uint8_t* dst) {
+            uint32_t v[32];
+            const int col = (D / 2) * h + 32 * c;
+            tmem_ld32(tl + T384 + col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                Vec16<__nv_bfloat16> qv;
+                qv.raw = qpre[4 * c + g];
+                float q8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q8[e] = qv.get(e) - __uint_as_float(v[8 * g + e]);
+                stage16(dst, r, h, 2 * g, make_uint4(__float_as_uint(q8[0]), __float_as_uint(q8[1]),
+                                                     __float_as_uint(q8[2]), __float_as_uint(q8[3])));
+                stage16(dst, r, h, 2 * g + 1, make_uint4(__float_as_uint(q8[4]), __float_as_uint(q8[5]),
+                                                         __float_as_uint(q8[6]), __float_as_uint(q8[7])));
+            }
+        };
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_Q), 0, wc, 52));
         if (t == 0) UT_TRACE(7);
         if (ok) {
@@ -634,30 +657,11 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(B_OPS3));
             if (t == 0) UT_TRACE(8);
-            // qhat = Q - Y W (fp32) through the staging tile, 32 columns of each
-            // half per round, while Z A runs
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                uint32_t v[32];
-                const int col = (D / 2) * h + 32 * c;
-                tmem_ld32(tl + T384 + col, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    Vec16<__nv_bfloat16> qv;
-                    qv.raw = qpre[4 * c + g];
-                    float q8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) q8[e] = qv.get(e) - __uint_as_float(v[8 * g + e]);
-                    stage16(sm + RS, r, h, 2 * g, make_uint4(__float_as_uint(q8[0]), __float_as_uint(q8[1]),
-                                                             __float_as_uint(q8[2]), __float_as_uint(q8[3])));
-                    stage16(sm + RS, r, h, 2 * g + 1, make_uint4(__float_as_uint(q8[4]), __float_as_uint(q8[5]),
-                                                                 __float_as_uint(q8[6]), __float_as_uint(q8[7])));
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(bar(B_STG1 + c));  // (c = 0 with the -Z tile)
-                if (c + 1 < D / 64 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE1 + c), 0, wc, 56)))) break;
-            }
+            // qhat = Q - Y W (fp32), columns 0-31 of each half, into the staging
+            // tile while Z A runs (columns 32-63 follow once Z A has freed R1)
+            stage_qhat(0, sm + RS);
+            fence_proxy_async_smem();
+            mbar_arrive(bar(B_STG1));  // with the -Z tile
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ZA), 0, wc, 53));
             if (t == 0) UT_TRACE(9);
         }
@@ -683,6 +687,11 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(B_OPS4));
             if (t == 0) UT_TRACE(10);
+            if (D == 128) {  // qhat columns 32-63 of each half into R1 (A is dead after Z A) while (Z A) W runs
+                stage_qhat(1, sm + R1);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(B_STG2));
+            }
         }
         // This thread's half of the K row, loaded while (Z A) W runs.
         uint4 kpre[D / 16];
@@ -694,8 +703,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_K), 0, wc, 54));
         if (t == 0) UT_TRACE(11);
-        // the last qhat store has read the staging tile before khat is staged there
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE0 + D / 64), 0, wc, 58));
+
         if (ok) {
             tc_fence_after();
             float n2 = 0.f;  // this thread's part of |khat_row|^2
@@ -715,11 +723,11 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                         k8[e] = kv.get(e) + __uint_as_float(v[8 * g + e]);
                         n2 = fmaf(k8[e], k8[e], n2);
                     }
-                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(k8));
+                    stage16(sm + R2, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(k8));
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_STG1 + D / 64));  // khat tile -> workspace
+            mbar_arrive(bar(B_STG1 + D / 64));  // khat tile (R2, free since Z A) -> workspace
             if (p.kmax2) {  // chunk max of |khat|^2 over rows < L (the solve temp is free)
                 float* red = reinterpret_cast<float*>(sm + RT);
                 red[r + 128 * h] = grow < p.L ? n2 : 0.f;
