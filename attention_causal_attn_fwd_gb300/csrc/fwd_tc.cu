@@ -73,11 +73,17 @@ static_assert(SM_CTL + 52 <= SM_TOTAL, "control words exceed the barrier region"
 
 constexpr int kHeadGroup = 8;
 
-// Phase timestamps of CTA 0 (SM cycle counter), compiled in only for
-// instrumented builds (-DPATH_TRACE): slot s of block iteration it.
+// Phase timestamps of one CTA (SM cycle counter), compiled in only for
+// instrumented builds (-DPATH_TRACE): slot s of block iteration it.  CTA 773
+// is a 32-block tile of the fourth head group at L = 4096 (a later wave, so
+// its code is warm in the instruction cache).
+#ifndef PATH_TRACE_CTA
+#define PATH_TRACE_CTA 773
+#endif
+constexpr int kTraceCta = PATH_TRACE_CTA;
 #ifdef PATH_TRACE
 #define TC_TRACE(slot, it) \
-    do { if (p.trace && blockIdx.x == 0 && (it) < 64) p.trace[(it) * 32 + (slot)] = clock64(); } while (0)
+    do { if (p.trace && blockIdx.x == kTraceCta && (it) < 64) p.trace[(it) * 32 + (slot)] = clock64(); } while (0)
 #else
 #define TC_TRACE(slot, it) do { } while (0)
 #endif
