@@ -611,17 +611,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             return __all_sync(0xffffffffu, mbar_wait(bar((blk & 1) ? B_WFULL1 : B_WFULL0),
                                                      (uint32_t)((blk >> 1) & 1), wc, 35));
         };
+        // This row of qhat (fp32), the initial q~: every load is issued before
+        // the wait for the diagonal, so their latency hides behind it (issued
+        // chunk by chunk between the TMEM stores, the loads were serialised).
+        float4 qh[D / 4];
+        if (n > 0) {
+            const float4* src = reinterpret_cast<const float4*>(p.qhat + ((size_t)bh * p.Lp + row0 + r) * D);
+#pragma unroll
+            for (int i = 0; i < D / 4; ++i) qh[i] = __ldg(src + i);
+        }
         bool ok = n > 0 && __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), 0, wc, 30));
         if (ok) {
-            // the diagonal MMA has consumed Q: load qhat (fp32) as the initial q~
+            // the diagonal MMA has consumed Q: qhat becomes the fp32 master and its bf16 copy
             tc_fence_after();
-            const float4* src = reinterpret_cast<const float4*>(p.qhat + ((size_t)bh * p.Lp + row0 + r) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 x = __ldg(src + 8 * c + j4);
+                    const float4 x = qh[8 * c + j4];
                     v[4 * j4 + 0] = __float_as_uint(x.x);
                     v[4 * j4 + 1] = __float_as_uint(x.y);
                     v[4 * j4 + 2] = __float_as_uint(x.z);
