@@ -404,13 +404,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float qn2 = 0.f;
             if (row0 + r < p.L) {
                 const uint4* qv = reinterpret_cast<const uint4*>(p.q + ((size_t)bh * p.L + row0 + r) * D);
-#pragma unroll 4
-                for (int g = 0; g < D / 8; ++g) {
-                    Vec16<__nv_bfloat16> v;
-                    v.raw = __ldg(qv + g);
+                Vec16<__nv_bfloat16> v[D / 8];  // every load in flight before the first use
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) qn2 = fmaf(v.get(e), v.get(e), qn2);
-                }
+                for (int g = 0; g < D / 8; ++g) v[g].raw = __ldg(qv + g);
+#pragma unroll
+                for (int g = 0; g < D / 8; ++g)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qn2 = fmaf(v[g].get(e), v[g].get(e), qn2);
             }
             named_bar_sync(2, 128);
             // |q~_i . khat_j| <= |q_i| |khat_j|: the transitions are non-expansive for
