@@ -42,7 +42,7 @@ __device__ __forceinline__ Vec16<T> transport(const Vec16<T>& kv, const float* w
 }
 
 constexpr int kDecNT = 256;
-constexpr int kDecUnroll = 6;
+constexpr int kDecUnroll = 8;
 
 // grid (splits, B*H).  Split s covers cache rows [s*R, min((s+1)*R, n_cached+1));
 // row n_cached is the new token.  Writes per-split (m, l, o) in log2 units.
