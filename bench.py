@@ -303,34 +303,66 @@ def run_ours(args, rank, world, local):
                                 "bytes_per_launch": avg_bytes},
                    "step_gbs": avg_bytes / (us_per_step * 1e-6) / 1e9}
 
-    # end to end through the public API with host buffers: pinned inputs -> device, forward, o -> host
+    # end to end through the public API with host buffers: pinned inputs -> device, forward, o -> host,
+    # every step.  Copies run on their own stream into double-buffered device inputs, so the next
+    # step's inputs cross while this step computes (the order per step is still copy in -> forward
+    # -> copy out, enforced with events).
     e2e = None
     if args.e2e_steps > 0:
         hq, hk, hv, hw = (t.pin_memory() for t in (x.q, x.k, x.v, x.w))
         hb = x.beta.pin_memory()
-        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        dq_, dk_, dv_, dw_, db_ = (torch.empty_like(t) for t in (q, k, v, w, beta))
+        hos = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+        dins = [[torch.empty_like(t) for t in (q, k, v, w, beta)] for _ in range(2)]
+        douts = [torch.empty_like(o) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hw, hb))
-        d2h = ho.numel() * ho.element_size()
+        d2h = hos[0].numel() * hos[0].element_size()
+        comp = torch.cuda.current_stream()
+        # one stream per input tensor (the copy engines run in parallel; beta rides with w) and
+        # one for the result
+        cps = [torch.cuda.Stream() for _ in range(4)]
+        out_s = torch.cuda.Stream()
+        freed = [torch.cuda.Event(), torch.cuda.Event()]   # forward done with buffer i
+        done = [torch.cuda.Event(), torch.cuda.Event()]    # output of buffer i written
+        read = [torch.cuda.Event(), torch.cuda.Event()]    # output of buffer i copied to the host
+        srcs = (hq, hk, hv, hw, hb)
 
-        def e2e_step():
-            for dst, src in ((dq_, hq), (dk_, hk), (dv_, hv), (dw_, hw), (db_, hb)):
-                dst.copy_(src, non_blocking=True)
-            P.path_attn_fwd(dq_, dk_, dv_, dw_, db_, scale=x.scale, out=o, workspace=ws_f)
-            ho.copy_(o, non_blocking=True)
+        def run_e2e(nsteps):
+            for sidx in range(nsteps):
+                i = sidx % 2
+                for j, dst in enumerate(dins[i]):
+                    cs = cps[min(j, 3)]
+                    cs.wait_event(freed[i])
+                    with torch.cuda.stream(cs):
+                        dst.copy_(srcs[j], non_blocking=True)
+                for cs in cps:
+                    comp.wait_stream(cs)
+                comp.wait_event(read[i])  # the previous copy-out of this output buffer has finished
+                P.path_attn_fwd(*dins[i], scale=x.scale, out=douts[i], workspace=ws_f)
+                freed[i].record(comp)
+                done[i].record(comp)
+                out_s.wait_event(done[i])
+                with torch.cuda.stream(out_s):
+                    hos[i].copy_(douts[i], non_blocking=True)
+                read[i].record(out_s)
+            comp.wait_stream(out_s)
 
-        e2e_step()
+        for ev in freed + read:
+            ev.record(comp)
+        run_e2e(2)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        b.record()
+        a.record(comp)
+        for cs in cps + [out_s]:
+            cs.wait_event(a)
+        run_e2e(args.e2e_steps)
+        b.record(comp)
         torch.cuda.synchronize()
         ms = max_over_ranks(a.elapsed_time(b), world)
         e2e = {"value": attn_flops * world * args.e2e_steps / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "overlap": "input copies on four streams and the result copy on a fifth, double-buffered: "
+                          "step s+1's inputs cross during step s"}
 
     # PaTH-FoX forwards at L=16384 and L=65536 (far blocks skipped exactly), timed separately,
     # not part of the step
@@ -432,7 +464,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=256)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--fox-steps", type=int, default=3)
     ap.add_argument("--cpu-heads", type=int, default=96)
