@@ -243,10 +243,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             // copies still in flight must land before the CTA exits
-            drain_wait(bar(B_QFULL), 0, p.limit_ns);
+            drain_wait(bar(B_QFULL), 0, p.limit_ns, p.hdr, 90);
             const int ful[6] = {B_WFULL0, B_KFULL, B_UFULL, B_VFULL0, B_VFULL1, B_WFULL1};
             for (int sl = 0; sl < 6; ++sl)
-                if (issued[sl] > 0) drain_wait(bar(ful[sl]), (uint32_t)((issued[sl] - 1) & 1), p.limit_ns);
+                if (issued[sl] > 0) drain_wait(bar(ful[sl]), (uint32_t)((issued[sl] - 1) & 1), p.limit_ns, p.hdr, 91);
         }
     } else if (warp == 1 || warp == 10) {
         // ------------------------------------------------------------------ MMA issuers
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // every MMA this thread issued completes before TMEM is released
             const int drain = (FOX || issuer_a) ? B_DRAIN : B_DRAIN2;
             mma_commit(bar(drain));
-            drain_wait(bar(drain), 0, p.limit_ns);
+            drain_wait(bar(drain), 0, p.limit_ns, p.hdr, 92);
         }
     } else if (warp < 6) {
         // ------------------------------------------------------------------ softmax warps

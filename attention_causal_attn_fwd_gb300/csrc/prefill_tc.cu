@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(pfk::kThreads, 1)
             // copies still in flight must land before the CTA exits
             const int ful[3] = {B_VFULL, B_WFULL, B_KFULL};
             for (int i = 0; i < 3; ++i)
-                if (issued[i] > 0) drain_wait(bar(ful[i]), (uint32_t)((issued[i] - 1) & 1), p.limit_ns);
+                if (issued[i] > 0) drain_wait(bar(ful[i]), (uint32_t)((issued[i] - 1) & 1), p.limit_ns, p.hdr, 95);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(pfk::kThreads, 1)
             }
             // every issued MMA completes before TMEM is released
             mma_commit(bar(B_DRAIN));
-            drain_wait(bar(B_DRAIN), 0, p.limit_ns);
+            drain_wait(bar(B_DRAIN), 0, p.limit_ns, p.hdr, 96);
         }
     } else {
         // ------------------------------------------------------------------ conversion warps

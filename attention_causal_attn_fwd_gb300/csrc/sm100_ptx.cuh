@@ -203,11 +203,18 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
     return sdesc_sw128(base + (uint32_t)kk * 2048u, 16384, 1024);
 }
 
-// Drain wait used after an abort: bounded, ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit) {
+// Drain wait before a CTA releases TMEM or exits (copies and MMAs in flight
+// must land): bounded, ignores the abort flag.  An expiry is recorded as
+// PATH_ERR_TIMEOUT (site) unless an earlier error is already recorded, so a
+// drain that waits on a phase that never completes cannot pass unnoticed.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned long long limit, WsHeader* hdr,
+                                           int site) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > limit) break;
+        if (globaltimer() - t0 > limit) {
+            report_status(hdr, PATH_ERR_TIMEOUT, site);
+            break;
+        }
 }
 
 // D[tmem] (+)= A[smem] * B[smem]

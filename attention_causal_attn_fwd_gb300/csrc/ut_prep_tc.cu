@@ -345,7 +345,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 tma_load_3d(sb + R1 + c * 16384, &tm_q, bar(B_LOAD), c * 64, row0, bh);
                 tma_load_3d(sb + R2 + c * 16384, &tm_k, bar(B_LOAD), c * 64, row0, bh);
             }
-            drain_wait(bar(B_LOAD), 0, p.limit_ns);
+            drain_wait(bar(B_LOAD), 0, p.limit_ns, p.hdr, 98);
             // Workspace stores: this thread issues each group once the compute
             // warps have staged it and frees its tiles once the stores have read
             // them, so no compute thread waits on a bulk store.
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 UT_TRACE(22);
             }
             mma_commit(bar(B_DRAIN));
-            drain_wait(bar(B_DRAIN), 0, p.limit_ns);
+            drain_wait(bar(B_DRAIN), 0, p.limit_ns, p.hdr, 99);
         }
     } else {
         // ---------------------------------------------------------------- compute warps (rows)

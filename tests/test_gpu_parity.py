@@ -16,13 +16,22 @@ from oracle import oracle as orc
 pytestmark = pytest.mark.gpu
 
 
+def _workspace(x: inputs.FwdInputs):
+    B, H, L, d = x.q.shape
+    return P.alloc_workspace(P.path_attn_workspace_bytes(B, H, L, d, x.q.dtype), "cuda")
+
+
 def _gpu_fwd(x: inputs.FwdInputs):
+    """GPU forward through the C ABI; the workspace status word must read PATH_OK afterwards (no
+    bounded wait, including a drain before exit, ran out)."""
     args = [cuda(t) for t in (x.q, x.k, x.v, x.w, x.beta)]
+    ws = _workspace(x)
     if x.log_f is not None:
-        o, lse = P.path_attn_fwd_fox(*args, cuda(x.log_f), scale=x.scale, lse=True)
+        o, lse = P.path_attn_fwd_fox(*args, cuda(x.log_f), scale=x.scale, lse=True, workspace=ws)
     else:
-        o, lse = P.path_attn_fwd(*args, scale=x.scale, lse=True)
+        o, lse = P.path_attn_fwd(*args, scale=x.scale, lse=True, workspace=ws)
     torch.cuda.synchronize()
+    assert P.path_get_status(ws) == P.PATH_OK
     return o, lse
 
 
@@ -196,8 +205,10 @@ def test_alibi_as_constant_forget_gate(dtype, d, beta_zero):
 def _relbias_case(x, rel):
     """GPU relative-bias forward against the oracle (table expanded over the batch)."""
     args = [cuda(t) for t in (x.q, x.k, x.v, x.w, x.beta)]
-    o, lse = P.path_attn_fwd_relbias(*args, cuda(rel), scale=x.scale, lse=True)
+    ws = _workspace(x)
+    o, lse = P.path_attn_fwd_relbias(*args, cuda(rel), scale=x.scale, lse=True, workspace=ws)
     torch.cuda.synchronize()
+    assert P.path_get_status(ws) == P.PATH_OK
     B = x.q.shape[0]
     f = inputs.f64
     rb = np.broadcast_to(f(rel)[None], x.beta.shape).copy()

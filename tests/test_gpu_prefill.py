@@ -42,8 +42,10 @@ def _check_cache(got, ref, dtype, what):
                                            ("bf16", 1, 1, 1500, 128)])
 def test_prefill_kcache_vs_oracle(dtype, B, H, L, d):
     x = inputs.make_fwd(B, H, L, d, dtype, seed=51, edge_frac=0.05)
-    kc = P.path_prefill_kcache(x.k.cuda(), x.w.cuda(), x.beta.cuda(), n_max=L + 5)
+    ws = P.alloc_workspace(P.path_prefill_workspace_bytes(B, H, L, d, x.k.dtype), "cuda")
+    kc = P.path_prefill_kcache(x.k.cuda(), x.w.cuda(), x.beta.cuda(), n_max=L + 5, workspace=ws)
     torch.cuda.synchronize()
+    assert P.path_get_status(ws) == P.PATH_OK
     assert torch.count_nonzero(kc[:, :, L:]) == 0  # rows beyond the prompt untouched
     for b in range(B):
         for h in range(H):
