@@ -3,16 +3,18 @@
 // Blockwise algorithm of "Resumo Técnico: Atenção PaTH"
 // (gist.science/pt/paper/2505.16381), §3 "Algoritmo Estilo FlashAttention":
 // boundary-adjusted queries/keys per chunk (from the UT-prep kernel,
-// ut_prep.cu), then a right-to-left scan over key/value blocks that carries
+// ut_prep_tc.cu), then a right-to-left scan over key/value blocks that carries
 // the Householder product on the query side, never forming the L x L matrix.
 //
 // One CTA owns a tile of 128 queries (= one chunk n of one head) and walks the
 // key/value blocks m = n (diagonal), n-1, ..., 0.  Per block m < n, with the
 // transported query q~ (fp32 master in TMEM, bf16 copy in shared memory):
-//   MMA1  [S_k | S_w] = q~ [khat_m ; W_m]^T          (M=128, N=256, K=d)
+//   S_w   S_w = q~ W_m^T                               (M=128, N=128, K=d)
+//   S_k   S_k = q~ khat_m^T                            (M=128, N=128, K=d)
 //   MMA3  q~ += bf16(S_w) (-U_m)                       (M=128, N=d, K=128)
-//   MMA2  O  += P V_m,  P = exp2(S_k * scale*log2e - m)  (M=128, N=d, K=128)
-// and the diagonal block uses S = Q K^T + Y (-Z)^T with the causal mask.
+//   P V   O  += P V_m,  P = exp2(S_k * scale*log2e - m)  (M=128, N=d, K=128)
+// and the diagonal block uses S = Q K^T + Y (-Z)^T with the causal mask.  The
+// logits may carry an additive bias (MODE 1 PaTH-FoX, MODE 2 relative position).
 // Online softmax keeps one query row per thread (TMEM lane = row), so row
 // max and sum need no cross-thread reduction.  The running max is only
 // raised (and O rescaled) when it grows by more than 2^8, which keeps every
@@ -30,7 +32,7 @@
 // Shared memory (1024-aligned, 128-byte swizzled tiles as TMA writes them):
 //   SM_Q  32 KB  Q (diagonal) then bf16 q~, K-major, 64-column chunks of 16 KB
 //   SM_KW 64 KB  per 64-column chunk c (32 KB): rows 0-127 khat_m (or K),
-//                rows 128-255 W_m (or -Z): one N=256 B operand for MMA1
+//                rows 128-255 W_m of even block iterations (or -Z)
 //   SM_V  64 KB  V_m, MN-major B operand (64-column boxes of 16 KB), two
 //                slots by block parity
 //   SM_U  32 KB  -U_m (MN-major) or, on the diagonal, Y (K-major)
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // Without FoX the scores stay raw (the scale is applied inside the
             // exponent, one FFMA each); with FoX they become log2-unit logits.
             const float sl2 = p.sl2;
-            // S_k is in registers: the next block's MMA1 may overwrite it (FoX
+            // S_k is in registers: the next block's S_k may overwrite it (FoX
             // first decides whether there is a next block)
             if (!FOX) {
                 tc_fence_before();
