@@ -436,8 +436,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]);
             }
-            // Without FoX the scores stay raw (the scale is applied inside the
-            // exponent, one FFMA each); with FoX they become log2-unit logits.
+            // Without a bias the scores stay raw (the scale is applied inside the
+            // exponent, one FFMA each); with one (FoX, relative) they become
+            // log2-unit logits.
             const float sl2 = p.sl2;
             // S_k is in registers: the next block's S_k may overwrite it (FoX
             // first decides whether there is a next block)

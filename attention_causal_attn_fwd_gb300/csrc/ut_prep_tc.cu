@@ -26,7 +26,8 @@
 // MN-major B operand and an MN-major ("transposed") A operand, so W and A are
 // staged once each.
 //
-// Roles (320 threads): warp 0 TMA + TMEM allocation, warp 1 MMA issue,
+// Roles (320 threads): warp 0 TMA loads, TMEM allocation and the workspace
+// stores (bulk tensor stores of staged tiles), warp 1 MMA issue,
 // warps 2-9 solve, conversions and stores (one TMEM lane = one chunk row; the
 // two warps sharing a lane quarter split the columns).  Waits are bounded;
 // a timeout sets PATH_ERR_TIMEOUT and every role stops, drains and frees TMEM.
