@@ -65,6 +65,9 @@ def _load():
             lib.path_oracle_decode.restype = None
             lib.path_oracle_kcache_update.argtypes = [_dp, ctypes.c_int, ctypes.c_int, _dp, ctypes.c_double]
             lib.path_oracle_kcache_update.restype = None
+            lib.path_oracle_bwd.argtypes = [_dp] * 7 + [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                         ctypes.c_double] + [_dp] * 6
+            lib.path_oracle_bwd.restype = None
             lib.path_oracle_threads.argtypes = []
             lib.path_oracle_threads.restype = ctypes.c_int
             _lib = lib
@@ -167,3 +170,30 @@ def kcache_update(kc, w, beta):
     n, d = kc.shape
     _load().path_oracle_kcache_update(_ptr(kc), n, d, _ptr(w), float(beta))
     return kc
+
+
+def path_attn_bwd(q, k, v, w, beta, dO, log_f=None, scale=None):
+    """Gradients of causal PaTH(-FoX) attention in fp64, by the chain rule through the walk.
+
+    q, k, v, w, dO: [..., L, d]; beta, log_f: [..., L].  dO is the gradient of the caller's loss
+    with respect to o.  Returns dict with dq, dk, dv, dw (shape of q), dbeta (shape of beta) and,
+    with log_f, dlog_f.
+    """
+    q, k, v, w, beta, dO = (_f64(x) for x in (q, k, v, w, beta, dO))
+    lf = None if log_f is None else _f64(log_f)
+    L, d = q.shape[-2], q.shape[-1]
+    BH = int(np.prod(q.shape[:-2])) if q.ndim > 2 else 1
+    for x in (k, v, w, dO):
+        assert x.shape == q.shape
+    assert beta.shape == q.shape[:-1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = {n: np.empty(q.shape) for n in ("dq", "dk", "dv", "dw")}
+    out["dbeta"] = np.empty(beta.shape)
+    dlf = np.empty(beta.shape) if lf is not None else None
+    _load().path_oracle_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(lf), _ptr(dO), BH, L, d,
+                            float(scale), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dw"]),
+                            _ptr(out["dbeta"]), _ptr(dlf))
+    if dlf is not None:
+        out["dlog_f"] = dlf
+    return out

@@ -206,3 +206,115 @@ void path_oracle_kcache_update(double* kc, int n, int d, const double* w, double
 #pragma omp parallel for schedule(static)
     for (int j = 0; j < n; ++j) apply_transition(kc + (size_t)j * d, w, beta, d);
 }
+
+/*
+ * Gradients of PaTH (or PaTH-FoX) causal attention for whole heads — the
+ * reverse mode of the walk above, written out by the chain rule.  The pages
+ * give the forward only; the gradient is fixed by it (§3 "Treinamento e
+ * Inferência Eficientes" trains the forward by backpropagation).
+ *
+ * Loss convention: the caller's scalar loss has gradient dO = dL/do.  Per row
+ * i the forward walk gives u_j = H_{j+1} ... H_i q_i (u_i = q_i) and
+ * s_ij = scale k_j . u_j + bias_ij, p_ij = softmax_j, o_i = sum_j p_ij v_j.  Then
+ *     dv_j  += p_ij dO_i
+ *     ds_ij  = p_ij (dO_i . v_j - dO_i . o_i)              (softmax gradient)
+ *     dk_j  += scale ds_ij u_j
+ * and walking back up the row (u_{j-1} = H_j u_j), with g the gradient with
+ * respect to the walk's current vector:
+ *     g <- scale ds_i0 k_0;  for j = 1..i:
+ *         dH_j  = g u_j^T    (g is dL/du_{j-1})
+ *         dbeta_j += -(w_j . g)(w_j . u_j)
+ *         dw_j    += -beta_j ((w_j . u_j) g + (w_j . g) u_j)
+ *         g <- H_j g + scale ds_ij k_j
+ *     dq_i = g.
+ * FoX: bias_ij = sum_{s=j+1..i} log f_s, so dlog_f_s += sum_{j<s} ds_ij for
+ * every s <= i of the row.
+ *
+ * Tensors as in path_oracle_fwd_rows ([BH, L, d] fp64; beta, log_f [BH, L]);
+ * dO [BH, L, d].  Outputs (overwritten): dq, dk, dv, dw [BH, L, d];
+ * dbeta [BH, L]; dlog_f [BH, L] (ignored when log_f is NULL).  OpenMP over
+ * heads; within a head the rows are summed in order.
+ */
+void path_oracle_bwd(const double* q, const double* k, const double* v, const double* w,
+                     const double* beta, const double* log_f, const double* dO,
+                     int BH, int L, int d, double scale,
+                     double* dq, double* dk, double* dv, double* dw, double* dbeta, double* dlog_f) {
+#pragma omp parallel
+    {
+        double* U = (double*)malloc(sizeof(double) * (size_t)L * d); /* u_j of the current row */
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* ds = (double*)malloc(sizeof(double) * (size_t)L);
+        double* o = (double*)malloc(sizeof(double) * (size_t)d);
+        double* g = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int bh = 0; bh < BH; ++bh) {
+            size_t ho = (size_t)bh * L;
+            const double *qh = q + ho * d, *kh = k + ho * d, *vh = v + ho * d, *wh = w + ho * d;
+            const double *bh_beta = beta + ho, *lf = log_f ? log_f + ho : NULL, *dOh = dO + ho * d;
+            double *dqh = dq + ho * d, *dkh = dk + ho * d, *dvh = dv + ho * d, *dwh = dw + ho * d;
+            double *dbh = dbeta + ho, *dlf = log_f ? dlog_f + ho : NULL;
+            memset(dqh, 0, sizeof(double) * (size_t)L * d);
+            memset(dkh, 0, sizeof(double) * (size_t)L * d);
+            memset(dvh, 0, sizeof(double) * (size_t)L * d);
+            memset(dwh, 0, sizeof(double) * (size_t)L * d);
+            memset(dbh, 0, sizeof(double) * (size_t)L);
+            if (dlf) memset(dlf, 0, sizeof(double) * (size_t)L);
+            for (int i = 0; i < L; ++i) {
+                /* forward walk of row i, keeping every u_j */
+                double* u = U + (size_t)i * d;
+                memcpy(u, qh + (size_t)i * d, sizeof(double) * (size_t)d);
+                double bias = 0.0;
+                for (int j = i; j >= 0; --j) {
+                    double* uj = U + (size_t)j * d;
+                    if (j < i) {
+                        memcpy(uj, uj + d, sizeof(double) * (size_t)d);
+                        apply_transition(uj, wh + (size_t)(j + 1) * d, bh_beta[j + 1], d);
+                    }
+                    s[j] = scale * dot(kh + (size_t)j * d, uj, d) + bias;
+                    if (lf) bias += lf[j];
+                }
+                softmax_combine(s, vh, i + 1, d, o);
+                double m = -INFINITY, l = 0.0;
+                for (int j = 0; j <= i; ++j) m = s[j] > m ? s[j] : m;
+                for (int j = 0; j <= i; ++j) l += exp(s[j] - m);
+                const double* dOi = dOh + (size_t)i * d;
+                double delta = dot(dOi, o, d);
+                for (int j = 0; j <= i; ++j) {
+                    double p = exp(s[j] - m) / l;
+                    ds[j] = p * (dot(dOi, vh + (size_t)j * d, d) - delta);
+                    double* dvj = dvh + (size_t)j * d;
+                    double* dkj = dkh + (size_t)j * d;
+                    const double* uj = U + (size_t)j * d;
+                    for (int c = 0; c < d; ++c) {
+                        dvj[c] += p * dOi[c];
+                        dkj[c] += scale * ds[j] * uj[c];
+                    }
+                }
+                /* back up the walk */
+                for (int c = 0; c < d; ++c) g[c] = scale * ds[0] * kh[c];
+                for (int j = 1; j <= i; ++j) {
+                    const double* wj = wh + (size_t)j * d;
+                    const double* uj = U + (size_t)j * d;
+                    double wu = dot(wj, uj, d), wg = dot(wj, g, d);
+                    dbh[j] += -wg * wu;
+                    double* dwj = dwh + (size_t)j * d;
+                    for (int c = 0; c < d; ++c) dwj[c] += -bh_beta[j] * (wu * g[c] + wg * uj[c]);
+                    for (int c = 0; c < d; ++c) g[c] += -bh_beta[j] * wg * wj[c] + scale * ds[j] * kh[(size_t)j * d + c];
+                }
+                memcpy(dqh + (size_t)i * d, g, sizeof(double) * (size_t)d);
+                if (dlf) {
+                    double pre = 0.0; /* sum_{j<s} ds_ij */
+                    for (int sp = 1; sp <= i; ++sp) {
+                        pre += ds[sp - 1];
+                        dlf[sp] += pre;
+                    }
+                }
+            }
+        }
+        free(U);
+        free(s);
+        free(ds);
+        free(o);
+        free(g);
+    }
+}

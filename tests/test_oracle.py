@@ -369,3 +369,133 @@ def test_linear_relbias_equals_constant_forget_gates():
     o2, l2 = orc.path_attn(q, k, v, w, beta, scale=0.4, log_f=np.full(L, -slope))
     np.testing.assert_allclose(o1, o2, atol=1e-12)
     np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- gradients
+_GRAD_NAMES = ("dq", "dk", "dv", "dw", "dbeta")
+
+
+def _fd_grads(q, k, v, w, beta, dO, log_f, scale, eps=1e-6):
+    """Central finite differences of sum(o * dO) through the forward oracle (brute force)."""
+    args = {"q": q, "k": k, "v": v, "w": w, "beta": beta}
+    if log_f is not None:
+        args["log_f"] = log_f
+
+    def loss(a):
+        o, _ = orc.path_attn(a["q"], a["k"], a["v"], a["w"], a["beta"], log_f=a.get("log_f"), scale=scale)
+        return float((o * dO).sum())
+
+    out = {}
+    for n, x in args.items():
+        g = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            a = dict(args)
+            xp = x.copy()
+            xp[idx] += eps
+            a[n] = xp
+            lp = loss(a)
+            xm = x.copy()
+            xm[idx] -= eps
+            a[n] = xm
+            g[idx] = (lp - loss(a)) / (2 * eps)
+        out["d" + n] = g
+    return out
+
+
+@pytest.mark.parametrize("fox", [False, True])
+@pytest.mark.parametrize("L,d,seed", [(7, 3, 91), (12, 4, 92)])
+def test_bwd_matches_finite_differences(L, d, seed, fox):
+    """Every gradient of the backward oracle equals central differences of the forward oracle
+    (beta = 0 and beta = 2 positions included)."""
+    rng = np.random.default_rng(seed)
+    q, k, v, w, beta = _rand_case(rng, L, d)
+    dO = rng.standard_normal((L, d))
+    lf = np.log(1.0 / (1.0 + np.exp(-(3.0 + rng.standard_normal(L))))) if fox else None
+    g = orc.path_attn_bwd(q, k, v, w, beta, dO, log_f=lf, scale=0.6)
+    fd = _fd_grads(q, k, v, w, beta, dO, lf, 0.6)
+    for n in _GRAD_NAMES + (("dlog_f",) if fox else ()):
+        np.testing.assert_allclose(g[n], fd[n], rtol=0, atol=2e-8, err_msg=n)
+
+
+def _torch_dense_loss(q, k, v, w, beta, dO, scale, log_f=None):
+    """sum(o * dO) with every path product built from explicit d x d matrices (torch fp64)."""
+    L, d = q.shape
+    eye = torch.eye(d, dtype=torch.float64)
+    H = [eye - beta[s] * torch.outer(w[s], w[s]) for s in range(L)]
+    rows = []
+    for i in range(L):
+        P = eye
+        logits = [None] * (i + 1)
+        for j in range(i, -1, -1):  # P = H_{j+1} ... H_i, ascending
+            s = scale * (k[j] @ P @ q[i])
+            if log_f is not None:
+                s = s + log_f[j + 1:i + 1].sum()
+            logits[j] = s
+            P = H[j] @ P
+        rows.append(torch.softmax(torch.stack(logits), 0) @ v[: i + 1])
+    return (torch.stack(rows) * dO).sum()
+
+
+@pytest.mark.parametrize("fox", [False, True])
+def test_bwd_matches_autograd_of_dense_products(fox):
+    """Brute force: torch autograd (fp64) of the explicit-matrix PaTH forward."""
+    rng = np.random.default_rng(93)
+    L, d = 10, 4
+    q, k, v, w, beta = _rand_case(rng, L, d)
+    dO = rng.standard_normal((L, d))
+    lf = -rng.uniform(0.0, 0.7, L) if fox else None
+    ts = [torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v, w, beta)]
+    tl = torch.tensor(lf, dtype=torch.float64, requires_grad=True) if fox else None
+    loss = _torch_dense_loss(*ts, torch.from_numpy(dO), 0.45, tl)
+    loss.backward()
+    g = orc.path_attn_bwd(q, k, v, w, beta, dO, log_f=lf, scale=0.45)
+    for n, t in zip(_GRAD_NAMES, ts):
+        np.testing.assert_allclose(g[n], t.grad.numpy(), rtol=0, atol=1e-12, err_msg=n)
+    if fox:
+        np.testing.assert_allclose(g["dlog_f"], tl.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_bwd_beta_zero_is_library_attention_backward():
+    """beta = 0: dq, dk, dv are those of causal softmax attention (torch SDPA autograd, fp64),
+    dw vanishes and dbeta_s = -sum over (i, j<s<=i) of the transition's first-order effect."""
+    rng = np.random.default_rng(94)
+    L, d = 33, 8
+    q, k, v, w, _ = _rand_case(rng, L, d)
+    dO = rng.standard_normal((L, d))
+    g = orc.path_attn_bwd(q, k, v, w, np.zeros(L), dO, scale=0.3)
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(tq[None], tk[None], tv[None], is_causal=True, scale=0.3)[0]
+    (o * torch.from_numpy(dO)).sum().backward()
+    for n, t in (("dq", tq), ("dk", tk), ("dv", tv)):
+        np.testing.assert_allclose(g[n], t.grad.numpy(), rtol=0, atol=1e-12, err_msg=n)
+    assert np.all(g["dw"] == 0.0)
+    # first order in beta_s: s_ij gains -beta_s scale (k_j.w_s)(w_s.q_i) for j < s <= i
+    S = 0.3 * q @ k.T
+    S = np.where(np.tril(np.ones((L, L))) > 0, S, -np.inf)
+    P = np.exp(S - S.max(1, keepdims=True))
+    P /= P.sum(1, keepdims=True)
+    dS = P * (dO @ v.T - (dO * (P @ v)).sum(1, keepdims=True))
+    kw, qw = k @ w.T, q @ w.T  # kw[j, s] = k_j.w_s, qw[i, s] = q_i.w_s
+    exp_db = np.array([-0.3 * sum(dS[i, j] * kw[j, s] * qw[i, s] for i in range(s, L) for j in range(s))
+                       for s in range(L)])
+    np.testing.assert_allclose(g["dbeta"], exp_db, rtol=0, atol=1e-12)
+
+
+def test_bwd_invariants():
+    """Softmax rows sum to one, so sum_j dv_j = sum_i dO_i; position 0's transition acts on
+    nothing, so dbeta_0 = 0, dw_0 = 0 and dlog f_0 = 0."""
+    rng = np.random.default_rng(95)
+    L, d = 40, 6
+    q, k, v, w, beta = _rand_case(rng, L, d)
+    dO = rng.standard_normal((L, d))
+    g = orc.path_attn_bwd(q, k, v, w, beta, dO, log_f=-rng.uniform(0, 1, L), scale=0.5)
+    np.testing.assert_allclose(g["dv"].sum(0), dO.sum(0), rtol=0, atol=1e-12)
+    assert g["dbeta"][0] == 0.0 and np.all(g["dw"][0] == 0.0) and g["dlog_f"][0] == 0.0
+    # batched heads give the same gradients as one head at a time
+    qb, kb, vb, wb, bb = (np.stack([x, x[::-1].copy()]) for x in (q, k, v, w, beta))
+    dOb = np.stack([dO, dO[::-1].copy()])
+    gb = orc.path_attn_bwd(qb, kb, vb, wb, bb, dOb, scale=0.5)
+    g1 = orc.path_attn_bwd(q[::-1].copy(), k[::-1].copy(), v[::-1].copy(), w[::-1].copy(), beta[::-1].copy(),
+                           dO[::-1].copy(), scale=0.5)
+    for n in _GRAD_NAMES:
+        np.testing.assert_allclose(gb[n][1], g1[n], rtol=0, atol=0)
