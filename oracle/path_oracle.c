@@ -232,89 +232,120 @@ void path_oracle_kcache_update(double* kc, int n, int d, const double* w, double
  *
  * Tensors as in path_oracle_fwd_rows ([BH, L, d] fp64; beta, log_f [BH, L]);
  * dO [BH, L, d].  Outputs (overwritten): dq, dk, dv, dw [BH, L, d];
- * dbeta [BH, L]; dlog_f [BH, L] (ignored when log_f is NULL).  OpenMP over
- * heads; within a head the rows are summed in order.
+ * dbeta [BH, L]; dlog_f [BH, L] (ignored when log_f is NULL).  The rows of a
+ * head run in parallel (OpenMP), each thread summing its rows' contributions
+ * into its own buffers, which are then added in thread order.
  */
+static void bwd_row(const double* qh, const double* kh, const double* vh, const double* wh,
+                    const double* bh_beta, const double* lf, const double* dOh, int i, int d, double scale,
+                    double* U, double* s, double* ds, double* o, double* g,
+                    double* dqh, double* dk, double* dv, double* dw, double* db, double* dlf) {
+    /* forward walk of row i, keeping every u_j */
+    double* u = U + (size_t)i * d;
+    memcpy(u, qh + (size_t)i * d, sizeof(double) * (size_t)d);
+    double bias = 0.0;
+    for (int j = i; j >= 0; --j) {
+        double* uj = U + (size_t)j * d;
+        if (j < i) {
+            memcpy(uj, uj + d, sizeof(double) * (size_t)d);
+            apply_transition(uj, wh + (size_t)(j + 1) * d, bh_beta[j + 1], d);
+        }
+        s[j] = scale * dot(kh + (size_t)j * d, uj, d) + bias;
+        if (lf) bias += lf[j];
+    }
+    softmax_combine(s, vh, i + 1, d, o);
+    double m = -INFINITY, l = 0.0;
+    for (int j = 0; j <= i; ++j) m = s[j] > m ? s[j] : m;
+    for (int j = 0; j <= i; ++j) l += exp(s[j] - m);
+    const double* dOi = dOh + (size_t)i * d;
+    double delta = dot(dOi, o, d);
+    for (int j = 0; j <= i; ++j) {
+        double p = exp(s[j] - m) / l;
+        ds[j] = p * (dot(dOi, vh + (size_t)j * d, d) - delta);
+        double* dvj = dv + (size_t)j * d;
+        double* dkj = dk + (size_t)j * d;
+        const double* uj = U + (size_t)j * d;
+        for (int c = 0; c < d; ++c) {
+            dvj[c] += p * dOi[c];
+            dkj[c] += scale * ds[j] * uj[c];
+        }
+    }
+    /* back up the walk */
+    for (int c = 0; c < d; ++c) g[c] = scale * ds[0] * kh[c];
+    for (int j = 1; j <= i; ++j) {
+        const double* wj = wh + (size_t)j * d;
+        const double* uj = U + (size_t)j * d;
+        double wu = dot(wj, uj, d), wg = dot(wj, g, d);
+        db[j] += -wg * wu;
+        double* dwj = dw + (size_t)j * d;
+        for (int c = 0; c < d; ++c) dwj[c] += -bh_beta[j] * (wu * g[c] + wg * uj[c]);
+        for (int c = 0; c < d; ++c) g[c] += -bh_beta[j] * wg * wj[c] + scale * ds[j] * kh[(size_t)j * d + c];
+    }
+    memcpy(dqh + (size_t)i * d, g, sizeof(double) * (size_t)d);
+    if (dlf) {
+        double pre = 0.0; /* sum_{j<s} ds_ij */
+        for (int sp = 1; sp <= i; ++sp) {
+            pre += ds[sp - 1];
+            dlf[sp] += pre;
+        }
+    }
+}
+
 void path_oracle_bwd(const double* q, const double* k, const double* v, const double* w,
                      const double* beta, const double* log_f, const double* dO,
                      int BH, int L, int d, double scale,
                      double* dq, double* dk, double* dv, double* dw, double* dbeta, double* dlog_f) {
+    const size_t Ld = (size_t)L * d;
+    for (int bh = 0; bh < BH; ++bh) {
+        size_t ho = (size_t)bh * L;
+        const double *qh = q + ho * d, *kh = k + ho * d, *vh = v + ho * d, *wh = w + ho * d;
+        const double *bb = beta + ho, *lf = log_f ? log_f + ho : NULL, *dOh = dO + ho * d;
+        double *dkh = dk + ho * d, *dvh = dv + ho * d, *dwh = dw + ho * d;
+        double *dbh = dbeta + ho, *dlfh = log_f ? dlog_f + ho : NULL;
+        memset(dkh, 0, sizeof(double) * Ld);
+        memset(dvh, 0, sizeof(double) * Ld);
+        memset(dwh, 0, sizeof(double) * Ld);
+        memset(dbh, 0, sizeof(double) * (size_t)L);
+        if (dlfh) memset(dlfh, 0, sizeof(double) * (size_t)L);
 #pragma omp parallel
-    {
-        double* U = (double*)malloc(sizeof(double) * (size_t)L * d); /* u_j of the current row */
-        double* s = (double*)malloc(sizeof(double) * (size_t)L);
-        double* ds = (double*)malloc(sizeof(double) * (size_t)L);
-        double* o = (double*)malloc(sizeof(double) * (size_t)d);
-        double* g = (double*)malloc(sizeof(double) * (size_t)d);
-#pragma omp for schedule(dynamic, 1)
-        for (int bh = 0; bh < BH; ++bh) {
-            size_t ho = (size_t)bh * L;
-            const double *qh = q + ho * d, *kh = k + ho * d, *vh = v + ho * d, *wh = w + ho * d;
-            const double *bh_beta = beta + ho, *lf = log_f ? log_f + ho : NULL, *dOh = dO + ho * d;
-            double *dqh = dq + ho * d, *dkh = dk + ho * d, *dvh = dv + ho * d, *dwh = dw + ho * d;
-            double *dbh = dbeta + ho, *dlf = log_f ? dlog_f + ho : NULL;
-            memset(dqh, 0, sizeof(double) * (size_t)L * d);
-            memset(dkh, 0, sizeof(double) * (size_t)L * d);
-            memset(dvh, 0, sizeof(double) * (size_t)L * d);
-            memset(dwh, 0, sizeof(double) * (size_t)L * d);
-            memset(dbh, 0, sizeof(double) * (size_t)L);
-            if (dlf) memset(dlf, 0, sizeof(double) * (size_t)L);
-            for (int i = 0; i < L; ++i) {
-                /* forward walk of row i, keeping every u_j */
-                double* u = U + (size_t)i * d;
-                memcpy(u, qh + (size_t)i * d, sizeof(double) * (size_t)d);
-                double bias = 0.0;
-                for (int j = i; j >= 0; --j) {
-                    double* uj = U + (size_t)j * d;
-                    if (j < i) {
-                        memcpy(uj, uj + d, sizeof(double) * (size_t)d);
-                        apply_transition(uj, wh + (size_t)(j + 1) * d, bh_beta[j + 1], d);
+        {
+            double* U = (double*)malloc(sizeof(double) * Ld); /* u_j of the current row */
+            double* s = (double*)malloc(sizeof(double) * (size_t)L);
+            double* ds = (double*)malloc(sizeof(double) * (size_t)L);
+            double* o = (double*)malloc(sizeof(double) * (size_t)d);
+            double* g = (double*)malloc(sizeof(double) * (size_t)d);
+            /* this thread's share of the per-key sums: dk, dv, dw, dbeta, dlog_f */
+            double* acc = (double*)calloc(3 * Ld + 2 * (size_t)L, sizeof(double));
+            double *tk = acc, *tv = acc + Ld, *tw = acc + 2 * Ld, *tb = acc + 3 * Ld, *tf = tb + L;
+#pragma omp for schedule(dynamic, 4)
+            for (int i = 0; i < L; ++i)
+                bwd_row(qh, kh, vh, wh, bb, lf, dOh, i, d, scale, U, s, ds, o, g, dq + ho * d, tk, tv, tw, tb,
+                        lf ? tf : NULL);
+#ifdef _OPENMP
+            const int nt = omp_get_num_threads(), me = omp_get_thread_num();
+#else
+            const int nt = 1, me = 0;
+#endif
+            for (int t = 0; t < nt; ++t) {
+#pragma omp barrier
+                if (t == me) {
+                    for (size_t x = 0; x < Ld; ++x) {
+                        dkh[x] += tk[x];
+                        dvh[x] += tv[x];
+                        dwh[x] += tw[x];
                     }
-                    s[j] = scale * dot(kh + (size_t)j * d, uj, d) + bias;
-                    if (lf) bias += lf[j];
-                }
-                softmax_combine(s, vh, i + 1, d, o);
-                double m = -INFINITY, l = 0.0;
-                for (int j = 0; j <= i; ++j) m = s[j] > m ? s[j] : m;
-                for (int j = 0; j <= i; ++j) l += exp(s[j] - m);
-                const double* dOi = dOh + (size_t)i * d;
-                double delta = dot(dOi, o, d);
-                for (int j = 0; j <= i; ++j) {
-                    double p = exp(s[j] - m) / l;
-                    ds[j] = p * (dot(dOi, vh + (size_t)j * d, d) - delta);
-                    double* dvj = dvh + (size_t)j * d;
-                    double* dkj = dkh + (size_t)j * d;
-                    const double* uj = U + (size_t)j * d;
-                    for (int c = 0; c < d; ++c) {
-                        dvj[c] += p * dOi[c];
-                        dkj[c] += scale * ds[j] * uj[c];
-                    }
-                }
-                /* back up the walk */
-                for (int c = 0; c < d; ++c) g[c] = scale * ds[0] * kh[c];
-                for (int j = 1; j <= i; ++j) {
-                    const double* wj = wh + (size_t)j * d;
-                    const double* uj = U + (size_t)j * d;
-                    double wu = dot(wj, uj, d), wg = dot(wj, g, d);
-                    dbh[j] += -wg * wu;
-                    double* dwj = dwh + (size_t)j * d;
-                    for (int c = 0; c < d; ++c) dwj[c] += -bh_beta[j] * (wu * g[c] + wg * uj[c]);
-                    for (int c = 0; c < d; ++c) g[c] += -bh_beta[j] * wg * wj[c] + scale * ds[j] * kh[(size_t)j * d + c];
-                }
-                memcpy(dqh + (size_t)i * d, g, sizeof(double) * (size_t)d);
-                if (dlf) {
-                    double pre = 0.0; /* sum_{j<s} ds_ij */
-                    for (int sp = 1; sp <= i; ++sp) {
-                        pre += ds[sp - 1];
-                        dlf[sp] += pre;
+                    for (int x = 0; x < L; ++x) {
+                        dbh[x] += tb[x];
+                        if (dlfh) dlfh[x] += tf[x];
                     }
                 }
             }
+            free(acc);
+            free(U);
+            free(s);
+            free(ds);
+            free(o);
+            free(g);
         }
-        free(U);
-        free(s);
-        free(ds);
-        free(o);
-        free(g);
     }
 }

@@ -497,5 +497,5 @@ def test_bwd_invariants():
     gb = orc.path_attn_bwd(qb, kb, vb, wb, bb, dOb, scale=0.5)
     g1 = orc.path_attn_bwd(q[::-1].copy(), k[::-1].copy(), v[::-1].copy(), w[::-1].copy(), beta[::-1].copy(),
                            dO[::-1].copy(), scale=0.5)
-    for n in _GRAD_NAMES:
-        np.testing.assert_allclose(gb[n][1], g1[n], rtol=0, atol=0)
+    for n in _GRAD_NAMES:  # rows are summed by threads in parallel: equal up to rounding order
+        np.testing.assert_allclose(gb[n][1], g1[n], rtol=0, atol=1e-12)
