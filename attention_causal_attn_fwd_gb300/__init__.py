@@ -35,7 +35,8 @@ _DT = {torch.float32: PATH_F32, torch.bfloat16: PATH_BF16}
 EXPORTED = ("path_version", "path_status_string", "path_attn_workspace_bytes", "path_attn_fwd",
             "path_attn_fwd_fox", "path_decode_workspace_bytes", "path_kcache_update", "path_decode_step",
             "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events", "path_decode_step_noalloc",
-            "path_prefill_workspace_bytes", "path_prefill_kcache", "path_attn_fwd_relbias")
+            "path_prefill_workspace_bytes", "path_prefill_kcache", "path_attn_fwd_relbias",
+            "path_attn_bwd_workspace_bytes", "path_attn_bwd")
 
 
 class PathLibraryError(RuntimeError):
@@ -77,6 +78,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.path_attn_fwd_fox.restype = _i
     lib.path_attn_fwd_relbias.argtypes = lib.path_attn_fwd_fox.argtypes
     lib.path_attn_fwd_relbias.restype = _i
+    lib.path_attn_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+    lib.path_attn_bwd_workspace_bytes.restype = _sz
+    lib.path_attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _fp, _fp, _vp, _fp, _vp, _vp, _vp, _vp, _vp, _fp, _fp,
+                                  _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _sz, _vp]
+    lib.path_attn_bwd.restype = _i
     lib.path_decode_workspace_bytes.argtypes = [_i, _i, _i, _i]
     lib.path_decode_workspace_bytes.restype = _sz
     lib.path_kcache_update.argtypes = [_vp, _i, _i, _i, _i, _i, _vp, _fp, _i, _vp]
@@ -200,6 +206,45 @@ def path_attn_fwd_relbias(q, k, v, w, beta, rel_bias, scale=None, lse=False, out
     if rel_bias is None:
         raise ValueError("rel_bias is required")
     return _fwd(q, k, v, w, beta, None, scale, lse, out, workspace, rel_bias=rel_bias)
+
+
+def path_attn_bwd_workspace_bytes(B: int, H: int, L: int, d: int, dtype: torch.dtype) -> int:
+    return int(load().path_attn_bwd_workspace_bytes(B, H, L, d, _DT[dtype]))
+
+
+def path_attn_bwd(q, k, v, w, beta, o, lse, dO, log_f=None, scale=None, workspace=None):
+    """Gradients of PaTH (or, with log_f, PaTH-FoX) attention for a loss with gradient dO w.r.t. o.
+
+    q, k, v, w, dO and the forward output o: [B, H, L, d] CUDA (fp32 or bf16); beta, lse (the
+    forward's log-sum-exp) and log_f: [B, H, L] fp32.  Returns a dict with dq, dk, dv, dw (dtype of
+    q), dbeta and, with log_f, dlog_f (fp32)."""
+    lib = load()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d]")
+    B, H, L, d = q.shape
+    dt = q.dtype
+    if dt not in _DT:
+        raise ValueError("dtype must be float32 or bfloat16")
+    for name, t in (("q", q), ("k", k), ("v", v), ("w", w), ("o", o), ("dO", dO)):
+        _dev(t, name, dt, (B, H, L, d))
+    for name, t in (("beta", beta), ("lse", lse)) + ((("log_f", log_f),) if log_f is not None else ()):
+        _dev(t, name, torch.float32, (B, H, L))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out = {n: torch.empty_like(q) for n in ("dq", "dk", "dv", "dw")}
+    out["dbeta"] = torch.empty_like(beta)
+    if log_f is not None:
+        out["dlog_f"] = torch.empty_like(beta)
+    need = lib.path_attn_bwd_workspace_bytes(B, H, L, d, _DT[dt])
+    if need == 0:
+        raise PathError(PATH_ERR_UNSUPPORTED, "path_attn_bwd")
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    _check(lib.path_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f), _ptr(o), _ptr(lse),
+                             _ptr(dO), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dw"]),
+                             _ptr(out["dbeta"]), _ptr(out.get("dlog_f")), B, H, L, d, _DT[dt], 1,
+                             ctypes.c_float(scale), _ptr(workspace), workspace.numel(), _stream()),
+           "path_attn_bwd")
+    return out
 
 
 def path_prefill_workspace_bytes(B: int, H: int, L: int, d: int, dtype: torch.dtype) -> int:

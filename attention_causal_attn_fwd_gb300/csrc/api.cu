@@ -21,6 +21,11 @@ cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w
 cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                         const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t, float* lse_t,
                         int BH, float scale, unsigned char* ws, const DecLayout& lay, cudaStream_t st);
+bool bwd_supported(int d);
+cudaError_t attn_bwd(int dtype, int d, const void* q, const void* k, const void* v, const void* w,
+                     const float* beta, const float* log_f, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, void* dw, float* dbeta, float* dlog_f, int BH, int L,
+                     float scale, unsigned char* ws, const BwdLayout& lay, cudaStream_t st);
 cudaError_t kcache_update_launch(int dtype, int d, void* kc, int n_cached, int n_max, const void* w_t,
                                  const float* beta_t, int BH, cudaStream_t st);
 
@@ -140,6 +145,40 @@ int path_prefill_kcache(const void* k, const void* w, const float* beta, void* k
                                    static_cast<unsigned char*>(workspace), lay, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
         std::fprintf(stderr, "pathattn: prefill launch failed: %s\n", cudaGetErrorString(e));
+        return PATH_ERR_CUDA;
+    }
+    return PATH_OK;
+}
+
+size_t path_attn_bwd_workspace_bytes(int B, int H, int L, int d, int dtype) {
+    if (B < 1 || H < 1 || L < 1 || (long long)B * H > 65535 || !bwd_supported(d)) return 0;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return 0;
+    return bwd_layout(B, H, L, d).total;
+}
+
+int path_attn_bwd(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                  const float* log_f, const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                  void* dv, void* dw, float* dbeta, float* dlog_f, int B, int H, int L, int d, int dtype,
+                  int causal, float scale, void* workspace, size_t workspace_bytes, path_stream_t stream) {
+    if (B < 1 || H < 1 || L < 1 || d < 1) return PATH_ERR_INVALID;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
+    if (!causal) return PATH_ERR_UNSUPPORTED;
+    if (!bwd_supported(d) || (long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
+    if ((long long)B * H * L > (1ll << 31) / 256) return PATH_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !w || !beta || !o || !lse || !dO || !dq || !dk || !dv || !dw || !dbeta)
+        return PATH_ERR_INVALID;
+    if (log_f && !dlog_f) return PATH_ERR_INVALID;
+    const void* ptrs[] = {q, k, v, w, beta, o, lse, dO, dq, dk, dv, dw, dbeta};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PATH_ERR_INVALID;
+    if (log_f && (!aligned16(log_f) || !aligned16(dlog_f))) return PATH_ERR_INVALID;
+    const BwdLayout lay = bwd_layout(B, H, L, d);
+    if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PATH_ERR_WORKSPACE;
+    cudaError_t e = attn_bwd(dtype, d, q, k, v, w, beta, log_f, o, lse, dO, dq, dk, dv, dw, dbeta,
+                             log_f ? dlog_f : nullptr, B * H, L, scale, static_cast<unsigned char*>(workspace), lay,
+                             reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "pathattn: backward launch failed: %s\n", cudaGetErrorString(e));
         return PATH_ERR_CUDA;
     }
     return PATH_OK;

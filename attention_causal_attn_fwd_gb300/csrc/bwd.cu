@@ -1,0 +1,689 @@
+// Backward pass of PaTH / PaTH-FoX causal attention: dq, dk, dv, dw, dbeta and
+// dlog f, in fp32 arithmetic on the CUDA cores.
+//
+// The forward ("Resumo Técnico: Atenção PaTH", §2 "Mecanismo Central" and
+// "Extensões: PaTH-FoX") is s_ij = scale k_j^T H_{j+1} ... H_i q_i (+ c_i - c_j,
+// c the cumulative sum of log f), H_s = I - beta_s w_s w_s^T,
+// o_i = sum_j softmax_j(s_i.) v_j.  §3 trains it by backpropagation; what
+// follows is its chain rule, organised in chunks of C = 64 positions like the
+// forward's blockwise scan.  Within chunk m (positions b..e):
+//
+//   P_m    = H_b ... H_e                       (chunk transition, d x d)
+//   qbar_i = H_b ... H_i q_i                   (query walked down its own chunk)
+//   khat_j = H_e ... H_{j+1} k_j               (key walked up to its chunk end)
+//
+// and for a key chunk m below a query chunk n the queries reach chunk m as
+// U_{n,n-1} = Qbar_n, U_{n,m-1} = U_{n,m} P_m^T, with S_nm = scale U_{n,m}
+// Khat_m^T + bias.  With dS = P o (dO V^T - Delta), Delta_i = dO_i . o_i:
+//
+//   dV_m     += P_nm^T dO_n
+//   dKhat_m  += scale dS_nm^T U_{n,m}
+//   G_{n,m}   = scale dS_nm Khat_m + G_{n,m-1} P_m        (G_{n,-1} = 0)
+//   dP_m     += G_{n,m-1}^T U_{n,m}
+//   dQbar_n   = G_{n,n-1}
+//
+// and the walks that built qbar, khat, P_m and the diagonal block are then
+// reversed inside each chunk.  A transition's gradient dH = g u^T becomes
+// dbeta = -(w.g)(w.u) and dw = -beta ((w.u) g + (w.g) u).
+//
+// Kernels, in stream order:
+//   bwd_prep   one CTA per chunk        qbar, khat, P_m, P_m^T, Delta
+//   bwd_chain  one CTA per query chunk  U chain down, G chain up; stores U,
+//                                       G and dS per (n, m) pair; dQbar
+//   bwd_reduce one CTA per key chunk    dV_m, dKhat_m, dP_m summed over the
+//                                       query chunks (each output owned by
+//                                       one CTA, so no global atomics)
+//   bwd_local  one CTA per chunk        diagonal block and the within-chunk
+//                                       walks in reverse; writes dq, dk, dv,
+//                                       dw, dbeta (shared-memory atomics)
+//   bwd_fox_suffix one CTA per head     dlog f_s = sum_{t >= s} dc_t
+// The contractions use the register-tiled shared-memory GEMM of simt_gemm.cuh.
+// Nothing waits on another CTA, so no kernel here has a spin wait.
+#include "common.cuh"
+#include "simt_gemm.cuh"
+#include "ut_prep.cuh"
+
+namespace pathattn {
+
+namespace {
+
+constexpr int kC = kBwdC;
+constexpr int kNT = 256;
+constexpr int kNW = kNT / 32;
+
+struct BwdParams {
+    const void *q, *k, *v, *w, *o, *dO;
+    const float *beta, *lse;
+    void *dq, *dk, *dv, *dw;
+    float *dbeta, *dlog_f;
+    float *qbar, *khat, *pm, *pmt, *delta, *cum, *dqbar, *dkhat, *dvoff, *dpm, *dcrow, *dccol, *dctot, *pairs;
+    int L, Lp, N;
+    size_t pair_floats, head_pairs;
+    float scale;
+    int fox;
+};
+
+// ------------------------------------------------------------------ warp-level vectors
+// A d-vector held by one warp: lane l owns elements l + 32 r (r < R); for d = 16
+// lanes 16..31 own nothing and hold zeros.
+template <int D> struct WV {
+    static constexpr int R = D >= 32 ? D / 32 : 1;
+    static __device__ __forceinline__ bool ok(int lane) { return D >= 32 || lane < D; }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+template <int D, typename G>
+__device__ __forceinline__ void vload(float (&a)[WV<D>::R], const G* src, int lane) {
+#pragma unroll
+    for (int r = 0; r < WV<D>::R; ++r) a[r] = WV<D>::ok(lane) ? to_f<G>(src[lane + 32 * r]) : 0.f;
+}
+template <int D, typename G>
+__device__ __forceinline__ void vstore(G* dst, const float (&a)[WV<D>::R], int lane) {
+    if (!WV<D>::ok(lane)) return;
+#pragma unroll
+    for (int r = 0; r < WV<D>::R; ++r) dst[lane + 32 * r] = from_f<G>(a[r]);
+}
+template <int D>
+__device__ __forceinline__ void vzero(float (&a)[WV<D>::R]) {
+#pragma unroll
+    for (int r = 0; r < WV<D>::R; ++r) a[r] = 0.f;
+}
+// a . s for a row s of D floats
+template <int D>
+__device__ __forceinline__ float vdot(const float (&a)[WV<D>::R], const float* s, int lane) {
+    float t = 0.f;
+    if (WV<D>::ok(lane)) {
+#pragma unroll
+        for (int r = 0; r < WV<D>::R; ++r) t = fmaf(a[r], s[lane + 32 * r], t);
+    }
+    return warp_sum(t);
+}
+template <int D>
+__device__ __forceinline__ float vdot(const float (&a)[WV<D>::R], const float (&b)[WV<D>::R]) {
+    float t = 0.f;
+#pragma unroll
+    for (int r = 0; r < WV<D>::R; ++r) t = fmaf(a[r], b[r], t);
+    return warp_sum(t);
+}
+// a <- a - coef * s
+template <int D>
+__device__ __forceinline__ void vaxpy(float (&a)[WV<D>::R], const float* s, float coef, int lane) {
+    if (!WV<D>::ok(lane)) return;
+#pragma unroll
+    for (int r = 0; r < WV<D>::R; ++r) a[r] = fmaf(-coef, s[lane + 32 * r], a[r]);
+}
+// a <- H a = a - beta (w . a) w, returns w . a
+template <int D>
+__device__ __forceinline__ float vstep(float (&a)[WV<D>::R], const float* w, float beta, int lane) {
+    const float t = vdot<D>(a, w, lane);
+    vaxpy<D>(a, w, beta * t, lane);
+    return t;
+}
+// shared-memory accumulate s += f * a
+template <int D>
+__device__ __forceinline__ void vred(float* s, const float (&a)[WV<D>::R], float f, int lane) {
+    if (!WV<D>::ok(lane)) return;
+#pragma unroll
+    for (int r = 0; r < WV<D>::R; ++r) atomicAdd(s + lane + 32 * r, f * a[r]);
+}
+
+// rows [0, rows) x [0, cols) of a row-major global array (leading dim lds) into
+// shared memory (leading dim ldd) as fp32; rows >= valid read as zero.
+template <typename G>
+__device__ __forceinline__ void to_smem(float* dst, int ldd, const G* src, int lds, int rows, int cols,
+                                        int valid) {
+    for (int idx = threadIdx.x; idx < rows * cols; idx += kNT) {
+        const int r = idx / cols, c = idx % cols;
+        dst[r * ldd + c] = r < valid ? to_f<G>(src[(size_t)r * lds + c]) : 0.f;
+    }
+}
+__device__ __forceinline__ void from_smem(float* dst, int ldd, const float* src, int lds, int rows, int cols,
+                                          float f = 1.f) {
+    for (int idx = threadIdx.x; idx < rows * cols; idx += kNT) {
+        const int r = idx / cols, c = idx % cols;
+        dst[(size_t)r * ldd + c] = f * src[r * lds + c];
+    }
+}
+
+// acc += sum_k a(m, k) b(k, n) with the thread tiling of block_gemm (no barriers).
+template <int M, int N, int K, class LA, class LB>
+__device__ __forceinline__ void gemm_acc(float (&acc)[GemmTile<M, N, kNT>::TM][GemmTile<M, N, kNT>::TN],
+                                         const LA& a, const LB& b) {
+    using G = GemmTile<M, N, kNT>;
+    const int tm = threadIdx.x / G::GN, tn = threadIdx.x % G::GN;
+#pragma unroll 4
+    for (int kk = 0; kk < K; ++kk) {
+        float av[G::TM], bv[G::TN];
+#pragma unroll
+        for (int i = 0; i < G::TM; ++i) av[i] = a(tm + i * G::GM, kk);
+#pragma unroll
+        for (int j = 0; j < G::TN; ++j) bv[j] = b(kk, tn + j * G::GN);
+#pragma unroll
+        for (int i = 0; i < G::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < G::TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+template <int M, int N>
+__device__ __forceinline__ void store_acc(float* dst, int ld,
+                                          const float (&acc)[GemmTile<M, N, kNT>::TM][GemmTile<M, N, kNT>::TN],
+                                          float f) {
+    using G = GemmTile<M, N, kNT>;
+    const int tm = threadIdx.x / G::GN, tn = threadIdx.x % G::GN;
+#pragma unroll
+    for (int i = 0; i < G::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < G::TN; ++j) dst[(size_t)(tm + i * G::GM) * ld + tn + j * G::GN] = f * acc[i][j];
+}
+
+// ------------------------------------------------------------------ shared-memory sizes (floats)
+template <int D> struct BwdSmem {
+    static constexpr int LDR = D + 1, LDS = kC + 1, LDP = D + 1;
+    static constexpr int prep = kC * D + kC + D * LDP + D;
+    static constexpr int chain = 4 * kC * LDR + kC * LDS + D * LDP + 5 * kC;
+    static constexpr int reduce = 4 * kC * LDR + 2 * kC * LDS + 4 * kC;
+    static constexpr int wbuf = (3 * kC > 2 * D ? 3 * kC : 2 * D);
+    static constexpr int local = 6 * kC * D + 4 * kC + kNW * wbuf;
+    static_assert(3 * kC * D >= D * LDP, "dP must fit over the key, value and dk tiles");
+    static_assert(chain * 4 <= 227 * 1024 && local * 4 <= 227 * 1024 && reduce * 4 <= 227 * 1024,
+                  "shared memory per CTA");
+};
+
+// ------------------------------------------------------------------ bwd_prep
+template <typename T, int D>
+__global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
+    constexpr int C = kC, LDP = BwdSmem<D>::LDP;
+    extern __shared__ float smem[];
+    float* sW = smem;          // [C][D]
+    float* sB = sW + C * D;    // [C]
+    float* sM = sB + C;        // [D][LDP]
+    float* sZ = sM + D * LDP;  // [D]
+    const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
+    const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
+    to_smem(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, D, c);
+    for (int r = threadIdx.x; r < C; r += kNT) sB[r] = r < c ? p.beta[hrow + r] : 0.f;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int r = wid; r < C; r += kNW) {
+        float u[WV<D>::R], x[WV<D>::R];
+        float dl = 0.f;
+        if (r < c) {
+            vload<D>(u, static_cast<const T*>(p.q) + (hrow + r) * D, lane);
+            for (int jj = r; jj >= 0; --jj) vstep<D>(u, sW + jj * D, sB[jj], lane);
+            vload<D>(x, static_cast<const T*>(p.k) + (hrow + r) * D, lane);
+            for (int tt = r + 1; tt < c; ++tt) vstep<D>(x, sW + tt * D, sB[tt], lane);
+            float oo[WV<D>::R], gg[WV<D>::R];
+            vload<D>(oo, static_cast<const T*>(p.o) + (hrow + r) * D, lane);
+            vload<D>(gg, static_cast<const T*>(p.dO) + (hrow + r) * D, lane);
+            dl = vdot<D>(oo, gg);
+        } else {
+            vzero<D>(u);
+            vzero<D>(x);
+        }
+        vstore<D>(p.qbar + (prow + r) * D, u, lane);
+        vstore<D>(p.khat + (prow + r) * D, x, lane);
+        if (lane == 0) p.delta[prow + r] = dl;
+    }
+    if (n < 1 || n > p.N - 2) return;  // P_m is used only for 1 <= m <= N-2
+    for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
+        const int r = idx / D, cc = idx % D;
+        sM[r * LDP + cc] = r == cc ? 1.f : 0.f;
+    }
+    __syncthreads();
+    for (int t = 0; t < c; ++t) {  // M <- M H_t = M - beta_t (M w_t) w_t^T
+        const float* wt = sW + t * D;
+        for (int r = threadIdx.x; r < D; r += kNT) {
+            float z = 0.f;
+            for (int cc = 0; cc < D; ++cc) z = fmaf(sM[r * LDP + cc], wt[cc], z);
+            sZ[r] = sB[t] * z;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
+            const int r = idx / D, cc = idx % D;
+            sM[r * LDP + cc] = fmaf(-sZ[r], wt[cc], sM[r * LDP + cc]);
+        }
+        __syncthreads();
+    }
+    float* pm = p.pm + ((size_t)bh * p.N + n) * D * D;
+    float* pmt = p.pmt + ((size_t)bh * p.N + n) * D * D;
+    for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
+        const int r = idx / D, cc = idx % D;
+        pm[idx] = sM[r * LDP + cc];
+        pmt[idx] = sM[cc * LDP + r];
+    }
+}
+
+// ------------------------------------------------------------------ bwd_chain
+template <typename T, int D>
+__global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
+    constexpr int C = kC, LDR = BwdSmem<D>::LDR, LDS = BwdSmem<D>::LDS, LDP = BwdSmem<D>::LDP;
+    extern __shared__ float smem[];
+    float* sU = smem;            // [C][LDR] queries reaching key chunk m
+    float* sO = sU + C * LDR;    // [C][LDR] dO_n; the G chain later
+    float* sK = sO + C * LDR;    // [C][LDR] khat_m
+    float* sV = sK + C * LDR;    // [C][LDR] v_m; scale dS khat later
+    float* sS = sV + C * LDR;    // [C][LDS] S, then dS
+    float* sP = sS + C * LDS;    // [D][LDP] P_m^T (down the chain), P_m (up)
+    float* sL = sP + D * LDP;    // [C] lse_i
+    float* sD = sL + C;          // [C] Delta_i
+    float* sCi = sD + C;         // [C] c_i
+    float* sCj = sCi + C;        // [C] c_j
+    float* sRs = sCj + C;        // [C] FoX row sums of dS
+    const int n = p.N - 1 - blockIdx.x, bh = blockIdx.y;  // longest chains first
+    const int b = n * C, c = min(C, p.L - b);
+    const size_t hbase = (size_t)bh * p.L, pbase = (size_t)bh * p.Lp;
+    const T* dO = static_cast<const T*>(p.dO);
+    const T* v = static_cast<const T*>(p.v);
+    const float scale = p.scale;
+    to_smem(sU, LDR, p.qbar + (pbase + b) * D, D, C, D, C);
+    to_smem(sO, LDR, dO + (hbase + b) * D, D, C, D, c);
+    for (int r = threadIdx.x; r < C; r += kNT) {
+        sL[r] = r < c ? p.lse[hbase + b + r] : 0.f;
+        sD[r] = p.delta[pbase + b + r];
+        sCi[r] = p.fox ? p.cum[pbase + b + r] : 0.f;
+        sRs[r] = 0.f;
+    }
+    float* pairs_n = p.pairs + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2) * p.pair_floats;
+    for (int m = n - 1; m >= 0; --m) {
+        const int bm = m * C;
+        float* pr = pairs_n + (size_t)m * p.pair_floats;  // U [C][D], G [C][D], dS [C][C]
+        __syncthreads();
+        to_smem(sK, LDR, p.khat + (pbase + bm) * D, D, C, D, C);
+        to_smem(sV, LDR, v + (hbase + bm) * D, D, C, D, C);  // key chunks below n are full
+        if (m >= 1) to_smem(sP, LDP, p.pmt + ((size_t)bh * p.N + m) * D * D, D, D, D, D);
+        for (int r = threadIdx.x; r < C; r += kNT) sCj[r] = p.fox ? p.cum[pbase + bm + r] : 0.f;
+        __syncthreads();
+        block_gemm<C, C, D, kNT>([&](int r, int kk) { return sU[r * LDR + kk]; },
+                                 [&](int kk, int j) { return sK[j * LDR + kk]; },
+                                 [&](int r, int j, float acc) { sS[r * LDS + j] = scale * acc + sCi[r] - sCj[j]; });
+        block_gemm<C, C, D, kNT>([&](int r, int kk) { return sO[r * LDR + kk]; },
+                                 [&](int kk, int j) { return sV[j * LDR + kk]; },
+                                 [&](int r, int j, float acc) {
+                                     float ds = 0.f;
+                                     if (r < c) ds = __expf(sS[r * LDS + j] - sL[r]) * (acc - sD[r]);
+                                     sS[r * LDS + j] = ds;
+                                     pr[2 * C * D + r * C + j] = ds;
+                                 });
+        if (p.fox)
+            for (int r = threadIdx.x; r < C; r += kNT) {
+                float t = 0.f;
+                for (int j = 0; j < C; ++j) t += sS[r * LDS + j];
+                sRs[r] += t;
+            }
+        from_smem(pr, D, sU, LDR, C, D);
+        if (m >= 1)  // U <- U P_m^T (the block_gemm barrier orders the store above before the overwrite)
+            block_gemm<C, D, D, kNT>([&](int r, int kk) { return sU[r * LDR + kk]; },
+                                     [&](int kk, int cc) { return sP[kk * LDP + cc]; },
+                                     [&](int r, int cc, float acc) { sU[r * LDR + cc] = acc; });
+    }
+    float* sG = sO;
+    float* sT = sV;
+    for (int m = 0; m < n; ++m) {
+        const int bm = m * C;
+        float* pr = pairs_n + (size_t)m * p.pair_floats;
+        __syncthreads();
+        to_smem(sK, LDR, p.khat + (pbase + bm) * D, D, C, D, C);
+        to_smem(sS, LDS, pr + 2 * C * D, C, C, C, C);
+        if (m >= 1) {
+            to_smem(sP, LDP, p.pm + ((size_t)bh * p.N + m) * D * D, D, D, D, D);
+            from_smem(pr + C * D, D, sG, LDR, C, D);  // G_{n,m-1}
+        }
+        __syncthreads();
+        float* dst = m == 0 ? sG : sT;
+        block_gemm<C, D, C, kNT>([&](int r, int kk) { return sS[r * LDS + kk]; },
+                                 [&](int kk, int cc) { return sK[kk * LDR + cc]; },
+                                 [&](int r, int cc, float acc) { dst[r * LDR + cc] = scale * acc; });
+        if (m >= 1)
+            block_gemm<C, D, D, kNT>([&](int r, int kk) { return sG[r * LDR + kk]; },
+                                     [&](int kk, int cc) { return sP[kk * LDP + cc]; },
+                                     [&](int r, int cc, float acc) { sG[r * LDR + cc] = acc + sT[r * LDR + cc]; });
+    }
+    from_smem(p.dqbar + (pbase + b) * D, D, sG, LDR, C, D);
+    if (p.fox)
+        for (int r = threadIdx.x; r < C; r += kNT) p.dcrow[pbase + b + r] = sRs[r];
+}
+
+// ------------------------------------------------------------------ bwd_reduce
+template <typename T, int D>
+__global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
+    constexpr int C = kC, LDR = BwdSmem<D>::LDR, LDS = BwdSmem<D>::LDS;
+    extern __shared__ float smem[];
+    float* sK = smem;           // [C][LDR] khat_m
+    float* sU = sK + C * LDR;   // [C][LDR] U_{n,m}
+    float* sO = sU + C * LDR;   // [C][LDR] dO_n
+    float* sG = sO + C * LDR;   // [C][LDR] G_{n,m-1}
+    float* sS = sG + C * LDR;   // [C][LDS] dS_nm
+    float* sA = sS + C * LDS;   // [C][LDS] softmax probabilities P_nm
+    float* sL = sA + C * LDS;   // [C] lse_i
+    float* sCi = sL + C;        // [C] c_i
+    float* sCj = sCi + C;       // [C] c_j
+    float* sCs = sCj + C;       // [C] FoX column sums of dS
+    const int m = blockIdx.x, bh = blockIdx.y, bm = m * C;  // m = 0 has the most query chunks
+    const size_t hbase = (size_t)bh * p.L, pbase = (size_t)bh * p.Lp;
+    const T* dO = static_cast<const T*>(p.dO);
+    const float scale = p.scale;
+    to_smem(sK, LDR, p.khat + (pbase + bm) * D, D, C, D, C);
+    for (int r = threadIdx.x; r < C; r += kNT) {
+        sCj[r] = p.fox ? p.cum[pbase + bm + r] : 0.f;
+        sCs[r] = 0.f;
+    }
+    using GV = GemmTile<C, D, kNT>;
+    using GP = GemmTile<D, D, kNT>;
+    float accV[GV::TM][GV::TN], accK[GV::TM][GV::TN], accP[GP::TM][GP::TN];
+#pragma unroll
+    for (int i = 0; i < GV::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < GV::TN; ++j) accV[i][j] = accK[i][j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < GP::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < GP::TN; ++j) accP[i][j] = 0.f;
+    for (int n = m + 1; n < p.N; ++n) {
+        const int b = n * C, c = min(C, p.L - b);
+        const float* pr = p.pairs + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2 + m) * p.pair_floats;
+        __syncthreads();
+        to_smem(sU, LDR, pr, D, C, D, C);
+        to_smem(sS, LDS, pr + 2 * C * D, C, C, C, C);
+        if (m >= 1) to_smem(sG, LDR, pr + C * D, D, C, D, C);
+        to_smem(sO, LDR, dO + (hbase + b) * D, D, C, D, c);
+        for (int r = threadIdx.x; r < C; r += kNT) {
+            sL[r] = r < c ? p.lse[hbase + b + r] : 0.f;
+            sCi[r] = p.fox ? p.cum[pbase + b + r] : 0.f;
+        }
+        __syncthreads();
+        block_gemm<C, C, D, kNT>([&](int r, int kk) { return sU[r * LDR + kk]; },
+                                 [&](int kk, int j) { return sK[j * LDR + kk]; },
+                                 [&](int r, int j, float acc) {
+                                     sA[r * LDS + j] = r < c ? __expf(scale * acc + sCi[r] - sCj[j] - sL[r]) : 0.f;
+                                 });
+        gemm_acc<C, D, C>(accV, [&](int j, int i) { return sA[i * LDS + j]; },
+                          [&](int i, int cc) { return sO[i * LDR + cc]; });
+        gemm_acc<C, D, C>(accK, [&](int j, int i) { return sS[i * LDS + j]; },
+                          [&](int i, int cc) { return sU[i * LDR + cc]; });
+        if (m >= 1)
+            gemm_acc<D, D, C>(accP, [&](int r, int i) { return sG[i * LDR + r]; },
+                              [&](int i, int cc) { return sU[i * LDR + cc]; });
+        if (p.fox)
+            for (int j = threadIdx.x; j < C; j += kNT) {
+                float t = 0.f;
+                for (int i = 0; i < C; ++i) t += sS[i * LDS + j];
+                sCs[j] += t;
+            }
+    }
+    store_acc<C, D>(p.dvoff + (pbase + bm) * D, D, accV, 1.f);
+    store_acc<C, D>(p.dkhat + (pbase + bm) * D, D, accK, scale);
+    if (m >= 1) store_acc<D, D>(p.dpm + ((size_t)bh * p.N + m) * D * D, D, accP, 1.f);
+    __syncthreads();
+    if (p.fox)
+        for (int j = threadIdx.x; j < C; j += kNT) p.dccol[pbase + bm + j] = sCs[j];
+}
+
+// ------------------------------------------------------------------ bwd_local
+template <typename T, int D>
+__global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
+    constexpr int C = kC, R = WV<D>::R, LDP = BwdSmem<D>::LDP, WB = BwdSmem<D>::wbuf;
+    extern __shared__ float smem[];
+    float* sW = smem;          // [C][D] w
+    float* sK = sW + C * D;    // [C][D] raw keys
+    float* sV = sK + C * D;    // [C][D] values
+    float* aK = sV + C * D;    // [C][D] dk
+    float* aV = aK + C * D;    // [C][D] dv, diagonal part
+    float* aW = aV + C * D;    // [C][D] dw
+    float* sB = aW + C * D;    // [C] beta
+    float* sC = sB + C;        // [C] c (FoX)
+    float* aB = sC + C;        // [C] dbeta
+    float* aC = aB + C;        // [C] dc (FoX), diagonal part
+    float* sBuf = aC + C;      // [kNW][WB] per-warp scalars / vectors
+    float* sDP = sK;           // [D][LDP] dP_n in the last phase (over sK, sV, aK)
+    const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
+    const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
+    const T* q = static_cast<const T*>(p.q);
+    const T* dO = static_cast<const T*>(p.dO);
+    const bool below = n >= 1;          // query chains from this chunk continue into earlier chunks
+    const bool above = n <= p.N - 2;    // later query chunks reach this chunk's keys
+    const float scale = p.scale;
+    to_smem(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, D, c);
+    to_smem(sK, D, static_cast<const T*>(p.k) + hrow * D, D, C, D, c);
+    to_smem(sV, D, static_cast<const T*>(p.v) + hrow * D, D, C, D, c);
+    for (int idx = threadIdx.x; idx < 3 * C * D; idx += kNT) aK[idx] = 0.f;  // aK, aV, aW
+    for (int r = threadIdx.x; r < C; r += kNT) {
+        sB[r] = r < c ? p.beta[hrow + r] : 0.f;
+        sC[r] = p.fox ? p.cum[prow + r] : 0.f;
+        aB[r] = 0.f;
+        aC[r] = 0.f;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    float* bds = sBuf + wid * WB;  // ds_ij of the warp's row
+    float* bal = bds + C;          // w . (walked vector) of the forward walk
+    float* bga = bal + C;          // w . (gradient) of the reverse walk
+
+    // (a) each query row of the chunk: its diagonal logits and the walk that built qbar
+    for (int r = wid; r < c; r += kNW) {
+        float u[R], gO[R], g[R];
+        vload<D>(u, q + (hrow + r) * D, lane);
+        vload<D>(gO, dO + (hrow + r) * D, lane);
+        const float lse = p.lse[hrow + r], del = p.delta[prow + r], ci = sC[r];
+        for (int jj = r; jj >= 0; --jj) {  // down: u = H_{j+1} ... H_i q_i
+            const float s = scale * vdot<D>(u, sK + jj * D, lane) + ci - sC[jj];
+            const float pij = __expf(s - lse);
+            const float ds = pij * (vdot<D>(gO, sV + jj * D, lane) - del);
+            vred<D>(aK + jj * D, u, scale * ds, lane);
+            vred<D>(aV + jj * D, gO, pij, lane);
+            const float al = vstep<D>(u, sW + jj * D, sB[jj], lane);
+            if (lane == 0) {
+                bds[jj] = ds;
+                bal[jj] = al;
+                if (p.fox) {
+                    atomicAdd(aC + r, ds);
+                    atomicAdd(aC + jj, -ds);
+                }
+            }
+        }
+        __syncwarp();
+        if (below) vload<D>(g, p.dqbar + (prow + r) * D, lane);
+        else vzero<D>(g);
+        for (int jj = 0; jj <= r; ++jj) {  // up: g is dL/du_{j-1}, then dL/du_j
+            const float* wj = sW + jj * D;
+            const float ga = vdot<D>(g, wj, lane), al = bal[jj];
+            vred<D>(aW + jj * D, g, -sB[jj] * al, lane);
+            if (lane == 0) {
+                atomicAdd(aB + jj, -ga * al);
+                bga[jj] = ga;
+            }
+            vaxpy<D>(g, wj, sB[jj] * ga, lane);
+            vaxpy<D>(g, sK + jj * D, -scale * bds[jj], lane);
+        }
+        vstore<D>(static_cast<T*>(p.dq) + (hrow + r) * D, g, lane);
+        __syncwarp();
+        vload<D>(u, q + (hrow + r) * D, lane);
+        for (int jj = r; jj >= 0; --jj) {  // down again: the (w . g) u half of dw
+            vred<D>(aW + jj * D, u, -sB[jj] * bga[jj], lane);
+            vaxpy<D>(u, sW + jj * D, sB[jj] * bal[jj], lane);
+        }
+        __syncwarp();
+    }
+    // (b) each key of the chunk: the walk that built khat (gradient from later query chunks)
+    if (above)
+        for (int r = wid; r < c; r += kNW) {
+            float x[R], gx[R];
+            vload<D>(x, sK + r * D, lane);
+            for (int tt = r + 1; tt < c; ++tt) {
+                const float al = vstep<D>(x, sW + tt * D, sB[tt], lane);
+                if (lane == 0) bal[tt] = al;
+            }
+            __syncwarp();
+            vload<D>(gx, p.dkhat + (prow + r) * D, lane);
+            for (int tt = c - 1; tt > r; --tt) {
+                const float* wt = sW + tt * D;
+                const float ga = vdot<D>(gx, wt, lane), al = bal[tt];
+                vred<D>(aW + tt * D, gx, -sB[tt] * al, lane);
+                if (lane == 0) {
+                    atomicAdd(aB + tt, -ga * al);
+                    bga[tt] = ga;
+                }
+                vaxpy<D>(gx, wt, sB[tt] * ga, lane);
+            }
+            vred<D>(aK + r * D, gx, 1.f, lane);
+            __syncwarp();
+            vload<D>(x, sK + r * D, lane);
+            for (int tt = r + 1; tt < c; ++tt) {
+                vred<D>(aW + tt * D, x, -sB[tt] * bga[tt], lane);
+                vaxpy<D>(x, sW + tt * D, sB[tt] * bal[tt], lane);
+            }
+            __syncwarp();
+        }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < c * D; idx += kNT) {
+        static_cast<T*>(p.dk)[hrow * D + idx] = from_f<T>(aK[idx]);
+        const float dv = aV[idx] + (above ? p.dvoff[prow * D + idx] : 0.f);
+        static_cast<T*>(p.dv)[hrow * D + idx] = from_f<T>(dv);
+    }
+    // (c) the chunk transition P_n = H_b ... H_e: dH_t = A_t^T dP B_t^T with
+    //     A_t = H_b ... H_{t-1}, B_t = H_{t+1} ... H_e
+    if (below && above) {
+        __syncthreads();
+        to_smem(sDP, LDP, p.dpm + ((size_t)bh * p.N + n) * D * D, D, D, D, D);
+        __syncthreads();
+        float* vw = sBuf + wid * WB;  // [2][D]: B_t^T w_t, A_t w_t
+        for (int r = wid; r < c; r += kNW) {
+            float wh[R], wb[R], y1[R], y2[R];
+            vload<D>(wh, sW + r * D, lane);
+            for (int tt = r + 1; tt < c; ++tt) vstep<D>(wh, sW + tt * D, sB[tt], lane);
+            vload<D>(wb, sW + r * D, lane);
+            for (int tt = r - 1; tt >= 0; --tt) vstep<D>(wb, sW + tt * D, sB[tt], lane);
+            vstore<D>(vw, wh, lane);
+            vstore<D>(vw + D, wb, lane);
+            __syncwarp();
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) {
+                const int e = lane + 32 * rr;
+                float s1 = 0.f, s2 = 0.f;
+                if (WV<D>::ok(lane))
+                    for (int cc = 0; cc < D; ++cc) {
+                        s1 = fmaf(sDP[e * LDP + cc], vw[cc], s1);      // (dP B_t^T w_t)_e
+                        s2 = fmaf(sDP[cc * LDP + e], vw[D + cc], s2);  // (dP^T A_t w_t)_e
+                    }
+                y1[rr] = s1;
+                y2[rr] = s2;
+            }
+            const float db = -vdot<D>(wb, y1);
+            for (int tt = 0; tt < r; ++tt) vstep<D>(y1, sW + tt * D, sB[tt], lane);       // A_t^T y1
+            for (int tt = c - 1; tt > r; --tt) vstep<D>(y2, sW + tt * D, sB[tt], lane);   // B_t y2
+            if (WV<D>::ok(lane))
+#pragma unroll
+                for (int rr = 0; rr < R; ++rr) aW[r * D + lane + 32 * rr] += -sB[r] * (y1[rr] + y2[rr]);
+            if (lane == 0) aB[r] += db;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < c * D; idx += kNT) static_cast<T*>(p.dw)[hrow * D + idx] = from_f<T>(aW[idx]);
+    for (int r = threadIdx.x; r < c; r += kNT) {
+        p.dbeta[hrow + r] = aB[r];
+        if (p.fox)
+            p.dctot[prow + r] = aC[r] + (below ? p.dcrow[prow + r] : 0.f) - (above ? p.dccol[prow + r] : 0.f);
+    }
+}
+
+// ------------------------------------------------------------------ FoX: dlog f_s = sum_{t >= s} dc_t
+__global__ void __launch_bounds__(1024) bwd_fox_suffix(const float* __restrict__ dctot, int L, int Lp,
+                                                       float* __restrict__ dlog_f) {
+    __shared__ double warp_tot[32];
+    __shared__ double carry_s;
+    const int bh = blockIdx.x;
+    const float* src = dctot + (size_t)bh * Lp;
+    float* dst = dlog_f + (size_t)bh * L;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (threadIdx.x == 0) carry_s = 0.0;
+    __syncthreads();
+    for (int base = 0; base < L; base += 1024) {
+        const int s = L - 1 - (base + (int)threadIdx.x);  // walks from the end of the head
+        double x = s >= 0 ? (double)src[s] : 0.0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const double y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) warp_tot[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            double t = warp_tot[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const double y = __shfl_up_sync(0xffffffffu, t, off);
+                if (lane >= off) t += y;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        const double carry = carry_s;
+        const double pre = wid > 0 ? warp_tot[wid - 1] : 0.0;
+        if (s >= 0) dst[s] = (float)(carry + pre + x);
+        __syncthreads();
+        if (threadIdx.x == 0) carry_s = carry + warp_tot[31];
+        __syncthreads();
+    }
+}
+
+template <typename T, int D>
+cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, cudaStream_t st) {
+    using S = BwdSmem<D>;
+    const size_t b_prep = S::prep * sizeof(float), b_chain = S::chain * sizeof(float),
+                 b_reduce = S::reduce * sizeof(float), b_local = S::local * sizeof(float);
+    cudaFuncSetAttribute(bwd_prep<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_prep);
+    cudaFuncSetAttribute(bwd_chain<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_chain);
+    cudaFuncSetAttribute(bwd_reduce<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_reduce);
+    cudaFuncSetAttribute(bwd_local<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_local);
+    if (log_f) fox_cumsum<<<BH, 1024, 0, st>>>(log_f, p.L, p.Lp, p.cum);
+    bwd_prep<T, D><<<dim3(p.N, BH), kNT, b_prep, st>>>(p);
+    mark_start(st);
+    if (p.N >= 2) {
+        bwd_chain<T, D><<<dim3(p.N - 1, BH), kNT, b_chain, st>>>(p);
+        bwd_reduce<T, D><<<dim3(p.N - 1, BH), kNT, b_reduce, st>>>(p);
+    }
+    mark_end(st);
+    bwd_local<T, D><<<dim3(p.N, BH), kNT, b_local, st>>>(p);
+    if (log_f) bwd_fox_suffix<<<BH, 1024, 0, st>>>(p.dctot, p.L, p.Lp, p.dlog_f);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_supported(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+cudaError_t attn_bwd(int dtype, int d, const void* q, const void* k, const void* v, const void* w,
+                     const float* beta, const float* log_f, const void* o, const float* lse, const void* dO,
+                     void* dq, void* dk, void* dv, void* dw, float* dbeta, float* dlog_f, int BH, int L,
+                     float scale, unsigned char* ws, const BwdLayout& lay, cudaStream_t st) {
+    BwdParams p;
+    p.q = q; p.k = k; p.v = v; p.w = w; p.o = o; p.dO = dO;
+    p.beta = beta; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv; p.dw = dw; p.dbeta = dbeta; p.dlog_f = dlog_f;
+    auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+    p.qbar = f(lay.qbar); p.khat = f(lay.khat); p.pm = f(lay.pm); p.pmt = f(lay.pmt);
+    p.delta = f(lay.delta); p.cum = f(lay.cum); p.dqbar = f(lay.dqbar); p.dkhat = f(lay.dkhat);
+    p.dvoff = f(lay.dvoff); p.dpm = f(lay.dpm); p.dcrow = f(lay.dcrow); p.dccol = f(lay.dccol);
+    p.dctot = f(lay.dctot); p.pairs = f(lay.pairs);
+    p.L = L; p.Lp = lay.Lp; p.N = lay.N;
+    p.pair_floats = lay.pair_floats; p.head_pairs = lay.head_pairs;
+    p.scale = scale;
+    p.fox = log_f != nullptr;
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), st);
+    if (e != cudaSuccess) return e;
+    const bool bf = dtype == PATH_BF16;
+    switch (d) {
+        case 16: return bf ? launch_bwd_t<__nv_bfloat16, 16>(p, BH, log_f, st) : launch_bwd_t<float, 16>(p, BH, log_f, st);
+        case 32: return bf ? launch_bwd_t<__nv_bfloat16, 32>(p, BH, log_f, st) : launch_bwd_t<float, 32>(p, BH, log_f, st);
+        case 64: return bf ? launch_bwd_t<__nv_bfloat16, 64>(p, BH, log_f, st) : launch_bwd_t<float, 64>(p, BH, log_f, st);
+        case 128: return bf ? launch_bwd_t<__nv_bfloat16, 128>(p, BH, log_f, st) : launch_bwd_t<float, 128>(p, BH, log_f, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pathattn

@@ -147,4 +147,56 @@ inline DecLayout dec_layout(int B, int H, int n_max, int d) {
     return s;
 }
 
+// ----------------------------------------------------------------------------- backward workspace
+// Chunk size of the backward pass (every d).  With N = ceil(L / C) chunks per
+// head and Lp = N * C padded rows (padded rows hold zeros):
+//   qbar  : float [BH, Lp, d]   queries walked down through their own chunk
+//   khat  : float [BH, Lp, d]   keys walked up to their chunk end
+//   pm    : float [BH, N, d, d] chunk transition P_m = H_b ... H_e (row-major)
+//   pmt   : float [BH, N, d, d] its transpose
+//   delta : float [BH, Lp]      dO_i . o_i
+//   cum   : float [BH, Lp]      inclusive cumulative sum of log f (PaTH-FoX)
+//   dqbar, dkhat, dvoff : float [BH, Lp, d]  gradients w.r.t. qbar and khat,
+//                         and the off-diagonal part of dv
+//   dpm   : float [BH, N, d, d] gradient w.r.t. P_m
+//   dcrow, dccol, dctot : float [BH, Lp]  FoX: gradient w.r.t. the cumulative
+//                         sums (row part, column part, total)
+//   pairs : float [BH, N(N-1)/2, 2 C d + C C]  per (query chunk n, key chunk
+//           m < n): the transported queries U_{n,m}, the chain gradient
+//           G_{n,m-1} and the logit gradient dS_{nm}
+constexpr int kBwdC = 64;
+struct BwdLayout {
+    size_t qbar, khat, pm, pmt, delta, cum, dqbar, dkhat, dvoff, dpm, dcrow, dccol, dctot, pairs, total;
+    int Lp, N;
+    size_t pair_floats;  // floats per (n, m) pair
+    size_t head_pairs;   // N (N - 1) / 2
+};
+inline BwdLayout bwd_layout(int B, int H, int L, int d) {
+    BwdLayout s;
+    const int C = kBwdC;
+    s.N = cdiv(L, C);
+    s.Lp = s.N * C;
+    const size_t BH = (size_t)B * H, rows = BH * s.Lp;
+    s.pair_floats = 2 * (size_t)C * d + (size_t)C * C;
+    s.head_pairs = (size_t)s.N * (s.N - 1) / 2;
+    size_t off = sizeof(WsHeader);
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
+    s.qbar = take(rows * d * sizeof(float));
+    s.khat = take(rows * d * sizeof(float));
+    s.pm = take(BH * s.N * d * d * sizeof(float));
+    s.pmt = take(BH * s.N * d * d * sizeof(float));
+    s.delta = take(rows * sizeof(float));
+    s.cum = take(rows * sizeof(float));
+    s.dqbar = take(rows * d * sizeof(float));
+    s.dkhat = take(rows * d * sizeof(float));
+    s.dvoff = take(rows * d * sizeof(float));
+    s.dpm = take(BH * s.N * d * d * sizeof(float));
+    s.dcrow = take(rows * sizeof(float));
+    s.dccol = take(rows * sizeof(float));
+    s.dctot = take(rows * sizeof(float));
+    s.pairs = take(BH * s.head_pairs * s.pair_floats * sizeof(float));
+    s.total = off;
+    return s;
+}
+
 }  // namespace pathattn

@@ -16,6 +16,10 @@ __device__ __forceinline__ void load_rows(S* dst, const G* src, int r0, int nrow
     }
 }
 
+// Inclusive cumulative sum of log f per head into cum [BH, Lp] (ut_prep.cu).
+__global__ void __launch_bounds__(1024) fox_cumsum(const float* __restrict__ log_f, int L, int Lp,
+                                                   float* __restrict__ cum);
+
 // Launch the per-chunk UT-prep kernel (and, when log_f is given, the FoX
 // cumulative sum) for chunk size C, filling the workspace regions of `lay`.
 cudaError_t launch_ut_prep(int dtype, int C, int d, const void* q, const void* k, const void* w, const float* beta,

@@ -433,6 +433,44 @@ def run_ours(args, rank, world, local):
                    "workload": "transported key cache of a B%d H%d L%d d%d bf16 prompt" % (fc.B, fc.H, fc.L, fc.d)}
         del kc_p, ws_p
 
+    # backward pass on the forward workload (timed separately, not part of the step): gradients of
+    # every input for a seeded dO, from the forward's own o and lse
+    bwd = None
+    if args.bwd_steps > 0:
+        o_b, lse_b = P.path_attn_fwd(q, k, v, w, beta, scale=x.scale, lse=True)
+        gen = torch.Generator(device=dev).manual_seed(1002)
+        dO_b = torch.randn(q.shape, generator=gen, device=dev).to(q.dtype)
+        ws_b = P.alloc_workspace(P.path_attn_bwd_workspace_bytes(fc.B, fc.H, fc.L, fc.d, q.dtype), dev)
+        P.path_attn_bwd(q, k, v, w, beta, o_b, lse_b, dO_b, scale=x.scale, workspace=ws_b)
+        torch.cuda.synchronize()
+        ev = [[mk() for _ in range(4)] for _ in range(args.bwd_steps)]
+        for e in ev:
+            P.path_debug_set_timing_events(e[2], e[3])
+            e[0].record()
+            P.path_attn_bwd(q, k, v, w, beta, o_b, lse_b, dO_b, scale=x.scale, workspace=ws_b)
+            e[1].record()
+        P.path_debug_set_timing_events(None, None)
+        torch.cuda.synchronize()
+        bms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        kms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+        # fp32 FLOPs of the chunk-pair kernels (bwd_chain + bwd_reduce), C = 64: per (query chunk,
+        # earlier key chunk) pair six C x C x d products (S twice, dO V^T, dS khat, P^T dO,
+        # dS^T U) and, past the first key chunk, three C x d x d ones (U P^T, G P, G^T U)
+        C, nc = 64, -(-fc.L // 64)
+        pairs = nc * (nc - 1) // 2
+        pair_flops = fc.B * fc.H * (pairs * 6 * 2 * C * C * fc.d + (pairs - (nc - 1)) * 3 * 2 * C * fc.d * fc.d)
+        fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x fp32 lanes x FMA x max SM clock
+        ach = pair_flops / (kms * 1e-3) / 1e12
+        bwd = {"ms": bms, "attn_equiv_tflops": 2.5 * fc.attn_flops / (bms * 1e-3) / 1e12, "steps": args.bwd_steps,
+               "workload": "PaTH backward B%d H%d L%d d%d bf16 (dq, dk, dv, dw, dbeta for a seeded dO); "
+                           "attention-equivalent FLOPs 2.5 x the forward's" % (fc.B, fc.H, fc.L, fc.d),
+               "workspace_gb": ws_b.numel() / 1e9,
+               "roofline": {"kernel": "bwd_chain + bwd_reduce (fp32 CUDA cores)", "bound": "alu", "achieved": ach,
+                            "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach / fp32_peak,
+                            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                            "traffic": None, "flops_per_launch": float(pair_flops), "kernel_ms": kms}}
+        del o_b, lse_b, dO_b, ws_b
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, dt, cores, desc = oracle_sample(args.cpu_heads)
@@ -450,7 +488,7 @@ def run_ours(args, rank, world, local):
                        "seq_len": fc.L, "parallelism": "replicas (b,h)-independent" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (forward 384 MiB of q,k,v,w; decode caches 13 GB)"},
             "fwd_ms": fwd_ms_max / args.steps, "fwd_kernel_ms": fk,
-            "decode": dec_obj, "prefill_kcache": prefill, "fox16k": fox.get("fox16k"), "fox64k": fox.get("fox64k"), "relbias_ggd": relb, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "decode": dec_obj, "prefill_kcache": prefill, "fox16k": fox.get("fox16k"), "fox64k": fox.get("fox64k"), "relbias_ggd": relb, "backward": bwd, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps}
     if rank == 0:
         print(json.dumps(line))
@@ -467,6 +505,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--prefill-steps", type=int, default=2)
     ap.add_argument("--fox-steps", type=int, default=3)
+    ap.add_argument("--bwd-steps", type=int, default=2)
     ap.add_argument("--cpu-heads", type=int, default=96)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fwd-B", type=int, default=8, help="forward batch (8 = the timed workload)")

@@ -126,6 +126,43 @@ int path_attn_fwd_relbias(const void* q, const void* k, const void* v, const voi
                           path_stream_t stream);
 
 /*
+ * Workspace size in bytes for path_attn_bwd.  The backward keeps, per head and
+ * per pair (query chunk n, key chunk m < n) of 64-position chunks, the queries
+ * transported to chunk m, the chain gradient and the logit gradient, so it grows
+ * as B*H*L^2 (about 15.5 GB at B=8, H=12, L=4096, d=128).  Returns 0 for
+ * unsupported sizes.
+ */
+size_t path_attn_bwd_workspace_bytes(int B, int H, int L, int d, int dtype);
+
+/*
+ * Gradients of PaTH (log_f == NULL) or PaTH-FoX causal attention with respect to
+ * every input: the chain rule of the forward of §2 "Mecanismo Central" (logit and
+ * transition equations) and "Extensões: PaTH-FoX", which §3 "Treinamento e
+ * Inferência Eficientes" trains by backpropagation.  For a loss with gradient dO
+ * with respect to o:
+ *   q, k, v, w, beta, log_f : the forward's inputs (as path_attn_fwd_fox; log_f
+ *                             may be NULL for plain PaTH)
+ *   o, lse : the forward's outputs for these inputs (lse is required)
+ *   dO     : [B, H, L, d], same dtype as q
+ *   dq, dk, dv, dw : [B, H, L, d], same dtype as q (written)
+ *   dbeta  : [B, H, L] float (written)
+ *   dlog_f : [B, H, L] float (written); required when log_f is given, ignored
+ *            otherwise
+ *   d in {16, 32, 64, 128} for PATH_F32 and PATH_BF16; B*H <= 65535; causal = 1
+ *   workspace : >= path_attn_bwd_workspace_bytes(B,H,L,d,dtype) bytes, device,
+ *            16-byte aligned, contents need not be initialised
+ * Arithmetic is fp32 on the CUDA cores; bf16 inputs are widened on load and the
+ * gradients rounded to bf16 (nearest even) on store.  dbeta at position 0 and
+ * dlog_f at position 0 are exactly zero (those enter no logit).  Outputs may not
+ * alias inputs.  Argument errors return before any launch; the kernels have no
+ * waits, so the status word stays PATH_OK.
+ */
+int path_attn_bwd(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                  const float* log_f, const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                  void* dv, void* dw, float* dbeta, float* dlog_f, int B, int H, int L, int d, int dtype,
+                  int causal, float scale, void* workspace, size_t workspace_bytes, path_stream_t stream);
+
+/*
  * Workspace size in bytes for path_decode_step (split-K partial results and a
  * status word) for caches of capacity n_max.  Returns 0 for unsupported sizes.
  */

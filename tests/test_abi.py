@@ -85,6 +85,31 @@ def test_forward_argument_errors(lib):
     assert rel == P.PATH_ERR_UNSUPPORTED  # non-causal
 
 
+def test_bwd_argument_errors(lib):
+    def bwd(**kw):
+        a = dict(log_f=None, dlog_f=None, lse=FAKE, d=64, dt=P.PATH_BF16, causal=1, BH=(2, 3), ws_bytes=1 << 40,
+                 dq=FAKE)
+        a.update(kw)
+        B, H = a["BH"]
+        return lib.path_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, a["log_f"], FAKE, a["lse"], FAKE, a["dq"], FAKE, FAKE,
+                                 FAKE, FAKE, a["dlog_f"], B, H, 300, a["d"], a["dt"], a["causal"],
+                                 ctypes.c_float(0.125), FAKE, a["ws_bytes"], None)
+    assert bwd(lse=None) == P.PATH_ERR_INVALID            # the forward's lse is required
+    assert bwd(dq=None) == P.PATH_ERR_INVALID
+    assert bwd(log_f=FAKE) == P.PATH_ERR_INVALID          # FoX needs dlog_f
+    assert bwd(dq=ctypes.c_void_p((1 << 20) + 4)) == P.PATH_ERR_INVALID  # misaligned
+    assert bwd(d=48) == P.PATH_ERR_UNSUPPORTED
+    assert bwd(dt=7) == P.PATH_ERR_UNSUPPORTED
+    assert bwd(causal=0) == P.PATH_ERR_UNSUPPORTED
+    assert bwd(BH=(300, 300)) == P.PATH_ERR_UNSUPPORTED   # B*H above the grid limit
+    assert bwd(ws_bytes=4096) == P.PATH_ERR_WORKSPACE
+    need = lib.path_attn_bwd_workspace_bytes(2, 3, 300, 64, P.PATH_BF16)
+    # 5 chunks of 64: 10 (query chunk, key chunk) pairs per head hold U, G (64 x 64) and dS (64 x 64)
+    assert need > 6 * 10 * (2 * 64 * 64 + 64 * 64) * 4
+    assert lib.path_attn_bwd_workspace_bytes(2, 3, 300, 48, P.PATH_BF16) == 0
+    assert lib.path_attn_bwd_workspace_bytes(2, 3, 300, 64, 9) == 0
+
+
 def test_decode_argument_errors(lib):
     def step(**kw):
         a = dict(n_cached=10, n_max=11, d=128, dt=P.PATH_BF16, ws_bytes=1 << 30, kc=FAKE)
