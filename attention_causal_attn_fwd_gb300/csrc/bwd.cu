@@ -50,6 +50,8 @@ namespace {
 constexpr int kC = kBwdC;
 constexpr int kNT = 256;
 constexpr int kNW = kNT / 32;
+constexpr int kNTL = 512;  // bwd_local: latency-bound walks, one warp per row / key / position
+constexpr int kNWL = kNTL / 32;
 
 struct BwdParams {
     const void *q, *k, *v, *w, *o, *dO;
@@ -132,14 +134,24 @@ __device__ __forceinline__ void vred(float* s, const float (&a)[WV<D>::R], float
     for (int r = 0; r < WV<D>::R; ++r) atomicAdd(s + lane + 32 * r, f * a[r]);
 }
 
-// rows [0, rows) x [0, cols) of a row-major global array (leading dim lds) into
-// shared memory (leading dim ldd) as fp32; rows >= valid read as zero.
-template <typename G>
-__device__ __forceinline__ void to_smem(float* dst, int ldd, const G* src, int lds, int rows, int cols,
-                                        int valid) {
-    for (int idx = threadIdx.x; idx < rows * cols; idx += kNT) {
-        const int r = idx / cols, c = idx % cols;
-        dst[r * ldd + c] = r < valid ? to_f<G>(src[(size_t)r * lds + c]) : 0.f;
+// Rows [0, rows) of a row-major global array of COLS columns (leading dim lds, rows starting
+// on 16-byte boundaries) into shared memory (leading dim ldd) as fp32; rows >= valid read as
+// zero.  16-byte loads, several in flight per thread; plain (coherent) loads, since a CTA
+// reads back pair data it wrote itself.
+template <typename G, int COLS, int NT = kNT>
+__device__ __forceinline__ void to_smem_v(float* dst, int ldd, const G* src, int lds, int rows, int valid) {
+    constexpr int V = 16 / sizeof(G);
+    constexpr int VPR = COLS / V;
+    static_assert(COLS % V == 0, "rows must be whole 16-byte vectors");
+    const int nvec = rows * VPR;
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < nvec; idx += NT) {
+        const int r = idx / VPR, cv = idx % VPR;
+        Vec16<G> x;
+        x.raw = r < valid ? ld_global_v4(src + (size_t)r * lds + cv * V) : make_uint4(0u, 0u, 0u, 0u);
+        float* d = dst + r * ldd + cv * V;
+#pragma unroll
+        for (int j = 0; j < V; ++j) d[j] = x.get(j);
     }
 }
 __device__ __forceinline__ void from_smem(float* dst, int ldd, const float* src, int lds, int rows, int cols,
@@ -188,7 +200,7 @@ template <int D> struct BwdSmem {
     static constexpr int chain = 4 * kC * LDR + kC * LDS + D * LDP + 5 * kC;
     static constexpr int reduce = 4 * kC * LDR + 2 * kC * LDS + 4 * kC;
     static constexpr int wbuf = (3 * kC > 2 * D ? 3 * kC : 2 * D);
-    static constexpr int local = 6 * kC * D + 4 * kC + kNW * wbuf;
+    static constexpr int local = 6 * kC * D + 4 * kC + kNWL * wbuf;
     static_assert(3 * kC * D >= D * LDP, "dP must fit over the key, value and dk tiles");
     static_assert(chain * 4 <= 227 * 1024 && local * 4 <= 227 * 1024 && reduce * 4 <= 227 * 1024,
                   "shared memory per CTA");
@@ -205,7 +217,7 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
     float* sZ = sM + D * LDP;  // [D]
     const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
     const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
-    to_smem(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, D, c);
+    to_smem_v<T, D>(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, c);
     for (int r = threadIdx.x; r < C; r += kNT) sB[r] = r < c ? p.beta[hrow + r] : 0.f;
     __syncthreads();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -237,10 +249,22 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
     __syncthreads();
     for (int t = 0; t < c; ++t) {  // M <- M H_t = M - beta_t (M w_t) w_t^T
         const float* wt = sW + t * D;
-        for (int r = threadIdx.x; r < D; r += kNT) {
-            float z = 0.f;
-            for (int cc = 0; cc < D; ++cc) z = fmaf(sM[r * LDP + cc], wt[cc], z);
-            sZ[r] = sB[t] * z;
+        // z = M w_t: two threads per row, four partial sums each (short dependency chains)
+        for (int h = threadIdx.x; h < 2 * D; h += kNT) {
+            const int r = h >> 1, c0 = (h & 1) * (D / 2);
+            float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+            const float* mr = sM + r * LDP + c0;
+            const float* wc = wt + c0;
+#pragma unroll 4
+            for (int cc = 0; cc < D / 2; cc += 4) {
+                z0 = fmaf(mr[cc], wc[cc], z0);
+                z1 = fmaf(mr[cc + 1], wc[cc + 1], z1);
+                z2 = fmaf(mr[cc + 2], wc[cc + 2], z2);
+                z3 = fmaf(mr[cc + 3], wc[cc + 3], z3);
+            }
+            float z = (z0 + z1) + (z2 + z3);
+            z += __shfl_xor_sync(0xffffffffu, z, 1);
+            if ((h & 1) == 0) sZ[r] = sB[t] * z;
         }
         __syncthreads();
         for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
@@ -280,8 +304,8 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
     const T* dO = static_cast<const T*>(p.dO);
     const T* v = static_cast<const T*>(p.v);
     const float scale = p.scale;
-    to_smem(sU, LDR, p.qbar + (pbase + b) * D, D, C, D, C);
-    to_smem(sO, LDR, dO + (hbase + b) * D, D, C, D, c);
+    to_smem_v<float, D>(sU, LDR, p.qbar + (pbase + b) * D, D, C, C);
+    to_smem_v<T, D>(sO, LDR, dO + (hbase + b) * D, D, C, c);
     for (int r = threadIdx.x; r < C; r += kNT) {
         sL[r] = r < c ? p.lse[hbase + b + r] : 0.f;
         sD[r] = p.delta[pbase + b + r];
@@ -293,9 +317,9 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
         const int bm = m * C;
         float* pr = pairs_n + (size_t)m * p.pair_floats;  // U [C][D], G [C][D], dS [C][C]
         __syncthreads();
-        to_smem(sK, LDR, p.khat + (pbase + bm) * D, D, C, D, C);
-        to_smem(sV, LDR, v + (hbase + bm) * D, D, C, D, C);  // key chunks below n are full
-        if (m >= 1) to_smem(sP, LDP, p.pmt + ((size_t)bh * p.N + m) * D * D, D, D, D, D);
+        to_smem_v<float, D>(sK, LDR, p.khat + (pbase + bm) * D, D, C, C);
+        to_smem_v<T, D>(sV, LDR, v + (hbase + bm) * D, D, C, C);  // key chunks below n are full
+        if (m >= 1) to_smem_v<float, D>(sP, LDP, p.pmt + ((size_t)bh * p.N + m) * D * D, D, D, D);
         for (int r = threadIdx.x; r < C; r += kNT) sCj[r] = p.fox ? p.cum[pbase + bm + r] : 0.f;
         __syncthreads();
         block_gemm<C, C, D, kNT>([&](int r, int kk) { return sU[r * LDR + kk]; },
@@ -327,10 +351,10 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
         const int bm = m * C;
         float* pr = pairs_n + (size_t)m * p.pair_floats;
         __syncthreads();
-        to_smem(sK, LDR, p.khat + (pbase + bm) * D, D, C, D, C);
-        to_smem(sS, LDS, pr + 2 * C * D, C, C, C, C);
+        to_smem_v<float, D>(sK, LDR, p.khat + (pbase + bm) * D, D, C, C);
+        to_smem_v<float, C>(sS, LDS, pr + 2 * C * D, C, C, C);
         if (m >= 1) {
-            to_smem(sP, LDP, p.pm + ((size_t)bh * p.N + m) * D * D, D, D, D, D);
+            to_smem_v<float, D>(sP, LDP, p.pm + ((size_t)bh * p.N + m) * D * D, D, D, D);
             from_smem(pr + C * D, D, sG, LDR, C, D);  // G_{n,m-1}
         }
         __syncthreads();
@@ -367,7 +391,7 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
     const size_t hbase = (size_t)bh * p.L, pbase = (size_t)bh * p.Lp;
     const T* dO = static_cast<const T*>(p.dO);
     const float scale = p.scale;
-    to_smem(sK, LDR, p.khat + (pbase + bm) * D, D, C, D, C);
+    to_smem_v<float, D>(sK, LDR, p.khat + (pbase + bm) * D, D, C, C);
     for (int r = threadIdx.x; r < C; r += kNT) {
         sCj[r] = p.fox ? p.cum[pbase + bm + r] : 0.f;
         sCs[r] = 0.f;
@@ -387,10 +411,10 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
         const int b = n * C, c = min(C, p.L - b);
         const float* pr = p.pairs + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2 + m) * p.pair_floats;
         __syncthreads();
-        to_smem(sU, LDR, pr, D, C, D, C);
-        to_smem(sS, LDS, pr + 2 * C * D, C, C, C, C);
-        if (m >= 1) to_smem(sG, LDR, pr + C * D, D, C, D, C);
-        to_smem(sO, LDR, dO + (hbase + b) * D, D, C, D, c);
+        to_smem_v<float, D>(sU, LDR, pr, D, C, C);
+        to_smem_v<float, C>(sS, LDS, pr + 2 * C * D, C, C, C);
+        if (m >= 1) to_smem_v<float, D>(sG, LDR, pr + C * D, D, C, C);
+        to_smem_v<T, D>(sO, LDR, dO + (hbase + b) * D, D, C, c);
         for (int r = threadIdx.x; r < C; r += kNT) {
             sL[r] = r < c ? p.lse[hbase + b + r] : 0.f;
             sCi[r] = p.fox ? p.cum[pbase + b + r] : 0.f;
@@ -425,7 +449,7 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
 
 // ------------------------------------------------------------------ bwd_local
 template <typename T, int D>
-__global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
+__global__ void __launch_bounds__(kNTL) bwd_local(BwdParams p) {
     constexpr int C = kC, R = WV<D>::R, LDP = BwdSmem<D>::LDP, WB = BwdSmem<D>::wbuf;
     extern __shared__ float smem[];
     float* sW = smem;          // [C][D] w
@@ -438,7 +462,7 @@ __global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
     float* sC = sB + C;        // [C] c (FoX)
     float* aB = sC + C;        // [C] dbeta
     float* aC = aB + C;        // [C] dc (FoX), diagonal part
-    float* sBuf = aC + C;      // [kNW][WB] per-warp scalars / vectors
+    float* sBuf = aC + C;      // [kNWL][WB] per-warp scalars / vectors
     float* sDP = sK;           // [D][LDP] dP_n in the last phase (over sK, sV, aK)
     const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
     const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
@@ -447,11 +471,11 @@ __global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
     const bool below = n >= 1;          // query chains from this chunk continue into earlier chunks
     const bool above = n <= p.N - 2;    // later query chunks reach this chunk's keys
     const float scale = p.scale;
-    to_smem(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, D, c);
-    to_smem(sK, D, static_cast<const T*>(p.k) + hrow * D, D, C, D, c);
-    to_smem(sV, D, static_cast<const T*>(p.v) + hrow * D, D, C, D, c);
-    for (int idx = threadIdx.x; idx < 3 * C * D; idx += kNT) aK[idx] = 0.f;  // aK, aV, aW
-    for (int r = threadIdx.x; r < C; r += kNT) {
+    to_smem_v<T, D, kNTL>(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, c);
+    to_smem_v<T, D, kNTL>(sK, D, static_cast<const T*>(p.k) + hrow * D, D, C, c);
+    to_smem_v<T, D, kNTL>(sV, D, static_cast<const T*>(p.v) + hrow * D, D, C, c);
+    for (int idx = threadIdx.x; idx < 3 * C * D; idx += kNTL) aK[idx] = 0.f;  // aK, aV, aW
+    for (int r = threadIdx.x; r < C; r += kNTL) {
         sB[r] = r < c ? p.beta[hrow + r] : 0.f;
         sC[r] = p.fox ? p.cum[prow + r] : 0.f;
         aB[r] = 0.f;
@@ -464,7 +488,7 @@ __global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
     float* bga = bal + C;          // w . (gradient) of the reverse walk
 
     // (a) each query row of the chunk: its diagonal logits and the walk that built qbar
-    for (int r = wid; r < c; r += kNW) {
+    for (int r = wid; r < c; r += kNWL) {
         float u[R], gO[R], g[R];
         vload<D>(u, q + (hrow + r) * D, lane);
         vload<D>(gO, dO + (hrow + r) * D, lane);
@@ -510,7 +534,7 @@ __global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
     }
     // (b) each key of the chunk: the walk that built khat (gradient from later query chunks)
     if (above)
-        for (int r = wid; r < c; r += kNW) {
+        for (int r = wid; r < c; r += kNWL) {
             float x[R], gx[R];
             vload<D>(x, sK + r * D, lane);
             for (int tt = r + 1; tt < c; ++tt) {
@@ -539,7 +563,7 @@ __global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
             __syncwarp();
         }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < c * D; idx += kNT) {
+    for (int idx = threadIdx.x; idx < c * D; idx += kNTL) {
         static_cast<T*>(p.dk)[hrow * D + idx] = from_f<T>(aK[idx]);
         const float dv = aV[idx] + (above ? p.dvoff[prow * D + idx] : 0.f);
         static_cast<T*>(p.dv)[hrow * D + idx] = from_f<T>(dv);
@@ -548,10 +572,10 @@ __global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
     //     A_t = H_b ... H_{t-1}, B_t = H_{t+1} ... H_e
     if (below && above) {
         __syncthreads();
-        to_smem(sDP, LDP, p.dpm + ((size_t)bh * p.N + n) * D * D, D, D, D, D);
+        to_smem_v<float, D, kNTL>(sDP, LDP, p.dpm + ((size_t)bh * p.N + n) * D * D, D, D, D);
         __syncthreads();
         float* vw = sBuf + wid * WB;  // [2][D]: B_t^T w_t, A_t w_t
-        for (int r = wid; r < c; r += kNW) {
+        for (int r = wid; r < c; r += kNWL) {
             float wh[R], wb[R], y1[R], y2[R];
             vload<D>(wh, sW + r * D, lane);
             for (int tt = r + 1; tt < c; ++tt) vstep<D>(wh, sW + tt * D, sB[tt], lane);
@@ -583,8 +607,8 @@ __global__ void __launch_bounds__(kNT) bwd_local(BwdParams p) {
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < c * D; idx += kNT) static_cast<T*>(p.dw)[hrow * D + idx] = from_f<T>(aW[idx]);
-    for (int r = threadIdx.x; r < c; r += kNT) {
+    for (int idx = threadIdx.x; idx < c * D; idx += kNTL) static_cast<T*>(p.dw)[hrow * D + idx] = from_f<T>(aW[idx]);
+    for (int r = threadIdx.x; r < c; r += kNTL) {
         p.dbeta[hrow + r] = aB[r];
         if (p.fox)
             p.dctot[prow + r] = aC[r] + (below ? p.dcrow[prow + r] : 0.f) - (above ? p.dccol[prow + r] : 0.f);
@@ -648,7 +672,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, cudaStr
         bwd_reduce<T, D><<<dim3(p.N - 1, BH), kNT, b_reduce, st>>>(p);
     }
     mark_end(st);
-    bwd_local<T, D><<<dim3(p.N, BH), kNT, b_local, st>>>(p);
+    bwd_local<T, D><<<dim3(p.N, BH), kNTL, b_local, st>>>(p);
     if (log_f) bwd_fox_suffix<<<BH, 1024, 0, st>>>(p.dctot, p.L, p.Lp, p.dlog_f);
     return cudaGetLastError();
 }
