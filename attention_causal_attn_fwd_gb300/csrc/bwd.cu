@@ -37,10 +37,9 @@
 //                                       walks in reverse; writes dq, dk, dv,
 //                                       dw, dbeta (shared-memory atomics)
 //   bwd_fox_suffix one CTA per head     dlog f_s = sum_{t >= s} dc_t
-// The contractions use the register-tiled shared-memory GEMM of simt_gemm.cuh.
+// The contractions are register-tiled fp32 GEMMs on K-major shared-memory operands.
 // Nothing waits on another CTA, so no kernel here has a spin wait.
 #include "common.cuh"
-#include "simt_gemm.cuh"
 #include "ut_prep.cuh"
 
 namespace pathattn {
@@ -154,51 +153,161 @@ __device__ __forceinline__ void to_smem_v(float* dst, int ldd, const G* src, int
         for (int j = 0; j < V; ++j) d[j] = x.get(j);
     }
 }
-__device__ __forceinline__ void from_smem(float* dst, int ldd, const float* src, int lds, int rows, int cols,
-                                          float f = 1.f) {
-    for (int idx = threadIdx.x; idx < rows * cols; idx += kNT) {
-        const int r = idx / cols, c = idx % cols;
-        dst[(size_t)r * ldd + c] = f * src[r * lds + c];
+
+// Transposing load: dst[c * ldd + r] = src[r * lds + c] for r < rows (zero for r >= valid),
+// c < COLS.  Consecutive threads take consecutive rows of one 16-byte column group, so the
+// shared-memory writes of a warp fall in distinct banks.
+template <typename G, int COLS>
+__device__ __forceinline__ void to_smem_t(float* dst, int ldd, const G* src, int lds, int rows, int valid) {
+    constexpr int V = 16 / sizeof(G);
+    static_assert(COLS % V == 0, "rows must be whole 16-byte vectors");
+    const int nvec = rows * (COLS / V);
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < nvec; idx += kNT) {
+        const int r = idx % rows, cv = idx / rows;
+        Vec16<G> x;
+        x.raw = r < valid ? ld_global_v4(src + (size_t)r * lds + cv * V) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < V; ++j) dst[(cv * V + j) * ldd + r] = x.get(j);
+    }
+}
+// Transposing store to global memory: dst[r * ldd + c] = src[c * lds + r], r < R, c < COLS
+// (R a multiple of 4, lds a multiple of 4 floats).
+template <int R, int COLS>
+__device__ __forceinline__ void from_smem_t(float* dst, int ldd, const float* src, int lds) {
+    for (int idx = threadIdx.x; idx < R * COLS / 4; idx += kNT) {
+        const int c = idx % COLS, r4 = (idx / COLS) * 4;
+        const float4 x = *reinterpret_cast<const float4*>(src + c * lds + r4);
+        dst[(size_t)r4 * ldd + c] = x.x;
+        dst[(size_t)(r4 + 1) * ldd + c] = x.y;
+        dst[(size_t)(r4 + 2) * ldd + c] = x.z;
+        dst[(size_t)(r4 + 3) * ldd + c] = x.w;
     }
 }
 
-// acc += sum_k a(m, k) b(k, n) with the thread tiling of block_gemm (no barriers).
-template <int M, int N, int K, class LA, class LB>
-__device__ __forceinline__ void gemm_acc(float (&acc)[GemmTile<M, N, kNT>::TM][GemmTile<M, N, kNT>::TN],
-                                         const LA& a, const LB& b) {
-    using G = GemmTile<M, N, kNT>;
-    const int tm = threadIdx.x / G::GN, tn = threadIdx.x % G::GN;
-#pragma unroll 4
-    for (int kk = 0; kk < K; ++kk) {
+// ------------------------------------------------------------------ register-tiled GEMM on K-major operands
+// Thread t owns the contiguous TM x TN output tile at rows m0 = (t / GN) TM, columns
+// n0 = (t % GN) TN.  A is read as A[k][m] and B as B[k][n] (K-major in shared memory, leading
+// dims and tile offsets multiples of 4 floats), so each k step fetches whole 16-byte vectors:
+// one 128-bit shared load per four values.
+template <int M, int N> struct VT {
+    static constexpr int TOT = M * N / kNT;
+    static constexpr int TN = TOT >= 32 ? 8 : (TOT >= 4 ? 4 : 1);
+    static constexpr int TM = TOT / TN;
+    static constexpr int GN = N / TN, GM = M / TM;
+    static_assert(TOT >= 1 && GM * GN == kNT && GM * TM == M && GN * TN == N, "gemm tiling");
+    static __device__ __forceinline__ int m0() { return (int)(threadIdx.x / GN) * TM; }
+    static __device__ __forceinline__ int n0() { return (int)(threadIdx.x % GN) * TN; }
+    using Acc = float[TM][TN];
+    static __device__ __forceinline__ void zero(Acc& a) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) a[i][j] = 0.f;
+    }
+};
+template <int W>
+__device__ __forceinline__ void lds_vec(float (&v)[W], const float* ptr) {
+    if constexpr (W % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < W; i += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(ptr + i);
+            v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+        }
+    } else if constexpr (W == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(ptr);
+        v[0] = x.x; v[1] = x.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = ptr[i];
+    }
+}
+template <int W>
+__device__ __forceinline__ void sts_vec(float* ptr, const float (&v)[W]) {
+    if constexpr (W % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < W; i += 4) *reinterpret_cast<float4*>(ptr + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else if constexpr (W == 2) {
+        *reinterpret_cast<float2*>(ptr) = make_float2(v[0], v[1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < W; ++i) ptr[i] = v[i];
+    }
+}
+// acc += A^T-major product: acc[i][j] += sum_k A[k][m0 + i] B[k][n0 + j]
+template <int M, int N, int K>
+__device__ __forceinline__ void vgemm(typename VT<M, N>::Acc& acc, const float* A, int lda, const float* B, int ldb) {
+    using G = VT<M, N>;
+    const float* a = A + G::m0();
+    const float* b = B + G::n0();
+#pragma unroll 2
+    for (int k = 0; k < K; ++k) {
         float av[G::TM], bv[G::TN];
-#pragma unroll
-        for (int i = 0; i < G::TM; ++i) av[i] = a(tm + i * G::GM, kk);
-#pragma unroll
-        for (int j = 0; j < G::TN; ++j) bv[j] = b(kk, tn + j * G::GN);
+        lds_vec<G::TM>(av, a + k * lda);
+        lds_vec<G::TN>(bv, b + k * ldb);
 #pragma unroll
         for (int i = 0; i < G::TM; ++i)
 #pragma unroll
             for (int j = 0; j < G::TN; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
 }
+// two products of the same shape and depth in one pass
+template <int M, int N, int K>
+__device__ __forceinline__ void vgemm2(typename VT<M, N>::Acc& c1, const float* A1, int lda1, const float* B1,
+                                       int ldb1, typename VT<M, N>::Acc& c2, const float* A2, int lda2,
+                                       const float* B2, int ldb2) {
+    using G = VT<M, N>;
+    const float *a1 = A1 + G::m0(), *b1 = B1 + G::n0(), *a2 = A2 + G::m0(), *b2 = B2 + G::n0();
+#pragma unroll 2
+    for (int k = 0; k < K; ++k) {
+        float av[G::TM], bv[G::TN], aw[G::TM], bw[G::TN];
+        lds_vec<G::TM>(av, a1 + k * lda1);
+        lds_vec<G::TN>(bv, b1 + k * ldb1);
+        lds_vec<G::TM>(aw, a2 + k * lda2);
+        lds_vec<G::TN>(bw, b2 + k * ldb2);
+#pragma unroll
+        for (int i = 0; i < G::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < G::TN; ++j) {
+                c1[i][j] = fmaf(av[i], bv[j], c1[i][j]);
+                c2[i][j] = fmaf(aw[i], bw[j], c2[i][j]);
+            }
+    }
+}
+// write f * acc to a row-major global array (leading dim ld) at the thread's tile
 template <int M, int N>
-__device__ __forceinline__ void store_acc(float* dst, int ld,
-                                          const float (&acc)[GemmTile<M, N, kNT>::TM][GemmTile<M, N, kNT>::TN],
-                                          float f) {
-    using G = GemmTile<M, N, kNT>;
-    const int tm = threadIdx.x / G::GN, tn = threadIdx.x % G::GN;
+__device__ __forceinline__ void store_tile(float* dst, int ld, const typename VT<M, N>::Acc& acc, float f) {
+    using G = VT<M, N>;
 #pragma unroll
-    for (int i = 0; i < G::TM; ++i)
+    for (int i = 0; i < G::TM; ++i) {
+        float v[G::TN];
 #pragma unroll
-        for (int j = 0; j < G::TN; ++j) dst[(size_t)(tm + i * G::GM) * ld + tn + j * G::GN] = f * acc[i][j];
+        for (int j = 0; j < G::TN; ++j) v[j] = f * acc[i][j];
+        sts_vec<G::TN>(dst + (size_t)(G::m0() + i) * ld + G::n0(), v);
+    }
+}
+// write acc transposed into shared memory: dst[(n0 + j) * ld + m0 + i] = acc[i][j]
+template <int M, int N>
+__device__ __forceinline__ void store_tile_t(float* dst, int ld, const typename VT<M, N>::Acc& acc) {
+    using G = VT<M, N>;
+#pragma unroll
+    for (int j = 0; j < G::TN; ++j) {
+        float v[G::TM];
+#pragma unroll
+        for (int i = 0; i < G::TM; ++i) v[i] = acc[i][j];
+        sts_vec<G::TM>(dst + (G::n0() + j) * ld + G::m0(), v);
+    }
 }
 
 // ------------------------------------------------------------------ shared-memory sizes (floats)
 template <int D> struct BwdSmem {
-    static constexpr int LDR = D + 1, LDS = kC + 1, LDP = D + 1;
+    static constexpr int LDP = D + 1;              // bwd_prep / bwd_local d x d tiles
+    static constexpr int LC = kC + 4, LD = D + 4;  // K-major GEMM operands (16-byte rows)
+    static constexpr int RK = (D * LC > kC * LD ? D * LC : kC * LD);
+    static constexpr int RV = (D * LC > kC * LC ? D * LC : kC * LC);
     static constexpr int prep = kC * D + kC + D * LDP + D;
-    static constexpr int chain = 4 * kC * LDR + kC * LDS + D * LDP + 5 * kC;
-    static constexpr int reduce = 4 * kC * LDR + 2 * kC * LDS + 4 * kC;
+    static constexpr int chain = 2 * D * LC + RK + RV + D * LD + 5 * kC;
+    static constexpr int reduce = 3 * kC * LD + 2 * kC * LC + kC;
     static constexpr int wbuf = (3 * kC > 2 * D ? 3 * kC : 2 * D);
     static constexpr int local = 6 * kC * D + 4 * kC + kNWL * wbuf;
     static_assert(3 * kC * D >= D * LDP, "dP must fit over the key, value and dk tiles");
@@ -283,29 +392,30 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
 }
 
 // ------------------------------------------------------------------ bwd_chain
+// Pair store layout (floats, per (n, m)): U [C][d], G [C][d], dS [C][C], P [C][C].
 template <typename T, int D>
 __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
-    constexpr int C = kC, LDR = BwdSmem<D>::LDR, LDS = BwdSmem<D>::LDS, LDP = BwdSmem<D>::LDP;
-    extern __shared__ float smem[];
-    float* sU = smem;            // [C][LDR] queries reaching key chunk m
-    float* sO = sU + C * LDR;    // [C][LDR] dO_n; the G chain later
-    float* sK = sO + C * LDR;    // [C][LDR] khat_m
-    float* sV = sK + C * LDR;    // [C][LDR] v_m; scale dS khat later
-    float* sS = sV + C * LDR;    // [C][LDS] S, then dS
-    float* sP = sS + C * LDS;    // [D][LDP] P_m^T (down the chain), P_m (up)
-    float* sL = sP + D * LDP;    // [C] lse_i
-    float* sD = sL + C;          // [C] Delta_i
-    float* sCi = sD + C;         // [C] c_i
-    float* sCj = sCi + C;        // [C] c_j
-    float* sRs = sCj + C;        // [C] FoX row sums of dS
+    using SM = BwdSmem<D>;
+    constexpr int C = kC, LC = SM::LC, LD = SM::LD;
+    extern __shared__ __align__(16) float smem[];
+    float* sUT = smem;             // [D][LC] U^T: the queries reaching key chunk m
+    float* sOT = sUT + D * LC;     // [D][LC] dO_n^T; G^T up the chain
+    float* sKT = sOT + D * LC;     // [D][LC] khat_m^T (down); khat_m [C][LD] (up)
+    float* sVT = sKT + SM::RK;     // [D][LC] v_m^T (down); dS_nm^T [C][LC] (up)
+    float* sP = sVT + SM::RV;      // [D][LD] P_m^T (down); P_m (up)
+    float* sL = sP + D * LD;       // [C] lse_i
+    float* sD = sL + C;            // [C] Delta_i
+    float* sCi = sD + C;           // [C] c_i
+    float* sCj = sCi + C;          // [C] c_j
+    float* sRs = sCj + C;          // [C] FoX row sums of dS
     const int n = p.N - 1 - blockIdx.x, bh = blockIdx.y;  // longest chains first
     const int b = n * C, c = min(C, p.L - b);
     const size_t hbase = (size_t)bh * p.L, pbase = (size_t)bh * p.Lp;
     const T* dO = static_cast<const T*>(p.dO);
     const T* v = static_cast<const T*>(p.v);
     const float scale = p.scale;
-    to_smem_v<float, D>(sU, LDR, p.qbar + (pbase + b) * D, D, C, C);
-    to_smem_v<T, D>(sO, LDR, dO + (hbase + b) * D, D, C, c);
+    to_smem_t<float, D>(sUT, LC, p.qbar + (pbase + b) * D, D, C, C);
+    to_smem_t<T, D>(sOT, LC, dO + (hbase + b) * D, D, C, c);
     for (int r = threadIdx.x; r < C; r += kNT) {
         sL[r] = r < c ? p.lse[hbase + b + r] : 0.f;
         sD[r] = p.delta[pbase + b + r];
@@ -313,61 +423,83 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
         sRs[r] = 0.f;
     }
     float* pairs_n = p.pairs + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2) * p.pair_floats;
+    using GS = VT<C, C>;
+    using GU = VT<C, D>;
     for (int m = n - 1; m >= 0; --m) {
         const int bm = m * C;
-        float* pr = pairs_n + (size_t)m * p.pair_floats;  // U [C][D], G [C][D], dS [C][C]
+        float* pr = pairs_n + (size_t)m * p.pair_floats;
         __syncthreads();
-        to_smem_v<float, D>(sK, LDR, p.khat + (pbase + bm) * D, D, C, C);
-        to_smem_v<T, D>(sV, LDR, v + (hbase + bm) * D, D, C, C);  // key chunks below n are full
-        if (m >= 1) to_smem_v<float, D>(sP, LDP, p.pmt + ((size_t)bh * p.N + m) * D * D, D, D, D);
+        to_smem_t<float, D>(sKT, LC, p.khat + (pbase + bm) * D, D, C, C);
+        to_smem_t<T, D>(sVT, LC, v + (hbase + bm) * D, D, C, C);  // key chunks below n are full
+        if (m >= 1) to_smem_v<float, D>(sP, LD, p.pmt + ((size_t)bh * p.N + m) * D * D, D, D, D);
         for (int r = threadIdx.x; r < C; r += kNT) sCj[r] = p.fox ? p.cum[pbase + bm + r] : 0.f;
         __syncthreads();
-        block_gemm<C, C, D, kNT>([&](int r, int kk) { return sU[r * LDR + kk]; },
-                                 [&](int kk, int j) { return sK[j * LDR + kk]; },
-                                 [&](int r, int j, float acc) { sS[r * LDS + j] = scale * acc + sCi[r] - sCj[j]; });
-        block_gemm<C, C, D, kNT>([&](int r, int kk) { return sO[r * LDR + kk]; },
-                                 [&](int kk, int j) { return sV[j * LDR + kk]; },
-                                 [&](int r, int j, float acc) {
-                                     float ds = 0.f;
-                                     if (r < c) ds = __expf(sS[r * LDS + j] - sL[r]) * (acc - sD[r]);
-                                     sS[r * LDS + j] = ds;
-                                     pr[2 * C * D + r * C + j] = ds;
-                                 });
-        if (p.fox)
-            for (int r = threadIdx.x; r < C; r += kNT) {
-                float t = 0.f;
-                for (int j = 0; j < C; ++j) t += sS[r * LDS + j];
-                sRs[r] += t;
+        // S = U khat^T and dO v^T in one pass; probabilities and dS straight from registers
+        typename GS::Acc aS, aP;
+        GS::zero(aS);
+        GS::zero(aP);
+        vgemm2<C, C, D>(aS, sUT, LC, sKT, LC, aP, sOT, LC, sVT, LC);
+        const int r0 = GS::m0(), j0 = GS::n0();
+#pragma unroll
+        for (int i = 0; i < GS::TM; ++i) {
+            const int r = r0 + i;
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < GS::TN; ++j) {
+                float pij = 0.f, ds = 0.f;
+                if (r < c) {
+                    pij = __expf(scale * aS[i][j] + sCi[r] - sCj[j0 + j] - sL[r]);
+                    ds = pij * (aP[i][j] - sD[r]);
+                }
+                aS[i][j] = pij;
+                aP[i][j] = ds;
+                rs += ds;
             }
-        from_smem(pr, D, sU, LDR, C, D);
-        if (m >= 1)  // U <- U P_m^T (the block_gemm barrier orders the store above before the overwrite)
-            block_gemm<C, D, D, kNT>([&](int r, int kk) { return sU[r * LDR + kk]; },
-                                     [&](int kk, int cc) { return sP[kk * LDP + cc]; },
-                                     [&](int r, int cc, float acc) { sU[r * LDR + cc] = acc; });
+            if (p.fox) {  // the GN threads of a row are consecutive lanes of one warp
+#pragma unroll
+                for (int o = 1; o < GS::GN; o <<= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+                if (threadIdx.x % GS::GN == 0) sRs[r] += rs;
+            }
+        }
+        store_tile<C, C>(pr + 2 * C * D, C, aP, 1.f);
+        store_tile<C, C>(pr + 2 * C * D + C * C, C, aS, 1.f);
+        from_smem_t<C, D>(pr, D, sUT, LC);  // U_{n,m}
+        if (m >= 1) {  // U <- U P_m^T
+            typename GU::Acc aU;
+            GU::zero(aU);
+            vgemm<C, D, D>(aU, sUT, LC, sP, LD);
+            __syncthreads();
+            store_tile_t<C, D>(sUT, LC, aU);
+        }
     }
-    float* sG = sO;
-    float* sT = sV;
+    float* sGT = sOT;
+    float* sK = sKT;
+    float* sST = sVT;
     for (int m = 0; m < n; ++m) {
         const int bm = m * C;
         float* pr = pairs_n + (size_t)m * p.pair_floats;
         __syncthreads();
-        to_smem_v<float, D>(sK, LDR, p.khat + (pbase + bm) * D, D, C, C);
-        to_smem_v<float, C>(sS, LDS, pr + 2 * C * D, C, C, C);
+        to_smem_v<float, D>(sK, LD, p.khat + (pbase + bm) * D, D, C, C);
+        to_smem_t<float, C>(sST, LC, pr + 2 * C * D, C, C, C);
         if (m >= 1) {
-            to_smem_v<float, D>(sP, LDP, p.pm + ((size_t)bh * p.N + m) * D * D, D, D, D);
-            from_smem(pr + C * D, D, sG, LDR, C, D);  // G_{n,m-1}
+            to_smem_v<float, D>(sP, LD, p.pm + ((size_t)bh * p.N + m) * D * D, D, D, D);
+            from_smem_t<C, D>(pr + C * D, D, sGT, LC);  // G_{n,m-1}
         }
         __syncthreads();
-        float* dst = m == 0 ? sG : sT;
-        block_gemm<C, D, C, kNT>([&](int r, int kk) { return sS[r * LDS + kk]; },
-                                 [&](int kk, int cc) { return sK[kk * LDR + cc]; },
-                                 [&](int r, int cc, float acc) { dst[r * LDR + cc] = scale * acc; });
-        if (m >= 1)
-            block_gemm<C, D, D, kNT>([&](int r, int kk) { return sG[r * LDR + kk]; },
-                                     [&](int kk, int cc) { return sP[kk * LDP + cc]; },
-                                     [&](int r, int cc, float acc) { sG[r * LDR + cc] = acc + sT[r * LDR + cc]; });
+        typename GU::Acc aT, aG;
+        GU::zero(aT);
+        GU::zero(aG);
+        vgemm<C, D, C>(aT, sST, LC, sK, LD);             // dS khat
+        if (m >= 1) vgemm<C, D, D>(aG, sGT, LC, sP, LD);  // G P_m
+#pragma unroll
+        for (int i = 0; i < GU::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < GU::TN; ++j) aG[i][j] = fmaf(scale, aT[i][j], aG[i][j]);
+        __syncthreads();
+        store_tile_t<C, D>(sGT, LC, aG);
     }
-    from_smem(p.dqbar + (pbase + b) * D, D, sG, LDR, C, D);
+    __syncthreads();
+    from_smem_t<C, D>(p.dqbar + (pbase + b) * D, D, sGT, LC);
     if (p.fox)
         for (int r = threadIdx.x; r < C; r += kNT) p.dcrow[pbase + b + r] = sRs[r];
 }
@@ -375,73 +507,49 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
 // ------------------------------------------------------------------ bwd_reduce
 template <typename T, int D>
 __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
-    constexpr int C = kC, LDR = BwdSmem<D>::LDR, LDS = BwdSmem<D>::LDS;
-    extern __shared__ float smem[];
-    float* sK = smem;           // [C][LDR] khat_m
-    float* sU = sK + C * LDR;   // [C][LDR] U_{n,m}
-    float* sO = sU + C * LDR;   // [C][LDR] dO_n
-    float* sG = sO + C * LDR;   // [C][LDR] G_{n,m-1}
-    float* sS = sG + C * LDR;   // [C][LDS] dS_nm
-    float* sA = sS + C * LDS;   // [C][LDS] softmax probabilities P_nm
-    float* sL = sA + C * LDS;   // [C] lse_i
-    float* sCi = sL + C;        // [C] c_i
-    float* sCj = sCi + C;       // [C] c_j
-    float* sCs = sCj + C;       // [C] FoX column sums of dS
+    using SM = BwdSmem<D>;
+    constexpr int C = kC, LC = SM::LC, LD = SM::LD;
+    extern __shared__ __align__(16) float smem[];
+    float* sU = smem;           // [C][LD] U_{n,m}
+    float* sG = sU + C * LD;    // [C][LD] G_{n,m-1}
+    float* sO = sG + C * LD;    // [C][LD] dO_n
+    float* sS = sO + C * LD;    // [C][LC] dS_nm
+    float* sA = sS + C * LC;    // [C][LC] softmax probabilities P_nm
+    float* sCs = sA + C * LC;   // [C] FoX column sums of dS
     const int m = blockIdx.x, bh = blockIdx.y, bm = m * C;  // m = 0 has the most query chunks
     const size_t hbase = (size_t)bh * p.L, pbase = (size_t)bh * p.Lp;
     const T* dO = static_cast<const T*>(p.dO);
-    const float scale = p.scale;
-    to_smem_v<float, D>(sK, LDR, p.khat + (pbase + bm) * D, D, C, C);
-    for (int r = threadIdx.x; r < C; r += kNT) {
-        sCj[r] = p.fox ? p.cum[pbase + bm + r] : 0.f;
-        sCs[r] = 0.f;
-    }
-    using GV = GemmTile<C, D, kNT>;
-    using GP = GemmTile<D, D, kNT>;
-    float accV[GV::TM][GV::TN], accK[GV::TM][GV::TN], accP[GP::TM][GP::TN];
-#pragma unroll
-    for (int i = 0; i < GV::TM; ++i)
-#pragma unroll
-        for (int j = 0; j < GV::TN; ++j) accV[i][j] = accK[i][j] = 0.f;
-#pragma unroll
-    for (int i = 0; i < GP::TM; ++i)
-#pragma unroll
-        for (int j = 0; j < GP::TN; ++j) accP[i][j] = 0.f;
+    for (int r = threadIdx.x; r < C; r += kNT) sCs[r] = 0.f;
+    using GV = VT<C, D>;
+    using GP = VT<D, D>;
+    typename GV::Acc accV, accK;
+    typename GP::Acc accP;
+    GV::zero(accV);
+    GV::zero(accK);
+    GP::zero(accP);
     for (int n = m + 1; n < p.N; ++n) {
         const int b = n * C, c = min(C, p.L - b);
         const float* pr = p.pairs + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2 + m) * p.pair_floats;
         __syncthreads();
-        to_smem_v<float, D>(sU, LDR, pr, D, C, C);
-        to_smem_v<float, C>(sS, LDS, pr + 2 * C * D, C, C, C);
-        if (m >= 1) to_smem_v<float, D>(sG, LDR, pr + C * D, D, C, C);
-        to_smem_v<T, D>(sO, LDR, dO + (hbase + b) * D, D, C, c);
-        for (int r = threadIdx.x; r < C; r += kNT) {
-            sL[r] = r < c ? p.lse[hbase + b + r] : 0.f;
-            sCi[r] = p.fox ? p.cum[pbase + b + r] : 0.f;
-        }
+        to_smem_v<float, D>(sU, LD, pr, D, C, C);
+        if (m >= 1) to_smem_v<float, D>(sG, LD, pr + C * D, D, C, C);
+        to_smem_v<T, D>(sO, LD, dO + (hbase + b) * D, D, C, c);
+        to_smem_v<float, C>(sS, LC, pr + 2 * C * D, C, C, C);
+        to_smem_v<float, C>(sA, LC, pr + 2 * C * D + C * C, C, C, C);
         __syncthreads();
-        block_gemm<C, C, D, kNT>([&](int r, int kk) { return sU[r * LDR + kk]; },
-                                 [&](int kk, int j) { return sK[j * LDR + kk]; },
-                                 [&](int r, int j, float acc) {
-                                     sA[r * LDS + j] = r < c ? __expf(scale * acc + sCi[r] - sCj[j] - sL[r]) : 0.f;
-                                 });
-        gemm_acc<C, D, C>(accV, [&](int j, int i) { return sA[i * LDS + j]; },
-                          [&](int i, int cc) { return sO[i * LDR + cc]; });
-        gemm_acc<C, D, C>(accK, [&](int j, int i) { return sS[i * LDS + j]; },
-                          [&](int i, int cc) { return sU[i * LDR + cc]; });
-        if (m >= 1)
-            gemm_acc<D, D, C>(accP, [&](int r, int i) { return sG[i * LDR + r]; },
-                              [&](int i, int cc) { return sU[i * LDR + cc]; });
+        vgemm<C, D, C>(accV, sA, LC, sO, LD);             // dV_m  += P^T dO_n
+        vgemm<C, D, C>(accK, sS, LC, sU, LD);             // dKhat += dS^T U   (scaled at the end)
+        if (m >= 1) vgemm<D, D, C>(accP, sG, LD, sU, LD);  // dP_m  += G^T U
         if (p.fox)
             for (int j = threadIdx.x; j < C; j += kNT) {
                 float t = 0.f;
-                for (int i = 0; i < C; ++i) t += sS[i * LDS + j];
+                for (int i = 0; i < C; ++i) t += sS[i * LC + j];
                 sCs[j] += t;
             }
     }
-    store_acc<C, D>(p.dvoff + (pbase + bm) * D, D, accV, 1.f);
-    store_acc<C, D>(p.dkhat + (pbase + bm) * D, D, accK, scale);
-    if (m >= 1) store_acc<D, D>(p.dpm + ((size_t)bh * p.N + m) * D * D, D, accP, 1.f);
+    store_tile<C, D>(p.dvoff + (pbase + bm) * D, D, accV, 1.f);
+    store_tile<C, D>(p.dkhat + (pbase + bm) * D, D, accK, p.scale);
+    if (m >= 1) store_tile<D, D>(p.dpm + ((size_t)bh * p.N + m) * D * D, D, accP, 1.f);
     __syncthreads();
     if (p.fox)
         for (int j = threadIdx.x; j < C; j += kNT) p.dccol[pbase + bm + j] = sCs[j];

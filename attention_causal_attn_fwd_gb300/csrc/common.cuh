@@ -161,9 +161,9 @@ inline DecLayout dec_layout(int B, int H, int n_max, int d) {
 //   dpm   : float [BH, N, d, d] gradient w.r.t. P_m
 //   dcrow, dccol, dctot : float [BH, Lp]  FoX: gradient w.r.t. the cumulative
 //                         sums (row part, column part, total)
-//   pairs : float [BH, N(N-1)/2, 2 C d + C C]  per (query chunk n, key chunk
-//           m < n): the transported queries U_{n,m}, the chain gradient
-//           G_{n,m-1} and the logit gradient dS_{nm}
+//   pairs : float [BH, N(N-1)/2, 2 C d + 2 C C]  per (query chunk n, key
+//           chunk m < n): the transported queries U_{n,m}, the chain gradient
+//           G_{n,m-1}, the logit gradient dS_{nm} and the probabilities P_{nm}
 constexpr int kBwdC = 64;
 struct BwdLayout {
     size_t qbar, khat, pm, pmt, delta, cum, dqbar, dkhat, dvoff, dpm, dcrow, dccol, dctot, pairs, total;
@@ -177,7 +177,7 @@ inline BwdLayout bwd_layout(int B, int H, int L, int d) {
     s.N = cdiv(L, C);
     s.Lp = s.N * C;
     const size_t BH = (size_t)B * H, rows = BH * s.Lp;
-    s.pair_floats = 2 * (size_t)C * d + (size_t)C * C;
+    s.pair_floats = 2 * (size_t)C * d + 2 * (size_t)C * C;
     s.head_pairs = (size_t)s.N * (s.N - 1) / 2;
     size_t off = sizeof(WsHeader);
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };

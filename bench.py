@@ -454,11 +454,11 @@ def run_ours(args, rank, world, local):
         bms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
         kms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
         # fp32 FLOPs of the chunk-pair kernels (bwd_chain + bwd_reduce), C = 64: per (query chunk,
-        # earlier key chunk) pair six C x C x d products (S twice, dO V^T, dS khat, P^T dO,
-        # dS^T U) and, past the first key chunk, three C x d x d ones (U P^T, G P, G^T U)
+        # earlier key chunk) pair five C x C x d products (S, dO V^T, dS khat, P^T dO, dS^T U) and,
+        # past the first key chunk, three C x d x d ones (U P^T, G P, G^T U)
         C, nc = 64, -(-fc.L // 64)
         pairs = nc * (nc - 1) // 2
-        pair_flops = fc.B * fc.H * (pairs * 6 * 2 * C * C * fc.d + (pairs - (nc - 1)) * 3 * 2 * C * fc.d * fc.d)
+        pair_flops = fc.B * fc.H * (pairs * 5 * 2 * C * C * fc.d + (pairs - (nc - 1)) * 3 * 2 * C * fc.d * fc.d)
         fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x fp32 lanes x FMA x max SM clock
         ach = pair_flops / (kms * 1e-3) / 1e12
         bwd = {"ms": bms, "attn_equiv_tflops": 2.5 * fc.attn_flops / (bms * 1e-3) / 1e12, "steps": args.bwd_steps,
