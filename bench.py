@@ -460,6 +460,8 @@ def run_ours(args, rank, world, local):
         pairs = nc * (nc - 1) // 2
         pair_flops = fc.B * fc.H * (pairs * 5 * 2 * C * C * fc.d + (pairs - (nc - 1)) * 3 * 2 * C * fc.d * fc.d)
         fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x fp32 lanes x FMA x max SM clock
+        tc, tr = _traffic("bwd_chain", fc.B * fc.H), _traffic("bwd_reduce", fc.B * fc.H)
+        bwd_traffic = tc + tr if tc is not None and tr is not None else None
         ach = pair_flops / (kms * 1e-3) / 1e12
         bwd = {"ms": bms, "attn_equiv_tflops": 2.5 * fc.attn_flops / (bms * 1e-3) / 1e12, "steps": args.bwd_steps,
                "workload": "PaTH backward B%d H%d L%d d%d bf16 (dq, dk, dv, dw, dbeta for a seeded dO); "
@@ -468,7 +470,7 @@ def run_ours(args, rank, world, local):
                "roofline": {"kernel": "bwd_chain + bwd_reduce (fp32 CUDA cores)", "bound": "alu", "achieved": ach,
                             "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach / fp32_peak,
                             "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                            "traffic": None, "flops_per_launch": float(pair_flops), "kernel_ms": kms}}
+                            "traffic": bwd_traffic, "flops_per_launch": float(pair_flops), "kernel_ms": kms}}
         del o_b, lse_b, dO_b, ws_b
 
     cpu = None
