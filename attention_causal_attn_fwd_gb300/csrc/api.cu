@@ -153,7 +153,7 @@ int path_prefill_kcache(const void* k, const void* w, const float* beta, void* k
 size_t path_attn_bwd_workspace_bytes(int B, int H, int L, int d, int dtype) {
     if (B < 1 || H < 1 || L < 1 || (long long)B * H > 65535 || !bwd_supported(d)) return 0;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return 0;
-    return bwd_layout(B, H, L, d).total;
+    return bwd_layout(B, H, L, d, elt_size(dtype)).total;
 }
 
 int path_attn_bwd(const void* q, const void* k, const void* v, const void* w, const float* beta,
@@ -172,7 +172,7 @@ int path_attn_bwd(const void* q, const void* k, const void* v, const void* w, co
     for (const void* p : ptrs)
         if (!aligned16(p)) return PATH_ERR_INVALID;
     if (log_f && (!aligned16(log_f) || !aligned16(dlog_f))) return PATH_ERR_INVALID;
-    const BwdLayout lay = bwd_layout(B, H, L, d);
+    const BwdLayout lay = bwd_layout(B, H, L, d, elt_size(dtype));
     if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PATH_ERR_WORKSPACE;
     cudaError_t e = attn_bwd(dtype, d, q, k, v, w, beta, log_f, o, lse, dO, dq, dk, dv, dw, dbeta,
                              log_f ? dlog_f : nullptr, B * H, L, scale, static_cast<unsigned char*>(workspace), lay,

@@ -32,7 +32,10 @@
 //                                       G and dS per (n, m) pair; dQbar
 //   bwd_reduce one CTA per key chunk    dV_m, dKhat_m, dP_m summed over the
 //                                       query chunks (each output owned by
-//                                       one CTA, so no global atomics)
+//                                       one CTA, so no global atomics); for
+//                                       bf16 at d = 128 bwd_reduce_tc
+//                                       (csrc/bwd_tc.cu) does this on the
+//                                       tensor cores from the bf16 pair store
 //   bwd_local  one CTA per chunk        diagonal block and the within-chunk
 //                                       walks in reverse; writes dq, dk, dv,
 //                                       dw, dbeta (shared-memory atomics)
@@ -43,6 +46,10 @@
 #include "ut_prep.cuh"
 
 namespace pathattn {
+
+cudaError_t launch_bwd_reduce_tc(const void* dO, const void* pairs, float* dvoff, float* dkhat, float* dpm, int BH,
+                                 int L, int Lp, int N, size_t head_pairs, float scale, WsHeader* hdr,
+                                 cudaStream_t st);
 
 namespace {
 
@@ -57,9 +64,10 @@ struct BwdParams {
     const float *beta, *lse;
     void *dq, *dk, *dv, *dw;
     float *dbeta, *dlog_f;
-    float *qbar, *khat, *pm, *pmt, *delta, *cum, *dqbar, *dkhat, *dvoff, *dpm, *dcrow, *dccol, *dctot, *pairs;
+    float *qbar, *khat, *pm, *pmt, *delta, *cum, *dqbar, *dkhat, *dvoff, *dpm, *dcrow, *dccol, *dctot;
+    void* pairs;  // pair store, elements of the input dtype
     int L, Lp, N;
-    size_t pair_floats, head_pairs;
+    size_t pair_elems, head_pairs;
     float scale;
     int fox;
 };
@@ -173,15 +181,15 @@ __device__ __forceinline__ void to_smem_t(float* dst, int ldd, const G* src, int
 }
 // Transposing store to global memory: dst[r * ldd + c] = src[c * lds + r], r < R, c < COLS
 // (R a multiple of 4, lds a multiple of 4 floats).
-template <int R, int COLS>
-__device__ __forceinline__ void from_smem_t(float* dst, int ldd, const float* src, int lds) {
+template <int R, int COLS, typename G>
+__device__ __forceinline__ void from_smem_t(G* dst, int ldd, const float* src, int lds) {
     for (int idx = threadIdx.x; idx < R * COLS / 4; idx += kNT) {
         const int c = idx % COLS, r4 = (idx / COLS) * 4;
         const float4 x = *reinterpret_cast<const float4*>(src + c * lds + r4);
-        dst[(size_t)r4 * ldd + c] = x.x;
-        dst[(size_t)(r4 + 1) * ldd + c] = x.y;
-        dst[(size_t)(r4 + 2) * ldd + c] = x.z;
-        dst[(size_t)(r4 + 3) * ldd + c] = x.w;
+        dst[(size_t)r4 * ldd + c] = from_f<G>(x.x);
+        dst[(size_t)(r4 + 1) * ldd + c] = from_f<G>(x.y);
+        dst[(size_t)(r4 + 2) * ldd + c] = from_f<G>(x.z);
+        dst[(size_t)(r4 + 3) * ldd + c] = from_f<G>(x.w);
     }
 }
 
@@ -275,15 +283,21 @@ __device__ __forceinline__ void vgemm2(typename VT<M, N>::Acc& c1, const float* 
     }
 }
 // write f * acc to a row-major global array (leading dim ld) at the thread's tile
-template <int M, int N>
-__device__ __forceinline__ void store_tile(float* dst, int ld, const typename VT<M, N>::Acc& acc, float f) {
+template <int M, int N, typename E = float>
+__device__ __forceinline__ void store_tile(E* dst, int ld, const typename VT<M, N>::Acc& acc, float f) {
     using G = VT<M, N>;
 #pragma unroll
     for (int i = 0; i < G::TM; ++i) {
         float v[G::TN];
 #pragma unroll
         for (int j = 0; j < G::TN; ++j) v[j] = f * acc[i][j];
-        sts_vec<G::TN>(dst + (size_t)(G::m0() + i) * ld + G::n0(), v);
+        E* d = dst + (size_t)(G::m0() + i) * ld + G::n0();
+        if constexpr (sizeof(E) == 4) {
+            sts_vec<G::TN>(reinterpret_cast<float*>(d), v);
+        } else {
+#pragma unroll
+            for (int j = 0; j < G::TN; ++j) d[j] = from_f<E>(v[j]);
+        }
     }
 }
 // write acc transposed into shared memory: dst[(n0 + j) * ld + m0 + i] = acc[i][j]
@@ -306,8 +320,8 @@ template <int D> struct BwdSmem {
     static constexpr int RK = (D * LC > kC * LD ? D * LC : kC * LD);
     static constexpr int RV = (D * LC > kC * LC ? D * LC : kC * LC);
     static constexpr int prep = kC * D + kC + D * LDP + D;
-    static constexpr int chain = 2 * D * LC + RK + RV + D * LD + 5 * kC;
-    static constexpr int reduce = 3 * kC * LD + 2 * kC * LC + kC;
+    static constexpr int chain = 2 * D * LC + RK + RV + D * LD + 6 * kC;
+    static constexpr int reduce = 3 * kC * LD + 2 * kC * LC;
     static constexpr int wbuf = (3 * kC > 2 * D ? 3 * kC : 2 * D);
     static constexpr int local = 6 * kC * D + 4 * kC + kNWL * wbuf;
     static_assert(3 * kC * D >= D * LDP, "dP must fit over the key, value and dk tiles");
@@ -408,6 +422,7 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
     float* sCi = sD + C;           // [C] c_i
     float* sCj = sCi + C;          // [C] c_j
     float* sRs = sCj + C;          // [C] FoX row sums of dS
+    float* sCs = sRs + C;          // [C] FoX column sums of dS_nm (added to the key chunk's dccol)
     const int n = p.N - 1 - blockIdx.x, bh = blockIdx.y;  // longest chains first
     const int b = n * C, c = min(C, p.L - b);
     const size_t hbase = (size_t)bh * p.L, pbase = (size_t)bh * p.Lp;
@@ -421,14 +436,20 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
         sD[r] = p.delta[pbase + b + r];
         sCi[r] = p.fox ? p.cum[pbase + b + r] : 0.f;
         sRs[r] = 0.f;
+        sCs[r] = 0.f;
     }
-    float* pairs_n = p.pairs + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2) * p.pair_floats;
+    T* pairs_n = static_cast<T*>(p.pairs) + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2) * p.pair_elems;
     using GS = VT<C, C>;
     using GU = VT<C, D>;
     for (int m = n - 1; m >= 0; --m) {
         const int bm = m * C;
-        float* pr = pairs_n + (size_t)m * p.pair_floats;
+        T* pr = pairs_n + (size_t)m * p.pair_elems;  // U [C][D], G [C][D], dS [C][C], P [C][C]
         __syncthreads();
+        if (p.fox && m < n - 1)  // the previous key chunk's column sums of dS
+            for (int j = threadIdx.x; j < C; j += kNT) {
+                atomicAdd(p.dccol + pbase + bm + C + j, sCs[j]);
+                sCs[j] = 0.f;
+            }
         to_smem_t<float, D>(sKT, LC, p.khat + (pbase + bm) * D, D, C, C);
         to_smem_t<T, D>(sVT, LC, v + (hbase + bm) * D, D, C, C);  // key chunks below n are full
         if (m >= 1) to_smem_v<float, D>(sP, LD, p.pmt + ((size_t)bh * p.N + m) * D * D, D, D, D);
@@ -461,8 +482,16 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
                 if (threadIdx.x % GS::GN == 0) sRs[r] += rs;
             }
         }
-        store_tile<C, C>(pr + 2 * C * D, C, aP, 1.f);
-        store_tile<C, C>(pr + 2 * C * D + C * C, C, aS, 1.f);
+        if (p.fox)
+#pragma unroll
+            for (int j = 0; j < GS::TN; ++j) {
+                float cs = 0.f;
+#pragma unroll
+                for (int i = 0; i < GS::TM; ++i) cs += aP[i][j];
+                atomicAdd(sCs + j0 + j, cs);
+            }
+        store_tile<C, C, T>(pr + 2 * C * D, C, aP, 1.f);
+        store_tile<C, C, T>(pr + 2 * C * D + C * C, C, aS, 1.f);
         from_smem_t<C, D>(pr, D, sUT, LC);  // U_{n,m}
         if (m >= 1) {  // U <- U P_m^T
             typename GU::Acc aU;
@@ -472,15 +501,18 @@ __global__ void __launch_bounds__(kNT) bwd_chain(BwdParams p) {
             store_tile_t<C, D>(sUT, LC, aU);
         }
     }
+    __syncthreads();
+    if (p.fox)  // key chunk 0's column sums
+        for (int j = threadIdx.x; j < C; j += kNT) atomicAdd(p.dccol + pbase + j, sCs[j]);
     float* sGT = sOT;
     float* sK = sKT;
     float* sST = sVT;
     for (int m = 0; m < n; ++m) {
         const int bm = m * C;
-        float* pr = pairs_n + (size_t)m * p.pair_floats;
+        T* pr = pairs_n + (size_t)m * p.pair_elems;
         __syncthreads();
         to_smem_v<float, D>(sK, LD, p.khat + (pbase + bm) * D, D, C, C);
-        to_smem_t<float, C>(sST, LC, pr + 2 * C * D, C, C, C);
+        to_smem_t<T, C>(sST, LC, pr + 2 * C * D, C, C, C);
         if (m >= 1) {
             to_smem_v<float, D>(sP, LD, p.pm + ((size_t)bh * p.N + m) * D * D, D, D, D);
             from_smem_t<C, D>(pr + C * D, D, sGT, LC);  // G_{n,m-1}
@@ -515,11 +547,9 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
     float* sO = sG + C * LD;    // [C][LD] dO_n
     float* sS = sO + C * LD;    // [C][LC] dS_nm
     float* sA = sS + C * LC;    // [C][LC] softmax probabilities P_nm
-    float* sCs = sA + C * LC;   // [C] FoX column sums of dS
     const int m = blockIdx.x, bh = blockIdx.y, bm = m * C;  // m = 0 has the most query chunks
     const size_t hbase = (size_t)bh * p.L, pbase = (size_t)bh * p.Lp;
     const T* dO = static_cast<const T*>(p.dO);
-    for (int r = threadIdx.x; r < C; r += kNT) sCs[r] = 0.f;
     using GV = VT<C, D>;
     using GP = VT<D, D>;
     typename GV::Acc accV, accK;
@@ -529,30 +559,21 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
     GP::zero(accP);
     for (int n = m + 1; n < p.N; ++n) {
         const int b = n * C, c = min(C, p.L - b);
-        const float* pr = p.pairs + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2 + m) * p.pair_floats;
+        const T* pr = static_cast<const T*>(p.pairs) + ((size_t)bh * p.head_pairs + (size_t)n * (n - 1) / 2 + m) * p.pair_elems;
         __syncthreads();
-        to_smem_v<float, D>(sU, LD, pr, D, C, C);
-        if (m >= 1) to_smem_v<float, D>(sG, LD, pr + C * D, D, C, C);
+        to_smem_v<T, D>(sU, LD, pr, D, C, C);
+        if (m >= 1) to_smem_v<T, D>(sG, LD, pr + C * D, D, C, C);
         to_smem_v<T, D>(sO, LD, dO + (hbase + b) * D, D, C, c);
-        to_smem_v<float, C>(sS, LC, pr + 2 * C * D, C, C, C);
-        to_smem_v<float, C>(sA, LC, pr + 2 * C * D + C * C, C, C, C);
+        to_smem_v<T, C>(sS, LC, pr + 2 * C * D, C, C, C);
+        to_smem_v<T, C>(sA, LC, pr + 2 * C * D + C * C, C, C, C);
         __syncthreads();
         vgemm<C, D, C>(accV, sA, LC, sO, LD);             // dV_m  += P^T dO_n
         vgemm<C, D, C>(accK, sS, LC, sU, LD);             // dKhat += dS^T U   (scaled at the end)
         if (m >= 1) vgemm<D, D, C>(accP, sG, LD, sU, LD);  // dP_m  += G^T U
-        if (p.fox)
-            for (int j = threadIdx.x; j < C; j += kNT) {
-                float t = 0.f;
-                for (int i = 0; i < C; ++i) t += sS[i * LC + j];
-                sCs[j] += t;
-            }
     }
     store_tile<C, D>(p.dvoff + (pbase + bm) * D, D, accV, 1.f);
     store_tile<C, D>(p.dkhat + (pbase + bm) * D, D, accK, p.scale);
     if (m >= 1) store_tile<D, D>(p.dpm + ((size_t)bh * p.N + m) * D * D, D, accP, 1.f);
-    __syncthreads();
-    if (p.fox)
-        for (int j = threadIdx.x; j < C; j += kNT) p.dccol[pbase + bm + j] = sCs[j];
 }
 
 // ------------------------------------------------------------------ bwd_local
@@ -764,7 +785,7 @@ __global__ void __launch_bounds__(1024) bwd_fox_suffix(const float* __restrict__
 }
 
 template <typename T, int D>
-cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, cudaStream_t st) {
+cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigned char* ws, cudaStream_t st) {
     using S = BwdSmem<D>;
     const size_t b_prep = S::prep * sizeof(float), b_chain = S::chain * sizeof(float),
                  b_reduce = S::reduce * sizeof(float), b_local = S::local * sizeof(float);
@@ -772,14 +793,23 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, cudaStr
     cudaFuncSetAttribute(bwd_chain<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_chain);
     cudaFuncSetAttribute(bwd_reduce<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_reduce);
     cudaFuncSetAttribute(bwd_local<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_local);
-    if (log_f) fox_cumsum<<<BH, 1024, 0, st>>>(log_f, p.L, p.Lp, p.cum);
-    bwd_prep<T, D><<<dim3(p.N, BH), kNT, b_prep, st>>>(p);
-    mark_start(st);
-    if (p.N >= 2) {
-        bwd_chain<T, D><<<dim3(p.N - 1, BH), kNT, b_chain, st>>>(p);
-        bwd_reduce<T, D><<<dim3(p.N - 1, BH), kNT, b_reduce, st>>>(p);
+    if (log_f) {
+        fox_cumsum<<<BH, 1024, 0, st>>>(log_f, p.L, p.Lp, p.cum);
+        cudaMemsetAsync(p.dccol, 0, (size_t)BH * p.Lp * sizeof(float), st);  // bwd_chain adds column sums
     }
-    mark_end(st);
+    bwd_prep<T, D><<<dim3(p.N, BH), kNT, b_prep, st>>>(p);
+    if (p.N >= 2) {
+        mark_start(st);
+        bwd_chain<T, D><<<dim3(p.N - 1, BH), kNT, b_chain, st>>>(p);
+        mark_end(st);
+        if constexpr (sizeof(T) == 2 && D == 128) {  // bf16 pairs: tensor-core reduction (csrc/bwd_tc.cu)
+            cudaError_t e = launch_bwd_reduce_tc(p.dO, p.pairs, p.dvoff, p.dkhat, p.dpm, BH, p.L, p.Lp, p.N,
+                                                 p.head_pairs, p.scale, reinterpret_cast<WsHeader*>(ws), st);
+            if (e != cudaSuccess) return e;
+        } else {
+            bwd_reduce<T, D><<<dim3(p.N - 1, BH), kNT, b_reduce, st>>>(p);
+        }
+    }
     bwd_local<T, D><<<dim3(p.N, BH), kNTL, b_local, st>>>(p);
     if (log_f) bwd_fox_suffix<<<BH, 1024, 0, st>>>(p.dctot, p.L, p.Lp, p.dlog_f);
     return cudaGetLastError();
@@ -801,19 +831,19 @@ cudaError_t attn_bwd(int dtype, int d, const void* q, const void* k, const void*
     p.qbar = f(lay.qbar); p.khat = f(lay.khat); p.pm = f(lay.pm); p.pmt = f(lay.pmt);
     p.delta = f(lay.delta); p.cum = f(lay.cum); p.dqbar = f(lay.dqbar); p.dkhat = f(lay.dkhat);
     p.dvoff = f(lay.dvoff); p.dpm = f(lay.dpm); p.dcrow = f(lay.dcrow); p.dccol = f(lay.dccol);
-    p.dctot = f(lay.dctot); p.pairs = f(lay.pairs);
+    p.dctot = f(lay.dctot); p.pairs = ws + lay.pairs;
     p.L = L; p.Lp = lay.Lp; p.N = lay.N;
-    p.pair_floats = lay.pair_floats; p.head_pairs = lay.head_pairs;
+    p.pair_elems = lay.pair_elems; p.head_pairs = lay.head_pairs;
     p.scale = scale;
     p.fox = log_f != nullptr;
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), st);
     if (e != cudaSuccess) return e;
     const bool bf = dtype == PATH_BF16;
     switch (d) {
-        case 16: return bf ? launch_bwd_t<__nv_bfloat16, 16>(p, BH, log_f, st) : launch_bwd_t<float, 16>(p, BH, log_f, st);
-        case 32: return bf ? launch_bwd_t<__nv_bfloat16, 32>(p, BH, log_f, st) : launch_bwd_t<float, 32>(p, BH, log_f, st);
-        case 64: return bf ? launch_bwd_t<__nv_bfloat16, 64>(p, BH, log_f, st) : launch_bwd_t<float, 64>(p, BH, log_f, st);
-        case 128: return bf ? launch_bwd_t<__nv_bfloat16, 128>(p, BH, log_f, st) : launch_bwd_t<float, 128>(p, BH, log_f, st);
+        case 16: return bf ? launch_bwd_t<__nv_bfloat16, 16>(p, BH, log_f, ws, st) : launch_bwd_t<float, 16>(p, BH, log_f, ws, st);
+        case 32: return bf ? launch_bwd_t<__nv_bfloat16, 32>(p, BH, log_f, ws, st) : launch_bwd_t<float, 32>(p, BH, log_f, ws, st);
+        case 64: return bf ? launch_bwd_t<__nv_bfloat16, 64>(p, BH, log_f, ws, st) : launch_bwd_t<float, 64>(p, BH, log_f, ws, st);
+        case 128: return bf ? launch_bwd_t<__nv_bfloat16, 128>(p, BH, log_f, ws, st) : launch_bwd_t<float, 128>(p, BH, log_f, ws, st);
         default: return cudaErrorInvalidValue;
     }
 }

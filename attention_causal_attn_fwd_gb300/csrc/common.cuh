@@ -161,23 +161,24 @@ inline DecLayout dec_layout(int B, int H, int n_max, int d) {
 //   dpm   : float [BH, N, d, d] gradient w.r.t. P_m
 //   dcrow, dccol, dctot : float [BH, Lp]  FoX: gradient w.r.t. the cumulative
 //                         sums (row part, column part, total)
-//   pairs : float [BH, N(N-1)/2, 2 C d + 2 C C]  per (query chunk n, key
-//           chunk m < n): the transported queries U_{n,m}, the chain gradient
-//           G_{n,m-1}, the logit gradient dS_{nm} and the probabilities P_{nm}
+//   pairs : T [BH, N(N-1)/2, 2 C d + 2 C C]  per (query chunk n, key chunk
+//           m < n): the transported queries U_{n,m}, the chain gradient
+//           G_{n,m-1}, the logit gradient dS_{nm} and the probabilities P_{nm},
+//           in the input dtype (bf16 pairs feed the tensor-core reduction)
 constexpr int kBwdC = 64;
 struct BwdLayout {
     size_t qbar, khat, pm, pmt, delta, cum, dqbar, dkhat, dvoff, dpm, dcrow, dccol, dctot, pairs, total;
     int Lp, N;
-    size_t pair_floats;  // floats per (n, m) pair
+    size_t pair_elems;   // elements per (n, m) pair
     size_t head_pairs;   // N (N - 1) / 2
 };
-inline BwdLayout bwd_layout(int B, int H, int L, int d) {
+inline BwdLayout bwd_layout(int B, int H, int L, int d, size_t elt) {
     BwdLayout s;
     const int C = kBwdC;
     s.N = cdiv(L, C);
     s.Lp = s.N * C;
     const size_t BH = (size_t)B * H, rows = BH * s.Lp;
-    s.pair_floats = 2 * (size_t)C * d + 2 * (size_t)C * C;
+    s.pair_elems = 2 * (size_t)C * d + 2 * (size_t)C * C;
     s.head_pairs = (size_t)s.N * (s.N - 1) / 2;
     size_t off = sizeof(WsHeader);
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
@@ -194,7 +195,7 @@ inline BwdLayout bwd_layout(int B, int H, int L, int d) {
     s.dcrow = take(rows * sizeof(float));
     s.dccol = take(rows * sizeof(float));
     s.dctot = take(rows * sizeof(float));
-    s.pairs = take(BH * s.head_pairs * s.pair_floats * sizeof(float));
+    s.pairs = take(BH * s.head_pairs * s.pair_elems * elt);
     s.total = off;
     return s;
 }

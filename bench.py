@@ -453,21 +453,20 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         bms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
         kms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
-        # fp32 FLOPs of the chunk-pair kernels (bwd_chain + bwd_reduce), C = 64: per (query chunk,
-        # earlier key chunk) pair five C x C x d products (S, dO V^T, dS khat, P^T dO, dS^T U) and,
-        # past the first key chunk, three C x d x d ones (U P^T, G P, G^T U)
+        # fp32 FLOPs of the chunk chains (bwd_chain, CUDA cores), C = 64: per (query chunk, earlier key
+        # chunk) pair three C x C x d products (S, dO v^T, dS khat) and, past the first key chunk, two
+        # C x d x d ones (U P^T, G P).  The per-key-chunk sums run on the tensor cores (bwd_reduce_tc).
         C, nc = 64, -(-fc.L // 64)
         pairs = nc * (nc - 1) // 2
-        pair_flops = fc.B * fc.H * (pairs * 5 * 2 * C * C * fc.d + (pairs - (nc - 1)) * 3 * 2 * C * fc.d * fc.d)
+        pair_flops = fc.B * fc.H * (pairs * 3 * 2 * C * C * fc.d + (pairs - (nc - 1)) * 2 * 2 * C * fc.d * fc.d)
         fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x fp32 lanes x FMA x max SM clock
-        tc, tr = _traffic("bwd_chain", fc.B * fc.H), _traffic("bwd_reduce", fc.B * fc.H)
-        bwd_traffic = tc + tr if tc is not None and tr is not None else None
+        bwd_traffic = _traffic("bwd_chain", fc.B * fc.H)
         ach = pair_flops / (kms * 1e-3) / 1e12
         bwd = {"ms": bms, "attn_equiv_tflops": 2.5 * fc.attn_flops / (bms * 1e-3) / 1e12, "steps": args.bwd_steps,
                "workload": "PaTH backward B%d H%d L%d d%d bf16 (dq, dk, dv, dw, dbeta for a seeded dO); "
                            "attention-equivalent FLOPs 2.5 x the forward's" % (fc.B, fc.H, fc.L, fc.d),
                "workspace_gb": ws_b.numel() / 1e9,
-               "roofline": {"kernel": "bwd_chain + bwd_reduce (fp32 CUDA cores)", "bound": "alu", "achieved": ach,
+               "roofline": {"kernel": "bwd_chain (fp32 CUDA cores)", "bound": "alu", "achieved": ach,
                             "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach / fp32_peak,
                             "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
                             "traffic": bwd_traffic, "flops_per_launch": float(pair_flops), "kernel_ms": kms}}

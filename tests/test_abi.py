@@ -104,8 +104,11 @@ def test_bwd_argument_errors(lib):
     assert bwd(BH=(300, 300)) == P.PATH_ERR_UNSUPPORTED   # B*H above the grid limit
     assert bwd(ws_bytes=4096) == P.PATH_ERR_WORKSPACE
     need = lib.path_attn_bwd_workspace_bytes(2, 3, 300, 64, P.PATH_BF16)
-    # 5 chunks of 64: 10 (query chunk, key chunk) pairs per head hold U, G (64 x 64) and dS (64 x 64)
-    assert need > 6 * 10 * (2 * 64 * 64 + 64 * 64) * 4
+    # 5 chunks of 64: 10 (query chunk, key chunk) pairs per head hold U, G (64 x 64), dS and P (64 x 64),
+    # in the input dtype (bf16 here; fp32 pairs for fp32 inputs)
+    assert need > 6 * 10 * (2 * 64 * 64 + 2 * 64 * 64) * 2
+    need32 = lib.path_attn_bwd_workspace_bytes(2, 3, 300, 64, P.PATH_F32)
+    assert need32 - need >= 6 * 10 * (2 * 64 * 64 + 2 * 64 * 64) * 2
     assert lib.path_attn_bwd_workspace_bytes(2, 3, 300, 48, P.PATH_BF16) == 0
     assert lib.path_attn_bwd_workspace_bytes(2, 3, 300, 64, 9) == 0
 
