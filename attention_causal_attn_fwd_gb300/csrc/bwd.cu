@@ -47,6 +47,10 @@
 
 namespace pathattn {
 
+cudaError_t launch_bwd_chain_tc(const void* dO, const void* v, const void* khat16, const void* phi, const void* plo,
+                                void* pairs, const float* qbar, const float* lse, const float* delta,
+                                const float* cum, float* dqbar, float* dcrow, float* dccol, int fox, int BH, int L,
+                                int Lp, int N, size_t head_pairs, float scale, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_bwd_reduce_tc(const void* dO, const void* pairs, float* dvoff, float* dkhat, float* dpm, int BH,
                                  int L, int Lp, int N, size_t head_pairs, float scale, WsHeader* hdr,
                                  cudaStream_t st);
@@ -65,6 +69,7 @@ struct BwdParams {
     void *dq, *dk, *dv, *dw;
     float *dbeta, *dlog_f;
     float *qbar, *khat, *pm, *pmt, *delta, *cum, *dqbar, *dkhat, *dvoff, *dpm, *dcrow, *dccol, *dctot;
+    __nv_bfloat16 *khat16, *phi, *plo;  // tensor-core chains only (else null)
     void* pairs;  // pair store, elements of the input dtype
     int L, Lp, N;
     size_t pair_elems, head_pairs;
@@ -362,6 +367,7 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
         }
         vstore<D>(p.qbar + (prow + r) * D, u, lane);
         vstore<D>(p.khat + (prow + r) * D, x, lane);
+        if (p.khat16) vstore<D>(p.khat16 + (prow + r) * D, x, lane);
         if (lane == 0) p.delta[prow + r] = dl;
     }
     if (n < 1 || n > p.N - 2) return;  // P_m is used only for 1 <= m <= N-2
@@ -402,6 +408,12 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
         const int r = idx / D, cc = idx % D;
         pm[idx] = sM[r * LDP + cc];
         pmt[idx] = sM[cc * LDP + r];
+        if (p.phi) {  // hi + lo bf16 split of P_m for the tensor-core chains
+            const float x = sM[r * LDP + cc];
+            const __nv_bfloat16 h = __float2bfloat16_rn(x);
+            p.phi[((size_t)bh * p.N + n) * D * D + idx] = h;
+            p.plo[((size_t)bh * p.N + n) * D * D + idx] = __float2bfloat16_rn(x - __bfloat162float(h));
+        }
     }
 }
 
@@ -799,9 +811,16 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigne
     }
     bwd_prep<T, D><<<dim3(p.N, BH), kNT, b_prep, st>>>(p);
     if (p.N >= 2) {
-        mark_start(st);
-        bwd_chain<T, D><<<dim3(p.N - 1, BH), kNT, b_chain, st>>>(p);
-        mark_end(st);
+        if constexpr (sizeof(T) == 2 && D == 128) {  // bf16: tensor-core chains (csrc/bwd_tc.cu)
+            cudaError_t e = launch_bwd_chain_tc(p.dO, p.v, p.khat16, p.phi, p.plo, p.pairs, p.qbar, p.lse, p.delta,
+                                                p.cum, p.dqbar, p.dcrow, p.dccol, p.fox, BH, p.L, p.Lp, p.N,
+                                                p.head_pairs, p.scale, reinterpret_cast<WsHeader*>(ws), st);
+            if (e != cudaSuccess) return e;
+        } else {
+            mark_start(st);
+            bwd_chain<T, D><<<dim3(p.N - 1, BH), kNT, b_chain, st>>>(p);
+            mark_end(st);
+        }
         if constexpr (sizeof(T) == 2 && D == 128) {  // bf16 pairs: tensor-core reduction (csrc/bwd_tc.cu)
             cudaError_t e = launch_bwd_reduce_tc(p.dO, p.pairs, p.dvoff, p.dkhat, p.dpm, BH, p.L, p.Lp, p.N,
                                                  p.head_pairs, p.scale, reinterpret_cast<WsHeader*>(ws), st);
@@ -832,6 +851,9 @@ cudaError_t attn_bwd(int dtype, int d, const void* q, const void* k, const void*
     p.delta = f(lay.delta); p.cum = f(lay.cum); p.dqbar = f(lay.dqbar); p.dkhat = f(lay.dkhat);
     p.dvoff = f(lay.dvoff); p.dpm = f(lay.dpm); p.dcrow = f(lay.dcrow); p.dccol = f(lay.dccol);
     p.dctot = f(lay.dctot); p.pairs = ws + lay.pairs;
+    p.khat16 = lay.khat16 ? reinterpret_cast<__nv_bfloat16*>(ws + lay.khat16) : nullptr;
+    p.phi = lay.phi ? reinterpret_cast<__nv_bfloat16*>(ws + lay.phi) : nullptr;
+    p.plo = lay.plo ? reinterpret_cast<__nv_bfloat16*>(ws + lay.plo) : nullptr;
     p.L = L; p.Lp = lay.Lp; p.N = lay.N;
     p.pair_elems = lay.pair_elems; p.head_pairs = lay.head_pairs;
     p.scale = scale;

@@ -154,6 +154,8 @@ inline DecLayout dec_layout(int B, int H, int n_max, int d) {
 //   khat  : float [BH, Lp, d]   keys walked up to their chunk end
 //   pm    : float [BH, N, d, d] chunk transition P_m = H_b ... H_e (row-major)
 //   pmt   : float [BH, N, d, d] its transpose
+//   khat16, phi, plo : bf16 copies for the tensor-core chains (bf16, d = 128
+//           only): khat [BH, Lp, d]; P_m split as hi + lo [BH, N, d, d]
 //   delta : float [BH, Lp]      dO_i . o_i
 //   cum   : float [BH, Lp]      inclusive cumulative sum of log f (PaTH-FoX)
 //   dqbar, dkhat, dvoff : float [BH, Lp, d]  gradients w.r.t. qbar and khat,
@@ -167,7 +169,7 @@ inline DecLayout dec_layout(int B, int H, int n_max, int d) {
 //           in the input dtype (bf16 pairs feed the tensor-core reduction)
 constexpr int kBwdC = 64;
 struct BwdLayout {
-    size_t qbar, khat, pm, pmt, delta, cum, dqbar, dkhat, dvoff, dpm, dcrow, dccol, dctot, pairs, total;
+    size_t qbar, khat, pm, pmt, khat16, phi, plo, delta, cum, dqbar, dkhat, dvoff, dpm, dcrow, dccol, dctot, pairs, total;
     int Lp, N;
     size_t pair_elems;   // elements per (n, m) pair
     size_t head_pairs;   // N (N - 1) / 2
@@ -186,6 +188,10 @@ inline BwdLayout bwd_layout(int B, int H, int L, int d, size_t elt) {
     s.khat = take(rows * d * sizeof(float));
     s.pm = take(BH * s.N * d * d * sizeof(float));
     s.pmt = take(BH * s.N * d * d * sizeof(float));
+    const bool tc = elt == 2 && d == 128;
+    s.khat16 = tc ? take(rows * d * 2) : 0;
+    s.phi = tc ? take(BH * s.N * d * d * 2) : 0;
+    s.plo = tc ? take(BH * s.N * d * d * 2) : 0;
     s.delta = take(rows * sizeof(float));
     s.cum = take(rows * sizeof(float));
     s.dqbar = take(rows * d * sizeof(float));
