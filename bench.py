@@ -453,23 +453,27 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         bms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
         kms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
-        # fp32 FLOPs of the chunk chains (bwd_chain, CUDA cores), C = 64: per (query chunk, earlier key
-        # chunk) pair three C x C x d products (S, dO v^T, dS khat) and, past the first key chunk, two
-        # C x d x d ones (U P^T, G P).  The per-key-chunk sums run on the tensor cores (bwd_reduce_tc).
-        C, nc = 64, -(-fc.L // 64)
-        pairs = nc * (nc - 1) // 2
-        pair_flops = fc.B * fc.H * (pairs * 3 * 2 * C * C * fc.d + (pairs - (nc - 1)) * 2 * 2 * C * fc.d * fc.d)
-        fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x fp32 lanes x FMA x max SM clock
-        bwd_traffic = _traffic("bwd_chain", fc.B * fc.H)
-        ach = pair_flops / (kms * 1e-3) / 1e12
+        # tensor-core FLOPs of the chunk chains (bwd_chain_tc; two 64-row query chunks per 128-row
+        # tile, nA = the longer chain): per step down S = U khat^T and dO v^T (M 128, N 64, K 128)
+        # and, past key chunk 0, U P^T as three hi/lo products (M 128, N 128, K 128); per step up
+        # dS khat (M 128, N 128, K 64) and, past key chunk 0, G P as three products
+        nc = -(-fc.L // 64)
+        chain_flops = 0
+        for kk in range(nc // 2):
+            nA = nc - 1 - 2 * kk
+            chain_flops += nA * (2 * 2 * 128 * 64 * 128 + 2 * 128 * 128 * 64) + (nA - 1) * 2 * 3 * 2 * 128 ** 3
+        chain_flops *= fc.B * fc.H
+        ach = chain_flops / (kms * 1e-3) / 1e12
+        bwd_traffic = _traffic("bwd_chain_tc", fc.B * fc.H)
         bwd = {"ms": bms, "attn_equiv_tflops": 2.5 * fc.attn_flops / (bms * 1e-3) / 1e12, "steps": args.bwd_steps,
                "workload": "PaTH backward B%d H%d L%d d%d bf16 (dq, dk, dv, dw, dbeta for a seeded dO); "
                            "attention-equivalent FLOPs 2.5 x the forward's" % (fc.B, fc.H, fc.L, fc.d),
                "workspace_gb": ws_b.numel() / 1e9,
-               "roofline": {"kernel": "bwd_chain (fp32 CUDA cores)", "bound": "alu", "achieved": ach,
-                            "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach / fp32_peak,
-                            "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                            "traffic": bwd_traffic, "flops_per_launch": float(pair_flops), "kernel_ms": kms}}
+               "roofline": {"kernel": "bwd_chain_tc (query-side chunk chains, tcgen05)", "bound": "tensor",
+                            "achieved": ach, "peak": bf16_tf, "unit": "TFLOP/s", "frac": ach / bf16_tf,
+                            "peak_source": peak_src + " bf16 burst", "traffic": bwd_traffic,
+                            "flops_per_launch": float(chain_flops), "flops_kind": "executed MMA FLOPs",
+                            "kernel_ms": kms}}
         del o_b, lse_b, dO_b, ws_b
 
     cpu = None
