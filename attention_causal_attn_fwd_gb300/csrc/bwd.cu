@@ -402,12 +402,14 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
         }
         __syncthreads();
     }
-    float* pm = p.pm + ((size_t)bh * p.N + n) * D * D;
-    float* pmt = p.pmt + ((size_t)bh * p.N + n) * D * D;
+    float* pm = p.pm ? p.pm + ((size_t)bh * p.N + n) * D * D : nullptr;
+    float* pmt = p.pmt ? p.pmt + ((size_t)bh * p.N + n) * D * D : nullptr;
     for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
         const int r = idx / D, cc = idx % D;
-        pm[idx] = sM[r * LDP + cc];
-        pmt[idx] = sM[cc * LDP + r];
+        if (pm) {
+            pm[idx] = sM[r * LDP + cc];
+            pmt[idx] = sM[cc * LDP + r];
+        }
         if (p.phi) {  // hi + lo bf16 split of P_m for the tensor-core chains
             const float x = sM[r * LDP + cc];
             const __nv_bfloat16 h = __float2bfloat16_rn(x);
@@ -847,7 +849,9 @@ cudaError_t attn_bwd(int dtype, int d, const void* q, const void* k, const void*
     p.beta = beta; p.lse = lse;
     p.dq = dq; p.dk = dk; p.dv = dv; p.dw = dw; p.dbeta = dbeta; p.dlog_f = dlog_f;
     auto f = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
-    p.qbar = f(lay.qbar); p.khat = f(lay.khat); p.pm = f(lay.pm); p.pmt = f(lay.pmt);
+    p.qbar = f(lay.qbar); p.khat = f(lay.khat);
+    p.pm = lay.pm ? f(lay.pm) : nullptr;
+    p.pmt = lay.pmt ? f(lay.pmt) : nullptr;
     p.delta = f(lay.delta); p.cum = f(lay.cum); p.dqbar = f(lay.dqbar); p.dkhat = f(lay.dkhat);
     p.dvoff = f(lay.dvoff); p.dpm = f(lay.dpm); p.dcrow = f(lay.dcrow); p.dccol = f(lay.dccol);
     p.dctot = f(lay.dctot); p.pairs = ws + lay.pairs;

@@ -153,7 +153,8 @@ inline DecLayout dec_layout(int B, int H, int n_max, int d) {
 //   qbar  : float [BH, Lp, d]   queries walked down through their own chunk
 //   khat  : float [BH, Lp, d]   keys walked up to their chunk end
 //   pm    : float [BH, N, d, d] chunk transition P_m = H_b ... H_e (row-major)
-//   pmt   : float [BH, N, d, d] its transpose
+//   pmt   : float [BH, N, d, d] its transpose (pm and pmt feed the CUDA-core
+//           chains only: absent for bf16 at d = 128)
 //   khat16, phi, plo : bf16 copies for the tensor-core chains (bf16, d = 128
 //           only): khat [BH, Lp, d]; P_m split as hi + lo [BH, N, d, d]
 //   delta : float [BH, Lp]      dO_i . o_i
@@ -186,9 +187,9 @@ inline BwdLayout bwd_layout(int B, int H, int L, int d, size_t elt) {
     auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
     s.qbar = take(rows * d * sizeof(float));
     s.khat = take(rows * d * sizeof(float));
-    s.pm = take(BH * s.N * d * d * sizeof(float));
-    s.pmt = take(BH * s.N * d * d * sizeof(float));
     const bool tc = elt == 2 && d == 128;
+    s.pm = tc ? 0 : take(BH * s.N * d * d * sizeof(float));
+    s.pmt = tc ? 0 : take(BH * s.N * d * d * sizeof(float));
     s.khat16 = tc ? take(rows * d * 2) : 0;
     s.phi = tc ? take(BH * s.N * d * d * 2) : 0;
     s.plo = tc ? take(BH * s.N * d * d * 2) : 0;
