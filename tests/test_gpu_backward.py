@@ -146,6 +146,15 @@ def test_bwd_small_bf16_config():
     _case(x, 1, "small_bf16")
 
 
+@pytest.mark.parametrize("B,H,L,fox", [(2, 3, 517, False), (1, 2, 130, True)])
+def test_bwd_bf16_d128_edge_betas(B, H, L, fox):
+    """The tensor-core chains and sums (bf16, d = 128) with 5 % / 5 % beta = 0 / beta = 2 positions, a ragged
+    last chunk, several heads and odd chunk counts (L = 517: 9 chunks, L = 130: 3), where chunk 0, which has no
+    chain, is the one left unpaired."""
+    x = inputs.make_fwd(B, H, L, 128, "bf16", seed=70 + L, beta_std=2.0, edge_frac=0.05, fox=fox)
+    _case(x, 70 + L, "bf16 d128 edges B%d H%d L%d fox=%s" % (B, H, L, fox))
+
+
 def test_bwd_bf16_fox_d128_ragged():
     x = inputs.make_fwd(1, 2, 333, 128, "bf16", seed=33, fox=True)
     _case(x, 33, "bf16 fox L333")
