@@ -62,6 +62,7 @@ constexpr int kNT = 256;
 constexpr int kNW = kNT / 32;
 constexpr int kNTL = 512;  // bwd_local: latency-bound walks, one warp per row / key / position
 constexpr int kNWL = kNTL / 32;
+constexpr int kNTP = 512;  // bwd_prep: sixteen latency-bound walks in flight per CTA
 
 struct BwdParams {
     const void *q, *k, *v, *w, *o, *dO;
@@ -336,7 +337,7 @@ template <int D> struct BwdSmem {
 
 // ------------------------------------------------------------------ bwd_prep
 template <typename T, int D>
-__global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
+__global__ void __launch_bounds__(kNTP) bwd_prep(BwdParams p) {
     constexpr int C = kC, LDP = BwdSmem<D>::LDP;
     extern __shared__ float smem[];
     float* sW = smem;          // [C][D]
@@ -345,11 +346,11 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
     float* sZ = sM + D * LDP;  // [D]
     const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
     const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
-    to_smem_v<T, D>(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, c);
-    for (int r = threadIdx.x; r < C; r += kNT) sB[r] = r < c ? p.beta[hrow + r] : 0.f;
+    to_smem_v<T, D, kNTP>(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, c);
+    for (int r = threadIdx.x; r < C; r += kNTP) sB[r] = r < c ? p.beta[hrow + r] : 0.f;
     __syncthreads();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int r = wid; r < C; r += kNW) {
+    for (int r = wid; r < C; r += kNTP / 32) {
         float u[WV<D>::R], x[WV<D>::R];
         float dl = 0.f;
         if (r < c) {
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
         if (lane == 0) p.delta[prow + r] = dl;
     }
     if (n < 1 || n > p.N - 2) return;  // P_m is used only for 1 <= m <= N-2
-    for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
+    for (int idx = threadIdx.x; idx < D * D; idx += kNTP) {
         const int r = idx / D, cc = idx % D;
         sM[r * LDP + cc] = r == cc ? 1.f : 0.f;
     }
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
     for (int t = 0; t < c; ++t) {  // M <- M H_t = M - beta_t (M w_t) w_t^T
         const float* wt = sW + t * D;
         // z = M w_t: two threads per row, four partial sums each (short dependency chains)
-        for (int h = threadIdx.x; h < 2 * D; h += kNT) {
+        for (int h = threadIdx.x; h < 2 * D; h += kNTP) {
             const int r = h >> 1, c0 = (h & 1) * (D / 2);
             float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
             const float* mr = sM + r * LDP + c0;
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
             if ((h & 1) == 0) sZ[r] = sB[t] * z;
         }
         __syncthreads();
-        for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
+        for (int idx = threadIdx.x; idx < D * D; idx += kNTP) {
             const int r = idx / D, cc = idx % D;
             sM[r * LDP + cc] = fmaf(-sZ[r], wt[cc], sM[r * LDP + cc]);
         }
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(kNT) bwd_prep(BwdParams p) {
     }
     float* pm = p.pm ? p.pm + ((size_t)bh * p.N + n) * D * D : nullptr;
     float* pmt = p.pmt ? p.pmt + ((size_t)bh * p.N + n) * D * D : nullptr;
-    for (int idx = threadIdx.x; idx < D * D; idx += kNT) {
+    for (int idx = threadIdx.x; idx < D * D; idx += kNTP) {
         const int r = idx / D, cc = idx % D;
         if (pm) {
             pm[idx] = sM[r * LDP + cc];
@@ -811,7 +812,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigne
         fox_cumsum<<<BH, 1024, 0, st>>>(log_f, p.L, p.Lp, p.cum);
         cudaMemsetAsync(p.dccol, 0, (size_t)BH * p.Lp * sizeof(float), st);  // bwd_chain adds column sums
     }
-    bwd_prep<T, D><<<dim3(p.N, BH), kNT, b_prep, st>>>(p);
+    bwd_prep<T, D><<<dim3(p.N, BH), kNTP, b_prep, st>>>(p);
     if (p.N >= 2) {
         if constexpr (sizeof(T) == 2 && D == 128) {  // bf16: tensor-core chains (csrc/bwd_tc.cu)
             cudaError_t e = launch_bwd_chain_tc(p.dO, p.v, p.khat16, p.phi, p.plo, p.pairs, p.qbar, p.lse, p.delta,
