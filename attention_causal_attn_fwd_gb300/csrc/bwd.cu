@@ -27,7 +27,9 @@
 // dbeta = -(w.g)(w.u) and dw = -beta ((w.u) g + (w.g) u).
 //
 // Kernels, in stream order:
-//   bwd_prep   one CTA per chunk        qbar, khat, P_m, P_m^T, Delta
+//   bwd_prep   one CTA per chunk        qbar, khat (walks), Delta
+//   bwd_pm     one CTA per inner chunk  P_m = I - W^T A W (compact form; fp32, or
+//                                       hi / lo bf16 for the tensor-core chains)
 //   bwd_chain  one CTA per query chunk  U chain down, G chain up; stores U,
 //                                       G and dS per (n, m) pair; dQbar
 //   bwd_reduce one CTA per key chunk    dV_m, dKhat_m, dP_m summed over the
@@ -325,7 +327,8 @@ template <int D> struct BwdSmem {
     static constexpr int LC = kC + 4, LD = D + 4;  // K-major GEMM operands (16-byte rows)
     static constexpr int RK = (D * LC > kC * LD ? D * LC : kC * LD);
     static constexpr int RV = (D * LC > kC * LC ? D * LC : kC * LC);
-    static constexpr int prep = kC * D + kC + D * LDP + D;
+    static constexpr int prep = kC * D + kC;
+    static constexpr int pm = D * (kC + 4) + 2 * kC * (D + 4) + 3 * kC * (kC + 4) + kC;
     static constexpr int chain = 2 * D * LC + RK + RV + D * LD + 6 * kC;
     static constexpr int reduce = 3 * kC * LD + 2 * kC * LC;
     static constexpr int wbuf = (3 * kC > 2 * D ? 3 * kC : 2 * D);
@@ -338,12 +341,10 @@ template <int D> struct BwdSmem {
 // ------------------------------------------------------------------ bwd_prep
 template <typename T, int D>
 __global__ void __launch_bounds__(kNTP) bwd_prep(BwdParams p) {
-    constexpr int C = kC, LDP = BwdSmem<D>::LDP;
+    constexpr int C = kC;
     extern __shared__ float smem[];
     float* sW = smem;          // [C][D]
     float* sB = sW + C * D;    // [C]
-    float* sM = sB + C;        // [D][LDP]
-    float* sZ = sM + D * LDP;  // [D]
     const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
     const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
     to_smem_v<T, D, kNTP>(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, c);
@@ -371,53 +372,93 @@ __global__ void __launch_bounds__(kNTP) bwd_prep(BwdParams p) {
         if (p.khat16) vstore<D>(p.khat16 + (prow + r) * D, x, lane);
         if (lane == 0) p.delta[prow + r] = dl;
     }
-    if (n < 1 || n > p.N - 2) return;  // P_m is used only for 1 <= m <= N-2
-    for (int idx = threadIdx.x; idx < D * D; idx += kNTP) {
-        const int r = idx / D, cc = idx % D;
-        sM[r * LDP + cc] = r == cc ? 1.f : 0.f;
+}
+
+// ------------------------------------------------------------------ bwd_pm
+// The chunk transition P_m = H_b ... H_e for 1 <= m <= N-2 in the compact form of
+// "Representação de Transformação UT" (§3): P_m = I - W^T A W with
+// A = (I + D triu_1(W W^T))^{-1} D, D = diag(beta): G = W W^T, the unit upper-triangular
+// inverse X = (I + D triu_1 G)^{-1} row by row from the bottom, A = X D, then two GEMMs.
+template <typename T, int D>
+__global__ void __launch_bounds__(kNT) bwd_pm(BwdParams p) {
+    constexpr int C = kC, LC = C + 4, LD = D + 4;
+    extern __shared__ __align__(16) float smem[];
+    float* sWT = smem;           // [D][LC] W^T
+    float* sW = sWT + D * LC;    // [C][LD] W
+    float* sG = sW + C * LD;     // [C][LC] G = W W^T
+    float* sX = sG + C * LC;     // [C][LC] X (row-major)
+    float* sAT = sX + C * LC;    // [C][LC] A^T
+    float* sAW = sAT + C * LC;   // [C][LD] A W
+    float* sB = sAW + C * LD;    // [C] beta
+    const int n = 1 + blockIdx.x, bh = blockIdx.y, b = n * C;  // chunks 1 .. N-2 are full
+    const size_t hrow = (size_t)bh * p.L + b;
+    const T* w = static_cast<const T*>(p.w) + hrow * D;
+    to_smem_v<T, D>(sW, LD, w, D, C, C);
+    to_smem_t<T, D>(sWT, LC, w, D, C, C);
+    for (int r = threadIdx.x; r < C; r += kNT) sB[r] = p.beta[hrow + r];
+    for (int idx = threadIdx.x; idx < C * LC; idx += kNT) sX[idx] = 0.f;
+    __syncthreads();
+    {  // G = W W^T
+        using GG = VT<C, C>;
+        typename GG::Acc acc;
+        GG::zero(acc);
+        vgemm<C, C, D>(acc, sWT, LC, sWT, LC);
+#pragma unroll
+        for (int i = 0; i < GG::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < GG::TN; ++j) sG[(GG::m0() + i) * LC + GG::n0() + j] = acc[i][j];
     }
     __syncthreads();
-    for (int t = 0; t < c; ++t) {  // M <- M H_t = M - beta_t (M w_t) w_t^T
-        const float* wt = sW + t * D;
-        // z = M w_t: two threads per row, four partial sums each (short dependency chains)
-        for (int h = threadIdx.x; h < 2 * D; h += kNTP) {
-            const int r = h >> 1, c0 = (h & 1) * (D / 2);
-            float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
-            const float* mr = sM + r * LDP + c0;
-            const float* wc = wt + c0;
-#pragma unroll 4
-            for (int cc = 0; cc < D / 2; cc += 4) {
-                z0 = fmaf(mr[cc], wc[cc], z0);
-                z1 = fmaf(mr[cc + 1], wc[cc + 1], z1);
-                z2 = fmaf(mr[cc + 2], wc[cc + 2], z2);
-                z3 = fmaf(mr[cc + 3], wc[cc + 3], z3);
+    // X[i][j] = [i == j] - beta_i sum_{i < k <= j} G[i][k] X[k][j]: four threads per column
+    for (int i = C - 1; i >= 0; --i) {
+        const int j = threadIdx.x >> 2, q = threadIdx.x & 3;
+        float t = 0.f;
+        if (j > i)
+            for (int k = i + 1 + q; k <= j; k += 4) t = fmaf(sG[i * LC + k], sX[k * LC + j], t);
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        t += __shfl_xor_sync(0xffffffffu, t, 2);
+        if (q == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
+        __syncthreads();
+    }
+    // A = X D, stored transposed for the next product's K-major A operand
+    for (int idx = threadIdx.x; idx < C * C; idx += kNT) {
+        const int i = idx / C, j = idx % C;
+        sAT[j * LC + i] = sX[i * LC + j] * sB[j];
+    }
+    __syncthreads();
+    {  // A W
+        using GA = VT<C, D>;
+        typename GA::Acc acc;
+        GA::zero(acc);
+        vgemm<C, D, C>(acc, sAT, LC, sW, LD);
+#pragma unroll
+        for (int i = 0; i < GA::TM; ++i)
+#pragma unroll
+            for (int j = 0; j < GA::TN; ++j) sAW[(GA::m0() + i) * LD + GA::n0() + j] = acc[i][j];
+    }
+    __syncthreads();
+    // P = I - W^T (A W)
+    using GP = VT<D, D>;
+    typename GP::Acc acc;
+    GP::zero(acc);
+    vgemm<D, D, C>(acc, sW, LD, sAW, LD);
+    const size_t base = ((size_t)bh * p.N + n) * D * D;
+#pragma unroll
+    for (int i = 0; i < GP::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < GP::TN; ++j) {
+            const int r = GP::m0() + i, cc = GP::n0() + j;
+            const float x = (r == cc ? 1.f : 0.f) - acc[i][j];
+            if (p.pm) {
+                p.pm[base + (size_t)r * D + cc] = x;
+                p.pmt[base + (size_t)cc * D + r] = x;
             }
-            float z = (z0 + z1) + (z2 + z3);
-            z += __shfl_xor_sync(0xffffffffu, z, 1);
-            if ((h & 1) == 0) sZ[r] = sB[t] * z;
+            if (p.phi) {  // hi + lo bf16 split for the tensor-core chains
+                const __nv_bfloat16 h = __float2bfloat16_rn(x);
+                p.phi[base + (size_t)r * D + cc] = h;
+                p.plo[base + (size_t)r * D + cc] = __float2bfloat16_rn(x - __bfloat162float(h));
+            }
         }
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < D * D; idx += kNTP) {
-            const int r = idx / D, cc = idx % D;
-            sM[r * LDP + cc] = fmaf(-sZ[r], wt[cc], sM[r * LDP + cc]);
-        }
-        __syncthreads();
-    }
-    float* pm = p.pm ? p.pm + ((size_t)bh * p.N + n) * D * D : nullptr;
-    float* pmt = p.pmt ? p.pmt + ((size_t)bh * p.N + n) * D * D : nullptr;
-    for (int idx = threadIdx.x; idx < D * D; idx += kNTP) {
-        const int r = idx / D, cc = idx % D;
-        if (pm) {
-            pm[idx] = sM[r * LDP + cc];
-            pmt[idx] = sM[cc * LDP + r];
-        }
-        if (p.phi) {  // hi + lo bf16 split of P_m for the tensor-core chains
-            const float x = sM[r * LDP + cc];
-            const __nv_bfloat16 h = __float2bfloat16_rn(x);
-            p.phi[((size_t)bh * p.N + n) * D * D + idx] = h;
-            p.plo[((size_t)bh * p.N + n) * D * D + idx] = __float2bfloat16_rn(x - __bfloat162float(h));
-        }
-    }
 }
 
 // ------------------------------------------------------------------ bwd_chain
@@ -813,6 +854,11 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigne
         cudaMemsetAsync(p.dccol, 0, (size_t)BH * p.Lp * sizeof(float), st);  // bwd_chain adds column sums
     }
     bwd_prep<T, D><<<dim3(p.N, BH), kNTP, b_prep, st>>>(p);
+    if (p.N >= 3) {
+        const size_t b_pm = S::pm * sizeof(float);
+        cudaFuncSetAttribute(bwd_pm<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_pm);
+        bwd_pm<T, D><<<dim3(p.N - 2, BH), kNT, b_pm, st>>>(p);
+    }
     if (p.N >= 2) {
         if constexpr (sizeof(T) == 2 && D == 128) {  // bf16: tensor-core chains (csrc/bwd_tc.cu)
             cudaError_t e = launch_bwd_chain_tc(p.dO, p.v, p.khat16, p.phi, p.plo, p.pairs, p.qbar, p.lse, p.delta,
