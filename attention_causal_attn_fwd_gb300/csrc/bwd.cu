@@ -31,7 +31,10 @@
 //   bwd_pm     one CTA per inner chunk  P_m = I - W^T A W (compact form; fp32, or
 //                                       hi / lo bf16 for the tensor-core chains)
 //   bwd_chain  one CTA per query chunk  U chain down, G chain up; stores U,
-//                                       G and dS per (n, m) pair; dQbar
+//                                       G, dS and P per (n, m) pair; dQbar;
+//                                       for bf16 at d = 128 bwd_chain_tc
+//                                       (csrc/bwd_tc.cu) runs the chains on
+//                                       the tensor cores
 //   bwd_reduce one CTA per key chunk    dV_m, dKhat_m, dP_m summed over the
 //                                       query chunks (each output owned by
 //                                       one CTA, so no global atomics); for
@@ -42,8 +45,9 @@
 //                                       walks in reverse; writes dq, dk, dv,
 //                                       dw, dbeta (shared-memory atomics)
 //   bwd_fox_suffix one CTA per head     dlog f_s = sum_{t >= s} dc_t
-// The contractions are register-tiled fp32 GEMMs on K-major shared-memory operands.
-// Nothing waits on another CTA, so no kernel here has a spin wait.
+// The contractions here are register-tiled fp32 GEMMs on K-major shared-memory operands.
+// Nothing here waits on another CTA, so these kernels have no spin waits (the
+// tensor-core kernels of csrc/bwd_tc.cu bound every wait).
 #include "common.cuh"
 #include "ut_prep.cuh"
 

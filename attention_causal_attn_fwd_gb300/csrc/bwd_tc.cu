@@ -1,4 +1,6 @@
-// Backward chunk-pair reduction on GB300 tensor cores (bf16, d = 128).
+// Backward kernels on GB300 tensor cores (bf16, d = 128): the per-key-chunk
+// reduction bwd_reduce_tc, and further down the query-side chunk chains
+// bwd_chain_tc that write its input.
 //
 // The backward of "Resumo Técnico: Atenção PaTH" (gist.science/pt/paper/2505.16381)
 // is organised in chunks of C = 64 positions (csrc/bwd.cu).  For one key chunk m
@@ -6,7 +8,7 @@
 //     dV_m^T    += dO_n^T P_nm          (d x C)
 //     dKhat_m^T += U_{n,m}^T dS_nm      (d x C; scaled on output)
 //     dP_m      += G_{n,m-1}^T U_{n,m}  (d x d; m >= 1)
-// from the bf16 pair store that bwd_chain writes and the caller's dO.  Every
+// from the bf16 pair store that bwd_chain_tc writes and the caller's dO.  Every
 // operand is read MN-major: the tiles are [64 rows = K][64- or 128-column = M/N]
 // as TMA writes them (128-byte swizzle, two 64-column halves 8 KB apart), so one
 // tile layout serves as the transposed A operand and as the B operand.
