@@ -152,11 +152,16 @@ size_t path_attn_bwd_workspace_bytes(int B, int H, int L, int d, int dtype);
  *   d in {16, 32, 64, 128} for PATH_F32 and PATH_BF16; B*H <= 65535; causal = 1
  *   workspace : >= path_attn_bwd_workspace_bytes(B,H,L,d,dtype) bytes, device,
  *            16-byte aligned, contents need not be initialised
- * Arithmetic is fp32 on the CUDA cores; bf16 inputs are widened on load and the
- * gradients rounded to bf16 (nearest even) on store.  dbeta at position 0 and
- * dlog_f at position 0 are exactly zero (those enter no logit).  Outputs may not
- * alias inputs.  Argument errors return before any launch; the kernels have no
- * waits, so the status word stays PATH_OK.
+ * Arithmetic: fp32 inputs run in fp32 on the CUDA cores.  bf16 inputs at d = 128
+ * run the query-side chunk chains and the per-key-chunk sums on the tensor cores
+ * (bf16 operands, fp32 accumulation; the carried states enter as hi + lo bf16
+ * parts) and the within-chunk walks in fp32; other bf16 sizes run in fp32 on the
+ * CUDA cores.  Gradients are rounded to the input dtype (nearest even) on store.
+ * dbeta and dlog_f at position 0 are exactly zero (those enter no logit).
+ * Outputs may not alias inputs.  Argument errors return before any launch.  The
+ * tensor-core kernels bound every wait; an expiry sets PATH_ERR_TIMEOUT in the
+ * workspace status word (read it with path_get_status), which otherwise stays
+ * PATH_OK.
  */
 int path_attn_bwd(const void* q, const void* k, const void* v, const void* w, const float* beta,
                   const float* log_f, const void* o, const float* lse, const void* dO, void* dq, void* dk,
