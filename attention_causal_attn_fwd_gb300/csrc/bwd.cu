@@ -66,8 +66,13 @@ namespace {
 constexpr int kC = kBwdC;
 constexpr int kNT = 256;
 constexpr int kNW = kNT / 32;
-constexpr int kNTL = 512;  // bwd_local: latency-bound walks, one warp per row / key / position
+constexpr int kNTL = 1024;  // bwd_local: latency-bound walks, one warp per row / key / position
 constexpr int kNWL = kNTL / 32;
+// Rows of a chunk in "snake" order over the walking warps: warp w takes rows w, 2 kNWL - 1 - w,
+// 2 kNWL + w, ...  A row's walk is as long as its distance from the chunk's first (or last)
+// position, so pairing a short walk with a long one gives every warp the same number of steps.
+// Row numbers grow with t, so a loop over t ends at the first row >= c.
+__device__ __forceinline__ int snake_row(int t, int wid) { return t * kNWL + ((t & 1) ? kNWL - 1 - wid : wid); }
 constexpr int kNTP = 512;  // bwd_prep: sixteen latency-bound walks in flight per CTA
 
 struct BwdParams {
@@ -335,8 +340,9 @@ template <int D> struct BwdSmem {
     static constexpr int pm = D * (kC + 4) + 2 * kC * (D + 4) + 3 * kC * (kC + 4) + kC;
     static constexpr int chain = 2 * D * LC + RK + RV + D * LD + 6 * kC;
     static constexpr int reduce = 3 * kC * LD + 2 * kC * LC;
-    static constexpr int wbuf = (3 * kC > 2 * D ? 3 * kC : 2 * D);
+    static constexpr int wbuf = 3 * kC;  // bwd_local per-warp scalars; its last phase keeps [2][D] per warp in aV
     static constexpr int local = 6 * kC * D + 4 * kC + kNWL * wbuf;
+    static_assert(kNWL * 2 * D <= kC * D, "the last phase's per-warp vectors must fit over aV");
     static_assert(3 * kC * D >= D * LDP, "dP must fit over the key, value and dk tiles");
     static_assert(chain * 4 <= 227 * 1024 && local * 4 <= 227 * 1024 && reduce * 4 <= 227 * 1024,
                   "shared memory per CTA");
@@ -638,7 +644,7 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
 
 // ------------------------------------------------------------------ bwd_local
 template <typename T, int D>
-__global__ void __launch_bounds__(kNTL) bwd_local(BwdParams p) {
+__global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     constexpr int C = kC, R = WV<D>::R, LDP = BwdSmem<D>::LDP, WB = BwdSmem<D>::wbuf;
     extern __shared__ float smem[];
     float* sW = smem;          // [C][D] w
@@ -651,7 +657,7 @@ __global__ void __launch_bounds__(kNTL) bwd_local(BwdParams p) {
     float* sC = sB + C;        // [C] c (FoX)
     float* aB = sC + C;        // [C] dbeta
     float* aC = aB + C;        // [C] dc (FoX), diagonal part
-    float* sBuf = aC + C;      // [kNWL][WB] per-warp scalars / vectors
+    float* sBuf = aC + C;      // [kNWL][WB] per-warp scalars
     float* sDP = sK;           // [D][LDP] dP_n in the last phase (over sK, sV, aK)
     const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
     const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
@@ -677,7 +683,7 @@ __global__ void __launch_bounds__(kNTL) bwd_local(BwdParams p) {
     float* bga = bal + C;          // w . (gradient) of the reverse walk
 
     // (a) each query row of the chunk: its diagonal logits and the walk that built qbar
-    for (int r = wid; r < c; r += kNWL) {
+    for (int t = 0, r; (r = snake_row(t, wid)) < c; ++t) {
         float u[R], gO[R], g[R];
         vload<D>(u, q + (hrow + r) * D, lane);
         vload<D>(gO, dO + (hrow + r) * D, lane);
@@ -723,7 +729,7 @@ __global__ void __launch_bounds__(kNTL) bwd_local(BwdParams p) {
     }
     // (b) each key of the chunk: the walk that built khat (gradient from later query chunks)
     if (above)
-        for (int r = wid; r < c; r += kNWL) {
+        for (int t = 0, r; (r = snake_row(t, wid)) < c; ++t) {
             float x[R], gx[R];
             vload<D>(x, sK + r * D, lane);
             for (int tt = r + 1; tt < c; ++tt) {
@@ -763,7 +769,7 @@ __global__ void __launch_bounds__(kNTL) bwd_local(BwdParams p) {
         __syncthreads();
         to_smem_v<float, D, kNTL>(sDP, LDP, p.dpm + ((size_t)bh * p.N + n) * D * D, D, D, D);
         __syncthreads();
-        float* vw = sBuf + wid * WB;  // [2][D]: B_t^T w_t, A_t w_t
+        float* vw = aV + wid * 2 * D;  // [2][D]: B_t^T w_t, A_t w_t (aV was written out above)
         for (int r = wid; r < c; r += kNWL) {
             float wh[R], wb[R], y1[R], y2[R];
             vload<D>(wh, sW + r * D, lane);
