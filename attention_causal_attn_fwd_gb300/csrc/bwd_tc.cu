@@ -236,11 +236,13 @@ constexpr uint32_t R_K = 98304;    // khat_m [64][128]
 constexpr uint32_t R_V = 114688;   // v_m [64][128]
 constexpr uint32_t R_PH = 131072;  // P_m hi [128][128]
 constexpr uint32_t R_PL = 163840;  // P_m lo [128][128]
-constexpr uint32_t RB = 196608;    // barriers
+constexpr uint32_t R_ST = 196608;  // per epilogue warp: its 32 rows of dS, then of P [32][64], 128-byte rows
+constexpr uint32_t RB = 229376;    // barriers
 enum { B_DO = 0, B_KV, B_KVE, B_P, B_PE, B_S, B_U, B_UP, B_READY, B_DRAIN, B_COUNT };
 constexpr uint32_t R_SLOT = RB + 96;  // TMEM address, abort flag
 static_assert(B_COUNT * 8 <= 96, "barriers overlap the TMEM slot");
 constexpr size_t kSmem = RB + 128 + 1024;
+static_assert(R_ST + 4 * 8192 <= RB && kSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_U = 128, TM_T = 256;  // TM_U holds U, then G P
 }  // namespace ctk
 
@@ -408,7 +410,17 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
         const float ci = (p.fox && valid) ? p.cum[prow] : 0.f;
         uint8_t* uh = sm + R_UH;
         uint8_t* ul = sm + R_UL;
+        uint8_t* stg = sm + R_ST + (uint32_t)(warp & 3) * 8192u;
+        const int r0 = r & ~31;  // the warp's first row within its chunk
         float rowsum = 0.f;
+        // the hi parts of the warp's 32 rows of U (or G), 256 bytes each, to 8 KB of contiguous rows at dst
+        auto copy_rows = [&](uint4* dst) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int row = 2 * k + (lane >> 4);
+                dst[32 * k + lane] = *reinterpret_cast<const uint4*>(uh + sw_off(32 * (warp & 3) + row, lane & 15, 16384));
+            }
+        };
         // initial U: qbar of chunk nA (chunk nB's rows start at zero and take qbar after key chunk nB)
         auto put_row = [&](const float* src) {  // src: 128 fp32 values (global) or nullptr for zeros
 #pragma unroll 4
@@ -459,13 +471,13 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
                         pw[j / 2] = pack_bf16x2(pr[0], pr[1]);
                         dw[j / 2] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    if (rec) {
-                        uint4* dsd = reinterpret_cast<uint4*>(rec + 2 * C * D + r * C + 32 * h);
-                        uint4* pd = reinterpret_cast<uint4*>(rec + 2 * C * D + C * C + r * C + 32 * h);
+                    if (rec) {  // row `lane` of the warp's staging tiles, 16-byte granules XOR-swizzled by row
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            dsd[q] = make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
-                            pd[q] = make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
+                            const uint32_t o = (uint32_t)lane * 128u + (uint32_t)(((4 * h + q) ^ (lane & 7)) << 4);
+                            *reinterpret_cast<uint4*>(stg + o) = make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
+                            *reinterpret_cast<uint4*>(stg + 4096 + o) =
+                                make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
                         }
                     }
                 }
@@ -478,10 +490,20 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
                         if (lane == (jj & 31)) atomicAdd(p.dccol + (size_t)bh * p.Lp + m * C + jj, t);
                     }
                 }
-                if (rec) {  // U_{chunk,m} (the hi part the logits used) to the pair store
-                    uint4* ud = reinterpret_cast<uint4*>(rec + r * D);
+                if (rec) {  // the warp's 32 rows of dS, P and U_{chunk,m} (the hi part the logits used) to the pair
+                            // store: each is one contiguous block there, written 512 bytes per instruction
+                    __syncwarp();
+                    uint4* dsd = reinterpret_cast<uint4*>(rec + 2 * C * D + r0 * C);
+                    uint4* pd = reinterpret_cast<uint4*>(rec + 2 * C * D + C * C + r0 * C);
 #pragma unroll
-                    for (int gr = 0; gr < 16; ++gr) ud[gr] = *reinterpret_cast<const uint4*>(uh + sw_off(i, gr, 16384));
+                    for (int k = 0; k < 8; ++k) {
+                        const int row = 4 * k + (lane >> 3);
+                        const uint32_t o = (uint32_t)row * 128u + (uint32_t)(((lane & 7) ^ (row & 7)) << 4);
+                        dsd[32 * k + lane] = *reinterpret_cast<const uint4*>(stg + o);
+                        pd[32 * k + lane] = *reinterpret_cast<const uint4*>(stg + 4096 + o);
+                    }
+                    copy_rows(reinterpret_cast<uint4*>(rec + r0 * D));
+                    __syncwarp();
                 }
                 if (m >= 1) {  // U <- U P_m^T, or qbar for chunk nB's rows once key chunk nB is passed
                     if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_U), (uint32_t)(su & 1), wc, 131)))) break;
@@ -509,10 +531,9 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_UP), (uint32_t)(upw & 1), wc, 132)))) break;
                 ++upw;
                 tc_fence_after();
-                if (rec && m >= 1) {  // G_{chunk,m-1} (hi part) to the pair store
-                    uint4* gd = reinterpret_cast<uint4*>(rec + C * D + r * D);
-#pragma unroll
-                    for (int gr = 0; gr < 16; ++gr) gd[gr] = *reinterpret_cast<const uint4*>(uh + sw_off(i, gr, 16384));
+                if (rec && m >= 1) {  // G_{chunk,m-1} (hi part) of the warp's rows to the pair store
+                    copy_rows(reinterpret_cast<uint4*>(rec + C * D + r0 * D));
+                    __syncwarp();
                 }
                 const bool last = valid && m == chunk - 1;  // the row's chain ends here: G is dqbar
 #pragma unroll
