@@ -862,6 +862,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigne
     if (log_f) {
         fox_cumsum<<<BH, 1024, 0, st>>>(log_f, p.L, p.Lp, p.cum);
         cudaMemsetAsync(p.dccol, 0, (size_t)BH * p.Lp * sizeof(float), st);  // bwd_chain adds column sums
+        cudaMemsetAsync(p.dcrow, 0, (size_t)BH * p.Lp * sizeof(float), st);  // bwd_chain_tc adds two halves per row
     }
     bwd_prep<T, D><<<dim3(p.N, BH), kNTP, b_prep, st>>>(p);
     if (p.N >= 3) {

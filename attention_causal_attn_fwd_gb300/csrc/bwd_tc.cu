@@ -227,8 +227,8 @@ bool make_map_rows64(CUtensorMap* mp, const void* base, uint64_t cols, uint64_t 
 
 namespace ctk {
 constexpr int C = 64, D = 128;
-constexpr int kThreads = 192;
-constexpr int kEpi = 128;
+constexpr int kThreads = 320;
+constexpr int kEpi = 256;          // warps 2-9: two per TMEM lane quarter, each owning half the columns
 constexpr uint32_t R_O = 0;        // dO [128][128] (down); dS [128][64] (up)
 constexpr uint32_t R_UH = 32768;   // U (then G) hi  [128][128]
 constexpr uint32_t R_UL = 65536;   // U (then G) lo  [128][128]
@@ -236,13 +236,13 @@ constexpr uint32_t R_K = 98304;    // khat_m [64][128]
 constexpr uint32_t R_V = 114688;   // v_m [64][128]
 constexpr uint32_t R_PH = 131072;  // P_m hi [128][128]
 constexpr uint32_t R_PL = 163840;  // P_m lo [128][128]
-constexpr uint32_t R_ST = 196608;  // per epilogue warp: its 32 rows of dS, then of P [32][64], 128-byte rows
+constexpr uint32_t R_ST = 196608;  // per epilogue warp: its 32 rows x 32 columns of dS, then of P, 64-byte rows
 constexpr uint32_t RB = 229376;    // barriers
 enum { B_DO = 0, B_KV, B_KVE, B_P, B_PE, B_S, B_U, B_UP, B_READY, B_DRAIN, B_COUNT };
 constexpr uint32_t R_SLOT = RB + 96;  // TMEM address, abort flag
 static_assert(B_COUNT * 8 <= 96, "barriers overlap the TMEM slot");
 constexpr size_t kSmem = RB + 128 + 1024;
-static_assert(R_ST + 4 * 8192 <= RB && kSmem <= 227 * 1024, "shared memory per CTA");
+static_assert(R_ST + 8 * 4096 <= RB && kSmem <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t TM_S = 0, TM_DP = 64, TM_U = 128, TM_T = 256;  // TM_U holds U, then G P
 }  // namespace ctk
 
@@ -264,6 +264,7 @@ __device__ __forceinline__ uint32_t sw_off(int r, int g, uint32_t half) {
     return (uint32_t)(g >> 3) * half + (uint32_t)r * 128u + ((uint32_t)((g & 7) ^ (r & 7)) << 4);
 }
 
+template <bool FOX>
 __global__ void __launch_bounds__(ctk::kThreads, 1)
     bwd_chain_tc(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_ph,
@@ -399,32 +400,43 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
             drain_wait(bar(B_DRAIN), 0, p.limit_ns, p.hdr, 129);
         }
     } else {
-        // ------------------------------------------------------------------ epilogue (warps 2-5)
-        const int i = 32 * (warp & 3) + lane;  // tile row = TMEM lane
-        const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        // ------------------------------------------------------------------ epilogue (warps 2-9)
+        // Warp w reads TMEM lanes 32 (w % 4) .. + 31 (the quarter its SM sub-partition may access);
+        // warps w and w + 4 share those rows, `half` 0 taking the first half of every row's columns
+        // (S / dP columns 0-31, U / G / T columns 0-63) and `half` 1 the second.  Each warp writes
+        // and copies out only its own columns, so the two need no synchronisation beyond READY.
+        const int qw = warp & 3, half = (warp - 2) >> 2;
+        const int i = 32 * qw + lane;  // tile row = TMEM lane
+        const uint32_t tl = tmem + ((uint32_t)(32 * qw) << 16);
         const int chunk = i < 64 ? nA : nB, r = i & 63;
         const int g = chunk * C + r;  // query position
         const bool valid = g < p.L;
         const size_t hrow = (size_t)bh * p.L + g, prow = (size_t)bh * p.Lp + g;
         const float lse = valid ? p.lse[hrow] : 0.f, del = valid ? p.delta[prow] : 0.f;
-        const float ci = (p.fox && valid) ? p.cum[prow] : 0.f;
+        const float ci = (FOX && valid) ? p.cum[prow] : 0.f;
+        // p_ij = 2^(scale log2e S_ij + off - log2e c_j); off = -inf for rows the chain does not cover
+        // at this key chunk gives p_ij = 0 without a select per element
+        constexpr float kLog2e = 1.4426950408889634f;
+        const float l2s = p.scale * kLog2e, off_in = (ci - lse) * kLog2e;
         uint8_t* uh = sm + R_UH;
         uint8_t* ul = sm + R_UL;
-        uint8_t* stg = sm + R_ST + (uint32_t)(warp & 3) * 8192u;
+        uint8_t* stg = sm + R_ST + (uint32_t)(warp - 2) * 4096u;
         const int r0 = r & ~31;  // the warp's first row within its chunk
         float rowsum = 0.f;
-        // the hi parts of the warp's 32 rows of U (or G), 256 bytes each, to 8 KB of contiguous rows at dst
-        auto copy_rows = [&](uint4* dst) {
+        // the hi parts of the warp's columns (64 of 128) of its 32 rows of U (or G) to the rows at dst
+        // (row stride 128 elements): one 128-byte segment per row, four rows per instruction
+        auto copy_rows = [&](__nv_bfloat16* dst) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int row = 2 * k + (lane >> 4);
-                dst[32 * k + lane] = *reinterpret_cast<const uint4*>(uh + sw_off(32 * (warp & 3) + row, lane & 15, 16384));
+            for (int k = 0; k < 8; ++k) {
+                const int row = 4 * k + (lane >> 3), gg = lane & 7;
+                *reinterpret_cast<uint4*>(dst + row * D + 64 * half + 8 * gg) =
+                    *reinterpret_cast<const uint4*>(uh + sw_off(32 * qw + row, 8 * half + gg, 16384));
             }
         };
         // initial U: qbar of chunk nA (chunk nB's rows start at zero and take qbar after key chunk nB)
-        auto put_row = [&](const float* src) {  // src: 128 fp32 values (global) or nullptr for zeros
+        auto put_row = [&](const float* src) {  // src: the row's 128 fp32 values (global) or nullptr for zeros
 #pragma unroll 4
-            for (int gr = 0; gr < 16; ++gr) {
+            for (int gr = 8 * half; gr < 8 * half + 8; ++gr) {
                 float v[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) v[e] = src ? src[8 * gr + e] : 0.f;
@@ -448,9 +460,10 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S), (uint32_t)(sd & 1), wc, 130)))) break;
                 ++sd;
                 tc_fence_after();
-                float csum[C];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                const float off = act ? off_in : -INFINITY;
+                float csum[32];
+                {
+                    const int h = half;
                     uint32_t sv[32], dv[32];
                     tmem_ld32(tl + TM_S + 32 * h, sv);
                     tmem_ld32(tl + TM_DP + 32 * h, dv);
@@ -461,48 +474,51 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
                         float pr[2], ds[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const int jj = 32 * h + j + e;
-                            const float cj = p.fox ? p.cum[(size_t)bh * p.Lp + m * C + jj] : 0.f;
-                            pr[e] = act ? __expf(p.scale * __uint_as_float(sv[j + e]) + ci - cj - lse) : 0.f;
+                            const int jj = 32 * h + j + e;  // key column
+                            float x = fmaf(l2s, __uint_as_float(sv[j + e]), off);
+                            if constexpr (FOX) x -= kLog2e * p.cum[(size_t)bh * p.Lp + m * C + jj];
+                            pr[e] = ex2_approx(x);
                             ds[e] = pr[e] * (__uint_as_float(dv[j + e]) - del);
-                            csum[jj] = ds[e];
-                            rowsum += ds[e];
+                            if constexpr (FOX) {
+                                csum[j + e] = ds[e];
+                                rowsum += ds[e];
+                            }
                         }
                         pw[j / 2] = pack_bf16x2(pr[0], pr[1]);
                         dw[j / 2] = pack_bf16x2(ds[0], ds[1]);
                     }
-                    if (rec) {  // row `lane` of the warp's staging tiles, 16-byte granules XOR-swizzled by row
+                    if (rec) {  // row `lane` of the warp's staging tiles, 16-byte granules XOR-swizzled by row pair
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const uint32_t o = (uint32_t)lane * 128u + (uint32_t)(((4 * h + q) ^ (lane & 7)) << 4);
+                            const uint32_t o = (uint32_t)lane * 64u + (uint32_t)((q ^ ((lane >> 1) & 3)) << 4);
                             *reinterpret_cast<uint4*>(stg + o) = make_uint4(dw[4 * q], dw[4 * q + 1], dw[4 * q + 2], dw[4 * q + 3]);
-                            *reinterpret_cast<uint4*>(stg + 4096 + o) =
+                            *reinterpret_cast<uint4*>(stg + 2048 + o) =
                                 make_uint4(pw[4 * q], pw[4 * q + 1], pw[4 * q + 2], pw[4 * q + 3]);
                         }
                     }
                 }
-                if (p.fox) {  // column sums of dS over the 32 rows of the warp, then across warps
+                if constexpr (FOX) {  // column sums of dS over the 32 rows of the warp, then across warps
 #pragma unroll
-                    for (int jj = 0; jj < C; ++jj) {
+                    for (int jj = 0; jj < 32; ++jj) {
                         float t = csum[jj];
 #pragma unroll
                         for (int o = 16; o; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                        if (lane == (jj & 31)) atomicAdd(p.dccol + (size_t)bh * p.Lp + m * C + jj, t);
+                        if (lane == jj) atomicAdd(p.dccol + (size_t)bh * p.Lp + m * C + 32 * half + jj, t);
                     }
                 }
-                if (rec) {  // the warp's 32 rows of dS, P and U_{chunk,m} (the hi part the logits used) to the pair
-                            // store: each is one contiguous block there, written 512 bytes per instruction
+                if (rec) {  // the warp's columns of its 32 rows of dS, P and U_{chunk,m} (the hi part the logits
+                            // used) to the pair store, whole 32-byte sectors, eight or four rows per instruction
                     __syncwarp();
-                    uint4* dsd = reinterpret_cast<uint4*>(rec + 2 * C * D + r0 * C);
-                    uint4* pd = reinterpret_cast<uint4*>(rec + 2 * C * D + C * C + r0 * C);
+                    __nv_bfloat16* dsd = rec + 2 * C * D + r0 * C + 32 * half;
+                    __nv_bfloat16* pd = dsd + C * C;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int row = 4 * k + (lane >> 3);
-                        const uint32_t o = (uint32_t)row * 128u + (uint32_t)(((lane & 7) ^ (row & 7)) << 4);
-                        dsd[32 * k + lane] = *reinterpret_cast<const uint4*>(stg + o);
-                        pd[32 * k + lane] = *reinterpret_cast<const uint4*>(stg + 4096 + o);
+                    for (int k = 0; k < 4; ++k) {
+                        const int row = 8 * k + (lane >> 2), gg = lane & 3;
+                        const uint32_t o = (uint32_t)row * 64u + (uint32_t)((gg ^ ((row >> 1) & 3)) << 4);
+                        *reinterpret_cast<uint4*>(dsd + row * C + 8 * gg) = *reinterpret_cast<const uint4*>(stg + o);
+                        *reinterpret_cast<uint4*>(pd + row * C + 8 * gg) = *reinterpret_cast<const uint4*>(stg + 2048 + o);
                     }
-                    copy_rows(reinterpret_cast<uint4*>(rec + r0 * D));
+                    copy_rows(rec + r0 * D);
                     __syncwarp();
                 }
                 if (m >= 1) {  // U <- U P_m^T, or qbar for chunk nB's rows once key chunk nB is passed
@@ -513,7 +529,7 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
                         put_row(valid ? p.qbar + prow * D : nullptr);
                     } else {
 #pragma unroll
-                        for (int h = 0; h < 4; ++h) {
+                        for (int h = 2 * half; h < 2 * half + 2; ++h) {
                             uint32_t v[32];
                             tmem_ld32(tl + TM_U + 32 * h, v);
                             tmem_wait_ld();
@@ -532,12 +548,13 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
                 ++upw;
                 tc_fence_after();
                 if (rec && m >= 1) {  // G_{chunk,m-1} (hi part) of the warp's rows to the pair store
-                    copy_rows(reinterpret_cast<uint4*>(rec + C * D + r0 * D));
+                    __syncwarp();  // rows written by other lanes in the previous step
+                    copy_rows(rec + C * D + r0 * D);
                     __syncwarp();
                 }
                 const bool last = valid && m == chunk - 1;  // the row's chain ends here: G is dqbar
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
+                for (int h = 2 * half; h < 2 * half + 2; ++h) {
                     uint32_t tv[32], gv[32];
                     tmem_ld32(tl + TM_T + 32 * h, tv);
                     if (m >= 1) tmem_ld32(tl + TM_U + 32 * h, gv);
@@ -560,7 +577,9 @@ __global__ void __launch_bounds__(ctk::kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(B_READY));
         }
-        if (p.fox && valid && chunk >= 1) p.dcrow[prow] = rowsum;
+        // the two warps of a row each hold the sum over their columns; dcrow was zeroed by the launcher,
+        // and a sum of two terms does not depend on their order
+        if (FOX && valid && chunk >= 1) atomicAdd(p.dcrow + prow, rowsum);
     }
 
     tc_fence_before();
@@ -607,10 +626,11 @@ cudaError_t launch_bwd_chain_tc(const void* dO, const void* v, const void* khat1
     p.pairs = static_cast<__nv_bfloat16*>(pairs);
     p.hdr = hdr;
     p.limit_ns = 2000000000ull;
-    cudaError_t e = cudaFuncSetAttribute(bwd_chain_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    auto kern = fox ? bwd_chain_tc<true> : bwd_chain_tc<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
     mark_start(st);
-    bwd_chain_tc<<<dim3(N / 2, BH), kThreads, kSmem, st>>>(mdo, mk, mv, mph, mpl, mds, p);
+    kern<<<dim3(N / 2, BH), kThreads, kSmem, st>>>(mdo, mk, mv, mph, mpl, mds, p);
     mark_end(st);
     return cudaGetLastError();
 }
