@@ -205,8 +205,10 @@ __global__ void __launch_bounds__(rtk::kThreads, 1)
 // part and bf16 khat, like the forward's scan.  Per pair the epilogue writes
 // U, G, dS and P (bf16) for bwd_reduce_tc and the FoX row / column sums.
 //
-// Roles (192 threads): warp 0 TMA, warp 1 MMA issue, warps 2-5 the epilogue
-// (one TMEM lane = one query row).  Every wait is bounded; on expiry the kernel
+// Roles (320 threads): warp 0 TMA, warp 1 MMA issue, warps 2-9 the epilogue,
+// two warps per TMEM lane quarter (one TMEM lane = one query row) that split
+// every row's columns.  FoX is a template parameter, so the non-FoX dS loop
+// carries no per-element test.  Every wait is bounded; on expiry the kernel
 // records PATH_ERR_TIMEOUT, every role stops, copies and MMAs drain and TMEM is
 // freed.
 namespace {
