@@ -158,6 +158,9 @@ size_t path_attn_bwd_workspace_bytes(int B, int H, int L, int d, int dtype);
  * parts) and the within-chunk walks in fp32; other bf16 sizes run in fp32 on the
  * CUDA cores.  Gradients are rounded to the input dtype (nearest even) on store.
  * dbeta and dlog_f at position 0 are exactly zero (those enter no logit).
+ * Repeated calls agree to rounding, not bit for bit: the within-chunk walks add
+ * into shared-memory accumulators, and the PaTH-FoX column sums into global ones,
+ * in an order that depends on scheduling.
  * Outputs may not alias inputs.  Argument errors return before any launch.  The
  * tensor-core kernels bound every wait; an expiry sets PATH_ERR_TIMEOUT in the
  * workspace status word (read it with path_get_status), which otherwise stays
