@@ -499,3 +499,50 @@ def test_bwd_invariants():
                            dO[::-1].copy(), scale=0.5)
     for n in _GRAD_NAMES:  # rows are summed by threads in parallel: equal up to rounding order
         np.testing.assert_allclose(gb[n][1], g1[n], rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- gradient pins catch planted mistakes
+def _bwd_walk_mutant(q, k, v, w, beta, dO, scale, mutation):
+    """A pure-Python copy of the backward oracle's row walk (no forget gates) with one planted mistake,
+    to show that the finite-difference pin rejects it.  Row i walks u_j = H_{j+1} ... H_i q_i down to
+    j = 0, then back up with g = dloss/du: g <- H_j g + scale ds_ij k_j, the transition H_j receiving
+    the outer product g u_j^T."""
+    L, d = q.shape
+    o, lse = orc.path_attn(q, k, v, w, beta, scale=scale)
+    Delta = (dO * o).sum(1)
+    grads = {n: np.zeros_like(x) for n, x in (("dq", q), ("dk", k), ("dv", v), ("dw", w), ("dbeta", beta))}
+    for i in range(L):
+        us, s, u = {}, {}, q[i].copy()
+        for j in range(i, -1, -1):
+            us[j], s[j] = u.copy(), scale * (k[j] @ u)
+            u = u - beta[j] * (w[j] @ u) * w[j]
+        g = np.zeros(d)
+        for j in range(i + 1):
+            p = np.exp(s[j] - lse[i])
+            ds = p * (dO[i] @ v[j] - (0.0 if mutation == "no_delta" else Delta[i]))
+            grads["dv"][j] += p * dO[i]
+            grads["dk"][j] += scale * ds * us[j]
+            wu, wg = w[j] @ us[j], w[j] @ g
+            grads["dbeta"][j] += (wg * wu) if mutation == "dbeta_sign" else -(wg * wu)
+            grads["dw"][j] += -beta[j] * (wu * g + (0.0 if mutation == "dw_one_term" else wg * us[j]))
+            if mutation == "walk_order":  # the logit's share taken before the transition instead of after
+                g = g + scale * ds * k[j]
+                g = g - beta[j] * (w[j] @ g) * w[j]
+            else:
+                g = g - beta[j] * wg * w[j] + scale * ds * k[j]
+        grads["dq"][i] += g
+    return grads
+
+
+@pytest.mark.parametrize("mutation", ["no_delta", "dbeta_sign", "dw_one_term", "walk_order"])
+def test_bwd_pins_reject_planted_mistakes(mutation):
+    rng = np.random.default_rng(96)
+    L, d = 6, 3
+    q, k, v, w, beta = _rand_case(rng, L, d)
+    dO = rng.standard_normal((L, d))
+    fd = _fd_grads(q, k, v, w, beta, dO, None, 0.6)
+    good = _bwd_walk_mutant(q, k, v, w, beta, dO, 0.6, None)
+    for n in _GRAD_NAMES:
+        np.testing.assert_allclose(good[n], fd[n], rtol=0, atol=2e-8, err_msg=n)
+    bad = _bwd_walk_mutant(q, k, v, w, beta, dO, 0.6, mutation)
+    assert max(float(np.abs(bad[n] - fd[n]).max()) for n in _GRAD_NAMES) > 1e-3
