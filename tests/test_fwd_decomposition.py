@@ -16,7 +16,8 @@ S_nm = scale q~ khat_m^T, q~ <- q~ + (q~ W_m^T)(-U_m), the logits of all blocks 
 softmax (with the forget-gate bias c_i - c_j of "Extensões: PaTH-FoX" when given).  This module
 writes those steps out with dense numpy products, and the tests check that they reproduce the
 oracle's o and lse to fp64 rounding for several chunk sizes, ragged last chunks and beta = 0 /
-beta = 2 positions.  It shares no code with the kernels and computes nothing the oracle relies on.
+beta = 2 positions; the prefill -> decode hand-off's suffix products are checked against explicit
+walks the same way.  It shares no code with the kernels and computes nothing the oracle relies on.
 """
 import numpy as np
 import pytest
@@ -101,3 +102,30 @@ def test_chunk_factors_carry_rows_to_the_chunk_ends():
         for t in range(i + 1, C):
             x = H(x, t)
         np.testing.assert_allclose(f["khat"][i], x, rtol=0, atol=1e-12)
+
+
+def test_blocked_prefill_cache_matches_walks():
+    """The prefill -> decode hand-off (§3 "Inferência"): the cache a prompt of L tokens leaves is
+    k~_j = H_{L-1} ... H_{j+1} k_j.  Blocked as the hand-off kernels do it: khat_j to its chunk's end,
+    then k~_j^T = khat_j^T N_{m+1} with the suffix products N_c = P_c ... P_last built right to left as
+    N_c = N_{c+1} - W_c^T (V_c N_{c+1}), V_c = A_c W_c (so P_c = I - W_c^T V_c)."""
+    rng = np.random.default_rng(31)
+    L, d, C = 45, 6, 8
+    q, k, _, w, beta = _case(rng, L, d)
+    N = -(-L // C)
+    Lp = N * C
+    pad = lambda x: np.concatenate([x, np.zeros((Lp - L,) + x.shape[1:])])
+    Q, K, W, B = pad(q), pad(k), pad(w), pad(beta)
+    f = [chunk_factors(W[n * C:(n + 1) * C], Q[n * C:(n + 1) * C], K[n * C:(n + 1) * C], B[n * C:(n + 1) * C])
+         for n in range(N)]
+    cache = np.zeros((Lp, d))
+    Nsuf = np.eye(d)  # N_{c+1}, empty past the last chunk
+    for c in range(N - 1, -1, -1):
+        cache[c * C:(c + 1) * C] = f[c]["khat"] @ Nsuf
+        Wc = W[c * C:(c + 1) * C]
+        Nsuf = Nsuf - Wc.T @ ((f[c]["A"] @ Wc) @ Nsuf)
+    for j in range(L):
+        x = k[j].copy()
+        for t in range(j + 1, L):
+            x = x - beta[t] * (w[t] @ x) * w[t]
+        np.testing.assert_allclose(cache[j], x, rtol=0, atol=1e-12)
