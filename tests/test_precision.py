@@ -38,3 +38,26 @@ def test_hi_lo_split_product_bound(M, K, N, seed):
     # bf16 operands alone are three orders of magnitude worse, which is why the split is used
     plain = (ha @ hb).astype(np.float64)
     assert np.max(np.abs(plain - exact) / mag) > 50 * np.max(np.abs(split - exact) / mag)
+
+
+def test_bf16_unit_w_transitions_stay_within_the_fox_skip_margin():
+    """The PaTH-FoX far-block skip bounds a transported logit by 2 |q| max |khat|: each H_s is
+    non-expansive for beta in [0, 2] and unit w, and the factor 2 is the margin for w rounded to bf16,
+    whose squared norm is off by at most ~2^-8 so that one transition can stretch the component
+    along w by at most 1 + 2^-7.  For random bf16 unit w (the inputs' recipe) the growth of a vector
+    walked through 4096 transitions with beta = 2 (the expanding extreme) stays far inside 2."""
+    rng = np.random.default_rng(41)
+    L, d = 4096, 128
+    w = rng.standard_normal((L, d)).astype(np.float32)
+    w /= np.linalg.norm(w, axis=1, keepdims=True)
+    w = _bf16(w).astype(np.float64)
+    n2 = (w * w).sum(1)
+    assert np.max(np.abs(n2 - 1.0)) <= 2.0 ** -8
+    for trial in range(4):
+        x = rng.standard_normal(d)
+        x0 = np.linalg.norm(x)
+        peak = 1.0
+        for s in range(L):
+            x = x - 2.0 * (w[s] @ x) * w[s]
+            peak = max(peak, np.linalg.norm(x) / x0)
+        assert peak < 1.05, peak
