@@ -102,6 +102,10 @@ int path_attn_fwd(const void* q, const void* k, const void* v, const void* w, co
  * PaTH-FoX forward (§2 "Extensões: PaTH-FoX"): as path_attn_fwd, with the
  * forget-gate bias  sum_{s=j+1..i} log_f[s]  added unscaled to the scaled
  * logit of (i, j).  log_f: [B, H, L] float (log of the forget gate, <= 0).
+ * The bf16 tensor-core path stops a query tile's scan once every key further
+ * left provably has weight exactly 0 in fp32 (bias plus a bound on the
+ * transported logit); the bound assumes the unchecked preconditions above
+ * (beta in [0, 2], |w| = 1, up to bf16 rounding of w).
  */
 int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w, const float* beta,
                       const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype,
