@@ -17,7 +17,7 @@
  *     time the historical keys are updated in place with the current step's
  *     transition.
  *
- * Readings taken where the page is silent (each also listed in the design doc):
+ * Readings taken where the page is silent:
  *   - the product is ascending, H_{j+1} H_{j+2} ... H_i (the only order under
  *     which the in-place key update of the "Inferência" bullet is exact);
  *   - the product is empty (= I) at j = i, and j = i takes part in the softmax;
