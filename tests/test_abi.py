@@ -87,13 +87,15 @@ def test_forward_argument_errors(lib):
 
 def test_bwd_argument_errors(lib):
     def bwd(**kw):
-        a = dict(log_f=None, dlog_f=None, lse=FAKE, d=64, dt=P.PATH_BF16, causal=1, BH=(2, 3), ws_bytes=1 << 40,
-                 dq=FAKE)
+        a = dict(log_f=None, dlog_f=None, lse=FAKE, d=64, dt=P.PATH_BF16, causal=1, BH=(2, 3), L=300,
+                 ws_bytes=1 << 40, dq=FAKE)
         a.update(kw)
         B, H = a["BH"]
         return lib.path_attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, a["log_f"], FAKE, a["lse"], FAKE, a["dq"], FAKE, FAKE,
-                                 FAKE, FAKE, a["dlog_f"], B, H, 300, a["d"], a["dt"], a["causal"],
+                                 FAKE, FAKE, a["dlog_f"], B, H, a["L"], a["d"], a["dt"], a["causal"],
                                  ctypes.c_float(0.125), FAKE, a["ws_bytes"], None)
+    assert bwd(L=0) == P.PATH_ERR_INVALID                 # empty sequence
+    assert bwd(BH=(0, 3)) == P.PATH_ERR_INVALID
     assert bwd(lse=None) == P.PATH_ERR_INVALID            # the forward's lse is required
     assert bwd(dq=None) == P.PATH_ERR_INVALID
     assert bwd(log_f=FAKE) == P.PATH_ERR_INVALID          # FoX needs dlog_f
