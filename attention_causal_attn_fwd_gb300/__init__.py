@@ -13,7 +13,7 @@ Functions keep the C names:
 - ``path_attn_fwd_relbias(q, k, v, w, beta, rel_bias, scale=None, lse=False)``
 - ``path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, scale=None)``
 - ``path_kcache_update(kcache, n_cached, w_t, beta_t)``
-- ``path_get_status(workspace)``, ``path_attn_workspace_bytes(...)``,
+- ``path_get_status(workspace)``, ``path_fwd_visited_blocks(workspace)``, ``path_attn_workspace_bytes(...)``,
   ``path_decode_workspace_bytes(...)``
 """
 from __future__ import annotations
@@ -36,7 +36,7 @@ EXPORTED = ("path_version", "path_status_string", "path_attn_workspace_bytes", "
             "path_attn_fwd_fox", "path_decode_workspace_bytes", "path_kcache_update", "path_decode_step",
             "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events", "path_decode_step_noalloc",
             "path_prefill_workspace_bytes", "path_prefill_kcache", "path_attn_fwd_relbias",
-            "path_attn_bwd_workspace_bytes", "path_attn_bwd")
+            "path_attn_bwd_workspace_bytes", "path_attn_bwd", "path_fwd_visited_blocks", "path_debug_set_fox_skip")
 
 
 class PathLibraryError(RuntimeError):
@@ -103,6 +103,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.path_debug_set_fault.restype = None
     lib.path_debug_set_timing_events.argtypes = [_vp, _vp]
     lib.path_debug_set_timing_events.restype = None
+    lib.path_fwd_visited_blocks.argtypes = [_vp, _vp]
+    lib.path_fwd_visited_blocks.restype = ctypes.c_longlong
+    lib.path_debug_set_fox_skip.argtypes = [_i]
+    lib.path_debug_set_fox_skip.restype = None
     if path is None:
         _lib = lib
     return lib
@@ -312,6 +316,16 @@ def path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached: int, 
 def path_get_status(workspace_tensor) -> int:
     """Status word of the last call that used this workspace (synchronises the current stream)."""
     return int(load().path_get_status(_ptr(workspace_tensor), _stream()))
+
+
+def path_fwd_visited_blocks(workspace_tensor) -> int:
+    """(query tile, key block) pairs the last bf16 forward on this workspace visited (synchronises)."""
+    return int(load().path_fwd_visited_blocks(_ptr(workspace_tensor), _stream()))
+
+
+def path_debug_set_fox_skip(enabled: bool):
+    """Turn the PaTH-FoX far-block stop of the bf16 forward on (default) or off (visit every block)."""
+    load().path_debug_set_fox_skip(1 if enabled else 0)
 
 
 def path_debug_set_fault(mask: int):

@@ -2,6 +2,7 @@
 // Host side only: argument validation, workspace carve-up and kernel dispatch.
 // Nothing here allocates device memory; every launch goes to the caller's stream.
 #include <atomic>
+#include <cstddef>
 #include <cstdio>
 
 #include "common.cuh"
@@ -15,7 +16,8 @@ int tc_chunk(int d);
 bool tc_supported(int d);
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
                         const float* log_f, const float* rel_bias, int H, void* o, float* lse, int BH, int L, int d,
-                        float scale, unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st);
+                        float scale, unsigned char* ws, const FwdLayout& lay, int fault_mask, const FwdOptions& opt,
+                        cudaStream_t st);
 cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w, const float* beta, void* kcache,
                            int BH, int L, int n_max, unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
 cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
@@ -30,6 +32,7 @@ cudaError_t kcache_update_launch(int dtype, int d, void* kc, int n_cached, int n
                                  const float* beta_t, int BH, cudaStream_t st);
 
 static std::atomic<int> g_fault_mask{0};
+static std::atomic<int> g_fox_no_skip{0};
 static std::atomic<void*> g_ev_start{nullptr}, g_ev_end{nullptr};
 
 void timing_events(cudaEvent_t* start, cudaEvent_t* end) {
@@ -57,7 +60,7 @@ static int fwd_common(const void* q, const void* k, const void* v, const void* w
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
     if (!causal) return PATH_ERR_UNSUPPORTED;
     if (!fwd_d_ok(d, dtype)) return PATH_ERR_UNSUPPORTED;
-    if ((long long)B * H * L > (1ll << 31) / 256) return PATH_ERR_UNSUPPORTED;
+    if ((long long)B * H * L > (1ll << 31) / 256 || (long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
     if (!q || !k || !v || !w || !beta || !o || (extra != 0 && !bias)) return PATH_ERR_INVALID;
     const void* ptrs[] = {q, k, v, w, beta, o};
     for (const void* p : ptrs)
@@ -73,7 +76,7 @@ static int fwd_common(const void* q, const void* k, const void* v, const void* w
         e = fwd_simt_f32(q, k, v, w, beta, log_f, rel_bias, H, o, lse, B * H, L, d, scale, wsb, lay, st);
     else
         e = fwd_tc_bf16(q, k, v, w, beta, log_f, rel_bias, H, o, lse, B * H, L, d, scale, wsb, lay,
-                        g_fault_mask.load(), st);
+                        g_fault_mask.load(), FwdOptions{g_fox_no_skip.load()}, st);
     if (e != cudaSuccess) {
         std::fprintf(stderr, "pathattn: forward launch failed: %s\n", cudaGetErrorString(e));
         return PATH_ERR_CUDA;
@@ -137,6 +140,7 @@ int path_prefill_kcache(const void* k, const void* w, const float* beta, void* k
     if (B < 1 || H < 1 || L < 1 || n_max < L) return PATH_ERR_INVALID;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
     if (!fwd_d_ok(d, dtype)) return PATH_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535 || (long long)B * H * L > (1ll << 31) / 256) return PATH_ERR_UNSUPPORTED;
     if (!k || !w || !beta || !kcache) return PATH_ERR_INVALID;
     if (!aligned16(k) || !aligned16(w) || !aligned16(beta) || !aligned16(kcache)) return PATH_ERR_INVALID;
     const FwdLayout lay = fwd_layout(B, H, L, d, fwd_chunk(d, dtype), elt_size(dtype), true);
@@ -193,7 +197,7 @@ int path_kcache_update(void* kcache, int B, int H, int n_cached, int n_max, int 
                        const float* beta_t, int dtype, path_stream_t stream) {
     if (B < 1 || H < 1 || n_max < 1 || n_cached < 0 || n_cached > n_max) return PATH_ERR_INVALID;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
-    if (!dec_d_ok(d)) return PATH_ERR_UNSUPPORTED;
+    if (!dec_d_ok(d) || (long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
     if (!kcache || !w_t || !beta_t) return PATH_ERR_INVALID;
     if (!aligned16(kcache) || !aligned16(w_t)) return PATH_ERR_INVALID;
     cudaError_t e = kcache_update_launch(dtype, d, kcache, n_cached, n_max, w_t, beta_t, B * H,
@@ -208,7 +212,7 @@ int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const vo
     if (B < 1 || H < 1 || n_max < 1 || n_cached < 0) return PATH_ERR_INVALID;
     if (n_cached + 1 > n_max) return PATH_ERR_INVALID;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
-    if (!dec_d_ok(d)) return PATH_ERR_UNSUPPORTED;
+    if (!dec_d_ok(d) || (long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
     if (!q_t || !k_t || !v_t || !w_t || !beta_t || !kcache || !vcache || !o_t) return PATH_ERR_INVALID;
     const void* ptrs[] = {q_t, k_t, v_t, w_t, kcache, vcache, o_t};
     for (const void* p : ptrs)
@@ -231,6 +235,20 @@ int path_get_status(const void* workspace, path_stream_t stream) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return PATH_ERR_CUDA;
     return status;
 }
+
+long long path_fwd_visited_blocks(const void* workspace, path_stream_t stream) {
+    if (!workspace) return -1;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned visited = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    if (cudaMemcpyAsync(&visited, static_cast<const unsigned char*>(workspace) + offsetof(WsHeader, visited),
+                        sizeof(unsigned), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    return (long long)visited;
+}
+
+void path_debug_set_fox_skip(int enabled) { g_fox_no_skip.store(enabled ? 0 : 1); }
 
 void path_debug_set_fault(int mask) { g_fault_mask.store(mask); }
 

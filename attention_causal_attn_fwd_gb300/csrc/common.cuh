@@ -66,7 +66,8 @@ struct WsHeader {
     int status;
     int fault_site;     // which wait expired (debugging aid)
     unsigned work_next; // tile counter for persistent schedulers
-    int pad[61];
+    unsigned visited;   // tensor-core forward: (query tile, key block) pairs visited, diagonal included
+    int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -97,7 +98,10 @@ __host__ __device__ constexpr int cdiv(int a, int b) { return (a + b - 1) / b; }
 // reads never cross into the next head; padded rows hold zeros.
 //   qhat : float [BH, Lp, d]  queries transported to their chunk start
 //   khat : T     [BH, Lp, d]  keys transported to their chunk end
-//   un   : T     [BH, Lp, d]  -U = -A^T W per chunk (query-side scan factor)
+//   un   : T     [BH, Lp, d]  query-side scan factor per chunk: -U = -A^T W
+//                             (fp32 CUDA-core path), or the transition
+//                             P - I = -W^T A W, d x d in the chunk's first d
+//                             rows (bf16 tensor-core path)
 //   y    : T     [BH, Lp, C]  Y = tril(Q W^T) A^T per chunk (diagonal blocks)
 //   zn   : T     [BH, Lp, C]  -Z = -triu_1(K W^T) per chunk (diagonal blocks)
 //   cum  : float [BH, Lp]     inclusive cumulative sum of log f (PaTH-FoX)
@@ -126,6 +130,12 @@ inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt, bool 
     s.total = off;
     return s;
 }
+
+// Options of the bf16 tensor-core forward that change no result: no_skip
+// visits every key block on the PaTH-FoX path (the far-block stop off).
+struct FwdOptions {
+    int no_skip;
+};
 
 // ----------------------------------------------------------------------------- decode workspace
 constexpr int kDecodeRowsPerSplit = 2048;

@@ -299,6 +299,8 @@ cudaError_t kcache_update_launch(int dtype, int d, void* kc, int n_cached, int n
 // Scratch for path_decode_step_noalloc: the split-K partials and the status
 // header live in this file-scope device array instead of a caller workspace.
 // Every GPU that loads the library holds it until the process exits.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -306,18 +308,47 @@ namespace pathattn {
 
 static __device__ __align__(256) unsigned char g_decode_scratch[PATH_DECODE_NOALLOC_SCRATCH_BYTES];
 
+// Unique id of the current device's primary context (driver entry points
+// fetched through the runtime, so the library does not link libcuda).  It
+// changes when the context is destroyed and recreated (cudaDeviceReset), which
+// unloads the module and with it the array.
+static bool current_context_id(unsigned long long* id) {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    if (!get_current || !get_id) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) != cudaSuccess ||
+            qa != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) != cudaSuccess ||
+            qb != cudaDriverEntryPointSuccess)
+            return false;
+        get_current = reinterpret_cast<GetCurrent>(a);
+        get_id = reinterpret_cast<GetId>(b);
+    }
+    CUcontext ctx = nullptr;
+    return get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr && get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 // Device address of g_decode_scratch for the current device, looked up once per
-// device.  In host code the array's name is only a host-side stand-in, so the
-// kernels are given this address instead.
+// device (and again after the device's context has been reset).  In host code
+// the array's name is only a host-side stand-in, so the kernels are given this
+// address instead.
 static int noalloc_scratch_address(unsigned char** out) {
     constexpr int kMaxDevices = 64;
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static unsigned long long ctx_id[kMaxDevices] = {};
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return PATH_ERR_CUDA;
     if (dev >= kMaxDevices) return PATH_ERR_UNSUPPORTED;
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);  // false while no context is current on this thread
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
+    if (!addr[dev] || !have_id || ctx_id[dev] != id) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (e != cudaSuccess || p == nullptr) {
@@ -325,7 +356,10 @@ static int noalloc_scratch_address(unsigned char** out) {
                          cudaGetErrorString(e));
             return PATH_ERR_CUDA;
         }
+        // the lookup made the device's context current: record which one the address belongs to
+        if (!current_context_id(&id)) return PATH_ERR_CUDA;
         addr[dev] = p;
+        ctx_id[dev] = id;
     }
     *out = static_cast<unsigned char*>(addr[dev]);
     return PATH_OK;
@@ -344,6 +378,7 @@ extern "C" int path_decode_step_noalloc(const void* q_t, const void* k_t, const 
     if (n_cached + 1 > n_max) return PATH_ERR_INVALID;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
     if (d != 16 && d != 32 && d != 64 && d != 128) return PATH_ERR_UNSUPPORTED;
+    if ((long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
     if (!q_t || !k_t || !v_t || !w_t || !beta_t || !kcache || !vcache || !o_t) return PATH_ERR_INVALID;
     const void* ptrs[] = {q_t, k_t, v_t, w_t, kcache, vcache, o_t};
     for (const void* p : ptrs)

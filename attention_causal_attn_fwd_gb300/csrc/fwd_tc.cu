@@ -8,36 +8,38 @@
 //
 // One CTA owns a tile of 128 queries (= one chunk n of one head) and walks the
 // key/value blocks m = n (diagonal), n-1, ..., 0.  Per block m < n, with the
-// transported query q~ (fp32 master in TMEM, bf16 copy in shared memory):
-//   S_w   S_w = q~ W_m^T                               (M=128, N=128, K=d)
-//   S_k   S_k = q~ khat_m^T                            (M=128, N=128, K=d)
-//   MMA3  q~ += bf16(S_w) (-U_m)                       (M=128, N=d, K=128)
-//   P V   O  += P V_m,  P = exp2(S_k * scale*log2e - m)  (M=128, N=d, K=128)
-// and the diagonal block uses S = Q K^T + Y (-Z)^T with the causal mask.  The
-// logits may carry an additive bias (MODE 1 PaTH-FoX, MODE 2 relative position).
+// transported query q~ (fp32 master and its bf16 copy, both in TMEM):
+//   S_k   S = q~ khat_m^T                                 (M=128, N=128, K=d)
+//   T     q~ += bf16(q~) (P_m - I)^T                      (M=128, N=d,   K=d)
+//   P V   O += P V_m,  P = exp2(S * scale*log2e - m)      (M=128, N=d,   K=128)
+// where P_m = I - W_m^T A_m W_m is the chunk's transition in the UT form of §3
+// "Representação de Transformação UT" (the UT prep writes P_m - I in bf16), so
+// the query moves through a whole chunk in one d x d product.  The diagonal
+// block uses S = Q K^T + Y (-Z)^T with the causal mask.  The logits may carry
+// an additive bias (MODE 1 PaTH-FoX, MODE 2 relative position).
 // Online softmax keeps one query row per thread (TMEM lane = row), so row
 // max and sum need no cross-thread reduction.  The running max is only
 // raised (and O rescaled) when it grows by more than 2^8, which keeps every
 // exponent <= 2^8 and makes rescales rare.
 //
-// Warp roles (352 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer (one lane) + TMEM allocation
-//   warp 1      tcgen05.mma issuer (one lane): S_w and MMA3 (with FoX: all MMAs)
-//   warps 2-5   softmax: S_k -> P (bf16, into TMEM), row statistics, epilogue
-//   warps 6-9   query transport: S_w -> bf16 (TMEM), fp32 q~ -> bf16 q~ (smem)
-//   warp 10     tcgen05.mma issuer (one lane): diagonal, S_k and P V (idle with FoX)
+//   warp 1      tcgen05.mma issuer (one lane), per block in the order
+//               S_k(it), T(it), P V(it-1): the transport of the next query
+//               overlaps P V, and the softmax of block it overlaps T and P V
+//   warps 2-5   softmax: S -> P (bf16, into TMEM), row statistics, epilogue
+//   warps 6-9   query transport: fp32 q~ master -> bf16 q~ (TMEM)
+// Every MMA reads its A operand from TMEM except the diagonal block's, so
+// shared memory carries only the B tiles (khat, P - I, V) and their TMA writes.
 //
-// TMEM (512 columns x 128 lanes, fp32): [0,128) S_k / P (bf16), [128,256) S_w /
-// bf16(S_w), [256,256+d) O, [384,384+d) q~ master.
-// Shared memory (1024-aligned, 128-byte swizzled tiles as TMA writes them):
-//   SM_Q  32 KB  Q (diagonal) then bf16 q~, K-major, 64-column chunks of 16 KB
-//   SM_KW 64 KB  per 64-column chunk c (32 KB): rows 0-127 khat_m (or K),
-//                rows 128-255 W_m of even block iterations (or -Z)
-//   SM_V  64 KB  V_m, MN-major B operand (64-column boxes of 16 KB), two
-//                slots by block parity
-//   SM_U  32 KB  -U_m (MN-major) or, on the diagonal, Y (K-major)
-//   SM_P  32 KB  W slot 1 (W of odd block iterations; slot 0 is interleaved
-//                with khat in SM_KW)
+// TMEM (512 columns x 128 lanes, 32-bit): [0,128) S (fp32), [128,192) P (bf16
+// pairs), [192,192+d/2) bf16 q~ (pairs), [256,256+d) O, [384,384+d) q~ master.
+// Shared memory (1024-aligned, 128-byte swizzled tiles as TMA writes them,
+// 64-column boxes of 16 KB), each operand double-buffered by block parity:
+//   K0/K1  khat_m of block iteration it in slot it & 1 (K0: K of the diagonal)
+//   M0/M1  P_m - I (K-major B)              (M0: Y of the diagonal)
+//   V0/V1  V_m, MN-major B                  (V0: V of the diagonal, V1: -Z)
+//   Q      Q of the diagonal
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
 // PATH_ERR_TIMEOUT in the workspace status word, every role stops, pending
 // copies and MMAs are drained (bounded) and TMEM is freed before exit.
@@ -53,20 +55,23 @@ namespace pathattn {
 using namespace sm100;
 
 constexpr int kTcC = 128;
-constexpr int kTcThreads = 352;
-constexpr uint32_t SM_Q = 0, SM_KW = 32768, SM_V = 98304, SM_U = 163840, SM_P = 196608, SM_BAR = 229376;
+constexpr int kTcThreads = 320;
+constexpr uint32_t SM_K0 = 0, SM_K1 = 32768, SM_M0 = 65536, SM_M1 = 98304, SM_V0 = 131072, SM_V1 = 163840,
+                   SM_Q = 196608, SM_BAR = 229376;
 constexpr uint32_t SM_TOTAL = SM_BAR + 256;
 constexpr size_t kTcSmem = SM_TOTAL + 1024;  // + alignment slack
-constexpr uint32_t TM_S = 0, TM_SW = 128, TM_O = 256, TM_Q = 384;
+constexpr uint32_t TM_S = 0, TM_P = 128, TM_QB = 192, TM_O = 256, TM_QM = 384;
 
 // Every barrier below is waited on in a way that it can never run two phases
-// ahead of its waiter (a parity wait cannot tell those apart).
-// Each operand slot (khat, W, -U, V) has its own full/empty pair, released
-// by the MMA that consumes it, so every refill starts as early as possible.
-// W and V are double-buffered by block parity (slot it & 1).
-enum Bar { B_QFULL = 0, B_KFULL, B_WFULL0, B_UFULL, B_VFULL0, B_KEMPTY, B_WEMPTY0, B_UEMPTY, B_VEMPTY0, B_SFULL,
-           B_SWREADY, B_PREADY, B_QUPD, B_QTREADY, B_ODONE, B_DRAIN, B_SREAD, B_VFULL1, B_VEMPTY1, B_WFULL1,
-           B_WEMPTY1, B_SWFULL, B_DRAIN2, B_COUNT };
+// ahead of its waiter (a parity wait cannot tell those apart): each one's next
+// completion needs an action its waiter takes after the current wait.
+enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_MFULL0, B_MFULL1, B_MEMPTY0, B_MEMPTY1,
+           B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1, B_SFULL, B_ODONE, B_QUPD, B_DRAIN, B_COUNT };
+// Named (hardware) barriers between the warps and the MMA warp; id 2 is the
+// softmax warps' own vote barrier.  Counts are threads: the MMA warp syncs,
+// the others arrive.
+constexpr int NB_SK = 3, NB_SK_COUNT = 32 + 128 + 128;  // MMA warp + softmax warps + transport warps
+constexpr int NB_PV = 4, NB_PV_COUNT = 32 + 128;        // MMA warp + softmax warps
 // Barriers at SM_BAR, then the control words (TMEM address, abort flag, FoX
 // stop index and votes, max |khat|^2) at SM_CTL, all inside SM_BAR + 256.
 constexpr uint32_t SM_CTL = SM_BAR + 192;
@@ -74,6 +79,10 @@ static_assert(B_COUNT * 8 <= 192, "barriers overlap the control words");
 static_assert(SM_CTL + 52 <= SM_TOTAL, "control words exceed the barrier region");
 
 constexpr int kHeadGroup = 8;
+
+// Use index of the V slot (it & 1) for block iteration it: slot 1 holds -Z of
+// the diagonal first, so its V_m uses are shifted by one.
+__host__ __device__ constexpr int v_use(int it) { return (it >> 1) + (it & 1); }
 
 // Phase timestamps of one CTA (SM cycle counter), compiled in only for
 // instrumented builds (-DPATH_TRACE): slot s of block iteration it.  CTA 773
@@ -105,6 +114,8 @@ struct TcParams {
     int H;
     int nch;
     int fault;                 // test hook: skip one producer signal
+    int no_skip;               // FoX: visit every block (the far-block stop disabled)
+    unsigned* visited;         // (query tile, key block) pairs visited, summed over tiles
 #ifdef PATH_TRACE
     unsigned long long* trace;
 #endif
@@ -115,28 +126,27 @@ struct TcParams {
 template <int D, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 1)
     path_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
-                const __grid_constant__ CUtensorMap tm_khat, const __grid_constant__ CUtensorMap tm_un,
-                const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_zn,
-                const TcParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_khat,
+                const __grid_constant__ CUtensorMap tm_pm, const __grid_constant__ CUtensorMap tm_y,
+                const __grid_constant__ CUtensorMap tm_zn, const TcParams p) {
     static_assert(D == 64 || D == 128, "head dim");
     constexpr bool FOX = MODE == 1, REL = MODE == 2;
     constexpr bool BIASED = MODE != 0;   // logits carry an additive bias (log2 units in the softmax)
-    constexpr int KCH = D / 64;          // 64-column chunks of the head dim
+    constexpr int KCH = D / 64;          // 64-column boxes of the head dim
     constexpr uint32_t ROWB = 128u * D * 2u;  // bytes of one [128 x D] bf16 tile
-    constexpr uint32_t IDESC_S128 = idesc_bf16(128, false);
-    constexpr uint32_t IDESC_PV = idesc_bf16(D, true);
+    constexpr uint32_t IDESC_S = idesc_bf16(128, false);   // N = 128 keys, B K-major
+    constexpr uint32_t IDESC_T = idesc_bf16(D, false);     // N = d, B K-major (P_m - I)
+    constexpr uint32_t IDESC_PV = idesc_bf16(D, true);     // N = d, B MN-major (V)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     const uint32_t bar0 = sb + SM_BAR;
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    // control words after the barriers (B_COUNT * 8 bytes)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_CTL);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + SM_CTL + 4);
     // PaTH-FoX far-block skipping: the scan stops before block iteration
-    // *stop_it (n + 1 = never); set by the softmax warps before they release S_k.
+    // *stop_it (n + 1 = never); set by the softmax warps before they release S.
     volatile int* stop_it = reinterpret_cast<volatile int*>(sm + SM_CTL + 8);
     int* votes = reinterpret_cast<int*>(sm + SM_CTL + 16);     // [2][4]
     float* s_kmax2 = reinterpret_cast<float*>(sm + SM_CTL + 48);
@@ -160,10 +170,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         uint32_t counts[B_COUNT];
         for (int i = 0; i < B_COUNT; ++i) counts[i] = 1;
-        counts[B_SWREADY] = counts[B_PREADY] = counts[B_QTREADY] = counts[B_SREAD] = 128;
         for (int i = 0; i < B_COUNT; ++i) mbar_init(bar(i), counts[i]);
         *abort_flag = 0;
         *stop_it = n + 1;
+        for (int i = 0; i < 8; ++i) votes[i] = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -179,60 +189,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_w);
-            prefetch_tmap(&tm_khat); prefetch_tmap(&tm_un); prefetch_tmap(&tm_y); prefetch_tmap(&tm_zn);
-            bool ok = true;
-            // diagonal block: Q, K (khat slot), -Z (W slot), Y (-U slot), V
+            prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_khat);
+            prefetch_tmap(&tm_pm); prefetch_tmap(&tm_y); prefetch_tmap(&tm_zn);
+            // diagonal block: Q, K (K slot 0), Y (M slot 0), -Z (V slot 1), V (V slot 0)
             mbar_expect_tx(bar(B_QFULL), ROWB);
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_Q + c * 16384, &tm_q, bar(B_QFULL), c * 64, row0, bh);
-            mbar_expect_tx(bar(B_KFULL), ROWB);
-            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_KW + c * 32768, &tm_k, bar(B_KFULL), c * 64, row0, bh);
-            mbar_expect_tx(bar(B_WFULL0), 32768);
-            for (int c = 0; c < 2; ++c)
-                tma_load_3d(sb + SM_KW + c * 32768 + 16384, &tm_zn, bar(B_WFULL0), c * 64, row0, bh);
-            mbar_expect_tx(bar(B_UFULL), 32768);
-            for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_U + c * 16384, &tm_y, bar(B_UFULL), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_KFULL0), ROWB);
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_K0 + c * 16384, &tm_k, bar(B_KFULL0), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_MFULL0), 32768);
+            for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_M0 + c * 16384, &tm_y, bar(B_MFULL0), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_VFULL1), 32768);
+            for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_V1 + c * 16384, &tm_zn, bar(B_VFULL1), c * 64, row0, bh);
             mbar_expect_tx(bar(B_VFULL0), ROWB);
-            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V + c * 16384, &tm_v, bar(B_VFULL0), c * 64, row0, bh);
-            // scan blocks: refill each slot as soon as its consumer has finished.
-            // khat / -U for block iteration it need the (it)-th completion of
-            // their empty barrier; W and V use slot it & 1 and, from it = 2 on,
-            // the (it >> 1)-th completion of that slot's empty barrier.  W and
-            // -U are not used by the last block (m = 0).
-            enum { SW = 0, SK, SU, SV };
-            // issued: W slot 0, khat, -U, V slot 0, V slot 1, W slot 1
-            int nxt[4] = {1, 1, 1, 1}, issued[6] = {1, 1, 1, 1, 0, 0};
-            const int emp[3] = {B_WEMPTY0, B_KEMPTY, B_UEMPTY};
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V0 + c * 16384, &tm_v, bar(B_VFULL0), c * 64, row0, bh);
+            // Scan blocks, three streams (khat, P - I, V), each block iteration it
+            // into slot it & 1 once that slot's previous contents were consumed
+            // (their empty barrier's matching completion).  P - I is not used by
+            // the last block (m = 0).
+            int nxt[3] = {1, 1, 1};
+            int issued[7] = {1, 1, 0, 1, 0, 1, 1};  // Q, K0, K1, M0, M1, V0, V1 (loads per full barrier)
             const uint64_t t0 = globaltimer();
-            for (uint32_t spin = 0; ok && (nxt[0] <= n || nxt[1] <= n || nxt[2] <= n || nxt[3] <= n); ++spin) {
+            bool ok = true;
+            for (uint32_t spin = 0; ok; ++spin) {
                 const int stop = FOX ? *stop_it : n + 1;
-                for (int sl = 0; sl < 4; ++sl) {
+                const int lim[3] = {min(n, stop - 1), min(n - 1, stop - 1), min(n, stop - 1)};
+                if (nxt[0] > lim[0] && nxt[1] > lim[1] && nxt[2] > lim[2]) break;
+                for (int sl = 0; sl < 3; ++sl) {
                     const int it = nxt[sl];
-                    if (it > n) continue;
-                    if (it >= stop) { nxt[sl] = n + 1; continue; }  // beyond the last block the scan visits
-                    if ((sl == SW || sl == SU) && it == n) { nxt[sl] = n + 1; continue; }
-                    if (sl == SV || sl == SW) {
-                        const int eb = sl == SV ? ((it & 1) ? B_VEMPTY1 : B_VEMPTY0) : ((it & 1) ? B_WEMPTY1 : B_WEMPTY0);
-                        if (it >= 2 && !mbar_test_wait(bar(eb), (uint32_t)(((it >> 1) - 1) & 1))) continue;
-                    } else if (!mbar_test_wait(bar(emp[sl]), (it - 1) & 1)) {
-                        continue;
-                    }
-                    const int r = (n - it) * kTcC;
+                    if (it > lim[sl]) continue;
+                    const int s = it & 1;
+                    const int u = sl == 2 ? v_use(it) : (it >> 1);
+                    const int eb = sl == 0 ? B_KEMPTY0 : sl == 1 ? B_MEMPTY0 : B_VEMPTY0;
+                    if (u >= 1 && !mbar_test_wait(bar(eb + s), (uint32_t)((u - 1) & 1))) continue;
                     nxt[sl] = it + 1;
-                    if (sl == SV && p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
-                    const int fb = sl == SW ? ((it & 1) ? B_WFULL1 : B_WFULL0)
-                                   : sl == SK ? B_KFULL : sl == SU ? B_UFULL : ((it & 1) ? B_VFULL1 : B_VFULL0);
+                    if (sl == 2 && p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
+                    const int fb = (sl == 0 ? B_KFULL0 : sl == 1 ? B_MFULL0 : B_VFULL0) + s;
+                    const uint32_t dst = sb + (sl == 0 ? SM_K0 : sl == 1 ? SM_M0 : SM_V0) + (uint32_t)s * 32768u;
+                    const CUtensorMap* map = sl == 0 ? &tm_khat : sl == 1 ? &tm_pm : &tm_v;
+                    const int r = (n - it) * kTcC;
                     mbar_expect_tx(bar(fb), ROWB);
-                    for (int c = 0; c < KCH; ++c) {
-                        if (sl == SK) tma_load_3d(sb + SM_KW + c * 32768, &tm_khat, bar(fb), c * 64, r, bh);
-                        if (sl == SW) {
-                            const uint32_t dst = (it & 1) ? sb + SM_P + c * 16384 : sb + SM_KW + c * 32768 + 16384;
-                            tma_load_3d(dst, &tm_w, bar(fb), c * 64, r, bh);
-                        }
-                        if (sl == SU) tma_load_3d(sb + SM_U + c * 16384, &tm_un, bar(fb), c * 64, r, bh);
-                        if (sl == SV) tma_load_3d(sb + SM_V + (it & 1) * 32768 + c * 16384, &tm_v, bar(fb), c * 64, r, bh);
-                    }
-                    ++issued[sl == SV ? 3 + (it & 1) : (sl == SW && (it & 1)) ? 5 : sl];
+                    for (int c = 0; c < KCH; ++c) tma_load_3d(dst + c * 16384, map, bar(fb), c * 64, r, bh);
+                    ++issued[1 + 2 * sl + s];
                     TC_TRACE(12 + sl, it);
                 }
                 if ((spin & 255u) == 255u) {
@@ -245,145 +242,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             // copies still in flight must land before the CTA exits
-            drain_wait(bar(B_QFULL), 0, p.limit_ns, p.hdr, 90);
-            const int ful[6] = {B_WFULL0, B_KFULL, B_UFULL, B_VFULL0, B_VFULL1, B_WFULL1};
-            for (int sl = 0; sl < 6; ++sl)
-                if (issued[sl] > 0) drain_wait(bar(ful[sl]), (uint32_t)((issued[sl] - 1) & 1), p.limit_ns, p.hdr, 91);
+            const int ful[7] = {B_QFULL, B_KFULL0, B_KFULL1, B_MFULL0, B_MFULL1, B_VFULL0, B_VFULL1};
+            for (int i = 0; i < 7; ++i)
+                if (issued[i] > 0) drain_wait(bar(ful[i]), (uint32_t)((issued[i] - 1) & 1), p.limit_ns, p.hdr, 91);
         }
-    } else if (warp == 1 || warp == 10) {
-        // ------------------------------------------------------------------ MMA issuers
-        // Issue is blocking (an MMA group's issue returns about when it has
-        // executed), and every barrier poll costs a few hundred cycles while SS
-        // MMAs hold the shared-memory port.  Without FoX two threads issue:
-        //   warp 1  (transport chain)  S_w(it), MMA3(it)             it = 1 .. n-1
-        //   warp 10 (softmax chain)    diagonal, P V(it-1), S_k(it)   it = 1 .. n
-        // so that one thread's waits overlap the other's MMAs.  Their TMEM
-        // columns are disjoint (S_w / q~ against S_k, P / O); the transport
-        // warps wait for S_k(it) as well as MMA3(it) before they overwrite the
-        // shared q~ tile.  With FoX (far-block stopping) warp 1 issues all of
-        // it in the order S_w(it), P V(it-1), S_k(it), MMA3(it).
-        const bool issuer_b = FOX ? warp == 1 : warp == 10;  // diagonal, P V, S_k
-        const bool issuer_a = warp == 1;                      // S_w, MMA3
-        if (lane == 0 && (issuer_a || issuer_b)) {
-            auto issue_pv = [&](int blk) {  // O (+)= P V for block iteration blk (P in TMEM)
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        // Issue blocks for about as long as a group executes and the tensor pipe
+        // queues little, so every pause between groups is a bubble.  This warp
+        // therefore waits on nothing but two named barriers per block (no
+        // shared-memory round trip): the warps that signal it have already
+        // waited for the copies the next MMAs read.
+        //   NB_SK(it)   T(it) and S_k(it) may go: bf16 q~(it) is in TMEM, khat_m and
+        //               P_m - I have landed (transport warps), S(it-1) has been read
+        //               and, with FoX, block it is known to be visited (softmax warps)
+        //   NB_PV(it)   P V(it) may go: P(it) is in TMEM and V_m has landed (softmax)
+        // T(it) goes first: the transport warps convert q~(it+1) while S_k(it) and
+        // P V(it-1) execute.  Lane 0 issues; the whole warp takes the barriers.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL0), 0, wc, 11) &&
+                                              mbar_wait(bar(B_MFULL0), 0, wc, 12) && mbar_wait(bar(B_VFULL1), 0, wc, 12));
+        if (ok && lane == 0) {
+            tc_fence_after();
+            // diagonal: S = Q K^T + Y (-Z)^T
+            for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_K0, kk, 16384), IDESC_S,
+                       kk > 0);
+            for (int kk = 0; kk < kTcC / 16; ++kk)
+                mma_ss(tmem + TM_S, kmajor_desc(sb + SM_M0, kk, 16384), kmajor_desc(sb + SM_V1, kk, 16384), IDESC_S, 1);
+            mma_commit(bar(B_SFULL));
+            mma_commit(bar(B_KEMPTY0));
+            mma_commit(bar(B_MEMPTY0));
+            mma_commit(bar(B_VEMPTY1));
+            TC_TRACE(0, 0);
+        }
+        __syncwarp();
+        auto issue_pv = [&](int blk) {  // O (+)= P V for block iteration blk (P in TMEM)
+            named_bar_sync(NB_PV, NB_PV_COUNT);
+            if (lane == 0) {
+                TC_TRACE(18, blk);
                 tc_fence_after();
-                const uint32_t vbuf = sb + SM_V + (uint32_t)(blk & 1) * 32768u;
+                const int s = blk & 1;
+                const uint32_t vbuf = sb + SM_V0 + (uint32_t)s * 32768u;
                 for (int kk = 0; kk < kTcC / 16; ++kk)
-                    mma_ts(tmem + TM_O, tmem + TM_S + kk * 8, mnmajor_desc(vbuf, kk), IDESC_PV,
+                    mma_ts(tmem + TM_O, tmem + TM_P + kk * 8, mnmajor_desc(vbuf, kk), IDESC_PV,
                            (blk > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(bar(B_ODONE));
-                mma_commit(bar((blk & 1) ? B_VEMPTY1 : B_VEMPTY0));
-            };
-            // P V of block blk needs its P (p_ready, (blk+1)-th completion) and
-            // its V slot (blk & 1, (blk >> 1)+1-th completion).  Without FoX the
-            // warps that arrive on P-ready, q~-ready and S_w-ready first wait for
-            // the V, khat / W and -U copies of that block, so the issuers only
-            // wait for the handoffs.
-            auto wait_pv = [&](int blk) {
-                return mbar_wait(bar(B_PREADY), (uint32_t)(blk & 1), wc, 18) &&
-                       (!FOX || mbar_wait(bar((blk & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((blk >> 1) & 1), wc, 19));
-            };
-            auto issue_sw = [&](int it) {  // S_w = q~ W^T (W slot it & 1)
-                tc_fence_after();
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t bdesc = (it & 1) ? kmajor_desc(sb + SM_P, kk, 16384)
-                                                    : kmajor_desc(sb + SM_KW + 16384, kk, 32768);
-                    mma_ss(tmem + TM_SW, kmajor_desc(sb + SM_Q, kk, 16384), bdesc, IDESC_S128, kk > 0);
+                mma_commit(bar(B_VEMPTY0 + s));
+                TC_TRACE(2, blk);
+            }
+            __syncwarp();
+        };
+        int last = n;  // last block iteration whose P V is issued
+        // The rounds of both named barriers run whatever happens: a warp that
+        // gives up (a bounded wait expired) still arrives on every remaining
+        // round, so this warp never blocks for good; MMAs issued after such a
+        // failure read stale but valid addresses and their results are unused.
+        if (ok) {
+            for (int it = 1; it <= n; ++it) {
+                const int m = n - it, s = it & 1;
+                named_bar_sync(NB_SK, NB_SK_COUNT);
+                if (FOX && *stop_it <= it) {  // every block from here on contributes exactly zero
+                    last = it - 1;
+                    break;
                 }
-                mma_commit(bar(B_SWFULL));
-                mma_commit(bar((it & 1) ? B_WEMPTY1 : B_WEMPTY0));
-                TC_TRACE(0, it);
-            };
-            auto issue_sk = [&](int it) {  // S_k = q~ khat^T
-                tc_fence_after();
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
-                           IDESC_S128, kk > 0);
-                mma_commit(bar(B_SFULL));
-                mma_commit(bar(B_KEMPTY));
-                TC_TRACE(1, it);
-            };
-            auto issue_m3 = [&](int it) {  // q~ += bf16(S_w) (-U)
-                tc_fence_after();
-                for (int kk = 0; kk < kTcC / 16; ++kk)
-                    mma_ts(tmem + TM_Q, tmem + TM_SW + kk * 8, mnmajor_desc(sb + SM_U, kk), IDESC_PV, 1);
-                mma_commit(bar(B_QUPD));
-                mma_commit(bar(B_UEMPTY));
-                TC_TRACE(3, it);
-            };
-            bool ok = true;
-            if (issuer_b) {
-                ok = mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL), 0, wc, 11) &&
-                     mbar_wait(bar(B_WFULL0), 0, wc, 12) && mbar_wait(bar(B_UFULL), 0, wc, 12);
-                if (ok) {
+                if (lane == 0) {
+                    TC_TRACE(15, it);
                     tc_fence_after();
-                    // diagonal: S = Q K^T + Y (-Z)^T
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KW, kk, 32768),
-                               IDESC_S128, kk > 0);
-                    for (int kk = 0; kk < kTcC / 16; ++kk)
-                        mma_ss(tmem + TM_S, kmajor_desc(sb + SM_U, kk, 16384),
-                               kmajor_desc(sb + SM_KW + 16384, kk, 32768), IDESC_S128, 1);
+                    if (m > 0) {  // q~ += bf16(q~) (P_m - I)^T
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ts(tmem + TM_QM, tmem + TM_QB + kk * 8,
+                                   kmajor_desc(sb + SM_M0 + s * 32768u, kk, 16384), IDESC_T, 1);
+                        mma_commit(bar(B_QUPD));
+                        mma_commit(bar(B_MEMPTY0 + s));
+                        TC_TRACE(3, it);
+                    }
+                    for (int kk = 0; kk < D / 16; ++kk)  // S = q~ khat^T
+                        mma_ts(tmem + TM_S, tmem + TM_QB + kk * 8, kmajor_desc(sb + SM_K0 + s * 32768u, kk, 16384),
+                               IDESC_S, kk > 0);
                     mma_commit(bar(B_SFULL));
-                    mma_commit(bar(B_KEMPTY));
-                    mma_commit(bar(B_WEMPTY0));
-                    mma_commit(bar(B_UEMPTY));
+                    mma_commit(bar(B_KEMPTY0 + s));
+                    TC_TRACE(1, it);
                 }
+                __syncwarp();
+                issue_pv(it - 1);
             }
-            if (FOX) {
-                // single issuer: S_w(it) -> P V(it-1) -> S_k(it) -> MMA3(it); P V and S_k
-                // cover the conversion of S_w, and S_k follows P V because it
-                // overwrites the TMEM columns that hold P.
-                int last = n;  // last block iteration whose P V is issued
-                for (int it = 1; it <= n && ok; ++it) {
-                    const int m = n - it;
-                    // the softmax warps decide first whether block it is visited
-                    if (!(ok = mbar_wait(bar(B_SREAD), (it - 1) & 1, wc, 15))) break;
-                    if (*stop_it <= it) {  // every block from here on contributes exactly zero
-                        last = it - 1;
-                        break;
-                    }
-                    if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
-                    if (m > 0) {
-                        if (!(ok = mbar_wait(bar((it & 1) ? B_WFULL1 : B_WFULL0), (uint32_t)((it >> 1) & 1), wc, 15)))
-                            break;
-                        issue_sw(it);
-                    }
-                    if (!(ok = wait_pv(it - 1))) break;
-                    issue_pv(it - 1);
-                    TC_TRACE(2, it);
-                    if (!(ok = mbar_wait(bar(B_KFULL), it & 1, wc, 15))) break;
-                    issue_sk(it);
-                    if (m > 0) {
-                        if (!(ok = mbar_wait(bar(B_UFULL), it & 1, wc, 16))) break;
-                        if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
-                        issue_m3(it);
-                    }
-                }
-                if (ok && wait_pv(last)) issue_pv(last);  // the last block's P V
-            } else if (issuer_b) {
-                for (int it = 1; it <= n && ok; ++it) {
-                    if (!(ok = wait_pv(it - 1))) break;
-                    TC_TRACE(20, it);
-                    issue_pv(it - 1);
-                    TC_TRACE(2, it);
-                    issue_sk(it);  // its khat and q~ were awaited before P-ready (softmax warps 3, 4)
-                }
-                if (ok && wait_pv(n)) issue_pv(n);  // the last block's P V
-            } else {
-                for (int it = 1; it < n && ok; ++it) {
-                    if (!(ok = mbar_wait(bar(B_QTREADY), (it - 1) & 1, wc, 14))) break;
-                    issue_sw(it);
-                    if (!(ok = mbar_wait(bar(B_SWREADY), (it - 1) & 1, wc, 17))) break;
-                    TC_TRACE(23, it);
-                    issue_m3(it);
-                }
-            }
-            // every MMA this thread issued completes before TMEM is released
-            const int drain = (FOX || issuer_a) ? B_DRAIN : B_DRAIN2;
-            mma_commit(bar(drain));
-            drain_wait(bar(drain), 0, p.limit_ns, p.hdr, 92);
+            issue_pv(last);  // the last block's P V
         }
+        // every MMA this warp issued completes before TMEM is released
+        if (lane == 0) {
+            mma_commit(bar(B_DRAIN));
+            drain_wait(bar(B_DRAIN), 0, p.limit_ns, p.hdr, 92);
+        }
+        __syncwarp();
     } else if (warp < 6) {
         // ------------------------------------------------------------------ softmax warps
         const int r = 32 * (warp & 3) + lane;  // query row within the tile (= TMEM lane)
@@ -395,6 +345,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float m_run = -INFINITY, l_run = 0.f;
         float m_true = -INFINITY;  // largest logit seen (log2 units)
         float qk_bound = 0.f;      // FoX: scale log2e |q_i| max_j |khat_j|, with a 2x margin
+        int sk_sent = 0, pv_sent = 0;  // named-barrier rounds this warp has arrived on (NB_SK from 1, NB_PV from 0)
         if (FOX && n > 0) {
             if (warp == 2) {  // max |khat|^2 over the chunks left of this tile
                 float x = 0.f;
@@ -428,23 +379,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (r == 0) TC_TRACE(4, it);
             tc_fence_after();
             float s[128];
+            {
+                uint32_t raw[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(tl + TM_S + 32 * c, raw);
+                for (int c = 0; c < 4; ++c) tmem_ld32(tl + TM_S + 32 * c, raw[c]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[j]);
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[c][j]);
             }
             // Without a bias the scores stay raw (the scale is applied inside the
             // exponent, one FFMA each); with one (FoX, relative) they become
             // log2-unit logits.
             const float sl2 = p.sl2;
-            // S_k is in registers: the next block's S_k may overwrite it (FoX
-            // first decides whether there is a next block)
-            if (!FOX) {
+            // S is in registers: the next block's S_k may overwrite it (FoX first
+            // decides whether there is a next block)
+            if (!FOX && it < n) {
                 tc_fence_before();
-                mbar_arrive(bar(B_SREAD));
+                named_bar_arrive(NB_SK, NB_SK_COUNT);
+                sk_sent = it + 1;
             }
             if (r == 0) TC_TRACE(5, it);
             if (FOX) {
@@ -490,20 +444,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool stop = false;
             if (FOX) {
                 m_true = fmaxf(m_true, mx);
-                if (m > 0) {
+                if (m > 0 && !p.no_skip) {
                     // Every key left of this block has bias <= c_i - c_(128 m - 1) and
                     // |logit| <= qk_bound: below m_true - 160 (log2) its exp2 is 0 in fp32.
                     const float bound = qk_bound + (ci - cumh[m * kTcC - 1]) * kL2e - m_true;
                     const bool sat = (row0 + r >= p.L) || bound < -160.0f;
                     const int vote = __all_sync(0xffffffffu, sat);
-                    if (lane == 0) votes[(it & 1) * 4 + (warp & 3)] = vote;
-                    named_bar_sync(2, 128);
-                    const int* vv = votes + (it & 1) * 4;
-                    stop = vv[0] && vv[1] && vv[2] && vv[3];
+                    // Votes carry the iteration (2 (it + 1) + vote), double-buffered by
+                    // it & 1: no warp can post iteration it + 2 before every warp has
+                    // read iteration it.  The poll is bounded (a warp that gave up on a
+                    // wait raises the abort flag instead of voting).
+                    volatile int* vv = votes + (it & 1) * 4;
+                    if (lane == 0) vv[warp & 3] = 2 * (it + 1) + vote;
+                    __syncwarp();
+                    int all = 1;
+                    const uint64_t tv = globaltimer();
+                    for (int w4 = 0; w4 < 4 && ok; ++w4) {
+                        int x;
+                        for (uint32_t spin = 0; ((x = vv[w4]) >> 1) != it + 1; ++spin)
+                            if ((spin & 255u) == 255u && (*abort_flag || globaltimer() - tv > p.limit_ns)) {
+                                if (!*abort_flag) { report_status(p.hdr, PATH_ERR_TIMEOUT, 23); *abort_flag = 1; }
+                                ok = false;
+                                break;
+                            }
+                        all &= x & 1;
+                    }
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    stop = all != 0;
                     if (stop && warp == 2 && lane == 0) *stop_it = it + 1;
                 }
-                tc_fence_before();
-                mbar_arrive(bar(B_SREAD));
+                if (it < n) {
+                    tc_fence_before();
+                    named_bar_arrive(NB_SK, NB_SK_COUNT);  // with the decision on block it + 1
+                    sk_sent = it + 1;
+                }
             }
             const float m_new = fmaxf(m_run, mx);
             const bool rescale = m_new > m_run + 8.0f;
@@ -524,53 +499,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float sum = ((psum[0] + psum[1]) + (psum[2] + psum[3])) + ((psum[4] + psum[5]) + (psum[6] + psum[7]));
             l_run = l_run * alpha + sum;
             if (r == 0) TC_TRACE(6, it);
-            // The O rescale uses warp-collective TMEM loads/stores, so the whole
-            // warp takes it when any of its rows needs it (alpha = 1 elsewhere).
-            if (__any_sync(0xffffffffu, rescale && it > 0)) {
-                // O is stable once the previous block's P V has completed
-                const bool ok2 = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (it - 1) & 1, wc, 21));
-                if (!ok2) { ok = false; break; }
+            // P and O are single-buffered: the previous block's P V must have completed
+            // before P is rewritten and O rescaled.  The rescale uses warp-collective
+            // TMEM loads/stores, so the whole warp takes it when any of its rows needs
+            // it (alpha = 1 elsewhere).
+            if (it > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (uint32_t)((it - 1) & 1), wc, 21));
+                if (!ok) break;
+                if (r == 0) TC_TRACE(11, it);
                 tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    tmem_ld32(tl + TM_O + 32 * c, ov);
-                    tmem_wait_ld();
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tl + TM_O + 32 * c, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-                    tmem_st32(tl + TM_O + 32 * c, ov);
+                        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+                        tmem_st32(tl + TM_O + 32 * c, ov);
+                    }
                 }
             }
             m_run = m_use;
-            // P (bf16 pairs) over S_k's first 64 columns: the A operand of P V.  The
-            // next S_k is issued after this P V, so it cannot overwrite P early.
-            tmem_st32(tl + TM_S, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-            tmem_st32(tl + TM_S + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+            tmem_st32(tl + TM_P, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+            tmem_st32(tl + TM_P + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
-            // Without FoX, P-ready also stands for the inputs of the issuer's next two
-            // MMAs: warp 2 waits for this block's V (P V), warp 3 for the next
-            // block's khat and warp 4 for the next q~ (S_k of block it + 1), each in
-            // parallel, so the issuer polls P-ready alone.
-            if (!FOX && warp == 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar((it & 1) ? B_VFULL1 : B_VFULL0), (uint32_t)((it >> 1) & 1), wc, 24));
-                if (!ok) break;
-            }
-            if (!FOX && warp == 3 && it < n) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_KFULL), (it + 1) & 1, wc, 25));
-                if (!ok) break;
-            }
-            if (!FOX && warp == 4 && it < n) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QTREADY), it & 1, wc, 26));
-                if (!ok) break;
-            }
+            // V_m of this block has landed before P V may go
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_VFULL0 + (it & 1)), (uint32_t)(v_use(it) & 1), wc, 24));
+            if (!ok) break;
             tc_fence_before();
-            mbar_arrive(bar(B_PREADY));
+            named_bar_arrive(NB_PV, NB_PV_COUNT);
+            pv_sent = it + 1;
             if (r == 0) TC_TRACE(7, it);
-            if (lane == 0) TC_TRACE(14 + warp, it);  // 16..19: P-ready arrival of warps 2..5
+            if (lane == 0) TC_TRACE(20 + (warp & 3), it);  // 20..23: P-ready arrival per softmax warp
             if (stop) {
                 last = it;
                 break;
             }
+        }
+        if (!ok) {  // give the MMA warp every round it may still wait for
+            for (int rr = sk_sent + 1; rr <= n; ++rr) named_bar_arrive(NB_SK, NB_SK_COUNT);
+            for (int rr = pv_sent; rr <= n; ++rr) named_bar_arrive(NB_PV, NB_PV_COUNT);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (uint32_t)(last & 1), wc, 22));
         if (ok) {
@@ -596,139 +565,98 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             if (p.lse && row < p.L) p.lse[(size_t)bh * p.L + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+            if (r == 0) atomicAdd(p.visited, (unsigned)(last + 1));
         }
     } else {
         // ------------------------------------------------------------------ query-transport warps
         const int r = 32 * (warp & 3) + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        uint8_t* qrow_s = sm + SM_Q + r * 128;  // this row's 128-byte line in chunk 0
-        const int sw = r & 7;
-        // bf16 q~ row -> swizzled K-major tile (16-byte granule g of chunk c at (g ^ (r & 7)))
-        auto put_granule = [&](int G, uint4 v) {
-            *reinterpret_cast<uint4*>(qrow_s + (G >> 3) * 16384 + (((G & 7) ^ sw) << 4)) = v;
-        };
-        // Without FoX, warp 6 waits for the W copy of block blk before q~-ready
-        // (S_w is the first MMA that reads q~), and for -U before S_w-ready.
-        auto loads_for_q = [&](int blk) -> bool {
-            if (FOX || warp != 6 || n - blk == 0) return true;
-            return __all_sync(0xffffffffu, mbar_wait(bar((blk & 1) ? B_WFULL1 : B_WFULL0),
-                                                     (uint32_t)((blk >> 1) & 1), wc, 35));
-        };
-        // This row of qhat (fp32), the initial q~: every load is issued before
-        // the wait for the diagonal, so their latency hides behind it (issued
-        // chunk by chunk between the TMEM stores, the loads were serialised).
-        float4 qh[D / 4];
-        if (n > 0) {
-            const float4* src = reinterpret_cast<const float4*>(p.qhat + ((size_t)bh * p.Lp + row0 + r) * D);
+        int sk_sent = 0;  // NB_SK rounds this warp has arrived on
+        // bf16 copy of 32 fp32 columns (raw bits) -> 16 packed columns of TMEM
+        auto put_bf16 = [&](int c, const uint32_t (&v)[32]) {
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < D / 4; ++i) qh[i] = __ldg(src + i);
-        }
-        bool ok = n > 0 && __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), 0, wc, 30));
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+            tmem_st16(tl + TM_QB + 16 * c, pk);
+        };
+        // Wait for barrier `b` (parity `par`) unless the FoX scan has stopped before
+        // block iteration `it`: 1 ready, 2 stopped, 3 failed.
+        auto wait_or_stop = [&](int b, uint32_t par, int it, int site) -> int {
+            if (!FOX) return __all_sync(0xffffffffu, mbar_wait(bar(b), par, wc, site)) ? 1 : 3;
+            int st = 0;
+            const uint64_t t0 = globaltimer();
+            for (uint32_t spin = 0; st == 0; ++spin) {
+                if (mbar_test_wait(bar(b), par)) st = 1;
+                else if (*stop_it <= it) st = 2;
+                else if ((spin & 255u) == 255u && (*abort_flag || globaltimer() - t0 > p.limit_ns)) {
+                    if (!*abort_flag) { report_status(p.hdr, PATH_ERR_TIMEOUT, site); *abort_flag = 1; }
+                    st = 3;
+                }
+            }
+            return (int)__reduce_max_sync(0xffffffffu, (unsigned)st);
+        };
+        // The copies block iteration it reads (khat, and P - I unless m = 0) have
+        // landed, then NB_SK(it) may complete.  A FoX scan that stops before block
+        // it still syncs NB_SK(it) (that is where the MMA warp learns of the stop),
+        // so the round is arrived on then too, without waiting for copies the
+        // producer may never issue.
+        auto release_block = [&](int it) -> int {
+            int st = wait_or_stop(B_KFULL0 + (it & 1), (uint32_t)((it >> 1) & 1), it, 34);
+            if (st == 1 && n - it > 0) st = wait_or_stop(B_MFULL0 + (it & 1), (uint32_t)((it >> 1) & 1), it, 35);
+            if (st == 1 || st == 2) {
+                tc_fence_before();
+                named_bar_arrive(NB_SK, NB_SK_COUNT);
+                sk_sent = it;
+            }
+            return st;
+        };
+        bool ok = n > 0;
+        int st = 1;
         if (ok) {
-            // the diagonal MMA has consumed Q: qhat becomes the fp32 master and its bf16 copy
-            tc_fence_after();
+            // qhat (fp32) of this row becomes the q~ master and its bf16 copy
+            const float4* src = reinterpret_cast<const float4*>(p.qhat + ((size_t)bh * p.Lp + row0 + r) * D);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 x = qh[8 * c + j4];
+                    const float4 x = __ldg(src + 8 * c + j4);
                     v[4 * j4 + 0] = __float_as_uint(x.x);
                     v[4 * j4 + 1] = __float_as_uint(x.y);
                     v[4 * j4 + 2] = __float_as_uint(x.z);
                     v[4 * j4 + 3] = __float_as_uint(x.w);
                 }
-                tmem_st32(tl + TM_Q + 32 * c, v);
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    uint4 q;
-                    q.x = pack_bf16x2(__uint_as_float(v[8 * g + 0]), __uint_as_float(v[8 * g + 1]));
-                    q.y = pack_bf16x2(__uint_as_float(v[8 * g + 2]), __uint_as_float(v[8 * g + 3]));
-                    q.z = pack_bf16x2(__uint_as_float(v[8 * g + 4]), __uint_as_float(v[8 * g + 5]));
-                    q.w = pack_bf16x2(__uint_as_float(v[8 * g + 6]), __uint_as_float(v[8 * g + 7]));
-                    put_granule(4 * c + g, q);
-                }
+                tmem_st32(tl + TM_QM + 32 * c, v);
+                put_bf16(c, v);
             }
             tmem_wait_st();
-            fence_proxy_async_smem();
-            ok = loads_for_q(1);
-            tc_fence_before();
-            if (ok) mbar_arrive(bar(B_QTREADY));
+            st = release_block(1);
+            ok = st == 1;
         }
-        for (int it = 1; it < n && ok; ++it) {  // block m = n - it > 0 needs the transport
-            if (FOX) {  // S_w of block iteration it, unless the scan stopped before it
-                int st = 0;  // 0 waiting, 1 ready, 2 stopped, 3 failed
-                const uint64_t t0 = globaltimer();
-                for (uint32_t spin = 0; st == 0; ++spin) {
-                    if (mbar_test_wait(bar(B_SWFULL), (it - 1) & 1)) st = 1;
-                    else if (*stop_it <= it) st = 2;
-                    else if ((spin & 255u) == 255u && (*abort_flag || globaltimer() - t0 > p.limit_ns)) {
-                        if (!*abort_flag) { report_status(p.hdr, PATH_ERR_TIMEOUT, 33); *abort_flag = 1; }
-                        st = 3;
-                    }
-                }
-                st = __reduce_max_sync(0xffffffffu, (unsigned)st);
-                if (st == 2) break;
-                ok = st == 1;
-            } else {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SWFULL), (it - 1) & 1, wc, 31));
-            }
-            if (!ok) break;
+        for (int it = 1; it < n && ok; ++it) {  // q~ for block iteration it + 1 (m = n - it > 0)
+            st = wait_or_stop(B_QUPD, (uint32_t)((it - 1) & 1), it, 31);  // T(it) has completed
+            if (st != 1) break;
             if (r == 0) TC_TRACE(8, it);
             tc_fence_after();
-            // S_w (fp32, columns [128,256)) -> bf16 pairs in columns [128,192)
-            {
-                uint32_t v[4][32];
+            uint32_t v[D / 32][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tl + TM_SW + 32 * c, v[c]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]), __uint_as_float(v[c][2 * j + 1]));
-                    tmem_st16(tl + TM_SW + 16 * c, pk);
-                }
-            }
-            tmem_wait_st();
-            if (!FOX && warp == 6 && !(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_UFULL), it & 1, wc, 36)))) break;
-            tc_fence_before();
-            mbar_arrive(bar(B_SWREADY));
-            if (lane == 0) TC_TRACE(22 + warp, it);  // 28..31: S_w-ready arrival of warps 6..9
-            if (r == 0) TC_TRACE(9, it);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QUPD), (it - 1) & 1, wc, 32));
-            // with two issuers S_k(it), which also reads the q~ tile, completes on its own
-            if (!FOX && ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 37));
-            if (!ok) break;
-            if (r == 0) TC_TRACE(10, it);
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + TM_QM + 32 * c, v[c]);
+            tmem_wait_ld();
+            // S_k(it), issued after T(it), still reads bf16 q~(it)
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 32)))) break;
             tc_fence_after();
-            {
-                uint32_t v[D / 32][32];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + TM_Q + 32 * c, v[c]);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        uint4 q;
-                        q.x = pack_bf16x2(__uint_as_float(v[c][8 * g + 0]), __uint_as_float(v[c][8 * g + 1]));
-                        q.y = pack_bf16x2(__uint_as_float(v[c][8 * g + 2]), __uint_as_float(v[c][8 * g + 3]));
-                        q.z = pack_bf16x2(__uint_as_float(v[c][8 * g + 4]), __uint_as_float(v[c][8 * g + 5]));
-                        q.w = pack_bf16x2(__uint_as_float(v[c][8 * g + 6]), __uint_as_float(v[c][8 * g + 7]));
-                        put_granule(4 * c + g, q);
-                    }
-            }
-            fence_proxy_async_smem();
-            if (!(ok = loads_for_q(it + 1))) break;
-            tc_fence_before();
-            mbar_arrive(bar(B_QTREADY));
-            if (r == 64) TC_TRACE(11, it);
-            if (lane == 0) TC_TRACE(18 + warp, it);  // 24..27: q~-ready arrival of warps 6..9
+            for (int c = 0; c < D / 32; ++c) put_bf16(c, v[c]);
+            tmem_wait_st();
+            st = release_block(it + 1);
+            if (st != 1) break;
+            if (r == 0) TC_TRACE(9, it);
+        }
+        if (st == 3) ok = false;
+        if (!ok && n > 0) {  // give the MMA warp every round it may still wait for
+            for (int rr = sk_sent + 1; rr <= n; ++rr) named_bar_arrive(NB_SK, NB_SK_COUNT);
         }
     }
-
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -757,14 +685,13 @@ namespace pathattn {
 #endif
 
 template <int D>
-static cudaError_t launch_tc(const void* q, const void* k, const void* v, const void* w, const float* log_f,
-                            const float* rel_bias, int H, void* o, float* lse, int BH, int L, float scale,
-                            unsigned char* ws, const FwdLayout& lay, int fault, cudaStream_t st) {
-    CUtensorMap mq, mk, mv, mw, mkh, mun, my, mzn;
+static cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* log_f, const float* rel_bias,
+                             int H, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
+                             const FwdLayout& lay, int fault, const FwdOptions& opt, cudaStream_t st) {
+    CUtensorMap mq, mk, mv, mkh, mpm, my, mzn;
     if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mv, v, D, L, BH) ||
-        !make_map(&mw, w, D, L, BH) || !make_map(&mkh, ws + lay.khat, D, lay.Lp, BH) ||
-        !make_map(&mun, ws + lay.un, D, lay.Lp, BH) || !make_map(&my, ws + lay.y, kTcC, lay.Lp, BH) ||
-        !make_map(&mzn, ws + lay.zn, kTcC, lay.Lp, BH))
+        !make_map(&mkh, ws + lay.khat, D, lay.Lp, BH) || !make_map(&mpm, ws + lay.un, D, lay.Lp, BH) ||
+        !make_map(&my, ws + lay.y, kTcC, lay.Lp, BH) || !make_map(&mzn, ws + lay.zn, kTcC, lay.Lp, BH))
         return cudaErrorInvalidValue;
     TcParams p;
     p.L = L;
@@ -784,6 +711,8 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     p.nch = lay.Lp / kTcC;
     p.rbias = rel_bias;
     p.H = H;
+    p.no_skip = opt.no_skip;
+    p.visited = &p.hdr->visited;
 #ifdef PATH_TRACE
     p.trace = trace_buffer();
 #endif
@@ -791,18 +720,19 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     mark_start(st);
-    kern<<<dim3(BH * p.ntiles), kTcThreads, kTcSmem, st>>>(mq, mk, mv, mw, mkh, mun, my, mzn, p);
+    kern<<<dim3(BH * p.ntiles), kTcThreads, kTcSmem, st>>>(mq, mk, mv, mkh, mpm, my, mzn, p);
     mark_end(st);
     return cudaGetLastError();
 }
 
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
                         const float* log_f, const float* rel_bias, int H, void* o, float* lse, int BH, int L, int d,
-                        float scale, unsigned char* ws, const FwdLayout& lay, int fault_mask, cudaStream_t st) {
+                        float scale, unsigned char* ws, const FwdLayout& lay, int fault_mask, const FwdOptions& opt,
+                        cudaStream_t st) {
     cudaError_t e = launch_ut_prep(PATH_BF16, kTcC, d, q, k, w, beta, log_f, BH, L, ws, lay, st);
     if (e != cudaSuccess) return e;
-    if (d == 64) return launch_tc<64>(q, k, v, w, log_f, rel_bias, H, o, lse, BH, L, scale, ws, lay, fault_mask, st);
-    if (d == 128) return launch_tc<128>(q, k, v, w, log_f, rel_bias, H, o, lse, BH, L, scale, ws, lay, fault_mask, st);
+    if (d == 64) return launch_tc<64>(q, k, v, log_f, rel_bias, H, o, lse, BH, L, scale, ws, lay, fault_mask, opt, st);
+    if (d == 128) return launch_tc<128>(q, k, v, log_f, rel_bias, H, o, lse, BH, L, scale, ws, lay, fault_mask, opt, st);
     return cudaErrorInvalidValue;
 }
 

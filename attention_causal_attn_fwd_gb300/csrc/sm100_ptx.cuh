@@ -195,6 +195,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_ab(int N, bool a_mn_major, boo
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive on a named barrier without waiting (producer side of a bar.sync).
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // K-major, 128-byte-swizzled operand: 64-column chunks `chunk_stride` apart,
 // k-step kk (16 columns) inside a chunk is a 32-byte offset.

@@ -2,20 +2,23 @@
 //
 // "Resumo Técnico: Atenção PaTH" (gist.science/pt/paper/2505.16381), §3
 // "Representação de Transformação UT": the product of a chunk's transitions
-// is I - W^T A W with A = (I + D triu_1(W W^T))^{-1} D, D = diag(beta); §3
+// is P = I - W^T A W with A = (I + D triu_1(W W^T))^{-1} D, D = diag(beta); §3
 // "Algoritmo Estilo FlashAttention", first sub-bullet: the chunk's
 // boundary-adjusted queries and keys.  Per chunk this kernel writes
-//     -U   = -A^T W                       (scan factor, bf16)
+//     P - I = W^T (-V),  V = A W          (scan transition, bf16, d x d)
 //      Y   = tril(Q W^T) A^T              (diagonal block, bf16)
 //     qhat = Q - Y W                      (fp32)
 //     -Z   = -triu_1(K W^T)               (diagonal block, bf16)
 //     khat = K - (Z A) W                  (bf16)
-// exactly the quantities of the CUDA-core version in ut_prep.cu.
+// and, for the prefill hand-off, V itself.  (The fp32 CUDA-core version in
+// ut_prep.cu writes -U = -A^T W in place of P - I: its scan applies the
+// transition as two products.)
 //
 // Products run as tcgen05 MMAs (M = 128) with fp32 accumulation in TMEM.
 // Operands that are not exact in bf16 (A, tril(QW^T), Y, Z, ZA) are split
 // into hi + lo bf16 parts and multiplied term by term (hi*hi + hi*lo + lo*hi),
-// which keeps those products close to fp32 accuracy.  The unit upper-
+// which keeps those products close to fp32 accuracy; -V enters P - I as one
+// bf16 operand (P - I is itself stored in bf16).  The unit upper-
 // triangular inverse X = (I + D triu_1(G))^{-1} (A = X D) is solved in fp32 on
 // CUDA cores, blocked: 16 x 16 diagonal blocks by back substitution, then
 // three doubling merges X_PQ = -X_PP (D G)_PQ X_QQ on a dense copy of X kept
@@ -59,12 +62,12 @@ constexpr uint32_t TOTAL = RS + 32768;
 constexpr size_t kSmem = TOTAL + 1024;
 constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 // B_STG*: a workspace-store group is staged (compute warps); B_FREE*: its
-// tiles have been read by the bulk stores (store thread).  Groups: 0 -U
-// (staging tile), Y (R3); 1 -Z (R3), qhat columns 0-31 of each half (staging
-// tile); 2 qhat columns 32-63 (d = 128; R1, free once Z A has completed);
-// last khat (R2, likewise free).
+// tiles have been read by the bulk stores (store thread).  Groups: 0 Y (R3);
+// 1 P - I (staging tile, which held -V as the operand of P - I); 2 -Z (R3),
+// qhat columns 0-31 of each half (staging tile); 3 qhat columns 32-63
+// (d = 128; R1, free once Z A has completed); last khat (R2, likewise free).
 enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN,
-       B_STG0, B_STG1, B_STG2, B_STG3, B_FREE0, B_FREE1, B_FREE2, B_FREE3, B_COUNT };
+       B_STG0, B_STG1, B_STG2, B_STG3, B_STG4, B_FREE0, B_FREE1, B_FREE2, B_FREE3, B_FREE4, B_COUNT };
 constexpr uint32_t RB_SLOT = 200;  // TMEM address and abort flag after the barriers
 static_assert(B_COUNT * 8 <= RB_SLOT && RB_SLOT + 8 <= 256, "barriers overlap the TMEM slot, abort flag or beta");
 }  // namespace utk
@@ -318,11 +321,14 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x, bh = blockIdx.y;
     const int row0 = chunk * C;
-    if (chunk == 0 && bh == 0 && threadIdx.x == 0) p.hdr->status = 0;
+    if (chunk == 0 && bh == 0 && threadIdx.x == 0) {
+        p.hdr->status = 0;
+        p.hdr->visited = 0;
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || i == B_OPS4 || (i >= B_STG0 && i <= B_STG3))
+            mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || i == B_OPS4 || (i >= B_STG0 && i <= B_STG4))
                                   ? kCompute : 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -350,19 +356,20 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             // Workspace stores: this thread issues each group once the compute
             // warps have staged it and frees its tiles once the stores have read
             // them, so no compute thread waits on a bulk store.
-            constexpr int kGroups = D == 128 ? 4 : 3;
+            constexpr int kGroups = D == 128 ? 5 : 4;
             bool ok = true;
             for (int g = 0; g < kGroups && ok; ++g) {
                 if (!(ok = mbar_wait_sleep(bar(B_STG0 + g), 0, wc, 45 + g))) break;
                 if (g == 0) {
-                    for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_un, sb + RS + b * 16384, 64 * b, row0, bh);
                     for (int b = 0; b < 2; ++b) tma_store_3d(&tm_y, sb + R3 + b * 16384, 64 * b, row0, bh);
-                } else if (g == 1 || (D == 128 && g == 2)) {
-                    const int c = g - 1;  // qhat columns 32c .. 32c+31 of each half
+                } else if (g == 1) {
+                    for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_un, sb + RS + b * 16384, 64 * b, row0, bh);
+                } else if (g == 2 || (D == 128 && g == 3)) {
+                    const int c = g - 2;  // qhat columns 32c .. 32c+31 of each half
                     const uint32_t src = sb + (c == 0 ? RS : R1);
                     for (int b = 0; b < 2; ++b)
                         tma_store_3d(&tm_qhat, src + b * 16384, (D / 2) * b + 32 * c, row0, bh);
-                    if (g == 1)
+                    if (g == 2)
                         for (int b = 0; b < 2; ++b) tma_store_3d(&tm_zn, sb + R3 + b * 16384, 64 * b, row0, bh);
                 } else {
                     for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_khat, sb + R2 + b * 16384, 64 * b, row0, bh);
@@ -392,11 +399,6 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             }
             if (ok) {
                 tc_fence_after();
-                // -U = -(A^T W): A^T is the MN-major view of A (hi, lo)
-                for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tmem + T384, mnmajor_desc(sb + R1, kk), mnmajor_desc(sb + R0, kk), ID_MNMN_D, kk > 0);
-                for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tmem + T384, mnmajor_desc(sb + R2, kk), mnmajor_desc(sb + R0, kk), ID_MNMN_D, 1);
                 // Y = Y' A^T = Y'hi Ahi + Y'hi Alo + Y'lo Ahi  (A rows as K-major B)
                 for (int kk = 0; kk < C / 16; ++kk)
                     mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), kmajor_desc(sb + R1, kk, 16384), ID_KK128, kk > 0);
@@ -405,12 +407,11 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 for (int kk = 0; kk < C / 16; ++kk)
                     mma_ss(tmem + T0, kmajor_desc(sb + R3 + 32768, kk, 16384), kmajor_desc(sb + R1, kk, 16384),
                            ID_KK128, 1);
-                if (p.vfac) {  // V = A W = Ahi W + Alo W (A rows as K-major A operand)
-                    for (int kk = 0; kk < C / 16; ++kk)
-                        mma_ss(tmem + T128, kmajor_desc(sb + R1, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, kk > 0);
-                    for (int kk = 0; kk < C / 16; ++kk)
-                        mma_ss(tmem + T128, kmajor_desc(sb + R2, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
-                }
+                // V = A W = Ahi W + Alo W (A rows as K-major A operand)
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T128, kmajor_desc(sb + R1, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, kk > 0);
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T128, kmajor_desc(sb + R2, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
                 mma_commit(bar(B_UY));
                 UT_TRACE(16);
                 ok = mbar_wait(bar(B_OPS2), 0, wc, 42);
@@ -423,6 +424,10 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     mma_ss(tmem + T384, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, kk > 0);
                 for (int kk = 0; kk < C / 16; ++kk)
                     mma_ss(tmem + T384, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
+                // P - I = W^T (-V): W^T is the MN-major view of the W tile (rows n >= d of
+                // that view are the zeroed second box when d = 64), -V the MN-major B
+                for (int kk = 0; kk < C / 16; ++kk)
+                    mma_ss(tmem + T128, mnmajor_desc(sb + R0, kk), mnmajor_desc(sb + RS, kk), ID_MNMN_D, kk > 0);
                 mma_commit(bar(B_Q));
                 UT_TRACE(18);
                 ok = mbar_wait(bar(B_OPS3), 0, wc, 43);
@@ -470,6 +475,10 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         uint8_t* opHi = sm + R3;
         uint8_t* opLo = sm + R3 + 32768;
         if (h == 0) sBeta[r] = grow < p.L ? p.beta[(size_t)bh * p.L + grow] : 0.f;
+        if (D == 64) {  // rows 64-127 of the W^T view (the unused second box of the W tile) read as zero
+            uint4* z = reinterpret_cast<uint4*>(sm + R0 + 16384);
+            for (int i = t; i < 16384 / 16; i += kCompute) z[i] = make_uint4(0, 0, 0, 0);
+        }
         // All compute warps wait on the same barriers, so they agree on `ok`
         // and reach the named barriers below together.
         if (t == 0) UT_TRACE(0);
@@ -550,31 +559,20 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         if (ok) {
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // -U row -> staging tile (bf16)
+            for (int c = 0; c < D / 64; ++c) {  // V = A W row -> -V (bf16 MN-major B operand of P - I)
                 uint32_t v[32];
                 const int col = (D / 2) * h + 32 * c;
-                tmem_ld32(tl + T384 + col, v);
+                tmem_ld32(tl + T128 + col, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    float u8[8];
+                    float v8[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) u8[e] = -__uint_as_float(v[8 * g + e]);
-                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(u8));
-                }
-            }
-            if (p.vfac) {
+                    for (int e = 0; e < 8; ++e) v8[e] = -__uint_as_float(v[8 * g + e]);
+                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(v8));
+                    if (p.vfac) {  // the prefill hand-off's key-side factor V
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {  // V = A W row -> global
-                    uint32_t v[32];
-                    const int col = (D / 2) * h + 32 * c;
-                    tmem_ld32(tl + T128 + col, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        float v8[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v8[e] = __uint_as_float(v[8 * g + e]);
+                        for (int e = 0; e < 8; ++e) v8[e] = -v8[e];
                         st_global_v4(p.vfac + ws_row * D + col + 8 * g, pack8(v8));
                     }
                 }
@@ -596,7 +594,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_OPS2));
-            mbar_arrive(bar(B_STG0));  // -U and Y tiles -> workspace
+            mbar_arrive(bar(B_STG0));  // Y tile -> workspace
             if (t == 0) UT_TRACE(6);
         }
         // This thread's half of the Q row, loaded while Y W runs on the tensor cores.
@@ -631,7 +629,23 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         if (t == 0) UT_TRACE(7);
         if (ok) {
             tc_fence_after();
-            // the -U and Y stores have read their tiles before R3 and RS are rewritten
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {  // P - I row (n) -> staging tile (bf16); -V there is consumed
+                uint32_t v[32];
+                const int col = (D / 2) * h + 32 * c;
+                tmem_ld32(tl + T128 + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float m8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m8[e] = __uint_as_float(v[8 * g + e]);
+                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(m8));
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(B_STG1));  // P - I -> workspace
+            // the Y store has read R3 before it is rewritten
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE0), 0, wc, 55));
         }
         if (ok) {
@@ -659,15 +673,19 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             mbar_arrive(bar(B_OPS3));
             if (t == 0) UT_TRACE(8);
             // qhat = Q - Y W (fp32), columns 0-31 of each half, into the staging
-            // tile while Z A runs (columns 32-63 follow once Z A has freed R1)
-            stage_qhat(0, sm + RS);
-            fence_proxy_async_smem();
-            mbar_arrive(bar(B_STG1));  // with the -Z tile
+            // tile (once the P - I store has read it) while Z A runs (columns
+            // 32-63 follow once Z A has freed R1)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE1), 0, wc, 56));
+            if (ok) {
+                stage_qhat(0, sm + RS);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(B_STG2));  // with the -Z tile
+            }
             if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ZA), 0, wc, 53));
             if (t == 0) UT_TRACE(9);
         }
-        // the -Z store (group 1) has read R3 before -(Z A) is written there
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE1), 0, wc, 57));
+        // the -Z store (group 2) has read R3 before -(Z A) is written there
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE2), 0, wc, 57));
         if (ok) {
             tc_fence_after();
 #pragma unroll
@@ -691,7 +709,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             if (D == 128) {  // qhat columns 32-63 of each half into R1 (A is dead after Z A) while (Z A) W runs
                 stage_qhat(1, sm + R1);
                 fence_proxy_async_smem();
-                mbar_arrive(bar(B_STG2));
+                mbar_arrive(bar(B_STG3));
             }
         }
         // This thread's half of the K row, loaded while (Z A) W runs.
@@ -728,7 +746,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_STG1 + D / 64));  // khat tile (R2, free since Z A) -> workspace
+            mbar_arrive(bar(B_STG2 + D / 64));  // khat tile (R2, free since Z A) -> workspace
             if (p.kmax2) {  // chunk max of |khat|^2 over rows < L (the solve temp is free)
                 float* red = reinterpret_cast<float*>(sm + RT);
                 red[r + 128 * h] = grow < p.L ? n2 : 0.f;

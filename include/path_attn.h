@@ -84,7 +84,8 @@ size_t path_attn_workspace_bytes(int B, int H, int L, int d, int dtype);
  *   o          : [B, H, L, d], same dtype as q (written)
  *   lse        : [B, H, L] float, natural-log log-sum-exp of the scaled logits
  *                per query (written), or NULL
- *   B, H >= 1; L >= 1; d in {16, 32, 64, 128} for PATH_F32, {64, 128} for PATH_BF16
+ *   B, H >= 1, B*H <= 65535; L >= 1; d in {16, 32, 64, 128} for PATH_F32, {64, 128}
+ *   for PATH_BF16
  *   causal     : must be 1 (the PaTH product is defined only for j <= i);
  *                0 returns PATH_ERR_UNSUPPORTED
  *   scale      : multiplies k_j^T(...)q_i (typically 1/sqrt(d))
@@ -208,7 +209,7 @@ int path_prefill_kcache(const void* k, const void* w, const float* beta, void* k
  * cached row j < n_cached,
  *     kcache[b,h,j,:] <- (I - beta_t[b,h] w_t[b,h] w_t[b,h]^T) kcache[b,h,j,:]
  * computed in fp32 and stored in the cache dtype (round to nearest even).
- *   kcache : [B, H, n_max, d] (updated in place); 0 <= n_cached <= n_max
+ *   kcache : [B, H, n_max, d] (updated in place); 0 <= n_cached <= n_max; B*H <= 65535
  *   w_t    : [B, H, d] cache dtype;  beta_t : [B, H] float
  *   d in {16, 32, 64, 128}
  */
@@ -224,7 +225,8 @@ int path_kcache_update(void* kcache, int B, int H, int n_cached, int n_max, int 
  *   3. o_t = softmax_j(scale * q_t . kcache[j]) vcache[j] over j = 0..n_cached,
  *      scoring each key with the value just stored.
  *   q_t, k_t, v_t, w_t : [B, H, d] cache dtype;  beta_t : [B, H] float
- *   kcache, vcache     : [B, H, n_max, d]; requires n_cached + 1 <= n_max
+ *   kcache, vcache     : [B, H, n_max, d]; requires n_cached + 1 <= n_max and
+ *                        B*H <= 65535 (else PATH_ERR_UNSUPPORTED)
  *                        (else PATH_ERR_INVALID); 0 <= n_cached
  *   o_t                : [B, H, d] cache dtype (written);  lse_t : [B, H] float or NULL
  *   workspace          : >= path_decode_workspace_bytes(B, H, n_max, d) bytes
@@ -243,6 +245,28 @@ int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const vo
  * PATH_ERR_CUDA if the synchronisation or read failed.
  */
 int path_get_status(const void* workspace, path_stream_t stream);
+
+/*
+ * Number of (query tile, key block) pairs, diagonal blocks included, that the
+ * most recent bf16 forward on `workspace` (path_attn_fwd, path_attn_fwd_fox or
+ * path_attn_fwd_relbias with dtype PATH_BF16) visited, summed over every head.
+ * Query tiles and key blocks are 128 positions, so a full causal pass visits
+ * B*H*N*(N+1)/2 of them with N = ceil(L/128); PaTH-FoX visits fewer when its
+ * far-block stop applies (§2 "Extensões: PaTH-FoX" workloads, §4 "Extrapolação
+ * de Comprimento").  Synchronises `stream` first.  Returns -1 if `workspace` is
+ * NULL or the read fails; the value is meaningless after an fp32 forward.
+ */
+long long path_fwd_visited_blocks(const void* workspace, path_stream_t stream);
+
+/*
+ * Test switch for the PaTH-FoX far-block stop of the bf16 forward: 0 makes
+ * later calls visit every key block, non-zero (the default) restores the stop.
+ * The stop only skips blocks whose every weight is exactly zero in fp32, so
+ * both settings give bit-identical outputs for inputs that meet the
+ * preconditions (beta in [0, 2], |w| = 1); the switch exists to test that.
+ * It is process-wide and not synchronised with calls already enqueued.
+ */
+void path_debug_set_fox_skip(int enabled);
 
 /*
  * Test hook for the device-side failure path.  A non-zero mask makes the next
@@ -278,7 +302,9 @@ void path_debug_set_timing_events(void* ev_start, void* ev_end);
  *     The 8 MiB covers B*H = 768 heads of d = 128 up to n_max = 43008.
  *   - The first call on each device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is tied to the device's context: after a
+ *     cudaDeviceReset the next call looks it up again (so, again, outside any
+ *     capture).
  *   - No call allocates or frees memory.  All calls share the one array, which
  *     keeps the previous call's contents; everything a step reads from it is
  *     written earlier in the same step.  Calls that can overlap on the GPU (two

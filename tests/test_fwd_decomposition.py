@@ -9,11 +9,14 @@ Transformação UT" instead: per chunk of C rows (W, Q, K, beta of the chunk, D 
   qhat  = Q - Y W,  Y = tril(Q W^T) A^T          each query carried to its chunk's start
   khat  = K - (Z A) W,  Z = triu_1(K W^T)        each key carried to its chunk's end
   -U    = -A^T W                                 so that x P_m^T = x - (x W^T) U for a row x
+  P - I = -W^T (A W)                             the chunk's transition P_m = H_b ... H_e, minus I
   S_nn  = scale (Q K^T - Y Z^T), j <= i          the diagonal block
 
 and a query tile then walks the earlier chunks m = n-1 .. 0 with q~ <- qhat_n:
-S_nm = scale q~ khat_m^T, q~ <- q~ + (q~ W_m^T)(-U_m), the logits of all blocks entering one
-softmax (with the forget-gate bias c_i - c_j of "Extensões: PaTH-FoX" when given).  This module
+S_nm = scale q~ khat_m^T, then q~ <- q~ P_m^T, the logits of all blocks entering one softmax (with the
+forget-gate bias c_i - c_j of "Extensões: PaTH-FoX" when given).  The transition is taken in one of
+two equal forms: q~ + (q~ W_m^T)(-U_m) (the fp32 CUDA-core scan) or q~ + q~ (P_m - I)^T (the bf16
+tensor-core scan, one d x d product).  This module
 writes those steps out with dense numpy products, and the tests check that they reproduce the
 oracle's o and lse to fp64 rounding for several chunk sizes, ragged last chunks and beta = 0 /
 beta = 2 positions; the prefill -> decode hand-off's suffix products are checked against explicit
@@ -32,10 +35,10 @@ def chunk_factors(Wc, Qc, Kc, bc):
     A = np.linalg.solve(np.eye(C) + D @ np.triu(Wc @ Wc.T, 1), D)
     Y = np.tril(Qc @ Wc.T) @ A.T
     Z = np.triu(Kc @ Wc.T, 1)
-    return dict(A=A, Y=Y, Z=Z, qhat=Qc - Y @ Wc, khat=Kc - (Z @ A) @ Wc, negU=-A.T @ Wc)
+    return dict(A=A, Y=Y, Z=Z, qhat=Qc - Y @ Wc, khat=Kc - (Z @ A) @ Wc, negU=-A.T @ Wc, PmI=-Wc.T @ (A @ Wc))
 
 
-def blocked_fwd(q, k, v, w, beta, scale, C, log_f=None):
+def blocked_fwd(q, k, v, w, beta, scale, C, log_f=None, transition="two_products"):
     L, d = q.shape
     N = -(-L // C)
     Lp = N * C
@@ -54,7 +57,10 @@ def blocked_fwd(q, k, v, w, beta, scale, C, log_f=None):
         for m in range(n - 1, -1, -1):
             cols = slice(m * C, (m + 1) * C)
             S[:, cols] = scale * qt @ f[m]["khat"].T
-            qt = qt + (qt @ W[cols].T) @ f[m]["negU"]
+            if transition == "two_products":
+                qt = qt + (qt @ W[cols].T) @ f[m]["negU"]
+            else:
+                qt = qt + qt @ f[m]["PmI"].T
         S = S + (c[rows, None] - c[None, :])
         S[:, L:] = -np.inf  # padded keys
         mx = S.max(1, keepdims=True)
@@ -74,16 +80,34 @@ def _case(rng, L, d):
     return q, k, v, w, beta
 
 
+@pytest.mark.parametrize("transition", ["two_products", "pm"])
 @pytest.mark.parametrize("L,d,C,fox", [(1, 4, 4, False), (13, 4, 4, False), (30, 6, 8, True), (64, 16, 16, False),
                                        (77, 8, 32, True), (40, 8, 64, False)])
-def test_blocked_forward_matches_oracle(L, d, C, fox):
+def test_blocked_forward_matches_oracle(L, d, C, fox, transition):
     rng = np.random.default_rng(200 + L)
     q, k, v, w, beta = _case(rng, L, d)
     lf = -rng.uniform(0.0, 1.0, L) if fox else None
     o_ref, lse_ref = orc.path_attn(q, k, v, w, beta, log_f=lf, scale=0.5)
-    o, lse = blocked_fwd(q, k, v, w, beta, 0.5, C, log_f=lf)
+    o, lse = blocked_fwd(q, k, v, w, beta, 0.5, C, log_f=lf, transition=transition)
     np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-11)
     np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-11)
+
+
+def test_chunk_transition_is_the_ordered_product():
+    """P_m - I from the UT factor equals H_b H_(b+1) ... H_e - I, built as explicit d x d matrices in
+    ascending order (beta = 0 and beta = 2 positions included); the descending product differs."""
+    rng = np.random.default_rng(17)
+    C, d = 10, 6
+    q, k, _, w, beta = _case(rng, C, d)
+    f = chunk_factors(w, q, k, beta)
+    P = np.eye(d)
+    for t in range(C):
+        P = P @ (np.eye(d) - beta[t] * np.outer(w[t], w[t]))
+    np.testing.assert_allclose(f["PmI"], P - np.eye(d), rtol=0, atol=1e-12)
+    Pdesc = np.eye(d)
+    for t in range(C - 1, -1, -1):
+        Pdesc = Pdesc @ (np.eye(d) - beta[t] * np.outer(w[t], w[t]))
+    assert np.abs(Pdesc - P).max() > 1e-3
 
 
 def test_chunk_factors_carry_rows_to_the_chunk_ends():
