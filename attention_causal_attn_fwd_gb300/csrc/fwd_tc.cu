@@ -8,15 +8,20 @@
 //
 // One CTA owns a tile of 128 queries (= one chunk n of one head) and walks the
 // key/value blocks m = n (diagonal), n-1, ..., 0.  Per block m < n, with the
-// transported query q~ (fp32 master and its bf16 copy, both in TMEM):
-//   S_k   S = q~ khat_m^T                                 (M=128, N=128, K=d)
-//   T     q~ += bf16(q~) (P_m - I)^T                      (M=128, N=d,   K=d)
-//   P V   O += P V_m,  P = exp2(S * scale*log2e - m)      (M=128, N=d,   K=128)
+// transported query q~ (fp32 master and its bf16 copy, both in TMEM), one
+// accumulating product gives the block's logits and the query's step through
+// the block:
+//   [S | q~] += bf16(q~) [khat_m ; P_m - I]^T             (M=128, N=128+d, K=d)
+//   O += P V_m,  P = exp2(S * scale*log2e - m)            (M=128, N=d,     K=128)
+// (the softmax warps zero S after reading it, so S starts from zero).
 // where P_m = I - W_m^T A_m W_m is the chunk's transition in the UT form of §3
 // "Representação de Transformação UT" (the UT prep writes P_m - I in bf16), so
-// the query moves through a whole chunk in one d x d product.  The diagonal
-// block uses S = Q K^T + Y (-Z)^T with the causal mask.  The logits may carry
-// an additive bias (MODE 1 PaTH-FoX, MODE 2 relative position).
+// the query moves through a whole chunk in one d x d product, and S and dq
+// share the A operand, which makes the instruction N = 256 wide (d = 128): a
+// single thread cannot issue the 128-wide ones fast enough to keep the pipe
+// busy.  The diagonal block uses S = Q K^T + Y (-Z)^T with the causal mask.
+// The logits may carry an additive bias (MODE 1 PaTH-FoX, MODE 2 relative
+// position).
 // Online softmax keeps one query row per thread (TMEM lane = row), so row
 // max and sum need no cross-thread reduction.  The running max is only
 // raised (and O rescaled) when it grows by more than 2^8, which keeps every
@@ -25,21 +30,23 @@
 // Warp roles (320 threads):
 //   warp 0      TMA producer (one lane) + TMEM allocation
 //   warp 1      tcgen05.mma issuer (one lane), per block in the order
-//               S_k(it), T(it), P V(it-1): the transport of the next query
-//               overlaps P V, and the softmax of block it overlaps T and P V
+//               [S | q~](it), P V(it-1): the transport of the next query
+//               overlaps P V, and the softmax of block it overlaps P V
 //   warps 2-5   softmax: S -> P (bf16, into TMEM), row statistics, epilogue
 //   warps 6-9   query transport: fp32 q~ master -> bf16 q~ (TMEM)
 // Every MMA reads its A operand from TMEM except the diagonal block's, so
 // shared memory carries only the B tiles (khat, P - I, V) and their TMA writes.
 //
-// TMEM (512 columns x 128 lanes, 32-bit): [0,128) S (fp32), [128,192) P (bf16
-// pairs), [192,192+d/2) bf16 q~ (pairs), [256,256+d) O, [384,384+d) q~ master.
+// TMEM (512 columns x 128 lanes, 32-bit): [0,128) S (fp32), [128,128+d) q~
+// master (fp32), [256,320) P (bf16 pairs), [320,320+d/2) bf16 q~ (pairs),
+// [384,384+d) O.
 // Shared memory (1024-aligned, 128-byte swizzled tiles as TMA writes them,
-// 64-column boxes of 16 KB), each operand double-buffered by block parity:
-//   K0/K1  khat_m of block iteration it in slot it & 1 (K0: K of the diagonal)
-//   M0/M1  P_m - I (K-major B)              (M0: Y of the diagonal)
-//   V0/V1  V_m, MN-major B                  (V0: V of the diagonal, V1: -Z)
-//   Q      Q of the diagonal
+// 64-column boxes of 16 KB), double-buffered by block parity:
+//   KM0/KM1  per 64-column box c (32 KB): rows 0-127 khat_m, rows 128-255
+//            P_m - I (one K-major B operand of N = 128 + d rows); KM0 holds K
+//            and Y of the diagonal in the same places
+//   V0/V1    V_m, MN-major B            (V0: V of the diagonal, V1: -Z)
+//   Q        Q of the diagonal
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
 // PATH_ERR_TIMEOUT in the workspace status word, every role stops, pending
 // copies and MMAs are drained (bounded) and TMEM is freed before exit.
@@ -56,17 +63,17 @@ using namespace sm100;
 
 constexpr int kTcC = 128;
 constexpr int kTcThreads = 320;
-constexpr uint32_t SM_K0 = 0, SM_K1 = 32768, SM_M0 = 65536, SM_M1 = 98304, SM_V0 = 131072, SM_V1 = 163840,
-                   SM_Q = 196608, SM_BAR = 229376;
+constexpr uint32_t SM_KM0 = 0, SM_V0 = 131072, SM_V1 = 163840, SM_Q = 196608, SM_BAR = 229376;
+constexpr uint32_t KM_SLOT = 65536;  // SM_KM1 = SM_KM0 + KM_SLOT
 constexpr uint32_t SM_TOTAL = SM_BAR + 256;
 constexpr size_t kTcSmem = SM_TOTAL + 1024;  // + alignment slack
-constexpr uint32_t TM_S = 0, TM_P = 128, TM_QB = 192, TM_O = 256, TM_QM = 384;
+constexpr uint32_t TM_S = 0, TM_QM = 128, TM_P = 256, TM_QB = 320, TM_O = 384;
 
 // Every barrier below is waited on in a way that it can never run two phases
 // ahead of its waiter (a parity wait cannot tell those apart): each one's next
 // completion needs an action its waiter takes after the current wait.
-enum Bar { B_QFULL = 0, B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1, B_MFULL0, B_MFULL1, B_MEMPTY0, B_MEMPTY1,
-           B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1, B_SFULL, B_ODONE, B_QUPD, B_DRAIN, B_COUNT };
+enum Bar { B_QFULL = 0, B_KMFULL0, B_KMFULL1, B_KMEMPTY0, B_KMEMPTY1, B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,
+           B_SDONE, B_ODONE, B_DRAIN, B_COUNT };
 // Named (hardware) barriers between the warps and the MMA warp; id 2 is the
 // softmax warps' own vote barrier.  Counts are threads: the MMA warp syncs,
 // the others arrive.
@@ -134,9 +141,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr bool BIASED = MODE != 0;   // logits carry an additive bias (log2 units in the softmax)
     constexpr int KCH = D / 64;          // 64-column boxes of the head dim
     constexpr uint32_t ROWB = 128u * D * 2u;  // bytes of one [128 x D] bf16 tile
-    constexpr uint32_t IDESC_S = idesc_bf16(128, false);   // N = 128 keys, B K-major
-    constexpr uint32_t IDESC_T = idesc_bf16(D, false);     // N = d, B K-major (P_m - I)
-    constexpr uint32_t IDESC_PV = idesc_bf16(D, true);     // N = d, B MN-major (V)
+    constexpr uint32_t IDESC_S = idesc_bf16(128, false);      // N = 128 keys, B K-major (diagonal)
+    constexpr uint32_t IDESC_SQ = idesc_bf16(128 + D, false); // N = 128 keys + d, B K-major [khat; P - I]
+    static_assert(TM_QM == TM_S + 128, "S and the q~ master form one N = 128 + d accumulator");
+    constexpr uint32_t IDESC_PV = idesc_bf16(D, true);        // N = d, B MN-major (V)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -191,44 +199,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_khat);
             prefetch_tmap(&tm_pm); prefetch_tmap(&tm_y); prefetch_tmap(&tm_zn);
-            // diagonal block: Q, K (K slot 0), Y (M slot 0), -Z (V slot 1), V (V slot 0)
+            // diagonal block: Q, K and Y (KM slot 0), -Z (V slot 1), V (V slot 0)
             mbar_expect_tx(bar(B_QFULL), ROWB);
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_Q + c * 16384, &tm_q, bar(B_QFULL), c * 64, row0, bh);
-            mbar_expect_tx(bar(B_KFULL0), ROWB);
-            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_K0 + c * 16384, &tm_k, bar(B_KFULL0), c * 64, row0, bh);
-            mbar_expect_tx(bar(B_MFULL0), 32768);
-            for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_M0 + c * 16384, &tm_y, bar(B_MFULL0), c * 64, row0, bh);
+            mbar_expect_tx(bar(B_KMFULL0), ROWB + 32768);
+            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_KM0 + c * 32768, &tm_k, bar(B_KMFULL0), c * 64, row0, bh);
+            for (int c = 0; c < 2; ++c)
+                tma_load_3d(sb + SM_KM0 + c * 32768 + 16384, &tm_y, bar(B_KMFULL0), c * 64, row0, bh);
             mbar_expect_tx(bar(B_VFULL1), 32768);
             for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_V1 + c * 16384, &tm_zn, bar(B_VFULL1), c * 64, row0, bh);
             mbar_expect_tx(bar(B_VFULL0), ROWB);
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V0 + c * 16384, &tm_v, bar(B_VFULL0), c * 64, row0, bh);
-            // Scan blocks, three streams (khat, P - I, V), each block iteration it
-            // into slot it & 1 once that slot's previous contents were consumed
-            // (their empty barrier's matching completion).  P - I is not used by
-            // the last block (m = 0).
-            int nxt[3] = {1, 1, 1};
-            int issued[7] = {1, 1, 0, 1, 0, 1, 1};  // Q, K0, K1, M0, M1, V0, V1 (loads per full barrier)
+            // Scan blocks, two streams: khat with P - I (one KM slot; the last block,
+            // m = 0, needs no P - I) and V, each block iteration it into slot it & 1
+            // once that slot's previous contents were consumed (their empty
+            // barrier's matching completion).
+            int nxt[2] = {1, 1};
+            int issued[5] = {1, 1, 0, 1, 1};  // Q, KM0, KM1, V0, V1 (loads per full barrier)
             const uint64_t t0 = globaltimer();
             bool ok = true;
             for (uint32_t spin = 0; ok; ++spin) {
-                const int stop = FOX ? *stop_it : n + 1;
-                const int lim[3] = {min(n, stop - 1), min(n - 1, stop - 1), min(n, stop - 1)};
-                if (nxt[0] > lim[0] && nxt[1] > lim[1] && nxt[2] > lim[2]) break;
-                for (int sl = 0; sl < 3; ++sl) {
+                const int lim = FOX ? min(n, *stop_it - 1) : n;
+                if (nxt[0] > lim && nxt[1] > lim) break;
+                for (int sl = 0; sl < 2; ++sl) {
                     const int it = nxt[sl];
-                    if (it > lim[sl]) continue;
+                    if (it > lim) continue;
                     const int s = it & 1;
-                    const int u = sl == 2 ? v_use(it) : (it >> 1);
-                    const int eb = sl == 0 ? B_KEMPTY0 : sl == 1 ? B_MEMPTY0 : B_VEMPTY0;
-                    if (u >= 1 && !mbar_test_wait(bar(eb + s), (uint32_t)((u - 1) & 1))) continue;
+                    const int u = sl == 1 ? v_use(it) : (it >> 1);
+                    const int eb = (sl == 0 ? B_KMEMPTY0 : B_VEMPTY0) + s;
+                    if (u >= 1 && !mbar_test_wait(bar(eb), (uint32_t)((u - 1) & 1))) continue;
                     nxt[sl] = it + 1;
-                    if (sl == 2 && p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
-                    const int fb = (sl == 0 ? B_KFULL0 : sl == 1 ? B_MFULL0 : B_VFULL0) + s;
-                    const uint32_t dst = sb + (sl == 0 ? SM_K0 : sl == 1 ? SM_M0 : SM_V0) + (uint32_t)s * 32768u;
-                    const CUtensorMap* map = sl == 0 ? &tm_khat : sl == 1 ? &tm_pm : &tm_v;
+                    if (sl == 1 && p.fault && it == 1) continue;  // test hook: the consumer's wait must expire
                     const int r = (n - it) * kTcC;
-                    mbar_expect_tx(bar(fb), ROWB);
-                    for (int c = 0; c < KCH; ++c) tma_load_3d(dst + c * 16384, map, bar(fb), c * 64, r, bh);
+                    if (sl == 0) {
+                        const uint32_t dst = sb + SM_KM0 + (uint32_t)s * KM_SLOT;
+                        const bool pm = n - it > 0;
+                        mbar_expect_tx(bar(B_KMFULL0 + s), pm ? 2 * ROWB : ROWB);
+                        for (int c = 0; c < KCH; ++c) {
+                            tma_load_3d(dst + c * 32768, &tm_khat, bar(B_KMFULL0 + s), c * 64, r, bh);
+                            if (pm) tma_load_3d(dst + c * 32768 + 16384, &tm_pm, bar(B_KMFULL0 + s), c * 64, r, bh);
+                        }
+                    } else {
+                        mbar_expect_tx(bar(B_VFULL0 + s), ROWB);
+                        for (int c = 0; c < KCH; ++c)
+                            tma_load_3d(sb + SM_V0 + (uint32_t)s * 32768u + c * 16384, &tm_v, bar(B_VFULL0 + s),
+                                        c * 64, r, bh);
+                    }
                     ++issued[1 + 2 * sl + s];
                     TC_TRACE(12 + sl, it);
                 }
@@ -242,8 +258,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             // copies still in flight must land before the CTA exits
-            const int ful[7] = {B_QFULL, B_KFULL0, B_KFULL1, B_MFULL0, B_MFULL1, B_VFULL0, B_VFULL1};
-            for (int i = 0; i < 7; ++i)
+            const int ful[5] = {B_QFULL, B_KMFULL0, B_KMFULL1, B_VFULL0, B_VFULL1};
+            for (int i = 0; i < 5; ++i)
                 if (issued[i] > 0) drain_wait(bar(ful[i]), (uint32_t)((issued[i] - 1) & 1), p.limit_ns, p.hdr, 91);
         }
     } else if (warp == 1) {
@@ -253,25 +269,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // therefore waits on nothing but two named barriers per block (no
         // shared-memory round trip): the warps that signal it have already
         // waited for the copies the next MMAs read.
-        //   NB_SK(it)   T(it) and S_k(it) may go: bf16 q~(it) is in TMEM, khat_m and
-        //               P_m - I have landed (transport warps), S(it-1) has been read
-        //               and, with FoX, block it is known to be visited (softmax warps)
+        //   NB_SK(it)   [S | q~](it) may go: bf16 q~(it) is in TMEM and khat_m,
+        //               P_m - I have landed (transport warps); S(it-1) has been
+        //               read and zeroed and, with FoX, block it is known to be
+        //               visited (softmax warps)
         //   NB_PV(it)   P V(it) may go: P(it) is in TMEM and V_m has landed (softmax)
-        // T(it) goes first: the transport warps convert q~(it+1) while S_k(it) and
-        // P V(it-1) execute.  Lane 0 issues; the whole warp takes the barriers.
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KFULL0), 0, wc, 11) &&
-                                              mbar_wait(bar(B_MFULL0), 0, wc, 12) && mbar_wait(bar(B_VFULL1), 0, wc, 12));
+        // Lane 0 issues; the whole warp takes the barriers.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KMFULL0), 0, wc, 11) &&
+                                              mbar_wait(bar(B_VFULL1), 0, wc, 12));
         if (ok && lane == 0) {
             tc_fence_after();
             // diagonal: S = Q K^T + Y (-Z)^T
             for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_K0, kk, 16384), IDESC_S,
+                mma_ss(tmem + TM_S, kmajor_desc(sb + SM_Q, kk, 16384), kmajor_desc(sb + SM_KM0, kk, 32768), IDESC_S,
                        kk > 0);
             for (int kk = 0; kk < kTcC / 16; ++kk)
-                mma_ss(tmem + TM_S, kmajor_desc(sb + SM_M0, kk, 16384), kmajor_desc(sb + SM_V1, kk, 16384), IDESC_S, 1);
-            mma_commit(bar(B_SFULL));
-            mma_commit(bar(B_KEMPTY0));
-            mma_commit(bar(B_MEMPTY0));
+                mma_ss(tmem + TM_S, kmajor_desc(sb + SM_KM0 + 16384, kk, 32768), kmajor_desc(sb + SM_V1, kk, 16384),
+                       IDESC_S, 1);
+            mma_commit(bar(B_SDONE));
+            mma_commit(bar(B_KMEMPTY0));
             mma_commit(bar(B_VEMPTY1));
             TC_TRACE(0, 0);
         }
@@ -299,7 +315,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // failure read stale but valid addresses and their results are unused.
         if (ok) {
             for (int it = 1; it <= n; ++it) {
-                const int m = n - it, s = it & 1;
+                const int s = it & 1;
                 named_bar_sync(NB_SK, NB_SK_COUNT);
                 if (FOX && *stop_it <= it) {  // every block from here on contributes exactly zero
                     last = it - 1;
@@ -308,19 +324,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) {
                     TC_TRACE(15, it);
                     tc_fence_after();
-                    if (m > 0) {  // q~ += bf16(q~) (P_m - I)^T
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ts(tmem + TM_QM, tmem + TM_QB + kk * 8,
-                                   kmajor_desc(sb + SM_M0 + s * 32768u, kk, 16384), IDESC_T, 1);
-                        mma_commit(bar(B_QUPD));
-                        mma_commit(bar(B_MEMPTY0 + s));
-                        TC_TRACE(3, it);
-                    }
-                    for (int kk = 0; kk < D / 16; ++kk)  // S = q~ khat^T
-                        mma_ts(tmem + TM_S, tmem + TM_QB + kk * 8, kmajor_desc(sb + SM_K0 + s * 32768u, kk, 16384),
-                               IDESC_S, kk > 0);
-                    mma_commit(bar(B_SFULL));
-                    mma_commit(bar(B_KEMPTY0 + s));
+                    // [S | q~] += bf16(q~) [khat ; P_m - I]^T  (for m = 0 the q~ half reads
+                    // stale slot contents; the master is not used again)
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ts(tmem + TM_S, tmem + TM_QB + kk * 8, kmajor_desc(sb + SM_KM0 + s * KM_SLOT, kk, 32768),
+                               IDESC_SQ, 1);
+                    mma_commit(bar(B_SDONE));
+                    mma_commit(bar(B_KMEMPTY0 + s));
                     TC_TRACE(1, it);
                 }
                 __syncwarp();
@@ -374,7 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         for (int it = 0; it <= n; ++it) {
             const int m = n - it;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 20));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SDONE), it & 1, wc, 20));
             if (!ok) break;
             if (r == 0) TC_TRACE(4, it);
             tc_fence_after();
@@ -388,6 +398,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) s[32 * c + j] = __uint_as_float(raw[c][j]);
+            }
+            if (it < n) {  // the next block's product accumulates into S
+                uint32_t z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = 0u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_st32(tl + TM_S + 32 * c, z);
+                tmem_wait_st();
             }
             // Without a bias the scores stay raw (the scale is applied inside the
             // exponent, one FFMA each); with one (FoX, relative) they become
@@ -601,8 +619,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // so the round is arrived on then too, without waiting for copies the
         // producer may never issue.
         auto release_block = [&](int it) -> int {
-            int st = wait_or_stop(B_KFULL0 + (it & 1), (uint32_t)((it >> 1) & 1), it, 34);
-            if (st == 1 && n - it > 0) st = wait_or_stop(B_MFULL0 + (it & 1), (uint32_t)((it >> 1) & 1), it, 35);
+            const int st = wait_or_stop(B_KMFULL0 + (it & 1), (uint32_t)((it >> 1) & 1), it, 34);
             if (st == 1 || st == 2) {
                 tc_fence_before();
                 named_bar_arrive(NB_SK, NB_SK_COUNT);
@@ -630,23 +647,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 put_bf16(c, v);
             }
             tmem_wait_st();
-            st = release_block(1);
-            ok = st == 1;
+            // A parity wait names a phase correctly only once the phase before it is
+            // known to be complete: a barrier still in phase k - 1 satisfies a wait
+            // for phase k at once.  The first phases of SDONE and of KM slot 0 belong
+            // to the diagonal block, so this warp observes the diagonal's product
+            // (SDONE phase 0, which follows its copies) before it waits for SDONE
+            // phase 1 and KM slot 0 phase 1 below.  SDONE cannot move past phase 1
+            // before this warp arrives on NB_SK(1).
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SDONE), 0, wc, 30));
+            if (ok) {
+                st = release_block(1);
+                ok = st == 1;
+            }
         }
         for (int it = 1; it < n && ok; ++it) {  // q~ for block iteration it + 1 (m = n - it > 0)
-            st = wait_or_stop(B_QUPD, (uint32_t)((it - 1) & 1), it, 31);  // T(it) has completed
+            // [S | q~](it) has completed: the master moved through chunk m and bf16
+            // q~(it) is no longer read
+            st = wait_or_stop(B_SDONE, (uint32_t)(it & 1), it, 31);
             if (st != 1) break;
             if (r == 0) TC_TRACE(8, it);
             tc_fence_after();
-            uint32_t v[D / 32][32];
+            {
+                uint32_t v[D / 32][32];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + TM_QM + 32 * c, v[c]);
-            tmem_wait_ld();
-            // S_k(it), issued after T(it), still reads bf16 q~(it)
-            if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, wc, 32)))) break;
-            tc_fence_after();
+                for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + TM_QM + 32 * c, v[c]);
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) put_bf16(c, v[c]);
+                for (int c = 0; c < D / 32; ++c) put_bf16(c, v[c]);
+            }
             tmem_wait_st();
             st = release_block(it + 1);
             if (st != 1) break;
