@@ -449,14 +449,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int j = 0; j < 128; ++j)
                     if (j > r) s[j] = -INFINITY;
             }
-            float mx;  // row max in log2 units (8 independent partial maxima)
+            float mx;  // row max in log2 units (8 independent chains of three-input maxima)
             {
                 float pm[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) pm[u] = s[u];
+                for (int u = 0; u < 8; ++u) pm[u] = fmaxf(s[u], s[u + 8]);
 #pragma unroll
-                for (int j = 8; j < 128; ++j) pm[j & 7] = fmaxf(pm[j & 7], s[j]);
-                mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                for (int j = 16; j < 128; j += 16)
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) pm[u] = fmax3(pm[u], s[j + u], s[j + 8 + u]);
+                mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
                 if (!BIASED) mx *= sl2;  // sl2 > 0: the max of raw scores scales
             }
             bool stop = false;
@@ -502,19 +504,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool rescale = m_new > m_run + 8.0f;
             const float m_use = rescale ? m_new : m_run;
             const float alpha = rescale ? ex2_approx(m_run - m_use) : 1.0f;
-            float psum[8];
+            // Probes of the two barriers P V(it) waits behind, issued before the last
+            // exponentials so their shared-memory round trip overlaps them; a
+            // blocking wait follows only if a probe saw the phase incomplete.
+            bool od_ready = it == 0, v_ready = false;
+            uint64_t psum[4];  // packed partial row sums (8 chains)
 #pragma unroll
-            for (int u = 0; u < 8; ++u) psum[u] = 0.f;
+            for (int u = 0; u < 4; ++u) psum[u] = 0ull;
             uint32_t pk[64];
             const float neg_m = -m_use;
+            const uint64_t nm2 = f32x2(neg_m, neg_m), sl2x2 = f32x2(sl2, sl2);
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
-                const float p0 = ex2_approx(BIASED ? s[2 * j] + neg_m : fmaf(s[2 * j], sl2, neg_m));
-                const float p1 = ex2_approx(BIASED ? s[2 * j + 1] + neg_m : fmaf(s[2 * j + 1], sl2, neg_m));
-                psum[j & 7] += p0 + p1;
+                if (j == 40) {
+                    if (it > 0) od_ready = mbar_test_wait(bar(B_ODONE), (uint32_t)((it - 1) & 1));
+                    v_ready = mbar_test_wait(bar(B_VFULL0 + (it & 1)), (uint32_t)(v_use(it) & 1));
+                }
+                const uint64_t sv = f32x2(s[2 * j], s[2 * j + 1]);
+                const uint64_t xv = BIASED ? add_f32x2(sv, nm2) : fma_f32x2(sv, sl2x2, nm2);
+                float x0, x1;
+                f32x2_split(xv, x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                psum[j & 3] = add_f32x2(psum[j & 3], f32x2(p0, p1));
                 pk[j] = pack_bf16x2(p0, p1);
             }
-            const float sum = ((psum[0] + psum[1]) + (psum[2] + psum[3])) + ((psum[4] + psum[5]) + (psum[6] + psum[7]));
+            float sum;
+            {
+                const uint64_t t = add_f32x2(add_f32x2(psum[0], psum[1]), add_f32x2(psum[2], psum[3]));
+                float a, b;
+                f32x2_split(t, a, b);
+                sum = a + b;
+            }
             l_run = l_run * alpha + sum;
             if (r == 0) TC_TRACE(6, it);
             // P and O are single-buffered: the previous block's P V must have completed
@@ -522,7 +542,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // TMEM loads/stores, so the whole warp takes it when any of its rows needs
             // it (alpha = 1 elsewhere).
             if (it > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (uint32_t)((it - 1) & 1), wc, 21));
+                ok = __all_sync(0xffffffffu, od_ready || mbar_wait(bar(B_ODONE), (uint32_t)((it - 1) & 1), wc, 21));
                 if (!ok) break;
                 if (r == 0) TC_TRACE(11, it);
                 tc_fence_after();
@@ -543,7 +563,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tmem_st32(tl + TM_P + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
             // V_m of this block has landed before P V may go
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_VFULL0 + (it & 1)), (uint32_t)(v_use(it) & 1), wc, 24));
+            ok = __all_sync(0xffffffffu,
+                            v_ready || mbar_wait(bar(B_VFULL0 + (it & 1)), (uint32_t)(v_use(it) & 1), wc, 24));
             if (!ok) break;
             tc_fence_before();
             named_bar_arrive(NB_PV, NB_PV_COUNT);
