@@ -28,7 +28,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libpathattn.so")
 
-PATH_OK, PATH_ERR_INVALID, PATH_ERR_UNSUPPORTED, PATH_ERR_CUDA, PATH_ERR_TIMEOUT, PATH_ERR_WORKSPACE = range(6)
+(PATH_OK, PATH_ERR_INVALID, PATH_ERR_UNSUPPORTED, PATH_ERR_CUDA, PATH_ERR_TIMEOUT, PATH_ERR_WORKSPACE,
+ PATH_ERR_BOUNDS) = range(7)
 PATH_F32, PATH_BF16 = 0, 1
 _DT = {torch.float32: PATH_F32, torch.bfloat16: PATH_BF16}
 

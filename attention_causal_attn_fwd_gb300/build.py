@@ -3,6 +3,11 @@
 Each .cu under csrc/ compiles to an object in parallel; the objects link into
 attention_causal_attn_fwd_gb300/_build/libpathattn.so.  Rebuilds only what
 changed (sources or headers newer than the object).
+
+build(variant="debug_bounds") makes the bounds-checked library in
+_build_debug_bounds/ (-DPATH_DEBUG_BOUNDS: device-side index checks of the
+plain global loads and stores record PATH_ERR_BOUNDS in the workspace status
+word instead of accessing out of range); the tests load it beside the normal one.
 """
 from __future__ import annotations
 
@@ -40,17 +45,28 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+VARIANTS = {"": [], "debug_bounds": ["-DPATH_DEBUG_BOUNDS"]}
+
+
+def lib_path(variant: str = "") -> str:
+    return LIB if not variant else os.path.join(PKG, "_build_" + variant, "libpathattn.so")
+
+
+def build(verbose: bool = False, ptxas_verbose: bool = False, variant: str = "") -> str:
+    build_dir = os.path.dirname(lib_path(variant))
+    lib = lib_path(variant)
+    extra = VARIANTS[variant]
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdrs = _headers()
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(build_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if ptxas_verbose or _stale(o, [s, __file__] + hdrs):
-            cmd = [nvcc()] + ARCH + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", s, "-o", o]
+            cmd = ([nvcc()] + ARCH + NVCC_FLAGS + extra + (["-Xptxas", "-v"] if ptxas_verbose else []) +
+                   ["-c", s, "-o", o])
             jobs.append(cmd)
 
     def run(cmd):
@@ -66,14 +82,14 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    if jobs or _stale(LIB, objs):
-        tmp = LIB + ".%d.tmp" % os.getpid()
+    if jobs or _stale(lib, objs):
+        tmp = lib + ".%d.tmp" % os.getpid()
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

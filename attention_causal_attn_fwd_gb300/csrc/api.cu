@@ -100,6 +100,7 @@ const char* path_status_string(int code) {
         case PATH_ERR_CUDA: return "CUDA runtime error";
         case PATH_ERR_TIMEOUT: return "device-side wait timed out";
         case PATH_ERR_WORKSPACE: return "workspace missing or too small";
+        case PATH_ERR_BOUNDS: return "device-side index check failed";
         default: return "unknown status";
     }
 }

@@ -75,6 +75,22 @@ __device__ __forceinline__ void report_status(WsHeader* h, int code, int site) {
     if (atomicCAS(&h->status, 0, code) == 0) h->fault_site = site;
 }
 
+// Index checks of the plain (non-TMA) global loads and stores, compiled in only
+// for the bounds-checked build (-DPATH_DEBUG_BOUNDS): an element range
+// [first, first + count) outside [0, size) records PATH_ERR_BOUNDS and the site
+// in the status word, and the caller skips the access.  The normal build
+// checks nothing.
+#ifdef PATH_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(long long first, long long count, long long size, WsHeader* h,
+                                          int site) {
+    if (first >= 0 && count >= 0 && first + count <= size) return true;
+    report_status(h, PATH_ERR_BOUNDS, site);
+    return false;
+}
+#else
+__device__ __forceinline__ bool in_bounds(long long, long long, long long, WsHeader*, int) { return true; }
+#endif
+
 // Optional events recorded around the dominant kernel of each call (set by
 // path_debug_set_timing_events; both null when unused).
 void timing_events(cudaEvent_t* start, cudaEvent_t* end);

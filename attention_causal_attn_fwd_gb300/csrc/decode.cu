@@ -68,11 +68,13 @@ __global__ void __launch_bounds__(kDecNT) decode_update_score(
     const int j1 = min(j0 + kDecodeRowsPerSplit, total);
 
     const size_t hv = (size_t)bh * D + li * G::EPL;  // this lane's slice of a [B,H,D] vector
+    const long long n_bh = gridDim.y, n_cache = (long long)gridDim.y * n_max * D;
+    const bool hv_ok = in_bounds((long long)hv, G::EPL, n_bh * D, hdr, 220);
     float wv[G::EPL], qv[G::EPL];
     {
         Vec16<T> a, b;
-        a.raw = ld_global_v4(w_t + hv);
-        b.raw = ld_global_v4(q_t + hv);
+        a.raw = hv_ok ? ld_global_v4(w_t + hv) : make_uint4(0, 0, 0, 0);
+        b.raw = hv_ok ? ld_global_v4(q_t + hv) : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int e = 0; e < G::EPL; ++e) {
             wv[e] = a.get(e);
@@ -97,13 +99,14 @@ __global__ void __launch_bounds__(kDecNT) decode_update_score(
 #pragma unroll
         for (int u = 0; u < kDecUnroll; ++u) {
             const int j = base + u * STRIDE;
-            if (j < j1) {
+            const bool row_ok = j < j1 && in_bounds(((long long)bh * n_max + j) * D + li * G::EPL, G::EPL, n_cache, hdr, 221);
+            if (row_ok) {
                 if (j < n_cached) {
                     kvec[u].raw = ld_global_stream_v4(kh + (size_t)j * D);
                     vvec[u].raw = ld_global_stream_v4(vh + (size_t)j * D);
                 } else {  // the new token: appended untransported
-                    kvec[u].raw = ld_global_v4(k_t + hv);
-                    vvec[u].raw = ld_global_v4(v_t + hv);
+                    kvec[u].raw = hv_ok ? ld_global_v4(k_t + hv) : make_uint4(0, 0, 0, 0);
+                    vvec[u].raw = hv_ok ? ld_global_v4(v_t + hv) : make_uint4(0, 0, 0, 0);
                 }
             } else {
                 kvec[u].raw = make_uint4(0, 0, 0, 0);
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(kDecNT) decode_update_score(
             const int j = base + u * STRIDE;
             const Vec16<T> tr = transport<T, D>(kvec[u], wv, beta);  // all lanes shuffle
             const Vec16<T> kn = (j < n_cached) ? tr : kvec[u];
-            if (j < j1) {
+            if (j < j1 && in_bounds(((long long)bh * n_max + j) * D + li * G::EPL, G::EPL, n_cache, hdr, 222)) {
                 st_global_v4(kh + (size_t)j * D, kn.raw);
                 if (j == n_cached) st_global_v4(vh + (size_t)j * D, vvec[u].raw);
             }
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kDecNT) decode_update_score(
         float o = 0.f;
         for (int g = 0; g < NG; ++g)
             if (s_m[g] != -INFINITY) o += s_o[g][c] * exp2f(s_m[g] - M);
-        part_o[pi * D + c] = o;
+        if (in_bounds((long long)pi * D + c, 1, (long long)gridDim.y * nsplit * D, hdr, 223)) part_o[pi * D + c] = o;
     }
     if (threadIdx.x == 0) {
         float L = 0.f;

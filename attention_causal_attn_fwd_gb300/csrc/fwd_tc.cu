@@ -350,7 +350,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const float* cumh = FOX ? p.cum + (size_t)bh * p.Lp : nullptr;
         const float* relh = REL ? p.rbias + (size_t)(bh % p.H) * p.L : nullptr;
-        const float ci = FOX ? cumh[row0 + r] : 0.f;
+        const long long n_bhlp = (long long)p.BH * p.Lp, n_bhl = (long long)p.BH * p.L;
+        const float ci = FOX && in_bounds((long long)bh * p.Lp + row0 + r, 1, n_bhlp, p.hdr, 200) ? cumh[row0 + r] : 0.f;
         constexpr float kL2e = 1.4426950408889634f;
         float m_run = -INFINITY, l_run = 0.f;
         float m_true = -INFINITY;  // largest logit seen (log2 units)
@@ -359,13 +360,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (FOX && n > 0) {
             if (warp == 2) {  // max |khat|^2 over the chunks left of this tile
                 float x = 0.f;
-                for (int c = lane; c < n; c += 32) x = fmaxf(x, p.kmax2[(size_t)bh * p.nch + c]);
+                for (int c = lane; c < n; c += 32)
+                    if (in_bounds((long long)bh * p.nch + c, 1, (long long)p.BH * p.nch, p.hdr, 201))
+                        x = fmaxf(x, p.kmax2[(size_t)bh * p.nch + c]);
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
                 if (lane == 0) *s_kmax2 = x;
             }
             float qn2 = 0.f;
-            if (row0 + r < p.L) {
+            if (row0 + r < p.L && in_bounds(((long long)bh * p.L + row0 + r) * D, D, n_bhl * D, p.hdr, 202)) {
                 const uint4* qv = reinterpret_cast<const uint4*>(p.q + ((size_t)bh * p.L + row0 + r) * D);
                 Vec16<__nv_bfloat16> v[D / 8];  // every load in flight before the first use
 #pragma unroll
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 sk_sent = it + 1;
             }
             if (r == 0) TC_TRACE(5, it);
-            if (FOX) {
+            if (FOX && in_bounds((long long)bh * p.Lp + m * kTcC, kTcC, n_bhlp, p.hdr, 203)) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const float4* cj = reinterpret_cast<const float4*>(cumh + m * kTcC + 32 * c);
@@ -433,7 +436,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            if (REL) {  // bias at distance i - j, clamped into the table (masked or padding entries)
+            if (REL && in_bounds((long long)(bh % p.H) * p.L, p.L, (long long)p.H * p.L, p.hdr, 204)) {
+                // bias at distance i - j, clamped into the table (masked or padding entries)
                 const int base = row0 + r - m * kTcC;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -467,7 +471,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (m > 0 && !p.no_skip) {
                     // Every key left of this block has bias <= c_i - c_(128 m - 1) and
                     // |logit| <= qk_bound: below m_true - 160 (log2) its exp2 is 0 in fp32.
-                    const float bound = qk_bound + (ci - cumh[m * kTcC - 1]) * kL2e - m_true;
+                    const float cprev = in_bounds((long long)bh * p.Lp + m * kTcC - 1, 1, n_bhlp, p.hdr, 205)
+                                            ? cumh[m * kTcC - 1] : ci;
+                    const float bound = qk_bound + (ci - cprev) * kL2e - m_true;
                     const bool sat = (row0 + r >= p.L) || bound < -160.0f;
                     const int vote = __all_sync(0xffffffffu, sat);
                     // Votes carry the iteration (2 (it + 1) + vote), double-buffered by
@@ -591,7 +597,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t ov[32];
                 tmem_ld32(tl + TM_O + 32 * c, ov);
                 tmem_wait_ld();
-                if (row < p.L) {
+                if (row < p.L && in_bounds(((long long)bh * p.L + row) * D + 32 * c, 32, n_bhl * D, p.hdr, 206)) {
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         uint4 v;
@@ -603,7 +609,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            if (p.lse && row < p.L) p.lse[(size_t)bh * p.L + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
+            if (p.lse && row < p.L && in_bounds((long long)bh * p.L + row, 1, n_bhl, p.hdr, 207))
+                p.lse[(size_t)bh * p.L + row] = (m_run + log2f(l_run)) * 0.6931471805599453f;
             if (r == 0) atomicAdd(p.visited, (unsigned)(last + 1));
         }
     } else {
@@ -652,7 +659,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int st = 1;
         if (ok) {
             // qhat (fp32) of this row becomes the q~ master and its bf16 copy
-            const float4* src = reinterpret_cast<const float4*>(p.qhat + ((size_t)bh * p.Lp + row0 + r) * D);
+            const bool src_ok =
+                in_bounds(((long long)bh * p.Lp + row0 + r) * D, D, (long long)p.BH * p.Lp * D, p.hdr, 208);
+            const float4* src = reinterpret_cast<const float4*>(p.qhat + (src_ok ? ((size_t)bh * p.Lp + row0 + r) * D : 0));
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];

@@ -82,7 +82,7 @@ static_assert(B_COUNT * 8 <= RB_SLOT && RB_SLOT + 8 <= 256, "barriers overlap th
 #endif
 
 struct UtParams {
-    int L, Lp;
+    int L, Lp, BH;
     const float* beta;           // [BH, L]
     const __nv_bfloat16* q;      // [BH, L, d] (row reads for the "Q -" epilogue)
     const __nv_bfloat16* k;
@@ -474,7 +474,10 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         float* sT = reinterpret_cast<float*>(sm + RT);
         uint8_t* opHi = sm + R3;
         uint8_t* opLo = sm + R3 + 32768;
-        if (h == 0) sBeta[r] = grow < p.L ? p.beta[(size_t)bh * p.L + grow] : 0.f;
+        const long long n_bhl = (long long)p.BH * p.L;
+        if (h == 0)
+            sBeta[r] = grow < p.L && in_bounds((long long)bh * p.L + grow, 1, n_bhl, p.hdr, 210)
+                           ? p.beta[(size_t)bh * p.L + grow] : 0.f;
         if (D == 64) {  // rows 64-127 of the W^T view (the unused second box of the W tile) read as zero
             uint4* z = reinterpret_cast<uint4*>(sm + R0 + 16384);
             for (int i = t; i < 16384 / 16; i += kCompute) z[i] = make_uint4(0, 0, 0, 0);
@@ -570,7 +573,8 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) v8[e] = -__uint_as_float(v[8 * g + e]);
                     stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(v8));
-                    if (p.vfac) {  // the prefill hand-off's key-side factor V
+                    if (p.vfac && in_bounds((long long)ws_row * D + col + 8 * g, 8, (long long)p.BH * p.Lp * D, p.hdr,
+                                            213)) {  // the prefill hand-off's key-side factor V
 #pragma unroll
                         for (int e = 0; e < 8; ++e) v8[e] = -v8[e];
                         st_global_v4(p.vfac + ws_row * D + col + 8 * g, pack8(v8));
@@ -603,7 +607,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             const __nv_bfloat16* qrow = p.q + ((size_t)bh * p.L + grow) * D;
 #pragma unroll
             for (int i = 0; i < D / 16; ++i)
-                qpre[i] = (ok && grow < p.L) ? ld_global_nc_v4(qrow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
+                qpre[i] = (ok && grow < p.L &&
+                           in_bounds(((long long)bh * p.L + grow) * D + (D / 2) * h + 8 * i, 8, n_bhl * D, p.hdr, 211))
+                              ? ld_global_nc_v4(qrow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
         }
         // qhat = Q - Y W (fp32, Y W in TMEM at T384), columns 32c .. 32c+31 of this
         // thread's half, into a staging tile laid out as two 32-column boxes
@@ -718,7 +724,9 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             const __nv_bfloat16* krow = p.k + ((size_t)bh * p.L + grow) * D;
 #pragma unroll
             for (int i = 0; i < D / 16; ++i)
-                kpre[i] = (ok && grow < p.L) ? ld_global_nc_v4(krow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
+                kpre[i] = (ok && grow < p.L &&
+                           in_bounds(((long long)bh * p.L + grow) * D + (D / 2) * h + 8 * i, 8, n_bhl * D, p.hdr, 212))
+                              ? ld_global_nc_v4(krow + (D / 2) * h + 8 * i) : make_uint4(0, 0, 0, 0);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_K), 0, wc, 54));
         if (t == 0) UT_TRACE(11);
@@ -758,7 +766,8 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     if (lane == 0) red[256 + (warp & 3)] = x;
                 }
                 named_bar_sync(1, kCompute);
-                if (t == 0) p.kmax2[(size_t)bh * p.nch + chunk] = fmaxf(fmaxf(red[256], red[257]), fmaxf(red[258], red[259]));
+                if (t == 0 && in_bounds((long long)bh * p.nch + chunk, 1, (long long)p.BH * p.nch, p.hdr, 214))
+                    p.kmax2[(size_t)bh * p.nch + chunk] = fmaxf(fmaxf(red[256], red[257]), fmaxf(red[258], red[259]));
             }
         }
     }
@@ -799,6 +808,7 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
     UtParams p;
     p.L = L;
     p.Lp = lay.Lp;
+    p.BH = BH;
     p.beta = beta;
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.k = static_cast<const __nv_bfloat16*>(k);

@@ -53,7 +53,9 @@ enum path_status {
     PATH_ERR_UNSUPPORTED = 2, /* valid request outside what is implemented (non-causal, d, dtype) */
     PATH_ERR_CUDA = 3,        /* the CUDA runtime reported an error */
     PATH_ERR_TIMEOUT = 4,     /* a device-side bounded wait expired (read via path_get_status) */
-    PATH_ERR_WORKSPACE = 5    /* workspace null or smaller than the *_workspace_bytes() value */
+    PATH_ERR_WORKSPACE = 5,   /* workspace null or smaller than the *_workspace_bytes() value */
+    PATH_ERR_BOUNDS = 6       /* a device-side index check failed (bounds-checked builds only, read via
+                                 path_get_status; the normal build has no such checks) */
 };
 
 enum path_dtype { PATH_F32 = 0, PATH_BF16 = 1 };

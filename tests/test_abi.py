@@ -71,6 +71,7 @@ def test_forward_argument_errors(lib):
     assert _fwd(lib, v=ctypes.c_void_p((1 << 20) + 4)) == P.PATH_ERR_INVALID  # misaligned
     assert _fwd(lib, ws_bytes=16) == P.PATH_ERR_WORKSPACE
     assert _fwd(lib, ws=None, ws_bytes=1 << 30) == P.PATH_ERR_WORKSPACE
+    assert _fwd(lib, B=300, H=300, L=1) == P.PATH_ERR_UNSUPPORTED  # B*H above the grid limit (65535)
     fox = lib.path_attn_fwd_fox(FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, 1, 1, 64, 16, P.PATH_F32, 1,
                                 ctypes.c_float(0.25), FAKE, 1 << 30, None)
     assert fox == P.PATH_ERR_INVALID  # log_f is required
@@ -129,6 +130,16 @@ def test_decode_argument_errors(lib):
     assert step(ws_bytes=8) == P.PATH_ERR_WORKSPACE
     assert lib.path_kcache_update(FAKE, 2, 3, 12, 11, 128, FAKE, FAKE, P.PATH_BF16, None) == P.PATH_ERR_INVALID
     assert lib.path_kcache_update(FAKE, 2, 3, 5, 11, 100, FAKE, FAKE, P.PATH_BF16, None) == P.PATH_ERR_UNSUPPORTED
+    # B*H goes on a grid dimension limited to 65535: rejected before any launch (d = 16 with a short cache
+    # would otherwise fit the no-alloc scratch too)
+    big = lib.path_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, FAKE, None, 256, 257, 16,
+                               ctypes.c_float(0.25), P.PATH_BF16, FAKE, 1 << 40, None)
+    assert big == P.PATH_ERR_UNSUPPORTED
+    assert lib.path_kcache_update(FAKE, 256, 257, 1, 2, 16, FAKE, FAKE, P.PATH_BF16, None) == P.PATH_ERR_UNSUPPORTED
+    assert lib.path_decode_step_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, FAKE, None, 256, 257, 16,
+                                        ctypes.c_float(0.25), P.PATH_BF16, None) == P.PATH_ERR_UNSUPPORTED
+    assert lib.path_prefill_kcache(FAKE, FAKE, FAKE, FAKE, 256, 257, 1, 1, 128, P.PATH_BF16, FAKE, 1 << 40,
+                                   None) == P.PATH_ERR_UNSUPPORTED
 
 
 def test_binding_refuses_cpu_tensors(lib):

@@ -114,3 +114,25 @@ def test_decode32k_full_size_sampled_heads():
                                                f(steps[4][:, b, h]), scale)
         check(to_np(o[:, b, h]), o_ref, torch.bfloat16, "decode32k head %d" % bh)
         check_lse(to_np(lse[:, b, h]), lse_ref, torch.bfloat16, "decode32k lse head %d" % bh)
+
+
+def test_kv_cache_checkpoint_and_resume_is_bit_identical():
+    """Checkpoint / resume ("Resumo Técnico: Atenção PaTH", §3 "Inferência": the transported key cache
+    and the value cache are the whole decoding state).  Decode 5 steps, copy both caches to host
+    memory, then continue 4 more steps twice: on the live caches, and on fresh device caches restored
+    from the host copy.  The continuations must agree bit for bit, outputs and caches."""
+    B, H, d, n0, T1, T2 = 2, 3, 128, 1500, 5, 4
+    kc, vc = inputs.make_decode_cache(B, H, n0, d, n0 + T1 + T2, "bf16", seed=44)
+    steps = [t.cuda() for t in inputs.make_decode_steps(B, H, d, T1 + T2, "bf16", seed=44)]
+    k, v = kc.cuda(), vc.cuda()
+    for t in range(T1):
+        P.path_decode_step(*(s[t] for s in steps), k, v, n0 + t)
+    torch.cuda.synchronize()
+    host_k, host_v = k.cpu(), v.cpu()  # the checkpoint
+    live = [P.path_decode_step(*(s[t] for s in steps), k, v, n0 + t) for t in range(T1, T1 + T2)]
+    k2, v2 = host_k.cuda(), host_v.cuda()  # resume on fresh buffers
+    resumed = [P.path_decode_step(*(s[t] for s in steps), k2, v2, n0 + t) for t in range(T1, T1 + T2)]
+    torch.cuda.synchronize()
+    for a, b in zip(live, resumed):
+        assert torch.equal(a, b)
+    assert torch.equal(k, k2) and torch.equal(v, v2)
