@@ -510,29 +510,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool rescale = m_new > m_run + 8.0f;
             const float m_use = rescale ? m_new : m_run;
             const float alpha = rescale ? ex2_approx(m_run - m_use) : 1.0f;
-            // Probes of the two barriers P V(it) waits behind, issued before the last
-            // exponentials so their shared-memory round trip overlaps them; a
-            // blocking wait follows only if a probe saw the phase incomplete.
-            bool od_ready = it == 0, v_ready = false;
+            // P and O are single-buffered: the previous block's P V must have completed
+            // before P is rewritten and O rescaled; waiting here, before the
+            // exponentials, lets P go to TMEM 32 columns at a time as it is formed
+            // (fewer live registers than holding the whole row).
+            if (it > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ODONE), (uint32_t)((it - 1) & 1), wc, 21));
+                if (!ok) break;
+                if (r == 0) TC_TRACE(11, it);
+                tc_fence_after();
+            }
+            // V_m of this block is probed mid-loop so its shared-memory round trip
+            // overlaps the exponentials; a blocking wait follows only if not ready.
+            bool v_ready = false;
             uint64_t psum[4];  // packed partial row sums (8 chains)
 #pragma unroll
             for (int u = 0; u < 4; ++u) psum[u] = 0ull;
-            uint32_t pk[64];
             const float neg_m = -m_use;
             const uint64_t nm2 = f32x2(neg_m, neg_m), sl2x2 = f32x2(sl2, sl2);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                if (j == 40) {
-                    if (it > 0) od_ready = mbar_test_wait(bar(B_ODONE), (uint32_t)((it - 1) & 1));
-                    v_ready = mbar_test_wait(bar(B_VFULL0 + (it & 1)), (uint32_t)(v_use(it) & 1));
+            for (int c = 0; c < 4; ++c) {
+                if (c == 2) v_ready = mbar_test_wait(bar(B_VFULL0 + (it & 1)), (uint32_t)(v_use(it) & 1));
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = 16 * c + jj;
+                    const uint64_t sv = f32x2(s[2 * j], s[2 * j + 1]);
+                    const uint64_t xv = BIASED ? add_f32x2(sv, nm2) : fma_f32x2(sv, sl2x2, nm2);
+                    float x0, x1;
+                    f32x2_split(xv, x0, x1);
+                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    psum[jj & 3] = add_f32x2(psum[jj & 3], f32x2(p0, p1));
+                    pk[jj] = pack_bf16x2(p0, p1);
                 }
-                const uint64_t sv = f32x2(s[2 * j], s[2 * j + 1]);
-                const uint64_t xv = BIASED ? add_f32x2(sv, nm2) : fma_f32x2(sv, sl2x2, nm2);
-                float x0, x1;
-                f32x2_split(xv, x0, x1);
-                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                psum[j & 3] = add_f32x2(psum[j & 3], f32x2(p0, p1));
-                pk[j] = pack_bf16x2(p0, p1);
+                tmem_st16(tl + TM_P + 16 * c, pk);
             }
             float sum;
             {
@@ -543,30 +554,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             l_run = l_run * alpha + sum;
             if (r == 0) TC_TRACE(6, it);
-            // P and O are single-buffered: the previous block's P V must have completed
-            // before P is rewritten and O rescaled.  The rescale uses warp-collective
-            // TMEM loads/stores, so the whole warp takes it when any of its rows needs
-            // it (alpha = 1 elsewhere).
-            if (it > 0) {
-                ok = __all_sync(0xffffffffu, od_ready || mbar_wait(bar(B_ODONE), (uint32_t)((it - 1) & 1), wc, 21));
-                if (!ok) break;
-                if (r == 0) TC_TRACE(11, it);
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
+            // The O rescale (rare: the running max grew by more than 2^8) uses
+            // warp-collective TMEM loads/stores, so the whole warp takes it when any
+            // of its rows needs it (alpha = 1 elsewhere).
+            if (it > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(tl + TM_O + 32 * c, ov);
-                        tmem_wait_ld();
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tl + TM_O + 32 * c, ov);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-                        tmem_st32(tl + TM_O + 32 * c, ov);
-                    }
+                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+                    tmem_st32(tl + TM_O + 32 * c, ov);
                 }
             }
             m_run = m_use;
-            tmem_st32(tl + TM_P, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-            tmem_st32(tl + TM_P + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
             tmem_wait_st();
             // V_m of this block has landed before P V may go
             ok = __all_sync(0xffffffffu,

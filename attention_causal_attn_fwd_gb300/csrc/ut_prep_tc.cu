@@ -18,11 +18,12 @@
 // Operands that are not exact in bf16 (A, tril(QW^T), Y, Z, ZA) are split
 // into hi + lo bf16 parts and multiplied term by term (hi*hi + hi*lo + lo*hi),
 // which keeps those products close to fp32 accuracy; -V enters P - I as one
-// bf16 operand (P - I is itself stored in bf16).  The unit upper-
-// triangular inverse X = (I + D triu_1(G))^{-1} (A = X D) is solved in fp32 on
-// CUDA cores, blocked: 16 x 16 diagonal blocks by back substitution, then
-// three doubling merges X_PQ = -X_PP (D G)_PQ X_QQ on a dense copy of X kept
-// in the shared memory that held Q and K.
+// bf16 operand (P - I is itself stored in bf16).  A = X D with the unit upper-
+// triangular X = (I + D triu_1(G))^{-1} is solved in fp32 on CUDA cores,
+// blocked: the 16 x 16 diagonal blocks of X by back substitution, scaled by D
+// into those of A, then three doubling merges A_PQ = -A_PP G_PQ A_QQ (which
+// is X_PQ D_Q for X_PQ = -X_PP D_P G_PQ X_QQ) on a dense copy of A kept in the
+// shared memory that held Q and K.
 //
 // One shared-memory layout — rows of 64-element, 128-byte-swizzled chunks,
 // exactly what a TMA box {64, 128} writes — serves as a K-major operand, an
@@ -66,7 +67,7 @@ constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 // 1 P - I (staging tile, which held -V as the operand of P - I); 2 -Z (R3),
 // qhat columns 0-31 of each half (staging tile); 3 qhat columns 32-63
 // (d = 128; R1, free once Z A has completed); last khat (R2, likewise free).
-enum { B_LOAD = 0, B_G, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN,
+enum { B_LOAD = 0, B_G, B_QK, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN,
        B_STG0, B_STG1, B_STG2, B_STG3, B_STG4, B_FREE0, B_FREE1, B_FREE2, B_FREE3, B_FREE4, B_COUNT };
 constexpr uint32_t RB_SLOT = 200;  // TMEM address and abort flag after the barriers
 static_assert(B_COUNT * 8 <= RB_SLOT && RB_SLOT + 8 <= 256, "barriers overlap the TMEM slot, abort flag or beta");
@@ -113,12 +114,12 @@ __device__ __forceinline__ void stage16(uint8_t* base, int r, int box, int g, ui
                               ((uint32_t)((g & 7) ^ (r & 7)) << 4)) = v;
 }
 
-// One doubling merge of the blocked inverse, for 256 threads t: for each pair
-// of S-blocks (P, Q = P + S) on the diagonal,
-//     T    = (D G)_PQ X_QQ
-//     X_PQ = -X_PP T
-// with X dense (zeros below the diagonal, ones on it), so the products are
-// plain register-tiled loops.  The k loop takes 4 steps at a time so that
+// One doubling merge of the blocked factor A = X D, for 256 threads t: for each
+// pair of S-blocks (P, Q = P + S) on the diagonal,
+//     T    = G_PQ A_QQ
+//     A_PQ = -A_PP T
+// with A dense (zeros below the diagonal), so the products are plain
+// register-tiled loops.  The k loop takes 4 steps at a time so that
 // every operand is read as 16- or 8-byte row segments (rows of G, X and T
 // start on 16-byte boundaries): 2 x (TM + 4) vector loads per 4 x TM x TN FMAs.
 template <int TN>
@@ -133,7 +134,7 @@ __device__ __forceinline__ void ld_row(float (&dst)[TN], const float* src) {
     }
 }
 template <int S, int TM, int TN>
-__device__ __forceinline__ void merge_level(const float* sG, const float* sB, float* sX, float* sT, int t) {
+__device__ __forceinline__ void merge_level(const float* sG, float* sX, float* sT, int t) {
     using namespace utk;
     constexpr int NP = C / (2 * S);
     constexpr int TR = S / TM, TC = S / TN;
@@ -164,7 +165,7 @@ __device__ __forceinline__ void merge_level(const float* sG, const float* sB, fl
 #pragma unroll
     for (int u = 0; u < TM; ++u)
 #pragma unroll
-        for (int v = 0; v < TN; ++v) sT[(p * S + i0 + u) * LDT + j0 + v] = sB[P + i0 + u] * acc[u][v];
+        for (int v = 0; v < TN; ++v) sT[(p * S + i0 + u) * LDT + j0 + v] = acc[u][v];
     named_bar_sync(1, kCompute);
 #pragma unroll
     for (int u = 0; u < TM; ++u)
@@ -192,14 +193,14 @@ __device__ __forceinline__ void merge_level(const float* sG, const float* sB, fl
 }
 
 // The same merge without the zero halves of the triangular factors:
-// T = (D G)_PQ X_QQ needs only k <= j and X_PQ = -X_PP T only k >= i (both X
+// T = G_PQ A_QQ needs only k <= j and A_PQ = -A_PP T only k >= i (both A
 // blocks are upper triangular).  Pass 1 gives each warp WC adjacent column
 // tiles and pass 2 WR adjacent row tiles, so a warp's k range is uniform; the
 // two warps that share a scheduler (compute warps cw and cw + 4) get
 // complementary ranges.  G is symmetric, so the G column needed for row
 // segment i0.. is read as 16- or 8-byte segments of row Q + k.
 template <int S, int TM, int TN>
-__device__ __forceinline__ void merge_level_tri(const float* sG, const float* sB, float* sX, float* sT, int t) {
+__device__ __forceinline__ void merge_level_tri(const float* sG, float* sX, float* sT, int t) {
     using namespace utk;
     constexpr int NP = C / (2 * S);
     constexpr int TR = S / TM, TC = S / TN;
@@ -212,7 +213,7 @@ __device__ __forceinline__ void merge_level_tri(const float* sG, const float* sB
     const int wp = cw < 4 ? cw % WPP : WPP - 1 - (cw - 4) % WPP;
     const int P = 2 * pr * S, Q = P + S;
     float acc[TM][TN];
-    {  // pass 1: T = (D G)_PQ X_QQ over k < kend
+    {  // pass 1: T = G_PQ A_QQ over k < kend
         const int i0 = (lane % TR) * TM, j0 = (wp * WC + lane / TR) * TN;
         const int kend = (wp + 1) * WC * TN;
 #pragma unroll
@@ -236,10 +237,10 @@ __device__ __forceinline__ void merge_level_tri(const float* sG, const float* sB
 #pragma unroll
         for (int u = 0; u < TM; ++u)
 #pragma unroll
-            for (int v = 0; v < TN; ++v) sT[(pr * S + i0 + u) * LDT + j0 + v] = sB[P + i0 + u] * acc[u][v];
+            for (int v = 0; v < TN; ++v) sT[(pr * S + i0 + u) * LDT + j0 + v] = acc[u][v];
     }
     named_bar_sync(1, kCompute);
-    {  // pass 2: X_PQ = -X_PP T over k >= kbeg
+    {  // pass 2: A_PQ = -A_PP T over k >= kbeg
         const int i0 = (wp * WR + lane / TC) * TM, j0 = (lane % TC) * TN;
         const int kbeg = wp * WR * TM;
 #pragma unroll
@@ -269,9 +270,9 @@ __device__ __forceinline__ void merge_level_tri(const float* sG, const float* sB
 }
 
 // The 16 x 16 diagonal blocks of X = (I + D triu_1(G))^{-1} (unit upper
-// triangular) by back substitution into the dense, zeroed sX [128][128], for
-// 256 threads t (the merges above then fill the rest); sG holds G (upper
-// part read).
+// triangular) by back substitution, written as those of A = X D (column j
+// scaled by beta_j) into the dense, zeroed sX [128][128], for 256 threads t
+// (the merges above then fill the rest); sG holds G (upper part read).
 __device__ __forceinline__ void solve_diag_blocks(const float* sG, const float* sB, float* sX, int t) {
     using namespace utk;
     if (t < 128) {  // 16 x 16 diagonal blocks: thread (block I, column j) back-substitutes its column
@@ -287,9 +288,10 @@ __device__ __forceinline__ void solve_diag_blocks(const float* sG, const float* 
             const float val = -sB[b0 + i] * acc;
             if (i < j) x[i] = val;
         }
+        const float bj = sB[b0 + j];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            if (i <= j) sX[(b0 + i) * C + b0 + j] = x[i];
+            if (i <= j) sX[(b0 + i) * C + b0 + j] = x[i] * bj;
     }
     named_bar_sync(1, kCompute);
 }
@@ -386,13 +388,16 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             UT_TRACE(13);
             if (ok) {
                 tc_fence_after();
-                for (int kk = 0; kk < D / 16; ++kk) {  // G = W W^T, Q W^T, K W^T
+                // G = W W^T first, on its own barrier (the solve needs only G), then Q W^T, K W^T
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + T0, kmajor_desc(sb + R0, kk, 16384), kmajor_desc(sb + R0, kk, 16384), ID_KK128, kk > 0);
+                mma_commit(bar(B_G));
+                for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t bw = kmajor_desc(sb + R0, kk, 16384);
-                    mma_ss(tmem + T0, kmajor_desc(sb + R0, kk, 16384), bw, ID_KK128, kk > 0);
                     mma_ss(tmem + T128, kmajor_desc(sb + R1, kk, 16384), bw, ID_KK128, kk > 0);
                     mma_ss(tmem + T256, kmajor_desc(sb + R2, kk, 16384), bw, ID_KK128, kk > 0);
                 }
-                mma_commit(bar(B_G));
+                mma_commit(bar(B_QK));
                 UT_TRACE(14);
                 ok = mbar_wait(bar(B_OPS1), 0, wc, 41);
                 UT_TRACE(15);
@@ -500,7 +505,11 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                         make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
                                     __uint_as_float(v[j + 3]));
             }
-            {  // Q and K are consumed: zero the dense X
+            // Q and K (under the dense A) must be consumed by Q W^T and K W^T first
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QK), 0, wc, 58));
+        }
+        if (ok) {
+            {  // zero the dense A
                 float4* x4 = reinterpret_cast<float4*>(sX);
                 for (int i = t; i < C * C / 4; i += kCompute) x4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -508,13 +517,13 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             if (t == 0) UT_TRACE(2);
             solve_diag_blocks(sG, sBeta, sX, t);
             if (t == 0) UT_TRACE(23);
-            merge_level<16, 2, 2>(sG, sBeta, sX, sT, t);
+            merge_level<16, 2, 2>(sG, sX, sT, t);
             if (t == 0) UT_TRACE(24);
-            merge_level_tri<32, 2, 4>(sG, sBeta, sX, sT, t);
+            merge_level_tri<32, 2, 4>(sG, sX, sT, t);
             if (t == 0) UT_TRACE(25);
-            merge_level_tri<64, 4, 4>(sG, sBeta, sX, sT, t);
+            merge_level_tri<64, 4, 4>(sG, sX, sT, t);
             if (t == 0) UT_TRACE(3);
-            // A = X D as hi/lo bf16 tiles.  The tiles overwrite the dense X, so
+            // A as hi/lo bf16 tiles.  The tiles overwrite the dense A, so
             // each thread first reads its 8 granules (8 consecutive columns of
             // one row; consecutive threads walk along a row, free of bank
             // conflicts) into registers, then writes them after a barrier.
@@ -527,7 +536,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     const float4 x1 = *reinterpret_cast<const float4*>(sX + row * C + 8 * G + 4);
                     const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) a[i][e] = xv[e] * sBeta[8 * G + e];
+                    for (int e = 0; e < 8; ++e) a[i][e] = xv[e];
                 }
                 named_bar_sync(1, kCompute);
 #pragma unroll

@@ -153,3 +153,30 @@ def test_blocked_prefill_cache_matches_walks():
         for t in range(j + 1, L):
             x = x - beta[t] * (w[t] @ x) * w[t]
         np.testing.assert_allclose(cache[j], x, rtol=0, atol=1e-12)
+
+
+def test_blocked_ut_factor_by_doubling_merges():
+    """The UT prep's blocked A = (I + D triu_1(G))^{-1} D: 16 x 16 diagonal blocks of X by back
+    substitution scaled by D, then doubling merges A_PQ = -A_PP G_PQ A_QQ at block sizes 16, 32, 64
+    (which is X_PQ D_Q for X_PQ = -X_PP D_P G_PQ X_QQ) equal the direct solve, with beta = 0 and
+    beta = 2 positions."""
+    rng = np.random.default_rng(23)
+    C, d = 128, 32
+    w = rng.standard_normal((C, d))
+    w /= np.linalg.norm(w, axis=1, keepdims=True)
+    beta = 2.0 / (1.0 + np.exp(-rng.standard_normal(C)))
+    beta[[3, 40, 77]] = 0.0
+    beta[[5, 64, 100]] = 2.0
+    G = w @ w.T
+    D = np.diag(beta)
+    A_ref = np.linalg.solve(np.eye(C) + D @ np.triu(G, 1), D)
+    A = np.zeros((C, C))
+    for b in range(0, C, 16):
+        blk = slice(b, b + 16)
+        X = np.linalg.inv(np.eye(16) + np.diag(beta[blk]) @ np.triu(G[blk, blk], 1))
+        A[blk, blk] = X @ np.diag(beta[blk])
+    for S in (16, 32, 64):
+        for P0 in range(0, C, 2 * S):
+            P, Q = slice(P0, P0 + S), slice(P0 + S, P0 + 2 * S)
+            A[P, Q] = -A[P, P] @ G[P, Q] @ A[Q, Q]
+    np.testing.assert_allclose(A, A_ref, rtol=0, atol=1e-12)
