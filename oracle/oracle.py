@@ -57,12 +57,16 @@ def _load():
             lib.path_oracle_fwd_rows.restype = None
             lib.path_oracle_fwd_rows_relbias.argtypes = lib.path_oracle_fwd_rows.argtypes
             lib.path_oracle_fwd_rows_relbias.restype = None
+            lib.path_oracle_fwd_rows_vt.argtypes = lib.path_oracle_fwd_rows.argtypes
+            lib.path_oracle_fwd_rows_vt.restype = None
             lib.path_oracle_logits.argtypes = [_dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_double, _dp]
             lib.path_oracle_logits.restype = None
             lib.path_oracle_decode.argtypes = [_dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _dp, _dp,
                                                _dp, _dp, _dp, ctypes.c_int, ctypes.c_double, _dp, _dp]
             lib.path_oracle_decode.restype = None
+            lib.path_oracle_decode_vt.argtypes = lib.path_oracle_decode.argtypes
+            lib.path_oracle_decode_vt.restype = None
             lib.path_oracle_kcache_update.argtypes = [_dp, ctypes.c_int, ctypes.c_int, _dp, ctypes.c_double]
             lib.path_oracle_kcache_update.restype = None
             lib.path_oracle_bwd.argtypes = [_dp] * 7 + [ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -87,7 +91,7 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(_dp)
 
 
-def path_attn(q, k, v, w, beta, log_f=None, scale=None, rows=None, rel_bias=None):
+def path_attn(q, k, v, w, beta, log_f=None, scale=None, rows=None, rel_bias=None, value_transport=False):
     """Causal PaTH(-FoX) attention in fp64.
 
     q, k, v, w: [..., L, d]; beta, log_f: [..., L].  Leading dims are flattened
@@ -99,6 +103,10 @@ def path_attn(q, k, v, w, beta, log_f=None, scale=None, rows=None, rel_bias=None
     unscaled to the logit of (i, j): a relative-position prior such as GGD-BAM's
     ("Resumo Técnico: Mecanismo de Atenção Bayesiana (BAM)", §"Solução Proposta:
     GGD-BAM") or ALiBi's, on top of the PaTH logits.
+
+    ``value_transport`` (exclusive with rel_bias) carries every value along the route to its query:
+    o_i = sum_j alpha_ij H_i ... H_{j+1} v_j ("Resumo Técnico: Por que Transformações Acumuladas
+    Extrapolam?", §"Principais Contribuições" 3 "Proteção do Lado de Valor").
     """
     q, k, v, w, beta = (_f64(x) for x in (q, k, v, w, beta))
     lf = None if log_f is None else _f64(log_f)
@@ -116,7 +124,10 @@ def path_attn(q, k, v, w, beta, log_f=None, scale=None, rows=None, rel_bias=None
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     lib = _load()
+    assert not (value_transport and rb is not None), "value transport takes no relative bias"
     fn, extra = (lib.path_oracle_fwd_rows, lf) if rb is None else (lib.path_oracle_fwd_rows_relbias, rb)
+    if value_transport:
+        fn = lib.path_oracle_fwd_rows_vt
     if rows is None:
         n = BH * L
         o = np.empty((n, d))
@@ -143,11 +154,13 @@ def path_logits(q, k, w, beta, log_f=None, scale=1.0):
     return S
 
 
-def path_decode(kc0, vc0, q, k, v, w, beta, scale):
+def path_decode(kc0, vc0, q, k, v, w, beta, scale, value_transport=False):
     """Decode T steps of ONE head from a cache of n0 transported keys.
 
     kc0, vc0: [n0, d]; q, k, v, w: [T, d]; beta: [T].  Returns (o [T, d],
-    lse [T], kc [n0+T, d], vc [n0+T, d]) where kc holds the final transported keys.
+    lse [T], kc [n0+T, d], vc [n0+T, d]) where kc holds the final transported keys
+    (and, with ``value_transport``, vc the transported values, vc0 being values
+    already carried to the cache's position).
     """
     kc0, vc0, q, k, v, w, beta = (_f64(x) for x in (kc0, vc0, q, k, v, w, beta))
     n0, d = kc0.shape
@@ -158,8 +171,9 @@ def path_decode(kc0, vc0, q, k, v, w, beta, scale):
     vc[:n0] = vc0
     o = np.empty((T, d))
     lse = np.empty(T)
-    _load().path_oracle_decode(_ptr(kc), _ptr(vc), n0, n0 + T, d, _ptr(q), _ptr(k), _ptr(v), _ptr(w),
-                               _ptr(beta), T, float(scale), _ptr(o), _ptr(lse))
+    fn = _load().path_oracle_decode_vt if value_transport else _load().path_oracle_decode
+    fn(_ptr(kc), _ptr(vc), n0, n0 + T, d, _ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), T, float(scale),
+       _ptr(o), _ptr(lse))
     return o, lse, kc, vc
 
 

@@ -201,6 +201,94 @@ void path_oracle_decode(double* kc, double* vc, int n0, int n_max, int d,
     free(s);
 }
 
+/*
+ * Value-side transport ("Resumo Técnico: Por que Transformações Acumuladas
+ * Extrapolam?", §"Metodologia" 1: the route transport P_{j->i} is the product of
+ * the per-token steps from source j to query i; §"Principais Contribuições" 3
+ * "Proteção do Lado de Valor": the same accumulated route transport applied to
+ * the values).  With PaTH's steps the route operator that carries key j to
+ * query i in the logit is P_{j->i} = H_i ... H_{j+1} (s_ij = q_i . P_{j->i} k_j,
+ * since every H_s is symmetric), so
+ *     o_i = sum_j alpha_ij P_{j->i} v_j,   alpha_ij = softmax_j(s_i.)
+ * with the logits (and FoX bias) of the plain forward.  Evaluated left to right:
+ *     acc <- alpha_i0 v_0;  for j = 1..i: acc <- H_j acc + alpha_ij v_j;  o_i = acc
+ * (after step j, acc holds sum_{j' <= j} alpha_ij' H_j ... H_{j'+1} v_j').
+ */
+static double vt_combine(const double* s, const double* v, const double* w, const double* beta, int n, int d,
+                         double* o) {
+    double m = -INFINITY;
+    for (int j = 0; j < n; ++j) m = s[j] > m ? s[j] : m;
+    double l = 0.0;
+    for (int j = 0; j < n; ++j) l += exp(s[j] - m);
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    for (int j = 0; j < n; ++j) {
+        if (j > 0) apply_transition(o, w + (size_t)j * d, beta[j], d);
+        const double a = exp(s[j] - m) / l;
+        const double* vj = v + (size_t)j * d;
+        for (int c = 0; c < d; ++c) o[c] += a * vj[c];
+    }
+    return m + log(l);
+}
+
+/* As path_oracle_fwd_rows, with value-side transport (log_f may be NULL). */
+void path_oracle_fwd_rows_vt(const double* q, const double* k, const double* v,
+                             const double* w, const double* beta, const double* log_f,
+                             int BH, int L, int d, double scale,
+                             const int64_t* rows, int64_t n_rows,
+                             double* o_rows, double* lse_rows) {
+    (void)BH;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        double* u = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            int64_t gi = rows ? rows[r] : r;
+            int64_t bh = gi / L;
+            int i = (int)(gi % L);
+            size_t hoff = (size_t)bh * (size_t)L;
+            row_logits(q + (size_t)gi * d, k + hoff * d, w + hoff * d, beta + hoff,
+                       log_f ? log_f + hoff : NULL, NULL, i, d, scale, s, u);
+            double lse = vt_combine(s, v + hoff * d, w + hoff * d, beta + hoff, i + 1, d,
+                                    o_rows + (size_t)r * d);
+            if (lse_rows) lse_rows[r] = lse;
+        }
+        free(s);
+        free(u);
+    }
+}
+
+/*
+ * Decode for ONE head with value-side transport: as path_oracle_decode, and the
+ * value cache is transported in place with the keys (v~_j = H_{t-1} ... H_{j+1} v_j,
+ * the values carried to the current position along the same route), so
+ * o_t = softmax_j(scale q_p . k~_j) v~_j over j = 0..p.
+ */
+void path_oracle_decode_vt(double* kc, double* vc, int n0, int n_max, int d,
+                           const double* q, const double* k, const double* v,
+                           const double* w, const double* beta, int T, double scale,
+                           double* o, double* lse) {
+    (void)n_max;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(n0 + T));
+    for (int t = 0; t < T; ++t) {
+        int p = n0 + t;
+        const double* wt = w + (size_t)t * d;
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j < p; ++j) {
+            apply_transition(kc + (size_t)j * d, wt, beta[t], d);
+            apply_transition(vc + (size_t)j * d, wt, beta[t], d);
+        }
+        memcpy(kc + (size_t)p * d, k + (size_t)t * d, sizeof(double) * (size_t)d);
+        memcpy(vc + (size_t)p * d, v + (size_t)t * d, sizeof(double) * (size_t)d);
+        const double* qt = q + (size_t)t * d;
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j <= p; ++j) s[j] = scale * dot(kc + (size_t)j * d, qt, d);
+        double l = softmax_combine(s, vc, p + 1, d, o + (size_t)t * d);
+        if (lse) lse[t] = l;
+    }
+    free(s);
+}
+
 /* The in-place key update alone: k~_j <- (I - beta w w^T) k~_j for j < n. */
 void path_oracle_kcache_update(double* kc, int n, int d, const double* w, double beta) {
 #pragma omp parallel for schedule(static)
