@@ -11,7 +11,8 @@ Functions keep the C names:
 - ``path_attn_fwd(q, k, v, w, beta, scale=None, lse=False)``
 - ``path_attn_fwd_fox(q, k, v, w, beta, log_f, scale=None, lse=False)``
 - ``path_attn_fwd_relbias(q, k, v, w, beta, rel_bias, scale=None, lse=False)``
-- ``path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, scale=None)``
+- ``path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, scale=None, value_transport=False)``
+- ``path_attn_fwd_vt(q, k, v, w, beta, log_f=None, scale=None, lse=False)`` (value-side transport)
 - ``path_kcache_update(kcache, n_cached, w_t, beta_t)``
 - ``path_get_status(workspace)``, ``path_fwd_visited_blocks(workspace)``, ``path_attn_workspace_bytes(...)``,
   ``path_decode_workspace_bytes(...)``
@@ -37,7 +38,8 @@ EXPORTED = ("path_version", "path_status_string", "path_attn_workspace_bytes", "
             "path_attn_fwd_fox", "path_decode_workspace_bytes", "path_kcache_update", "path_decode_step",
             "path_get_status", "path_debug_set_fault", "path_debug_set_timing_events", "path_decode_step_noalloc",
             "path_prefill_workspace_bytes", "path_prefill_kcache", "path_attn_fwd_relbias",
-            "path_attn_bwd_workspace_bytes", "path_attn_bwd", "path_fwd_visited_blocks", "path_debug_set_fox_skip")
+            "path_attn_bwd_workspace_bytes", "path_attn_bwd", "path_fwd_visited_blocks", "path_debug_set_fox_skip",
+            "path_decode_step_vt", "path_attn_fwd_vt_workspace_bytes", "path_attn_fwd_vt")
 
 
 class PathLibraryError(RuntimeError):
@@ -91,6 +93,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.path_decode_step.argtypes = [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _i, _i, _vp, _fp, _i, _i, _i,
                                      ctypes.c_float, _i, _vp, _sz, _vp]
     lib.path_decode_step.restype = _i
+    lib.path_decode_step_vt.argtypes = lib.path_decode_step.argtypes
+    lib.path_decode_step_vt.restype = _i
+    lib.path_attn_fwd_vt_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+    lib.path_attn_fwd_vt_workspace_bytes.restype = _sz
+    lib.path_attn_fwd_vt.argtypes = lib.path_attn_fwd_fox.argtypes
+    lib.path_attn_fwd_vt.restype = _i
     lib.path_decode_step_noalloc.argtypes = [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _i, _i, _vp, _fp, _i, _i, _i,
                                              ctypes.c_float, _i, _vp]
     lib.path_decode_step_noalloc.restype = _i
@@ -213,6 +221,34 @@ def path_attn_fwd_relbias(q, k, v, w, beta, rel_bias, scale=None, lse=False, out
     return _fwd(q, k, v, w, beta, None, scale, lse, out, workspace, rel_bias=rel_bias)
 
 
+def path_attn_fwd_vt(q, k, v, w, beta, log_f=None, scale=None, lse=False, out=None, workspace=None):
+    """PaTH(-FoX) forward with value-side transport: o_i = sum_j softmax_j(s_i.) H_i ... H_{j+1} v_j."""
+    lib = load()
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, L, d]")
+    B, H, L, d = q.shape
+    dt = q.dtype
+    if dt not in _DT:
+        raise ValueError("dtype must be float32 or bfloat16")
+    for name, t in (("q", q), ("k", k), ("v", v), ("w", w)):
+        _dev(t, name, dt, (B, H, L, d))
+    _dev(beta, "beta", torch.float32, (B, H, L))
+    if log_f is not None:
+        _dev(log_f, "log_f", torch.float32, (B, H, L))
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else _dev(out, "out", dt, (B, H, L, d))
+    lse_t = torch.empty((B, H, L), dtype=torch.float32, device=q.device) if lse else None
+    need = lib.path_attn_fwd_vt_workspace_bytes(B, H, L, d, _DT[dt])
+    if need == 0:
+        raise PathError(PATH_ERR_UNSUPPORTED, "path_attn_fwd_vt")
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    _check(lib.path_attn_fwd_vt(_ptr(q), _ptr(k), _ptr(v), _ptr(w), _ptr(beta), _ptr(log_f), _ptr(o), _ptr(lse_t),
+                                B, H, L, d, _DT[dt], 1, ctypes.c_float(scale), _ptr(workspace), workspace.numel(),
+                                _stream()), "path_attn_fwd_vt")
+    return (o, lse_t) if lse else o
+
+
 def path_attn_bwd_workspace_bytes(B: int, H: int, L: int, d: int, dtype: torch.dtype) -> int:
     return int(load().path_attn_bwd_workspace_bytes(B, H, L, d, _DT[dtype]))
 
@@ -292,8 +328,10 @@ def path_kcache_update(kcache, n_cached: int, w_t, beta_t):
 
 
 def path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached: int, scale=None, out=None,
-                     lse=False, workspace=None):
-    """One decode step for all heads; updates kcache/vcache in place and returns o_t [B, H, d]."""
+                     lse=False, workspace=None, value_transport=False):
+    """One decode step for all heads; updates kcache/vcache in place and returns o_t [B, H, d].
+
+    value_transport=True calls path_decode_step_vt: the value cache is transported in place with the keys."""
     lib = load()
     B, H, n_max, d = kcache.shape
     dt = kcache.dtype
@@ -307,10 +345,11 @@ def path_decode_step(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached: int, 
     lse_t = torch.empty((B, H), dtype=torch.float32, device=q_t.device) if lse else None
     if workspace is None:
         workspace = alloc_workspace(lib.path_decode_workspace_bytes(B, H, n_max, d), q_t.device)
-    _check(lib.path_decode_step(_ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(kcache),
-                                _ptr(vcache), int(n_cached), n_max, _ptr(o), _ptr(lse_t), B, H, d,
-                                ctypes.c_float(scale), _DT[dt], _ptr(workspace), workspace.numel(), _stream()),
-           "path_decode_step")
+    fn, name = (lib.path_decode_step_vt, "path_decode_step_vt") if value_transport else \
+        (lib.path_decode_step, "path_decode_step")
+    _check(fn(_ptr(q_t), _ptr(k_t), _ptr(v_t), _ptr(w_t), _ptr(beta_t), _ptr(kcache), _ptr(vcache), int(n_cached),
+              n_max, _ptr(o), _ptr(lse_t), B, H, d, ctypes.c_float(scale), _DT[dt], _ptr(workspace),
+              workspace.numel(), _stream()), name)
     return (o, lse_t) if lse else o
 
 

@@ -22,7 +22,11 @@ cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w
                            int BH, int L, int n_max, unsigned char* ws, const FwdLayout& lay, cudaStream_t st);
 cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                         const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t, float* lse_t,
-                        int BH, float scale, unsigned char* ws, const DecLayout& lay, cudaStream_t st);
+                        int BH, float scale, unsigned char* ws, const DecLayout& lay, bool vt, cudaStream_t st);
+bool fwd_vt_supported(int d, int L);
+cudaError_t fwd_vt(int dtype, int d, const void* q, const void* k, const void* v, const void* w, const float* beta,
+                   const float* log_f, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
+                   cudaStream_t st);
 bool bwd_supported(int d);
 cudaError_t attn_bwd(int dtype, int d, const void* q, const void* k, const void* v, const void* w,
                      const float* beta, const float* log_f, const void* o, const float* lse, const void* dO,
@@ -206,10 +210,10 @@ int path_kcache_update(void* kcache, int B, int H, int n_cached, int n_max, int 
     return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA;
 }
 
-int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const void* w_t, const float* beta_t,
-                     void* kcache, void* vcache, int n_cached, int n_max, void* o_t, float* lse_t, int B, int H,
-                     int d, float scale, int dtype, void* workspace, size_t workspace_bytes,
-                     path_stream_t stream) {
+static int decode_common(const void* q_t, const void* k_t, const void* v_t, const void* w_t, const float* beta_t,
+                         void* kcache, void* vcache, int n_cached, int n_max, void* o_t, float* lse_t, int B, int H,
+                         int d, float scale, int dtype, void* workspace, size_t workspace_bytes, bool vt,
+                         path_stream_t stream) {
     if (B < 1 || H < 1 || n_max < 1 || n_cached < 0) return PATH_ERR_INVALID;
     if (n_cached + 1 > n_max) return PATH_ERR_INVALID;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
@@ -221,9 +225,53 @@ int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const vo
     const DecLayout lay = dec_layout(B, H, n_max, d);
     if (!workspace || workspace_bytes < lay.total || !aligned16(workspace)) return PATH_ERR_WORKSPACE;
     cudaError_t e = decode_step(dtype, d, q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, n_max, o_t, lse_t,
-                                B * H, scale, static_cast<unsigned char*>(workspace), lay,
+                                B * H, scale, static_cast<unsigned char*>(workspace), lay, vt,
                                 reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA;
+}
+
+int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const void* w_t, const float* beta_t,
+                     void* kcache, void* vcache, int n_cached, int n_max, void* o_t, float* lse_t, int B, int H,
+                     int d, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                     path_stream_t stream) {
+    return decode_common(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, n_max, o_t, lse_t, B, H, d, scale,
+                         dtype, workspace, workspace_bytes, false, stream);
+}
+
+int path_decode_step_vt(const void* q_t, const void* k_t, const void* v_t, const void* w_t, const float* beta_t,
+                        void* kcache, void* vcache, int n_cached, int n_max, void* o_t, float* lse_t, int B, int H,
+                        int d, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                        path_stream_t stream) {
+    return decode_common(q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, n_max, o_t, lse_t, B, H, d, scale,
+                         dtype, workspace, workspace_bytes, true, stream);
+}
+
+size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype) {
+    if (B < 1 || H < 1 || L < 1 || (long long)B * H > 65535 || !fwd_vt_supported(d, L)) return 0;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return 0;
+    return sizeof(WsHeader);
+}
+
+int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                     const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype, int causal,
+                     float scale, void* workspace, size_t workspace_bytes, path_stream_t stream) {
+    if (B < 1 || H < 1 || L < 1 || d < 1) return PATH_ERR_INVALID;
+    if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
+    if (!causal || !fwd_vt_supported(d, L) || (long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
+    if ((long long)B * H * L > (1ll << 31) / 256) return PATH_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !w || !beta || !o) return PATH_ERR_INVALID;
+    const void* ptrs[] = {q, k, v, w, beta, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return PATH_ERR_INVALID;
+    if ((log_f && !aligned16(log_f)) || (lse && !aligned16(lse))) return PATH_ERR_INVALID;
+    if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned16(workspace)) return PATH_ERR_WORKSPACE;
+    cudaError_t e = fwd_vt(dtype, d, q, k, v, w, beta, log_f, o, lse, B * H, L, scale,
+                           static_cast<unsigned char*>(workspace), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        std::fprintf(stderr, "pathattn: value-transport forward launch failed: %s\n", cudaGetErrorString(e));
+        return PATH_ERR_CUDA;
+    }
+    return PATH_OK;
 }
 
 int path_get_status(const void* workspace, path_stream_t stream) {

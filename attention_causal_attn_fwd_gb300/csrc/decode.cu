@@ -46,7 +46,11 @@ constexpr int kDecUnroll = 8;
 
 // grid (splits, B*H).  Split s covers cache rows [s*R, min((s+1)*R, n_cached+1));
 // row n_cached is the new token.  Writes per-split (m, l, o) in log2 units.
-template <typename T, int D>
+// VT: value-side transport ("Resumo Técnico: Por que Transformações Acumuladas
+// Extrapolam?", §"Principais Contribuições" 3): the cached values are carried
+// along the same route as the keys, v~_j <- H_t v~_j in place, and the step
+// attends to the stored (transported) values.
+template <typename T, int D, bool VT = false>
 __global__ void __launch_bounds__(kDecNT) decode_update_score(
     const T* __restrict__ q_t, const T* __restrict__ k_t, const T* __restrict__ v_t, const T* __restrict__ w_t,
     const float* __restrict__ beta_t, T* __restrict__ kcache, T* __restrict__ vcache, int n_cached, int n_max,
@@ -120,9 +124,13 @@ __global__ void __launch_bounds__(kDecNT) decode_update_score(
             const int j = base + u * STRIDE;
             const Vec16<T> tr = transport<T, D>(kvec[u], wv, beta);  // all lanes shuffle
             const Vec16<T> kn = (j < n_cached) ? tr : kvec[u];
+            if (VT) {
+                const Vec16<T> trv = transport<T, D>(vvec[u], wv, beta);  // all lanes shuffle
+                if (j < n_cached) vvec[u] = trv;
+            }
             if (j < j1 && in_bounds(((long long)bh * n_max + j) * D + li * G::EPL, G::EPL, n_cache, hdr, 222)) {
                 st_global_v4(kh + (size_t)j * D, kn.raw);
-                if (j == n_cached) st_global_v4(vh + (size_t)j * D, vvec[u].raw);
+                if (VT || j == n_cached) st_global_v4(vh + (size_t)j * D, vvec[u].raw);
             }
             float part = 0.f;
 #pragma unroll
@@ -236,13 +244,14 @@ template <typename T, int D>
 static cudaError_t launch_decode_t(const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                                    const float* beta_t, void* kcache, void* vcache, int n_cached, int n_max,
                                    void* o_t, float* lse_t, int BH, float scale, unsigned char* ws,
-                                   const DecLayout& lay, cudaStream_t st) {
+                                   const DecLayout& lay, bool vt, cudaStream_t st) {
     const int nsplit = decode_splits(n_cached + 1);
     float* pm = reinterpret_cast<float*>(ws + lay.part_m);
     float* pl = reinterpret_cast<float*>(ws + lay.part_l);
     float* po = reinterpret_cast<float*>(ws + lay.part_o);
+    auto kern = vt ? decode_update_score<T, D, true> : decode_update_score<T, D, false>;
     mark_start(st);
-    decode_update_score<T, D><<<dim3(nsplit, BH), kDecNT, 0, st>>>(
+    kern<<<dim3(nsplit, BH), kDecNT, 0, st>>>(
         static_cast<const T*>(q_t), static_cast<const T*>(k_t), static_cast<const T*>(v_t),
         static_cast<const T*>(w_t), beta_t, static_cast<T*>(kcache), static_cast<T*>(vcache), n_cached, n_max,
         scale * 1.4426950408889634f, pm, pl, po, reinterpret_cast<WsHeader*>(ws));
@@ -255,22 +264,22 @@ template <typename T>
 static cudaError_t launch_decode_d(int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                                    const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t,
                                    float* lse_t, int BH, float scale, unsigned char* ws, const DecLayout& lay,
-                                   cudaStream_t st) {
+                                   bool vt, cudaStream_t st) {
     switch (d) {
-        case 16: return launch_decode_t<T, 16>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, st);
-        case 32: return launch_decode_t<T, 32>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, st);
-        case 64: return launch_decode_t<T, 64>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, st);
-        case 128: return launch_decode_t<T, 128>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, st);
+        case 16: return launch_decode_t<T, 16>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, vt, st);
+        case 32: return launch_decode_t<T, 32>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, vt, st);
+        case 64: return launch_decode_t<T, 64>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, vt, st);
+        case 128: return launch_decode_t<T, 128>(q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, vt, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                         const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t, float* lse_t,
-                        int BH, float scale, unsigned char* ws, const DecLayout& lay, cudaStream_t st) {
+                        int BH, float scale, unsigned char* ws, const DecLayout& lay, bool vt, cudaStream_t st) {
     if (dtype == PATH_F32)
-        return launch_decode_d<float>(d, q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, st);
-    return launch_decode_d<__nv_bfloat16>(d, q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, st);
+        return launch_decode_d<float>(d, q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, vt, st);
+    return launch_decode_d<__nv_bfloat16>(d, q_t, k_t, v_t, w_t, beta_t, kc, vc, n_cached, n_max, o_t, lse_t, BH, scale, ws, lay, vt, st);
 }
 
 template <typename T>
@@ -398,6 +407,6 @@ extern "C" int path_decode_step_noalloc(const void* q_t, const void* k_t, const 
     const int rc = noalloc_scratch_address(&ws);
     if (rc != PATH_OK) return rc;
     const cudaError_t e = decode_step(dtype, d, q_t, k_t, v_t, w_t, beta_t, kcache, vcache, n_cached, n_max, o_t,
-                                      lse_t, B * H, scale, ws, lay, reinterpret_cast<cudaStream_t>(stream));
+                                      lse_t, B * H, scale, ws, lay, false, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PATH_OK : PATH_ERR_CUDA;
 }

@@ -241,6 +241,47 @@ int path_decode_step(const void* q_t, const void* k_t, const void* v_t, const vo
                      size_t workspace_bytes, path_stream_t stream);
 
 /*
+ * One decode step with value-side transport ("Resumo Técnico: Por que
+ * Transformações Acumuladas Extrapolam?", §"Metodologia" 1 route transport
+ * P_{j->i}, §"Principais Contribuições" 3 "Proteção do Lado de Valor": the
+ * accumulated route transport applied to the values as well as the keys).  As
+ * path_decode_step, with the value cache transported in place alongside the
+ * keys:
+ *   1. kcache[j] <- H_t kcache[j] and vcache[j] <- H_t vcache[j] for j < n_cached
+ *      (fp32 math, stored in the cache dtype)
+ *   2. kcache[n_cached] <- k_t, vcache[n_cached] <- v_t (untransported)
+ *   3. o_t = softmax_j(scale * q_t . kcache[j]) vcache[j], scoring and summing
+ *      the values just stored.
+ * The value cache therefore holds v~_j = H_{t-1} ... H_{j+1} v_j; after a prompt
+ * of L tokens it is what path_prefill_kcache computes with v in place of k.
+ * Arguments, sizes, workspace and errors as path_decode_step.
+ */
+int path_decode_step_vt(const void* q_t, const void* k_t, const void* v_t, const void* w_t,
+                        const float* beta_t, void* kcache, void* vcache, int n_cached, int n_max, void* o_t,
+                        float* lse_t, int B, int H, int d, float scale, int dtype, void* workspace,
+                        size_t workspace_bytes, path_stream_t stream);
+
+/*
+ * Workspace size in bytes for path_attn_fwd_vt (a status word only).  Returns 0
+ * for unsupported sizes.
+ */
+size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype);
+
+/*
+ * PaTH (log_f == NULL) or PaTH-FoX forward with value-side transport (the
+ * operator of path_decode_step_vt over a whole sequence):
+ *     o_i = sum_j softmax_j(s_i.) H_i ... H_{j+1} v_j
+ * with the logits s_ij of path_attn_fwd / path_attn_fwd_fox (lse is theirs too).
+ * Arguments as path_attn_fwd_fox (log_f nullable); d in {16, 32, 64, 128} for
+ * PATH_F32 and PATH_BF16, L <= 8192 (the row's logits are kept in shared
+ * memory), B*H <= 65535.  Runs on CUDA cores in fp32, one warp per query row
+ * walking its keys twice; results are rounded to the input dtype.
+ */
+int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                     const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype, int causal,
+                     float scale, void* workspace, size_t workspace_bytes, path_stream_t stream);
+
+/*
  * Status of the most recent call that used `workspace` (each call clears the
  * word when it starts).  Synchronises `stream` first.  Returns a path_status
  * code: PATH_OK, PATH_ERR_TIMEOUT if a device-side bounded wait expired, or
