@@ -49,9 +49,11 @@ constexpr int kDecUnroll = 8;
 // VT: value-side transport ("Resumo Técnico: Por que Transformações Acumuladas
 // Extrapolam?", §"Principais Contribuições" 3): the cached values are carried
 // along the same route as the keys, v~_j <- H_t v~_j in place, and the step
-// attends to the stored (transported) values.
+// attends to the stored (transported) values.  The value transport needs a
+// few more registers; VT builds are held to 128 (two CTAs per SM, the memory
+// parallelism the step depends on) at the cost of a 12-byte spill.
 template <typename T, int D, bool VT = false>
-__global__ void __launch_bounds__(kDecNT) decode_update_score(
+__global__ void __launch_bounds__(kDecNT, VT ? 2 : 0) decode_update_score(
     const T* __restrict__ q_t, const T* __restrict__ k_t, const T* __restrict__ v_t, const T* __restrict__ w_t,
     const float* __restrict__ beta_t, T* __restrict__ kcache, T* __restrict__ vcache, int n_cached, int n_max,
     float scale_log2, float* __restrict__ part_m, float* __restrict__ part_l, float* __restrict__ part_o,

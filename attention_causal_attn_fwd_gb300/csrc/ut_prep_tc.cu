@@ -9,13 +9,13 @@
 //      Y   = tril(Q W^T) A^T              (diagonal block, bf16)
 //     qhat = Q - Y W                      (fp32)
 //     -Z   = -triu_1(K W^T)               (diagonal block, bf16)
-//     khat = K - (Z A) W                  (bf16)
+//     khat = K - (Z A) W = K - Z V        (bf16)
 // and, for the prefill hand-off, V itself.  (The fp32 CUDA-core version in
 // ut_prep.cu writes -U = -A^T W in place of P - I: its scan applies the
 // transition as two products.)
 //
 // Products run as tcgen05 MMAs (M = 128) with fp32 accumulation in TMEM.
-// Operands that are not exact in bf16 (A, tril(QW^T), Y, Z, ZA) are split
+// Operands that are not exact in bf16 (A, tril(QW^T), Y, Z, V) are split
 // into hi + lo bf16 parts and multiplied term by term (hi*hi + hi*lo + lo*hi),
 // which keeps those products close to fp32 accuracy; -V enters P - I as one
 // bf16 operand (P - I is itself stored in bf16).  A = X D with the unit upper-
@@ -49,9 +49,9 @@ namespace utk {
 constexpr int C = 128;
 constexpr int kThreads = 320;
 constexpr int kCompute = 256;   // warps 2-9: two warps per TMEM lane quarter
-constexpr uint32_t R0 = 0;        // W            (K-major / MN-major source)
-constexpr uint32_t R1 = 32768;    // Q, then solve temp, then A_hi
-constexpr uint32_t R2 = 65536;    // K, then A_lo
+constexpr uint32_t R0 = 0;        // W            (K-major / MN-major source), then qhat staging
+constexpr uint32_t R1 = 32768;    // Q, then solve temp, then A_hi, then V_hi
+constexpr uint32_t R2 = 65536;    // K, then A_lo, then V_lo, then khat staging
 constexpr uint32_t R3 = 98304;    // G fp32 [128][132] for the solve, then hi/lo operand (hi, hi + 32 KB = lo)
 constexpr int LDG = 132;          // rows start on 16-byte boundaries
 constexpr uint32_t RB = R3 + 128 * LDG * 4;  // barriers, beta
@@ -66,8 +66,9 @@ constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 // tiles have been read by the bulk stores (store thread).  Groups: 0 Y (R3);
 // 1 P - I (staging tile, which held -V as the operand of P - I); 2 -Z (R3),
 // qhat columns 0-31 of each half (staging tile); 3 qhat columns 32-63
-// (d = 128; R1, free once Z A has completed); last khat (R2, likewise free).
-enum { B_LOAD = 0, B_G, B_QK, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_ZA, B_OPS4, B_K, B_DRAIN,
+// (d = 128; R0, free once Y W and P - I have completed); last khat (R2, free
+// once Z V has completed).
+enum { B_LOAD = 0, B_G, B_QK, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_K, B_DRAIN,
        B_STG0, B_STG1, B_STG2, B_STG3, B_STG4, B_FREE0, B_FREE1, B_FREE2, B_FREE3, B_FREE4, B_COUNT };
 constexpr uint32_t RB_SLOT = 200;  // TMEM address and abort flag after the barriers
 static_assert(B_COUNT * 8 <= RB_SLOT && RB_SLOT + 8 <= 256, "barriers overlap the TMEM slot, abort flag or beta");
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || i == B_OPS4 || (i >= B_STG0 && i <= B_STG4))
+            mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || (i >= B_STG0 && i <= B_STG4))
                                   ? kCompute : 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                     for (int b = 0; b < D / 64; ++b) tma_store_3d(&tm_un, sb + RS + b * 16384, 64 * b, row0, bh);
                 } else if (g == 2 || (D == 128 && g == 3)) {
                     const int c = g - 2;  // qhat columns 32c .. 32c+31 of each half
-                    const uint32_t src = sb + (c == 0 ? RS : R1);
+                    const uint32_t src = sb + (c == 0 ? RS : R0);
                     for (int b = 0; b < 2; ++b)
                         tma_store_3d(&tm_qhat, src + b * 16384, (D / 2) * b + 32 * c, row0, bh);
                     if (g == 2)
@@ -440,28 +441,16 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             }
             if (ok) {
                 tc_fence_after();
-                // Z A = Zhi Ahi + Zhi Alo + Zlo Ahi  (A as MN-major B)
+                // (Z A) W = Z V: -(Z V) = (-Z)hi Vhi + (-Z)hi Vlo + (-Z)lo Vhi  (V as MN-major B)
                 for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R1, kk), ID_KMN_128, kk > 0);
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R1, kk), ID_KMN_D, kk > 0);
                 for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R2, kk), ID_KMN_128, 1);
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R2, kk), ID_KMN_D, 1);
                 for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tmem + T0, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R1, kk),
-                           ID_KMN_128, 1);
-                mma_commit(bar(B_ZA));
-                UT_TRACE(20);
-                ok = mbar_wait(bar(B_OPS4), 0, wc, 44);
-                UT_TRACE(21);
-            }
-            if (ok) {
-                tc_fence_after();
-                // (Z A) W
-                for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tmem + T128, kmajor_desc(sb + R3, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, kk > 0);
-                for (int kk = 0; kk < C / 16; ++kk)
-                    mma_ss(tmem + T128, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R0, kk), ID_KMN_D, 1);
+                    mma_ss(tmem + T0, kmajor_desc(sb + R3 + 32768, kk, 16384), mnmajor_desc(sb + R1, kk), ID_KMN_D,
+                           1);
                 mma_commit(bar(B_K));
-                UT_TRACE(22);
+                UT_TRACE(20);
             }
             mma_commit(bar(B_DRAIN));
             drain_wait(bar(B_DRAIN), 0, p.limit_ns, p.hdr, 99);
@@ -570,24 +559,28 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         }
         if (ok) {
             tc_fence_after();
+            // V = A W row -> -V (bf16 MN-major B operand of P - I) and V as a hi/lo
+            // MN-major B operand of Z V over A (A is no longer read once Y and V
+            // have completed)
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // V = A W row -> -V (bf16 MN-major B operand of P - I)
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t v[32];
                 const int col = (D / 2) * h + 32 * c;
                 tmem_ld32(tl + T128 + col, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    float v8[8];
+                    float v8[8], nv8[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v8[e] = -__uint_as_float(v[8 * g + e]);
-                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(v8));
-                    if (p.vfac && in_bounds((long long)ws_row * D + col + 8 * g, 8, (long long)p.BH * p.Lp * D, p.hdr,
-                                            213)) {  // the prefill hand-off's key-side factor V
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v8[e] = -v8[e];
-                        st_global_v4(p.vfac + ws_row * D + col + 8 * g, pack8(v8));
+                    for (int e = 0; e < 8; ++e) {
+                        v8[e] = __uint_as_float(v[8 * g + e]);
+                        nv8[e] = -v8[e];
                     }
+                    stage16(sm + RS, r, (col + 8 * g) >> 6, ((col + 8 * g) & 63) >> 3, pack8(nv8));
+                    put_hilo(sm + R1, sm + R2, r, (col + 8 * g) >> 3, v8);
+                    if (p.vfac && in_bounds((long long)ws_row * D + col + 8 * g, 8, (long long)p.BH * p.Lp * D, p.hdr,
+                                            213))  // the prefill hand-off's key-side factor V
+                        st_global_v4(p.vfac + ws_row * D + col + 8 * g, pack8(v8));
                 }
             }
 #pragma unroll
@@ -665,7 +658,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         }
         if (ok) {
             // Z = triu_1(K W^T) -> hi/lo operand, negated: its hi part is the bf16 -Z
-            // output, Z A comes out as -(Z A) and (Z A) W as -(Z A) W
+            // output, and Z V comes out as -(Z V)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t v[32];
@@ -687,47 +680,22 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             tc_fence_before();
             mbar_arrive(bar(B_OPS3));
             if (t == 0) UT_TRACE(8);
-            // qhat = Q - Y W (fp32), columns 0-31 of each half, into the staging
-            // tile (once the P - I store has read it) while Z A runs (columns
-            // 32-63 follow once Z A has freed R1)
+            // qhat = Q - Y W (fp32) while Z V runs: columns 0-31 of each half into the
+            // staging tile (once the P - I store has read it), columns 32-63 into R0
+            // (W is no longer read once Y W and P - I have completed)
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE1), 0, wc, 56));
             if (ok) {
                 stage_qhat(0, sm + RS);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(B_STG2));  // with the -Z tile
-            }
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_ZA), 0, wc, 53));
-            if (t == 0) UT_TRACE(9);
-        }
-        // the -Z store (group 2) has read R3 before -(Z A) is written there
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_FREE2), 0, wc, 57));
-        if (ok) {
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {  // -(Z A) -> hi/lo operand
-                uint32_t v[32];
-                const int col = 64 * h + 32 * c;
-                tmem_ld32(tl + T0 + col, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float z8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) z8[e] = __uint_as_float(v[8 * g + e]);
-                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, z8);
+                if (D == 128) {
+                    stage_qhat(1, sm + R0);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(B_STG3));
                 }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(bar(B_OPS4));
-            if (t == 0) UT_TRACE(10);
-            if (D == 128) {  // qhat columns 32-63 of each half into R1 (A is dead after Z A) while (Z A) W runs
-                stage_qhat(1, sm + R1);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(B_STG3));
-            }
         }
-        // This thread's half of the K row, loaded while (Z A) W runs.
+        // This thread's half of the K row, loaded while Z V runs.
         uint4 kpre[D / 16];
         {
             const __nv_bfloat16* krow = p.k + ((size_t)bh * p.L + grow) * D;
@@ -744,10 +712,10 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             tc_fence_after();
             float n2 = 0.f;  // this thread's part of |khat_row|^2
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // khat = K - (Z A) W; TMEM holds -(Z A) W
+            for (int c = 0; c < D / 64; ++c) {  // khat = K - Z V; TMEM holds -(Z V)
                 uint32_t v[32];
                 const int col = (D / 2) * h + 32 * c;
-                tmem_ld32(tl + T128 + col, v);
+                tmem_ld32(tl + T0 + col, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
@@ -763,7 +731,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(bar(B_STG2 + D / 64));  // khat tile (R2, free since Z A) -> workspace
+            mbar_arrive(bar(B_STG2 + D / 64));  // khat tile (R2, free since Z V) -> workspace
             if (p.kmax2) {  // chunk max of |khat|^2 over rows < L (the solve temp is free)
                 float* red = reinterpret_cast<float*>(sm + RT);
                 red[r + 128 * h] = grow < p.L ? n2 : 0.f;

@@ -386,6 +386,58 @@ def run_ours(args, rank, world, local):
                           "overlap": "inputs copied on a side stream, double-buffered; o_t copied out on a third"}
         del hin, hout, dbuf, obuf
 
+    # value-side transport (the route transport applied to the values as well): the decode step that
+    # transports both caches in place, on the decode workload, and the CUDA-core forward on one batch
+    # of the forward workload's heads.  Timed separately, not part of the step.
+    vt = None
+    if Td and args.vt_steps > 0:
+        Tv = min(args.vt_steps, Td)
+        ev = [(mk(), mk()) for _ in range(Tv)]
+        for t in range(2):
+            P.path_decode_step(dq[t], dk[t], dv[t], dw[t], db[t], kc, vc, dc.n0 + t, scale=dc.d ** -0.5,
+                               out=od[t], workspace=ws_d, value_transport=True)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for t in range(Tv):
+            P.path_debug_set_timing_events(ev[t][0], ev[t][1])
+            P.path_decode_step(dq[t], dk[t], dv[t], dw[t], db[t], kc, vc, dc.n0 + t, scale=dc.d ** -0.5,
+                               out=od[t], workspace=ws_d, value_transport=True)
+        P.path_debug_set_timing_events(None, None)
+        b.record()
+        torch.cuda.synchronize()
+        # algorithmic bytes: K and V each read and written once per cached row
+        vbytes = statistics.mean(4.0 * dc.B * dc.H * (dc.n0 + t) * dc.d * 2 for t in range(Tv))
+        vk = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+        vgbs = vbytes / (vk * 1e-3) / 1e9
+        vt = {"decode": {"us_per_step": a.elapsed_time(b) * 1e3 / Tv, "steps": Tv, "cache_tokens": dc.n0,
+                         "roofline": {"kernel": "decode_update_score (value transport)", "bound": "hbm",
+                                      "achieved": vgbs, "peak": hbm_gbs, "unit": "GB/s", "frac": vgbs / hbm_gbs,
+                                      "peak_source": peak_src, "frac_of_spec": vgbs / SPEC_HBM_GBS,
+                                      "bytes_per_launch": vbytes, "kernel_ms": vk},
+                         "workload": "decode B%d H%d d%d bf16 at a %d-token cache; K and V transported in place"
+                                     % (dc.B, dc.H, dc.d, dc.n0)}}
+        if args.vt_fwd_steps > 0:
+            vq, vk_, vv, vw, vb = (t[:1] for t in (q, k, v, w, beta))
+            vo = torch.empty_like(vq)
+            vws = P.alloc_workspace(P.load().path_attn_fwd_vt_workspace_bytes(1, fc.H, fc.L, fc.d, P._DT[vq.dtype]),
+                                    dev)
+            P.path_attn_fwd_vt(vq, vk_, vv, vw, vb, scale=x.scale, out=vo, workspace=vws)
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(args.vt_fwd_steps):
+                P.path_attn_fwd_vt(vq, vk_, vv, vw, vb, scale=x.scale, out=vo, workspace=vws)
+            b.record()
+            torch.cuda.synchronize()
+            fms_vt = a.elapsed_time(b) / args.vt_fwd_steps
+            vflops = fc.attn_flops / fc.B
+            vt["forward"] = {"ms": fms_vt, "steps": args.vt_fwd_steps,
+                             "attn_equiv_tflops": vflops / (fms_vt * 1e-3) / 1e12,
+                             "workload": "value-transport forward B1 H%d L%d d%d bf16 (CUDA cores, one warp per "
+                                         "query row, two walks per row)" % (fc.H, fc.L, fc.d)}
+            del vo, vws
+
     # end to end through the public API with host buffers: pinned inputs -> device, forward, o -> host,
     # every step.  Copies run on their own stream into double-buffered device inputs, so the next
     # step's inputs cross while this step computes (the order per step is still copy in -> forward
@@ -590,7 +642,7 @@ def run_ours(args, rank, world, local):
                        "seq_len": fc.L, "parallelism": "replicas (b,h)-independent" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (forward 384 MiB of q,k,v,w; decode caches 13 GB)"},
             "fwd_ms": fwd_ms_max / args.steps, "fwd_kernel_ms": fk, "whole_call": lines["whole_call"],
-            "decode": dec_obj, "prefill_kcache": prefill, "fox16k": fox.get("fox16k"), "fox64k": fox.get("fox64k"), "relbias_ggd": relb, "backward": bwd, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+            "decode": dec_obj, "value_transport": vt, "prefill_kcache": prefill, "fox16k": fox.get("fox16k"), "fox64k": fox.get("fox64k"), "relbias_ggd": relb, "backward": bwd, "roofline": lines["roofline"], "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": launches_per_step * args.steps}
     if rank == 0:
         print(json.dumps(line))
@@ -607,6 +659,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--decode-e2e-steps", type=int, default=64)
     ap.add_argument("--prefill-steps", type=int, default=2)
+    ap.add_argument("--vt-steps", type=int, default=16, help="value-transport decode steps (0 = skip)")
+    ap.add_argument("--vt-fwd-steps", type=int, default=2, help="value-transport forward calls (0 = skip)")
     ap.add_argument("--fox-steps", type=int, default=3)
     ap.add_argument("--bwd-steps", type=int, default=2)
     ap.add_argument("--cpu-heads", type=int, default=96)
