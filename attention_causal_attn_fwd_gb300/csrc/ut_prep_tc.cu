@@ -60,6 +60,15 @@ constexpr int LDT = 68;
 constexpr uint32_t RS = RT + 64 * LDT * 4;    // output staging tile for TMA stores (32 KB)
 static_assert(RS % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte boundaries");
 constexpr uint32_t TOTAL = RS + 32768;
+// Operand tiles of the level-64 merge on the tensor cores (hi part, lo part
+// 16 KB / 8 KB after it): G_PQ (rows 0-63 of an M = 128 K-major tile) in the
+// staging tile; A_QQ, then T, as a 64-row MN-major B in the solve temp; A_PP
+// (K-major, rows 0-63) over rows 64-127 of the fp32 G, which the merge at 64
+// no longer reads.
+constexpr uint32_t RM_GPQ = RS, RM_B = RT, RM_APP = R3 + 34816;
+static_assert(RM_APP % 1024 == 0 && RM_APP + 32768 <= RB, "A_PP tiles overlap the barriers");
+static_assert(64 * 132 * 4 <= 34816, "A_PP tiles overlap rows 0-63 of G, which G_PQ still reads");
+static_assert(64 * LDT * 4 >= 16384, "the solve temp holds the hi and lo 8 KB B tiles");
 constexpr size_t kSmem = TOTAL + 1024;
 constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 // B_STG*: a workspace-store group is staged (compute warps); B_FREE*: its
@@ -68,7 +77,9 @@ constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
 // qhat columns 0-31 of each half (staging tile); 3 qhat columns 32-63
 // (d = 128; R0, free once Y W and P - I have completed); last khat (R2, free
 // once Z V has completed).
-enum { B_LOAD = 0, B_G, B_QK, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_K, B_DRAIN,
+// B_M64*: the merge at level 64 on the tensor cores (operands staged, T done,
+// T staged, A_PQ done).
+enum { B_LOAD = 0, B_G, B_QK, B_M64A, B_M64T, B_M64B, B_M64R, B_OPS1, B_UY, B_OPS2, B_Q, B_OPS3, B_K, B_DRAIN,
        B_STG0, B_STG1, B_STG2, B_STG3, B_STG4, B_FREE0, B_FREE1, B_FREE2, B_FREE3, B_FREE4, B_COUNT };
 constexpr uint32_t RB_SLOT = 200;  // TMEM address and abort flag after the barriers
 static_assert(B_COUNT * 8 <= RB_SLOT && RB_SLOT + 8 <= 256, "barriers overlap the TMEM slot, abort flag or beta");
@@ -310,7 +321,6 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     constexpr uint32_t TILE = 128u * D * 2u;
     constexpr uint32_t ID_KK128 = idesc_bf16_ab(128, false, false);
     constexpr uint32_t ID_KMN_D = idesc_bf16_ab(D, false, true);
-    constexpr uint32_t ID_KMN_128 = idesc_bf16_ab(128, false, true);
     constexpr uint32_t ID_MNMN_D = idesc_bf16_ab(D, true, true);
 
     extern __shared__ uint8_t smem_raw[];
@@ -331,7 +341,8 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < B_COUNT; ++i)
-            mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || (i >= B_STG0 && i <= B_STG4))
+            mbar_init(bar(i), (i == B_OPS1 || i == B_OPS2 || i == B_OPS3 || i == B_M64A || i == B_M64B ||
+                               (i >= B_STG0 && i <= B_STG4))
                                   ? kCompute : 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -400,7 +411,34 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 }
                 mma_commit(bar(B_QK));
                 UT_TRACE(14);
-                ok = mbar_wait(bar(B_OPS1), 0, wc, 41);
+                // the merge at level 64: T = G_PQ A_QQ, then A_PQ = -(A_PP T), both as
+                // hi*hi + hi*lo + lo*hi with M = 128 (rows 64-127 unused), N = 64, K = 64
+                constexpr uint32_t ID_M64 = idesc_bf16_ab(64, false, true);
+                ok = mbar_wait(bar(B_M64A), 0, wc, 46);
+                if (ok) {
+                    tc_fence_after();
+                    for (int part = 0; part < 3; ++part) {
+                        const uint32_t a = sb + RM_GPQ + (part == 2 ? 16384u : 0u);
+                        const uint32_t b = sb + RM_B + (part == 1 ? 8192u : 0u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + T384, kmajor_desc(a, kk, 16384), mnmajor_desc(b, kk), ID_M64,
+                                   (part > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar(B_M64T));
+                    ok = mbar_wait(bar(B_M64B), 0, wc, 47);
+                }
+                if (ok) {
+                    tc_fence_after();
+                    for (int part = 0; part < 3; ++part) {
+                        const uint32_t a = sb + RM_APP + (part == 2 ? 16384u : 0u);
+                        const uint32_t b = sb + RM_B + (part == 1 ? 8192u : 0u);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + T384 + 64, kmajor_desc(a, kk, 16384), mnmajor_desc(b, kk), ID_M64,
+                                   (part > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar(B_M64R));
+                    ok = mbar_wait(bar(B_OPS1), 0, wc, 41);
+                }
                 UT_TRACE(15);
             }
             if (ok) {
@@ -510,7 +548,63 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             if (t == 0) UT_TRACE(24);
             merge_level_tri<32, 2, 4>(sG, sX, sT, t);
             if (t == 0) UT_TRACE(25);
-            merge_level_tri<64, 4, 4>(sG, sX, sT, t);
+            // The merge at level 64 (P = rows 0-63, Q = rows 64-127) on the tensor
+            // cores: G_PQ, A_QQ and A_PP to hi/lo bf16 tiles, T = G_PQ A_QQ, T to
+            // hi/lo, A_PQ = -(A_PP T) back into the dense A.
+            {
+                const int row = t >> 2, c0 = 16 * (t & 3);  // 64 rows x 4 segments of 16 columns
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    float v8[8];
+                    const int col = c0 + 8 * g;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v8[e] = sG[row * LDG + 64 + col + e];
+                    put_hilo(sm + RM_GPQ, sm + RM_GPQ + 16384, row, col >> 3, v8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v8[e] = sX[(64 + row) * C + 64 + col + e];
+                    put_hilo(sm + RM_B, sm + RM_B + 8192, row, col >> 3, v8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v8[e] = sX[row * C + col + e];
+                    put_hilo(sm + RM_APP, sm + RM_APP + 16384, row, col >> 3, v8);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(B_M64A));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_M64T), 0, wc, 59));
+            if (ok) {
+                tc_fence_after();
+                if (r < 64) {  // T row r (this warp's 32 columns) -> MN-major B rows
+                    uint32_t v[32];
+                    tmem_ld32(tl + T384 + 32 * h, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float v8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v8[e] = __uint_as_float(v[8 * g + e]);
+                        put_hilo(sm + RM_B, sm + RM_B + 8192, r, 4 * h + g, v8);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(B_M64B));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(B_M64R), 0, wc, 60));
+            }
+            if (ok) {
+                tc_fence_after();
+                if (r < 64) {  // A_PQ row r = -(A_PP T) row r
+                    uint32_t v[32];
+                    tmem_ld32(tl + T384 + 64 + 32 * h, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4*>(sX + r * C + 64 + 32 * h + j) =
+                            make_float4(-__uint_as_float(v[j]), -__uint_as_float(v[j + 1]), -__uint_as_float(v[j + 2]),
+                                        -__uint_as_float(v[j + 3]));
+                }
+            }
+            named_bar_sync(1, kCompute);
             if (t == 0) UT_TRACE(3);
             // A as hi/lo bf16 tiles.  The tiles overwrite the dense A, so
             // each thread first reads its 8 granules (8 consecutive columns of

@@ -170,3 +170,16 @@ def test_bwd_760m_shaped_sampled_heads():
     ref = _oracle(x, dO, heads=heads)
     got = {n: np.stack([to_np(t[b, h]) for (b, h) in heads]) for n, t in g.items()}
     _compare(got, ref, torch.bfloat16, "760m sampled heads")
+
+
+def test_bwd_fox16k_two_whole_heads():
+    """The PaTH-FoX long-context workload, B1 H12 L16384 d128 bf16 (log f = logsigmoid(N(3,1))),
+    backward run whole; heads 0 and 11 compared with the oracle over every position, dlog f
+    included."""
+    x = inputs.FWD_CONFIGS["fox16k_bf16"].make()
+    dO = _dO(x.q.shape, torch.bfloat16, 16)
+    g = _gpu_bwd(x, dO)
+    heads = [(0, 0), (0, 11)]
+    ref = _oracle(x, dO, heads=heads)
+    got = {n: np.stack([to_np(t[b, h]) for (b, h) in heads]) for n, t in g.items()}
+    _compare(got, ref, torch.bfloat16, "fox16k whole heads")
