@@ -61,13 +61,10 @@ constexpr uint32_t RS = RT + 64 * LDT * 4;    // output staging tile for TMA sto
 static_assert(RS % 1024 == 0, "128-byte-swizzled tiles start on 1024-byte boundaries");
 constexpr uint32_t TOTAL = RS + 32768;
 // Operand tiles of the level-64 merge on the tensor cores (hi part, lo part
-// 16 KB / 8 KB after it): G_PQ (rows 0-63 of an M = 128 K-major tile) in the
-// staging tile; A_QQ, then T, as a 64-row MN-major B in the solve temp; A_PP
-// (K-major, rows 0-63) over rows 64-127 of the fp32 G, which the merge at 64
-// no longer reads.
-constexpr uint32_t RM_GPQ = RS, RM_B = RT, RM_APP = R3 + 34816;
-static_assert(RM_APP % 1024 == 0 && RM_APP + 32768 <= RB, "A_PP tiles overlap the barriers");
-static_assert(64 * 132 * 4 <= 34816, "A_PP tiles overlap rows 0-63 of G, which G_PQ still reads");
+// 16 KB / 8 KB after it): G_PQ, then A_PP (rows 0-63 of an M = 128 K-major
+// tile) in the staging tile; A_QQ, then T, as a 64-row MN-major B in the
+// solve temp.
+constexpr uint32_t RM_A = RS, RM_B = RT;
 static_assert(64 * LDT * 4 >= 16384, "the solve temp holds the hi and lo 8 KB B tiles");
 constexpr size_t kSmem = TOTAL + 1024;
 constexpr uint32_t T0 = 0, T128 = 128, T256 = 256, T384 = 384;
@@ -418,7 +415,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 if (ok) {
                     tc_fence_after();
                     for (int part = 0; part < 3; ++part) {
-                        const uint32_t a = sb + RM_GPQ + (part == 2 ? 16384u : 0u);
+                        const uint32_t a = sb + RM_A + (part == 2 ? 16384u : 0u);
                         const uint32_t b = sb + RM_B + (part == 1 ? 8192u : 0u);
                         for (int kk = 0; kk < 4; ++kk)
                             mma_ss(tmem + T384, kmajor_desc(a, kk, 16384), mnmajor_desc(b, kk), ID_M64,
@@ -430,7 +427,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 if (ok) {
                     tc_fence_after();
                     for (int part = 0; part < 3; ++part) {
-                        const uint32_t a = sb + RM_APP + (part == 2 ? 16384u : 0u);
+                        const uint32_t a = sb + RM_A + (part == 2 ? 16384u : 0u);
                         const uint32_t b = sb + RM_B + (part == 1 ? 8192u : 0u);
                         for (int kk = 0; kk < 4; ++kk)
                             mma_ss(tmem + T384 + 64, kmajor_desc(a, kk, 16384), mnmajor_desc(b, kk), ID_M64,
@@ -549,23 +546,22 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
             merge_level_tri<32, 2, 4>(sG, sX, sT, t);
             if (t == 0) UT_TRACE(25);
             // The merge at level 64 (P = rows 0-63, Q = rows 64-127) on the tensor
-            // cores: G_PQ, A_QQ and A_PP to hi/lo bf16 tiles, T = G_PQ A_QQ, T to
-            // hi/lo, A_PQ = -(A_PP T) back into the dense A.
+            // cores: G_PQ and A_QQ to hi/lo bf16 tiles, T = G_PQ A_QQ; T and A_PP to
+            // hi/lo, A_PQ = -(A_PP T) back into the dense A.  Y' = tril(Q W^T) goes to
+            // its hi/lo operand tiles (over G, no longer read) while A_PP T runs.
             {
                 const int row = t >> 2, c0 = 16 * (t & 3);  // 64 rows x 4 segments of 16 columns
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
-                    float v8[8];
                     const int col = c0 + 8 * g;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v8[e] = sG[row * LDG + 64 + col + e];
-                    put_hilo(sm + RM_GPQ, sm + RM_GPQ + 16384, row, col >> 3, v8);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v8[e] = sX[(64 + row) * C + 64 + col + e];
-                    put_hilo(sm + RM_B, sm + RM_B + 8192, row, col >> 3, v8);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v8[e] = sX[row * C + col + e];
-                    put_hilo(sm + RM_APP, sm + RM_APP + 16384, row, col >> 3, v8);
+                    const float4 g0 = *reinterpret_cast<const float4*>(sG + row * LDG + 64 + col);
+                    const float4 g1 = *reinterpret_cast<const float4*>(sG + row * LDG + 64 + col + 4);
+                    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                    put_hilo(sm + RM_A, sm + RM_A + 16384, row, col >> 3, gv);
+                    const float4 a0 = *reinterpret_cast<const float4*>(sX + (64 + row) * C + 64 + col);
+                    const float4 a1 = *reinterpret_cast<const float4*>(sX + (64 + row) * C + 64 + col + 4);
+                    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                    put_hilo(sm + RM_B, sm + RM_B + 8192, row, col >> 3, av);
                 }
             }
             fence_proxy_async_smem();
@@ -585,10 +581,36 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                         for (int e = 0; e < 8; ++e) v8[e] = __uint_as_float(v[8 * g + e]);
                         put_hilo(sm + RM_B, sm + RM_B + 8192, r, 4 * h + g, v8);
                     }
+                } else {  // A_PP row r - 64 (32 columns) -> K-major A rows, over G_PQ
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = 32 * h + 8 * g;
+                        const float4 a0 = *reinterpret_cast<const float4*>(sX + (r - 64) * C + col);
+                        const float4 a1 = *reinterpret_cast<const float4*>(sX + (r - 64) * C + col + 4);
+                        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        put_hilo(sm + RM_A, sm + RM_A + 16384, r - 64, col >> 3, av);
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar(B_M64B));
+                // Y' = tril(Q W^T) -> hi/lo operand (every thread's G reads came before B_M64T)
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tl + T128 + 64 * h + 32 * c, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float y8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int b = 64 * h + 32 * c + 8 * g + e;
+                            y8[e] = b <= r ? __uint_as_float(v[8 * g + e]) : 0.f;
+                        }
+                        put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, y8);
+                    }
+                }
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(B_M64R), 0, wc, 60));
             }
             if (ok) {
@@ -626,22 +648,6 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 for (int i = 0; i < 8; ++i) {
                     const int q = t + kCompute * i;
                     put_hilo(sm + R1, sm + R2, q >> 4, q & 15, a[i]);
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {  // Y' = tril(Q W^T) -> hi/lo operand (G is no longer read)
-                uint32_t v[32];
-                tmem_ld32(tl + T128 + 64 * h + 32 * c, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float y8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int b = 64 * h + 32 * c + 8 * g + e;
-                        y8[e] = b <= r ? __uint_as_float(v[8 * g + e]) : 0.f;
-                    }
-                    put_hilo(opHi, opLo, r, 8 * h + 4 * c + g, y8);
                 }
             }
             fence_proxy_async_smem();
