@@ -102,8 +102,13 @@ constexpr int kTraceCta = PATH_TRACE_CTA;
 #ifdef PATH_TRACE
 #define TC_TRACE(slot, it) \
     do { if (p.trace && blockIdx.x == kTraceCta && (it) < 64) p.trace[(it) * 32 + (slot)] = clock64(); } while (0)
+// Per-CTA global-timer stamps (every CTA): 0 entry, 1 diagonal issued, 2 exit, 3 SM id.
+constexpr int kTraceCtaBase = 64 * 32, kTraceMaxCtas = 65536;
+#define TC_CTA(slot, val) \
+    do { if (p.trace && blockIdx.x < kTraceMaxCtas) p.trace[kTraceCtaBase + blockIdx.x * 4 + (slot)] = (val); } while (0)
 #else
 #define TC_TRACE(slot, it) do { } while (0)
+#define TC_CTA(slot, val) do { } while (0)
 #endif
 
 struct TcParams {
@@ -160,6 +165,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float* s_kmax2 = reinterpret_cast<float*>(sm + SM_CTL + 48);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        TC_CTA(0, globaltimer());
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        TC_CTA(3, smid);
+    }
     // Launch order: heads in groups of kHeadGroup; inside a group, tiles
     // longest first with the heads interleaved.  The ~150 resident CTAs then
     // cover a few heads each, so their key/value blocks are re-read from L2,
@@ -290,6 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_commit(bar(B_KMEMPTY0));
             mma_commit(bar(B_VEMPTY1));
             TC_TRACE(0, 0);
+            TC_CTA(1, globaltimer());
         }
         __syncwarp();
         auto issue_pv = [&](int blk) {  // O (+)= P V for block iteration blk (P in TMEM)
@@ -723,6 +735,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    if (threadIdx.x == 0) TC_CTA(2, globaltimer());
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -732,14 +745,21 @@ bool tc_supported(int d) { return d == 64 || d == 128; }
 #ifdef PATH_TRACE
 static unsigned long long* trace_buffer() {
     static unsigned long long* buf = nullptr;
-    if (!buf && cudaMalloc(&buf, 64 * 32 * sizeof(unsigned long long)) == cudaSuccess)
-        cudaMemset(buf, 0, 64 * 32 * sizeof(unsigned long long));
+    const size_t n = kTraceCtaBase + (size_t)kTraceMaxCtas * 4;
+    if (!buf && cudaMalloc(&buf, n * sizeof(unsigned long long)) == cudaSuccess)
+        cudaMemset(buf, 0, n * sizeof(unsigned long long));
     return buf;
 }
 }  // namespace pathattn
 extern "C" void path_trace_dump(unsigned long long* host) {
     cudaDeviceSynchronize();
     cudaMemcpy(host, pathattn::trace_buffer(), 64 * 32 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+}
+// Per-CTA stamps of the last launch: ncta x {entry, diagonal issued, exit, SM id}.
+extern "C" void path_trace_cta_dump(unsigned long long* host, int ncta) {
+    cudaDeviceSynchronize();
+    cudaMemcpy(host, pathattn::trace_buffer() + pathattn::kTraceCtaBase,
+               (size_t)ncta * 4 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
 }
 namespace pathattn {
 #endif

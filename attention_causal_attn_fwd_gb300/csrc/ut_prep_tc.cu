@@ -87,8 +87,16 @@ static_assert(B_COUNT * 8 <= RB_SLOT && RB_SLOT + 8 <= 256, "barriers overlap th
 #ifdef PATH_TRACE
 #define UT_TRACE(slot) \
     do { if (p.trace && blockIdx.x == 10 && blockIdx.y == 40) p.trace[(slot)] = clock64(); } while (0)
+// Per-CTA global-timer stamps (every CTA): 0 entry, 1 compute warps' start, 2 exit, 3 SM id.
+constexpr int kUtTraceCtaBase = 64, kUtTraceMaxCtas = 65536;
+#define UT_CTA(slot, val)                                                                           \
+    do {                                                                                            \
+        const unsigned cta_ = blockIdx.y * gridDim.x + blockIdx.x;                                  \
+        if (p.trace && cta_ < kUtTraceMaxCtas) p.trace[kUtTraceCtaBase + cta_ * 4 + (slot)] = (val); \
+    } while (0)
 #else
 #define UT_TRACE(slot) do { } while (0)
+#define UT_CTA(slot, val) do { } while (0)
 #endif
 
 struct UtParams {
@@ -104,6 +112,7 @@ struct UtParams {
     __nv_bfloat16* vfac;         // [BH, Lp, d] V = A W (prefill cache only) or null
     float* kmax2;                // [BH, nch] max |khat|^2 per chunk (PaTH-FoX) or null
     int nch;
+    int ahead;                   // L2 prefetch of the inputs of the CTA launched `ahead` later (0: none)
     WsHeader* hdr;
     unsigned long long limit_ns;
 #ifdef PATH_TRACE
@@ -329,11 +338,19 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     float* sBeta = reinterpret_cast<float*>(sm + RB + 256);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunk = blockIdx.x, bh = blockIdx.y;
+    // Heads run last to first: the scan starts with the first head group, whose
+    // outputs are then the most recently written (still in L2).
+    const int chunk = blockIdx.x, bh = (int)gridDim.y - 1 - (int)blockIdx.y;
     const int row0 = chunk * C;
-    if (chunk == 0 && bh == 0 && threadIdx.x == 0) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {  // the first CTA launched
         p.hdr->status = 0;
         p.hdr->visited = 0;
+    }
+    if (threadIdx.x == 0) {
+        UT_CTA(0, globaltimer());
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        UT_CTA(3, smid);
     }
 
     if (threadIdx.x == 0) {
@@ -362,6 +379,18 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
                 tma_load_3d(sb + R0 + c * 16384, &tm_w, bar(B_LOAD), c * 64, row0, bh);
                 tma_load_3d(sb + R1 + c * 16384, &tm_q, bar(B_LOAD), c * 64, row0, bh);
                 tma_load_3d(sb + R2 + c * 16384, &tm_k, bar(B_LOAD), c * 64, row0, bh);
+            }
+            // warm L2 for the inputs of the CTA launched `ahead` after this one
+            if (p.ahead > 0) {
+                const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x) + p.ahead;
+                if (lin < (int)(gridDim.x * gridDim.y)) {
+                    const int c2 = lin % (int)gridDim.x, bh2 = (int)gridDim.y - 1 - lin / (int)gridDim.x;
+                    for (int c = 0; c < KCH; ++c) {
+                        tma_prefetch_3d(&tm_w, c * 64, c2 * C, bh2);
+                        tma_prefetch_3d(&tm_q, c * 64, c2 * C, bh2);
+                        tma_prefetch_3d(&tm_k, c * 64, c2 * C, bh2);
+                    }
+                }
             }
             drain_wait(bar(B_LOAD), 0, p.limit_ns, p.hdr, 98);
             // Workspace stores: this thread issues each group once the compute
@@ -514,6 +543,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         // All compute warps wait on the same barriers, so they agree on `ok`
         // and reach the named barriers below together.
         if (t == 0) UT_TRACE(0);
+        if (t == 0) UT_CTA(1, globaltimer());
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_G), 0, wc, 50));
         if (t == 0) UT_TRACE(1);
         if (ok) {
@@ -856,19 +886,27 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+    if (threadIdx.x == 0) UT_CTA(2, globaltimer());
 }
 
 #ifdef PATH_TRACE
 static unsigned long long* ut_trace_buffer() {
     static unsigned long long* buf = nullptr;
-    if (!buf && cudaMalloc(&buf, 64 * sizeof(unsigned long long)) == cudaSuccess)
-        cudaMemset(buf, 0, 64 * sizeof(unsigned long long));
+    const size_t n = kUtTraceCtaBase + (size_t)kUtTraceMaxCtas * 4;
+    if (!buf && cudaMalloc(&buf, n * sizeof(unsigned long long)) == cudaSuccess)
+        cudaMemset(buf, 0, n * sizeof(unsigned long long));
     return buf;
 }
 }  // namespace pathattn
 extern "C" void path_ut_trace_dump(unsigned long long* host) {
     cudaDeviceSynchronize();
     cudaMemcpy(host, pathattn::ut_trace_buffer(), 64 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
+}
+// Per-CTA stamps of the last launch: ncta x {entry, compute start, exit, SM id}.
+extern "C" void path_ut_trace_cta_dump(unsigned long long* host, int ncta) {
+    cudaDeviceSynchronize();
+    cudaMemcpy(host, pathattn::ut_trace_buffer() + pathattn::kUtTraceCtaBase,
+               (size_t)ncta * 4 * sizeof(unsigned long long), cudaMemcpyDeviceToHost);
 }
 namespace pathattn {
 #endif
@@ -897,6 +935,14 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
     p.vfac = lay.vfac ? reinterpret_cast<__nv_bfloat16*>(ws + lay.vfac) : nullptr;
     p.kmax2 = want_kmax ? reinterpret_cast<float*>(ws + lay.kmax) : nullptr;
     p.nch = lay.Lp / utk::C;
+    {  // one CTA per SM is resident: prefetch for the CTA one wave ahead
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
+                                                      cudaSuccess)
+            p.ahead = sms;
+        else
+            p.ahead = 0;
+    }
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.limit_ns = 2000000000ull;
 #ifdef PATH_TRACE
