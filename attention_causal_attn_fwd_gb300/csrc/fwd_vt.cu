@@ -66,6 +66,11 @@ __global__ void __launch_bounds__(32 * kVtWarps) path_fwd_vt_rows(
         const int c = 32 * e + lane;
         return c < D ? to_f<T>(row[c]) : 0.f;
     };
+    // rows of this head read or written below lie inside the [B*H, L, D] tensors (checked in
+    // the bounds-checked build only)
+    const long long n_rows = (long long)gridDim.y * L;
+    auto row_ok = [&](int j, int site) { return in_bounds((long long)(hoff + j) * D, D, n_rows * D, hdr, site); };
+    if (!row_ok(i, 224) || !in_bounds((long long)hoff, i + 1, n_rows, hdr, 225)) return;
 
     // walk 1: logits, the query carried backwards through H_i, H_{i-1}, ...
     float u[E];
@@ -73,6 +78,7 @@ __global__ void __launch_bounds__(32 * kVtWarps) path_fwd_vt_rows(
     for (int e = 0; e < E; ++e) u[e] = ld(q + (hoff + i) * D, e);
     float bias = 0.f;  // sum_{s=j+1..i} log f_s
     for (int j = i; j >= 0; --j) {
+        if (!row_ok(j, 226)) break;
         float2 part = make_float2(0.f, 0.f);
         float wj[E];
 #pragma unroll
@@ -103,6 +109,7 @@ __global__ void __launch_bounds__(32 * kVtWarps) path_fwd_vt_rows(
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
     for (int j = 0; j <= i; ++j) {
+        if (!row_ok(j, 227)) break;
         float wj[E];
         if (j > 0) {
             float part = 0.f;
