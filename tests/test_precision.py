@@ -1,6 +1,6 @@
 """The hi + lo bf16 operand split that the tensor-core kernels use for quantities that are not exact
-in bf16 (the UT factor A, tril(Q W^T), Y, Z, Z A, the transported-query master q~, the backward's
-carried U and G, the chunk transitions P_m), checked on the CPU against its error bound.
+in bf16 (the UT factor A and its doubling merge, tril(Q W^T), Y, Z, A W, the backward's carried U
+and G, the chunk transitions P_m), checked on the CPU against its error bound.
 
 x = hi + lo + r with hi = bf16(x), lo = bf16(x - hi): |x - hi| <= 2^-9 |x| and |r| <= 2^-18 |x|
 (round to nearest, 8 significant bits).  A product a b is taken as hi_a hi_b + hi_a lo_b + lo_a hi_b,
@@ -61,3 +61,32 @@ def test_bf16_unit_w_transitions_stay_within_the_fox_skip_margin():
             x = x - 2.0 * (w[s] @ x) * w[s]
             peak = max(peak, np.linalg.norm(x) / x0)
         assert peak < 1.05, peak
+
+
+def test_hi_lo_merge_at_64_keeps_the_solve_accurate():
+    """The UT prep's last doubling merge, A_PQ = -A_PP (G_PQ A_QQ), runs as two hi/lo products on the
+    tensor cores (the intermediate T = G_PQ A_QQ rounded to fp32 and split again).  With unit w and
+    beta in [0, 2] (5 % each at 0 and 2) the merged block stays within 1e-4 of max |A_PQ| of the exact
+    solve, the precision its own hi/lo operands carry into the later products (2^-16 relative)."""
+    rng = np.random.default_rng(11)
+    C, d = 128, 128
+    worst = 0.0
+    for _ in range(8):
+        w = rng.standard_normal((C, d))
+        w /= np.linalg.norm(w, axis=1, keepdims=True)
+        w = _bf16(w).astype(np.float64)
+        beta = 2.0 / (1.0 + np.exp(-2.0 * rng.standard_normal(C)))
+        u = rng.random(C)
+        beta[u < 0.05] = 0.0
+        beta[(u >= 0.05) & (u < 0.10)] = 2.0
+        G = (w @ w.T).astype(np.float32).astype(np.float64)
+        A = np.linalg.solve(np.eye(C) + np.diag(beta) @ np.triu(G, 1), np.diag(beta))
+        P, Q = slice(0, 64), slice(64, 128)
+        gh, gl = _split(G[P, Q])
+        ah, al = _split(A[Q, Q])
+        T = (gh @ ah + gh @ al + gl @ ah).astype(np.float32)
+        th, tl = _split(T)
+        ph, pl = _split(A[P, P])
+        apq = -(ph.astype(np.float64) @ th + ph.astype(np.float64) @ tl + pl.astype(np.float64) @ th)
+        worst = max(worst, np.abs(apq - A[P, Q]).max() / np.abs(A[P, Q]).max())
+    assert worst <= 1e-4, worst
