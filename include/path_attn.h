@@ -108,7 +108,7 @@ int path_attn_fwd(const void* q, const void* k, const void* v, const void* w, co
  * The bf16 tensor-core path stops a query tile's scan once every key further
  * left provably has weight exactly 0 in fp32 (bias plus a bound on the
  * transported logit); the bound assumes the unchecked preconditions above
- * (beta in [0, 2], |w| = 1, up to bf16 rounding of w).
+ * (beta in [0, 2], |w| = 1, up to bf16 rounding of w) and log_f <= 0.
  */
 int path_attn_fwd_fox(const void* q, const void* k, const void* v, const void* w, const float* beta,
                       const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype,
@@ -306,7 +306,8 @@ long long path_fwd_visited_blocks(const void* workspace, path_stream_t stream);
  * later calls visit every key block, non-zero (the default) restores the stop.
  * The stop only skips blocks whose every weight is exactly zero in fp32, so
  * both settings give bit-identical outputs for inputs that meet the
- * preconditions (beta in [0, 2], |w| = 1); the switch exists to test that.
+ * preconditions (beta in [0, 2], |w| = 1, log f <= 0); the switch exists to
+ * test that.
  * It is process-wide and not synchronised with calls already enqueued.
  */
 void path_debug_set_fox_skip(int enabled);
