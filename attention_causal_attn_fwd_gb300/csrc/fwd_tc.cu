@@ -85,7 +85,7 @@ constexpr uint32_t SM_CTL = SM_BAR + 192;
 static_assert(B_COUNT * 8 <= 192, "barriers overlap the control words");
 static_assert(SM_CTL + 52 <= SM_TOTAL, "control words exceed the barrier region");
 
-constexpr int kHeadGroup = 8;
+constexpr int kHeadGroup = 4;
 
 // Use index of the V slot (it & 1) for block iteration it: slot 1 holds -Z of
 // the diagonal first, so its V_m uses are shifted by one.
