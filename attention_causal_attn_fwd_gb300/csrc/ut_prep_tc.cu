@@ -935,11 +935,12 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
     p.vfac = lay.vfac ? reinterpret_cast<__nv_bfloat16*>(ws + lay.vfac) : nullptr;
     p.kmax2 = want_kmax ? reinterpret_cast<float*>(ws + lay.kmax) : nullptr;
     p.nch = lay.Lp / utk::C;
-    {  // one CTA per SM is resident: prefetch for the CTA one wave ahead
+    {  // one CTA per SM is resident: prefetch for the CTA half a wave ahead (A/B: anything from an
+       // eighth to three quarters of a wave does equally well, a whole wave or more is slower)
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) ==
                                                       cudaSuccess)
-            p.ahead = sms;
+            p.ahead = sms / 2;
         else
             p.ahead = 0;
     }
