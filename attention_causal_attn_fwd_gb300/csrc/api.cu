@@ -23,7 +23,8 @@ cudaError_t prefill_kcache(int dtype, int C, int d, const void* k, const void* w
 cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, const void* v_t, const void* w_t,
                         const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t, float* lse_t,
                         int BH, float scale, unsigned char* ws, const DecLayout& lay, bool vt, cudaStream_t st);
-bool fwd_vt_supported(int d, int L);
+bool fwd_vt_supported(int d);
+size_t fwd_vt_workspace_bytes(long long BH, int L, int d);
 cudaError_t fwd_vt(int dtype, int d, const void* q, const void* k, const void* v, const void* w, const float* beta,
                    const float* log_f, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
                    cudaStream_t st);
@@ -247,9 +248,10 @@ int path_decode_step_vt(const void* q_t, const void* k_t, const void* v_t, const
 }
 
 size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype) {
-    if (B < 1 || H < 1 || L < 1 || (long long)B * H > 65535 || !fwd_vt_supported(d, L)) return 0;
+    if (B < 1 || H < 1 || L < 1 || (long long)B * H > 65535 || !fwd_vt_supported(d)) return 0;
+    if ((long long)B * H * L > (1ll << 31) / 256) return 0;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return 0;
-    return sizeof(WsHeader);
+    return fwd_vt_workspace_bytes((long long)B * H, L, d);
 }
 
 int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w, const float* beta,
@@ -257,14 +259,15 @@ int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w,
                      float scale, void* workspace, size_t workspace_bytes, path_stream_t stream) {
     if (B < 1 || H < 1 || L < 1 || d < 1) return PATH_ERR_INVALID;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return PATH_ERR_UNSUPPORTED;
-    if (!causal || !fwd_vt_supported(d, L) || (long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
+    if (!causal || !fwd_vt_supported(d) || (long long)B * H > 65535) return PATH_ERR_UNSUPPORTED;
     if ((long long)B * H * L > (1ll << 31) / 256) return PATH_ERR_UNSUPPORTED;
     if (!q || !k || !v || !w || !beta || !o) return PATH_ERR_INVALID;
     const void* ptrs[] = {q, k, v, w, beta, o};
     for (const void* p : ptrs)
         if (!aligned16(p)) return PATH_ERR_INVALID;
     if ((log_f && !aligned16(log_f)) || (lse && !aligned16(lse))) return PATH_ERR_INVALID;
-    if (!workspace || workspace_bytes < sizeof(WsHeader) || !aligned16(workspace)) return PATH_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < fwd_vt_workspace_bytes((long long)B * H, L, d) || !aligned16(workspace))
+        return PATH_ERR_WORKSPACE;
     cudaError_t e = fwd_vt(dtype, d, q, k, v, w, beta, log_f, o, lse, B * H, L, scale,
                            static_cast<unsigned char*>(workspace), reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {

@@ -262,8 +262,9 @@ int path_decode_step_vt(const void* q_t, const void* k_t, const void* v_t, const
                         size_t workspace_bytes, path_stream_t stream);
 
 /*
- * Workspace size in bytes for path_attn_fwd_vt (a status word only).  Returns 0
- * for unsupported sizes.
+ * Workspace size in bytes for path_attn_fwd_vt: the status header plus a logits
+ * scratch of 16 * ceil(L / 32) * 32 bytes per warp of the launch (at most 256 MB;
+ * past that fewer warps run).  Returns 0 for unsupported sizes.
  */
 size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype);
 
@@ -273,9 +274,12 @@ size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype);
  *     o_i = sum_j softmax_j(s_i.) H_i ... H_{j+1} v_j
  * with the logits s_ij of path_attn_fwd / path_attn_fwd_fox (lse is theirs too).
  * Arguments as path_attn_fwd_fox (log_f nullable); d in {16, 32, 64, 128} for
- * PATH_F32 and PATH_BF16, L <= 8192 (the row's logits are kept in shared
- * memory), B*H <= 65535.  Runs on CUDA cores in fp32, one warp per query row
- * walking its keys twice; results are rounded to the input dtype.
+ * PATH_F32 and PATH_BF16, B*H <= 65535, B*H*L <= 2^23.  `workspace` holds at
+ * least path_attn_fwd_vt_workspace_bytes(B, H, L, d, dtype) bytes (else
+ * PATH_ERR_WORKSPACE); its contents need no initialisation.  Runs on CUDA cores
+ * in fp32: each warp takes four consecutive query rows and walks their keys twice
+ * (the logits right to left into its workspace slot, then the outputs left to
+ * right); results are rounded to the input dtype.
  */
 int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w, const float* beta,
                      const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype, int causal,

@@ -47,6 +47,42 @@ def test_fwd_vt_beta_zero_equals_plain_forward():
     assert float((o_vt.float() - o.float()).abs().max()) <= 2e-2
 
 
+@pytest.mark.parametrize("dtype,H,d,fox", [("bf16", 12, 128, True), ("f32", 16, 64, False)])
+def test_fwd_vt_second_band(dtype, H, d, fox):
+    """More groups of 4 query rows than warps in the launch (L = 1024: 3072 groups on 2432 warps at
+    d = 128, 4096 on 3648 at d = 64), so warps take a second group, in the reversed order."""
+    x = inputs.make_fwd(1, H, 1024, d, dtype, seed=530 + d, fox=fox, edge_frac=0.05)
+    o, lse = _vt_fwd(x)
+    f = inputs.f64
+    o_ref, lse_ref = orc.path_attn(*(f(t) for t in (x.q, x.k, x.v, x.w, x.beta)),
+                                   None if x.log_f is None else f(x.log_f), x.scale, value_transport=True)
+    check(to_np(o), o_ref, x.q.dtype, "fwd vt second band %s d%d" % (dtype, d))
+    check_lse(to_np(lse), lse_ref, x.q.dtype, "fwd vt second band lse")
+
+
+def _sampled_rows(BH, L, n, seed):
+    rng = np.random.default_rng(seed)
+    heads = np.arange(BH)
+    fixed = np.concatenate([heads * L, heads * L + L - 1, heads * L + L - 2])
+    return np.unique(np.concatenate([fixed, rng.integers(0, BH * L, n)]))
+
+
+@pytest.mark.parametrize("H,L,d,fox", [(12, 4096, 128, False), (2, 9000, 64, True)])
+def test_fwd_vt_long_sampled_rows(H, L, d, fox):
+    """The timed value-transport workload (B1 H12 L4096 d128 bf16) and a PaTH-FoX sequence longer
+    than 8192 tokens, checked on sampled rows: the first and last two of every head and 64 drawn at
+    random."""
+    x = inputs.make_fwd(1, H, L, d, "bf16", seed=540 + L, fox=fox)
+    o, lse = _vt_fwd(x)
+    rows = _sampled_rows(H, L, 64, seed=L)
+    f = inputs.f64
+    o_ref, lse_ref = orc.path_attn(*(f(t) for t in (x.q, x.k, x.v, x.w, x.beta)),
+                                   None if x.log_f is None else f(x.log_f), x.scale, rows=rows,
+                                   value_transport=True)
+    check(to_np(o).reshape(-1, d)[rows], o_ref, x.q.dtype, "fwd vt sampled L%d" % L)
+    check_lse(to_np(lse).reshape(-1)[rows], lse_ref, x.q.dtype, "fwd vt sampled lse L%d" % L)
+
+
 def _decode_vt(kc, vc, n0, steps, scale):
     q, k, v, w, beta = (cuda(t) for t in steps)
     ws = P.alloc_workspace(P.path_decode_workspace_bytes(*kc.shape), kc.device)
