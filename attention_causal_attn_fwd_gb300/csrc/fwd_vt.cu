@@ -35,9 +35,10 @@ namespace pathattn {
 constexpr int kVtRows = 4;                        // query rows per warp
 constexpr int kVtWarps = 8;                       // warps per CTA
 constexpr int kVtSms = 152;
-// resident CTAs per SM: the d = 128 walks hold 4 x 128-element rows per lane group
-// and need more than the 80 registers of three CTAs
-__host__ __device__ constexpr int vt_ctas_per_sm(int d) { return d >= 128 ? 2 : 3; }
+// Resident CTAs per SM.  Three CTAs cap the walks at 80 registers; at d = 128 that
+// spills about 80 bytes a thread and still beats two CTAs without spills (125
+// registers), since the walks are latency-bound.
+__host__ __device__ constexpr int vt_ctas_per_sm(int) { return 3; }
 constexpr size_t kVtScratchCap = size_t(256) << 20;  // logits scratch limit (bytes)
 
 // E consecutive elements of one row, loaded and stored as one vector.
@@ -135,14 +136,11 @@ __global__ void __launch_bounds__(32 * kVtWarps, vt_ctas_per_sm(D)) path_fwd_vt_
         const int bh = (int)(g % BH);
         const int i0 = (ngr - 1 - (int)(g / BH)) * R;
         const int imax = min(i0 + R, L) - 1;
-        const size_t hoff = (size_t)bh * L;
+        // 32-bit offsets from the kernel arguments (B*H*L*D < 2^31) keep the walks' registers low
+        const int hr = bh * L;        // the head's first row
+        const int ho = hr * D + col;  // element offset of the lane's first column in that row
         // the head's rows lie inside the [B*H, L, D] tensors (checked in the bounds-checked build only)
-        if (!in_bounds((long long)hoff * D, (long long)L * D, (long long)BH * L * D, hdr, 224)) return;
-        const T* kh = k + hoff * D + col;
-        const T* vh = v + hoff * D + col;
-        const T* wh = w + hoff * D + col;
-        const float* bb = beta + hoff;
-        const float* lf = FOX ? log_f + hoff : nullptr;
+        if (!in_bounds((long long)hr * D, (long long)L * D, (long long)BH * L * D, hdr, 224)) return;
         int ir[R];  // last key of each row; -1 past the end of the sequence
 #pragma unroll
         for (int r = 0; r < R; ++r) ir[r] = i0 + r <= imax ? i0 + r : -1;
@@ -152,18 +150,18 @@ __global__ void __launch_bounds__(32 * kVtWarps, vt_ctas_per_sm(D)) path_fwd_vt_
         float u[R][E];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const Frag<T, E> f = load_frag<T, E>(q + (hoff + i0 + r) * D + col, lane_ok && ir[r] >= 0);
+            const Frag<T, E> f = load_frag<T, E>(q + ho + (i0 + r) * D, lane_ok && ir[r] >= 0);
 #pragma unroll
             for (int e = 0; e < E; ++e) u[r][e] = f.get(e);
         }
         float bias = 0.f, mx = -INFINITY;  // of row r_l: sum_{s=j+1..i} log f_s, running max
-        Frag<T, E> kf0 = load_frag<T, E>(kh + (size_t)imax * D, lane_ok);
-        Frag<T, E> wf0 = load_frag<T, E>(wh + (size_t)imax * D, lane_ok);
-        float bf0 = bb[imax], lf0 = FOX ? lf[imax] : 0.f;
+        Frag<T, E> kf0 = load_frag<T, E>(k + ho + imax * D, lane_ok);
+        Frag<T, E> wf0 = load_frag<T, E>(w + ho + imax * D, lane_ok);
+        float bf0 = beta[hr + imax], lf0 = FOX ? log_f[hr + imax] : 0.f;
         const int j1 = max(imax - 1, 0);
-        Frag<T, E> kf1 = load_frag<T, E>(kh + (size_t)j1 * D, lane_ok);
-        Frag<T, E> wf1 = load_frag<T, E>(wh + (size_t)j1 * D, lane_ok);
-        float bf1 = bb[j1], lf1 = FOX ? lf[j1] : 0.f;
+        Frag<T, E> kf1 = load_frag<T, E>(k + ho + j1 * D, lane_ok);
+        Frag<T, E> wf1 = load_frag<T, E>(w + ho + j1 * D, lane_ok);
+        float bf1 = beta[hr + j1], lf1 = FOX ? log_f[hr + j1] : 0.f;
 #pragma unroll 2
         for (int j = imax; j >= 0; --j) {
             const Frag<T, E> kc = kf0, wc = wf0;
@@ -173,10 +171,10 @@ __global__ void __launch_bounds__(32 * kVtWarps, vt_ctas_per_sm(D)) path_fwd_vt_
             bf0 = bf1;
             lf0 = lf1;
             const int jn = max(j - 2, 0);
-            kf1 = load_frag<T, E>(kh + (size_t)jn * D, lane_ok);
-            wf1 = load_frag<T, E>(wh + (size_t)jn * D, lane_ok);
-            bf1 = bb[jn];
-            if (FOX) lf1 = lf[jn];
+            kf1 = load_frag<T, E>(k + ho + jn * D, lane_ok);
+            wf1 = load_frag<T, E>(w + ho + jn * D, lane_ok);
+            bf1 = beta[hr + jn];
+            if (FOX) lf1 = log_f[hr + jn];
             float x[2 * R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -225,13 +223,13 @@ __global__ void __launch_bounds__(32 * kVtWarps, vt_ctas_per_sm(D)) path_fwd_vt_
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
         }
-        wf0 = load_frag<T, E>(wh, lane_ok);
-        Frag<T, E> vf0 = load_frag<T, E>(vh, lane_ok);
-        bf0 = bb[0];
+        wf0 = load_frag<T, E>(w + ho, lane_ok);
+        Frag<T, E> vf0 = load_frag<T, E>(v + ho, lane_ok);
+        bf0 = beta[hr];
         const int j2 = min(1, imax);
-        wf1 = load_frag<T, E>(wh + (size_t)j2 * D, lane_ok);
-        Frag<T, E> vf1 = load_frag<T, E>(vh + (size_t)j2 * D, lane_ok);
-        bf1 = bb[j2];
+        wf1 = load_frag<T, E>(w + ho + j2 * D, lane_ok);
+        Frag<T, E> vf1 = load_frag<T, E>(v + ho + j2 * D, lane_ok);
+        bf1 = beta[hr + j2];
 #pragma unroll 2
         for (int j = 0; j <= imax; ++j) {
             if ((j & 31) == 0) {  // weights of keys j .. j+31, one per lane
@@ -252,9 +250,9 @@ __global__ void __launch_bounds__(32 * kVtWarps, vt_ctas_per_sm(D)) path_fwd_vt_
             vf0 = vf1;
             bf0 = bf1;
             const int jn = min(j + 2, imax);
-            wf1 = load_frag<T, E>(wh + (size_t)jn * D, lane_ok);
-            vf1 = load_frag<T, E>(vh + (size_t)jn * D, lane_ok);
-            bf1 = bb[jn];
+            wf1 = load_frag<T, E>(w + ho + jn * D, lane_ok);
+            vf1 = load_frag<T, E>(v + ho + jn * D, lane_ok);
+            bf1 = beta[hr + jn];
             const float4 a4 = st[j & 31];
             const float a[R] = {a4.x, a4.y, a4.z, a4.w};
             float x[R];
@@ -283,9 +281,9 @@ __global__ void __launch_bounds__(32 * kVtWarps, vt_ctas_per_sm(D)) path_fwd_vt_
                 Frag<T, E> f;
 #pragma unroll
                 for (int e = 0; e < E; ++e) f.x[e] = from_f<T>(acc[r][e] * inv_l);
-                *reinterpret_cast<Frag<T, E>*>(o + (hoff + i0 + r) * D + col) = f;
+                *reinterpret_cast<Frag<T, E>*>(o + ho + (i0 + r) * D) = f;
             }
-            if (lse && lane == 0) lse[hoff + i0 + r] = m[r] + logf(l);
+            if (lse && lane == 0) lse[hr + i0 + r] = m[r] + logf(l);
         }
         __syncwarp();  // the next group's staging writes come after every lane's reads
     }
