@@ -46,7 +46,9 @@
 //            P_m - I (one K-major B operand of N = 128 + d rows); KM0 holds K
 //            and Y of the diagonal in the same places
 //   V0/V1    V_m, MN-major B            (V0: V of the diagonal, V1: -Z)
-//   Q        Q of the diagonal
+//   Q        Q of the diagonal; once the diagonal's product has completed, the
+//            softmax warps stage each block's bias values there (FoX: c_j;
+//            relative bias: the table window of the block)
 // Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
 // PATH_ERR_TIMEOUT in the workspace status word, every role stops, pending
 // copies and MMAs are drained (bounded) and TMEM is freed before exit.
@@ -397,6 +399,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         int last = n;
         bool ok = true;
+        // FoX: c_j of the block's 128 keys, one float4 per lane, loaded a block ahead and
+        // staged per warp in the Q tile (free once the diagonal's product has completed)
+        float4 c_next = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (FOX && in_bounds((long long)bh * p.Lp + n * kTcC, kTcC, n_bhlp, p.hdr, 203))
+            c_next = __ldg(reinterpret_cast<const float4*>(cumh + n * kTcC) + lane);
+        // relative bias: the 159 table entries (distances) this warp's rows meet in key
+        // block mb, five per lane, loaded a block ahead and staged like c_j
+        const bool rel_ok = REL && in_bounds((long long)(bh % p.H) * p.L, p.L, (long long)p.H * p.L, p.hdr, 204);
+        float r_next[5];
+        auto load_rel = [&](int mb) {
+            const int dmin = row0 - mb * kTcC + 32 * (warp & 3) - 127;
+#pragma unroll
+            for (int k = 0; k < 5; ++k) r_next[k] = __ldg(relh + min(max(dmin + lane + 32 * k, 0), p.L - 1));
+        };
+        if (rel_ok) load_rel(n);
         for (int it = 0; it <= n; ++it) {
             const int m = n - it;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SDONE), it & 1, wc, 20));
@@ -434,13 +451,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 sk_sent = it + 1;
             }
             if (r == 0) TC_TRACE(5, it);
-            if (FOX && in_bounds((long long)bh * p.Lp + m * kTcC, kTcC, n_bhlp, p.hdr, 203)) {
+            if (FOX) {
+                float4* cs = reinterpret_cast<float4*>(sm + SM_Q) + (warp & 3) * 64 + (it & 1) * 32;
+                cs[lane] = c_next;
+                __syncwarp();
+                if (m > 0 && in_bounds((long long)bh * p.Lp + (m - 1) * kTcC, kTcC, n_bhlp, p.hdr, 203))
+                    c_next = __ldg(reinterpret_cast<const float4*>(cumh + (m - 1) * kTcC) + lane);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const float4* cj = reinterpret_cast<const float4*>(cumh + m * kTcC + 32 * c);
+                    const float4* cj = cs + 8 * c;
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 cv = __ldg(cj + j4);
+                        const float4 cv = cj[j4];
                         s[32 * c + 4 * j4 + 0] = fmaf(s[32 * c + 4 * j4 + 0], sl2, (ci - cv.x) * kL2e);
                         s[32 * c + 4 * j4 + 1] = fmaf(s[32 * c + 4 * j4 + 1], sl2, (ci - cv.y) * kL2e);
                         s[32 * c + 4 * j4 + 2] = fmaf(s[32 * c + 4 * j4 + 2], sl2, (ci - cv.z) * kL2e);
@@ -448,17 +470,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
             }
-            if (REL && in_bounds((long long)(bh % p.H) * p.L, p.L, (long long)p.H * p.L, p.hdr, 204)) {
-                // bias at distance i - j, clamped into the table (masked or padding entries)
-                const int base = row0 + r - m * kTcC;
+            if (rel_ok) {
+                // bias at distance i - j, clamped into the table (masked or padding entries):
+                // entry lane - j + 127 of the warp's window
+                float* rs = reinterpret_cast<float*>(sm + SM_Q) + (warp & 3) * 320 + (it & 1) * 160;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float bv[32];
+                for (int k = 0; k < 5; ++k) rs[lane + 32 * k] = r_next[k];
+                __syncwarp();
+                if (m > 0) load_rel(m - 1);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) bv[j] = __ldg(relh + min(max(base - 32 * c - j, 0), p.L - 1));
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) s[32 * c + j] = fmaf(s[32 * c + j], sl2, bv[j] * kL2e);
-                }
+                for (int j = 0; j < 128; ++j) s[j] = fmaf(s[j], sl2, rs[lane - j + 127] * kL2e);
             }
             if (it == 0) {
 #pragma unroll
