@@ -33,7 +33,8 @@
 //               [S | q~](it), P V(it-1): the transport of the next query
 //               overlaps P V, and the softmax of block it overlaps P V
 //   warps 2-5   softmax: S -> P (bf16, into TMEM), row statistics, epilogue
-//   warps 6-9   query transport: fp32 q~ master -> bf16 q~ (TMEM)
+//   warps 6-9   query transport: fp32 q~ master -> bf16 q~ (TMEM), the first half of
+//               its columns released before the second is converted
 // Every MMA reads its A operand from TMEM except the diagonal block's, so
 // shared memory carries only the B tiles (khat, P - I, V) and their TMA writes.
 //
@@ -81,6 +82,7 @@ enum Bar { B_QFULL = 0, B_KMFULL0, B_KMFULL1, B_KMEMPTY0, B_KMEMPTY1, B_VFULL0, 
 // the others arrive.
 constexpr int NB_SK = 3, NB_SK_COUNT = 32 + 128 + 128;  // MMA warp + softmax warps + transport warps
 constexpr int NB_PV = 4, NB_PV_COUNT = 32 + 128;        // MMA warp + softmax warps
+constexpr int NB_SKB = 5, NB_SKB_COUNT = 32 + 128;      // MMA warp + transport warps
 // Barriers at SM_BAR, then the control words (TMEM address, abort flag, FoX
 // stop index and votes, max |khat|^2) at SM_CTL, all inside SM_BAR + 256.
 constexpr uint32_t SM_CTL = SM_BAR + 192;
@@ -282,10 +284,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // therefore waits on nothing but two named barriers per block (no
         // shared-memory round trip): the warps that signal it have already
         // waited for the copies the next MMAs read.
-        //   NB_SK(it)   [S | q~](it) may go: bf16 q~(it) is in TMEM and khat_m,
-        //               P_m - I have landed (transport warps); S(it-1) has been
-        //               read and zeroed and, with FoX, block it is known to be
-        //               visited (softmax warps)
+        //   NB_SK(it)   the first half (in K) of [S | q~](it) may go: the first half
+        //               of bf16 q~(it) is in TMEM and khat_m, P_m - I have landed
+        //               (transport warps); S(it-1) has been read and zeroed and, with
+        //               FoX, block it is known to be visited (softmax warps)
+        //   NB_SKB(it)  its second half may go: the rest of bf16 q~(it) (transport)
         //   NB_PV(it)   P V(it) may go: P(it) is in TMEM and V_m has landed (softmax)
         // Lane 0 issues; the whole warp takes the barriers.
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QFULL), 0, wc, 10) && mbar_wait(bar(B_KMFULL0), 0, wc, 11) &&
@@ -335,12 +338,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     last = it - 1;
                     break;
                 }
+                // [S | q~] += bf16(q~) [khat ; P_m - I]^T  (for m = 0 the q~ half reads
+                // stale slot contents; the master is not used again), in two halves of K:
+                // the first half of bf16 q~ is released (NB_SK) before the transport warps
+                // convert the second (NB_SKB)
                 if (lane == 0) {
                     TC_TRACE(15, it);
                     tc_fence_after();
-                    // [S | q~] += bf16(q~) [khat ; P_m - I]^T  (for m = 0 the q~ half reads
-                    // stale slot contents; the master is not used again)
-                    for (int kk = 0; kk < D / 16; ++kk)
+                    for (int kk = 0; kk < D / 32; ++kk)
+                        mma_ts(tmem + TM_S, tmem + TM_QB + kk * 8, kmajor_desc(sb + SM_KM0 + s * KM_SLOT, kk, 32768),
+                               IDESC_SQ, 1);
+                }
+                __syncwarp();
+                named_bar_sync(NB_SKB, NB_SKB_COUNT);
+                if (lane == 0) {
+                    tc_fence_after();
+                    for (int kk = D / 32; kk < D / 16; ++kk)
                         mma_ts(tmem + TM_S, tmem + TM_QB + kk * 8, kmajor_desc(sb + SM_KM0 + s * KM_SLOT, kk, 32768),
                                IDESC_SQ, 1);
                     mma_commit(bar(B_SDONE));
@@ -652,7 +665,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------------ query-transport warps
         const int r = 32 * (warp & 3) + lane;
         const uint32_t tl = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        int sk_sent = 0;  // NB_SK rounds this warp has arrived on
+        int sk_sent = 0;   // NB_SK rounds this warp has arrived on
+        int skb_sent = 0;  // NB_SKB rounds (the second half of bf16 q~)
+        auto release_second = [&](int it) {
+            tc_fence_before();
+            named_bar_arrive(NB_SKB, NB_SKB_COUNT);
+            skb_sent = it;
+        };
         // bf16 copy of 32 fp32 columns (raw bits) -> 16 packed columns of TMEM
         auto put_bf16 = [&](int c, const uint32_t (&v)[32]) {
             uint32_t pk[16];
@@ -723,6 +742,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (ok) {
                 st = release_block(1);
                 ok = st == 1;
+                if (ok) release_second(1);
             }
         }
         for (int it = 1; it < n && ok; ++it) {  // q~ for block iteration it + 1 (m = n - it > 0)
@@ -732,22 +752,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (st != 1) break;
             if (r == 0) TC_TRACE(8, it);
             tc_fence_after();
-            {
-                uint32_t v[D / 32][32];
+            uint32_t v[D / 32][32];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + TM_QM + 32 * c, v[c]);
-                tmem_wait_ld();
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tl + TM_QM + 32 * c, v[c]);
+            tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) put_bf16(c, v[c]);
-            }
+            for (int c = 0; c < D / 64; ++c) put_bf16(c, v[c]);
             tmem_wait_st();
             st = release_block(it + 1);
             if (st != 1) break;
+#pragma unroll
+            for (int c = D / 64; c < D / 32; ++c) put_bf16(c, v[c]);
+            tmem_wait_st();
+            release_second(it + 1);
             if (r == 0) TC_TRACE(9, it);
         }
         if (st == 3) ok = false;
         if (!ok && n > 0) {  // give the MMA warp every round it may still wait for
             for (int rr = sk_sent + 1; rr <= n; ++rr) named_bar_arrive(NB_SK, NB_SK_COUNT);
+            for (int rr = skb_sent + 1; rr <= n; ++rr) named_bar_arrive(NB_SKB, NB_SKB_COUNT);
         }
     }
     tc_fence_before();
