@@ -514,7 +514,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool stop = false;
             if (FOX) {
                 m_true = fmaxf(m_true, mx);
-                if (m > 0 && !p.no_skip) {
+                // The warps vote on every fourth block only: a vote holds them together
+                // for a shared-memory round trip, and a stop found up to three blocks late
+                // only adds blocks whose P is exactly zero (A/B at L = 16384: 6 % more
+                // blocks, 4 % less time than a vote per block).
+                if (m > 0 && !p.no_skip && (it & 3) == 0) {
                     // Every key left of this block has bias <= c_i - c_(128 m - 1) and
                     // |logit| <= qk_bound: below m_true - 160 (log2) its exp2 is 0 in fp32.
                     const float cprev = in_bounds((long long)bh * p.Lp + m * kTcC - 1, 1, n_bhlp, p.hdr, 205)
