@@ -129,7 +129,13 @@ __global__ void __launch_bounds__(NT) ut_prep_simt(const T* __restrict__ q, cons
 }
 
 // Inclusive cumulative sum of log f per head (PaTH-FoX bias c_i - c_j =
-// sum_{s=j+1..i} log f_s), accumulated in fp64 and stored as fp32.
+// sum_{s=j+1..i} log f_s), accumulated in fp64 and stored as fp32 for every
+// position below Lp (positions >= L add zero).  One CTA per head walks the head
+// in segments of 1024 x kCumRun positions: each thread sums its run of kCumRun
+// consecutive positions serially, the run totals are scanned across the CTA
+// (warp shuffles, then the 32 warp totals), and each thread writes its run with
+// the prefix and the carry of the earlier segments.
+constexpr int kCumRun = 16;
 __global__ void __launch_bounds__(1024) fox_cumsum(const float* __restrict__ log_f, int L, int Lp,
                                                    float* __restrict__ cum) {
     __shared__ double warp_tot[32];
@@ -140,12 +146,19 @@ __global__ void __launch_bounds__(1024) fox_cumsum(const float* __restrict__ log
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     if (threadIdx.x == 0) carry_s = 0.0;
     __syncthreads();
-    for (int base = 0; base < Lp; base += 1024) {
-        const int i = base + threadIdx.x;
-        double x = i < L ? (double)src[i] : 0.0;
+    for (int base = 0; base < Lp; base += 1024 * kCumRun) {
+        const int i0 = base + (int)threadIdx.x * kCumRun;
+        double run[kCumRun];
+        double acc = 0.0;
+#pragma unroll
+        for (int e = 0; e < kCumRun; ++e) {
+            acc += i0 + e < L ? (double)src[i0 + e] : 0.0;
+            run[e] = acc;
+        }
+        double x = acc;  // inclusive scan of the run totals over the CTA
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            double y = __shfl_up_sync(0xffffffffu, x, off);
+            const double y = __shfl_up_sync(0xffffffffu, x, off);
             if (lane >= off) x += y;
         }
         if (lane == 31) warp_tot[wid] = x;
@@ -154,17 +167,18 @@ __global__ void __launch_bounds__(1024) fox_cumsum(const float* __restrict__ log
             double t = warp_tot[lane];
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                double y = __shfl_up_sync(0xffffffffu, t, off);
+                const double y = __shfl_up_sync(0xffffffffu, t, off);
                 if (lane >= off) t += y;
             }
             warp_tot[lane] = t;
         }
         __syncthreads();
-        const double carry = carry_s;
-        x += carry + (wid > 0 ? warp_tot[wid - 1] : 0.0);
-        if (i < Lp) dst[i] = (float)x;
+        const double prefix = carry_s + (wid > 0 ? warp_tot[wid - 1] : 0.0) + (x - acc);
+#pragma unroll
+        for (int e = 0; e < kCumRun; ++e)
+            if (i0 + e < Lp) dst[i0 + e] = (float)(prefix + run[e]);
         __syncthreads();
-        if (threadIdx.x == 1023) carry_s = x;
+        if (threadIdx.x == 1023) carry_s = prefix + acc;
         __syncthreads();
     }
 }
