@@ -485,14 +485,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (rel_ok) {
                 // bias at distance i - j, clamped into the table (masked or padding entries):
-                // entry lane - j + 127 of the warp's window
-                float* rs = reinterpret_cast<float*>(sm + SM_Q) + (warp & 3) * 320 + (it & 1) * 160;
+                // entry lane - j + 127 of the warp's window.  The window is stored four
+                // times (168 floats apart, which spreads a phase of eight lanes over all banks),
+                // copy c shifted down by c entries, so that the four entries a lane
+                // needs for keys 4t .. 4t + 3 (lane + 124 - 4t .. lane + 127 - 4t) form one
+                // aligned float4 of copy lane & 3.  Entries are stored in log2 units.
+                float* rs = reinterpret_cast<float*>(sm + SM_Q) + (warp & 3) * 1344 + (it & 1) * 672;
 #pragma unroll
-                for (int k = 0; k < 5; ++k) rs[lane + 32 * k] = r_next[k];
+                for (int k = 0; k < 5; ++k)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int y = lane + 32 * k - c;
+                        if (y >= 0) rs[c * 168 + y] = r_next[k] * kL2e;
+                    }
                 __syncwarp();
                 if (m > 0) load_rel(m - 1);
+                const float4* rq = reinterpret_cast<const float4*>(rs + (lane & 3) * 168 + (lane & ~3) + 124);
 #pragma unroll
-                for (int j = 0; j < 128; ++j) s[j] = fmaf(s[j], sl2, rs[lane - j + 127] * kL2e);
+                for (int t = 0; t < 32; ++t) {
+                    const float4 b = rq[-t];
+                    s[4 * t + 3] = fmaf(s[4 * t + 3], sl2, b.x);
+                    s[4 * t + 2] = fmaf(s[4 * t + 2], sl2, b.y);
+                    s[4 * t + 1] = fmaf(s[4 * t + 1], sl2, b.z);
+                    s[4 * t + 0] = fmaf(s[4 * t + 0], sl2, b.w);
+                }
             }
             if (it == 0) {
 #pragma unroll
