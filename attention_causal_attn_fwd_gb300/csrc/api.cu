@@ -24,7 +24,7 @@ cudaError_t decode_step(int dtype, int d, const void* q_t, const void* k_t, cons
                         const float* beta_t, void* kc, void* vc, int n_cached, int n_max, void* o_t, float* lse_t,
                         int BH, float scale, unsigned char* ws, const DecLayout& lay, bool vt, cudaStream_t st);
 bool fwd_vt_supported(int d);
-size_t fwd_vt_workspace_bytes(long long BH, int L, int d);
+size_t fwd_vt_workspace_bytes(long long BH, int L, int d, int dtype);
 cudaError_t fwd_vt(int dtype, int d, const void* q, const void* k, const void* v, const void* w, const float* beta,
                    const float* log_f, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
                    cudaStream_t st);
@@ -251,7 +251,7 @@ size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype) {
     if (B < 1 || H < 1 || L < 1 || (long long)B * H > 65535 || !fwd_vt_supported(d)) return 0;
     if ((long long)B * H * L > (1ll << 31) / 256) return 0;
     if (dtype != PATH_F32 && dtype != PATH_BF16) return 0;
-    return fwd_vt_workspace_bytes((long long)B * H, L, d);
+    return fwd_vt_workspace_bytes((long long)B * H, L, d, dtype);
 }
 
 int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w, const float* beta,
@@ -266,7 +266,7 @@ int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w,
     for (const void* p : ptrs)
         if (!aligned16(p)) return PATH_ERR_INVALID;
     if ((log_f && !aligned16(log_f)) || (lse && !aligned16(lse))) return PATH_ERR_INVALID;
-    if (!workspace || workspace_bytes < fwd_vt_workspace_bytes((long long)B * H, L, d) || !aligned16(workspace))
+    if (!workspace || workspace_bytes < fwd_vt_workspace_bytes((long long)B * H, L, d, dtype) || !aligned16(workspace))
         return PATH_ERR_WORKSPACE;
     cudaError_t e = fwd_vt(dtype, d, q, k, v, w, beta, log_f, o, lse, B * H, L, scale,
                            static_cast<unsigned char*>(workspace), reinterpret_cast<cudaStream_t>(stream));

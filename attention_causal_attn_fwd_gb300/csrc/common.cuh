@@ -147,6 +147,38 @@ inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt, bool 
     return s;
 }
 
+// Workspace of the blockwise value-transport forward (bf16, d = 128, chunks of 128):
+// the forward's layout for the key side (lay), a second copy of it for the UT prep
+// run with v in the key slot (lay2, same offsets shifted past lay; only its khat,
+// each value moved to the end of its chunk, is read), the pair store of carried
+// value blocks ([B*H, max(1, N (N - 1) / 2) * 128, d] bf16, N = ceil(L / 128)), the
+// scan's output X ([B*H, L, d] bf16) and its LSE ([B*H, L] fp32).
+struct VtBlockLayout {
+    FwdLayout lay, lay2;
+    size_t pairs, x, lse, total;
+    int N;
+    long long pair_rows;  // rows of the pair store per head
+};
+inline VtBlockLayout vt_block_layout(int B, int H, int L, int d) {
+    VtBlockLayout v;
+    v.lay = fwd_layout(B, H, L, d, 128, 2);
+    const size_t shift = v.lay.total - sizeof(WsHeader);
+    v.lay2 = v.lay;
+    v.lay2.qhat += shift; v.lay2.khat += shift; v.lay2.un += shift; v.lay2.y += shift; v.lay2.zn += shift;
+    v.lay2.cum += shift; v.lay2.kmax += shift; v.lay2.vfac = 0; v.lay2.total += shift;
+    v.N = cdiv(L, 128);
+    const long long npairs = (long long)v.N * (v.N - 1) / 2;
+    v.pair_rows = (npairs > 0 ? npairs : 1) * 128;
+    const size_t BH = (size_t)B * H;
+    size_t off = v.lay2.total;
+    auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 1024); return o; };
+    v.pairs = take(BH * (size_t)v.pair_rows * d * 2);
+    v.x = take(BH * (size_t)L * d * 2);
+    v.lse = take(BH * (size_t)L * sizeof(float));
+    v.total = off;
+    return v;
+}
+
 // Options of the bf16 tensor-core forward that change no result: no_skip
 // visits every key block on the PaTH-FoX path (the far-block stop off).
 struct FwdOptions {

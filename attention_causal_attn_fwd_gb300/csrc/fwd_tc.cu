@@ -139,12 +139,19 @@ struct TcParams {
 
 // MODE 0: PaTH; 1: PaTH-FoX (forget-gate bias, far blocks skipped); 2: PaTH
 // with a relative-position bias table rel[h][i - j].
-template <int D, int MODE>
+// VT (value-side transport, the blockwise form): key block m of query tile n
+// takes its values from the pair store (tm_vp: the block's values carried to
+// the start of chunk n, rows (n (n - 1) / 2 + m) * 128 of the head), and the
+// diagonal block's values are zero (the TMA fill of rows below 0), so O holds
+// only the earlier blocks' terms; the diagonal's are added by the walks that
+// follow (csrc/fwd_vt.cu).
+template <int D, int MODE, bool VT = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     path_fwd_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_khat,
                 const __grid_constant__ CUtensorMap tm_pm, const __grid_constant__ CUtensorMap tm_y,
-                const __grid_constant__ CUtensorMap tm_zn, const TcParams p) {
+                const __grid_constant__ CUtensorMap tm_zn, const __grid_constant__ CUtensorMap tm_vp,
+                const TcParams p) {
     static_assert(D == 64 || D == 128, "head dim");
     constexpr bool FOX = MODE == 1, REL = MODE == 2;
     constexpr bool BIASED = MODE != 0;   // logits carry an additive bias (log2 units in the softmax)
@@ -214,6 +221,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             prefetch_tmap(&tm_q); prefetch_tmap(&tm_k); prefetch_tmap(&tm_v); prefetch_tmap(&tm_khat);
             prefetch_tmap(&tm_pm); prefetch_tmap(&tm_y); prefetch_tmap(&tm_zn);
+            if (VT) prefetch_tmap(&tm_vp);
             // diagonal block: Q, K and Y (KM slot 0), -Z (V slot 1), V (V slot 0)
             mbar_expect_tx(bar(B_QFULL), ROWB);
             for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_Q + c * 16384, &tm_q, bar(B_QFULL), c * 64, row0, bh);
@@ -224,7 +232,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_expect_tx(bar(B_VFULL1), 32768);
             for (int c = 0; c < 2; ++c) tma_load_3d(sb + SM_V1 + c * 16384, &tm_zn, bar(B_VFULL1), c * 64, row0, bh);
             mbar_expect_tx(bar(B_VFULL0), ROWB);
-            for (int c = 0; c < KCH; ++c) tma_load_3d(sb + SM_V0 + c * 16384, &tm_v, bar(B_VFULL0), c * 64, row0, bh);
+            for (int c = 0; c < KCH; ++c)
+                tma_load_3d(sb + SM_V0 + c * 16384, &tm_v, bar(B_VFULL0), c * 64, VT ? -kTcC : row0, bh);
             // Scan blocks, two streams: khat with P - I (one KM slot; the last block,
             // m = 0, needs no P - I) and V, each block iteration it into slot it & 1
             // once that slot's previous contents were consumed (their empty
@@ -256,9 +265,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                     } else {
                         mbar_expect_tx(bar(B_VFULL0 + s), ROWB);
+                        const int vr = VT ? (n * (n - 1) / 2 + (n - it)) * kTcC : r;
                         for (int c = 0; c < KCH; ++c)
-                            tma_load_3d(sb + SM_V0 + (uint32_t)s * 32768u + c * 16384, &tm_v, bar(B_VFULL0 + s),
-                                        c * 64, r, bh);
+                            tma_load_3d(sb + SM_V0 + (uint32_t)s * 32768u + c * 16384, VT ? &tm_vp : &tm_v,
+                                        bar(B_VFULL0 + s), c * 64, vr, bh);
                     }
                     ++issued[1 + 2 * sl + s];
                     TC_TRACE(12 + sl, it);
@@ -831,11 +841,15 @@ namespace pathattn {
 template <int D>
 static cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* log_f, const float* rel_bias,
                              int H, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
-                             const FwdLayout& lay, int fault, const FwdOptions& opt, cudaStream_t st) {
-    CUtensorMap mq, mk, mv, mkh, mpm, my, mzn;
+                             const FwdLayout& lay, int fault, const FwdOptions& opt, cudaStream_t st,
+                             const void* vpairs = nullptr) {
+    CUtensorMap mq, mk, mv, mkh, mpm, my, mzn, mvp;
+    const int ntiles = cdiv(L, kTcC);
+    const int pair_rows = max(1, ntiles * (ntiles - 1) / 2) * kTcC;
     if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mv, v, D, L, BH) ||
         !make_map(&mkh, ws + lay.khat, D, lay.Lp, BH) || !make_map(&mpm, ws + lay.un, D, lay.Lp, BH) ||
-        !make_map(&my, ws + lay.y, kTcC, lay.Lp, BH) || !make_map(&mzn, ws + lay.zn, kTcC, lay.Lp, BH))
+        !make_map(&my, ws + lay.y, kTcC, lay.Lp, BH) || !make_map(&mzn, ws + lay.zn, kTcC, lay.Lp, BH) ||
+        !make_map(&mvp, vpairs ? vpairs : v, D, vpairs ? pair_rows : L, BH))
         return cudaErrorInvalidValue;
     TcParams p;
     p.L = L;
@@ -860,13 +874,52 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
 #ifdef PATH_TRACE
     p.trace = trace_buffer();
 #endif
-    auto kern = log_f ? path_fwd_tc<D, 1> : rel_bias ? path_fwd_tc<D, 2> : path_fwd_tc<D, 0>;
+    auto kern = vpairs ? (log_f ? path_fwd_tc<D, 1, true> : path_fwd_tc<D, 0, true>)
+                       : log_f ? path_fwd_tc<D, 1> : rel_bias ? path_fwd_tc<D, 2> : path_fwd_tc<D, 0>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     mark_start(st);
-    kern<<<dim3(BH * p.ntiles), kTcThreads, kTcSmem, st>>>(mq, mk, mv, mkh, mpm, my, mzn, p);
+    kern<<<dim3(BH * p.ntiles), kTcThreads, kTcSmem, st>>>(mq, mk, mv, mkh, mpm, my, mzn, mvp, p);
     mark_end(st);
     return cudaGetLastError();
+}
+
+cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w, const float* beta, int BH, int L,
+                              unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st,
+                              bool reset_header);
+cudaError_t launch_vt_chain(const void* vhat, const void* pmi, void* pairs, int BH, int Lp, int N,
+                            long long pair_rows, cudaStream_t st);
+cudaError_t launch_vt_diag(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                           const float* log_f, const void* x, const float* lse_in, void* o, float* lse_out, int BH,
+                           int L, float scale, WsHeader* hdr, cudaStream_t st);
+
+// PaTH(-FoX) forward with value-side transport in the blockwise form (bf16, d = 128):
+//   1. the UT prep and FoX sums of the key side, as for path_attn_fwd;
+//   2. the UT prep run with v in the key slot, whose khat is each value moved to
+//      the end of its chunk (vhat_j = H_e ... H_{j+1} v_j);
+//   3. the value chains: per key chunk m, Vtil_{m+1,m} = Vhat_m and
+//      Vtil_{n+1,m} = Vtil_{n,m} P_n^T (CUDA cores, fp32, stored bf16 per pair);
+//   4. the scan with the pair store as the value operand and a zero diagonal:
+//      X_i = sum over earlier chunks of alpha_ij (H_{b-1} ... H_{j+1} v_j), and LSE;
+//   5. per row, the walks of the diagonal chunk: acc <- H_j acc + alpha_ij v_j from
+//      acc = X_i over j = b .. i, which applies H_i ... H_b to X_i and adds the
+//      diagonal's terms.
+cudaError_t fwd_tc_vt_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                           const float* log_f, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
+                           const VtBlockLayout& vl, cudaStream_t st) {
+    cudaError_t e = launch_ut_prep(PATH_BF16, kTcC, 128, q, k, w, beta, log_f, BH, L, ws, vl.lay, st);
+    if (e != cudaSuccess) return e;
+    e = launch_ut_prep_tc(128, q, v, w, beta, BH, L, ws, vl.lay2, false, st, false);
+    if (e != cudaSuccess) return e;
+    e = launch_vt_chain(ws + vl.lay2.khat, ws + vl.lay.un, ws + vl.pairs, BH, vl.lay.Lp, vl.N, vl.pair_rows, st);
+    if (e != cudaSuccess) return e;
+    FwdOptions opt;
+    opt.no_skip = 0;
+    e = launch_tc<128>(q, k, v, log_f, nullptr, 1, ws + vl.x, reinterpret_cast<float*>(ws + vl.lse), BH, L, scale,
+                       ws, vl.lay, 0, opt, st, ws + vl.pairs);
+    if (e != cudaSuccess) return e;
+    return launch_vt_diag(q, k, v, w, beta, log_f, ws + vl.x, reinterpret_cast<const float*>(ws + vl.lse), o, lse,
+                          BH, L, scale, reinterpret_cast<WsHeader*>(ws), st);
 }
 
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,

@@ -291,7 +291,28 @@ __global__ void __launch_bounds__(32 * kVtWarps, vt_ctas_per_sm(D)) path_fwd_vt_
 
 bool fwd_vt_supported(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
-size_t fwd_vt_workspace_bytes(long long BH, int L, int d) { return vt_plan(BH, L, d).bytes; }
+cudaError_t fwd_tc_vt_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
+                           const float* log_f, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
+                           const VtBlockLayout& vl, cudaStream_t st);
+
+// bf16 at d = 128 runs the blockwise form (csrc/fwd_tc.cu, fwd_tc_vt_bf16: the UT prep
+// and the scan on the tensor cores, the value chains and the diagonal walks of
+// csrc/fwd_vt_block.cu) while its workspace, dominated by the pair store of O(L^2 d)
+// bytes per head, stays under 64 GB; every other case runs the row walks above.
+constexpr size_t kVtBlockCap = size_t(64) << 30;
+static bool vt_blockwise(int dtype, int d, long long BH, int L, VtBlockLayout* out) {
+    if (dtype != PATH_BF16 || d != 128 || BH > 65535) return false;
+    const VtBlockLayout v = vt_block_layout(1, (int)BH, L, 128);
+    if (v.total > kVtBlockCap) return false;
+    if (out) *out = v;
+    return true;
+}
+
+size_t fwd_vt_workspace_bytes(long long BH, int L, int d, int dtype) {
+    VtBlockLayout vl;
+    if (vt_blockwise(dtype, d, BH, L, &vl)) return vl.total;
+    return vt_plan(BH, L, d).bytes;
+}
 
 template <typename T, int D, bool FOX>
 static cudaError_t launch_vt(const void* q, const void* k, const void* v, const void* w, const float* beta,
@@ -332,6 +353,9 @@ static cudaError_t launch_vt_d(int d, const void* q, const void* k, const void* 
 cudaError_t fwd_vt(int dtype, int d, const void* q, const void* k, const void* v, const void* w, const float* beta,
                    const float* log_f, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
                    cudaStream_t st) {
+    VtBlockLayout vl;
+    if (vt_blockwise(dtype, d, BH, L, &vl))
+        return fwd_tc_vt_bf16(q, k, v, w, beta, log_f, o, lse, BH, L, scale, ws, vl, st);
     if (dtype == PATH_F32) return launch_vt_d<float>(d, q, k, v, w, beta, log_f, o, lse, BH, L, scale, ws, st);
     return launch_vt_d<__nv_bfloat16>(d, q, k, v, w, beta, log_f, o, lse, BH, L, scale, ws, st);
 }

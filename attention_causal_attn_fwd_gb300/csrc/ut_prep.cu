@@ -20,7 +20,8 @@
 namespace pathattn {
 
 cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w, const float* beta, int BH, int L,
-                              unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st);
+                              unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st,
+                              bool reset_header = true);
 
 template <typename T, int C, int D, int NT>
 struct UtSmem {

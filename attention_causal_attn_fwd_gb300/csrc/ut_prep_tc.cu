@@ -113,6 +113,7 @@ struct UtParams {
     float* kmax2;                // [BH, nch] max |khat|^2 per chunk (PaTH-FoX) or null
     int nch;
     int ahead;                   // L2 prefetch of the inputs of the CTA launched `ahead` later (0: none)
+    int reset;                   // the first CTA clears the workspace header's status and visited count
     WsHeader* hdr;
     unsigned long long limit_ns;
 #ifdef PATH_TRACE
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(utk::kThreads, 1)
     // outputs are then the most recently written (still in L2).
     const int chunk = blockIdx.x, bh = (int)gridDim.y - 1 - (int)blockIdx.y;
     const int row0 = chunk * C;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {  // the first CTA launched
+    if (p.reset && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {  // the first CTA launched
         p.hdr->status = 0;
         p.hdr->visited = 0;
     }
@@ -913,7 +914,8 @@ namespace pathattn {
 
 template <int D>
 static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, const float* beta, int BH, int L,
-                                  unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st) {
+                                  unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st,
+                                  bool reset_header) {
     CUtensorMap mq, mk, mw, mun, my, mzn, mkh, mqh;
     if (!make_map(&mq, q, D, L, BH) || !make_map(&mk, k, D, L, BH) || !make_map(&mw, w, D, L, BH) ||
         !make_map(&mun, ws + lay.un, D, lay.Lp, BH) || !make_map(&my, ws + lay.y, utk::C, lay.Lp, BH) ||
@@ -944,6 +946,7 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
         else
             p.ahead = 0;
     }
+    p.reset = reset_header ? 1 : 0;
     p.hdr = reinterpret_cast<WsHeader*>(ws);
     p.limit_ns = 2000000000ull;
 #ifdef PATH_TRACE
@@ -957,9 +960,10 @@ static cudaError_t launch_ut_tc_d(const void* q, const void* k, const void* w, c
 }
 
 cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w, const float* beta, int BH, int L,
-                              unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st) {
-    if (d == 64) return launch_ut_tc_d<64>(q, k, w, beta, BH, L, ws, lay, want_kmax, st);
-    if (d == 128) return launch_ut_tc_d<128>(q, k, w, beta, BH, L, ws, lay, want_kmax, st);
+                              unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st,
+                              bool reset_header) {
+    if (d == 64) return launch_ut_tc_d<64>(q, k, w, beta, BH, L, ws, lay, want_kmax, st, reset_header);
+    if (d == 128) return launch_ut_tc_d<128>(q, k, w, beta, BH, L, ws, lay, want_kmax, st, reset_header);
     return cudaErrorInvalidValue;
 }
 

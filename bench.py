@@ -434,8 +434,9 @@ def run_ours(args, rank, world, local):
             vflops = fc.attn_flops / fc.B
             vt["forward"] = {"ms": fms_vt, "steps": args.vt_fwd_steps,
                              "attn_equiv_tflops": vflops / (fms_vt * 1e-3) / 1e12,
-                             "workload": "value-transport forward B1 H%d L%d d%d bf16 (CUDA cores, four query "
-                                         "rows per warp, two walks per row)" % (fc.H, fc.L, fc.d)}
+                             "workload": "value-transport forward B1 H%d L%d d%d bf16 (blockwise: UT prep of keys "
+                                         "and values, value chains, tensor-core scan over the carried value "
+                                         "blocks, diagonal walks)" % (fc.H, fc.L, fc.d)}
             del vo, vws
 
     # end to end through the public API with host buffers: pinned inputs -> device, forward, o -> host,

@@ -262,9 +262,12 @@ int path_decode_step_vt(const void* q_t, const void* k_t, const void* v_t, const
                         size_t workspace_bytes, path_stream_t stream);
 
 /*
- * Workspace size in bytes for path_attn_fwd_vt: the status header plus a logits
- * scratch of 16 * ceil(L / 32) * 32 bytes per warp of the launch (at most 256 MB;
- * past that fewer warps run).  Returns 0 for unsupported sizes.
+ * Workspace size in bytes for path_attn_fwd_vt.  For bf16 at d = 128 (the
+ * blockwise form below) it holds two forward layouts, the pair store of carried
+ * value blocks, B*H * max(1, N (N - 1) / 2) * 128 * d bf16 with N = ceil(L / 128),
+ * and the scan's output and LSE; otherwise the status header plus a logits
+ * scratch of 16 * ceil(L / 32) * 32 bytes per warp (at most 256 MB; past that
+ * fewer warps run).  Returns 0 for unsupported sizes.
  */
 size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype);
 
@@ -276,10 +279,18 @@ size_t path_attn_fwd_vt_workspace_bytes(int B, int H, int L, int d, int dtype);
  * Arguments as path_attn_fwd_fox (log_f nullable); d in {16, 32, 64, 128} for
  * PATH_F32 and PATH_BF16, B*H <= 65535, B*H*L <= 2^23.  `workspace` holds at
  * least path_attn_fwd_vt_workspace_bytes(B, H, L, d, dtype) bytes (else
- * PATH_ERR_WORKSPACE); its contents need no initialisation.  Runs on CUDA cores
- * in fp32: each warp takes four consecutive query rows and walks their keys twice
- * (the logits right to left into its workspace slot, then the outputs left to
- * right); results are rounded to the input dtype.
+ * PATH_ERR_WORKSPACE); its contents need no initialisation.
+ * bf16 at d = 128 (while that workspace stays under 64 GB) runs blockwise: the
+ * UT prep of the keys and, with v in the key slot, of the values (each value
+ * moved to the end of its chunk); per key chunk m a chain carrying its values
+ * through every later chunk transition (CUDA cores, fp32, stored bf16 per
+ * (query chunk, key chunk) pair); the tensor-core scan with those blocks as its
+ * values and a zero diagonal; and per row the walks of the diagonal chunk, which
+ * carry the scan's output through the row's own chunk and add the diagonal's
+ * terms.  Every other case runs on CUDA cores in fp32: each warp takes four
+ * consecutive query rows and walks their keys twice (the logits right to left
+ * into its workspace slot, then the outputs left to right).  Results are
+ * rounded to the input dtype.
  */
 int path_attn_fwd_vt(const void* q, const void* k, const void* v, const void* w, const float* beta,
                      const float* log_f, void* o, float* lse, int B, int H, int L, int d, int dtype, int causal,
