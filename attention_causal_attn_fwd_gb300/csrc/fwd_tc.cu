@@ -888,7 +888,7 @@ cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w
                               unsigned char* ws, const FwdLayout& lay, bool want_kmax, cudaStream_t st,
                               bool reset_header);
 cudaError_t launch_vt_chain(const void* vhat, const void* pmi, void* pairs, int BH, int Lp, int N,
-                            long long pair_rows, cudaStream_t st);
+                            long long pair_rows, WsHeader* hdr, cudaStream_t st);
 cudaError_t launch_vt_diag(const void* q, const void* k, const void* v, const void* w, const float* beta,
                            const float* log_f, const void* x, const float* lse_in, void* o, float* lse_out, int BH,
                            int L, float scale, WsHeader* hdr, cudaStream_t st);
@@ -898,7 +898,8 @@ cudaError_t launch_vt_diag(const void* q, const void* k, const void* v, const vo
 //   2. the UT prep run with v in the key slot, whose khat is each value moved to
 //      the end of its chunk (vhat_j = H_e ... H_{j+1} v_j);
 //   3. the value chains: per key chunk m, Vtil_{m+1,m} = Vhat_m and
-//      Vtil_{n+1,m} = Vtil_{n,m} P_n^T (CUDA cores, fp32, stored bf16 per pair);
+//      Vtil_{n+1,m} = Vtil_{n,m} P_n^T (tensor cores, fp32 master in TMEM, stored
+//      bf16 per pair);
 //   4. the scan with the pair store as the value operand and a zero diagonal:
 //      X_i = sum over earlier chunks of alpha_ij (H_{b-1} ... H_{j+1} v_j), and LSE;
 //   5. per row, the walks of the diagonal chunk: acc <- H_j acc + alpha_ij v_j from
@@ -911,7 +912,8 @@ cudaError_t fwd_tc_vt_bf16(const void* q, const void* k, const void* v, const vo
     if (e != cudaSuccess) return e;
     e = launch_ut_prep_tc(128, q, v, w, beta, BH, L, ws, vl.lay2, false, st, false);
     if (e != cudaSuccess) return e;
-    e = launch_vt_chain(ws + vl.lay2.khat, ws + vl.lay.un, ws + vl.pairs, BH, vl.lay.Lp, vl.N, vl.pair_rows, st);
+    e = launch_vt_chain(ws + vl.lay2.khat, ws + vl.lay.un, ws + vl.pairs, BH, vl.lay.Lp, vl.N, vl.pair_rows,
+                        reinterpret_cast<WsHeader*>(ws), st);
     if (e != cudaSuccess) return e;
     FwdOptions opt;
     opt.no_skip = 0;

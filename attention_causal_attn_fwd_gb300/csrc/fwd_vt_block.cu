@@ -1,6 +1,7 @@
-// The two CUDA-core stages of the blockwise value-transport forward (bf16,
-// d = 128, chunks of 128); the tensor-core stages are the UT prep and the scan
-// (csrc/ut_prep_tc.cu, csrc/fwd_tc.cu, fwd_tc_vt_bf16).
+// Two stages of the blockwise value-transport forward (bf16, d = 128, chunks of
+// 128): the value chains (tensor cores) and the diagonal walks (CUDA cores); the
+// other stages are the UT prep and the scan (csrc/ut_prep_tc.cu, csrc/fwd_tc.cu,
+// fwd_tc_vt_bf16).
 //
 // "Resumo Técnico: Por que Transformações Acumuladas Extrapolam?", §"Principais
 // Contribuições" 3: o_i = sum_j alpha_ij H_i ... H_{j+1} v_j with the PaTH steps
@@ -8,21 +9,30 @@
 // Central"), blocked as in that page's §3 "Algoritmo Estilo FlashAttention".
 // With P_c = H_{e_c} ... H_{b_c} the transition of chunk c and vhat_j the value
 // moved to the end of its chunk:
-//   vt_value_chain  Vtil_{n,m} = Vhat_m (P_{n-1} ... P_{m+1})^T for every pair m < n:
-//                   row j of it is v_j carried to the position just before chunk n;
+//   vt_value_chain  Vtil_{n,m} = Vhat_m (P_{n-1} ... P_{m+1})^T for every pair m < n
+//                   (tensor cores): row j of it is v_j carried to the position just
+//                   before chunk n;
 //   vt_diag_walks   o_i = H_i ... H_b X_i + sum_{b <= j <= i} alpha_ij H_i ... H_{j+1} v_j,
 //                   X_i = sum_{j < b} alpha_ij (row j of Vtil_{n,m(j)}) from the scan,
 //                   alpha_ij = exp(s_ij - lse_i) with the scan's LSE.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
+#include "sm100_ptx.cuh"
+#include "tma_host.cuh"
 
 namespace pathattn {
 
 namespace {
 
 constexpr int kVcC = 128;  // chunk (= d)
-constexpr int kVcLd = kVcC + 4;
-constexpr int kVcThreads = 256;
-constexpr size_t kVcSmem = 2 * kVcC * kVcLd * sizeof(float);
+constexpr int kVcThreads = 128;
+constexpr uint32_t VC_SLOT = 32768;                 // one P - I tile (two 64-column boxes of 16 KB)
+constexpr uint32_t VC_BAR = 2 * VC_SLOT;            // full0, full1, mma, drain; then TMEM address, abort
+constexpr size_t kVcSmem = VC_BAR + 64 + 1024;      // + alignment slack
+constexpr uint32_t VC_TM_M = 0, VC_TM_A = 128;      // TMEM: fp32 master [0,128), bf16 copy [128,192)
+enum VcBar { VB_FULL0 = 0, VB_FULL1, VB_MMA, VB_DRAIN };
 
 __device__ __forceinline__ long long pair_index(int n, int m) { return (long long)n * (n - 1) / 2 + m; }
 
@@ -33,85 +43,135 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-// grid (B*H, N - 1), 256 threads; CTA (bh, m) runs the chain of key chunk m (N - 2 - m
-// products), so the longest chains, of every head, are launched first.
-// Vtil is kept transposed in shared memory (VT[k][i] = Vtil[i][k], fp32) so that
-// each thread's 8 x 8 output tile reads 8 consecutive floats of each operand row.
-// P_c^T = I + (P - I) as the UT prep stores it (its row k, column c is entry
-// (k, c) of P_c^T - I), so one step is Vtil += Vtil (P - I).
-__global__ void __launch_bounds__(kVcThreads, 1)
-    vt_value_chain(const __nv_bfloat16* __restrict__ vhat, const __nv_bfloat16* __restrict__ pmi,
-                   __nv_bfloat16* __restrict__ pairs, int Lp, int N, long long pair_rows) {
-    extern __shared__ float vc_smem[];
-    float* VT = vc_smem;                // [k][i]
-    float* PM = vc_smem + kVcC * kVcLd;  // [k][c]
+// grid (B*H, N - 1), 128 threads (thread = row of the block = TMEM lane); CTA (bh, m)
+// runs the chain of key chunk m, N - 2 - m products, the longest chains of every head
+// launched first.  The fp32 master of Vtil stays in TMEM and each step accumulates
+// bf16(Vtil) (P_n - I)^T-as-the-UT-prep-stores-it into it (one M128 N128 K128 product,
+// A from TMEM, P - I from shared memory as an MN-major B operand, as V is in the
+// scan), so the identity part is exact and only the correction is rounded, as for
+// the scan's query transport.  The bf16 copy of each step's result is both the
+// next product's A operand and the pair store's block.  Thread 0 issues the TMA
+// copies (two P - I tiles in flight) and the MMAs; every wait is bounded.
+__global__ void __launch_bounds__(kVcThreads, 2)
+    vt_value_chain(const __grid_constant__ CUtensorMap tm_pm, const __nv_bfloat16* __restrict__ vhat,
+                   __nv_bfloat16* __restrict__ pairs, int Lp, int N, long long pair_rows, WsHeader* hdr,
+                   unsigned long long limit_ns) {
+    using namespace sm100;
+    extern __shared__ uint8_t vc_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vc_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    auto bar = [&](int k) { return sb + VC_BAR + 8u * (uint32_t)k; };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + VC_BAR + 32);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + VC_BAR + 36);
     const int bh = blockIdx.x, m = blockIdx.y;
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int i = threadIdx.x, warp = i >> 5;
     if (m >= N - 1) return;
-    const __nv_bfloat16* vh = vhat + ((size_t)bh * Lp + (size_t)m * kVcC) * kVcC;
-    __nv_bfloat16* ph = pairs + (size_t)bh * (size_t)pair_rows * kVcC;
-    {  // Vtil_{m+1,m} = Vhat_m: to the pair store as it is, and transposed to fp32
-        __nv_bfloat16* dst = ph + (size_t)pair_index(m + 1, m) * kVcC * kVcC;
-        for (int idx = tid; idx < kVcC * 16; idx += kVcThreads) {
-            const int i = idx >> 4, g = idx & 15;
-            const uint4 raw = *reinterpret_cast<const uint4*>(vh + (size_t)i * kVcC + 8 * g);
-            *reinterpret_cast<uint4*>(dst + (size_t)i * kVcC + 8 * g) = raw;
-            const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                VT[(8 * g + 2 * e) * kVcLd + i] = bf_lo(w4[e]);
-                VT[(8 * g + 2 * e + 1) * kVcLd + i] = bf_hi(w4[e]);
-            }
+    const int steps = N - 2 - m;
+    constexpr uint32_t IDESC = idesc_bf16(kVcC, true);
+    if (i == 0) {
+        for (int k = 0; k < 4; ++k) mbar_init(bar(k), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+    const WaitCtl wc{abort_flag, hdr, limit_ns};
+    int issued[2] = {0, 0};  // thread 0: copies issued per slot
+    bool mma_issued = false; // thread 0
+    if (i == 0) {
+        prefetch_tmap(&tm_pm);
+        for (int t = 0; t < 2 && t < steps; ++t) {
+            mbar_expect_tx(bar(VB_FULL0 + t), VC_SLOT);
+            for (int c = 0; c < 2; ++c)
+                tma_load_3d(sb + (uint32_t)t * VC_SLOT + c * 16384, &tm_pm, bar(VB_FULL0 + t), c * 64,
+                            (m + 1 + t) * kVcC, bh);
+            ++issued[t];
         }
     }
-    for (int n = m + 1; n <= N - 2; ++n) {  // Vtil_{n+1,m} = Vtil_{n,m} P_n^T
-        const __nv_bfloat16* pm = pmi + ((size_t)bh * Lp + (size_t)n * kVcC) * kVcC;
-        for (int idx = tid; idx < kVcC * 16; idx += kVcThreads) {
-            const int k = idx >> 4, g = idx & 15;
-            const uint4 raw = *reinterpret_cast<const uint4*>(pm + (size_t)k * kVcC + 8 * g);
-            float4* d4 = reinterpret_cast<float4*>(PM + k * kVcLd + 8 * g);
-            d4[0] = make_float4(bf_lo(raw.x), bf_hi(raw.x), bf_lo(raw.y), bf_hi(raw.y));
-            d4[1] = make_float4(bf_lo(raw.z), bf_hi(raw.z), bf_lo(raw.w), bf_hi(raw.w));
+    __nv_bfloat16* ph = pairs + (size_t)bh * (size_t)pair_rows * kVcC;
+    {  // Vtil_{m+1,m} = Vhat_m: to the pair store as it is, to the master and its bf16 copy
+        const uint4* src = reinterpret_cast<const uint4*>(vhat + ((size_t)bh * Lp + (size_t)m * kVcC + i) * kVcC);
+        uint4* dst = reinterpret_cast<uint4*>(ph + ((size_t)pair_index(m + 1, m) * kVcC + i) * kVcC);
+        uint32_t raw[64];
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {
+            const uint4 x = src[g];
+            dst[g] = x;
+            raw[4 * g] = x.x; raw[4 * g + 1] = x.y; raw[4 * g + 2] = x.z; raw[4 * g + 3] = x.w;
         }
-        __syncthreads();
-        float acc[8][8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int c = 0; c < 4; ++c) {
+            uint32_t f[32];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[r][q] = 0.f;
-#pragma unroll 4
-        for (int k = 0; k < kVcC; ++k) {
-            const float4 a0 = *reinterpret_cast<const float4*>(VT + k * kVcLd + 8 * ty);
-            const float4 a1 = *reinterpret_cast<const float4*>(VT + k * kVcLd + 8 * ty + 4);
-            const float4 b0 = *reinterpret_cast<const float4*>(PM + k * kVcLd + 8 * tx);
-            const float4 b1 = *reinterpret_cast<const float4*>(PM + k * kVcLd + 8 * tx + 4);
-            const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-            for (int r = 0; r < 8; ++r)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[r][q] = fmaf(a[r], b[q], acc[r][q]);
-        }
-        __syncthreads();  // every read of Vtil_{n,m} is done
-        __nv_bfloat16* dst = ph + (size_t)pair_index(n + 1, m) * kVcC * kVcC;
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int i = 8 * ty + r;
-            float v8[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int c = 8 * tx + q;
-                v8[q] = VT[c * kVcLd + i] + acc[r][q];
-                VT[c * kVcLd + i] = v8[q];
+            for (int j = 0; j < 16; ++j) {
+                f[2 * j] = raw[16 * c + j] << 16;
+                f[2 * j + 1] = raw[16 * c + j] & 0xffff0000u;
             }
-            uint4 o;
-            o.x = pack_bf16x2_rn(v8[0], v8[1]);
-            o.y = pack_bf16x2_rn(v8[2], v8[3]);
-            o.z = pack_bf16x2_rn(v8[4], v8[5]);
-            o.w = pack_bf16x2_rn(v8[6], v8[7]);
-            *reinterpret_cast<uint4*>(dst + (size_t)i * kVcC + 8 * tx) = o;
+            tmem_st32(tl + VC_TM_M + 32 * c, f);
+            tmem_st16(tl + VC_TM_A + 16 * c, &raw[16 * c]);
         }
-        __syncthreads();
+        tmem_wait_st();
+    }
+    bool ok = true;
+    for (int t = 0; t < steps; ++t) {  // Vtil_{n+1,m} = Vtil_{n,m} P_n^T, n = m + 1 + t
+        const int n = m + 1 + t, s = t & 1;
+        tc_fence_before();
+        __syncthreads();  // the bf16 copy of Vtil_{n,m} is in TMEM
+        if (i == 0) {
+            if (mbar_wait(bar(VB_FULL0 + s), (uint32_t)((t >> 1) & 1), wc, 70)) {
+                tc_fence_after();
+                for (int kk = 0; kk < kVcC / 16; ++kk)
+                    mma_ts(tmem + VC_TM_M, tmem + VC_TM_A + kk * 8, mnmajor_desc(sb + (uint32_t)s * VC_SLOT, kk),
+                           IDESC, 1);
+                mma_commit(bar(VB_MMA));
+                mma_issued = true;
+            }
+        }
+        ok = __syncthreads_and(mbar_wait(bar(VB_MMA), (uint32_t)(t & 1), wc, 71)) != 0;
+        if (!ok) break;
+        tc_fence_after();
+        if (i == 0 && t + 2 < steps) {  // the slot is free again: P - I of step t + 2
+            mbar_expect_tx(bar(VB_FULL0 + s), VC_SLOT);
+            for (int c = 0; c < 2; ++c)
+                tma_load_3d(sb + (uint32_t)s * VC_SLOT + c * 16384, &tm_pm, bar(VB_FULL0 + s), c * 64,
+                            (n + 2) * kVcC, bh);
+            ++issued[s];
+        }
+        uint4* dst = reinterpret_cast<uint4*>(ph + ((size_t)pair_index(n + 1, m) * kVcC + i) * kVcC);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t f[32], pk[16];
+            tmem_ld32(tl + VC_TM_M + 32 * c, f);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2_rn(__uint_as_float(f[2 * j]), __uint_as_float(f[2 * j + 1]));
+            tmem_st16(tl + VC_TM_A + 16 * c, pk);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) dst[4 * c + g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+        }
+        tmem_wait_st();
+    }
+    // copies and MMAs in flight land before TMEM is released
+    if (i == 0) {
+        if (mma_issued) {
+            mma_commit(bar(VB_DRAIN));
+            drain_wait(bar(VB_DRAIN), 0, limit_ns, hdr, 95);
+        }
+        for (int k = 0; k < 2; ++k)
+            if (issued[k] > 0) drain_wait(bar(VB_FULL0 + k), (uint32_t)((issued[k] - 1) & 1), limit_ns, hdr, 96);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
     }
 }
 
@@ -284,13 +344,15 @@ __global__ void __launch_bounds__(32 * kDwWarps) vt_diag_walks(
 }  // namespace
 
 cudaError_t launch_vt_chain(const void* vhat, const void* pmi, void* pairs, int BH, int Lp, int N,
-                            long long pair_rows, cudaStream_t st) {
+                            long long pair_rows, WsHeader* hdr, cudaStream_t st) {
     if (N < 2) return cudaSuccess;
+    CUtensorMap mpm;
+    if (!make_map(&mpm, pmi, kVcC, Lp, BH)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(vt_value_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kVcSmem);
     if (e != cudaSuccess) return e;
     vt_value_chain<<<dim3(BH, N - 1), kVcThreads, kVcSmem, st>>>(
-        static_cast<const __nv_bfloat16*>(vhat), static_cast<const __nv_bfloat16*>(pmi),
-        static_cast<__nv_bfloat16*>(pairs), Lp, N, pair_rows);
+        mpm, static_cast<const __nv_bfloat16*>(vhat), static_cast<__nv_bfloat16*>(pairs), Lp, N, pair_rows, hdr,
+        2000000000ull);
     return cudaGetLastError();
 }
 
