@@ -152,10 +152,11 @@ inline FwdLayout fwd_layout(int B, int H, int L, int d, int C, size_t elt, bool 
 // run with v in the key slot (lay2, same offsets shifted past lay; only its khat,
 // each value moved to the end of its chunk, is read), the pair store of carried
 // value blocks ([B*H, max(1, N (N - 1) / 2) * 128, d] bf16, N = ceil(L / 128)), the
-// scan's output X ([B*H, L, d] bf16) and its LSE ([B*H, L] fp32).
+// scan's output X ([B*H, L, d] bf16), its LSE ([B*H, L] fp32), the diagonal block's P
+// ([B*H, L, 128] bf16) and the max it was formed with ([B*H, L] fp32).
 struct VtBlockLayout {
     FwdLayout lay, lay2;
-    size_t pairs, x, lse, total;
+    size_t pairs, x, lse, pdiag, m0, total;
     int N;
     long long pair_rows;  // rows of the pair store per head
 };
@@ -175,6 +176,8 @@ inline VtBlockLayout vt_block_layout(int B, int H, int L, int d) {
     v.pairs = take(BH * (size_t)v.pair_rows * d * 2);
     v.x = take(BH * (size_t)L * d * 2);
     v.lse = take(BH * (size_t)L * sizeof(float));
+    v.pdiag = take(BH * (size_t)L * 128 * 2);
+    v.m0 = take(BH * (size_t)L * sizeof(float));
     v.total = off;
     return v;
 }

@@ -132,6 +132,8 @@ struct TcParams {
     int fault;                 // test hook: skip one producer signal
     int no_skip;               // FoX: visit every block (the far-block stop disabled)
     unsigned* visited;         // (query tile, key block) pairs visited, summed over tiles
+    __nv_bfloat16* pdiag;      // VT: the diagonal block's P, [BH, L, 128] bf16
+    float* m0;                 // VT: the max the diagonal's P was formed with (log2 units), [BH, L]
 #ifdef PATH_TRACE
     unsigned long long* trace;
 #endif
@@ -620,6 +622,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     pk[jj] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(tl + TM_P + 16 * c, pk);
+                if (VT && it == 0 && row0 + r < p.L) {  // the diagonal's P for the walks that follow
+                    uint4* pd = reinterpret_cast<uint4*>(p.pdiag + ((size_t)bh * p.L + row0 + r) * kTcC + 32 * c);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) pd[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+                }
             }
             float sum;
             {
@@ -644,6 +651,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_st32(tl + TM_O + 32 * c, ov);
                 }
             }
+            if (VT && it == 0 && row0 + r < p.L) p.m0[(size_t)bh * p.L + row0 + r] = m_use;
             m_run = m_use;
             tmem_wait_st();
             // V_m of this block has landed before P V may go
@@ -842,7 +850,7 @@ template <int D>
 static cudaError_t launch_tc(const void* q, const void* k, const void* v, const float* log_f, const float* rel_bias,
                              int H, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
                              const FwdLayout& lay, int fault, const FwdOptions& opt, cudaStream_t st,
-                             const void* vpairs = nullptr) {
+                             const void* vpairs = nullptr, void* pdiag = nullptr, float* m0 = nullptr) {
     CUtensorMap mq, mk, mv, mkh, mpm, my, mzn, mvp;
     const int ntiles = cdiv(L, kTcC);
     const int pair_rows = max(1, ntiles * (ntiles - 1) / 2) * kTcC;
@@ -871,6 +879,8 @@ static cudaError_t launch_tc(const void* q, const void* k, const void* v, const 
     p.H = H;
     p.no_skip = opt.no_skip;
     p.visited = &p.hdr->visited;
+    p.pdiag = static_cast<__nv_bfloat16*>(pdiag);
+    p.m0 = m0;
 #ifdef PATH_TRACE
     p.trace = trace_buffer();
 #endif
@@ -889,9 +899,9 @@ cudaError_t launch_ut_prep_tc(int d, const void* q, const void* k, const void* w
                               bool reset_header);
 cudaError_t launch_vt_chain(const void* vhat, const void* pmi, void* pairs, int BH, int Lp, int N,
                             long long pair_rows, WsHeader* hdr, cudaStream_t st);
-cudaError_t launch_vt_diag(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                           const float* log_f, const void* x, const float* lse_in, void* o, float* lse_out, int BH,
-                           int L, float scale, WsHeader* hdr, cudaStream_t st);
+cudaError_t launch_vt_diag(const void* v, const void* w, const float* beta, const void* x, const void* pdiag,
+                           const float* m0, const float* lse_in, void* o, float* lse_out, int BH, int L,
+                           WsHeader* hdr, cudaStream_t st);
 
 // PaTH(-FoX) forward with value-side transport in the blockwise form (bf16, d = 128):
 //   1. the UT prep and FoX sums of the key side, as for path_attn_fwd;
@@ -901,10 +911,11 @@ cudaError_t launch_vt_diag(const void* q, const void* k, const void* v, const vo
 //      Vtil_{n+1,m} = Vtil_{n,m} P_n^T (tensor cores, fp32 master in TMEM, stored
 //      bf16 per pair);
 //   4. the scan with the pair store as the value operand and a zero diagonal:
-//      X_i = sum over earlier chunks of alpha_ij (H_{b-1} ... H_{j+1} v_j), and LSE;
-//   5. per row, the walks of the diagonal chunk: acc <- H_j acc + alpha_ij v_j from
-//      acc = X_i over j = b .. i, which applies H_i ... H_b to X_i and adds the
-//      diagonal's terms.
+//      X_i = sum over earlier chunks of alpha_ij (H_{b-1} ... H_{j+1} v_j), LSE, and
+//      the diagonal block's P (bf16) with the max it was formed with;
+//   5. per row, the walk of the diagonal chunk: acc <- H_j acc + alpha_ij v_j from
+//      acc = X_i over j = b .. i (alpha from that P, the max and the LSE), which
+//      applies H_i ... H_b to X_i and adds the diagonal's terms.
 cudaError_t fwd_tc_vt_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,
                            const float* log_f, void* o, float* lse, int BH, int L, float scale, unsigned char* ws,
                            const VtBlockLayout& vl, cudaStream_t st) {
@@ -918,10 +929,11 @@ cudaError_t fwd_tc_vt_bf16(const void* q, const void* k, const void* v, const vo
     FwdOptions opt;
     opt.no_skip = 0;
     e = launch_tc<128>(q, k, v, log_f, nullptr, 1, ws + vl.x, reinterpret_cast<float*>(ws + vl.lse), BH, L, scale,
-                       ws, vl.lay, 0, opt, st, ws + vl.pairs);
+                       ws, vl.lay, 0, opt, st, ws + vl.pairs, ws + vl.pdiag, reinterpret_cast<float*>(ws + vl.m0));
     if (e != cudaSuccess) return e;
-    return launch_vt_diag(q, k, v, w, beta, log_f, ws + vl.x, reinterpret_cast<const float*>(ws + vl.lse), o, lse,
-                          BH, L, scale, reinterpret_cast<WsHeader*>(ws), st);
+    return launch_vt_diag(v, w, beta, ws + vl.x, ws + vl.pdiag, reinterpret_cast<const float*>(ws + vl.m0),
+                          reinterpret_cast<const float*>(ws + vl.lse), o, lse, BH, L, reinterpret_cast<WsHeader*>(ws),
+                          st);
 }
 
 cudaError_t fwd_tc_bf16(const void* q, const void* k, const void* v, const void* w, const float* beta,

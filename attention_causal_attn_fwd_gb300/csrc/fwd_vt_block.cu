@@ -14,7 +14,7 @@
 //                   before chunk n;
 //   vt_diag_walks   o_i = H_i ... H_b X_i + sum_{b <= j <= i} alpha_ij H_i ... H_{j+1} v_j,
 //                   X_i = sum_{j < b} alpha_ij (row j of Vtil_{n,m(j)}) from the scan,
-//                   alpha_ij = exp(s_ij - lse_i) with the scan's LSE.
+//                   alpha_ij = exp(s_ij - lse_i) from the scan's diagonal P and LSE.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -179,21 +179,6 @@ __global__ void __launch_bounds__(kVcThreads, 2)
 constexpr int kDwRows = 4;   // query rows per warp, in lockstep
 constexpr int kDwWarps = 8;
 
-// Sums 8 values over the warp; every lane returns the total of value (lane >> 2) & 7.
-__device__ __forceinline__ float dw_sum_8(const float (&x)[8], int lane) {
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-    float y[4], z[2];
-#pragma unroll
-    for (int v = 0; v < 4; ++v)
-        y[v] = (b4 ? x[v + 4] : x[v]) + __shfl_xor_sync(0xffffffffu, b4 ? x[v] : x[v + 4], 16);
-#pragma unroll
-    for (int v = 0; v < 2; ++v)
-        z[v] = (b3 ? y[v + 2] : y[v]) + __shfl_xor_sync(0xffffffffu, b3 ? y[v] : y[v + 2], 8);
-    float a = (b2 ? z[1] : z[0]) + __shfl_xor_sync(0xffffffffu, b2 ? z[0] : z[1], 4);
-    a += __shfl_xor_sync(0xffffffffu, a, 2);
-    a += __shfl_xor_sync(0xffffffffu, a, 1);
-    return a;
-}
 // Sums 4 values over the warp; every lane returns the total of value (lane >> 3) & 3.
 __device__ __forceinline__ float dw_sum_4(const float (&x)[4], int lane) {
     const bool b4 = lane & 16, b3 = lane & 8;
@@ -209,18 +194,19 @@ __device__ __forceinline__ float dw_sum_4(const float (&x)[4], int lane) {
 }
 
 // grid (ceil(B*H*L / 4 / kDwWarps)), kDwWarps warps; warp = 4 consecutive query rows of one
-// head (one chunk, since 128 is a multiple of 4).  A lane holds 4 consecutive elements of
-// every d = 128 vector.  Walk 1 (right to left, j = i .. b): the logits s_ij of the diagonal
-// chunk, staged in shared memory; walk 2 (left to right, j = b .. i): acc <- H_j acc +
-// alpha_ij v_j from acc = X_i.
-template <bool FOX>
+// head (one chunk, since 128 is a multiple of 4), walked in lockstep.  A lane holds 4
+// consecutive elements of every d = 128 vector.  The weights of the diagonal chunk come
+// from the scan: alpha_ij = P_ij 2^(m0_i - lse_i log2 e), with P the diagonal block's
+// bf16 probabilities formed against the max m0_i; 32 keys at a time, one per lane.  The
+// walk (left to right, j = b .. i) is acc <- H_j acc + alpha_ij v_j from acc = X_i.
 __global__ void __launch_bounds__(32 * kDwWarps) vt_diag_walks(
-    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
-    const __nv_bfloat16* __restrict__ w, const float* __restrict__ beta, const float* __restrict__ log_f,
-    const __nv_bfloat16* __restrict__ x, const float* __restrict__ lse_in, __nv_bfloat16* __restrict__ o,
-    float* __restrict__ lse_out, int BH, int L, float scale, WsHeader* hdr) {
+    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ w, const float* __restrict__ beta,
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ pdiag, const float* __restrict__ m0,
+    const float* __restrict__ lse_in, __nv_bfloat16* __restrict__ o, float* __restrict__ lse_out, int BH, int L,
+    WsHeader* hdr) {
     constexpr int D = 128, E = 4, R = kDwRows;
-    __shared__ float4 stage_all[kDwWarps][kVcC];  // [j - b][row]: logits, then weights
+    constexpr float kL2e = 1.4426950408889634f;
+    __shared__ float4 stage_all[kDwWarps][kVcC];  // [j - b][row]: weights
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ngr = cdiv(L, R);
     const long long g = (long long)blockIdx.x * kDwWarps + warp;
@@ -233,72 +219,35 @@ __global__ void __launch_bounds__(32 * kDwWarps) vt_diag_walks(
     const int ho = hr * D + lane * E;
     if (!in_bounds((long long)hr * D, (long long)L * D, (long long)BH * L * D, hdr, 230)) return;
     float4* st = stage_all[warp];
-    const int r_l = lane >> 3;
     int ir[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) ir[r] = i0 + r <= imax ? i0 + r : -1;
-    const int il = i0 + r_l <= imax ? i0 + r_l : -1;
     auto ld4 = [&](const __nv_bfloat16* p, float (&f)[E]) {
         const uint2 raw = *reinterpret_cast<const uint2*>(p);
         f[0] = bf_lo(raw.x); f[1] = bf_hi(raw.x); f[2] = bf_lo(raw.y); f[3] = bf_hi(raw.y);
     };
-
-    // walk 1: the diagonal chunk's logits, each query carried backwards through H_i, H_{i-1}, ...
-    float u[R][E];
+    float lse_r[R], fac[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        if (ir[r] >= 0) ld4(q + ho + (i0 + r) * D, u[r]);
-        else
-#pragma unroll
-            for (int e = 0; e < E; ++e) u[r][e] = 0.f;
+        lse_r[r] = ir[r] >= 0 ? lse_in[hr + i0 + r] : 0.f;
+        fac[r] = ir[r] >= 0 ? exp2f(m0[hr + i0 + r] - lse_r[r] * kL2e) : 0.f;
     }
-    float bias = 0.f;  // of row r_l: sum_{s=j+1..i} log f_s
-    for (int j = imax; j >= jlo; --j) {
-        float kj[E], wj[E];
-        ld4(k + ho + j * D, kj);
-        ld4(w + ho + j * D, wj);
-        const float bj = beta[hr + j];
-        float xs[2 * R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float a = 0.f, b = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-                a = fmaf(kj[e], u[r][e], a);
-                b = fmaf(wj[e], u[r][e], b);
-            }
-            xs[2 * r] = a;
-            xs[2 * r + 1] = b;
-        }
-        const float sum = dw_sum_8(xs, lane);  // lanes 8r..8r+3: k_j . u_r; 8r+4..8r+7: w_j . u_r
-        const float s = fmaf(scale, sum, bias);
-        if (FOX && j <= il) bias += log_f[hr + j];
-        if ((lane & 7) == 0) reinterpret_cast<float*>(&st[j - jlo])[r_l] = s;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float t = j <= ir[r] ? bj * __shfl_sync(0xffffffffu, sum, 8 * r + 4) : 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) u[r][e] = fmaf(-t, wj[e], u[r][e]);
-        }
-    }
-    __syncwarp();
-    // weights alpha_ij = exp(s_ij - lse_i), 32 keys at a time (lane = key)
-    float lse_r[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) lse_r[r] = ir[r] >= 0 ? lse_in[hr + i0 + r] : 0.f;
     for (int jb = jlo; jb <= imax; jb += 32) {
         const int j = jb + lane;
-        float4 sv = j <= imax ? st[j - jlo] : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float sr[R] = {sv.x, sv.y, sv.z, sv.w};
         float ew[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) ew[r] = j <= ir[r] ? expf(sr[r] - lse_r[r]) : 0.f;
-        __syncwarp();
+        for (int r = 0; r < R; ++r) {
+            ew[r] = 0.f;
+            if (j <= ir[r]) {
+                const unsigned short raw =
+                    *reinterpret_cast<const unsigned short*>(pdiag + ((size_t)hr + i0 + r) * kVcC + (j - jlo));
+                ew[r] = __uint_as_float((uint32_t)raw << 16) * fac[r];
+            }
+        }
         if (j <= imax) st[j - jlo] = make_float4(ew[0], ew[1], ew[2], ew[3]);
     }
     __syncwarp();
 
-    // walk 2: from acc = X_i, the diagonal chunk's steps and terms
     float acc[R][E];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -307,11 +256,22 @@ __global__ void __launch_bounds__(32 * kDwWarps) vt_diag_walks(
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[r][e] = 0.f;
     }
+    float wn[E], vn[E];
+    ld4(w + ho + jlo * D, wn);
+    ld4(v + ho + jlo * D, vn);
+    float bn = beta[hr + jlo];
     for (int j = jlo; j <= imax; ++j) {
         float wj[E], vj[E];
-        ld4(w + ho + j * D, wj);
-        ld4(v + ho + j * D, vj);
-        const float bj = beta[hr + j];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            wj[e] = wn[e];
+            vj[e] = vn[e];
+        }
+        const float bj = bn;
+        const int jn = min(j + 1, imax);
+        ld4(w + ho + jn * D, wn);
+        ld4(v + ho + jn * D, vn);
+        bn = beta[hr + jn];
         const float4 a4 = st[j - jlo];
         const float a[R] = {a4.x, a4.y, a4.z, a4.w};
         float xs[R];
@@ -356,17 +316,16 @@ cudaError_t launch_vt_chain(const void* vhat, const void* pmi, void* pairs, int 
     return cudaGetLastError();
 }
 
-cudaError_t launch_vt_diag(const void* q, const void* k, const void* v, const void* w, const float* beta,
-                           const float* log_f, const void* x, const float* lse_in, void* o, float* lse_out, int BH,
-                           int L, float scale, WsHeader* hdr, cudaStream_t st) {
+cudaError_t launch_vt_diag(const void* v, const void* w, const float* beta, const void* x, const void* pdiag,
+                           const float* m0, const float* lse_in, void* o, float* lse_out, int BH, int L,
+                           WsHeader* hdr, cudaStream_t st) {
     const long long groups = (long long)BH * cdiv(L, kDwRows);
     const int ctas = (int)((groups + kDwWarps - 1) / kDwWarps);
-    auto kern = log_f ? vt_diag_walks<true> : vt_diag_walks<false>;
     mark_start(st);
-    kern<<<ctas, 32 * kDwWarps, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
-        static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(w), beta, log_f,
-        static_cast<const __nv_bfloat16*>(x), lse_in, static_cast<__nv_bfloat16*>(o), lse_out, BH, L, scale, hdr);
+    vt_diag_walks<<<ctas, 32 * kDwWarps, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(w), beta,
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(pdiag), m0, lse_in,
+        static_cast<__nv_bfloat16*>(o), lse_out, BH, L, hdr);
     mark_end(st);
     return cudaGetLastError();
 }

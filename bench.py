@@ -419,10 +419,10 @@ def run_ours(args, rank, world, local):
                          "workload": "decode B%d H%d d%d bf16 at a %d-token cache; K and V transported in place"
                                      % (dc.B, dc.H, dc.d, dc.n0)}}
         if args.vt_fwd_steps > 0:
-            vq, vk_, vv, vw, vb = (t[:1] for t in (q, k, v, w, beta))
+            vq, vk_, vv, vw, vb = q, k, v, w, beta  # the forward's workload
             vo = torch.empty_like(vq)
-            vws = P.alloc_workspace(P.load().path_attn_fwd_vt_workspace_bytes(1, fc.H, fc.L, fc.d, P._DT[vq.dtype]),
-                                    dev)
+            vws = P.alloc_workspace(P.load().path_attn_fwd_vt_workspace_bytes(fc.B, fc.H, fc.L, fc.d,
+                                                                              P._DT[vq.dtype]), dev)
             P.path_attn_fwd_vt(vq, vk_, vv, vw, vb, scale=x.scale, out=vo, workspace=vws)
             torch.cuda.synchronize()
             a.record()
@@ -431,12 +431,12 @@ def run_ours(args, rank, world, local):
             b.record()
             torch.cuda.synchronize()
             fms_vt = a.elapsed_time(b) / args.vt_fwd_steps
-            vflops = fc.attn_flops / fc.B
+            vflops = fc.attn_flops
             vt["forward"] = {"ms": fms_vt, "steps": args.vt_fwd_steps,
                              "attn_equiv_tflops": vflops / (fms_vt * 1e-3) / 1e12,
-                             "workload": "value-transport forward B1 H%d L%d d%d bf16 (blockwise: UT prep of keys "
-                                         "and values, value chains, tensor-core scan over the carried value "
-                                         "blocks, diagonal walks)" % (fc.H, fc.L, fc.d)}
+                             "workload": "value-transport forward B%d H%d L%d d%d bf16 (blockwise: UT prep of "
+                                         "keys and values, value chains, tensor-core scan over the carried value "
+                                         "blocks, diagonal walks)" % (fc.B, fc.H, fc.L, fc.d)}
             del vo, vws
 
     # end to end through the public API with host buffers: pinned inputs -> device, forward, o -> host,

@@ -67,14 +67,15 @@ def _sampled_rows(BH, L, n, seed):
     return np.unique(np.concatenate([fixed, rng.integers(0, BH * L, n)]))
 
 
-@pytest.mark.parametrize("H,L,d,fox", [(12, 4096, 128, False), (2, 9000, 64, True)])
-def test_fwd_vt_long_sampled_rows(H, L, d, fox):
-    """The timed value-transport workload (B1 H12 L4096 d128 bf16) and a PaTH-FoX sequence longer
-    than 8192 tokens, checked on sampled rows: the first and last two of every head and 64 drawn at
-    random."""
-    x = inputs.make_fwd(1, H, L, d, "bf16", seed=540 + L, fox=fox)
+@pytest.mark.parametrize("B,H,L,d,fox", [(8, 12, 4096, 128, False), (1, 12, 4096, 128, True),
+                                         (2, 2, 9000, 128, True), (1, 2, 9000, 64, True)])
+def test_fwd_vt_long_sampled_rows(B, H, L, d, fox):
+    """The timed value-transport workload (B8 H12 L4096 d128 bf16), its PaTH-FoX variant at B1, and
+    PaTH-FoX sequences longer than 8192 tokens (blockwise at d = 128, row walks at d = 64), checked
+    on sampled rows: the first and last two of every head and 64 drawn at random."""
+    x = inputs.make_fwd(B, H, L, d, "bf16", seed=540 + L, fox=fox)
     o, lse = _vt_fwd(x)
-    rows = _sampled_rows(H, L, 64, seed=L)
+    rows = _sampled_rows(B * H, L, 64, seed=L)
     f = inputs.f64
     o_ref, lse_ref = orc.path_attn(*(f(t) for t in (x.q, x.k, x.v, x.w, x.beta)),
                                    None if x.log_f is None else f(x.log_f), x.scale, rows=rows,
