@@ -198,8 +198,10 @@ __device__ __forceinline__ float dw_sum_4(const float (&x)[4], int lane) {
 // consecutive elements of every d = 128 vector.  The weights of the diagonal chunk come
 // from the scan: alpha_ij = P_ij 2^(m0_i - lse_i log2 e), with P the diagonal block's
 // bf16 probabilities formed against the max m0_i; 32 keys at a time, one per lane.  The
-// walk (left to right, j = b .. i) is acc <- H_j acc + alpha_ij v_j from acc = X_i.
-__global__ void __launch_bounds__(32 * kDwWarps) vt_diag_walks(
+// walk (left to right, j = b .. i) is acc <- H_j acc + alpha_ij v_j from acc = X_i.  The
+// walk is latency-bound: four CTAs per SM (64 registers) beat three (A/B 0.574 against 0.611 ms
+// for the whole B1 H12 L4096 call), eight rows per warp or two were slower.
+__global__ void __launch_bounds__(32 * kDwWarps, 4) vt_diag_walks(
     const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ w, const float* __restrict__ beta,
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ pdiag, const float* __restrict__ m0,
     const float* __restrict__ lse_in, __nv_bfloat16* __restrict__ o, float* __restrict__ lse_out, int BH, int L,
