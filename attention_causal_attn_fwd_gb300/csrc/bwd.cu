@@ -42,8 +42,9 @@
 //                                       (csrc/bwd_tc.cu) does this on the
 //                                       tensor cores from the bf16 pair store
 //   bwd_local  one CTA per chunk        diagonal block and the within-chunk
-//                                       walks in reverse; writes dq, dk, dv,
-//                                       dw, dbeta (shared-memory atomics)
+//                                       walks in reverse, in the compact form
+//                                       (products and one triangular
+//                                       inverse); writes dq, dk, dv, dw, dbeta
 //   bwd_fox_suffix one CTA per head     dlog f_s = sum_{t >= s} dc_t
 // The contractions here are register-tiled fp32 GEMMs on K-major shared-memory operands.
 // Nothing here waits on another CTA, so these kernels have no spin waits (the
@@ -66,13 +67,6 @@ namespace {
 constexpr int kC = kBwdC;
 constexpr int kNT = 256;
 constexpr int kNW = kNT / 32;
-constexpr int kNTL = 1024;  // bwd_local: latency-bound walks, one warp per row / key / position
-constexpr int kNWL = kNTL / 32;
-// Rows of a chunk in "snake" order over the walking warps: warp w takes rows w, 2 kNWL - 1 - w,
-// 2 kNWL + w, ...  A row's walk is as long as its distance from the chunk's first (or last)
-// position, so pairing a short walk with a long one gives every warp the same number of steps.
-// Row numbers grow with t, so a loop over t ends at the first row >= c.
-__device__ __forceinline__ int snake_row(int t, int wid) { return t * kNWL + ((t & 1) ? kNWL - 1 - wid : wid); }
 constexpr int kNTP = 512;  // bwd_prep: sixteen latency-bound walks in flight per CTA
 
 struct BwdParams {
@@ -150,14 +144,6 @@ __device__ __forceinline__ float vstep(float (&a)[WV<D>::R], const float* w, flo
     vaxpy<D>(a, w, beta * t, lane);
     return t;
 }
-// shared-memory accumulate s += f * a
-template <int D>
-__device__ __forceinline__ void vred(float* s, const float (&a)[WV<D>::R], float f, int lane) {
-    if (!WV<D>::ok(lane)) return;
-#pragma unroll
-    for (int r = 0; r < WV<D>::R; ++r) atomicAdd(s + lane + 32 * r, f * a[r]);
-}
-
 // Rows [0, rows) of a row-major global array of COLS columns (leading dim lds, rows starting
 // on 16-byte boundaries) into shared memory (leading dim ldd) as fp32; rows >= valid read as
 // zero.  16-byte loads, several in flight per thread; plain (coherent) loads, since a CTA
@@ -332,7 +318,6 @@ __device__ __forceinline__ void store_tile_t(float* dst, int ld, const typename 
 
 // ------------------------------------------------------------------ shared-memory sizes (floats)
 template <int D> struct BwdSmem {
-    static constexpr int LDP = D + 1;              // bwd_prep / bwd_local d x d tiles
     static constexpr int LC = kC + 4, LD = D + 4;  // K-major GEMM operands (16-byte rows)
     static constexpr int RK = (D * LC > kC * LD ? D * LC : kC * LD);
     static constexpr int RV = (D * LC > kC * LC ? D * LC : kC * LC);
@@ -340,10 +325,8 @@ template <int D> struct BwdSmem {
     static constexpr int pm = D * (kC + 4) + 2 * kC * (D + 4) + 3 * kC * (kC + 4) + kC;
     static constexpr int chain = 2 * D * LC + RK + RV + D * LD + 6 * kC;
     static constexpr int reduce = 3 * kC * LD + 2 * kC * LC;
-    static constexpr int wbuf = 3 * kC;  // bwd_local per-warp scalars; its last phase keeps [2][D] per warp in aV
-    static constexpr int local = 6 * kC * D + 4 * kC + kNWL * wbuf;
-    static_assert(kNWL * 2 * D <= kC * D, "the last phase's per-warp vectors must fit over aV");
-    static_assert(3 * kC * D >= D * LDP, "dP must fit over the key, value and dk tiles");
+    static constexpr int slot = kC * LC;              // bwd_local: one C x (C + 4) tile
+    static constexpr int local = 13 * slot + 6 * kC;  // thirteen slots, six per-position vectors
     static_assert(chain * 4 <= 227 * 1024 && local * 4 <= 227 * 1024 && reduce * 4 <= 227 * 1024,
                   "shared memory per CTA");
 };
@@ -643,167 +626,420 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
 }
 
 // ------------------------------------------------------------------ bwd_local
+// The diagonal block and the within-chunk walks, reversed in the compact ("UT") form of
+// "Representação de Transformação UT" (§3) instead of position by position.  For chunk n with
+// rows W, Q, K of w, q, k (C rows, padded rows zero, beta = 0 there):
+//
+//   G = W W^T,  X = (I + D triu_1 G)^{-1} (unit upper triangular),  A = X D,  D = diag(beta)
+//   H_{a} ... H_{b} = I - W_{a:b}^T A_{a:b} W_{a:b} for a <= b (a principal block of A), so
+//   Qm = tril(Q W^T) (b <= i), Km = striu(K W^T) (a > j),  Y = Qm A^T,  Z = Km A,
+//   qbar = Q - Y W,  khat = K - Z W,  P_n = I - W^T A W,
+//   S = scale (Q K^T - Y Km^T) + c_i - c_j on j <= i        (the diagonal logits)
+//
+// Given dQbar (from the chains), dKhat and dP_n (from the per-key-chunk sums) and
+// dS = P o (dO V^T - Delta) on the diagonal block, the reverse mode of these products is
+//
+//   dV  = P^T dO,  dZ = -dKhat W^T,  dY = -dQbar W^T - dSs Km       (dSs = scale dS)
+//   dKw = striu(-dSs^T Y + dZ A^T),  dQw = tril(dY A)
+//   dA  = Km^T dZ + dY^T Qm - W dP W^T,  dbeta_b += sum_a X_ab dA_ab
+//   dM  = -X^T (dA D) X^T,  dG = striu(D dM),  dbeta_a += sum_{b>a} dM_ab G_ab
+//   dW  = -Y^T dQbar - Z^T dKhat - A (W dP^T) - A^T (W dP) + dQw^T Q + dKw^T K + (dG + dG^T) W
+//   dQ  = dQbar + dSs K + dQw W,   dK = dKhat + dSs^T Q + dKw W
+//
+// every step a register-tiled fp32 product on shared-memory operands; the only sequential
+// part is the triangular inverse.  Thirteen shared-memory slots of one C x (C + 4) tile each
+// hold the operands; a d x C or C x d tile takes two adjacent slots at d = 128 and the d x d
+// gradient dP four.  The slot of every matrix and the phase that frees it are listed beside
+// the code.
+
+// Thread tiling of an M x N output over the kNT threads: TM consecutive rows by TN consecutive
+// columns per thread.  MM numbers the tiles down the rows first (a warp spans many rows and one
+// or two column groups), otherwise across the columns first.
+template <int M, int N, bool MM> struct TT {
+    static constexpr int TOT = M * N / kNT;
+    static constexpr int TN = TOT >= 32 ? 8 : (TOT >= 4 ? 4 : 1);
+    static constexpr int TM = TOT / TN;
+    static constexpr int GN = N / TN, GM = M / TM;
+    static_assert(TOT >= 1 && GM * GN == kNT && GM * TM == M && GN * TN == N, "tiling");
+    static __device__ __forceinline__ int m0() { return (MM ? (int)threadIdx.x % GM : (int)threadIdx.x / GN) * TM; }
+    static __device__ __forceinline__ int n0() { return (MM ? (int)threadIdx.x / GM : (int)threadIdx.x % GN) * TN; }
+    using Acc = float[TM][TN];
+    static __device__ __forceinline__ void zero(Acc& a) {
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j) a[i][j] = 0.f;
+    }
+};
+
+// acc[i][j] += (or -=) sum_k a(m0 + i, k) b(k, n0 + j).  A is K-major (a(m, k) = A[k lda + m])
+// when AK, else row-major (A[m lda + k]); B is K-major (b(k, n) = B[k ldb + n]) when BK, else
+// B[n ldb + k].  Four k per step, every shared-memory load 16 bytes wide (or the tile's width).
+// A row-major A is read conflict-free with the column-first tiling, a row-major B with the
+// row-first one (leading dims of C + 4 floats).
+template <int M, int N, int K, bool MM, bool AK, bool BK, bool NEG = false>
+__device__ __forceinline__ void mmul(typename TT<M, N, MM>::Acc& acc, const float* A, int lda, const float* B,
+                                     int ldb) {
+    using G = TT<M, N, MM>;
+    constexpr int TM = G::TM, TN = G::TN;
+    static_assert(K % 4 == 0, "depth");
+    const int m0 = G::m0(), n0 = G::n0();
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float a[4][TM], b[4][TN];
+        if constexpr (AK) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) lds_vec<TM>(a[kk], A + (k + kk) * lda + m0);
+        } else {
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const float4 x = *reinterpret_cast<const float4*>(A + (m0 + i) * lda + k);
+                a[0][i] = x.x; a[1][i] = x.y; a[2][i] = x.z; a[3][i] = x.w;
+            }
+        }
+        if constexpr (BK) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) lds_vec<TN>(b[kk], B + (k + kk) * ldb + n0);
+        } else {
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const float4 x = *reinterpret_cast<const float4*>(B + (n0 + j) * ldb + k);
+                b[0][j] = x.x; b[1][j] = x.y; b[2][j] = x.z; b[3][j] = x.w;
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const float av = NEG ? -a[kk][i] : a[kk][i];
+#pragma unroll
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(av, b[kk][j], acc[i][j]);
+            }
+    }
+}
+
+// dst[r ld + col] = f(r, col, acc) over the thread's tile, or dst[col ld + r] when TR
+template <int M, int N, bool MM, bool TR, typename F>
+__device__ __forceinline__ void mstore(float* dst, int ld, const typename TT<M, N, MM>::Acc& acc, F f) {
+    using G = TT<M, N, MM>;
+    const int m0 = G::m0(), n0 = G::n0();
+    if constexpr (!TR) {
+#pragma unroll
+        for (int i = 0; i < G::TM; ++i) {
+            float v[G::TN];
+#pragma unroll
+            for (int j = 0; j < G::TN; ++j) v[j] = f(m0 + i, n0 + j, acc[i][j]);
+            sts_vec<G::TN>(dst + (m0 + i) * ld + n0, v);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < G::TN; ++j) {
+            float v[G::TM];
+#pragma unroll
+            for (int i = 0; i < G::TM; ++i) v[i] = f(m0 + i, n0 + j, acc[i][j]);
+            sts_vec<G::TM>(dst + (n0 + j) * ld + m0, v);
+        }
+    }
+}
+
+// rows r < c of a C x D result to global memory: dst[r][e] = acc + (add ? add[r][e] : 0)
+template <int D, typename E>
+__device__ __forceinline__ void mstore_out(E* dst, const typename TT<kC, D, false>::Acc& acc, const float* add,
+                                           int c) {
+    using G = TT<kC, D, false>;
+    const int m0 = G::m0(), n0 = G::n0();
+#pragma unroll
+    for (int i = 0; i < G::TM; ++i) {
+        const int r = m0 + i;
+        if (r >= c) continue;
+#pragma unroll
+        for (int j = 0; j < G::TN; ++j) {
+            const float x = acc[i][j] + (add ? add[(size_t)r * D + n0 + j] : 0.f);
+            dst[(size_t)r * D + n0 + j] = from_f<E>(x);
+        }
+    }
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
-    constexpr int C = kC, R = WV<D>::R, LDP = BwdSmem<D>::LDP, WB = BwdSmem<D>::wbuf;
-    extern __shared__ float smem[];
-    float* sW = smem;          // [C][D] w
-    float* sK = sW + C * D;    // [C][D] raw keys
-    float* sV = sK + C * D;    // [C][D] values
-    float* aK = sV + C * D;    // [C][D] dk
-    float* aV = aK + C * D;    // [C][D] dv, diagonal part
-    float* aW = aV + C * D;    // [C][D] dw
-    float* sB = aW + C * D;    // [C] beta
-    float* sC = sB + C;        // [C] c (FoX)
-    float* aB = sC + C;        // [C] dbeta
-    float* aC = aB + C;        // [C] dc (FoX), diagonal part
-    float* sBuf = aC + C;      // [kNWL][WB] per-warp scalars
-    float* sDP = sK;           // [D][LDP] dP_n in the last phase (over sK, sV, aK)
+__global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
+    constexpr int C = kC, LC = C + 4, LD = D + 4, U = BwdSmem<D>::slot;
+    constexpr int KH = D < 64 ? D : 64, NH = D / KH;  // d x C operands in pieces of KH rows
+    static_assert(C == 64 && kNT == 4 * C, "the triangular inverse takes four threads per column");
+    static_assert(C * LD <= 2 * U && D * LC <= 2 * U && D * LD <= 4 * U && KH * LC <= U, "slot sizes");
+    extern __shared__ __align__(16) float smem[];
+    auto slot = [&](int i) { return smem + i * U; };
+    float* sB = smem + 13 * U;  // [C] beta
+    float* sC = sB + C;         // [C] c (FoX)
+    float* sL = sC + C;         // [C] lse
+    float* sDl = sL + C;        // [C] Delta
+    float* aB = sDl + C;        // [C] dbeta
+    float* aC = aB + C;         // [C] dc (FoX), diagonal part
     const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
     const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
-    const T* q = static_cast<const T*>(p.q);
-    const T* dO = static_cast<const T*>(p.dO);
-    const bool below = n >= 1;          // query chains from this chunk continue into earlier chunks
-    const bool above = n <= p.N - 2;    // later query chunks reach this chunk's keys
+    const T* q = static_cast<const T*>(p.q) + hrow * D;
+    const T* k = static_cast<const T*>(p.k) + hrow * D;
+    const T* w = static_cast<const T*>(p.w) + hrow * D;
+    const T* dO = static_cast<const T*>(p.dO) + hrow * D;
+    const bool below = n >= 1;        // query chains from this chunk continue into earlier chunks
+    const bool above = n <= p.N - 2;  // later query chunks reach this chunk's keys
+    const bool hasP = below && above; // the chunk transition P_n was used
     const float scale = p.scale;
-    to_smem_v<T, D, kNTL>(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, c);
-    to_smem_v<T, D, kNTL>(sK, D, static_cast<const T*>(p.k) + hrow * D, D, C, c);
-    to_smem_v<T, D, kNTL>(sV, D, static_cast<const T*>(p.v) + hrow * D, D, C, c);
-    for (int idx = threadIdx.x; idx < 3 * C * D; idx += kNTL) aK[idx] = 0.f;  // aK, aV, aW
-    for (int r = threadIdx.x; r < C; r += kNTL) {
+    using GS = TT<C, C, true>;   // C x C, rows first
+    using GN = TT<C, C, false>;  // C x C, columns first
+    using GR = TT<C, D, false>;  // C x d
+    auto id = [](int, int, float x) { return x; };
+
+    for (int r = threadIdx.x; r < C; r += kNT) {
         sB[r] = r < c ? p.beta[hrow + r] : 0.f;
         sC[r] = p.fox ? p.cum[prow + r] : 0.f;
+        sL[r] = r < c ? p.lse[hrow + r] : 0.f;
+        sDl[r] = r < c ? p.delta[prow + r] : 0.f;
         aB[r] = 0.f;
         aC[r] = 0.f;
     }
+    for (int idx = threadIdx.x; idx < U; idx += kNT) slot(7)[idx] = 0.f;
+    to_smem_t<T, D>(slot(0), LC, w, D, C, c);  // W^T [D][LC] in slots 0-1 (until the dY phase)
     __syncthreads();
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    float* bds = sBuf + wid * WB;  // ds_ij of the warp's row
-    float* bal = bds + C;          // w . (walked vector) of the forward walk
-    float* bga = bal + C;          // w . (gradient) of the reverse walk
-
-    // (a) each query row of the chunk: its diagonal logits and the walk that built qbar
-    for (int t = 0, r; (r = snake_row(t, wid)) < c; ++t) {
-        float u[R], gO[R], g[R];
-        vload<D>(u, q + (hrow + r) * D, lane);
-        vload<D>(gO, dO + (hrow + r) * D, lane);
-        const float lse = p.lse[hrow + r], del = p.delta[prow + r], ci = sC[r];
-        for (int jj = r; jj >= 0; --jj) {  // down: u = H_{j+1} ... H_i q_i
-            const float s = scale * vdot<D>(u, sK + jj * D, lane) + ci - sC[jj];
-            const float pij = __expf(s - lse);
-            const float ds = pij * (vdot<D>(gO, sV + jj * D, lane) - del);
-            vred<D>(aK + jj * D, u, scale * ds, lane);
-            vred<D>(aV + jj * D, gO, pij, lane);
-            const float al = vstep<D>(u, sW + jj * D, sB[jj], lane);
-            if (lane == 0) {
-                bds[jj] = ds;
-                bal[jj] = al;
-                if (p.fox) {
-                    atomicAdd(aC + r, ds);
-                    atomicAdd(aC + jj, -ds);
+    {  // G = W W^T -> slot 6 (until dM)
+        typename GN::Acc g;
+        GN::zero(g);
+        mmul<C, C, D, false, true, true>(g, slot(0), LC, slot(0), LC);
+        mstore<C, C, false, false>(slot(6), LC, g, id);
+    }
+    __syncthreads();
+    {  // X[i][j] = [i == j] - beta_i sum_{i < k <= j} G[i][k] X[k][j], rows from the bottom -> slot 7 (until dM)
+        const float* sG = slot(6);
+        float* sX = slot(7);
+        const int j = threadIdx.x >> 2, qq = threadIdx.x & 3;
+        for (int i = C - 1; i >= 0; --i) {
+            float t = 0.f;
+            if (j > i)
+                for (int kk = i + 1 + qq; kk <= j; kk += 4) t = fmaf(sG[i * LC + kk], sX[kk * LC + j], t);
+            t += __shfl_xor_sync(0xffffffffu, t, 1);
+            t += __shfl_xor_sync(0xffffffffu, t, 2);
+            if (qq == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
+            __syncthreads();
+        }
+        for (int idx = threadIdx.x; idx < C * C; idx += kNT) {  // A = X D -> slot 8 (until dQm)
+            const int r = idx / C, cc = idx % C;
+            slot(8)[r * LC + cc] = sX[r * LC + cc] * sB[cc];
+        }
+    }
+    typename GR::Acc aW;  // dW, accumulated across the phases
+    GR::zero(aW);
+    if (hasP) {  // the chunk transition: dW -= A^T (W dP) + A (W dP^T), E = W dP W^T -> slot 9 (until dA)
+        const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
+        to_smem_v<float, D>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5
+        __syncthreads();
+        typename GR::Acc r;
+        GR::zero(r);
+        mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);  // R1 = W dP
+        __syncthreads();
+        mstore<C, D, false, false>(slot(2), LD, r, id);  // R1 [C][LD], slots 2-3
+        mstore<C, D, false, true>(slot(4), LC, r, id);   // R1^T [D][LC], slots 4-5
+        __syncthreads();
+        mmul<C, D, C, false, true, true, true>(aW, slot(8), LC, slot(2), LD);  // -= A^T R1
+        {
+            typename GN::Acc e;
+            GN::zero(e);
+            mmul<C, C, D, false, true, true>(e, slot(4), LC, slot(0), LC);  // E = R1 W^T
+            mstore<C, C, false, false>(slot(9), LC, e, id);
+        }
+        __syncthreads();
+        to_smem_t<float, D>(slot(2), LD, dP, D, D, D);  // dP^T [D][LD], slots 2-5
+        __syncthreads();
+        GR::zero(r);
+        mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);  // R2 = W dP^T
+        __syncthreads();
+        mstore<C, D, false, false>(slot(2), LD, r, id);
+        __syncthreads();
+        mmul<C, D, C, false, false, true, true>(aW, slot(8), LC, slot(2), LD);  // -= A R2
+    }
+    __syncthreads();
+    to_smem_t<T, D>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
+    to_smem_t<T, D>(slot(4), LC, k, D, C, c);  // K^T, slots 4-5
+    __syncthreads();
+    typename GS::Acc aS;  // Q K^T - Y Km^T, then the probabilities
+    GS::zero(aS);
+    {
+        typename GS::Acc qw, kw;
+        GS::zero(qw);
+        GS::zero(kw);
+        mmul<C, C, D, true, true, true>(qw, slot(2), LC, slot(0), LC);
+        mmul<C, C, D, true, true, true>(kw, slot(4), LC, slot(0), LC);
+        mmul<C, C, D, true, true, true>(aS, slot(2), LC, slot(4), LC);
+        __syncthreads();
+        mstore<C, C, true, true>(slot(10), LC, qw, [](int i, int bb, float x) { return bb <= i ? x : 0.f; });  // Qm^T (until dA)
+        mstore<C, C, true, false>(slot(11), LC, kw, [](int j, int a, float x) { return a > j ? x : 0.f; });    // Km (until dA)
+    }
+    __syncthreads();
+    {
+        typename GS::Acc y;
+        GS::zero(y);
+        mmul<C, C, C, true, true, false>(y, slot(10), LC, slot(8), LC);  // Y = Qm A^T
+        mstore<C, C, true, true>(slot(12), LC, y, id);                   // Y^T -> slot 12 (until the end)
+        typename GN::Acc z;
+        GN::zero(z);
+        mmul<C, C, C, false, false, true>(z, slot(11), LC, slot(8), LC);  // Z = Km A
+        mstore<C, C, false, false>(slot(2), LC, z, id);                   // -> slot 2 (until the end)
+    }
+    __syncthreads();
+    to_smem_t<T, D>(slot(0), LC, dO, D, C, c);                                   // dO^T, slots 0-1
+    to_smem_t<T, D>(slot(4), LC, static_cast<const T*>(p.v) + hrow * D, D, C, c);  // V^T, slots 4-5
+    mmul<C, C, C, true, true, false, true>(aS, slot(12), LC, slot(11), LC);  // -= Y Km^T
+    __syncthreads();
+    {
+        typename GS::Acc dp;
+        GS::zero(dp);
+        mmul<C, C, D, true, true, true>(dp, slot(0), LC, slot(4), LC);  // dO V^T
+        const int m0 = GS::m0(), n0 = GS::n0();
+        float cs[GS::TN];
+#pragma unroll
+        for (int j = 0; j < GS::TN; ++j) cs[j] = 0.f;
+#pragma unroll
+        for (int i = 0; i < GS::TM; ++i) {
+            const int r = m0 + i;
+            float rs = 0.f;
+#pragma unroll
+            for (int j = 0; j < GS::TN; ++j) {
+                const int col = n0 + j;
+                float pij = 0.f, ds = 0.f;
+                if (r < c && col <= r) {
+                    pij = __expf(scale * aS[i][j] + sC[r] - sC[col] - sL[r]);
+                    ds = pij * (dp[i][j] - sDl[r]);
+                }
+                aS[i][j] = pij;
+                dp[i][j] = scale * ds;
+                rs += ds;
+                cs[j] += ds;
+            }
+            if (p.fox) atomicAdd(aC + r, rs);
+        }
+        if (p.fox)
+#pragma unroll
+            for (int j = 0; j < GS::TN; ++j) atomicAdd(aC + n0 + j, -cs[j]);
+        __syncthreads();
+        mstore<C, C, true, false>(slot(3), LC, aS, id);  // P -> slot 3 (until dV)
+        mstore<C, C, true, false>(slot(0), LC, dp, id);  // dSs -> slot 0 (until the end)
+    }
+    to_smem_v<T, D>(slot(4), LD, dO, D, C, c);  // dO [C][LD], slots 4-5
+    __syncthreads();
+    {  // dV = P^T dO (+ the off-diagonal part from the per-key-chunk sums)
+        typename GR::Acc dv;
+        GR::zero(dv);
+        mmul<C, D, C, false, true, true>(dv, slot(3), LC, slot(4), LD);
+        mstore_out<D>(static_cast<T*>(p.dv) + hrow * D, dv, above ? p.dvoff + prow * D : nullptr, c);
+    }
+    __syncthreads();
+    {  // dZ = -dKhat W^T, dY = -dQbar W^T - dSs Km
+        typename GN::Acc dz, dy;
+        GN::zero(dz);
+        GN::zero(dy);
+#pragma unroll 1
+        for (int h = 0; h < NH; ++h) {
+            to_smem_t<T, KH>(slot(1), LC, w + h * KH, D, C, c);
+            if (above) to_smem_t<float, KH>(slot(3), LC, p.dkhat + prow * D + h * KH, D, C, C);
+            if (below) to_smem_t<float, KH>(slot(4), LC, p.dqbar + prow * D + h * KH, D, C, c);
+            __syncthreads();
+            if (above) mmul<C, C, KH, false, true, true>(dz, slot(3), LC, slot(1), LC);
+            if (below) mmul<C, C, KH, false, true, true>(dy, slot(4), LC, slot(1), LC);
+            __syncthreads();
+        }
+        mmul<C, C, C, false, false, true>(dy, slot(0), LC, slot(11), LC);
+        mstore<C, C, false, true>(slot(1), LC, dz, [](int, int, float x) { return -x; });   // dZ^T -> slot 1 (until dA)
+        mstore<C, C, false, false>(slot(3), LC, dy, [](int, int, float x) { return -x; });  // dY -> slot 3 (until dA)
+    }
+    __syncthreads();
+    {
+        typename GS::Acc dk;
+        GS::zero(dk);
+        mmul<C, C, C, true, true, false, true>(dk, slot(0), LC, slot(12), LC);  // -dSs^T Y
+        mmul<C, C, C, true, true, false>(dk, slot(1), LC, slot(8), LC);         // + dZ A^T
+        mstore<C, C, true, false>(slot(4), LC, dk, [](int j, int a, float x) { return a > j ? x : 0.f; });  // dKw -> slot 4
+        typename GN::Acc dq;
+        GN::zero(dq);
+        mmul<C, C, C, false, false, true>(dq, slot(3), LC, slot(8), LC);  // dY A
+        mstore<C, C, false, false>(slot(5), LC, dq, [](int i, int bb, float x) { return bb <= i ? x : 0.f; });  // dQw -> slot 5
+    }
+    __syncthreads();
+    {  // dA = Km^T dZ + dY^T Qm - E;  dbeta from A = X D;  dX = dA D -> dX^T in slot 8
+        typename GS::Acc da;
+        GS::zero(da);
+        mmul<C, C, C, true, true, false>(da, slot(11), LC, slot(1), LC);
+        mmul<C, C, C, true, true, false>(da, slot(3), LC, slot(10), LC);
+        const int m0 = GS::m0(), n0 = GS::n0();
+        const float* sX = slot(7);
+#pragma unroll
+        for (int j = 0; j < GS::TN; ++j) {
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < GS::TM; ++i) {
+                if (hasP) da[i][j] -= slot(9)[(m0 + i) * LC + n0 + j];
+                s = fmaf(sX[(m0 + i) * LC + n0 + j], da[i][j], s);
+            }
+            atomicAdd(aB + n0 + j, s);
+        }
+        mstore<C, C, true, true>(slot(8), LC, da, [&](int, int bb, float x) { return x * sB[bb]; });
+    }
+    __syncthreads();
+    {  // dM = -X^T (dX X^T);  dG = striu(D dM) stored as dG + dG^T
+        typename GS::Acc t1;
+        GS::zero(t1);
+        mmul<C, C, C, true, true, false>(t1, slot(8), LC, slot(7), LC);
+        mstore<C, C, true, false>(slot(9), LC, t1, id);
+        __syncthreads();
+        typename GN::Acc dm;
+        GN::zero(dm);
+        mmul<C, C, C, false, true, true, true>(dm, slot(7), LC, slot(9), LC);
+        const int m0 = GN::m0(), n0 = GN::n0();
+        float* dG = slot(10);
+#pragma unroll
+        for (int i = 0; i < GN::TM; ++i) {
+            const int a = m0 + i;
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < GN::TN; ++j) {
+                const int bb = n0 + j;
+                if (bb > a) {
+                    s = fmaf(dm[i][j], slot(6)[a * LC + bb], s);
+                    const float g = sB[a] * dm[i][j];
+                    dG[a * LC + bb] = g;
+                    dG[bb * LC + a] = g;
+                } else if (bb == a) {
+                    dG[a * LC + a] = 0.f;
                 }
             }
-        }
-        __syncwarp();
-        if (below) vload<D>(g, p.dqbar + (prow + r) * D, lane);
-        else vzero<D>(g);
-        for (int jj = 0; jj <= r; ++jj) {  // up: g is dL/du_{j-1}, then dL/du_j
-            const float* wj = sW + jj * D;
-            const float ga = vdot<D>(g, wj, lane), al = bal[jj];
-            vred<D>(aW + jj * D, g, -sB[jj] * al, lane);
-            if (lane == 0) {
-                atomicAdd(aB + jj, -ga * al);
-                bga[jj] = ga;
-            }
-            vaxpy<D>(g, wj, sB[jj] * ga, lane);
-            vaxpy<D>(g, sK + jj * D, -scale * bds[jj], lane);
-        }
-        vstore<D>(static_cast<T*>(p.dq) + (hrow + r) * D, g, lane);
-        __syncwarp();
-        vload<D>(u, q + (hrow + r) * D, lane);
-        for (int jj = r; jj >= 0; --jj) {  // down again: the (w . g) u half of dw
-            vred<D>(aW + jj * D, u, -sB[jj] * bga[jj], lane);
-            vaxpy<D>(u, sW + jj * D, sB[jj] * bal[jj], lane);
-        }
-        __syncwarp();
-    }
-    // (b) each key of the chunk: the walk that built khat (gradient from later query chunks)
-    if (above)
-        for (int t = 0, r; (r = snake_row(t, wid)) < c; ++t) {
-            float x[R], gx[R];
-            vload<D>(x, sK + r * D, lane);
-            for (int tt = r + 1; tt < c; ++tt) {
-                const float al = vstep<D>(x, sW + tt * D, sB[tt], lane);
-                if (lane == 0) bal[tt] = al;
-            }
-            __syncwarp();
-            vload<D>(gx, p.dkhat + (prow + r) * D, lane);
-            for (int tt = c - 1; tt > r; --tt) {
-                const float* wt = sW + tt * D;
-                const float ga = vdot<D>(gx, wt, lane), al = bal[tt];
-                vred<D>(aW + tt * D, gx, -sB[tt] * al, lane);
-                if (lane == 0) {
-                    atomicAdd(aB + tt, -ga * al);
-                    bga[tt] = ga;
-                }
-                vaxpy<D>(gx, wt, sB[tt] * ga, lane);
-            }
-            vred<D>(aK + r * D, gx, 1.f, lane);
-            __syncwarp();
-            vload<D>(x, sK + r * D, lane);
-            for (int tt = r + 1; tt < c; ++tt) {
-                vred<D>(aW + tt * D, x, -sB[tt] * bga[tt], lane);
-                vaxpy<D>(x, sW + tt * D, sB[tt] * bal[tt], lane);
-            }
-            __syncwarp();
-        }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < c * D; idx += kNTL) {
-        static_cast<T*>(p.dk)[hrow * D + idx] = from_f<T>(aK[idx]);
-        const float dv = aV[idx] + (above ? p.dvoff[prow * D + idx] : 0.f);
-        static_cast<T*>(p.dv)[hrow * D + idx] = from_f<T>(dv);
-    }
-    // (c) the chunk transition P_n = H_b ... H_e: dH_t = A_t^T dP B_t^T with
-    //     A_t = H_b ... H_{t-1}, B_t = H_{t+1} ... H_e
-    if (below && above) {
-        __syncthreads();
-        to_smem_v<float, D, kNTL>(sDP, LDP, p.dpm + ((size_t)bh * p.N + n) * D * D, D, D, D);
-        __syncthreads();
-        float* vw = aV + wid * 2 * D;  // [2][D]: B_t^T w_t, A_t w_t (aV was written out above)
-        for (int r = wid; r < c; r += kNWL) {
-            float wh[R], wb[R], y1[R], y2[R];
-            vload<D>(wh, sW + r * D, lane);
-            for (int tt = r + 1; tt < c; ++tt) vstep<D>(wh, sW + tt * D, sB[tt], lane);
-            vload<D>(wb, sW + r * D, lane);
-            for (int tt = r - 1; tt >= 0; --tt) vstep<D>(wb, sW + tt * D, sB[tt], lane);
-            vstore<D>(vw, wh, lane);
-            vstore<D>(vw + D, wb, lane);
-            __syncwarp();
-#pragma unroll
-            for (int rr = 0; rr < R; ++rr) {
-                const int e = lane + 32 * rr;
-                float s1 = 0.f, s2 = 0.f;
-                if (WV<D>::ok(lane))
-                    for (int cc = 0; cc < D; ++cc) {
-                        s1 = fmaf(sDP[e * LDP + cc], vw[cc], s1);      // (dP B_t^T w_t)_e
-                        s2 = fmaf(sDP[cc * LDP + e], vw[D + cc], s2);  // (dP^T A_t w_t)_e
-                    }
-                y1[rr] = s1;
-                y2[rr] = s2;
-            }
-            const float db = -vdot<D>(wb, y1);
-            for (int tt = 0; tt < r; ++tt) vstep<D>(y1, sW + tt * D, sB[tt], lane);       // A_t^T y1
-            for (int tt = c - 1; tt > r; --tt) vstep<D>(y2, sW + tt * D, sB[tt], lane);   // B_t y2
-            if (WV<D>::ok(lane))
-#pragma unroll
-                for (int rr = 0; rr < R; ++rr) aW[r * D + lane + 32 * rr] += -sB[r] * (y1[rr] + y2[rr]);
-            if (lane == 0) aB[r] += db;
-            __syncwarp();
+            atomicAdd(aB + a, s);
         }
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < c * D; idx += kNTL) static_cast<T*>(p.dw)[hrow * D + idx] = from_f<T>(aW[idx]);
-    for (int r = threadIdx.x; r < c; r += kNTL) {
+    if (below) to_smem_v<float, D>(slot(6), LD, p.dqbar + prow * D, D, C, c);  // slots 6-7
+    if (above) to_smem_v<float, D>(slot(8), LD, p.dkhat + prow * D, D, C, C);  // slots 8-9
+    __syncthreads();
+    if (below) mmul<C, D, C, false, false, true, true>(aW, slot(12), LC, slot(6), LD);  // -= Y^T dQbar
+    if (above) mmul<C, D, C, false, true, true, true>(aW, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
+    __syncthreads();
+    to_smem_v<T, D>(slot(6), LD, q, D, C, c);
+    to_smem_v<T, D>(slot(8), LD, k, D, C, c);
+    __syncthreads();
+    typename GR::Acc aQ, aK;
+    GR::zero(aQ);
+    GR::zero(aK);
+    mmul<C, D, C, false, true, true>(aW, slot(5), LC, slot(6), LD);   // += dQw^T Q
+    mmul<C, D, C, false, true, true>(aW, slot(4), LC, slot(8), LD);   // += dKw^T K
+    mmul<C, D, C, false, false, true>(aQ, slot(0), LC, slot(8), LD);  // dSs K
+    mmul<C, D, C, false, true, true>(aK, slot(0), LC, slot(6), LD);   // dSs^T Q
+    __syncthreads();
+    to_smem_v<T, D>(slot(6), LD, w, D, C, c);
+    __syncthreads();
+    mmul<C, D, C, false, true, true>(aW, slot(10), LC, slot(6), LD);   // += (dG + dG^T) W
+    mmul<C, D, C, false, false, true>(aQ, slot(5), LC, slot(6), LD);  // += dQw W
+    mmul<C, D, C, false, false, true>(aK, slot(4), LC, slot(6), LD);  // += dKw W
+    mstore_out<D>(static_cast<T*>(p.dq) + hrow * D, aQ, below ? p.dqbar + prow * D : nullptr, c);
+    mstore_out<D>(static_cast<T*>(p.dk) + hrow * D, aK, above ? p.dkhat + prow * D : nullptr, c);
+    mstore_out<D>(static_cast<T*>(p.dw) + hrow * D, aW, nullptr, c);
+    __syncthreads();
+    for (int r = threadIdx.x; r < c; r += kNT) {
         p.dbeta[hrow + r] = aB[r];
         if (p.fox)
             p.dctot[prow + r] = aC[r] + (below ? p.dcrow[prow + r] : 0.f) - (above ? p.dccol[prow + r] : 0.f);
@@ -889,7 +1125,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigne
             bwd_reduce<T, D><<<dim3(p.N - 1, BH), kNT, b_reduce, st>>>(p);
         }
     }
-    bwd_local<T, D><<<dim3(p.N, BH), kNTL, b_local, st>>>(p);
+    bwd_local<T, D><<<dim3(p.N, BH), kNT, b_local, st>>>(p);
     if (log_f) bwd_fox_suffix<<<BH, 1024, 0, st>>>(p.dctot, p.L, p.Lp, p.dlog_f);
     return cudaGetLastError();
 }
