@@ -742,20 +742,45 @@ __device__ __forceinline__ void mstore(float* dst, int ld, const typename TT<M, 
     }
 }
 
-// rows r < c of a C x D result to global memory: dst[r][e] = acc + (add ? add[r][e] : 0)
+// rows r < c of a C x D result to global memory: dst[r][e] = acc + (add ? add[r][e] : 0); the
+// addends are all loaded before the first store, and each thread's row segment is stored whole
 template <int D, typename E>
 __device__ __forceinline__ void mstore_out(E* dst, const typename TT<kC, D, false>::Acc& acc, const float* add,
                                            int c) {
     using G = TT<kC, D, false>;
+    constexpr int TN = G::TN;
     const int m0 = G::m0(), n0 = G::n0();
+    float v[G::TM][TN];
 #pragma unroll
     for (int i = 0; i < G::TM; ++i) {
-        const int r = m0 + i;
-        if (r >= c) continue;
+        const bool ok = add && m0 + i < c;
 #pragma unroll
-        for (int j = 0; j < G::TN; ++j) {
-            const float x = acc[i][j] + (add ? add[(size_t)r * D + n0 + j] : 0.f);
-            dst[(size_t)r * D + n0 + j] = from_f<E>(x);
+        for (int j = 0; j < TN; j += 4) {
+            const float4 x = ok ? *reinterpret_cast<const float4*>(add + (size_t)(m0 + i) * D + n0 + j)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[i][j] = acc[i][j] + x.x;
+            v[i][j + 1] = acc[i][j + 1] + x.y;
+            v[i][j + 2] = acc[i][j + 2] + x.z;
+            v[i][j + 3] = acc[i][j + 3] + x.w;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < G::TM; ++i) {
+        if (m0 + i >= c) continue;
+        E* d = dst + (size_t)(m0 + i) * D + n0;
+        if constexpr (sizeof(E) == 4) {
+#pragma unroll
+            for (int j = 0; j < TN; j += 4)
+                *reinterpret_cast<float4*>(d + j) = make_float4(v[i][j], v[i][j + 1], v[i][j + 2], v[i][j + 3]);
+        } else {
+            uint32_t u[TN / 2];
+#pragma unroll
+            for (int j = 0; j < TN / 2; ++j) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[i][2 * j], v[i][2 * j + 1]);
+                u[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            if constexpr (TN == 8) *reinterpret_cast<uint4*>(d) = make_uint4(u[0], u[1], u[2], u[3]);
+            else *reinterpret_cast<uint2*>(d) = make_uint2(u[0], u[1]);
         }
     }
 }
@@ -807,17 +832,49 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         mstore<C, C, false, false>(slot(6), LC, g, id);
     }
     __syncthreads();
-    {  // X[i][j] = [i == j] - beta_i sum_{i < k <= j} G[i][k] X[k][j], rows from the bottom -> slot 7 (until dM)
+    {  // X = (I + D triu_1 G)^{-1} -> slot 7 (until dM): the 16 x 16 diagonal blocks row by row from
+       // the bottom (one warp each), then two doubling merges X_12 = -X_11 (D G_12) X_22
         const float* sG = slot(6);
         float* sX = slot(7);
-        const int j = threadIdx.x >> 2, qq = threadIdx.x & 3;
-        for (int i = C - 1; i >= 0; --i) {
-            float t = 0.f;
-            if (j > i)
-                for (int kk = i + 1 + qq; kk <= j; kk += 4) t = fmaf(sG[i * LC + kk], sX[kk * LC + j], t);
-            t += __shfl_xor_sync(0xffffffffu, t, 1);
-            t += __shfl_xor_sync(0xffffffffu, t, 2);
-            if (qq == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        if (wid < C / 16) {
+            const int j = 16 * wid + (lane & 15), h = lane >> 4;
+            for (int i = 16 * wid + 15; i >= 16 * wid; --i) {
+                float t = 0.f;
+                for (int kk = i + 1 + h; kk <= j; kk += 2) t = fmaf(sG[i * LC + kk], sX[kk * LC + j], t);
+                t += __shfl_xor_sync(0xffffffffu, t, 16);
+                if (h == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        for (int s = 16; s < C; s *= 2) {  // blocks of s rows merged in pairs; s * s * C / (2 s) elements
+            const int per = C * s / (2 * kNT);  // per thread: 2, then 4
+            float v[4];
+            for (int e = 0; e < per; ++e) {  // T = D G_12 X_22, written over the X_12 block
+                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
+                float t = 0.f;
+                for (int kk = 2 * s * pr + s; kk <= bb; ++kk) t = fmaf(sG[a * LC + kk], sX[kk * LC + bb], t);
+                v[e] = sB[a] * t;
+            }
+            for (int e = 0; e < per; ++e) {
+                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
+            }
+            __syncthreads();
+            for (int e = 0; e < per; ++e) {  // X_12 = -X_11 T
+                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
+                float t = 0.f;
+                for (int kk = a; kk < 2 * s * pr + s; ++kk) t = fmaf(sX[a * LC + kk], sX[kk * LC + bb], t);
+                v[e] = -t;
+            }
+            __syncthreads();
+            for (int e = 0; e < per; ++e) {
+                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
+            }
             __syncthreads();
         }
         for (int idx = threadIdx.x; idx < C * C; idx += kNT) {  // A = X D -> slot 8 (until dQm)
