@@ -67,6 +67,7 @@ namespace {
 constexpr int kC = kBwdC;
 constexpr int kNT = 256;
 constexpr int kNW = kNT / 32;
+constexpr int kNTL = 256;  // bwd_local
 constexpr int kNTP = 512;  // bwd_prep: sixteen latency-bound walks in flight per CTA
 
 struct BwdParams {
@@ -168,13 +169,13 @@ __device__ __forceinline__ void to_smem_v(float* dst, int ldd, const G* src, int
 // Transposing load: dst[c * ldd + r] = src[r * lds + c] for r < rows (zero for r >= valid),
 // c < COLS.  Consecutive threads take consecutive rows of one 16-byte column group, so the
 // shared-memory writes of a warp fall in distinct banks.
-template <typename G, int COLS>
+template <typename G, int COLS, int NT = kNT>
 __device__ __forceinline__ void to_smem_t(float* dst, int ldd, const G* src, int lds, int rows, int valid) {
     constexpr int V = 16 / sizeof(G);
     static_assert(COLS % V == 0, "rows must be whole 16-byte vectors");
     const int nvec = rows * (COLS / V);
 #pragma unroll 4
-    for (int idx = threadIdx.x; idx < nvec; idx += kNT) {
+    for (int idx = threadIdx.x; idx < nvec; idx += NT) {
         const int r = idx % rows, cv = idx / rows;
         Vec16<G> x;
         x.raw = r < valid ? ld_global_v4(src + (size_t)r * lds + cv * V) : make_uint4(0u, 0u, 0u, 0u);
@@ -652,15 +653,15 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
 // gradient dP four.  The slot of every matrix and the phase that frees it are listed beside
 // the code.
 
-// Thread tiling of an M x N output over the kNT threads: TM consecutive rows by TN consecutive
-// columns per thread.  MM numbers the tiles down the rows first (a warp spans many rows and one
-// or two column groups), otherwise across the columns first.
+// Thread tiling of an M x N output over the kNTL threads of bwd_local: TM consecutive rows by TN
+// consecutive columns per thread.  MM numbers the tiles down the rows first (a warp spans many
+// rows and one or two column groups), otherwise across the columns first.
 template <int M, int N, bool MM> struct TT {
-    static constexpr int TOT = M * N / kNT;
+    static constexpr int TOT = M * N / kNTL;
     static constexpr int TN = TOT >= 32 ? 8 : (TOT >= 4 ? 4 : 1);
     static constexpr int TM = TOT / TN;
     static constexpr int GN = N / TN, GM = M / TM;
-    static_assert(TOT >= 1 && GM * GN == kNT && GM * TM == M && GN * TN == N, "tiling");
+    static_assert(TOT >= 1 && GM * GN == kNTL && GM * TM == M && GN * TN == N, "tiling");
     static __device__ __forceinline__ int m0() { return (MM ? (int)threadIdx.x % GM : (int)threadIdx.x / GN) * TM; }
     static __device__ __forceinline__ int n0() { return (MM ? (int)threadIdx.x / GM : (int)threadIdx.x % GN) * TN; }
     using Acc = float[TM][TN];
@@ -676,16 +677,22 @@ template <int M, int N, bool MM> struct TT {
 // when AK, else row-major (A[m lda + k]); B is K-major (b(k, n) = B[k ldb + n]) when BK, else
 // B[n ldb + k].  Four k per step, every shared-memory load 16 bytes wide (or the tile's width).
 // A row-major A is read conflict-free with the column-first tiling, a row-major B with the
-// row-first one (leading dims of C + 4 floats).
-template <int M, int N, int K, bool MM, bool AK, bool BK, bool NEG = false>
+// row-first one (leading dims of C + 4 floats).  KR states a triangular A (m and k both chunk
+// positions): KR = 1 when a(m, k) = 0 for k < m, KR = 2 when a(m, k) = 0 for k > m; the
+// thread then runs only the k that can meet its rows (with the column-first tiling a warp holds
+// two row groups, so its threads stop together).
+template <int M, int N, int K, bool MM, bool AK, bool BK, bool NEG = false, int KR = 0>
 __device__ __forceinline__ void mmul(typename TT<M, N, MM>::Acc& acc, const float* A, int lda, const float* B,
                                      int ldb) {
     using G = TT<M, N, MM>;
     constexpr int TM = G::TM, TN = G::TN;
     static_assert(K % 4 == 0, "depth");
+    static_assert(KR == 0 || M == K, "a triangular A is square");
     const int m0 = G::m0(), n0 = G::n0();
+    const int kb = KR == 1 ? (m0 & ~3) : 0;
+    const int ke = KR == 2 ? min(K, (m0 + TM + 3) & ~3) : K;
 #pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
+    for (int k = kb; k < ke; k += 4) {
         float a[4][TM], b[4][TN];
         if constexpr (AK) {
 #pragma unroll
@@ -750,46 +757,58 @@ __device__ __forceinline__ void mstore_out(E* dst, const typename TT<kC, D, fals
     using G = TT<kC, D, false>;
     constexpr int TN = G::TN;
     const int m0 = G::m0(), n0 = G::n0();
-    float v[G::TM][TN];
+    if constexpr (TN % 4 != 0) {
 #pragma unroll
-    for (int i = 0; i < G::TM; ++i) {
-        const bool ok = add && m0 + i < c;
+        for (int i = 0; i < G::TM; ++i)
+            if (m0 + i < c)
 #pragma unroll
-        for (int j = 0; j < TN; j += 4) {
-            const float4 x = ok ? *reinterpret_cast<const float4*>(add + (size_t)(m0 + i) * D + n0 + j)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[i][j] = acc[i][j] + x.x;
-            v[i][j + 1] = acc[i][j + 1] + x.y;
-            v[i][j + 2] = acc[i][j + 2] + x.z;
-            v[i][j + 3] = acc[i][j + 3] + x.w;
-        }
-    }
+                for (int j = 0; j < TN; ++j) {
+                    const size_t o = (size_t)(m0 + i) * D + n0 + j;
+                    dst[o] = from_f<E>(acc[i][j] + (add ? add[o] : 0.f));
+                }
+        return;
+    } else {
+        float v[G::TM][TN];
 #pragma unroll
-    for (int i = 0; i < G::TM; ++i) {
-        if (m0 + i >= c) continue;
-        E* d = dst + (size_t)(m0 + i) * D + n0;
-        if constexpr (sizeof(E) == 4) {
+        for (int i = 0; i < G::TM; ++i) {
+            const bool ok = add && m0 + i < c;
 #pragma unroll
-            for (int j = 0; j < TN; j += 4)
-                *reinterpret_cast<float4*>(d + j) = make_float4(v[i][j], v[i][j + 1], v[i][j + 2], v[i][j + 3]);
-        } else {
-            uint32_t u[TN / 2];
-#pragma unroll
-            for (int j = 0; j < TN / 2; ++j) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(v[i][2 * j], v[i][2 * j + 1]);
-                u[j] = *reinterpret_cast<const uint32_t*>(&h);
+            for (int j = 0; j < TN; j += 4) {
+                const float4 x = ok ? *reinterpret_cast<const float4*>(add + (size_t)(m0 + i) * D + n0 + j)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                v[i][j] = acc[i][j] + x.x;
+                v[i][j + 1] = acc[i][j + 1] + x.y;
+                v[i][j + 2] = acc[i][j + 2] + x.z;
+                v[i][j + 3] = acc[i][j + 3] + x.w;
             }
-            if constexpr (TN == 8) *reinterpret_cast<uint4*>(d) = make_uint4(u[0], u[1], u[2], u[3]);
-            else *reinterpret_cast<uint2*>(d) = make_uint2(u[0], u[1]);
+        }
+#pragma unroll
+        for (int i = 0; i < G::TM; ++i) {
+            if (m0 + i >= c) continue;
+            E* d = dst + (size_t)(m0 + i) * D + n0;
+            if constexpr (sizeof(E) == 4) {
+#pragma unroll
+                for (int j = 0; j < TN; j += 4)
+                    *reinterpret_cast<float4*>(d + j) = make_float4(v[i][j], v[i][j + 1], v[i][j + 2], v[i][j + 3]);
+            } else {
+                uint32_t u[TN / 2];
+#pragma unroll
+                for (int j = 0; j < TN / 2; ++j) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[i][2 * j], v[i][2 * j + 1]);
+                    u[j] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                if constexpr (TN == 8) *reinterpret_cast<uint4*>(d) = make_uint4(u[0], u[1], u[2], u[3]);
+                else *reinterpret_cast<uint2*>(d) = make_uint2(u[0], u[1]);
+            }
         }
     }
 }
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
+__global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     constexpr int C = kC, LC = C + 4, LD = D + 4, U = BwdSmem<D>::slot;
     constexpr int KH = D < 64 ? D : 64, NH = D / KH;  // d x C operands in pieces of KH rows
-    static_assert(C == 64 && kNT == 4 * C, "the triangular inverse takes four threads per column");
+    static_assert(C == 64 && (C * 8) % kNTL == 0 && C * 32 / (2 * kNTL) <= 4, "inverse merges: whole elements per thread");
     static_assert(C * LD <= 2 * U && D * LC <= 2 * U && D * LD <= 4 * U && KH * LC <= U, "slot sizes");
     extern __shared__ __align__(16) float smem[];
     auto slot = [&](int i) { return smem + i * U; };
@@ -814,7 +833,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
     using GR = TT<C, D, false>;  // C x d
     auto id = [](int, int, float x) { return x; };
 
-    for (int r = threadIdx.x; r < C; r += kNT) {
+    for (int r = threadIdx.x; r < C; r += kNTL) {
         sB[r] = r < c ? p.beta[hrow + r] : 0.f;
         sC[r] = p.fox ? p.cum[prow + r] : 0.f;
         sL[r] = r < c ? p.lse[hrow + r] : 0.f;
@@ -822,8 +841,8 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         aB[r] = 0.f;
         aC[r] = 0.f;
     }
-    for (int idx = threadIdx.x; idx < U; idx += kNT) slot(7)[idx] = 0.f;
-    to_smem_t<T, D>(slot(0), LC, w, D, C, c);  // W^T [D][LC] in slots 0-1 (until the dY phase)
+    for (int idx = threadIdx.x; idx < U; idx += kNTL) slot(7)[idx] = 0.f;
+    to_smem_t<T, D, kNTL>(slot(0), LC, w, D, C, c);  // W^T [D][LC] in slots 0-1 (until the dY phase)
     __syncthreads();
     {  // G = W W^T -> slot 6 (until dM)
         typename GN::Acc g;
@@ -849,22 +868,22 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         }
         __syncthreads();
         for (int s = 16; s < C; s *= 2) {  // blocks of s rows merged in pairs; s * s * C / (2 s) elements
-            const int per = C * s / (2 * kNT);  // per thread: 2, then 4
+            const int per = C * s / (2 * kNTL);  // elements per thread
             float v[4];
             for (int e = 0; e < per; ++e) {  // T = D G_12 X_22, written over the X_12 block
-                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
                 const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
                 float t = 0.f;
                 for (int kk = 2 * s * pr + s; kk <= bb; ++kk) t = fmaf(sG[a * LC + kk], sX[kk * LC + bb], t);
                 v[e] = sB[a] * t;
             }
             for (int e = 0; e < per; ++e) {
-                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
                 sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
             }
             __syncthreads();
             for (int e = 0; e < per; ++e) {  // X_12 = -X_11 T
-                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
                 const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
                 float t = 0.f;
                 for (int kk = a; kk < 2 * s * pr + s; ++kk) t = fmaf(sX[a * LC + kk], sX[kk * LC + bb], t);
@@ -872,12 +891,12 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
             }
             __syncthreads();
             for (int e = 0; e < per; ++e) {
-                const int idx = threadIdx.x + e * kNT, pr = idx / (s * s), rem = idx % (s * s);
+                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
                 sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
             }
             __syncthreads();
         }
-        for (int idx = threadIdx.x; idx < C * C; idx += kNT) {  // A = X D -> slot 8 (until dQm)
+        for (int idx = threadIdx.x; idx < C * C; idx += kNTL) {  // A = X D -> slot 8 (until dQm)
             const int r = idx / C, cc = idx % C;
             slot(8)[r * LC + cc] = sX[r * LC + cc] * sB[cc];
         }
@@ -886,7 +905,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
     GR::zero(aW);
     if (hasP) {  // the chunk transition: dW -= A^T (W dP) + A (W dP^T), E = W dP W^T -> slot 9 (until dA)
         const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
-        to_smem_v<float, D>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5
+        to_smem_v<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5
         __syncthreads();
         typename GR::Acc r;
         GR::zero(r);
@@ -895,7 +914,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         mstore<C, D, false, false>(slot(2), LD, r, id);  // R1 [C][LD], slots 2-3
         mstore<C, D, false, true>(slot(4), LC, r, id);   // R1^T [D][LC], slots 4-5
         __syncthreads();
-        mmul<C, D, C, false, true, true, true>(aW, slot(8), LC, slot(2), LD);  // -= A^T R1
+        mmul<C, D, C, false, true, true, true, 2>(aW, slot(8), LC, slot(2), LD);  // -= A^T R1
         {
             typename GN::Acc e;
             GN::zero(e);
@@ -903,18 +922,18 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
             mstore<C, C, false, false>(slot(9), LC, e, id);
         }
         __syncthreads();
-        to_smem_t<float, D>(slot(2), LD, dP, D, D, D);  // dP^T [D][LD], slots 2-5
+        to_smem_t<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP^T [D][LD], slots 2-5
         __syncthreads();
         GR::zero(r);
         mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);  // R2 = W dP^T
         __syncthreads();
         mstore<C, D, false, false>(slot(2), LD, r, id);
         __syncthreads();
-        mmul<C, D, C, false, false, true, true>(aW, slot(8), LC, slot(2), LD);  // -= A R2
+        mmul<C, D, C, false, false, true, true, 1>(aW, slot(8), LC, slot(2), LD);  // -= A R2
     }
     __syncthreads();
-    to_smem_t<T, D>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
-    to_smem_t<T, D>(slot(4), LC, k, D, C, c);  // K^T, slots 4-5
+    to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
+    to_smem_t<T, D, kNTL>(slot(4), LC, k, D, C, c);  // K^T, slots 4-5
     __syncthreads();
     typename GS::Acc aS;  // Q K^T - Y Km^T, then the probabilities
     GS::zero(aS);
@@ -937,12 +956,12 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         mstore<C, C, true, true>(slot(12), LC, y, id);                   // Y^T -> slot 12 (until the end)
         typename GN::Acc z;
         GN::zero(z);
-        mmul<C, C, C, false, false, true>(z, slot(11), LC, slot(8), LC);  // Z = Km A
+        mmul<C, C, C, false, false, true, false, 1>(z, slot(11), LC, slot(8), LC);  // Z = Km A
         mstore<C, C, false, false>(slot(2), LC, z, id);                   // -> slot 2 (until the end)
     }
     __syncthreads();
-    to_smem_t<T, D>(slot(0), LC, dO, D, C, c);                                   // dO^T, slots 0-1
-    to_smem_t<T, D>(slot(4), LC, static_cast<const T*>(p.v) + hrow * D, D, C, c);  // V^T, slots 4-5
+    to_smem_t<T, D, kNTL>(slot(0), LC, dO, D, C, c);                                   // dO^T, slots 0-1
+    to_smem_t<T, D, kNTL>(slot(4), LC, static_cast<const T*>(p.v) + hrow * D, D, C, c);  // V^T, slots 4-5
     mmul<C, C, C, true, true, false, true>(aS, slot(12), LC, slot(11), LC);  // -= Y Km^T
     __syncthreads();
     {
@@ -979,12 +998,12 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         mstore<C, C, true, false>(slot(3), LC, aS, id);  // P -> slot 3 (until dV)
         mstore<C, C, true, false>(slot(0), LC, dp, id);  // dSs -> slot 0 (until the end)
     }
-    to_smem_v<T, D>(slot(4), LD, dO, D, C, c);  // dO [C][LD], slots 4-5
+    to_smem_v<T, D, kNTL>(slot(4), LD, dO, D, C, c);  // dO [C][LD], slots 4-5
     __syncthreads();
     {  // dV = P^T dO (+ the off-diagonal part from the per-key-chunk sums)
         typename GR::Acc dv;
         GR::zero(dv);
-        mmul<C, D, C, false, true, true>(dv, slot(3), LC, slot(4), LD);
+        mmul<C, D, C, false, true, true, false, 1>(dv, slot(3), LC, slot(4), LD);
         mstore_out<D>(static_cast<T*>(p.dv) + hrow * D, dv, above ? p.dvoff + prow * D : nullptr, c);
     }
     __syncthreads();
@@ -994,15 +1013,15 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         GN::zero(dy);
 #pragma unroll 1
         for (int h = 0; h < NH; ++h) {
-            to_smem_t<T, KH>(slot(1), LC, w + h * KH, D, C, c);
-            if (above) to_smem_t<float, KH>(slot(3), LC, p.dkhat + prow * D + h * KH, D, C, C);
-            if (below) to_smem_t<float, KH>(slot(4), LC, p.dqbar + prow * D + h * KH, D, C, c);
+            to_smem_t<T, KH, kNTL>(slot(1), LC, w + h * KH, D, C, c);
+            if (above) to_smem_t<float, KH, kNTL>(slot(3), LC, p.dkhat + prow * D + h * KH, D, C, C);
+            if (below) to_smem_t<float, KH, kNTL>(slot(4), LC, p.dqbar + prow * D + h * KH, D, C, c);
             __syncthreads();
             if (above) mmul<C, C, KH, false, true, true>(dz, slot(3), LC, slot(1), LC);
             if (below) mmul<C, C, KH, false, true, true>(dy, slot(4), LC, slot(1), LC);
             __syncthreads();
         }
-        mmul<C, C, C, false, false, true>(dy, slot(0), LC, slot(11), LC);
+        mmul<C, C, C, false, false, true, false, 2>(dy, slot(0), LC, slot(11), LC);
         mstore<C, C, false, true>(slot(1), LC, dz, [](int, int, float x) { return -x; });   // dZ^T -> slot 1 (until dA)
         mstore<C, C, false, false>(slot(3), LC, dy, [](int, int, float x) { return -x; });  // dY -> slot 3 (until dA)
     }
@@ -1047,7 +1066,7 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         __syncthreads();
         typename GN::Acc dm;
         GN::zero(dm);
-        mmul<C, C, C, false, true, true, true>(dm, slot(7), LC, slot(9), LC);
+        mmul<C, C, C, false, true, true, true, 2>(dm, slot(7), LC, slot(9), LC);
         const int m0 = GN::m0(), n0 = GN::n0();
         float* dG = slot(10);
 #pragma unroll
@@ -1070,33 +1089,33 @@ __global__ void __launch_bounds__(kNT, 1) bwd_local(BwdParams p) {
         }
     }
     __syncthreads();
-    if (below) to_smem_v<float, D>(slot(6), LD, p.dqbar + prow * D, D, C, c);  // slots 6-7
-    if (above) to_smem_v<float, D>(slot(8), LD, p.dkhat + prow * D, D, C, C);  // slots 8-9
+    if (below) to_smem_v<float, D, kNTL>(slot(6), LD, p.dqbar + prow * D, D, C, c);  // slots 6-7
+    if (above) to_smem_v<float, D, kNTL>(slot(8), LD, p.dkhat + prow * D, D, C, C);  // slots 8-9
     __syncthreads();
-    if (below) mmul<C, D, C, false, false, true, true>(aW, slot(12), LC, slot(6), LD);  // -= Y^T dQbar
-    if (above) mmul<C, D, C, false, true, true, true>(aW, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
+    if (below) mmul<C, D, C, false, false, true, true, 1>(aW, slot(12), LC, slot(6), LD);  // -= Y^T dQbar
+    if (above) mmul<C, D, C, false, true, true, true, 2>(aW, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
     __syncthreads();
-    to_smem_v<T, D>(slot(6), LD, q, D, C, c);
-    to_smem_v<T, D>(slot(8), LD, k, D, C, c);
+    to_smem_v<T, D, kNTL>(slot(6), LD, q, D, C, c);
+    to_smem_v<T, D, kNTL>(slot(8), LD, k, D, C, c);
     __syncthreads();
     typename GR::Acc aQ, aK;
     GR::zero(aQ);
     GR::zero(aK);
-    mmul<C, D, C, false, true, true>(aW, slot(5), LC, slot(6), LD);   // += dQw^T Q
-    mmul<C, D, C, false, true, true>(aW, slot(4), LC, slot(8), LD);   // += dKw^T K
-    mmul<C, D, C, false, false, true>(aQ, slot(0), LC, slot(8), LD);  // dSs K
-    mmul<C, D, C, false, true, true>(aK, slot(0), LC, slot(6), LD);   // dSs^T Q
+    mmul<C, D, C, false, true, true, false, 1>(aW, slot(5), LC, slot(6), LD);   // += dQw^T Q
+    mmul<C, D, C, false, true, true, false, 2>(aW, slot(4), LC, slot(8), LD);   // += dKw^T K
+    mmul<C, D, C, false, false, true, false, 2>(aQ, slot(0), LC, slot(8), LD);  // dSs K
+    mmul<C, D, C, false, true, true, false, 1>(aK, slot(0), LC, slot(6), LD);   // dSs^T Q
     __syncthreads();
-    to_smem_v<T, D>(slot(6), LD, w, D, C, c);
+    to_smem_v<T, D, kNTL>(slot(6), LD, w, D, C, c);
     __syncthreads();
     mmul<C, D, C, false, true, true>(aW, slot(10), LC, slot(6), LD);   // += (dG + dG^T) W
-    mmul<C, D, C, false, false, true>(aQ, slot(5), LC, slot(6), LD);  // += dQw W
-    mmul<C, D, C, false, false, true>(aK, slot(4), LC, slot(6), LD);  // += dKw W
+    mmul<C, D, C, false, false, true, false, 2>(aQ, slot(5), LC, slot(6), LD);  // += dQw W
+    mmul<C, D, C, false, false, true, false, 1>(aK, slot(4), LC, slot(6), LD);  // += dKw W
     mstore_out<D>(static_cast<T*>(p.dq) + hrow * D, aQ, below ? p.dqbar + prow * D : nullptr, c);
     mstore_out<D>(static_cast<T*>(p.dk) + hrow * D, aK, above ? p.dkhat + prow * D : nullptr, c);
     mstore_out<D>(static_cast<T*>(p.dw) + hrow * D, aW, nullptr, c);
     __syncthreads();
-    for (int r = threadIdx.x; r < c; r += kNT) {
+    for (int r = threadIdx.x; r < c; r += kNTL) {
         p.dbeta[hrow + r] = aB[r];
         if (p.fox)
             p.dctot[prow + r] = aC[r] + (below ? p.dcrow[prow + r] : 0.f) - (above ? p.dccol[prow + r] : 0.f);
@@ -1182,7 +1201,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigne
             bwd_reduce<T, D><<<dim3(p.N - 1, BH), kNT, b_reduce, st>>>(p);
         }
     }
-    bwd_local<T, D><<<dim3(p.N, BH), kNT, b_local, st>>>(p);
+    bwd_local<T, D><<<dim3(p.N, BH), kNTL, b_local, st>>>(p);
     if (log_f) bwd_fox_suffix<<<BH, 1024, 0, st>>>(p.dctot, p.L, p.Lp, p.dlog_f);
     return cudaGetLastError();
 }
