@@ -27,9 +27,10 @@
 // dbeta = -(w.g)(w.u) and dw = -beta ((w.u) g + (w.g) u).
 //
 // Kernels, in stream order:
-//   bwd_prep   one CTA per chunk        qbar, khat (walks), Delta
-//   bwd_pm     one CTA per inner chunk  P_m = I - W^T A W (compact form; fp32, or
-//                                       hi / lo bf16 for the tensor-core chains)
+//   bwd_prep   one CTA per chunk        qbar, khat, Delta and, for the inner
+//                                       chunks, P_m = I - W^T A W, all in the
+//                                       compact form (fp32 P_m, or hi / lo bf16
+//                                       for the tensor-core chains)
 //   bwd_chain  one CTA per query chunk  U chain down, G chain up; stores U,
 //                                       G, dS and P per (n, m) pair; dQbar;
 //                                       for bf16 at d = 128 bwd_chain_tc
@@ -66,9 +67,7 @@ namespace {
 
 constexpr int kC = kBwdC;
 constexpr int kNT = 256;
-constexpr int kNW = kNT / 32;
 constexpr int kNTL = 256;  // bwd_local
-constexpr int kNTP = 512;  // bwd_prep: sixteen latency-bound walks in flight per CTA
 
 struct BwdParams {
     const void *q, *k, *v, *w, *o, *dO;
@@ -103,27 +102,6 @@ __device__ __forceinline__ void vload(float (&a)[WV<D>::R], const G* src, int la
 #pragma unroll
     for (int r = 0; r < WV<D>::R; ++r) a[r] = WV<D>::ok(lane) ? to_f<G>(src[lane + 32 * r]) : 0.f;
 }
-template <int D, typename G>
-__device__ __forceinline__ void vstore(G* dst, const float (&a)[WV<D>::R], int lane) {
-    if (!WV<D>::ok(lane)) return;
-#pragma unroll
-    for (int r = 0; r < WV<D>::R; ++r) dst[lane + 32 * r] = from_f<G>(a[r]);
-}
-template <int D>
-__device__ __forceinline__ void vzero(float (&a)[WV<D>::R]) {
-#pragma unroll
-    for (int r = 0; r < WV<D>::R; ++r) a[r] = 0.f;
-}
-// a . s for a row s of D floats
-template <int D>
-__device__ __forceinline__ float vdot(const float (&a)[WV<D>::R], const float* s, int lane) {
-    float t = 0.f;
-    if (WV<D>::ok(lane)) {
-#pragma unroll
-        for (int r = 0; r < WV<D>::R; ++r) t = fmaf(a[r], s[lane + 32 * r], t);
-    }
-    return warp_sum(t);
-}
 template <int D>
 __device__ __forceinline__ float vdot(const float (&a)[WV<D>::R], const float (&b)[WV<D>::R]) {
     float t = 0.f;
@@ -131,20 +109,7 @@ __device__ __forceinline__ float vdot(const float (&a)[WV<D>::R], const float (&
     for (int r = 0; r < WV<D>::R; ++r) t = fmaf(a[r], b[r], t);
     return warp_sum(t);
 }
-// a <- a - coef * s
-template <int D>
-__device__ __forceinline__ void vaxpy(float (&a)[WV<D>::R], const float* s, float coef, int lane) {
-    if (!WV<D>::ok(lane)) return;
-#pragma unroll
-    for (int r = 0; r < WV<D>::R; ++r) a[r] = fmaf(-coef, s[lane + 32 * r], a[r]);
-}
-// a <- H a = a - beta (w . a) w, returns w . a
-template <int D>
-__device__ __forceinline__ float vstep(float (&a)[WV<D>::R], const float* w, float beta, int lane) {
-    const float t = vdot<D>(a, w, lane);
-    vaxpy<D>(a, w, beta * t, lane);
-    return t;
-}
+
 // Rows [0, rows) of a row-major global array of COLS columns (leading dim lds, rows starting
 // on 16-byte boundaries) into shared memory (leading dim ldd) as fp32; rows >= valid read as
 // zero.  16-byte loads, several in flight per thread; plain (coherent) loads, since a CTA
@@ -322,138 +287,14 @@ template <int D> struct BwdSmem {
     static constexpr int LC = kC + 4, LD = D + 4;  // K-major GEMM operands (16-byte rows)
     static constexpr int RK = (D * LC > kC * LD ? D * LC : kC * LD);
     static constexpr int RV = (D * LC > kC * LC ? D * LC : kC * LC);
-    static constexpr int prep = kC * D + kC;
-    static constexpr int pm = D * (kC + 4) + 2 * kC * (D + 4) + 3 * kC * (kC + 4) + kC;
     static constexpr int chain = 2 * D * LC + RK + RV + D * LD + 6 * kC;
     static constexpr int reduce = 3 * kC * LD + 2 * kC * LC;
     static constexpr int slot = kC * LC;              // bwd_local: one C x (C + 4) tile
     static constexpr int local = 13 * slot + 6 * kC;  // thirteen slots, six per-position vectors
+    static constexpr int prep = 11 * slot + kC;       // bwd_prep: eleven slots and beta
     static_assert(chain * 4 <= 227 * 1024 && local * 4 <= 227 * 1024 && reduce * 4 <= 227 * 1024,
                   "shared memory per CTA");
 };
-
-// ------------------------------------------------------------------ bwd_prep
-template <typename T, int D>
-__global__ void __launch_bounds__(kNTP) bwd_prep(BwdParams p) {
-    constexpr int C = kC;
-    extern __shared__ float smem[];
-    float* sW = smem;          // [C][D]
-    float* sB = sW + C * D;    // [C]
-    const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
-    const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
-    to_smem_v<T, D, kNTP>(sW, D, static_cast<const T*>(p.w) + hrow * D, D, C, c);
-    for (int r = threadIdx.x; r < C; r += kNTP) sB[r] = r < c ? p.beta[hrow + r] : 0.f;
-    __syncthreads();
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int r = wid; r < C; r += kNTP / 32) {
-        float u[WV<D>::R], x[WV<D>::R];
-        float dl = 0.f;
-        if (r < c) {
-            vload<D>(u, static_cast<const T*>(p.q) + (hrow + r) * D, lane);
-            for (int jj = r; jj >= 0; --jj) vstep<D>(u, sW + jj * D, sB[jj], lane);
-            vload<D>(x, static_cast<const T*>(p.k) + (hrow + r) * D, lane);
-            for (int tt = r + 1; tt < c; ++tt) vstep<D>(x, sW + tt * D, sB[tt], lane);
-            float oo[WV<D>::R], gg[WV<D>::R];
-            vload<D>(oo, static_cast<const T*>(p.o) + (hrow + r) * D, lane);
-            vload<D>(gg, static_cast<const T*>(p.dO) + (hrow + r) * D, lane);
-            dl = vdot<D>(oo, gg);
-        } else {
-            vzero<D>(u);
-            vzero<D>(x);
-        }
-        vstore<D>(p.qbar + (prow + r) * D, u, lane);
-        vstore<D>(p.khat + (prow + r) * D, x, lane);
-        if (p.khat16) vstore<D>(p.khat16 + (prow + r) * D, x, lane);
-        if (lane == 0) p.delta[prow + r] = dl;
-    }
-}
-
-// ------------------------------------------------------------------ bwd_pm
-// The chunk transition P_m = H_b ... H_e for 1 <= m <= N-2 in the compact form of
-// "Representação de Transformação UT" (§3): P_m = I - W^T A W with
-// A = (I + D triu_1(W W^T))^{-1} D, D = diag(beta): G = W W^T, the unit upper-triangular
-// inverse X = (I + D triu_1 G)^{-1} row by row from the bottom, A = X D, then two GEMMs.
-template <typename T, int D>
-__global__ void __launch_bounds__(kNT) bwd_pm(BwdParams p) {
-    constexpr int C = kC, LC = C + 4, LD = D + 4;
-    extern __shared__ __align__(16) float smem[];
-    float* sWT = smem;           // [D][LC] W^T
-    float* sW = sWT + D * LC;    // [C][LD] W
-    float* sG = sW + C * LD;     // [C][LC] G = W W^T
-    float* sX = sG + C * LC;     // [C][LC] X (row-major)
-    float* sAT = sX + C * LC;    // [C][LC] A^T
-    float* sAW = sAT + C * LC;   // [C][LD] A W
-    float* sB = sAW + C * LD;    // [C] beta
-    const int n = 1 + blockIdx.x, bh = blockIdx.y, b = n * C;  // chunks 1 .. N-2 are full
-    const size_t hrow = (size_t)bh * p.L + b;
-    const T* w = static_cast<const T*>(p.w) + hrow * D;
-    to_smem_v<T, D>(sW, LD, w, D, C, C);
-    to_smem_t<T, D>(sWT, LC, w, D, C, C);
-    for (int r = threadIdx.x; r < C; r += kNT) sB[r] = p.beta[hrow + r];
-    for (int idx = threadIdx.x; idx < C * LC; idx += kNT) sX[idx] = 0.f;
-    __syncthreads();
-    {  // G = W W^T
-        using GG = VT<C, C>;
-        typename GG::Acc acc;
-        GG::zero(acc);
-        vgemm<C, C, D>(acc, sWT, LC, sWT, LC);
-#pragma unroll
-        for (int i = 0; i < GG::TM; ++i)
-#pragma unroll
-            for (int j = 0; j < GG::TN; ++j) sG[(GG::m0() + i) * LC + GG::n0() + j] = acc[i][j];
-    }
-    __syncthreads();
-    // X[i][j] = [i == j] - beta_i sum_{i < k <= j} G[i][k] X[k][j]: four threads per column
-    for (int i = C - 1; i >= 0; --i) {
-        const int j = threadIdx.x >> 2, q = threadIdx.x & 3;
-        float t = 0.f;
-        if (j > i)
-            for (int k = i + 1 + q; k <= j; k += 4) t = fmaf(sG[i * LC + k], sX[k * LC + j], t);
-        t += __shfl_xor_sync(0xffffffffu, t, 1);
-        t += __shfl_xor_sync(0xffffffffu, t, 2);
-        if (q == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
-        __syncthreads();
-    }
-    // A = X D, stored transposed for the next product's K-major A operand
-    for (int idx = threadIdx.x; idx < C * C; idx += kNT) {
-        const int i = idx / C, j = idx % C;
-        sAT[j * LC + i] = sX[i * LC + j] * sB[j];
-    }
-    __syncthreads();
-    {  // A W
-        using GA = VT<C, D>;
-        typename GA::Acc acc;
-        GA::zero(acc);
-        vgemm<C, D, C>(acc, sAT, LC, sW, LD);
-#pragma unroll
-        for (int i = 0; i < GA::TM; ++i)
-#pragma unroll
-            for (int j = 0; j < GA::TN; ++j) sAW[(GA::m0() + i) * LD + GA::n0() + j] = acc[i][j];
-    }
-    __syncthreads();
-    // P = I - W^T (A W)
-    using GP = VT<D, D>;
-    typename GP::Acc acc;
-    GP::zero(acc);
-    vgemm<D, D, C>(acc, sW, LD, sAW, LD);
-    const size_t base = ((size_t)bh * p.N + n) * D * D;
-#pragma unroll
-    for (int i = 0; i < GP::TM; ++i)
-#pragma unroll
-        for (int j = 0; j < GP::TN; ++j) {
-            const int r = GP::m0() + i, cc = GP::n0() + j;
-            const float x = (r == cc ? 1.f : 0.f) - acc[i][j];
-            if (p.pm) {
-                p.pm[base + (size_t)r * D + cc] = x;
-                p.pmt[base + (size_t)cc * D + r] = x;
-            }
-            if (p.phi) {  // hi + lo bf16 split for the tensor-core chains
-                const __nv_bfloat16 h = __float2bfloat16_rn(x);
-                p.phi[base + (size_t)r * D + cc] = h;
-                p.plo[base + (size_t)r * D + cc] = __float2bfloat16_rn(x - __bfloat162float(h));
-            }
-        }
-}
 
 // ------------------------------------------------------------------ bwd_chain
 // Pair store layout (floats, per (n, m)): U [C][d], G [C][d], dS [C][C], P [C][C].
@@ -804,6 +645,189 @@ __device__ __forceinline__ void mstore_out(E* dst, const typename TT<kC, D, fals
     }
 }
 
+// X = (I + D triu_1 G)^{-1} (unit upper triangular) and A = X D, D = diag(beta), for a chunk of
+// C = 64 positions: the 16 x 16 diagonal blocks row by row from the bottom (one warp each,
+// X_ij = [i == j] - beta_i sum_{i < k <= j} G_ik X_kj), then two doubling merges
+// X_12 = -X_11 (D G_12) X_22.  sX must hold zeros on entry; the caller synchronises after.
+template <int C, int LC>
+__device__ __forceinline__ void ut_inverse(const float* sG, float* sX, float* sA, const float* sB) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (wid < C / 16) {
+        const int j = 16 * wid + (lane & 15), h = lane >> 4;
+        for (int i = 16 * wid + 15; i >= 16 * wid; --i) {
+            float t = 0.f;
+            for (int kk = i + 1 + h; kk <= j; kk += 2) t = fmaf(sG[i * LC + kk], sX[kk * LC + j], t);
+            t += __shfl_xor_sync(0xffffffffu, t, 16);
+            if (h == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    for (int s = 16; s < C; s *= 2) {  // blocks of s rows merged in pairs: C s / 2 elements
+        const int per = C * s / (2 * kNTL);  // elements per thread
+        float v[4];
+        for (int e = 0; e < per; ++e) {  // T = D G_12 X_22, written over the X_12 block
+            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
+            const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
+            float t = 0.f;
+            for (int kk = 2 * s * pr + s; kk <= bb; ++kk) t = fmaf(sG[a * LC + kk], sX[kk * LC + bb], t);
+            v[e] = sB[a] * t;
+        }
+        for (int e = 0; e < per; ++e) {
+            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
+            sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
+        }
+        __syncthreads();
+        for (int e = 0; e < per; ++e) {  // X_12 = -X_11 T
+            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
+            const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
+            float t = 0.f;
+            for (int kk = a; kk < 2 * s * pr + s; ++kk) t = fmaf(sX[a * LC + kk], sX[kk * LC + bb], t);
+            v[e] = -t;
+        }
+        __syncthreads();
+        for (int e = 0; e < per; ++e) {
+            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
+            sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
+        }
+        __syncthreads();
+    }
+    for (int idx = threadIdx.x; idx < C * C; idx += kNTL) {
+        const int r = idx / C, cc = idx % C;
+        sA[r * LC + cc] = sX[r * LC + cc] * sB[cc];
+    }
+}
+
+// rows r < C of a C x D result: dst[r][e] = src[r][e] - acc for r < c, 0 for the padded rows
+// (fp32, and a bf16 copy when dst16 is set)
+template <int D, typename S>
+__device__ __forceinline__ void mstore_diff(float* dst, __nv_bfloat16* dst16, const S* src,
+                                            const typename TT<kC, D, false>::Acc& acc, int c) {
+    using G = TT<kC, D, false>;
+    const int m0 = G::m0(), n0 = G::n0();
+#pragma unroll
+    for (int i = 0; i < G::TM; ++i) {
+        const int r = m0 + i;
+        float v[G::TN];
+#pragma unroll
+        for (int j = 0; j < G::TN; ++j) v[j] = r < c ? to_f<S>(src[(size_t)r * D + n0 + j]) - acc[i][j] : 0.f;
+        sts_vec<G::TN>(dst + (size_t)r * D + n0, v);
+        if (dst16)
+#pragma unroll
+            for (int j = 0; j < G::TN; ++j) dst16[(size_t)r * D + n0 + j] = __float2bfloat16_rn(v[j]);
+    }
+}
+
+// ------------------------------------------------------------------ bwd_prep
+// Per chunk, in the compact form of "Representação de Transformação UT" (§3): with G, X and A as
+// in bwd_local, Qm = tril(Q W^T), Km = striu(K W^T), Y = Qm A^T and Z = Km A,
+//   qbar = Q - Y W  (H_b ... H_i q_i),   khat = K - Z W  (H_e ... H_{j+1} k_j),
+//   P_n  = I - W^T (A W) for the inner chunks 1 <= n <= N - 2 (fp32 P and P^T, or hi / lo bf16),
+// and Delta_i = dO_i . o_i.  Eleven shared-memory slots as in bwd_local.
+template <typename T, int D>
+__global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
+    constexpr int C = kC, LC = C + 4, LD = D + 4, U = BwdSmem<D>::slot;
+    static_assert(C * LD <= 2 * U && D * LC <= 2 * U, "slot sizes");
+    extern __shared__ __align__(16) float smem[];
+    auto slot = [&](int i) { return smem + i * U; };
+    float* sB = smem + 11 * U;  // [C] beta
+    const int n = blockIdx.x, bh = blockIdx.y, b = n * C, c = min(C, p.L - b);
+    const size_t hrow = (size_t)bh * p.L + b, prow = (size_t)bh * p.Lp + b;
+    const T* q = static_cast<const T*>(p.q) + hrow * D;
+    const T* k = static_cast<const T*>(p.k) + hrow * D;
+    const T* w = static_cast<const T*>(p.w) + hrow * D;
+    using GN = TT<C, C, false>;
+    using GS = TT<C, C, true>;
+    using GR = TT<C, D, false>;
+    auto id = [](int, int, float x) { return x; };
+    for (int r = threadIdx.x; r < C; r += kNTL) sB[r] = r < c ? p.beta[hrow + r] : 0.f;
+    for (int idx = threadIdx.x; idx < U; idx += kNTL) slot(7)[idx] = 0.f;
+    to_smem_t<T, D, kNTL>(slot(0), LC, w, D, C, c);  // W^T, slots 0-1
+    to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
+    to_smem_t<T, D, kNTL>(slot(4), LC, k, D, C, c);  // K^T, slots 4-5
+    {  // Delta_i = dO_i . o_i, one warp per row
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        for (int r = wid; r < C; r += kNTL / 32) {
+            float dl = 0.f;
+            if (r < c) {
+                float oo[WV<D>::R], gg[WV<D>::R];
+                vload<D>(oo, static_cast<const T*>(p.o) + (hrow + r) * D, lane);
+                vload<D>(gg, static_cast<const T*>(p.dO) + (hrow + r) * D, lane);
+                dl = vdot<D>(oo, gg);
+            }
+            if (lane == 0) p.delta[prow + r] = dl;
+        }
+    }
+    __syncthreads();
+    {
+        typename GN::Acc g, qw, kw;
+        GN::zero(g);
+        GN::zero(qw);
+        GN::zero(kw);
+        mmul<C, C, D, false, true, true>(g, slot(0), LC, slot(0), LC);   // G = W W^T
+        mmul<C, C, D, false, true, true>(qw, slot(2), LC, slot(0), LC);  // Q W^T
+        mmul<C, C, D, false, true, true>(kw, slot(4), LC, slot(0), LC);  // K W^T
+        __syncthreads();
+        mstore<C, C, false, false>(slot(6), LC, g, id);
+        mstore<C, C, false, true>(slot(2), LC, qw, [](int i, int bb, float x) { return bb <= i ? x : 0.f; });  // Qm^T
+        mstore<C, C, false, false>(slot(4), LC, kw, [](int j, int a, float x) { return a > j ? x : 0.f; });    // Km
+    }
+    __syncthreads();
+    ut_inverse<C, LC>(slot(6), slot(7), slot(8), sB);  // X -> slot 7, A -> slot 8
+    __syncthreads();
+    to_smem_v<T, D, kNTL>(slot(0), LD, w, D, C, c);  // W [C][LD], slots 0-1
+    {
+        typename GS::Acc y;
+        GS::zero(y);
+        mmul<C, C, C, true, true, false>(y, slot(2), LC, slot(8), LC);  // Y = Qm A^T
+        mstore<C, C, true, true>(slot(3), LC, y, id);                   // Y^T
+        typename GN::Acc z;
+        GN::zero(z);
+        mmul<C, C, C, false, false, true, false, 1>(z, slot(4), LC, slot(8), LC);  // Z = Km A
+        mstore<C, C, false, false>(slot(5), LC, z, id);
+    }
+    __syncthreads();
+    {
+        typename GR::Acc acc;
+        GR::zero(acc);
+        mmul<C, D, C, false, true, true, false, 2>(acc, slot(3), LC, slot(0), LD);  // Y W
+        mstore_diff<D>(p.qbar + prow * D, nullptr, q, acc, c);
+        GR::zero(acc);
+        mmul<C, D, C, false, false, true, false, 1>(acc, slot(5), LC, slot(0), LD);  // Z W
+        mstore_diff<D>(p.khat + prow * D, p.khat16 ? p.khat16 + prow * D : nullptr, k, acc, c);
+    }
+    if (n < 1 || n > p.N - 2) return;
+    {
+        typename GR::Acc aw;
+        GR::zero(aw);
+        mmul<C, D, C, false, false, true, false, 1>(aw, slot(8), LC, slot(0), LD);  // A W
+        mstore<C, D, false, false>(slot(9), LD, aw, id);                            // slots 9-10
+    }
+    __syncthreads();
+    using GP = TT<D, D, false>;
+    typename GP::Acc pa;
+    GP::zero(pa);
+    mmul<D, D, C, false, true, true>(pa, slot(0), LD, slot(9), LD);  // W^T (A W)
+    const size_t base = ((size_t)bh * p.N + n) * D * D;
+    const int m0 = GP::m0(), n0 = GP::n0();
+#pragma unroll
+    for (int i = 0; i < GP::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < GP::TN; ++j) {
+            const int r = m0 + i, cc = n0 + j;
+            const float x = (r == cc ? 1.f : 0.f) - pa[i][j];
+            if (p.pm) {
+                p.pm[base + (size_t)r * D + cc] = x;
+                p.pmt[base + (size_t)cc * D + r] = x;
+            }
+            if (p.phi) {  // hi + lo bf16 split for the tensor-core chains
+                const __nv_bfloat16 h = __float2bfloat16_rn(x);
+                p.phi[base + (size_t)r * D + cc] = h;
+                p.plo[base + (size_t)r * D + cc] = __float2bfloat16_rn(x - __bfloat162float(h));
+            }
+        }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     constexpr int C = kC, LC = C + 4, LD = D + 4, U = BwdSmem<D>::slot;
@@ -851,56 +875,8 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         mstore<C, C, false, false>(slot(6), LC, g, id);
     }
     __syncthreads();
-    {  // X = (I + D triu_1 G)^{-1} -> slot 7 (until dM): the 16 x 16 diagonal blocks row by row from
-       // the bottom (one warp each), then two doubling merges X_12 = -X_11 (D G_12) X_22
-        const float* sG = slot(6);
-        float* sX = slot(7);
-        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-        if (wid < C / 16) {
-            const int j = 16 * wid + (lane & 15), h = lane >> 4;
-            for (int i = 16 * wid + 15; i >= 16 * wid; --i) {
-                float t = 0.f;
-                for (int kk = i + 1 + h; kk <= j; kk += 2) t = fmaf(sG[i * LC + kk], sX[kk * LC + j], t);
-                t += __shfl_xor_sync(0xffffffffu, t, 16);
-                if (h == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
-                __syncwarp();
-            }
-        }
-        __syncthreads();
-        for (int s = 16; s < C; s *= 2) {  // blocks of s rows merged in pairs; s * s * C / (2 s) elements
-            const int per = C * s / (2 * kNTL);  // elements per thread
-            float v[4];
-            for (int e = 0; e < per; ++e) {  // T = D G_12 X_22, written over the X_12 block
-                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-                const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
-                float t = 0.f;
-                for (int kk = 2 * s * pr + s; kk <= bb; ++kk) t = fmaf(sG[a * LC + kk], sX[kk * LC + bb], t);
-                v[e] = sB[a] * t;
-            }
-            for (int e = 0; e < per; ++e) {
-                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-                sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
-            }
-            __syncthreads();
-            for (int e = 0; e < per; ++e) {  // X_12 = -X_11 T
-                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-                const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
-                float t = 0.f;
-                for (int kk = a; kk < 2 * s * pr + s; ++kk) t = fmaf(sX[a * LC + kk], sX[kk * LC + bb], t);
-                v[e] = -t;
-            }
-            __syncthreads();
-            for (int e = 0; e < per; ++e) {
-                const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-                sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
-            }
-            __syncthreads();
-        }
-        for (int idx = threadIdx.x; idx < C * C; idx += kNTL) {  // A = X D -> slot 8 (until dQm)
-            const int r = idx / C, cc = idx % C;
-            slot(8)[r * LC + cc] = sX[r * LC + cc] * sB[cc];
-        }
-    }
+    ut_inverse<C, LC>(slot(6), slot(7), slot(8), sB);  // X -> slot 7 (until dM), A = X D -> slot 8 (until dQm)
+    __syncthreads();
     typename GR::Acc aW;  // dW, accumulated across the phases
     GR::zero(aW);
     if (hasP) {  // the chunk transition: dW -= A^T (W dP) + A (W dP^T), E = W dP W^T -> slot 9 (until dA)
@@ -1176,12 +1152,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, int BH, const float* log_f, unsigne
         cudaMemsetAsync(p.dccol, 0, (size_t)BH * p.Lp * sizeof(float), st);  // bwd_chain adds column sums
         cudaMemsetAsync(p.dcrow, 0, (size_t)BH * p.Lp * sizeof(float), st);  // bwd_chain_tc adds two halves per row
     }
-    bwd_prep<T, D><<<dim3(p.N, BH), kNTP, b_prep, st>>>(p);
-    if (p.N >= 3) {
-        const size_t b_pm = S::pm * sizeof(float);
-        cudaFuncSetAttribute(bwd_pm<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b_pm);
-        bwd_pm<T, D><<<dim3(p.N - 2, BH), kNT, b_pm, st>>>(p);
-    }
+    bwd_prep<T, D><<<dim3(p.N, BH), kNTL, b_prep, st>>>(p);
     if (p.N >= 2) {
         if constexpr (sizeof(T) == 2 && D == 128) {  // bf16: tensor-core chains (csrc/bwd_tc.cu)
             cudaError_t e = launch_bwd_chain_tc(p.dO, p.v, p.khat16, p.phi, p.plo, p.pairs, p.qbar, p.lse, p.delta,
