@@ -83,33 +83,6 @@ struct BwdParams {
     int fox;
 };
 
-// ------------------------------------------------------------------ warp-level vectors
-// A d-vector held by one warp: lane l owns elements l + 32 r (r < R); for d = 16
-// lanes 16..31 own nothing and hold zeros.
-template <int D> struct WV {
-    static constexpr int R = D >= 32 ? D / 32 : 1;
-    static __device__ __forceinline__ bool ok(int lane) { return D >= 32 || lane < D; }
-};
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
-template <int D, typename G>
-__device__ __forceinline__ void vload(float (&a)[WV<D>::R], const G* src, int lane) {
-#pragma unroll
-    for (int r = 0; r < WV<D>::R; ++r) a[r] = WV<D>::ok(lane) ? to_f<G>(src[lane + 32 * r]) : 0.f;
-}
-template <int D>
-__device__ __forceinline__ float vdot(const float (&a)[WV<D>::R], const float (&b)[WV<D>::R]) {
-    float t = 0.f;
-#pragma unroll
-    for (int r = 0; r < WV<D>::R; ++r) t = fmaf(a[r], b[r], t);
-    return warp_sum(t);
-}
-
 // Rows [0, rows) of a row-major global array of COLS columns (leading dim lds, rows starting
 // on 16-byte boundaries) into shared memory (leading dim ldd) as fp32; rows >= valid read as
 // zero.  16-byte loads, several in flight per thread; plain (coherent) loads, since a CTA
@@ -590,6 +563,53 @@ __device__ __forceinline__ void mstore(float* dst, int ld, const typename TT<M, 
     }
 }
 
+// W consecutive values of a global row as fp32 (16- or 8-byte loads; W a multiple of 4)
+template <int W, typename S>
+__device__ __forceinline__ void ld_row(float (&v)[W], const S* src) {
+    static_assert(W % 4 == 0, "row segment");
+    if constexpr (sizeof(S) == 4) {
+#pragma unroll
+        for (int j = 0; j < W; j += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + j);
+            v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < W; j += 4) {
+            const uint2 x = *reinterpret_cast<const uint2*>(src + j);
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+            v[j] = a.x; v[j + 1] = a.y; v[j + 2] = b.x; v[j + 3] = b.y;
+        }
+    }
+}
+// W consecutive values to a global row (W a multiple of 4): fp32 as 16-byte stores, bf16 packed
+// into 16-byte (W = 8) or 8-byte stores
+template <int W, typename E>
+__device__ __forceinline__ void st_row(E* dst, const float (&v)[W]) {
+    static_assert(W % 4 == 0, "row segment");
+    if constexpr (sizeof(E) == 4) {
+#pragma unroll
+        for (int j = 0; j < W; j += 4)
+            *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    } else {
+        uint32_t u[W / 2];
+#pragma unroll
+        for (int j = 0; j < W / 2; ++j) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+            u[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        if constexpr (W % 8 == 0) {
+#pragma unroll
+            for (int j = 0; j < W / 2; j += 4)
+                *reinterpret_cast<uint4*>(dst + 2 * j) = make_uint4(u[j], u[j + 1], u[j + 2], u[j + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < W / 2; j += 2) *reinterpret_cast<uint2*>(dst + 2 * j) = make_uint2(u[j], u[j + 1]);
+        }
+    }
+}
+
 // rows r < c of a C x D result to global memory: dst[r][e] = acc + (add ? add[r][e] : 0); the
 // addends are all loaded before the first store, and each thread's row segment is stored whole
 template <int D, typename E>
@@ -624,24 +644,8 @@ __device__ __forceinline__ void mstore_out(E* dst, const typename TT<kC, D, fals
             }
         }
 #pragma unroll
-        for (int i = 0; i < G::TM; ++i) {
-            if (m0 + i >= c) continue;
-            E* d = dst + (size_t)(m0 + i) * D + n0;
-            if constexpr (sizeof(E) == 4) {
-#pragma unroll
-                for (int j = 0; j < TN; j += 4)
-                    *reinterpret_cast<float4*>(d + j) = make_float4(v[i][j], v[i][j + 1], v[i][j + 2], v[i][j + 3]);
-            } else {
-                uint32_t u[TN / 2];
-#pragma unroll
-                for (int j = 0; j < TN / 2; ++j) {
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(v[i][2 * j], v[i][2 * j + 1]);
-                    u[j] = *reinterpret_cast<const uint32_t*>(&h);
-                }
-                if constexpr (TN == 8) *reinterpret_cast<uint4*>(d) = make_uint4(u[0], u[1], u[2], u[3]);
-                else *reinterpret_cast<uint2*>(d) = make_uint2(u[0], u[1]);
-            }
-        }
+        for (int i = 0; i < G::TM; ++i)
+            if (m0 + i < c) st_row<TN>(dst + (size_t)(m0 + i) * D + n0, v[i]);
     }
 }
 
@@ -705,16 +709,22 @@ __device__ __forceinline__ void mstore_diff(float* dst, __nv_bfloat16* dst16, co
                                             const typename TT<kC, D, false>::Acc& acc, int c) {
     using G = TT<kC, D, false>;
     const int m0 = G::m0(), n0 = G::n0();
+    static_assert(G::TN % 4 == 0, "row segments of whole 4-vectors");
+    float v[G::TM][G::TN];
 #pragma unroll
     for (int i = 0; i < G::TM; ++i) {
-        const int r = m0 + i;
-        float v[G::TN];
+        if (m0 + i < c) ld_row<G::TN>(v[i], src + (size_t)(m0 + i) * D + n0);
+        else
 #pragma unroll
-        for (int j = 0; j < G::TN; ++j) v[j] = r < c ? to_f<S>(src[(size_t)r * D + n0 + j]) - acc[i][j] : 0.f;
-        sts_vec<G::TN>(dst + (size_t)r * D + n0, v);
-        if (dst16)
+            for (int j = 0; j < G::TN; ++j) v[i][j] = 0.f;
+    }
 #pragma unroll
-            for (int j = 0; j < G::TN; ++j) dst16[(size_t)r * D + n0 + j] = __float2bfloat16_rn(v[j]);
+    for (int i = 0; i < G::TM; ++i) {
+        const bool ok = m0 + i < c;
+#pragma unroll
+        for (int j = 0; j < G::TN; ++j) v[i][j] = ok ? v[i][j] - acc[i][j] : 0.f;
+        st_row<G::TN>(dst + (size_t)(m0 + i) * D + n0, v[i]);
+        if (dst16) st_row<G::TN>(dst16 + (size_t)(m0 + i) * D + n0, v[i]);
     }
 }
 
@@ -745,18 +755,24 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
     to_smem_t<T, D, kNTL>(slot(0), LC, w, D, C, c);  // W^T, slots 0-1
     to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
     to_smem_t<T, D, kNTL>(slot(4), LC, k, D, C, c);  // K^T, slots 4-5
-    {  // Delta_i = dO_i . o_i, one warp per row
-        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-        for (int r = wid; r < C; r += kNTL / 32) {
-            float dl = 0.f;
-            if (r < c) {
-                float oo[WV<D>::R], gg[WV<D>::R];
-                vload<D>(oo, static_cast<const T*>(p.o) + (hrow + r) * D, lane);
-                vload<D>(gg, static_cast<const T*>(p.dO) + (hrow + r) * D, lane);
-                dl = vdot<D>(oo, gg);
+    {  // Delta_i = dO_i . o_i: four threads per row, each a quarter of it
+        static_assert(kNTL == 4 * C, "four threads per row");
+        const int r = threadIdx.x >> 2, part = threadIdx.x & 3;
+        float t = 0.f;
+        if (r < c) {
+            const T* orow = static_cast<const T*>(p.o) + (hrow + r) * D + part * (D / 4);
+            const T* grow = static_cast<const T*>(p.dO) + (hrow + r) * D + part * (D / 4);
+#pragma unroll
+            for (int j = 0; j < D / 4; j += 4) {
+                float a[4], g[4];
+                ld_row<4>(a, orow + j);
+                ld_row<4>(g, grow + j);
+                t = fmaf(a[0], g[0], fmaf(a[1], g[1], fmaf(a[2], g[2], fmaf(a[3], g[3], t))));
             }
-            if (lane == 0) p.delta[prow + r] = dl;
         }
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        t += __shfl_xor_sync(0xffffffffu, t, 2);
+        if (part == 0) p.delta[prow + r] = t;
     }
     __syncthreads();
     {
@@ -813,19 +829,44 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
 #pragma unroll
     for (int i = 0; i < GP::TM; ++i)
 #pragma unroll
+        for (int j = 0; j < GP::TN; ++j) pa[i][j] = (m0 + i == n0 + j ? 1.f : 0.f) - pa[i][j];
+    if (p.pm) {  // fp32 P and P^T
+#pragma unroll
+        for (int i = 0; i < GP::TM; ++i) {
+            if constexpr (GP::TN % 4 == 0) st_row<GP::TN>(p.pm + base + (size_t)(m0 + i) * D + n0, pa[i]);
+            else
+#pragma unroll
+                for (int j = 0; j < GP::TN; ++j) p.pm[base + (size_t)(m0 + i) * D + n0 + j] = pa[i][j];
+        }
+#pragma unroll
         for (int j = 0; j < GP::TN; ++j) {
-            const int r = m0 + i, cc = n0 + j;
-            const float x = (r == cc ? 1.f : 0.f) - pa[i][j];
-            if (p.pm) {
-                p.pm[base + (size_t)r * D + cc] = x;
-                p.pmt[base + (size_t)cc * D + r] = x;
-            }
-            if (p.phi) {  // hi + lo bf16 split for the tensor-core chains
-                const __nv_bfloat16 h = __float2bfloat16_rn(x);
-                p.phi[base + (size_t)r * D + cc] = h;
-                p.plo[base + (size_t)r * D + cc] = __float2bfloat16_rn(x - __bfloat162float(h));
+            float t[GP::TM];
+#pragma unroll
+            for (int i = 0; i < GP::TM; ++i) t[i] = pa[i][j];
+            if constexpr (GP::TM % 4 == 0) st_row<GP::TM>(p.pmt + base + (size_t)(n0 + j) * D + m0, t);
+            else
+#pragma unroll
+                for (int i = 0; i < GP::TM; ++i) p.pmt[base + (size_t)(n0 + j) * D + m0 + i] = t[i];
+        }
+    }
+    if (p.phi) {  // hi + lo bf16 split for the tensor-core chains (d = 128)
+#pragma unroll
+        for (int i = 0; i < GP::TM; ++i) {
+            float lo[GP::TN];
+#pragma unroll
+            for (int j = 0; j < GP::TN; ++j) lo[j] = pa[i][j] - __bfloat162float(__float2bfloat16_rn(pa[i][j]));
+            if constexpr (GP::TN % 4 == 0) {
+                st_row<GP::TN>(p.phi + base + (size_t)(m0 + i) * D + n0, pa[i]);
+                st_row<GP::TN>(p.plo + base + (size_t)(m0 + i) * D + n0, lo);
+            } else {
+#pragma unroll
+                for (int j = 0; j < GP::TN; ++j) {
+                    p.phi[base + (size_t)(m0 + i) * D + n0 + j] = __float2bfloat16_rn(pa[i][j]);
+                    p.plo[base + (size_t)(m0 + i) * D + n0 + j] = __float2bfloat16_rn(lo[j]);
+                }
             }
         }
+    }
 }
 
 template <typename T, int D>
