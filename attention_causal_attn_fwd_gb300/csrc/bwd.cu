@@ -649,53 +649,70 @@ __device__ __forceinline__ void mstore_out(E* dst, const typename TT<kC, D, fals
     }
 }
 
+// One doubling merge of the triangular inverse: for each pair of S-row blocks on the diagonal,
+// X_12 = -X_11 (D G_12) X_22, written over the X_12 block.  Every thread owns PER elements of
+// the pairs' X_12 blocks and sums them side by side over whole blocks (the zeros of the
+// triangular X_11 and X_22 add nothing).
+template <int C, int LC, int S>
+__device__ __forceinline__ void ut_merge(const float* sG, float* sX, const float* sB) {
+    constexpr int PER = C * S / (2 * kNTL);
+    static_assert(PER >= 1 && PER * 2 * kNTL == C * S, "whole elements per thread");
+    int a[PER], bb[PER], kb[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+        const int idx = threadIdx.x + e * kNTL, pr = idx / (S * S), rem = idx % (S * S);
+        kb[e] = 2 * S * pr;
+        a[e] = kb[e] + rem / S;
+        bb[e] = kb[e] + S + rem % S;
+    }
+    float v[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) v[e] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < S; ++kk)  // T = D G_12 X_22
+#pragma unroll
+        for (int e = 0; e < PER; ++e)
+            v[e] = fmaf(sG[a[e] * LC + kb[e] + S + kk], sX[(kb[e] + S + kk) * LC + bb[e]], v[e]);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) sX[a[e] * LC + bb[e]] = sB[a[e]] * v[e];
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < PER; ++e) v[e] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < S; ++kk)  // X_12 = -X_11 T
+#pragma unroll
+        for (int e = 0; e < PER; ++e) v[e] = fmaf(sX[a[e] * LC + kb[e] + kk], sX[(kb[e] + kk) * LC + bb[e]], v[e]);
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < PER; ++e) sX[a[e] * LC + bb[e]] = -v[e];
+    __syncthreads();
+}
+
 // X = (I + D triu_1 G)^{-1} (unit upper triangular) and A = X D, D = diag(beta), for a chunk of
 // C = 64 positions: the 16 x 16 diagonal blocks row by row from the bottom (one warp each,
-// X_ij = [i == j] - beta_i sum_{i < k <= j} G_ik X_kj), then two doubling merges
-// X_12 = -X_11 (D G_12) X_22.  sX must hold zeros on entry; the caller synchronises after.
+// X_ij = [i == j] - beta_i sum_{i < k <= j} G_ik X_kj), then two doubling merges.  sX must hold
+// zeros on entry; the caller synchronises after.
 template <int C, int LC>
 __device__ __forceinline__ void ut_inverse(const float* sG, float* sX, float* sA, const float* sB) {
+    static_assert(C == 64, "two merges after the 16 x 16 blocks");
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     if (wid < C / 16) {
         const int j = 16 * wid + (lane & 15), h = lane >> 4;
         for (int i = 16 * wid + 15; i >= 16 * wid; --i) {
             float t = 0.f;
-            for (int kk = i + 1 + h; kk <= j; kk += 2) t = fmaf(sG[i * LC + kk], sX[kk * LC + j], t);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {  // k = i + 1 + h + 2u <= j, at most eight terms per lane
+                const int kk = i + 1 + h + 2 * u;
+                if (kk <= j) t = fmaf(sG[i * LC + kk], sX[kk * LC + j], t);
+            }
             t += __shfl_xor_sync(0xffffffffu, t, 16);
             if (h == 0 && j >= i) sX[i * LC + j] = (j == i ? 1.f : 0.f) - sB[i] * t;
             __syncwarp();
         }
     }
     __syncthreads();
-    for (int s = 16; s < C; s *= 2) {  // blocks of s rows merged in pairs: C s / 2 elements
-        const int per = C * s / (2 * kNTL);  // elements per thread
-        float v[4];
-        for (int e = 0; e < per; ++e) {  // T = D G_12 X_22, written over the X_12 block
-            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-            const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
-            float t = 0.f;
-            for (int kk = 2 * s * pr + s; kk <= bb; ++kk) t = fmaf(sG[a * LC + kk], sX[kk * LC + bb], t);
-            v[e] = sB[a] * t;
-        }
-        for (int e = 0; e < per; ++e) {
-            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-            sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
-        }
-        __syncthreads();
-        for (int e = 0; e < per; ++e) {  // X_12 = -X_11 T
-            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-            const int a = 2 * s * pr + rem / s, bb = 2 * s * pr + s + rem % s;
-            float t = 0.f;
-            for (int kk = a; kk < 2 * s * pr + s; ++kk) t = fmaf(sX[a * LC + kk], sX[kk * LC + bb], t);
-            v[e] = -t;
-        }
-        __syncthreads();
-        for (int e = 0; e < per; ++e) {
-            const int idx = threadIdx.x + e * kNTL, pr = idx / (s * s), rem = idx % (s * s);
-            sX[(2 * s * pr + rem / s) * LC + 2 * s * pr + s + rem % s] = v[e];
-        }
-        __syncthreads();
-    }
+    ut_merge<C, LC, 16>(sG, sX, sB);
+    ut_merge<C, LC, 32>(sG, sX, sB);
     for (int idx = threadIdx.x; idx < C * C; idx += kNTL) {
         const int r = idx / C, cc = idx % C;
         sA[r * LC + cc] = sX[r * LC + cc] * sB[cc];
