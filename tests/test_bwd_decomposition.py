@@ -19,6 +19,17 @@ csrc/bwd.cu and csrc/bwd_tc.cu stage by stage; the tests check that they reprodu
 dq, dk, dv, dw, dbeta (and dlog f) to fp64 rounding for several chunk sizes, ragged last chunks,
 beta = 0 and beta = 2 positions, with and without forget gates.  It shares no code with the
 kernels and computes nothing the oracle relies on.
+
+The kernels form prep and local in the compact form of §3 "Representação de Transformação UT"
+instead of walking (form="compact" below).  For a chunk with rows W, Q, K and D = diag(beta):
+
+  G = W W^T,  X = (I + D triu_1 G)^-1,  A = X D   (H_a ... H_b = I - W^T A W over a..b, a principal
+                                                  block of A for a sub-range)
+  Qm = tril(Q W^T), Km = striu(K W^T), Y = Qm A^T, Z = Km A
+  qbar = Q - Y W,  khat = K - Z W,  P = I - W^T A W,  S_diag = scale (Q K^T - Y Km^T) + c_i - c_j
+
+and local is the reverse mode of these products (compact_local); both forms are held to the
+oracle with the same bound.
 """
 import numpy as np
 import pytest
@@ -31,7 +42,50 @@ def _H(x, w, b):
     return x - b * (x @ w)[..., None] * w
 
 
-def chunked_bwd(q, k, v, w, beta, dO, log_f, scale, C):
+def _ut_factors(W, beta):
+    """G = W W^T, X = (I + D triu_1 G)^-1 and A = X D: H_b ... H_e = I - W^T A W for the chunk."""
+    G = W @ W.T
+    X = np.linalg.inv(np.eye(len(beta)) + np.diag(beta) @ np.triu(G, 1))
+    return G, X, X * beta[None, :]
+
+
+def compact_prep(Q, K, W, beta):
+    """qbar, khat and the chunk transition of one chunk from products (no walks)."""
+    _, _, A = _ut_factors(W, beta)
+    Y = np.tril(Q @ W.T) @ A.T
+    Z = np.triu(K @ W.T, 1) @ A
+    return Q - Y @ W, K - Z @ W, np.eye(W.shape[1]) - W.T @ A @ W
+
+
+def compact_local(Q, K, V, W, beta, dO, lse, Delta, c, dQb, dKh, dP, scale):
+    """The reverse mode of compact_prep and of the diagonal block's logits, for one chunk; returns
+    dq, dk, the diagonal part of dv, dw, dbeta and the diagonal part of dc."""
+    C = len(beta)
+    G, X, A = _ut_factors(W, beta)
+    le, gt = np.tril(np.ones((C, C))), np.triu(np.ones((C, C)), 1)
+    Qm, Km = (Q @ W.T) * le, (K @ W.T) * gt
+    Y, Z = Qm @ A.T, Km @ A
+    S = scale * (Q @ K.T - Y @ Km.T) + c[:, None] - c[None, :]
+    Pr = np.where(le > 0, np.exp(np.where(le > 0, S, 0.0) - lse[:, None]), 0.0)
+    dS = Pr * (dO @ V.T - Delta[:, None])
+    dSs = scale * dS
+    dZ = -dKh @ W.T
+    dY = -dQb @ W.T - dSs @ Km
+    dKw = (-dSs.T @ Y + dZ @ A.T) * gt
+    dQw = (dY @ A) * le
+    R1, R2 = W @ dP, W @ dP.T
+    dA = Km.T @ dZ + dY.T @ Qm - R1 @ W.T
+    dbeta = (X * dA).sum(0)                 # A = X D
+    dM = -X.T @ (dA * beta[None, :]) @ X.T  # X = M^-1, M = I + D triu_1 G
+    dbeta += (dM * G * gt).sum(1)
+    dG = beta[:, None] * dM * gt
+    dW = (-A.T @ R1 - A @ R2 - Y.T @ dQb - Z.T @ dKh + dQw.T @ Q + dKw.T @ K + (dG + dG.T) @ W)
+    dQ = dQb + dSs @ K + dQw @ W
+    dK = dKh + dSs.T @ Q + dKw @ W
+    return dQ, dK, Pr.T @ dO, dW, dbeta, dS.sum(1) - dS.sum(0)
+
+
+def chunked_bwd(q, k, v, w, beta, dO, log_f, scale, C, form="walks"):
     L, d = q.shape
     N = -(-L // C)
     span = lambda n: (n * C, min(L, n * C + C))
@@ -43,6 +97,9 @@ def chunked_bwd(q, k, v, w, beta, dO, log_f, scale, C):
     qbar, khat, Pm = np.zeros((L, d)), np.zeros((L, d)), np.zeros((N, d, d))
     for n in range(N):
         b, e = span(n)
+        if form == "compact":
+            qbar[b:e], khat[b:e], Pm[n] = compact_prep(q[b:e], k[b:e], w[b:e], beta[b:e])
+            continue
         for i in range(b, e):
             u = q[i].copy()
             for j in range(i, b - 1, -1):
@@ -105,6 +162,14 @@ def chunked_bwd(q, k, v, w, beta, dO, log_f, scale, C):
 
     for n in range(N):
         b, e = span(n)
+        if form == "compact":
+            dPn = dPm[n] if 1 <= n <= N - 2 else np.zeros((d, d))
+            r = compact_local(q[b:e], k[b:e], v[b:e], w[b:e], beta[b:e], dO[b:e], lse[b:e], Delta[b:e], c[b:e],
+                              dqbar[b:e], dkhat[b:e], dPn, scale)
+            dq[b:e], dk[b:e], dw[b:e], db[b:e] = r[0], r[1], r[3], r[4]
+            dv[b:e] += r[2]
+            dc[b:e] += r[5]
+            continue
         for i in range(b, e):  # (a) row i: diagonal logits and the walk that built qbar_i
             us, s, u = {}, {}, q[i].copy()
             for j in range(i, b - 1, -1):
@@ -152,9 +217,10 @@ def chunked_bwd(q, k, v, w, beta, dO, log_f, scale, C):
     return out
 
 
+@pytest.mark.parametrize("form", ["walks", "compact"])
 @pytest.mark.parametrize("L,d,C,fox", [(20, 4, 6, False), (23, 5, 4, True), (64, 8, 16, True), (33, 6, 8, False),
                                        (9, 3, 16, True)])
-def test_chunked_backward_matches_oracle(L, d, C, fox):
+def test_chunked_backward_matches_oracle(L, d, C, fox, form):
     """Several chunks with ragged last chunks (and one chunk larger than L); beta = 0 at position 3
     and beta = 2 at position 5 where present."""
     rng = np.random.default_rng(100 + L)
@@ -166,7 +232,7 @@ def test_chunked_backward_matches_oracle(L, d, C, fox):
         beta[3], beta[5] = 0.0, 2.0
     lf = -rng.uniform(0.0, 1.0, L) if fox else None
     ref = orc.path_attn_bwd(q, k, v, w, beta, dO, log_f=lf, scale=0.5)
-    got = chunked_bwd(q, k, v, w, beta, dO, lf, 0.5, C)
+    got = chunked_bwd(q, k, v, w, beta, dO, lf, 0.5, C, form)
     assert set(got) == set(ref)
     for name in ref:
         scale = max(float(np.abs(ref[name]).max()), 1e-12)
