@@ -649,6 +649,127 @@ __device__ __forceinline__ void mstore_out(E* dst, const typename TT<kC, D, fals
     }
 }
 
+// ------------------------------------------------------------------ warp-level bf16 tensor-core products
+// mma.sync m16n8k16 (bf16 operands, fp32 accumulation) on fp32 shared-memory operands, for the
+// bf16 path.  An operand that holds bf16 values exactly (w, q, k, v, dO) enters as it is; any
+// other is split into hi = bf16(x) and lo = bf16(x - hi) and the product takes hi B + lo B (or
+// A hi + A lo): what it drops is below 2^-16 of each term.
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {  // x0 in the low half
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 f = __bfloat1622float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = pack_bf16(x0 - f.x, x1 - f.y);
+}
+
+// Warp tiling of an M x N output over the eight warps of a 256-thread CTA: a 2 x 4 grid of warps,
+// each owning MT x NT tiles of 16 x 8 in the mma.sync accumulator layout (lane l holds rows
+// l / 4 and l / 4 + 8, columns 2 (l % 4) and 2 (l % 4) + 1 of every tile).
+template <int M, int N> struct WT {
+    static constexpr int WM = 2, WN = 4;
+    static constexpr int MT = M / (WM * 16), NT = N / (WN * 8);
+    static_assert(MT >= 1 && NT >= 1 && MT * WM * 16 == M && NT * WN * 8 == N, "warp tiling");
+    using Acc = float[MT][NT][4];
+    static __device__ __forceinline__ int mb() { return (int)(threadIdx.x >> 5) / WN * (M / WM); }
+    static __device__ __forceinline__ int nb() { return (int)(threadIdx.x >> 5) % WN * (N / WN); }
+    static __device__ __forceinline__ int row(int mt, int i) {
+        return mb() + mt * 16 + (int)((threadIdx.x & 31) >> 2) + 8 * (i >> 1);
+    }
+    static __device__ __forceinline__ int col(int nt, int i) { return nb() + nt * 8 + 2 * (int)(threadIdx.x & 3) + (i & 1); }
+    static __device__ __forceinline__ void zero(Acc& a) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[mt][nt][i] = 0.f;
+    }
+};
+
+// acc += sum_k a(m, k) b(k, n) over the warp's tiles, operands fp32 in shared memory with the
+// layouts of mmul (AK: a(m, k) = A[k lda + m], else A[m lda + k]; BK: b(k, n) = B[k ldb + n],
+// else B[n ldb + k]).  ASPL / BSPL split that operand into hi + lo.  KR as in mmul, per warp.
+// With leading dims of 4 mod 32 floats the K-major fragment reads are free of bank conflicts.
+template <int M, int N, int K, bool AK, bool BK, bool ASPL, bool BSPL, int KR = 0>
+__device__ __forceinline__ void mma_mul(typename WT<M, N>::Acc& acc, const float* A, int lda, const float* B,
+                                        int ldb) {
+    using W = WT<M, N>;
+    static_assert(K % 16 == 0, "depth");
+    static_assert(KR == 0 || M == K, "a triangular A is square");
+    const int g = (threadIdx.x & 31) >> 2, t = threadIdx.x & 3;
+    const int mb = W::mb(), nb = W::nb();
+    const int kb = KR == 1 ? (mb & ~15) : 0;
+    const int ke = KR == 2 ? min(K, mb + M / W::WM) : K;
+#pragma unroll 1
+    for (int k0 = kb; k0 < ke; k0 += 16) {
+        uint32_t ah[W::MT][4], al[W::MT][4], bh[W::NT][2], bl[W::NT][2];
+#pragma unroll
+        for (int mt = 0; mt < W::MT; ++mt)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int m = mb + mt * 16 + g + 8 * (r & 1), k = k0 + 2 * t + 8 * (r >> 1);
+                float x0, x1;
+                if constexpr (AK) {
+                    x0 = A[k * lda + m];
+                    x1 = A[(k + 1) * lda + m];
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(A + m * lda + k);
+                    x0 = v.x;
+                    x1 = v.y;
+                }
+                if constexpr (ASPL) split_bf16(x0, x1, ah[mt][r], al[mt][r]);
+                else ah[mt][r] = pack_bf16(x0, x1);
+            }
+#pragma unroll
+        for (int nt = 0; nt < W::NT; ++nt)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int k = k0 + 2 * t + 8 * r, n = nb + nt * 8 + g;
+                float x0, x1;
+                if constexpr (BK) {
+                    x0 = B[k * ldb + n];
+                    x1 = B[(k + 1) * ldb + n];
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(B + n * ldb + k);
+                    x0 = v.x;
+                    x1 = v.y;
+                }
+                if constexpr (BSPL) split_bf16(x0, x1, bh[nt][r], bl[nt][r]);
+                else bh[nt][r] = pack_bf16(x0, x1);
+            }
+#pragma unroll
+        for (int mt = 0; mt < W::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < W::NT; ++nt) {
+                mma16816(acc[mt][nt], ah[mt], bh[nt]);
+                if constexpr (ASPL) mma16816(acc[mt][nt], al[mt], bh[nt]);
+                if constexpr (BSPL) mma16816(acc[mt][nt], ah[mt], bl[nt]);
+            }
+    }
+}
+
+// f(row, col, v0, v1) for each pair of adjacent columns (col, col + 1) the lane holds
+template <int M, int N, typename F>
+__device__ __forceinline__ void frag_pairs(const typename WT<M, N>::Acc& acc, F f) {
+    using W = WT<M, N>;
+#pragma unroll
+    for (int mt = 0; mt < W::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < W::NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) f(W::row(mt, 2 * h), W::col(nt, 0), acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
+}
+
 // One doubling merge of the triangular inverse: for each pair of S-row blocks on the diagonal,
 // X_12 = -X_11 (D G_12) X_22, written over the X_12 block.  Every thread owns PER elements of
 // the pairs' X_12 blocks and sums them side by side over whole blocks (the zeros of the
@@ -719,6 +840,11 @@ __device__ __forceinline__ void ut_inverse(const float* sG, float* sX, float* sA
     }
 }
 
+// two consecutive bf16 values of a row as floats
+__device__ __forceinline__ float2 to_f2(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
 // rows r < C of a C x D result: dst[r][e] = src[r][e] - acc for r < c, 0 for the padded rows
 // (fp32, and a bf16 copy when dst16 is set)
 template <int D, typename S>
@@ -754,6 +880,7 @@ __device__ __forceinline__ void mstore_diff(float* dst, __nv_bfloat16* dst16, co
 template <typename T, int D>
 __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
     constexpr int C = kC, LC = C + 4, LD = D + 4, U = BwdSmem<D>::slot;
+    constexpr bool TC = sizeof(T) == 2 && D >= 64;  // bf16 operands: the products on the tensor cores
     static_assert(C * LD <= 2 * U && D * LC <= 2 * U, "slot sizes");
     extern __shared__ __align__(16) float smem[];
     auto slot = [&](int i) { return smem + i * U; };
@@ -792,7 +919,28 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
         if (part == 0) p.delta[prow + r] = t;
     }
     __syncthreads();
-    {
+    if constexpr (TC) {  // G = W W^T, Q W^T, K W^T: bf16 operands, one product each
+        using WC = WT<C, C>;
+        typename WC::Acc g, qw, kw;
+        WC::zero(g);
+        WC::zero(qw);
+        WC::zero(kw);
+        mma_mul<C, C, D, true, true, false, false>(g, slot(0), LC, slot(0), LC);
+        mma_mul<C, C, D, true, true, false, false>(qw, slot(2), LC, slot(0), LC);
+        mma_mul<C, C, D, true, true, false, false>(kw, slot(4), LC, slot(0), LC);
+        __syncthreads();
+        float *sG = slot(6), *sQT = slot(2), *sKm = slot(4);
+        frag_pairs<C, C>(g, [&](int r, int cc, float v0, float v1) {
+            *reinterpret_cast<float2*>(sG + r * LC + cc) = make_float2(v0, v1);
+        });
+        frag_pairs<C, C>(qw, [&](int r, int cc, float v0, float v1) {  // Qm^T
+            sQT[cc * LC + r] = cc <= r ? v0 : 0.f;
+            sQT[(cc + 1) * LC + r] = cc + 1 <= r ? v1 : 0.f;
+        });
+        frag_pairs<C, C>(kw, [&](int r, int cc, float v0, float v1) {  // Km
+            *reinterpret_cast<float2*>(sKm + r * LC + cc) = make_float2(cc > r ? v0 : 0.f, cc + 1 > r ? v1 : 0.f);
+        });
+    } else {
         typename GN::Acc g, qw, kw;
         GN::zero(g);
         GN::zero(qw);
@@ -820,7 +968,42 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
         mstore<C, C, false, false>(slot(5), LC, z, id);
     }
     __syncthreads();
-    {
+    if constexpr (TC) {  // Y W and Z W (Y, Z split into hi + lo), then qbar = Q - Y W, khat = K - Z W
+        using WR = WT<C, D>;
+        typename WR::Acc yw, zw;
+        WR::zero(yw);
+        WR::zero(zw);
+        mma_mul<C, D, C, true, true, true, false, 2>(yw, slot(3), LC, slot(0), LD);
+        mma_mul<C, D, C, false, true, true, false, 1>(zw, slot(5), LC, slot(0), LD);
+        float* qb = p.qbar + prow * D;
+        float* kh = p.khat + prow * D;
+        __nv_bfloat16* kh16 = p.khat16 ? p.khat16 + prow * D : nullptr;
+        frag_pairs<C, D>(yw, [&](int r, int cc, float v0, float v1) {
+            float2 x = make_float2(0.f, 0.f);
+            if (r < c) {
+                const float2 f = to_f2(q + (size_t)r * D + cc);
+                x = make_float2(f.x - v0, f.y - v1);
+            }
+            *reinterpret_cast<float2*>(qb + (size_t)r * D + cc) = x;
+        });
+        frag_pairs<C, D>(zw, [&](int r, int cc, float v0, float v1) {
+            float2 x = make_float2(0.f, 0.f);
+            if (r < c) {
+                const float2 f = to_f2(k + (size_t)r * D + cc);
+                x = make_float2(f.x - v0, f.y - v1);
+            }
+            *reinterpret_cast<float2*>(kh + (size_t)r * D + cc) = x;
+            if (kh16) *reinterpret_cast<__nv_bfloat162*>(kh16 + (size_t)r * D + cc) = __floats2bfloat162_rn(x.x, x.y);
+        });
+        if (n < 1 || n > p.N - 2) return;
+        typename WR::Acc aw;
+        WR::zero(aw);
+        mma_mul<C, D, C, false, true, true, false, 1>(aw, slot(8), LC, slot(0), LD);  // A W
+        float* sAW = slot(9);  // [C][LD], slots 9-10
+        frag_pairs<C, D>(aw, [&](int r, int cc, float v0, float v1) {
+            *reinterpret_cast<float2*>(sAW + r * LD + cc) = make_float2(v0, v1);
+        });
+    } else {
         typename GR::Acc acc;
         GR::zero(acc);
         mmul<C, D, C, false, true, true, false, 2>(acc, slot(3), LC, slot(0), LD);  // Y W
@@ -828,20 +1011,40 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
         GR::zero(acc);
         mmul<C, D, C, false, false, true, false, 1>(acc, slot(5), LC, slot(0), LD);  // Z W
         mstore_diff<D>(p.khat + prow * D, p.khat16 ? p.khat16 + prow * D : nullptr, k, acc, c);
-    }
-    if (n < 1 || n > p.N - 2) return;
-    {
+        if (n < 1 || n > p.N - 2) return;
         typename GR::Acc aw;
         GR::zero(aw);
         mmul<C, D, C, false, false, true, false, 1>(aw, slot(8), LC, slot(0), LD);  // A W
         mstore<C, D, false, false>(slot(9), LD, aw, id);                            // slots 9-10
     }
     __syncthreads();
+    const size_t base = ((size_t)bh * p.N + n) * D * D;
+    if constexpr (TC) {  // P = I - W^T (A W), A W split into hi + lo
+        using WP = WT<D, D>;
+        typename WP::Acc pa;
+        WP::zero(pa);
+        mma_mul<D, D, C, true, true, false, true>(pa, slot(0), LD, slot(9), LD);
+        frag_pairs<D, D>(pa, [&](int r, int cc, float v0, float v1) {
+            const float x0 = (r == cc ? 1.f : 0.f) - v0, x1 = (r == cc + 1 ? 1.f : 0.f) - v1;
+            const size_t o = base + (size_t)r * D + cc;
+            if (p.pm) {
+                *reinterpret_cast<float2*>(p.pm + o) = make_float2(x0, x1);
+                p.pmt[base + (size_t)cc * D + r] = x0;
+                p.pmt[base + (size_t)(cc + 1) * D + r] = x1;
+            }
+            if (p.phi) {
+                uint32_t hi, lo;
+                split_bf16(x0, x1, hi, lo);
+                *reinterpret_cast<uint32_t*>(p.phi + o) = hi;
+                *reinterpret_cast<uint32_t*>(p.plo + o) = lo;
+            }
+        });
+        return;
+    }
     using GP = TT<D, D, false>;
     typename GP::Acc pa;
     GP::zero(pa);
     mmul<D, D, C, false, true, true>(pa, slot(0), LD, slot(9), LD);  // W^T (A W)
-    const size_t base = ((size_t)bh * p.N + n) * D * D;
     const int m0 = GP::m0(), n0 = GP::n0();
 #pragma unroll
     for (int i = 0; i < GP::TM; ++i)
