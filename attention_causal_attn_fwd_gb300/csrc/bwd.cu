@@ -770,6 +770,39 @@ __device__ __forceinline__ void frag_pairs(const typename WT<M, N>::Acc& acc, F 
             for (int h = 0; h < 2; ++h) f(W::row(mt, 2 * h), W::col(nt, 0), acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]);
 }
 
+// dst[r ld + col] = f(r, col, v) over the lane's elements (dst[col ld + r] when TR)
+template <int M, int N, bool TR = false, typename F>
+__device__ __forceinline__ void frag_store(float* dst, int ld, const typename WT<M, N>::Acc& acc, F f) {
+    frag_pairs<M, N>(acc, [&](int r, int cc, float v0, float v1) {
+        const float x0 = f(r, cc, v0), x1 = f(r, cc + 1, v1);
+        if constexpr (TR) {
+            dst[cc * ld + r] = x0;
+            dst[(cc + 1) * ld + r] = x1;
+        } else {
+            *reinterpret_cast<float2*>(dst + r * ld + cc) = make_float2(x0, x1);
+        }
+    });
+}
+template <int M, int N, bool TR = false>
+__device__ __forceinline__ void frag_store(float* dst, int ld, const typename WT<M, N>::Acc& acc) {
+    frag_store<M, N, TR>(dst, ld, acc, [](int, int, float x) { return x; });
+}
+// rows r < c of a C x D result to global bf16: dst[r][e] = acc + (add ? add[r][e] : 0)
+template <int D>
+__device__ __forceinline__ void frag_out(__nv_bfloat16* dst, const typename WT<kC, D>::Acc& acc, const float* add,
+                                         int c) {
+    frag_pairs<kC, D>(acc, [&](int r, int cc, float v0, float v1) {
+        if (r >= c) return;
+        const size_t o = (size_t)r * D + cc;
+        if (add) {
+            const float2 a = *reinterpret_cast<const float2*>(add + o);
+            v0 += a.x;
+            v1 += a.y;
+        }
+        *reinterpret_cast<__nv_bfloat162*>(dst + o) = __floats2bfloat162_rn(v0, v1);
+    });
+}
+
 // One doubling merge of the triangular inverse: for each pair of S-row blocks on the diagonal,
 // X_12 = -X_11 (D G_12) X_22, written over the X_12 block.  Every thread owns PER elements of
 // the pairs' X_12 blocks and sums them side by side over whole blocks (the zeros of the
@@ -1093,6 +1126,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     constexpr int C = kC, LC = C + 4, LD = D + 4, U = BwdSmem<D>::slot;
     constexpr int KH = D < 64 ? D : 64, NH = D / KH;  // d x C operands in pieces of KH rows
+    constexpr bool TC = sizeof(T) == 2 && D >= 64;  // bf16 operands: most products on the tensor cores
     static_assert(C == 64 && (C * 8) % kNTL == 0 && C * 32 / (2 * kNTL) <= 4, "inverse merges: whole elements per thread");
     static_assert(C * LD <= 2 * U && D * LC <= 2 * U && D * LD <= 4 * U && KH * LC <= U, "slot sizes");
     extern __shared__ __align__(16) float smem[];
@@ -1129,7 +1163,12 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     for (int idx = threadIdx.x; idx < U; idx += kNTL) slot(7)[idx] = 0.f;
     to_smem_t<T, D, kNTL>(slot(0), LC, w, D, C, c);  // W^T [D][LC] in slots 0-1 (until the dY phase)
     __syncthreads();
-    {  // G = W W^T -> slot 6 (until dM)
+    if constexpr (TC) {  // G = W W^T -> slot 6 (until dM)
+        typename WT<C, C>::Acc g;
+        WT<C, C>::zero(g);
+        mma_mul<C, C, D, true, true, false, false>(g, slot(0), LC, slot(0), LC);
+        frag_store<C, C>(slot(6), LC, g);
+    } else {
         typename GN::Acc g;
         GN::zero(g);
         mmul<C, C, D, false, true, true>(g, slot(0), LC, slot(0), LC);
@@ -1144,27 +1183,42 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
         to_smem_v<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5
         __syncthreads();
-        typename GR::Acc r;
-        GR::zero(r);
-        mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);  // R1 = W dP
-        __syncthreads();
-        mstore<C, D, false, false>(slot(2), LD, r, id);  // R1 [C][LD], slots 2-3
-        mstore<C, D, false, true>(slot(4), LC, r, id);   // R1^T [D][LC], slots 4-5
+        // R = W dP (then W dP^T), dP split into hi + lo on the tensor cores
+        auto w_times = [&](bool transposed_too) {
+            if constexpr (TC) {
+                typename WT<C, D>::Acc r;
+                WT<C, D>::zero(r);
+                mma_mul<C, D, D, true, true, false, true>(r, slot(0), LC, slot(2), LD);
+                __syncthreads();
+                frag_store<C, D>(slot(2), LD, r);                           // R [C][LD], slots 2-3
+                if (transposed_too) frag_store<C, D, true>(slot(4), LC, r);  // R^T [D][LC], slots 4-5
+            } else {
+                typename GR::Acc r;
+                GR::zero(r);
+                mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);
+                __syncthreads();
+                mstore<C, D, false, false>(slot(2), LD, r, id);
+                if (transposed_too) mstore<C, D, false, true>(slot(4), LC, r, id);
+            }
+        };
+        w_times(true);  // R1 = W dP
         __syncthreads();
         mmul<C, D, C, false, true, true, true, 2>(aW, slot(8), LC, slot(2), LD);  // -= A^T R1
-        {
+        if constexpr (TC) {  // E = R1 W^T
+            typename WT<C, C>::Acc e;
+            WT<C, C>::zero(e);
+            mma_mul<C, C, D, true, true, true, false>(e, slot(4), LC, slot(0), LC);
+            frag_store<C, C>(slot(9), LC, e);
+        } else {
             typename GN::Acc e;
             GN::zero(e);
-            mmul<C, C, D, false, true, true>(e, slot(4), LC, slot(0), LC);  // E = R1 W^T
+            mmul<C, C, D, false, true, true>(e, slot(4), LC, slot(0), LC);
             mstore<C, C, false, false>(slot(9), LC, e, id);
         }
         __syncthreads();
         to_smem_t<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP^T [D][LD], slots 2-5
         __syncthreads();
-        GR::zero(r);
-        mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);  // R2 = W dP^T
-        __syncthreads();
-        mstore<C, D, false, false>(slot(2), LD, r, id);
+        w_times(false);  // R2 = W dP^T
         __syncthreads();
         mmul<C, D, C, false, false, true, true, 1>(aW, slot(8), LC, slot(2), LD);  // -= A R2
     }
@@ -1172,9 +1226,21 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
     to_smem_t<T, D, kNTL>(slot(4), LC, k, D, C, c);  // K^T, slots 4-5
     __syncthreads();
-    typename GS::Acc aS;  // Q K^T - Y Km^T, then the probabilities
+    typename GS::Acc aS;        // Q K^T - Y Km^T, then the probabilities (CUDA cores)
+    typename WT<C, C>::Acc sT;  // Q K^T, then the probabilities (tensor cores)
     GS::zero(aS);
-    {
+    WT<C, C>::zero(sT);
+    if constexpr (TC) {
+        typename WT<C, C>::Acc qw, kw;
+        WT<C, C>::zero(qw);
+        WT<C, C>::zero(kw);
+        mma_mul<C, C, D, true, true, false, false>(qw, slot(2), LC, slot(0), LC);
+        mma_mul<C, C, D, true, true, false, false>(kw, slot(4), LC, slot(0), LC);
+        mma_mul<C, C, D, true, true, false, false>(sT, slot(2), LC, slot(4), LC);
+        __syncthreads();
+        frag_store<C, C, true>(slot(10), LC, qw, [](int i, int bb, float x) { return bb <= i ? x : 0.f; });  // Qm^T (until dA)
+        frag_store<C, C>(slot(11), LC, kw, [](int j, int a, float x) { return a > j ? x : 0.f; });          // Km (until dA)
+    } else {
         typename GS::Acc qw, kw;
         GS::zero(qw);
         GS::zero(kw);
@@ -1199,68 +1265,147 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     __syncthreads();
     to_smem_t<T, D, kNTL>(slot(0), LC, dO, D, C, c);                                   // dO^T, slots 0-1
     to_smem_t<T, D, kNTL>(slot(4), LC, static_cast<const T*>(p.v) + hrow * D, D, C, c);  // V^T, slots 4-5
-    mmul<C, C, C, true, true, false, true>(aS, slot(12), LC, slot(11), LC);  // -= Y Km^T
-    __syncthreads();
-    {
-        typename GS::Acc dp;
-        GS::zero(dp);
-        mmul<C, C, D, true, true, true>(dp, slot(0), LC, slot(4), LC);  // dO V^T
-        const int m0 = GS::m0(), n0 = GS::n0();
-        float cs[GS::TN];
-#pragma unroll
-        for (int j = 0; j < GS::TN; ++j) cs[j] = 0.f;
-#pragma unroll
-        for (int i = 0; i < GS::TM; ++i) {
-            const int r = m0 + i;
-            float rs = 0.f;
-#pragma unroll
-            for (int j = 0; j < GS::TN; ++j) {
-                const int col = n0 + j;
-                float pij = 0.f, ds = 0.f;
-                if (r < c && col <= r) {
-                    pij = __expf(scale * aS[i][j] + sC[r] - sC[col] - sL[r]);
-                    ds = pij * (dp[i][j] - sDl[r]);
-                }
-                aS[i][j] = pij;
-                dp[i][j] = scale * ds;
-                rs += ds;
-                cs[j] += ds;
-            }
-            if (p.fox) atomicAdd(aC + r, rs);
+    if constexpr (TC) {
+        {
+            typename GS::Acc ykm;
+            GS::zero(ykm);
+            mmul<C, C, C, true, true, false>(ykm, slot(12), LC, slot(11), LC);  // Y Km^T -> slot 3 (until P)
+            mstore<C, C, true, false>(slot(3), LC, ykm, id);
         }
-        if (p.fox)
-#pragma unroll
-            for (int j = 0; j < GS::TN; ++j) atomicAdd(aC + n0 + j, -cs[j]);
         __syncthreads();
-        mstore<C, C, true, false>(slot(3), LC, aS, id);  // P -> slot 3 (until dV)
-        mstore<C, C, true, false>(slot(0), LC, dp, id);  // dSs -> slot 0 (until the end)
+        using WC = WT<C, C>;
+        typename WC::Acc dp;
+        WC::zero(dp);
+        mma_mul<C, C, D, true, true, false, false>(dp, slot(0), LC, slot(4), LC);  // dO V^T
+        const float* sY = slot(3);
+        float rs[WC::MT][2], cs[WC::NT][2];
+#pragma unroll
+        for (int mt = 0; mt < WC::MT; ++mt) rs[mt][0] = rs[mt][1] = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < WC::NT; ++nt) cs[nt][0] = cs[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < WC::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < WC::NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = WC::row(mt, i), col = WC::col(nt, i);
+                    float pij = 0.f, ds = 0.f;
+                    if (r < c && col <= r) {
+                        pij = __expf(scale * (sT[mt][nt][i] - sY[r * LC + col]) + sC[r] - sC[col] - sL[r]);
+                        ds = pij * (dp[mt][nt][i] - sDl[r]);
+                    }
+                    sT[mt][nt][i] = pij;
+                    dp[mt][nt][i] = scale * ds;
+                    rs[mt][i >> 1] += ds;
+                    cs[nt][i & 1] += ds;
+                }
+        if (p.fox) {
+#pragma unroll
+            for (int mt = 0; mt < WC::MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) atomicAdd(aC + WC::row(mt, 2 * h), rs[mt][h]);
+#pragma unroll
+            for (int nt = 0; nt < WC::NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) atomicAdd(aC + WC::col(nt, e), -cs[nt][e]);
+        }
+        __syncthreads();
+        frag_store<C, C>(slot(3), LC, sT);  // P -> slot 3 (until dV)
+        frag_store<C, C>(slot(0), LC, dp);  // dSs -> slot 0 (until the end)
+    } else {
+    mmul<C, C, C, true, true, false, true>(aS, slot(12), LC, slot(11), LC);  // -= Y Km^T
+        __syncthreads();
+        {
+            typename GS::Acc dp;
+            GS::zero(dp);
+            mmul<C, C, D, true, true, true>(dp, slot(0), LC, slot(4), LC);  // dO V^T
+            const int m0 = GS::m0(), n0 = GS::n0();
+            float cs[GS::TN];
+#pragma unroll
+            for (int j = 0; j < GS::TN; ++j) cs[j] = 0.f;
+#pragma unroll
+            for (int i = 0; i < GS::TM; ++i) {
+                const int r = m0 + i;
+                float rs = 0.f;
+#pragma unroll
+                for (int j = 0; j < GS::TN; ++j) {
+                    const int col = n0 + j;
+                    float pij = 0.f, ds = 0.f;
+                    if (r < c && col <= r) {
+                        pij = __expf(scale * aS[i][j] + sC[r] - sC[col] - sL[r]);
+                        ds = pij * (dp[i][j] - sDl[r]);
+                    }
+                    aS[i][j] = pij;
+                    dp[i][j] = scale * ds;
+                    rs += ds;
+                    cs[j] += ds;
+                }
+                if (p.fox) atomicAdd(aC + r, rs);
+            }
+            if (p.fox)
+#pragma unroll
+                for (int j = 0; j < GS::TN; ++j) atomicAdd(aC + n0 + j, -cs[j]);
+            __syncthreads();
+            mstore<C, C, true, false>(slot(3), LC, aS, id);  // P -> slot 3 (until dV)
+            mstore<C, C, true, false>(slot(0), LC, dp, id);  // dSs -> slot 0 (until the end)
+        }
     }
     to_smem_v<T, D, kNTL>(slot(4), LD, dO, D, C, c);  // dO [C][LD], slots 4-5
     __syncthreads();
-    {  // dV = P^T dO (+ the off-diagonal part from the per-key-chunk sums)
+    if constexpr (TC) {  // dV = P^T dO (+ the off-diagonal part from the per-key-chunk sums), P split
+        typename WT<C, D>::Acc dv;
+        WT<C, D>::zero(dv);
+        mma_mul<C, D, C, true, true, true, false, 1>(dv, slot(3), LC, slot(4), LD);
+        frag_out<D>(reinterpret_cast<__nv_bfloat16*>(p.dv) + hrow * D, dv, above ? p.dvoff + prow * D : nullptr, c);
+    } else {
         typename GR::Acc dv;
         GR::zero(dv);
         mmul<C, D, C, false, true, true, false, 1>(dv, slot(3), LC, slot(4), LD);
         mstore_out<D>(static_cast<T*>(p.dv) + hrow * D, dv, above ? p.dvoff + prow * D : nullptr, c);
     }
     __syncthreads();
-    {  // dZ = -dKhat W^T, dY = -dQbar W^T - dSs Km
-        typename GN::Acc dz, dy;
-        GN::zero(dz);
-        GN::zero(dy);
+    if constexpr (TC) {  // dZ = -dKhat W^T and -dQbar W^T on the tensor cores, then dY = -dQbar W^T - dSs Km
+        typename WT<C, C>::Acc dz, dy;
+        WT<C, C>::zero(dz);
+        WT<C, C>::zero(dy);
 #pragma unroll 1
         for (int h = 0; h < NH; ++h) {
             to_smem_t<T, KH, kNTL>(slot(1), LC, w + h * KH, D, C, c);
             if (above) to_smem_t<float, KH, kNTL>(slot(3), LC, p.dkhat + prow * D + h * KH, D, C, C);
             if (below) to_smem_t<float, KH, kNTL>(slot(4), LC, p.dqbar + prow * D + h * KH, D, C, c);
             __syncthreads();
-            if (above) mmul<C, C, KH, false, true, true>(dz, slot(3), LC, slot(1), LC);
-            if (below) mmul<C, C, KH, false, true, true>(dy, slot(4), LC, slot(1), LC);
+            if (above) mma_mul<C, C, KH, true, true, true, false>(dz, slot(3), LC, slot(1), LC);
+            if (below) mma_mul<C, C, KH, true, true, true, false>(dy, slot(4), LC, slot(1), LC);
             __syncthreads();
         }
-        mmul<C, C, C, false, false, true, false, 2>(dy, slot(0), LC, slot(11), LC);
-        mstore<C, C, false, true>(slot(1), LC, dz, [](int, int, float x) { return -x; });   // dZ^T -> slot 1 (until dA)
-        mstore<C, C, false, false>(slot(3), LC, dy, [](int, int, float x) { return -x; });  // dY -> slot 3 (until dA)
+        auto neg = [](int, int, float x) { return -x; };
+        frag_store<C, C, true>(slot(1), LC, dz, neg);  // dZ^T -> slot 1 (until dA)
+        frag_store<C, C>(slot(3), LC, dy, neg);        // -dQbar W^T -> slot 3
+        __syncthreads();
+        typename GN::Acc d2;
+        GN::zero(d2);
+        mmul<C, C, C, false, false, true, false, 2>(d2, slot(0), LC, slot(11), LC);  // dSs Km
+        mstore<C, C, false, false>(slot(3), LC, d2, [&](int r, int cc, float x) { return slot(3)[r * LC + cc] - x; });  // dY (until dA)
+    } else {
+    {  // dZ = -dKhat W^T, dY = -dQbar W^T - dSs Km
+            typename GN::Acc dz, dy;
+            GN::zero(dz);
+            GN::zero(dy);
+#pragma unroll 1
+            for (int h = 0; h < NH; ++h) {
+                to_smem_t<T, KH, kNTL>(slot(1), LC, w + h * KH, D, C, c);
+                if (above) to_smem_t<float, KH, kNTL>(slot(3), LC, p.dkhat + prow * D + h * KH, D, C, C);
+                if (below) to_smem_t<float, KH, kNTL>(slot(4), LC, p.dqbar + prow * D + h * KH, D, C, c);
+                __syncthreads();
+                if (above) mmul<C, C, KH, false, true, true>(dz, slot(3), LC, slot(1), LC);
+                if (below) mmul<C, C, KH, false, true, true>(dy, slot(4), LC, slot(1), LC);
+                __syncthreads();
+            }
+            mmul<C, C, C, false, false, true, false, 2>(dy, slot(0), LC, slot(11), LC);
+            mstore<C, C, false, true>(slot(1), LC, dz, [](int, int, float x) { return -x; });   // dZ^T -> slot 1 (until dA)
+            mstore<C, C, false, false>(slot(3), LC, dy, [](int, int, float x) { return -x; });  // dY -> slot 3 (until dA)
+        }
     }
     __syncthreads();
     {
@@ -1335,22 +1480,45 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     to_smem_v<T, D, kNTL>(slot(6), LD, q, D, C, c);
     to_smem_v<T, D, kNTL>(slot(8), LD, k, D, C, c);
     __syncthreads();
+    if constexpr (TC) {  // the products with q, k and w on the tensor cores (their partners split)
+        using WR = WT<C, D>;
+        typename WR::Acc wq, aQ, aK;  // the tensor-core part of dW, and dQ, dK
+        WR::zero(wq);
+        WR::zero(aQ);
+        WR::zero(aK);
+        mma_mul<C, D, C, true, true, true, false, 1>(wq, slot(5), LC, slot(6), LD);   // dQw^T Q
+        mma_mul<C, D, C, true, true, true, false, 2>(wq, slot(4), LC, slot(8), LD);   // dKw^T K
+        mma_mul<C, D, C, false, true, true, false, 2>(aQ, slot(0), LC, slot(8), LD);  // dSs K
+        mma_mul<C, D, C, true, true, true, false, 1>(aK, slot(0), LC, slot(6), LD);   // dSs^T Q
+        __syncthreads();
+        to_smem_v<T, D, kNTL>(slot(6), LD, w, D, C, c);
+        __syncthreads();
+        mma_mul<C, D, C, true, true, true, false>(wq, slot(10), LC, slot(6), LD);      // (dG + dG^T) W
+        mma_mul<C, D, C, false, true, true, false, 2>(aQ, slot(5), LC, slot(6), LD);  // dQw W
+        mma_mul<C, D, C, false, true, true, false, 1>(aK, slot(4), LC, slot(6), LD);  // dKw W
+        frag_out<D>(reinterpret_cast<__nv_bfloat16*>(p.dq) + hrow * D, aQ, below ? p.dqbar + prow * D : nullptr, c);
+        frag_out<D>(reinterpret_cast<__nv_bfloat16*>(p.dk) + hrow * D, aK, above ? p.dkhat + prow * D : nullptr, c);
+        frag_store<C, D>(slot(8), D, wq);  // dense [C][D] over slots 8-9 (k is no longer read)
+        __syncthreads();
+        mstore_out<D>(static_cast<T*>(p.dw) + hrow * D, aW, slot(8), c);
+    } else {
     typename GR::Acc aQ, aK;
-    GR::zero(aQ);
-    GR::zero(aK);
-    mmul<C, D, C, false, true, true, false, 1>(aW, slot(5), LC, slot(6), LD);   // += dQw^T Q
-    mmul<C, D, C, false, true, true, false, 2>(aW, slot(4), LC, slot(8), LD);   // += dKw^T K
-    mmul<C, D, C, false, false, true, false, 2>(aQ, slot(0), LC, slot(8), LD);  // dSs K
-    mmul<C, D, C, false, true, true, false, 1>(aK, slot(0), LC, slot(6), LD);   // dSs^T Q
-    __syncthreads();
-    to_smem_v<T, D, kNTL>(slot(6), LD, w, D, C, c);
-    __syncthreads();
-    mmul<C, D, C, false, true, true>(aW, slot(10), LC, slot(6), LD);   // += (dG + dG^T) W
-    mmul<C, D, C, false, false, true, false, 2>(aQ, slot(5), LC, slot(6), LD);  // += dQw W
-    mmul<C, D, C, false, false, true, false, 1>(aK, slot(4), LC, slot(6), LD);  // += dKw W
-    mstore_out<D>(static_cast<T*>(p.dq) + hrow * D, aQ, below ? p.dqbar + prow * D : nullptr, c);
-    mstore_out<D>(static_cast<T*>(p.dk) + hrow * D, aK, above ? p.dkhat + prow * D : nullptr, c);
-    mstore_out<D>(static_cast<T*>(p.dw) + hrow * D, aW, nullptr, c);
+        GR::zero(aQ);
+        GR::zero(aK);
+        mmul<C, D, C, false, true, true, false, 1>(aW, slot(5), LC, slot(6), LD);   // += dQw^T Q
+        mmul<C, D, C, false, true, true, false, 2>(aW, slot(4), LC, slot(8), LD);   // += dKw^T K
+        mmul<C, D, C, false, false, true, false, 2>(aQ, slot(0), LC, slot(8), LD);  // dSs K
+        mmul<C, D, C, false, true, true, false, 1>(aK, slot(0), LC, slot(6), LD);   // dSs^T Q
+        __syncthreads();
+        to_smem_v<T, D, kNTL>(slot(6), LD, w, D, C, c);
+        __syncthreads();
+        mmul<C, D, C, false, true, true>(aW, slot(10), LC, slot(6), LD);   // += (dG + dG^T) W
+        mmul<C, D, C, false, false, true, false, 2>(aQ, slot(5), LC, slot(6), LD);  // += dQw W
+        mmul<C, D, C, false, false, true, false, 1>(aK, slot(4), LC, slot(6), LD);  // += dKw W
+        mstore_out<D>(static_cast<T*>(p.dq) + hrow * D, aQ, below ? p.dqbar + prow * D : nullptr, c);
+        mstore_out<D>(static_cast<T*>(p.dk) + hrow * D, aK, above ? p.dkhat + prow * D : nullptr, c);
+        mstore_out<D>(static_cast<T*>(p.dw) + hrow * D, aW, nullptr, c);
+    }
     __syncthreads();
     for (int r = threadIdx.x; r < c; r += kNTL) {
         p.dbeta[hrow + r] = aB[r];
