@@ -698,9 +698,10 @@ template <int M, int N> struct WT {
 
 // acc += sum_k a(m, k) b(k, n) over the warp's tiles, operands fp32 in shared memory with the
 // layouts of mmul (AK: a(m, k) = A[k lda + m], else A[m lda + k]; BK: b(k, n) = B[k ldb + n],
-// else B[n ldb + k]).  ASPL / BSPL split that operand into hi + lo.  KR as in mmul, per warp.
-// With leading dims of 4 mod 32 floats the K-major fragment reads are free of bank conflicts.
-template <int M, int N, int K, bool AK, bool BK, bool ASPL, bool BSPL, int KR = 0>
+// else B[n ldb + k]).  ASPL / BSPL split that operand into hi + lo (both: three products, the
+// lo x lo term dropped).  NEG subtracts the product.  KR as in mmul, per warp.  With leading dims
+// of 4 mod 32 floats the K-major fragment reads are free of bank conflicts.
+template <int M, int N, int K, bool AK, bool BK, bool ASPL, bool BSPL, int KR = 0, bool NEG = false>
 __device__ __forceinline__ void mma_mul(typename WT<M, N>::Acc& acc, const float* A, int lda, const float* B,
                                         int ldb) {
     using W = WT<M, N>;
@@ -729,6 +730,10 @@ __device__ __forceinline__ void mma_mul(typename WT<M, N>::Acc& acc, const float
                 }
                 if constexpr (ASPL) split_bf16(x0, x1, ah[mt][r], al[mt][r]);
                 else ah[mt][r] = pack_bf16(x0, x1);
+                if constexpr (NEG) {  // flip the sign bits of both halves
+                    ah[mt][r] ^= 0x80008000u;
+                    if constexpr (ASPL) al[mt][r] ^= 0x80008000u;
+                }
             }
 #pragma unroll
         for (int nt = 0; nt < W::NT; ++nt)
@@ -1177,8 +1182,11 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     __syncthreads();
     ut_inverse<C, LC>(slot(6), slot(7), slot(8), sB);  // X -> slot 7 (until dM), A = X D -> slot 8 (until dQm)
     __syncthreads();
-    typename GR::Acc aW;  // dW, accumulated across the phases
+    typename GR::Acc aW;  // dW, accumulated across the phases (CUDA cores)
+    using WD = WT<C, TC ? D : 64>;  // (a valid, unused shape off the tensor-core path)
+    typename WD::Acc aWf;             // dW (tensor cores)
     GR::zero(aW);
+    WD::zero(aWf);
     if (hasP) {  // the chunk transition: dW -= A^T (W dP) + A (W dP^T), E = W dP W^T -> slot 9 (until dA)
         const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
         to_smem_v<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5
@@ -1203,7 +1211,8 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         };
         w_times(true);  // R1 = W dP
         __syncthreads();
-        mmul<C, D, C, false, true, true, true, 2>(aW, slot(8), LC, slot(2), LD);  // -= A^T R1
+        if constexpr (TC) mma_mul<C, D, C, true, true, true, true, 2, true>(aWf, slot(8), LC, slot(2), LD);  // -= A^T R1
+        else mmul<C, D, C, false, true, true, true, 2>(aW, slot(8), LC, slot(2), LD);
         if constexpr (TC) {  // E = R1 W^T
             typename WT<C, C>::Acc e;
             WT<C, C>::zero(e);
@@ -1220,7 +1229,8 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         __syncthreads();
         w_times(false);  // R2 = W dP^T
         __syncthreads();
-        mmul<C, D, C, false, false, true, true, 1>(aW, slot(8), LC, slot(2), LD);  // -= A R2
+        if constexpr (TC) mma_mul<C, D, C, false, true, true, true, 1, true>(aWf, slot(8), LC, slot(2), LD);  // -= A R2
+        else mmul<C, D, C, false, false, true, true, 1>(aW, slot(8), LC, slot(2), LD);
     }
     __syncthreads();
     to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
@@ -1252,7 +1262,15 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         mstore<C, C, true, false>(slot(11), LC, kw, [](int j, int a, float x) { return a > j ? x : 0.f; });    // Km (until dA)
     }
     __syncthreads();
-    {
+    if constexpr (TC) {  // fp32 operands: three products each
+        typename WT<C, C>::Acc y, z;
+        WT<C, C>::zero(y);
+        WT<C, C>::zero(z);
+        mma_mul<C, C, C, true, false, true, true, 2>(y, slot(10), LC, slot(8), LC);  // Y = Qm A^T
+        mma_mul<C, C, C, false, true, true, true, 1>(z, slot(11), LC, slot(8), LC);  // Z = Km A
+        frag_store<C, C, true>(slot(12), LC, y);  // Y^T -> slot 12 (until the end)
+        frag_store<C, C>(slot(2), LC, z);         // -> slot 2 (until the end)
+    } else {
         typename GS::Acc y;
         GS::zero(y);
         mmul<C, C, C, true, true, false>(y, slot(10), LC, slot(8), LC);  // Y = Qm A^T
@@ -1266,18 +1284,12 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     to_smem_t<T, D, kNTL>(slot(0), LC, dO, D, C, c);                                   // dO^T, slots 0-1
     to_smem_t<T, D, kNTL>(slot(4), LC, static_cast<const T*>(p.v) + hrow * D, D, C, c);  // V^T, slots 4-5
     if constexpr (TC) {
-        {
-            typename GS::Acc ykm;
-            GS::zero(ykm);
-            mmul<C, C, C, true, true, false>(ykm, slot(12), LC, slot(11), LC);  // Y Km^T -> slot 3 (until P)
-            mstore<C, C, true, false>(slot(3), LC, ykm, id);
-        }
+        mma_mul<C, C, C, true, false, true, true, 2, true>(sT, slot(12), LC, slot(11), LC);  // -= Y Km^T
         __syncthreads();
         using WC = WT<C, C>;
         typename WC::Acc dp;
         WC::zero(dp);
         mma_mul<C, C, D, true, true, false, false>(dp, slot(0), LC, slot(4), LC);  // dO V^T
-        const float* sY = slot(3);
         float rs[WC::MT][2], cs[WC::NT][2];
 #pragma unroll
         for (int mt = 0; mt < WC::MT; ++mt) rs[mt][0] = rs[mt][1] = 0.f;
@@ -1292,7 +1304,7 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
                     const int r = WC::row(mt, i), col = WC::col(nt, i);
                     float pij = 0.f, ds = 0.f;
                     if (r < c && col <= r) {
-                        pij = __expf(scale * (sT[mt][nt][i] - sY[r * LC + col]) + sC[r] - sC[col] - sL[r]);
+                        pij = __expf(scale * sT[mt][nt][i] + sC[r] - sC[col] - sL[r]);
                         ds = pij * (dp[mt][nt][i] - sDl[r]);
                     }
                     sT[mt][nt][i] = pij;
@@ -1314,7 +1326,7 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         frag_store<C, C>(slot(3), LC, sT);  // P -> slot 3 (until dV)
         frag_store<C, C>(slot(0), LC, dp);  // dSs -> slot 0 (until the end)
     } else {
-    mmul<C, C, C, true, true, false, true>(aS, slot(12), LC, slot(11), LC);  // -= Y Km^T
+        mmul<C, C, C, true, true, false, true>(aS, slot(12), LC, slot(11), LC);  // -= Y Km^T
         __syncthreads();
         {
             typename GS::Acc dp;
@@ -1379,16 +1391,12 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
             if (below) mma_mul<C, C, KH, true, true, true, false>(dy, slot(4), LC, slot(1), LC);
             __syncthreads();
         }
+        mma_mul<C, C, C, false, true, true, true, 2>(dy, slot(0), LC, slot(11), LC);  // + dSs Km
         auto neg = [](int, int, float x) { return -x; };
         frag_store<C, C, true>(slot(1), LC, dz, neg);  // dZ^T -> slot 1 (until dA)
-        frag_store<C, C>(slot(3), LC, dy, neg);        // -dQbar W^T -> slot 3
-        __syncthreads();
-        typename GN::Acc d2;
-        GN::zero(d2);
-        mmul<C, C, C, false, false, true, false, 2>(d2, slot(0), LC, slot(11), LC);  // dSs Km
-        mstore<C, C, false, false>(slot(3), LC, d2, [&](int r, int cc, float x) { return slot(3)[r * LC + cc] - x; });  // dY (until dA)
+        frag_store<C, C>(slot(3), LC, dy, neg);        // dY -> slot 3 (until dA)
     } else {
-    {  // dZ = -dKhat W^T, dY = -dQbar W^T - dSs Km
+        {  // dZ = -dKhat W^T, dY = -dQbar W^T - dSs Km
             typename GN::Acc dz, dy;
             GN::zero(dz);
             GN::zero(dy);
@@ -1408,7 +1416,16 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         }
     }
     __syncthreads();
-    {
+    if constexpr (TC) {
+        typename WT<C, C>::Acc dk, dq;
+        WT<C, C>::zero(dk);
+        WT<C, C>::zero(dq);
+        mma_mul<C, C, C, true, false, true, true, 1, true>(dk, slot(0), LC, slot(12), LC);  // -dSs^T Y
+        mma_mul<C, C, C, true, false, true, true>(dk, slot(1), LC, slot(8), LC);           // + dZ A^T
+        mma_mul<C, C, C, false, true, true, true>(dq, slot(3), LC, slot(8), LC);           // dY A
+        frag_store<C, C>(slot(4), LC, dk, [](int j, int a, float x) { return a > j ? x : 0.f; });   // dKw -> slot 4
+        frag_store<C, C>(slot(5), LC, dq, [](int i, int bb, float x) { return bb <= i ? x : 0.f; });  // dQw -> slot 5
+    } else {
         typename GS::Acc dk;
         GS::zero(dk);
         mmul<C, C, C, true, true, false, true>(dk, slot(0), LC, slot(12), LC);  // -dSs^T Y
@@ -1420,7 +1437,32 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         mstore<C, C, false, false>(slot(5), LC, dq, [](int i, int bb, float x) { return bb <= i ? x : 0.f; });  // dQw -> slot 5
     }
     __syncthreads();
-    {  // dA = Km^T dZ + dY^T Qm - E;  dbeta from A = X D;  dX = dA D -> dX^T in slot 8
+    if constexpr (TC) {  // dA = Km^T dZ + dY^T Qm - E;  dbeta from A = X D;  dX = dA D -> dX^T in slot 8
+        using WC = WT<C, C>;
+        typename WC::Acc da;
+        WC::zero(da);
+        mma_mul<C, C, C, true, false, true, true, 2>(da, slot(11), LC, slot(1), LC);
+        mma_mul<C, C, C, true, false, true, true>(da, slot(3), LC, slot(10), LC);
+        const float* sX = slot(7);
+        float cs[WC::NT][2];
+#pragma unroll
+        for (int nt = 0; nt < WC::NT; ++nt) cs[nt][0] = cs[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < WC::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < WC::NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = WC::row(mt, i), col = WC::col(nt, i);
+                    if (hasP) da[mt][nt][i] -= slot(9)[r * LC + col];
+                    cs[nt][i & 1] = fmaf(sX[r * LC + col], da[mt][nt][i], cs[nt][i & 1]);
+                }
+#pragma unroll
+        for (int nt = 0; nt < WC::NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) atomicAdd(aB + WC::col(nt, e), cs[nt][e]);
+        frag_store<C, C, true>(slot(8), LC, da, [&](int, int bb, float x) { return x * sB[bb]; });
+    } else {
         typename GS::Acc da;
         GS::zero(da);
         mmul<C, C, C, true, true, false>(da, slot(11), LC, slot(1), LC);
@@ -1440,7 +1482,41 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         mstore<C, C, true, true>(slot(8), LC, da, [&](int, int bb, float x) { return x * sB[bb]; });
     }
     __syncthreads();
-    {  // dM = -X^T (dX X^T);  dG = striu(D dM) stored as dG + dG^T
+    if constexpr (TC) {  // dM = -X^T (dX X^T);  dG = striu(D dM) stored as dG + dG^T
+        using WC = WT<C, C>;
+        typename WC::Acc t1, dm;
+        WC::zero(t1);
+        WC::zero(dm);
+        mma_mul<C, C, C, true, false, true, true>(t1, slot(8), LC, slot(7), LC);
+        frag_store<C, C>(slot(9), LC, t1);
+        __syncthreads();
+        mma_mul<C, C, C, true, true, true, true, 2, true>(dm, slot(7), LC, slot(9), LC);
+        float* dG = slot(10);
+        float rsum[WC::MT][2];
+#pragma unroll
+        for (int mt = 0; mt < WC::MT; ++mt) rsum[mt][0] = rsum[mt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < WC::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < WC::NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int a = WC::row(mt, i), bb = WC::col(nt, i);
+                    const float v = dm[mt][nt][i];
+                    if (bb > a) {
+                        rsum[mt][i >> 1] = fmaf(v, slot(6)[a * LC + bb], rsum[mt][i >> 1]);
+                        const float gv = sB[a] * v;
+                        dG[a * LC + bb] = gv;
+                        dG[bb * LC + a] = gv;
+                    } else if (bb == a) {
+                        dG[a * LC + a] = 0.f;
+                    }
+                }
+#pragma unroll
+        for (int mt = 0; mt < WC::MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) atomicAdd(aB + WC::row(mt, 2 * h), rsum[mt][h]);
+    } else {
         typename GS::Acc t1;
         GS::zero(t1);
         mmul<C, C, C, true, true, false>(t1, slot(8), LC, slot(7), LC);
@@ -1474,16 +1550,21 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     if (below) to_smem_v<float, D, kNTL>(slot(6), LD, p.dqbar + prow * D, D, C, c);  // slots 6-7
     if (above) to_smem_v<float, D, kNTL>(slot(8), LD, p.dkhat + prow * D, D, C, C);  // slots 8-9
     __syncthreads();
-    if (below) mmul<C, D, C, false, false, true, true, 1>(aW, slot(12), LC, slot(6), LD);  // -= Y^T dQbar
-    if (above) mmul<C, D, C, false, true, true, true, 2>(aW, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
+    if constexpr (TC) {
+        if (below) mma_mul<C, D, C, false, true, true, true, 1, true>(aWf, slot(12), LC, slot(6), LD);  // -= Y^T dQbar
+        if (above) mma_mul<C, D, C, true, true, true, true, 2, true>(aWf, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
+    } else {
+        if (below) mmul<C, D, C, false, false, true, true, 1>(aW, slot(12), LC, slot(6), LD);  // -= Y^T dQbar
+        if (above) mmul<C, D, C, false, true, true, true, 2>(aW, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
+    }
     __syncthreads();
     to_smem_v<T, D, kNTL>(slot(6), LD, q, D, C, c);
     to_smem_v<T, D, kNTL>(slot(8), LD, k, D, C, c);
     __syncthreads();
     if constexpr (TC) {  // the products with q, k and w on the tensor cores (their partners split)
         using WR = WT<C, D>;
-        typename WR::Acc wq, aQ, aK;  // the tensor-core part of dW, and dQ, dK
-        WR::zero(wq);
+        typename WR::Acc aQ, aK;
+        auto& wq = aWf;
         WR::zero(aQ);
         WR::zero(aK);
         mma_mul<C, D, C, true, true, true, false, 1>(wq, slot(5), LC, slot(6), LD);   // dQw^T Q
@@ -1498,11 +1579,9 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         mma_mul<C, D, C, false, true, true, false, 1>(aK, slot(4), LC, slot(6), LD);  // dKw W
         frag_out<D>(reinterpret_cast<__nv_bfloat16*>(p.dq) + hrow * D, aQ, below ? p.dqbar + prow * D : nullptr, c);
         frag_out<D>(reinterpret_cast<__nv_bfloat16*>(p.dk) + hrow * D, aK, above ? p.dkhat + prow * D : nullptr, c);
-        frag_store<C, D>(slot(8), D, wq);  // dense [C][D] over slots 8-9 (k is no longer read)
-        __syncthreads();
-        mstore_out<D>(static_cast<T*>(p.dw) + hrow * D, aW, slot(8), c);
+        frag_out<D>(reinterpret_cast<__nv_bfloat16*>(p.dw) + hrow * D, wq, nullptr, c);
     } else {
-    typename GR::Acc aQ, aK;
+        typename GR::Acc aQ, aK;
         GR::zero(aQ);
         GR::zero(aK);
         mmul<C, D, C, false, true, true, false, 1>(aW, slot(5), LC, slot(6), LD);   // += dQw^T Q
