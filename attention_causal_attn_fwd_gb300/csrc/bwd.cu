@@ -995,7 +995,15 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
     ut_inverse<C, LC>(slot(6), slot(7), slot(8), sB);  // X -> slot 7, A -> slot 8
     __syncthreads();
     to_smem_v<T, D, kNTL>(slot(0), LD, w, D, C, c);  // W [C][LD], slots 0-1
-    {
+    if constexpr (TC) {  // fp32 operands: three products each
+        typename WT<C, C>::Acc y, z;
+        WT<C, C>::zero(y);
+        WT<C, C>::zero(z);
+        mma_mul<C, C, C, true, false, true, true, 2>(y, slot(2), LC, slot(8), LC);  // Y = Qm A^T
+        mma_mul<C, C, C, false, true, true, true, 1>(z, slot(4), LC, slot(8), LC);  // Z = Km A
+        frag_store<C, C, true>(slot(3), LC, y);  // Y^T
+        frag_store<C, C>(slot(5), LC, z);
+    } else {
         typename GS::Acc y;
         GS::zero(y);
         mmul<C, C, C, true, true, false>(y, slot(2), LC, slot(8), LC);  // Y = Qm A^T
