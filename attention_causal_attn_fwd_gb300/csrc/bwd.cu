@@ -792,20 +792,34 @@ template <int M, int N, bool TR = false>
 __device__ __forceinline__ void frag_store(float* dst, int ld, const typename WT<M, N>::Acc& acc) {
     frag_store<M, N, TR>(dst, ld, acc, [](int, int, float x) { return x; });
 }
-// rows r < c of a C x D result to global bf16: dst[r][e] = acc + (add ? add[r][e] : 0)
+// rows r < c of a C x D result to global bf16: dst[r][e] = acc + (add ? add[r][e] : 0); the addends
+// are all loaded before the first store
 template <int D>
 __device__ __forceinline__ void frag_out(__nv_bfloat16* dst, const typename WT<kC, D>::Acc& acc, const float* add,
                                          int c) {
-    frag_pairs<kC, D>(acc, [&](int r, int cc, float v0, float v1) {
-        if (r >= c) return;
-        const size_t o = (size_t)r * D + cc;
-        if (add) {
-            const float2 a = *reinterpret_cast<const float2*>(add + o);
-            v0 += a.x;
-            v1 += a.y;
-        }
-        *reinterpret_cast<__nv_bfloat162*>(dst + o) = __floats2bfloat162_rn(v0, v1);
-    });
+    using W = WT<kC, D>;
+    float2 a[W::MT][W::NT][2];
+#pragma unroll
+    for (int mt = 0; mt < W::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < W::NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = W::row(mt, 2 * h);
+                a[mt][nt][h] = add && r < c ? *reinterpret_cast<const float2*>(add + (size_t)r * D + W::col(nt, 0))
+                                            : make_float2(0.f, 0.f);
+            }
+#pragma unroll
+    for (int mt = 0; mt < W::MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < W::NT; ++nt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = W::row(mt, 2 * h);
+                if (r < c)
+                    *reinterpret_cast<__nv_bfloat162*>(dst + (size_t)r * D + W::col(nt, 0)) = __floats2bfloat162_rn(
+                        acc[mt][nt][2 * h] + a[mt][nt][h].x, acc[mt][nt][2 * h + 1] + a[mt][nt][h].y);
+            }
 }
 
 // One doubling merge of the triangular inverse: for each pair of S-row blocks on the diagonal,
@@ -1024,23 +1038,35 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
         float* qb = p.qbar + prow * D;
         float* kh = p.khat + prow * D;
         __nv_bfloat16* kh16 = p.khat16 ? p.khat16 + prow * D : nullptr;
-        frag_pairs<C, D>(yw, [&](int r, int cc, float v0, float v1) {
-            float2 x = make_float2(0.f, 0.f);
-            if (r < c) {
-                const float2 f = to_f2(q + (size_t)r * D + cc);
-                x = make_float2(f.x - v0, f.y - v1);
-            }
-            *reinterpret_cast<float2*>(qb + (size_t)r * D + cc) = x;
-        });
-        frag_pairs<C, D>(zw, [&](int r, int cc, float v0, float v1) {
-            float2 x = make_float2(0.f, 0.f);
-            if (r < c) {
-                const float2 f = to_f2(k + (size_t)r * D + cc);
-                x = make_float2(f.x - v0, f.y - v1);
-            }
-            *reinterpret_cast<float2*>(kh + (size_t)r * D + cc) = x;
-            if (kh16) *reinterpret_cast<__nv_bfloat162*>(kh16 + (size_t)r * D + cc) = __floats2bfloat162_rn(x.x, x.y);
-        });
+        // qbar = Q - Y W and khat = K - Z W; the q and k values are all loaded before the first store
+        float2 xq[WR::MT][WR::NT][2], xk[WR::MT][WR::NT][2];
+#pragma unroll
+        for (int mt = 0; mt < WR::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < WR::NT; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = WR::row(mt, 2 * h), cc = WR::col(nt, 0);
+                    const bool ok = r < c;
+                    xq[mt][nt][h] = ok ? to_f2(q + (size_t)r * D + cc) : make_float2(0.f, 0.f);
+                    xk[mt][nt][h] = ok ? to_f2(k + (size_t)r * D + cc) : make_float2(0.f, 0.f);
+                }
+#pragma unroll
+        for (int mt = 0; mt < WR::MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < WR::NT; ++nt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = WR::row(mt, 2 * h), cc = WR::col(nt, 0);
+                    const bool ok = r < c;  // padded rows are written as zeros
+                    const float2 a = ok ? make_float2(xq[mt][nt][h].x - yw[mt][nt][2 * h], xq[mt][nt][h].y - yw[mt][nt][2 * h + 1])
+                                        : make_float2(0.f, 0.f);
+                    const float2 b = ok ? make_float2(xk[mt][nt][h].x - zw[mt][nt][2 * h], xk[mt][nt][h].y - zw[mt][nt][2 * h + 1])
+                                        : make_float2(0.f, 0.f);
+                    *reinterpret_cast<float2*>(qb + (size_t)r * D + cc) = a;
+                    *reinterpret_cast<float2*>(kh + (size_t)r * D + cc) = b;
+                    if (kh16) *reinterpret_cast<__nv_bfloat162*>(kh16 + (size_t)r * D + cc) = __floats2bfloat162_rn(b.x, b.y);
+                }
         if (n < 1 || n > p.N - 2) return;
         typename WR::Acc aw;
         WR::zero(aw);
@@ -1199,46 +1225,48 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
         to_smem_v<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5
         __syncthreads();
-        // R = W dP (then W dP^T), dP split into hi + lo on the tensor cores
-        auto w_times = [&](bool transposed_too) {
-            if constexpr (TC) {
-                typename WT<C, D>::Acc r;
-                WT<C, D>::zero(r);
-                mma_mul<C, D, D, true, true, false, true>(r, slot(0), LC, slot(2), LD);
-                __syncthreads();
-                frag_store<C, D>(slot(2), LD, r);                           // R [C][LD], slots 2-3
-                if (transposed_too) frag_store<C, D, true>(slot(4), LC, r);  // R^T [D][LC], slots 4-5
-            } else {
-                typename GR::Acc r;
-                GR::zero(r);
-                mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);
-                __syncthreads();
-                mstore<C, D, false, false>(slot(2), LD, r, id);
-                if (transposed_too) mstore<C, D, false, true>(slot(4), LC, r, id);
-            }
-        };
-        w_times(true);  // R1 = W dP
-        __syncthreads();
-        if constexpr (TC) mma_mul<C, D, C, true, true, true, true, 2, true>(aWf, slot(8), LC, slot(2), LD);  // -= A^T R1
-        else mmul<C, D, C, false, true, true, true, 2>(aW, slot(8), LC, slot(2), LD);
-        if constexpr (TC) {  // E = R1 W^T
-            typename WT<C, C>::Acc e;
+        if constexpr (TC) {  // R1 = W dP and R2 = W dP^T from the one copy of dP (split into hi + lo)
+            typename WT<C, D>::Acc r1, r2;
+            WT<C, D>::zero(r1);
+            WT<C, D>::zero(r2);
+            mma_mul<C, D, D, true, true, false, true>(r1, slot(0), LC, slot(2), LD);
+            mma_mul<C, D, D, true, false, false, true>(r2, slot(0), LC, slot(2), LD);
+            __syncthreads();
+            frag_store<C, D>(slot(2), LD, r1);         // R1 [C][LD], slots 2-3
+            frag_store<C, D, true>(slot(4), LC, r1);   // R1^T [D][LC], slots 4-5
+            frag_store<C, D>(slot(10), LD, r2);        // R2 [C][LD], slots 10-11 (free until Qm^T and Km)
+            __syncthreads();
+            mma_mul<C, D, C, true, true, true, true, 2, true>(aWf, slot(8), LC, slot(2), LD);    // -= A^T R1
+            mma_mul<C, D, C, false, true, true, true, 1, true>(aWf, slot(8), LC, slot(10), LD);  // -= A R2
+            typename WT<C, C>::Acc e;  // E = R1 W^T
             WT<C, C>::zero(e);
             mma_mul<C, C, D, true, true, true, false>(e, slot(4), LC, slot(0), LC);
             frag_store<C, C>(slot(9), LC, e);
         } else {
-            typename GN::Acc e;
-            GN::zero(e);
-            mmul<C, C, D, false, true, true>(e, slot(4), LC, slot(0), LC);
-            mstore<C, C, false, false>(slot(9), LC, e, id);
+            typename GR::Acc r;
+            GR::zero(r);
+            mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);  // R1 = W dP
+            __syncthreads();
+            mstore<C, D, false, false>(slot(2), LD, r, id);  // R1 [C][LD], slots 2-3
+            mstore<C, D, false, true>(slot(4), LC, r, id);   // R1^T [D][LC], slots 4-5
+            __syncthreads();
+            mmul<C, D, C, false, true, true, true, 2>(aW, slot(8), LC, slot(2), LD);  // -= A^T R1
+            {
+                typename GN::Acc e;
+                GN::zero(e);
+                mmul<C, C, D, false, true, true>(e, slot(4), LC, slot(0), LC);  // E = R1 W^T
+                mstore<C, C, false, false>(slot(9), LC, e, id);
+            }
+            __syncthreads();
+            to_smem_t<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP^T [D][LD], slots 2-5
+            __syncthreads();
+            GR::zero(r);
+            mmul<C, D, D, false, true, true>(r, slot(0), LC, slot(2), LD);  // R2 = W dP^T
+            __syncthreads();
+            mstore<C, D, false, false>(slot(2), LD, r, id);
+            __syncthreads();
+            mmul<C, D, C, false, false, true, true, 1>(aW, slot(8), LC, slot(2), LD);  // -= A R2
         }
-        __syncthreads();
-        to_smem_t<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP^T [D][LD], slots 2-5
-        __syncthreads();
-        w_times(false);  // R2 = W dP^T
-        __syncthreads();
-        if constexpr (TC) mma_mul<C, D, C, false, true, true, true, 1, true>(aWf, slot(8), LC, slot(2), LD);  // -= A R2
-        else mmul<C, D, C, false, false, true, true, 1>(aW, slot(8), LC, slot(2), LD);
     }
     __syncthreads();
     to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
