@@ -563,6 +563,33 @@ __device__ __forceinline__ void mstore(float* dst, int ld, const typename TT<M, 
     }
 }
 
+// A ROWS x COLS block of a row-major global array (leading dim lds; rows >= valid read as zero),
+// held in registers between its load and a transposing store dst[c ldd + r] (the layout
+// to_smem_t writes), so that the load can be issued ahead of the phase that frees dst.
+template <typename G, int COLS, int ROWS>
+struct TileRegs {
+    static constexpr int V = 16 / sizeof(G), NV = ROWS * (COLS / V) / kNTL;
+    static_assert(COLS % V == 0 && NV * kNTL == ROWS * (COLS / V), "whole 16-byte vectors per thread");
+    uint4 x[NV];
+    __device__ __forceinline__ void load(const G* src, int lds, int valid) {
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            const int idx = threadIdx.x + e * kNTL, r = idx % ROWS, cv = idx / ROWS;
+            x[e] = r < valid ? ld_global_v4(src + (size_t)r * lds + cv * V) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    __device__ __forceinline__ void store_t(float* dst, int ldd) const {
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            const int idx = threadIdx.x + e * kNTL, r = idx % ROWS, cv = idx / ROWS;
+            Vec16<G> v;
+            v.raw = x[e];
+#pragma unroll
+            for (int j = 0; j < V; ++j) dst[(cv * V + j) * ldd + r] = v.get(j);
+        }
+    }
+};
+
 // W consecutive values of a global row as fp32 (16- or 8-byte loads; W a multiple of 4)
 template <int W, typename S>
 __device__ __forceinline__ void ld_row(float (&v)[W], const S* src) {
@@ -1201,6 +1228,8 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     }
     for (int idx = threadIdx.x; idx < U; idx += kNTL) slot(7)[idx] = 0.f;
     to_smem_t<T, D, kNTL>(slot(0), LC, w, D, C, c);  // W^T [D][LC] in slots 0-1 (until the dY phase)
+    const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
+    if (hasP) to_smem_v<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5, read after the inverse
     __syncthreads();
     if constexpr (TC) {  // G = W W^T -> slot 6 (until dM)
         typename WT<C, C>::Acc g;
@@ -1222,9 +1251,6 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     GR::zero(aW);
     WD::zero(aWf);
     if (hasP) {  // the chunk transition: dW -= A^T (W dP) + A (W dP^T), E = W dP W^T -> slot 9 (until dA)
-        const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
-        to_smem_v<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5
-        __syncthreads();
         if constexpr (TC) {  // R1 = W dP and R2 = W dP^T from the one copy of dP (split into hi + lo)
             typename WT<C, D>::Acc r1, r2;
             WT<C, D>::zero(r1);
@@ -1417,15 +1443,32 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         typename WT<C, C>::Acc dz, dy;
         WT<C, C>::zero(dz);
         WT<C, C>::zero(dy);
+        // d in pieces of KH rows; piece h + 1 is loaded into registers while piece h's products run
+        TileRegs<T, KH, C> rw;
+        TileRegs<float, KH, C> rk, rq;
+        auto fetch = [&](int h) {
+            rw.load(w + h * KH, D, c);
+            if (above) rk.load(p.dkhat + prow * D + h * KH, D, C);
+            if (below) rq.load(p.dqbar + prow * D + h * KH, D, c);
+        };
+        auto place = [&]() {
+            rw.store_t(slot(1), LC);
+            if (above) rk.store_t(slot(3), LC);
+            if (below) rq.store_t(slot(4), LC);
+        };
+        fetch(0);
+        place();
+        __syncthreads();
 #pragma unroll 1
         for (int h = 0; h < NH; ++h) {
-            to_smem_t<T, KH, kNTL>(slot(1), LC, w + h * KH, D, C, c);
-            if (above) to_smem_t<float, KH, kNTL>(slot(3), LC, p.dkhat + prow * D + h * KH, D, C, C);
-            if (below) to_smem_t<float, KH, kNTL>(slot(4), LC, p.dqbar + prow * D + h * KH, D, C, c);
-            __syncthreads();
+            if (h + 1 < NH) fetch(h + 1);
             if (above) mma_mul<C, C, KH, true, true, true, false>(dz, slot(3), LC, slot(1), LC);
             if (below) mma_mul<C, C, KH, true, true, true, false>(dy, slot(4), LC, slot(1), LC);
             __syncthreads();
+            if (h + 1 < NH) {
+                place();
+                __syncthreads();
+            }
         }
         mma_mul<C, C, C, false, true, true, true, 2>(dy, slot(0), LC, slot(11), LC);  // + dSs Km
         auto neg = [](int, int, float x) { return -x; };
