@@ -564,8 +564,9 @@ __device__ __forceinline__ void mstore(float* dst, int ld, const typename TT<M, 
 }
 
 // A ROWS x COLS block of a row-major global array (leading dim lds; rows >= valid read as zero),
-// held in registers between its load and a transposing store dst[c ldd + r] (the layout
-// to_smem_t writes), so that the load can be issued ahead of the phase that frees dst.
+// held in registers between its load and its store to shared memory, so that the load can be
+// issued ahead of the phase that frees the destination: load + store_t give the transposed
+// layout of to_smem_t, load_r + store_r the row-major one of to_smem_v.
 template <typename G, int COLS, int ROWS>
 struct TileRegs {
     static constexpr int V = 16 / sizeof(G), NV = ROWS * (COLS / V) / kNTL;
@@ -576,6 +577,25 @@ struct TileRegs {
         for (int e = 0; e < NV; ++e) {
             const int idx = threadIdx.x + e * kNTL, r = idx % ROWS, cv = idx / ROWS;
             x[e] = r < valid ? ld_global_v4(src + (size_t)r * lds + cv * V) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    // row-major store dst[r ldd + c] of a tile loaded with load_r
+    __device__ __forceinline__ void load_r(const G* src, int lds, int valid) {
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            const int idx = threadIdx.x + e * kNTL, r = idx / (COLS / V), cv = idx % (COLS / V);
+            x[e] = r < valid ? ld_global_v4(src + (size_t)r * lds + cv * V) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    __device__ __forceinline__ void store_r(float* dst, int ldd) const {
+#pragma unroll
+        for (int e = 0; e < NV; ++e) {
+            const int idx = threadIdx.x + e * kNTL, r = idx / (COLS / V), cv = idx % (COLS / V);
+            Vec16<G> v;
+            v.raw = x[e];
+            float* d = dst + r * ldd + cv * V;
+#pragma unroll
+            for (int j = 0; j < V; ++j) d[j] = v.get(j);
         }
     }
     __device__ __forceinline__ void store_t(float* dst, int ldd) const {
@@ -1250,8 +1270,12 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     typename WD::Acc aWf;             // dW (tensor cores)
     GR::zero(aW);
     WD::zero(aWf);
+    using TRg = TileRegs<T, TC ? D : 64, C>;  // (a valid, unused shape off the tensor-core path)
+    TRg pq, pk;  // q and k, loaded while the transition's products run (tensor-core path)
     if (hasP) {  // the chunk transition: dW -= A^T (W dP) + A (W dP^T), E = W dP W^T -> slot 9 (until dA)
         if constexpr (TC) {  // R1 = W dP and R2 = W dP^T from the one copy of dP (split into hi + lo)
+            pq.load(q, D, c);
+            pk.load(k, D, c);
             typename WT<C, D>::Acc r1, r2;
             WT<C, D>::zero(r1);
             WT<C, D>::zero(r2);
@@ -1295,8 +1319,13 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         }
     }
     __syncthreads();
-    to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);  // Q^T, slots 2-3
-    to_smem_t<T, D, kNTL>(slot(4), LC, k, D, C, c);  // K^T, slots 4-5
+    if (TC && hasP) {
+        pq.store_t(slot(2), LC);  // Q^T, slots 2-3
+        pk.store_t(slot(4), LC);  // K^T, slots 4-5
+    } else {
+        to_smem_t<T, D, kNTL>(slot(2), LC, q, D, C, c);
+        to_smem_t<T, D, kNTL>(slot(4), LC, k, D, C, c);
+    }
     __syncthreads();
     typename GS::Acc aS;        // Q K^T - Y Km^T, then the probabilities (CUDA cores)
     typename WT<C, C>::Acc sT;  // Q K^T, then the probabilities (tensor cores)
@@ -1630,6 +1659,8 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     if (above) to_smem_v<float, D, kNTL>(slot(8), LD, p.dkhat + prow * D, D, C, C);  // slots 8-9
     __syncthreads();
     if constexpr (TC) {
+        pq.load_r(q, D, c);  // q and k for the next phase, in flight meanwhile
+        pk.load_r(k, D, c);
         if (below) mma_mul<C, D, C, false, true, true, true, 1, true>(aWf, slot(12), LC, slot(6), LD);  // -= Y^T dQbar
         if (above) mma_mul<C, D, C, true, true, true, true, 2, true>(aWf, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
     } else {
@@ -1637,8 +1668,13 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         if (above) mmul<C, D, C, false, true, true, true, 2>(aW, slot(2), LC, slot(8), LD);    // -= Z^T dKhat
     }
     __syncthreads();
-    to_smem_v<T, D, kNTL>(slot(6), LD, q, D, C, c);
-    to_smem_v<T, D, kNTL>(slot(8), LD, k, D, C, c);
+    if constexpr (TC) {
+        pq.store_r(slot(6), LD);
+        pk.store_r(slot(8), LD);
+    } else {
+        to_smem_v<T, D, kNTL>(slot(6), LD, q, D, C, c);
+        to_smem_v<T, D, kNTL>(slot(8), LD, k, D, C, c);
+    }
     __syncthreads();
     if constexpr (TC) {  // the products with q, k and w on the tensor cores (their partners split)
         using WR = WT<C, D>;
@@ -1646,12 +1682,13 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         auto& wq = aWf;
         WR::zero(aQ);
         WR::zero(aK);
+        pq.load_r(w, D, c);  // w for the last products, in flight meanwhile
         mma_mul<C, D, C, true, true, true, false, 1>(wq, slot(5), LC, slot(6), LD);   // dQw^T Q
         mma_mul<C, D, C, true, true, true, false, 2>(wq, slot(4), LC, slot(8), LD);   // dKw^T K
         mma_mul<C, D, C, false, true, true, false, 2>(aQ, slot(0), LC, slot(8), LD);  // dSs K
         mma_mul<C, D, C, true, true, true, false, 1>(aK, slot(0), LC, slot(6), LD);   // dSs^T Q
         __syncthreads();
-        to_smem_v<T, D, kNTL>(slot(6), LD, w, D, C, c);
+        pq.store_r(slot(6), LD);
         __syncthreads();
         mma_mul<C, D, C, true, true, true, false>(wq, slot(10), LC, slot(6), LD);      // (dG + dG^T) W
         mma_mul<C, D, C, false, true, true, false, 2>(aQ, slot(5), LC, slot(6), LD);  // dQw W
