@@ -1053,9 +1053,12 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
         mstore<C, C, false, false>(slot(4), LC, kw, [](int j, int a, float x) { return a > j ? x : 0.f; });    // Km
     }
     __syncthreads();
+    TileRegs<T, TC ? D : 64, C> pw;  // W [C][LD] for slots 0-1, in flight during the inverse
+    if constexpr (TC) pw.load_r(w, D, c);
+    else to_smem_v<T, D, kNTL>(slot(0), LD, w, D, C, c);
     ut_inverse<C, LC>(slot(6), slot(7), slot(8), sB);  // X -> slot 7, A -> slot 8
+    if constexpr (TC) pw.store_r(slot(0), LD);
     __syncthreads();
-    to_smem_v<T, D, kNTL>(slot(0), LD, w, D, C, c);  // W [C][LD], slots 0-1
     if constexpr (TC) {  // fp32 operands: three products each
         typename WT<C, C>::Acc y, z;
         WT<C, C>::zero(y);
