@@ -162,12 +162,15 @@ size_t path_attn_bwd_workspace_bytes(int B, int H, int L, int d, int dtype);
  * Arithmetic: fp32 inputs run in fp32 on the CUDA cores.  bf16 inputs at d = 128
  * run the query-side chunk chains and the per-key-chunk sums on the tensor cores
  * (bf16 operands, fp32 accumulation; the carried states enter as hi + lo bf16
- * parts) and the within-chunk walks in fp32; other bf16 sizes run in fp32 on the
- * CUDA cores.  Gradients are rounded to the input dtype (nearest even) on store.
- * dbeta and dlog_f at position 0 are exactly zero (those enter no logit).
- * Repeated calls agree to rounding, not bit for bit: the within-chunk walks add
- * into shared-memory accumulators, and the PaTH-FoX column sums into global ones,
- * in an order that depends on scheduling.
+ * parts).  The within-chunk parts (qbar, khat, the chunk transitions, the
+ * diagonal block and the reverse of the within-chunk products) are products of
+ * the compact ("UT") form: for bf16 at d >= 64 on the tensor cores (fp32
+ * operands other than q, k, v, w, dO enter as hi + lo bf16 parts), otherwise in
+ * fp32 on the CUDA cores.  Gradients are rounded to the input dtype (nearest
+ * even) on store.  dbeta and dlog_f at position 0 are exactly zero (those enter
+ * no logit).  Repeated calls agree to rounding in dbeta and dlog_f, not bit for
+ * bit (their partial sums are added into shared- and global-memory accumulators
+ * in an order that depends on scheduling); dq, dk, dv and dw repeat exactly.
  * Outputs may not alias inputs.  Argument errors return before any launch.  The
  * tensor-core kernels bound every wait; an expiry sets PATH_ERR_TIMEOUT in the
  * workspace status word (read it with path_get_status), which otherwise stays

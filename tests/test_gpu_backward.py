@@ -38,10 +38,14 @@ def _dO(shape, dtype, seed):
 def _gpu_bwd(x: inputs.FwdInputs, dO: torch.Tensor):
     args = [cuda(t) for t in (x.q, x.k, x.v, x.w, x.beta)]
     lf = cuda(x.log_f)
+    # the bf16 forward runs at d = 64 and 128; below that a caller forms o and lse in fp32 from the
+    # same (bf16) values and rounds o to bf16, as done here
+    fargs = args if (x.q.dtype == torch.float32 or x.q.shape[-1] >= 64) else [a.float() for a in args[:4]] + args[4:]
     if lf is not None:
-        o, lse = P.path_attn_fwd_fox(*args, lf, scale=x.scale, lse=True)
+        o, lse = P.path_attn_fwd_fox(*fargs, lf, scale=x.scale, lse=True)
     else:
-        o, lse = P.path_attn_fwd(*args, scale=x.scale, lse=True)
+        o, lse = P.path_attn_fwd(*fargs, scale=x.scale, lse=True)
+    o = o.to(x.q.dtype)
     B, H, L, d = x.q.shape
     ws = P.alloc_workspace(P.path_attn_bwd_workspace_bytes(B, H, L, d, x.q.dtype), "cuda")
     g = P.path_attn_bwd(*args, o, lse, cuda(dO), log_f=lf, scale=x.scale, workspace=ws)
@@ -158,6 +162,15 @@ def test_bwd_bf16_d128_edge_betas(B, H, L, fox):
 def test_bwd_bf16_fox_d128_ragged():
     x = inputs.make_fwd(1, 2, 333, 128, "bf16", seed=33, fox=True)
     _case(x, 33, "bf16 fox L333")
+
+
+@pytest.mark.parametrize("B,H,L,d,fox", [(2, 1, 177, 64, True), (1, 2, 200, 32, True), (1, 2, 130, 16, False)])
+def test_bwd_bf16_small_d_ragged(B, H, L, d, fox):
+    """bf16 below d = 128 with ragged last chunks and beta = 0 / 2 positions: at d = 64 the within-chunk
+    stage and the prep run their products on the tensor cores (mma.sync), at d = 16 and 32 on the
+    CUDA cores."""
+    x = inputs.make_fwd(B, H, L, d, "bf16", seed=90 + d, beta_std=2.0, edge_frac=0.05, fox=fox)
+    _case(x, 90 + L, "bf16 B%d H%d L%d d%d fox=%s" % (B, H, L, d, fox))
 
 
 def test_bwd_760m_shaped_sampled_heads():
