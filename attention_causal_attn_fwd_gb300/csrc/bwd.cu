@@ -47,9 +47,11 @@
 //                                       (products and one triangular
 //                                       inverse); writes dq, dk, dv, dw, dbeta
 //   bwd_fox_suffix one CTA per head     dlog f_s = sum_{t >= s} dc_t
-// The contractions here are register-tiled fp32 GEMMs on K-major shared-memory operands.
-// Nothing here waits on another CTA, so these kernels have no spin waits (the
-// tensor-core kernels of csrc/bwd_tc.cu bound every wait).
+// The contractions here are register-tiled fp32 GEMMs on shared-memory operands, except
+// in bwd_prep and bwd_local for bf16 at d >= 64, where they run as warp-level mma.sync
+// (bf16 operands, fp32 accumulation; fp32 operands other than the bf16 inputs enter as
+// hi + lo parts).  Nothing here waits on another CTA, so these kernels have no spin
+// waits (the tensor-core kernels of csrc/bwd_tc.cu bound every wait).
 #include "common.cuh"
 #include "ut_prep.cuh"
 
