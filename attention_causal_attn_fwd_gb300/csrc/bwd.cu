@@ -76,7 +76,7 @@ struct BwdParams {
     const float *beta, *lse;
     void *dq, *dk, *dv, *dw;
     float *dbeta, *dlog_f;
-    float *qbar, *khat, *pm, *pmt, *delta, *cum, *dqbar, *dkhat, *dvoff, *dpm, *dcrow, *dccol, *dctot;
+    float *qbar, *khat, *pm, *pmt, *xinv, *delta, *cum, *dqbar, *dkhat, *dvoff, *dpm, *dcrow, *dccol, *dctot;
     __nv_bfloat16 *khat16, *phi, *plo;  // tensor-core chains only (else null)
     void* pairs;  // pair store, elements of the input dtype
     int L, Lp, N;
@@ -1061,6 +1061,13 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_prep(BwdParams p) {
     ut_inverse<C, LC>(slot(6), slot(7), slot(8), sB);  // X -> slot 7, A -> slot 8
     if constexpr (TC) pw.store_r(slot(0), LD);
     __syncthreads();
+    {  // X for bwd_local, which needs the same factor
+        float* xg = p.xinv + ((size_t)bh * p.N + n) * C * C;
+        for (int idx = threadIdx.x; idx < C * C / 4; idx += kNTL) {
+            const int r = idx / (C / 4), c4 = (idx % (C / 4)) * 4;
+            *reinterpret_cast<float4*>(xg + r * C + c4) = *reinterpret_cast<const float4*>(slot(7) + r * LC + c4);
+        }
+    }
     if constexpr (TC) {  // fp32 operands: three products each
         typename WT<C, C>::Acc y, z;
         WT<C, C>::zero(y);
@@ -1218,7 +1225,7 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
     constexpr int C = kC, LC = C + 4, LD = D + 4, U = BwdSmem<D>::slot;
     constexpr int KH = D < 64 ? D : 64, NH = D / KH;  // d x C operands in pieces of KH rows
     constexpr bool TC = sizeof(T) == 2 && D >= 64;  // bf16 operands: most products on the tensor cores
-    static_assert(C == 64 && (C * 8) % kNTL == 0 && C * 32 / (2 * kNTL) <= 4, "inverse merges: whole elements per thread");
+    static_assert(C == 64, "chunks of 64 positions");
     static_assert(C * LD <= 2 * U && D * LC <= 2 * U && D * LD <= 4 * U && KH * LC <= U, "slot sizes");
     extern __shared__ __align__(16) float smem[];
     auto slot = [&](int i) { return smem + i * U; };
@@ -1251,7 +1258,7 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         aB[r] = 0.f;
         aC[r] = 0.f;
     }
-    for (int idx = threadIdx.x; idx < U; idx += kNTL) slot(7)[idx] = 0.f;
+    to_smem_v<float, C, kNTL>(slot(7), LC, p.xinv + ((size_t)bh * p.N + n) * C * C, C, C, C);  // X (bwd_prep) -> slot 7 (until dM)
     to_smem_t<T, D, kNTL>(slot(0), LC, w, D, C, c);  // W^T [D][LC] in slots 0-1 (until the dY phase)
     const float* dP = p.dpm + ((size_t)bh * p.N + n) * D * D;
     if (hasP) to_smem_v<float, D, kNTL>(slot(2), LD, dP, D, D, D);  // dP [D][LD], slots 2-5, read after the inverse
@@ -1268,7 +1275,10 @@ __global__ void __launch_bounds__(kNTL, 1) bwd_local(BwdParams p) {
         mstore<C, C, false, false>(slot(6), LC, g, id);
     }
     __syncthreads();
-    ut_inverse<C, LC>(slot(6), slot(7), slot(8), sB);  // X -> slot 7 (until dM), A = X D -> slot 8 (until dQm)
+    for (int idx = threadIdx.x; idx < C * C; idx += kNTL) {  // A = X D -> slot 8 (until dQm)
+        const int r = idx / C, cc = idx % C;
+        slot(8)[r * LC + cc] = slot(7)[r * LC + cc] * sB[cc];
+    }
     __syncthreads();
     typename GR::Acc aW;  // dW, accumulated across the phases (CUDA cores)
     using WD = WT<C, TC ? D : 64>;  // (a valid, unused shape off the tensor-core path)
@@ -1822,6 +1832,7 @@ cudaError_t attn_bwd(int dtype, int d, const void* q, const void* k, const void*
     p.qbar = f(lay.qbar); p.khat = f(lay.khat);
     p.pm = lay.pm ? f(lay.pm) : nullptr;
     p.pmt = lay.pmt ? f(lay.pmt) : nullptr;
+    p.xinv = f(lay.xinv);
     p.delta = f(lay.delta); p.cum = f(lay.cum); p.dqbar = f(lay.dqbar); p.dkhat = f(lay.dkhat);
     p.dvoff = f(lay.dvoff); p.dpm = f(lay.dpm); p.dcrow = f(lay.dcrow); p.dccol = f(lay.dccol);
     p.dctot = f(lay.dctot); p.pairs = ws + lay.pairs;

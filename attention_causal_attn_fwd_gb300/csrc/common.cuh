@@ -231,7 +231,8 @@ inline DecLayout dec_layout(int B, int H, int n_max, int d) {
 //           in the input dtype (bf16 pairs feed the tensor-core reduction)
 constexpr int kBwdC = 64;
 struct BwdLayout {
-    size_t qbar, khat, pm, pmt, khat16, phi, plo, delta, cum, dqbar, dkhat, dvoff, dpm, dcrow, dccol, dctot, pairs, total;
+    size_t qbar, khat, pm, pmt, khat16, phi, plo, xinv, delta, cum, dqbar, dkhat, dvoff, dpm, dcrow, dccol, dctot, pairs,
+        total;
     int Lp, N;
     size_t pair_elems;   // elements per (n, m) pair
     size_t head_pairs;   // N (N - 1) / 2
@@ -254,6 +255,7 @@ inline BwdLayout bwd_layout(int B, int H, int L, int d, size_t elt) {
     s.khat16 = tc ? take(rows * d * 2) : 0;
     s.phi = tc ? take(BH * s.N * d * d * 2) : 0;
     s.plo = tc ? take(BH * s.N * d * d * 2) : 0;
+    s.xinv = take(BH * s.N * C * C * sizeof(float));  // each chunk's (I + D triu_1 W W^T)^-1, prep -> local
     s.delta = take(rows * sizeof(float));
     s.cum = take(rows * sizeof(float));
     s.dqbar = take(rows * d * sizeof(float));
