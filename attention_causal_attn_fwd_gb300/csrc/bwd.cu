@@ -30,7 +30,8 @@
 //   bwd_prep   one CTA per chunk        qbar, khat, Delta and, for the inner
 //                                       chunks, P_m = I - W^T A W, all in the
 //                                       compact form (fp32 P_m, or hi / lo bf16
-//                                       for the tensor-core chains)
+//                                       for the tensor-core chains); keeps the
+//                                       triangular factor for bwd_local
 //   bwd_chain  one CTA per query chunk  U chain down, G chain up; stores U,
 //                                       G, dS and P per (n, m) pair; dQbar;
 //                                       for bf16 at d = 128 bwd_chain_tc
@@ -44,8 +45,9 @@
 //                                       tensor cores from the bf16 pair store
 //   bwd_local  one CTA per chunk        diagonal block and the within-chunk
 //                                       walks in reverse, in the compact form
-//                                       (products and one triangular
-//                                       inverse); writes dq, dk, dv, dw, dbeta
+//                                       (products, with the triangular
+//                                       factor that bwd_prep formed); writes
+//                                       dq, dk, dv, dw, dbeta
 //   bwd_fox_suffix one CTA per head     dlog f_s = sum_{t >= s} dc_t
 // The contractions here are register-tiled fp32 GEMMs on shared-memory operands, except
 // in bwd_prep and bwd_local for bf16 at d >= 64, where they run as warp-level mma.sync
@@ -463,8 +465,9 @@ __global__ void __launch_bounds__(kNT) bwd_reduce(BwdParams p) {
 //   dW  = -Y^T dQbar - Z^T dKhat - A (W dP^T) - A^T (W dP) + dQw^T Q + dKw^T K + (dG + dG^T) W
 //   dQ  = dQbar + dSs K + dQw W,   dK = dKhat + dSs^T Q + dKw W
 //
-// every step a register-tiled fp32 product on shared-memory operands; the only sequential
-// part is the triangular inverse.  Thirteen shared-memory slots of one C x (C + 4) tile each
+// every step a product on shared-memory operands (register-tiled fp32, or mma.sync for bf16 at
+// d >= 64); X is formed once, by bwd_prep (its only sequential part, the triangular inverse), and
+// read from the workspace here.  Thirteen shared-memory slots of one C x (C + 4) tile each
 // hold the operands; a d x C or C x d tile takes two adjacent slots at d = 128 and the d x d
 // gradient dP four.  The slot of every matrix and the phase that frees it are listed beside
 // the code.
