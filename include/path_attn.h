@@ -136,7 +136,7 @@ int path_attn_fwd_relbias(const void* q, const void* k, const void* v, const voi
  * Workspace size in bytes for path_attn_bwd.  The backward keeps, per head and
  * per pair (query chunk n, key chunk m < n) of 64-position chunks, the queries
  * transported to chunk m, the chain gradient, the logit gradient and the softmax
- * probabilities in the input dtype, so it grows as B*H*L^2 (about 11 GB for
+ * probabilities in the input dtype, so it grows as B*H*L^2 (about 11.5 GB for
  * bf16 at B=8, H=12, L=4096, d=128; about twice that for fp32).  Returns 0 for
  * unsupported sizes.
  */
