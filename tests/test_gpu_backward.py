@@ -173,6 +173,14 @@ def test_bwd_bf16_small_d_ragged(B, H, L, d, fox):
     _case(x, 90 + L, "bf16 B%d H%d L%d d%d fox=%s" % (B, H, L, d, fox))
 
 
+@pytest.mark.parametrize("L,fox", [(64, True), (100, False), (1, True)])
+def test_bwd_bf16_d128_one_or_two_chunks(L, fox):
+    """bf16 d = 128 with one chunk (no chains: only the diagonal block and the within-chunk products) or
+    two (one chain step and no inner chunk, so no chunk transition P_m enters)."""
+    x = inputs.make_fwd(2, 2, L, 128, "bf16", seed=120 + L, beta_std=2.0, edge_frac=0.05, fox=fox)
+    _case(x, 120 + L, "bf16 d128 L%d fox=%s" % (L, fox))
+
+
 def test_bwd_760m_shaped_sampled_heads():
     """The bench's backward workload, B8 H12 L4096 d128 bf16, run whole; two heads (first and
     last) compared with the oracle over every position."""
